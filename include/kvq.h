@@ -1,0 +1,184 @@
+/*
+ * kvq.h -- C ABI of libkvq: decode attention over a sub-byte quantized paged KV cache
+ * on NVIDIA GB300 (sm_103a).
+ *
+ * Operations (the method follows the pages int4_per_token_head.py,
+ * triton_turboquant_decode.py and kpool_compress.py of tduncan/Nvidia-Optimization-Stack-VLLM):
+ *   kvq_write_int4    reshape_and_cache_int4 / _reshape_cache_int4_kernel
+ *   kvq_decode_int4   unified_attention_int4 / _attn_packed (split-KV) + log-sum-exp merge
+ *   kvq_decode_tq     triton_turboquant_decode_attention / _tq_decode_stage1 (KEY_FP8) + merge
+ *   kvq_fwht128       fwht128_quant_fp8 / _fwht_quant_kernel
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument is a DEVICE pointer owned by the caller; the library allocates
+ *     no memory on any call path and keeps no pointer after the call returns.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default stream). KVQ_OK means
+ *     the kernels were enqueued; data-dependent errors detected on the device (a block id
+ *     outside [0, num_blocks), a slot outside the pool, a sequence longer than its block-table
+ *     row) skip the offending access and raise a sticky device flag that kvq_device_error()
+ *     reports.
+ *   - Arguments are validated before anything is launched; a rejected call launches nothing
+ *     and returns KVQ_ERR_INVALID_ARG or KVQ_ERR_UNSUPPORTED. Empty work (T == 0, rows == 0,
+ *     B == 0) is a successful no-op.
+ *   - Layouts are C-contiguous unless strides are given. Sizes are element counts.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+struct CUstream_st;
+/* The same type as cudaStream_t. */
+typedef struct CUstream_st *kvq_stream_t;
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, inconsistent sizes or strides    */
+  KVQ_ERR_UNSUPPORTED = 2,  /* a shape outside the compiled set (D, block size, group)   */
+  KVQ_ERR_WORKSPACE = 3,    /* workspace smaller than kvq_decode_workspace_bytes()        */
+  KVQ_ERR_OUT_OF_RANGE = 4, /* device-side index check failed (see kvq_device_error)     */
+  KVQ_ERR_CUDA = 5          /* a CUDA runtime call or kernel launch failed                */
+} kvq_status;
+
+typedef enum { KVQ_BF16 = 0, KVQ_F16 = 1, KVQ_F32 = 2 } kvq_dtype;
+
+/* Static, human-readable name of a status. Never NULL. */
+KVQ_API const char *kvq_status_string(kvq_status status);
+
+/* ABI revision of this header (bumped on any signature change). */
+KVQ_API int32_t kvq_abi_version(void);
+
+/*
+ * kvq_write_int4 -- rotate, quantize to INT4 and scatter K and V rows into the paged cache.
+ * Defined by int4_per_token_head.py, reshape_and_cache_int4 and _reshape_cache_int4_kernel.
+ *
+ * For every token t with slot_mapping[t] >= 0 and every kv head h, separately for K and V:
+ *   r = bf16(H_D (x * rht_signs))    unnormalised Walsh-Hadamard butterfly in fp32, cast to bf16
+ *                                     (identity when rht_signs == NULL)
+ *   scale = max((max r - min r) / 15, 1e-6); zp = clamp(round_half_away(-min r / scale), 0, 15)
+ *   q_i = clamp(round_half_away(r_i * (1/scale) + zp), 0, 15)     (IEEE fp32, no fused mul-add)
+ *   cache[slot / block_size][slot % block_size][h][j] = q_{2j} | q_{2j+1} << 4
+ *   scale_cache[...][h] = fp32 word (bits(scale) & ~0xF) | zp
+ * The result is bit-exact: the same bytes for the same inputs, whatever the launch.
+ *
+ *   key, value        bf16 [T, Hk, D]; element (t, h, d) at ptr + t*stride_t + h*stride_h + d.
+ *                     Base 16-byte aligned; strides multiples of 8 elements.
+ *   k_cache, v_cache  uint8 [num_blocks, block_size, Hk, D/2], 16-byte aligned.
+ *   k_scale, v_scale  fp32 words [num_blocks, block_size, Hk], 4-byte aligned.
+ *   slot_mapping      int64 [T]; entries < 0 are skipped; entries >= num_blocks*block_size are
+ *                     skipped and flagged. Two tokens with the same slot race (caller error).
+ *   rht_signs         fp32 [D] of +1/-1, or NULL for no rotation.
+ *   D                 64 or 128.
+ */
+KVQ_API kvq_status kvq_write_int4(const void *key, const void *value, int64_t k_stride_t,
+                          int64_t k_stride_h, int64_t v_stride_t, int64_t v_stride_h,
+                          uint8_t *k_cache, uint8_t *v_cache, float *k_scale, float *v_scale,
+                          const int64_t *slot_mapping, const float *rht_signs, int32_t T,
+                          int32_t Hk, int32_t D, int32_t block_size, int64_t num_blocks,
+                          kvq_stream_t stream);
+
+/*
+ * kvq_decode_workspace_bytes -- scratch size for kvq_decode_int4 / kvq_decode_tq.
+ * num_splits > 0: every sequence is cut into num_splits ranges of ceil(L / num_splits) positions
+ * (triton_turboquant_decode.py, _tq_decode_stage1). num_splits == 0: the library balances the
+ * pages of the whole batch over a fixed number of CTAs derived from the CURRENT device's SM
+ * count, so query with the device that will run the call current. Returns 0 for invalid sizes.
+ */
+KVQ_API size_t kvq_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hk, int32_t D,
+                                  int32_t num_splits);
+
+/*
+ * kvq_decode_int4 -- paged decode attention over the INT4 cache written by kvq_write_int4.
+ * Defined by int4_per_token_head.py, unified_attention_int4 and _attn_packed (decode, 3D mode),
+ * with the split results combined by a log-sum-exp merge (the reduce_segments step).
+ *
+ *   q_rot = bf16(H_D (q * rht_signs));  sm = softmax_scale / D          (rht_signs != NULL)
+ *   for b, query head hq (kv head hq / (Hq/Hk)), positions n < seq_lens[b]:
+ *     k_n, v_n = (nibble - zp) * scale' read from page block_table[b][n / 16], row n % 16
+ *     o = sum_n softmax_n(sm * q_rot . k_n) v_n
+ *   out[b][hq] = H_D(o) * rht_signs / D   (o itself when rht_signs == NULL, with sm = softmax_scale)
+ * Rows with seq_lens[b] == 0 are written as zeros.
+ *
+ *   q            bf16 [B, Hq, D] contiguous, 16-byte aligned.
+ *   k_cache...   as kvq_write_int4; block_size must be 16.
+ *   block_table  int32 [B, max_blocks]; entries at or past page ceil(seq_lens[b]/16) are not read.
+ *   seq_lens     int32 [B]; values are clamped to [0, 16*max_blocks] (a clamp raises the flag).
+ *   workspace    >= kvq_decode_workspace_bytes(B, Hq, Hk, D, num_splits) bytes, 16-byte aligned;
+ *                contents need no initialisation and are clobbered. Calls that share a workspace
+ *                must be ordered on one stream.
+ *   out          [B, Hq, D] of out_dtype (KVQ_BF16 / KVQ_F16 / KVQ_F32), contiguous, written in full.
+ *   Supported: D in {64, 128}; Hq % Hk == 0 with Hq / Hk <= 8; Hk in {1, 2, 4, 8} or a multiple of 8.
+ * Numerics: fp32 accumulation (tensor-core products of exact nibbles with fp16 operands);
+ * agrees with the float64 definition on the same cache to well within 2e-3 abs / 1e-2 rel.
+ */
+KVQ_API kvq_status kvq_decode_int4(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                           const float *k_scale, const float *v_scale,
+                           const int32_t *block_table, int32_t max_blocks,
+                           const int32_t *seq_lens, const float *rht_signs, float softmax_scale,
+                           int32_t num_splits, void *workspace, size_t workspace_bytes,
+                           void *out, kvq_dtype out_dtype, int32_t B, int32_t Hq, int32_t Hk,
+                           int32_t D, int32_t block_size, int64_t num_blocks,
+                           kvq_stream_t stream);
+
+/*
+ * kvq_decode_tq -- paged decode attention over the TurboQuant combined slot with FP8 keys.
+ * Defined by triton_turboquant_decode.py, triton_turboquant_decode_attention and
+ * _tq_decode_stage1 with KEY_FP8 = 1, followed by the split merge (_fwd_kernel_stage2).
+ *
+ * Slot of (page, row, kv head), slot_bytes long, slot_bytes % 16 == 0:
+ *   [0, D)            E4M3FN key codes
+ *   [D, D + VDB)      value indices, VDB = ceil(D * value_bits / 8): 4-bit two per byte (even d
+ *                     low nibble), 3-bit an LSB-first bit stream
+ *   [D + VDB, +2)     value scale, fp16 little-endian;  [D + VDB + 2, +4) value zero, fp16
+ *   score = attn_scale * sum_d q_d * k_d;   v_d = idx_d * scale + zero
+ *
+ *   q         fp32 [B, Hq, D] contiguous (already in the cache's rotated space), 16-byte aligned.
+ *   kv_cache  uint8 [num_blocks, block_size(=16), Hk, slot_bytes], 16-byte aligned.
+ *   out       fp32 [B, Hq, D] contiguous; rows with seq_lens[b] == 0 are zeros.
+ *   value_bits 3 or 4; D 64 or 128; other arguments as kvq_decode_int4.
+ */
+KVQ_API kvq_status kvq_decode_tq(const float *q, const uint8_t *kv_cache, int32_t slot_bytes,
+                         int32_t value_bits, const int32_t *block_table, int32_t max_blocks,
+                         const int32_t *seq_lens, float attn_scale, int32_t num_splits,
+                         void *workspace, size_t workspace_bytes, float *out, int32_t B,
+                         int32_t Hq, int32_t Hk, int32_t D, int32_t block_size,
+                         int64_t num_blocks, kvq_stream_t stream);
+
+/*
+ * kvq_fwht128 -- fused normalised Walsh-Hadamard-128 rotation + per-row power-of-two FP8 quant.
+ * Defined by kpool_compress.py, fwht128_quant_fp8 and _fwht_quant_kernel.
+ *   x = bf16(FWHT128(row) * fp32(0.08838834764831845));  a = max(max |x|, 1e-4)
+ *   s = smallest power of two >= a * fp32(1/448);   y = e4m3_rne(clamp(x / s, -448, 448))
+ *   x         bf16 [rows, 128] contiguous, 16-byte aligned.
+ *   y_e4m3    uint8 [rows, 128] (E4M3FN codes), 8-byte aligned.    row_scale  fp32 [rows] (s).
+ * Bit-exact.
+ */
+KVQ_API kvq_status kvq_fwht128(const void *x, uint8_t *y_e4m3, float *row_scale, int64_t rows,
+                       kvq_stream_t stream);
+
+/*
+ * kvq_device_error -- synchronize `stream`, then read and clear the sticky device-side flags
+ * of every libkvq kernel on the current device. *flags (may be NULL) receives their bitwise OR:
+ *   1 block-table entry outside [0, num_blocks)   2 seq_len above 16 * max_blocks (clamped)
+ *   4 slot_mapping entry beyond the pool
+ * Returns KVQ_OK when no flag was set, KVQ_ERR_OUT_OF_RANGE otherwise, KVQ_ERR_CUDA if the
+ * synchronization or the read failed.
+ */
+KVQ_API kvq_status kvq_device_error(kvq_stream_t stream, uint32_t *flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -1,0 +1,236 @@
+// Split-KV plumbing shared by the INT4 and TurboQuant decode kernels: work partition,
+// partial-result layout and the log-sum-exp merge (+ optional inverse rotation) kernel.
+//
+// Partition. A CTA covers the kv heads [blockIdx.y * heads_per_cta, +heads_per_cta) of one
+// contiguous piece of one or more sequences:
+//   * fixed splits (num_splits = S > 0): CTA x handles sequence x / S, split x % S, i.e. the
+//     positions [s * ceil(L/S), min((s + 1) * ceil(L/S), L)) -- the split range of
+//     triton_turboquant_decode.py, _tq_decode_stage1; partial slot = x;
+//   * balanced (num_splits = 0): the 16-token pages of the whole batch, concatenated in
+//     sequence order, are cut into gridDim.x equal runs; CTA c walks its run and emits one
+//     partial per sequence piece, at slot c + b. seg_first[b] / seg_last[b] record the first
+//     and last CTA that touched sequence b.
+// Inside a CTA, warp w serves kv head w % heads_per_cta and, when heads_per_cta < 8, every
+// warps_per_head-th page of the piece (warps_per_head = 8 / heads_per_cta). Every warp writes
+// its own partial (sub-slot w / heads_per_cta): o = acc / l and lse = m + log2(l) in the base-2
+// domain (scores are pre-multiplied by log2(e)); an empty warp writes lse = -inf.
+// The merge combines sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M) -- the stage-2 reduction
+// that triton_turboquant_decode.py (_fwd_kernel_stage2) and int4_per_token_head.py
+// (reduce_segments) call but do not show; then, for the INT4 cache, H(o) * d1 / D
+// (int4_per_token_head.py, unified_attention_int4: inverse single_rht divided by head_size).
+#pragma once
+
+#include "kvq_device.cuh"
+
+namespace kvq {
+
+struct SplitArgs {
+  const int32_t *seq_lens;
+  int32_t max_blocks;
+  int32_t num_splits;  // 0 = balanced
+  int32_t B, Hq, Hk, G;
+  int32_t heads_per_cta, warps_per_head;
+  long long slots;     // partial slots in the workspace (before the warps_per_head factor)
+  float *part_o;       // [(slots * warps_per_head), Hq, D]
+  float *part_lse;     // [(slots * warps_per_head), Hq]
+  int32_t *seg_first;  // [B] (balanced only)
+  int32_t *seg_last;   // [B]
+};
+
+__device__ __forceinline__ int clamped_len(const SplitArgs &a, int b, unsigned *flags) {
+  int L = __ldg(a.seq_lens + b);
+  const int cap = a.max_blocks * kPage;
+  if (L > cap) {
+    if (flags != nullptr) atomicOr(flags, ERR_SEQLEN);
+    L = cap;
+  }
+  return L < 0 ? 0 : L;
+}
+
+// Block-wide inclusive scan of one int64 per thread (256 threads); returns the inclusive
+// prefix and writes the block total to *total.
+__device__ __forceinline__ long long block_scan_256(long long v, long long *scratch, long long *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long n = __shfl_up_sync(FULL, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) scratch[warp] = v;
+  __syncthreads();
+  long long before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const long long s = scratch[w];
+    if (w < warp) before += s;
+    all += s;
+  }
+  __syncthreads();
+  *total = all;
+  return v + before;
+}
+
+// Calls seg(b, t0, t1, slot) for every sequence piece of this CTA (all threads, same order).
+template <typename SegFn>
+__device__ __forceinline__ void for_each_piece(const SplitArgs &a, unsigned *flags, SegFn &&seg) {
+  if (a.num_splits > 0) {
+    const int b = blockIdx.x / a.num_splits, s = blockIdx.x % a.num_splits;
+    const int L = clamped_len(a, b, flags);
+    const int span = (L + a.num_splits - 1) / a.num_splits;
+    const int t0 = s * span;
+    const int t1 = min(t0 + span, L);
+    if (t0 < t1) seg(b, t0, t1, static_cast<long long>(blockIdx.x));
+    return;
+  }
+  __shared__ long long s_scan[8];
+  __shared__ long long s_first_p;
+  __shared__ int s_first_b;
+  long long P_tot = 0;
+  for (int base = 0; base < a.B; base += 256) {
+    const int b = base + threadIdx.x;
+    const long long np = b < a.B ? (clamped_len(a, b, flags) + kPage - 1) / kPage : 0;
+    long long chunk;
+    block_scan_256(np, s_scan, &chunk);
+    P_tot += chunk;
+  }
+  const long long C = gridDim.x, c = blockIdx.x;
+  const long long pb = c * P_tot / C, pe = (c + 1) * P_tot / C;
+  if (pb >= pe) return;
+  if (threadIdx.x == 0) s_first_b = -1;
+  __syncthreads();
+  long long running = 0;
+  for (int base = 0; base < a.B; base += 256) {
+    const int b = base + threadIdx.x;
+    const long long np = b < a.B ? (clamped_len(a, b, flags) + kPage - 1) / kPage : 0;
+    long long chunk;
+    const long long incl = block_scan_256(np, s_scan, &chunk) + running;
+    const long long excl = incl - np;
+    if (np > 0 && excl <= pb && pb < incl) {
+      s_first_b = b;
+      s_first_p = excl;
+    }
+    running += chunk;
+    __syncthreads();
+    if (s_first_b >= 0) break;
+  }
+  int b = s_first_b;
+  long long P = s_first_p;
+  while (P < pe && b < a.B) {
+    const int L = clamped_len(a, b, flags);
+    const long long np = (L + kPage - 1) / kPage;
+    if (np > 0) {
+      const long long lo = max(pb, P) - P, hi = min(pe, P + np) - P;
+      const int t0 = static_cast<int>(lo * kPage);
+      const int t1 = static_cast<int>(min(hi * kPage, static_cast<long long>(L)));
+      if (threadIdx.x == 0) {
+        if (P >= pb) a.seg_first[b] = static_cast<int>(c);
+        if (P + np <= pe) a.seg_last[b] = static_cast<int>(c);
+      }
+      seg(b, t0, t1, c + b);
+    }
+    P += np;
+    ++b;
+  }
+}
+
+// Writes one warp's partial: thread (g, t) holds, for heads 2t and 2t + 1, the D/8 consecutive
+// dims [g * D/8, (g+1) * D/8) in o0 / o1; lse in base 2.
+template <int D>
+__device__ __forceinline__ void store_partial(const SplitArgs &a, long long slot, int sub, int h,
+                                              int lane, const float (&o0)[D / 8],
+                                              const float (&o1)[D / 8], float lse0, float lse1) {
+  const int g = lane >> 2, t = lane & 3;
+  const long long row = (slot * a.warps_per_head + sub) * a.Hq + static_cast<long long>(h) * a.G;
+  const int n0 = 2 * t, n1 = 2 * t + 1;
+  if (n0 < a.G) {
+    float4 *dst = reinterpret_cast<float4 *>(a.part_o + (row + n0) * D + g * (D / 8));
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) dst[i] = make_float4(o0[4 * i], o0[4 * i + 1], o0[4 * i + 2], o0[4 * i + 3]);
+    if (g == 0) a.part_lse[row + n0] = lse0;
+  }
+  if (n1 < a.G) {
+    float4 *dst = reinterpret_cast<float4 *>(a.part_o + (row + n1) * D + g * (D / 8));
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) dst[i] = make_float4(o1[4 * i], o1[4 * i + 1], o1[4 * i + 2], o1[4 * i + 3]);
+    if (g == 0) a.part_lse[row + n1] = lse1;
+  }
+}
+
+struct MergeArgs {
+  SplitArgs s;
+  const float *signs;  // inverse rotation H(o) * d1 / D when non-null
+  void *out;
+  int32_t out_dtype;   // kvq_dtype
+};
+
+// One warp per (b, hq); lane owns dims lane + 32 j.
+template <int D>
+__global__ void __launch_bounds__(256) merge_kernel(const MergeArgs m) {
+  constexpr int J = D / 32;
+  const int lane = threadIdx.x & 31;
+  const long long idx = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const SplitArgs &a = m.s;
+  if (idx >= static_cast<long long>(a.B) * a.Hq) return;
+  const int b = static_cast<int>(idx / a.Hq), hq = static_cast<int>(idx % a.Hq);
+  const int L = clamped_len(a, b, nullptr);  // the decode kernel already flagged it
+  float o[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) o[j] = 0.f;
+  if (L > 0) {
+    long long s_lo, s_hi;  // slot range [s_lo, s_hi)
+    if (a.num_splits > 0) {
+      const int span = (L + a.num_splits - 1) / a.num_splits;
+      s_lo = static_cast<long long>(b) * a.num_splits;
+      s_hi = s_lo + (L + span - 1) / span;
+    } else {
+      s_lo = static_cast<long long>(__ldg(a.seg_first + b)) + b;
+      s_hi = static_cast<long long>(__ldg(a.seg_last + b)) + b + 1;
+    }
+    // never index outside the workspace, whatever its contents
+    s_lo = max(0LL, min(s_lo, a.slots));
+    s_hi = max(s_lo, min(s_hi, a.slots));
+    const int W = a.warps_per_head;
+    float M = -INFINITY;
+    for (long long s = s_lo; s < s_hi; ++s)
+      for (int w = 0; w < W; ++w) M = fmaxf(M, a.part_lse[(s * W + w) * a.Hq + hq]);
+    float den = 0.f;
+    for (long long s = s_lo; s < s_hi; ++s) {
+      for (int w = 0; w < W; ++w) {
+        const long long r = (s * W + w) * a.Hq + hq;
+        const float lse = a.part_lse[r];
+        if (lse == -INFINITY) continue;
+        const float wgt = exp2f(lse - M);
+        den += wgt;
+        const float *src = a.part_o + r * D;
+#pragma unroll
+        for (int j = 0; j < J; ++j) o[j] = fmaf(wgt, src[lane + 32 * j], o[j]);
+      }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+    for (int j = 0; j < J; ++j) o[j] *= inv;
+    if (m.signs != nullptr) {
+#pragma unroll
+      for (int mask = 1; mask < 32; mask <<= 1) {
+#pragma unroll
+        for (int j = 0; j < J; ++j) o[j] = butterfly_xor(o[j], lane, mask);
+      }
+      butterfly_local<J>(o);
+#pragma unroll
+      for (int j = 0; j < J; ++j) o[j] *= __ldg(m.signs + lane + 32 * j) * (1.0f / D);
+    }
+  }
+  const long long base = idx * D;
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const long long e = base + lane + 32 * j;
+    if (m.out_dtype == KVQ_F32)
+      static_cast<float *>(m.out)[e] = o[j];
+    else if (m.out_dtype == KVQ_BF16)
+      static_cast<__nv_bfloat16 *>(m.out)[e] = __float2bfloat16_rn(o[j]);
+    else
+      static_cast<__half *>(m.out)[e] = __float2half_rn(o[j]);
+  }
+}
+
+}  // namespace kvq

@@ -1,0 +1,414 @@
+// kvq_decode_tq: split-KV paged decode attention over the TurboQuant combined K+V slot with
+// FP8 (E4M3FN) keys and 4-bit or 3-bit uniform values.
+//
+// Follows triton_turboquant_decode.py, _tq_decode_stage1 with KEY_FP8 = 1: per token the key is
+// the E4M3 decode of the slot's first D bytes and score = ATTN_SCALE * sum_d q_d k_d; values are
+// idx * scale + zero with scale and zero fp16 words after the value bytes (4-bit: dimension d in
+// byte d / 2, high nibble for odd d; 3-bit: LSB-first stream); an online softmax accumulates
+// acc / l and lse per split, and the splits are merged by log-sum-exp (decode_common.cuh).
+//
+// GB300 design: the INT4 kernel's structure (one warp per kv head and run of pages, private
+// cp.async ring, mma.m16n8k16 for both contractions). Keys go to fp16 with the hardware
+// E4M3x2 -> f16x2 conversion (exact); q (fp32) is split into fp16 hi + lo parts, two MMAs per
+// k-step, so the score keeps ~22 bits. Values enter as exact integers (1024 + idx) with
+// P_v = p * scale in fp16, and sum_n p_n * zero_n is added in fp32.
+
+#include "decode_common.cuh"
+#include "kvq_host.h"
+
+namespace kvq {
+
+__device__ unsigned g_flags_decode_tq = 0;
+
+struct TqParams {
+  SplitArgs s;
+  const float *q;
+  const uint8_t *cache;
+  const int32_t *block_table;
+  int32_t slot_bytes;
+  float sc_log2;  // attn_scale * log2(e)
+  int64_t num_blocks;
+};
+
+constexpr uint32_t kMagicTq = 0x64006400u;
+
+template <int D, int VBITS>
+struct TqGeom {
+  static constexpr int KCH = D / 4;             // K bytes per lane per row
+  static constexpr int KCHUNKS = KCH / 16;      // 16-byte copies per row
+  static constexpr int KB = 2 * 32 * KCH;       // two rows
+  static constexpr int VDB = (D * VBITS + 7) / 8;
+  static constexpr int VCH = VBITS == 4 ? D / 16 : 8;  // bytes per lane per token in the ring
+  static constexpr int VB = 4 * 32 * VCH;
+  static constexpr int STAGE = KB + VB + 128;
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int MT = D / 16;
+  static constexpr int QBYTES = 2 * 8 * D * 2;  // fp16 hi and lo
+};
+
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two_bytes) {
+  const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes), __NV_E4M3);
+  return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+}
+
+template <int D, int VBITS, int NSTAGE>
+__device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8_t *qarea, int b,
+                                         int h, int sub, int t0, int t1, long long slot) {
+  using Gm = TqGeom<D, VBITS>;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int G = p.s.G, WPH = p.s.warps_per_head, Hk = p.s.Hk;
+  const int SB = p.slot_bytes;
+
+  const int pg0 = t0 / kPage, pglast = (t1 - 1) / kPage;
+  const int first = pg0 + sub;
+  const int n_my = first <= pglast ? (pglast - first) / WPH + 1 : 0;
+  const int32_t *bt_row = p.block_table + static_cast<long long>(b) * p.s.max_blocks;
+  auto load_bids = [&](int batch) -> int {
+    const int k = batch * 32 + lane;
+    return k < n_my ? __ldg(bt_row + first + k * WPH) : 0;
+  };
+  int bids_cur = load_bids(0);
+  int bids_next = load_bids(1);
+
+  // -------- query -> fp16 hi / lo parts in shared memory, then B fragments
+  {
+    constexpr int J = D / 32;
+    const float *qb = p.q + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(h) * G) * D;
+    __half *qh = reinterpret_cast<__half *>(qarea);
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const int e = lane + 32 * j;
+        const float x = n < G ? qb[n * D + e] : 0.f;
+        const __half hi = __float2half_rn(x);
+        qh[n * D + e] = hi;
+        qh[8 * D + n * D + e] = __float2half_rn(x - __half2float(hi));
+      }
+    }
+  }
+  __syncwarp();
+  uint32_t qhi[Gm::KSTEPS][2], qlo[Gm::KSTEPS][2];
+  {
+    const __half *qh = reinterpret_cast<const __half *>(qarea) + g * D + t * Gm::KCH;
+#pragma unroll
+    for (int ks = 0; ks < Gm::KSTEPS; ++ks) {
+      const __half *r = qh + 4 * ks;
+      qhi[ks][0] = h2_as_u32(__halves2half2(r[0], r[1]));
+      qhi[ks][1] = h2_as_u32(__halves2half2(r[2], r[3]));
+      qlo[ks][0] = h2_as_u32(__halves2half2(r[8 * D + 0], r[8 * D + 1]));
+      qlo[ks][1] = h2_as_u32(__halves2half2(r[8 * D + 2], r[8 * D + 3]));
+    }
+  }
+  __syncwarp();
+
+  const uint32_t ring_s = smem_u32(ring);
+  const long long row_stride = static_cast<long long>(Hk) * SB;
+  // 3-bit: the lane's 2*D/16 value bits start at bit offset 3 * (D/8) * g of the value bytes
+  constexpr int kV3Bytes = 3 * D / 64;  // bytes per lane (6 at D = 128, 3 at D = 64)
+  const int v3_off = D + kV3Bytes * g;
+  const int v3_al = v3_off & ~3;
+  auto issue = [&](int k) {
+    const int kk = k & 31;
+    if (k > 0 && kk == 0) {
+      bids_cur = bids_next;
+      bids_next = load_bids((k >> 5) + 1);
+    }
+    const int blk = __shfl_sync(FULL, bids_cur, kk);
+    const bool in = k < n_my;
+    const bool ok = in && blk >= 0 && blk < p.num_blocks;
+    if (in && !ok && lane == 0) atomicOr(&g_flags_decode_tq, ERR_BLOCK);
+    const uint32_t st = ring_s + (k % NSTAGE) * Gm::STAGE;
+    const uint8_t *base = p.cache + (static_cast<long long>(ok ? blk : 0) * kPage * Hk + h) * SB;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+#pragma unroll
+      for (int c = 0; c < Gm::KCHUNKS; ++c) {
+        cp_async<16>(st + ((r * Gm::KCHUNKS + c) * 32 + lane) * 16,
+                     base + (g + 8 * r) * row_stride + t * Gm::KCH + 16 * c, ok);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int tok = 2 * t + (i & 1) + 8 * (i >> 1);
+      const uint8_t *row = base + tok * row_stride;
+      const uint32_t dst = st + Gm::KB + (i * 32 + lane) * Gm::VCH;
+      if constexpr (VBITS == 4) {
+        cp_async<Gm::VCH>(dst, row + D + g * Gm::VCH, ok);
+      } else {
+        cp_async<4>(dst, row + v3_al, ok);
+        cp_async<4>(dst + 4, row + v3_al + 4, ok);
+      }
+    }
+    cp_async<4>(st + Gm::KB + Gm::VB + lane * 4, base + (lane & 15) * row_stride + D + Gm::VDB, ok);
+    cp_async_commit();
+  };
+
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float pz0 = 0.f, pz1 = 0.f, ps0 = 0.f, ps1 = 0.f;
+  float acc[Gm::MT][4];
+#pragma unroll
+  for (int i = 0; i < Gm::MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+#pragma unroll
+  for (int k = 0; k < NSTAGE - 1; ++k) issue(k);
+
+  for (int k = 0; k < n_my; ++k) {
+    issue(k + NSTAGE - 1);
+    cp_async_wait<NSTAGE - 1>();
+    __syncwarp();
+    const uint32_t st = ring_s + (k % NSTAGE) * Gm::STAGE;
+    const int nb = (first + k * WPH) * kPage;
+    const bool ok0 = nb + g >= t0 && nb + g < t1;
+    const bool ok1 = nb + g + 8 >= t0 && nb + g + 8 < t1;
+
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ch = 0; ch < Gm::KCHUNKS; ++ch) {
+      const uint4 ra = lds128(st + (ch * 32 + lane) * 16);
+      const uint4 rb = lds128(st + ((Gm::KCHUNKS + ch) * 32 + lane) * 16);
+      const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int ks = 4 * ch + i;
+        const uint32_t a0 = e4m3x2_to_h2(wa[i] & 0xffffu), a2 = e4m3x2_to_h2(wa[i] >> 16);
+        const uint32_t a1 = e4m3x2_to_h2(wb[i] & 0xffffu), a3 = e4m3x2_to_h2(wb[i] >> 16);
+        mma_f16_16816(c, a0, a1, a2, a3, qhi[ks][0], qhi[ks][1]);
+        mma_f16_16816(c, a0, a1, a2, a3, qlo[ks][0], qlo[ks][1]);
+      }
+    }
+    const uint32_t sb = st + Gm::KB + Gm::VB;
+    const uint32_t sz0 = lds32(sb + g * 4), sz1 = lds32(sb + (g + 8) * 4);
+    const float s00 = ok0 ? c[0] * p.sc_log2 : -INFINITY;
+    const float s01 = ok0 ? c[1] * p.sc_log2 : -INFINITY;
+    const float s10 = ok1 ? c[2] * p.sc_log2 : -INFINITY;
+    const float s11 = ok1 ? c[3] * p.sc_log2 : -INFINITY;
+
+    const float mx0 = fmaxf(m0, warp_max_g(fmaxf(s00, s10)));
+    const float mx1 = fmaxf(m1, warp_max_g(fmaxf(s01, s11)));
+    const float r0 = mx0 == -INFINITY ? 0.f : mx0, r1 = mx1 == -INFINITY ? 0.f : mx1;
+    const float al0 = exp2f(m0 - r0), al1 = exp2f(m1 - r1);
+    m0 = mx0;
+    m1 = mx1;
+    const float p00 = exp2f(s00 - r0), p10 = exp2f(s10 - r0);
+    const float p01 = exp2f(s01 - r1), p11 = exp2f(s11 - r1);
+    l0 = l0 * al0 + (p00 + p10);
+    l1 = l1 * al1 + (p01 + p11);
+
+    const float2 szf0 = __half22float2(u32_as_h2(sz0)), szf1 = __half22float2(u32_as_h2(sz1));  // (scale, zero)
+    const __half2 X0 = __floats2half2_rn(ok0 ? p00 * szf0.x : 0.f, ok1 ? p10 * szf1.x : 0.f);
+    const __half2 X1 = __floats2half2_rn(ok0 ? p01 * szf0.x : 0.f, ok1 ? p11 * szf1.x : 0.f);
+    const float2 f0 = __half22float2(X0), f1 = __half22float2(X1);
+    ps0 = ps0 * al0 + (f0.x + f0.y);
+    ps1 = ps1 * al1 + (f1.x + f1.y);
+    pz0 = pz0 * al0 + ((ok0 ? p00 * szf0.y : 0.f) + (ok1 ? p10 * szf1.y : 0.f));
+    pz1 = pz1 * al1 + ((ok0 ? p01 * szf0.y : 0.f) + (ok1 ? p11 * szf1.y : 0.f));
+#pragma unroll
+    for (int i = 0; i < Gm::MT; ++i) {
+      acc[i][0] *= al0;
+      acc[i][1] *= al1;
+      acc[i][2] *= al0;
+      acc[i][3] *= al1;
+    }
+    const int src0 = 8 * t + (g >> 1), src1 = src0 + 4;
+    const uint32_t x0 = h2_as_u32(X0), x1 = h2_as_u32(X1);
+    const uint32_t y0 = __shfl_sync(FULL, x0, src0), y1 = __shfl_sync(FULL, x1, src0);
+    const uint32_t z0 = __shfl_sync(FULL, x0, src1), z1 = __shfl_sync(FULL, x1, src1);
+    const uint32_t ya = (g & 1) ? y1 : y0, za = (g & 1) ? z1 : z0;
+    const uint32_t b01 = __byte_perm(ya, za, 0x5410), b23 = __byte_perm(ya, za, 0x7632);
+
+    if constexpr (VBITS == 4) {
+      constexpr int VW = Gm::VCH / 4;
+      uint32_t va[VW], vb[VW], vc[VW], vd[VW];
+      if constexpr (VW == 2) {
+        const uint2 A = lds64(st + Gm::KB + lane * 8), B2 = lds64(st + Gm::KB + (32 + lane) * 8);
+        const uint2 C = lds64(st + Gm::KB + (64 + lane) * 8), E = lds64(st + Gm::KB + (96 + lane) * 8);
+        va[0] = A.x; va[1] = A.y; vb[0] = B2.x; vb[1] = B2.y;
+        vc[0] = C.x; vc[1] = C.y; vd[0] = E.x; vd[1] = E.y;
+      } else {
+        va[0] = lds32(st + Gm::KB + lane * 4);
+        vb[0] = lds32(st + Gm::KB + (32 + lane) * 4);
+        vc[0] = lds32(st + Gm::KB + (64 + lane) * 4);
+        vd[0] = lds32(st + Gm::KB + (96 + lane) * 4);
+      }
+#pragma unroll
+      for (int wi = 0; wi < VW; ++wi) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const uint32_t sel = hf ? 0x7632u : 0x5410u;
+          const uint32_t x = __byte_perm(va[wi], vb[wi], sel), y = __byte_perm(vc[wi], vd[wi], sel);
+          const int mt = 4 * wi + 2 * hf;
+          mma_f16_16816(acc[mt], and_or(x, 0x000F000Fu, kMagicTq), and_or(x, 0x00F000F0u, kMagicTq),
+                        and_or(y, 0x000F000Fu, kMagicTq), and_or(y, 0x00F000F0u, kMagicTq), b01, b23);
+          const uint32_t x8 = x >> 8, y8 = y >> 8;
+          mma_f16_16816(acc[mt + 1], and_or(x8, 0x000F000Fu, kMagicTq), and_or(x8, 0x00F000F0u, kMagicTq),
+                        and_or(y8, 0x000F000Fu, kMagicTq), and_or(y8, 0x00F000F0u, kMagicTq), b01, b23);
+        }
+      }
+    } else {
+      // 3-bit: the lane's D/8 indices per token, LSB first, starting (v3_off - v3_al) bytes in
+      const int sh = 8 * (v3_off - v3_al);
+      unsigned long long w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint2 r = lds64(st + Gm::KB + (i * 32 + lane) * 8);
+        w[i] = ((static_cast<unsigned long long>(r.y) << 32) | r.x) >> sh;
+      }
+#pragma unroll
+      for (int mt = 0; mt < Gm::MT; ++mt) {
+        uint32_t a[4];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {          // r = 0: dim 2 mt (row g), r = 1: dim 2 mt + 1 (row g + 8)
+          const int bit = 3 * (2 * mt + r);
+#pragma unroll
+          for (int tp = 0; tp < 2; ++tp) {     // tokens (2t, 2t+1) then (2t+8, 2t+9)
+            const uint32_t lo = static_cast<uint32_t>(w[2 * tp] >> bit) & 7u;
+            const uint32_t hi = static_cast<uint32_t>(w[2 * tp + 1] >> bit) & 7u;
+            a[2 * tp + r] = lo | (hi << 16) | kMagicTq;
+          }
+        }
+        mma_f16_16816(acc[mt], a[0], a[1], a[2], a[3], b01, b23);
+      }
+    }
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+  __syncwarp();
+
+  l0 = warp_sum_g(l0);
+  l1 = warp_sum_g(l1);
+  ps0 = warp_sum_g(ps0);
+  ps1 = warp_sum_g(ps1);
+  pz0 = warp_sum_g(pz0);
+  pz1 = warp_sum_g(pz1);
+  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+  const float off0 = 1024.f * ps0, off1 = 1024.f * ps1;
+  constexpr float hs = VBITS == 4 ? 0.0625f : 1.0f;  // high-nibble rows carry a factor 16
+  float o0[D / 8], o1[D / 8];
+#pragma unroll
+  for (int mt = 0; mt < Gm::MT; ++mt) {
+    o0[2 * mt] = (acc[mt][0] - off0 + pz0) * inv0;
+    o1[2 * mt] = (acc[mt][1] - off1 + pz1) * inv1;
+    o0[2 * mt + 1] = ((acc[mt][2] - off0) * hs + pz0) * inv0;
+    o1[2 * mt + 1] = ((acc[mt][3] - off1) * hs + pz1) * inv1;
+  }
+  const float lse0 = l0 > 0.f ? m0 + log2f(l0) : -INFINITY;
+  const float lse1 = l1 > 0.f ? m1 + log2f(l1) : -INFINITY;
+  store_partial<D>(p.s, slot, sub, h, lane, o0, o1, lse0, lse1);
+}
+
+template <int D, int VBITS, int NSTAGE>
+__global__ void __launch_bounds__(256, 2) decode_tq_kernel(const TqParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  using Gm = TqGeom<D, VBITS>;
+  const int warp = threadIdx.x >> 5;
+  uint8_t *ring = smem + warp * (NSTAGE * Gm::STAGE + Gm::QBYTES);
+  uint8_t *qarea = ring + NSTAGE * Gm::STAGE;
+  const int hl = warp % p.s.heads_per_cta;
+  const int sub = warp / p.s.heads_per_cta;
+  const int h = blockIdx.y * p.s.heads_per_cta + hl;
+  for_each_piece(p.s, &g_flags_decode_tq, [&](int b, int t0, int t1, long long slot) {
+    tq_piece<D, VBITS, NSTAGE>(p, ring, qarea, b, h, sub, t0, t1, slot);
+  });
+}
+
+constexpr int kStagesTq = 3;
+
+bool take_flags_decode_tq(cudaStream_t stream, unsigned *host_word) {
+  static const unsigned zero = 0;
+  if (cudaMemcpyFromSymbolAsync(host_word, g_flags_decode_tq, sizeof(unsigned), 0,
+                                cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return false;
+  return cudaMemcpyToSymbolAsync(g_flags_decode_tq, &zero, sizeof(unsigned), 0,
+                                 cudaMemcpyHostToDevice, stream) == cudaSuccess;
+}
+
+template <int D, int VBITS>
+static kvq_status launch_tq(const TqParams &p, const SplitPlan &plan, const MergeArgs &m,
+                            cudaStream_t s) {
+  using Gm = TqGeom<D, VBITS>;
+  const size_t smem = 8 * static_cast<size_t>(kStagesTq * Gm::STAGE + Gm::QBYTES);
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(decode_tq_kernel<D, VBITS, kStagesTq>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+    attr_set = true;
+  }
+  const dim3 grid(plan.seg_ctas, plan.head_groups);
+  decode_tq_kernel<D, VBITS, kStagesTq><<<grid, 256, smem, s>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  const long long rows = static_cast<long long>(p.s.B) * p.s.Hq;
+  merge_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(m);
+  return launch_status();
+}
+
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" kvq_status kvq_decode_tq(const float *q, const uint8_t *kv_cache, int32_t slot_bytes,
+                                    int32_t value_bits, const int32_t *block_table,
+                                    int32_t max_blocks, const int32_t *seq_lens, float attn_scale,
+                                    int32_t num_splits, void *workspace, size_t workspace_bytes,
+                                    float *out, int32_t B, int32_t Hq, int32_t Hk, int32_t D,
+                                    int32_t block_size, int64_t num_blocks, kvq_stream_t stream) {
+  if (B < 0 || Hq < 1 || Hk < 1 || max_blocks < 0 || num_splits < 0 || num_blocks < 1)
+    return KVQ_ERR_INVALID_ARG;
+  if (Hq % Hk != 0) return KVQ_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return KVQ_ERR_UNSUPPORTED;
+  if (value_bits != 3 && value_bits != 4) return KVQ_ERR_UNSUPPORTED;
+  if (block_size != kPage || Hq / Hk > 8) return KVQ_ERR_UNSUPPORTED;
+  const int vdb = (D * value_bits + 7) / 8;
+  if (slot_bytes % 16 != 0 || slot_bytes < D + vdb + 4) return KVQ_ERR_INVALID_ARG;
+  if (!(attn_scale > 0.f) || !(attn_scale < INFINITY)) return KVQ_ERR_INVALID_ARG;
+  SplitPlan plan;
+  if (!make_plan(B, Hk, num_splits, &plan)) return KVQ_ERR_UNSUPPORTED;
+  if (B == 0) return KVQ_OK;
+  if (!q || !kv_cache || !block_table || !seq_lens || !out || !workspace) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(block_table, 4) ||
+      !aligned(seq_lens, 4) || !aligned(out, 16) || !aligned(workspace, 16))
+    return KVQ_ERR_INVALID_ARG;
+  if (max_blocks < 1) return KVQ_ERR_INVALID_ARG;
+  if (workspace_bytes < kvq::workspace_bytes(B, Hq, D, plan)) return KVQ_ERR_WORKSPACE;
+
+  SplitArgs sa;
+  sa.seq_lens = seq_lens;
+  sa.max_blocks = max_blocks;
+  sa.num_splits = num_splits;
+  sa.B = B;
+  sa.Hq = Hq;
+  sa.Hk = Hk;
+  sa.G = Hq / Hk;
+  sa.heads_per_cta = plan.heads_per_cta;
+  sa.warps_per_head = plan.warps_per_head;
+  sa.slots = plan.slots;
+  const long long prows = plan.slots * plan.warps_per_head * Hq;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  sa.part_o = reinterpret_cast<float *>(ws);
+  size_t off = ((prows * D * sizeof(float)) + 255) / 256 * 256;
+  sa.part_lse = reinterpret_cast<float *>(ws + off);
+  off += ((prows * sizeof(float)) + 255) / 256 * 256;
+  sa.seg_first = reinterpret_cast<int32_t *>(ws + off);
+  off += ((B * sizeof(int32_t)) + 255) / 256 * 256;
+  sa.seg_last = reinterpret_cast<int32_t *>(ws + off);
+
+  TqParams p;
+  p.s = sa;
+  p.q = q;
+  p.cache = kv_cache;
+  p.block_table = block_table;
+  p.slot_bytes = slot_bytes;
+  p.sc_log2 = static_cast<float>(static_cast<double>(attn_scale) * 1.4426950408889634);
+  p.num_blocks = num_blocks;
+  MergeArgs m;
+  m.s = sa;
+  m.signs = nullptr;
+  m.out = out;
+  m.out_dtype = KVQ_F32;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (D == 128) return value_bits == 4 ? launch_tq<128, 4>(p, plan, m, s) : launch_tq<128, 3>(p, plan, m, s);
+  return value_bits == 4 ? launch_tq<64, 4>(p, plan, m, s) : launch_tq<64, 3>(p, plan, m, s);
+}

@@ -1,0 +1,138 @@
+// Device helpers shared by the libkvq kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+constexpr unsigned FULL = 0xffffffffu;
+constexpr int kPage = 16;  // tokens per page: one MMA M-tile of the read kernels
+
+// Device-side error flags (kvq_device_error).
+enum : unsigned { ERR_BLOCK = 1u, ERR_SEQLEN = 2u, ERR_SLOT = 4u };
+
+// ---------------------------------------------------------------------------------------------
+// Exact fp32 building blocks (IEEE round-to-nearest, never contracted into an FMA).
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_round(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// round half away from zero, then float -> int32 truncating and saturating (NaN -> 0)
+__device__ __forceinline__ int round_half_away(float x) {
+  return x >= 0.f ? __float2int_rz(__fadd_rn(x, 0.5f)) : __float2int_rz(__fsub_rn(x, 0.5f));
+}
+
+// One butterfly stage across lanes: element i pairs with i ^ (lane_mask * elems_per_lane).
+// The lower element keeps a + b, the upper one gets a - b (a = lower, b = upper).
+__device__ __forceinline__ float butterfly_xor(float self, int lane, int mask) {
+  const float other = __shfl_xor_sync(FULL, self, mask);
+  return (lane & mask) ? __fsub_rn(other, self) : __fadd_rn(self, other);
+}
+
+// In-register butterfly stages h = 1, 2, ..., N/2 over N consecutive elements.
+template <int N>
+__device__ __forceinline__ void butterfly_local(float (&x)[N]) {
+#pragma unroll
+  for (int h = 1; h < N; h <<= 1) {
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      if (!(j & h)) {
+        const float a = x[j], b = x[j + h];
+        x[j] = __fadd_rn(a, b);
+        x[j + h] = __fsub_rn(a, b);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// dst = (a & mask) | magic  in one LOP3
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t mask, uint32_t magic) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(magic));
+  return d;
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Asynchronous global -> shared copies (LDGSTS). src_bytes == 0 zero-fills without reading.
+template <int BYTES>
+__device__ __forceinline__ void cp_async(uint32_t dst, const void *src, bool valid) {
+  const int n = valid ? BYTES : 0;
+  if constexpr (BYTES == 16) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
+                 : "memory");
+  } else {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;" ::"r"(dst), "l"(src), "n"(BYTES),
+                 "r"(n)
+                 : "memory");
+  }
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+
+__device__ __forceinline__ float warp_max_g(float v) {  // over the 8 lanes sharing lane & 3
+  v = fmaxf(v, __shfl_xor_sync(FULL, v, 4));
+  v = fmaxf(v, __shfl_xor_sync(FULL, v, 8));
+  v = fmaxf(v, __shfl_xor_sync(FULL, v, 16));
+  return v;
+}
+__device__ __forceinline__ float warp_sum_g(float v) {
+  v += __shfl_xor_sync(FULL, v, 4);
+  v += __shfl_xor_sync(FULL, v, 8);
+  v += __shfl_xor_sync(FULL, v, 16);
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(FULL, v, m);
+  return v;
+}
+
+}  // namespace kvq

@@ -1,0 +1,38 @@
+// Host-side helpers shared by the libkvq translation units (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Status of the launch just enqueued.
+inline kvq_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+// SM count of the current device (cached per device).
+int sm_count();
+
+// Read-and-clear of each translation unit's device flag word (enqueued on `stream`, then the
+// caller synchronizes). Each returns false when the CUDA calls failed.
+bool take_flags_write(cudaStream_t stream, unsigned *host_word);
+bool take_flags_decode_int4(cudaStream_t stream, unsigned *host_word);
+bool take_flags_decode_tq(cudaStream_t stream, unsigned *host_word);
+
+// Split-partition geometry shared by workspace sizing and the launches.
+struct SplitPlan {
+  int heads_per_cta;   // kv heads one CTA covers (<= 8)
+  int head_groups;     // Hk / heads_per_cta
+  int warps_per_head;  // 8 / heads_per_cta
+  int seg_ctas;        // CTAs along the sequence axis (grid.x)
+  long long slots;     // partial-result slots (before the warps_per_head factor)
+};
+bool make_plan(int B, int Hk, int num_splits, SplitPlan *plan);
+size_t workspace_bytes(int B, int Hq, int D, const SplitPlan &plan);
+
+}  // namespace kvq

@@ -1,0 +1,211 @@
+"""Python binding of libkvq (include/kvq.h): argument marshalling only.
+
+Every function takes CUDA torch tensors, checks dtype / device / layout, and passes raw device
+pointers plus the current torch stream to the C ABI; all compute runs in libkvq's kernels.
+There is no fallback: if libkvq.so cannot be built or loaded, or a call returns an error status,
+an exception is raised.
+"""
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+KVQ_OK = 0
+KVQ_ERR_INVALID_ARG = 1
+KVQ_ERR_UNSUPPORTED = 2
+KVQ_ERR_WORKSPACE = 3
+KVQ_ERR_OUT_OF_RANGE = 4
+KVQ_ERR_CUDA = 5
+KVQ_BF16, KVQ_F16, KVQ_F32 = 0, 1, 2
+
+# the C API's declared functions, in header order
+C_FUNCTIONS = ("kvq_status_string", "kvq_abi_version", "kvq_write_int4", "kvq_decode_workspace_bytes",
+               "kvq_decode_int4", "kvq_decode_tq", "kvq_fwht128", "kvq_device_error")
+
+_lock = threading.Lock()
+_handle = None
+
+c_i32, c_i64, c_sz, c_p, c_f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
+_SIGS = {
+    "kvq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "kvq_abi_version": (c_i32, []),
+    "kvq_write_int4": (ctypes.c_int, [c_p, c_p, c_i64, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_p, c_p, c_p,
+                                      c_i32, c_i32, c_i32, c_i32, c_i64, c_p]),
+    "kvq_decode_workspace_bytes": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32]),
+    "kvq_decode_int4": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_f32, c_i32, c_p, c_sz,
+                                       c_p, ctypes.c_int, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_p]),
+    "kvq_decode_tq": (ctypes.c_int, [c_p, c_p, c_i32, c_i32, c_p, c_i32, c_p, c_f32, c_i32, c_p, c_sz, c_p,
+                                     c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_p]),
+    "kvq_fwht128": (ctypes.c_int, [c_p, c_p, c_p, c_i64, c_p]),
+    "kvq_device_error": (ctypes.c_int, [c_p, ctypes.POINTER(ctypes.c_uint32)]),
+}
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__("%s: %s" % (where, kvq_status_string(status)))
+
+
+def library_path():
+    return _build.LIB
+
+
+def lib():
+    """The loaded libkvq (built in-tree on first use if it is missing or stale)."""
+    global _handle
+    with _lock:
+        if _handle is None:
+            path = _build.build()
+            h = ctypes.CDLL(path)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(h, name)
+                fn.restype = res
+                fn.argtypes = args
+            _handle = h
+        return _handle
+
+
+def kvq_status_string(status):
+    return lib().kvq_status_string(int(status)).decode()
+
+
+def kvq_abi_version():
+    return int(lib().kvq_abi_version())
+
+
+def _check(status, where):
+    if status != KVQ_OK:
+        raise KvqError(status, where)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype=None, contiguous=True):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if contiguous and not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def _out_code(dtype):
+    return {torch.bfloat16: KVQ_BF16, torch.float16: KVQ_F16, torch.float32: KVQ_F32}[dtype]
+
+
+def kvq_write_int4(key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, rht_signs=None, stream=None):
+    """reshape_and_cache_int4: key/value [T, Hk, D] bf16 (last dim contiguous) into the paged cache."""
+    _need(key, "key", torch.bfloat16, contiguous=False)
+    _need(value, "value", torch.bfloat16, contiguous=False)
+    if key.stride(-1) != 1 or value.stride(-1) != 1 or key.shape != value.shape:
+        raise ValueError("key/value must have the same shape and a contiguous last dim")
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.uint8)
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _need(t, n, torch.float32)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    if rht_signs is not None:
+        _need(rht_signs, "rht_signs", torch.float32)
+    T, Hk, D = key.shape
+    nb, bs = k_cache.shape[0], k_cache.shape[1]
+    if tuple(k_cache.shape) != (nb, bs, Hk, D // 2) or tuple(k_scale.shape) != (nb, bs, Hk):
+        raise ValueError("cache shapes do not match key")
+    _check(lib().kvq_write_int4(_ptr(key), _ptr(value), key.stride(0), key.stride(1), value.stride(0),
+                                value.stride(1), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                _ptr(slot_mapping), _ptr(rht_signs), T, Hk, D, bs, nb, _stream(stream)),
+           "kvq_write_int4")
+
+
+def kvq_decode_workspace_bytes(B, Hq, Hk, D, num_splits=0):
+    return int(lib().kvq_decode_workspace_bytes(B, Hq, Hk, D, num_splits))
+
+
+def _workspace(workspace, need, device):
+    if workspace is None:
+        return torch.empty((max(need, 16),), dtype=torch.uint8, device=device)
+    _need(workspace, "workspace", torch.uint8)
+    return workspace
+
+
+def kvq_decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, rht_signs, softmax_scale,
+                    out=None, workspace=None, num_splits=0, out_dtype=None, stream=None):
+    """unified_attention_int4 (decode): q [B, Hq, D] bf16 -> out [B, Hq, D]. Returns out."""
+    _need(q, "q", torch.bfloat16)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.uint8)
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _need(t, n, torch.float32)
+    _need(block_table, "block_table", torch.int32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    if rht_signs is not None:
+        _need(rht_signs, "rht_signs", torch.float32)
+    B, Hq, D = q.shape
+    nb, bs, Hk = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype or torch.float32, device=q.device)
+    _need(out, "out")
+    need = kvq_decode_workspace_bytes(B, Hq, Hk, D, num_splits)
+    workspace = _workspace(workspace, need, q.device)
+    _check(lib().kvq_decode_int4(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                 _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(rht_signs),
+                                 float(softmax_scale), num_splits, _ptr(workspace), workspace.numel(),
+                                 _ptr(out), _out_code(out.dtype), B, Hq, Hk, D, bs, nb, _stream(stream)),
+           "kvq_decode_int4")
+    return out
+
+
+def kvq_decode_tq(q, kv_cache, value_bits, block_table, seq_lens, attn_scale, out=None, workspace=None,
+                  num_splits=0, stream=None):
+    """TurboQuant FP8-key decode: q [B, Hq, D] fp32, kv_cache [nb, 16, Hk, slot_bytes] uint8."""
+    _need(q, "q", torch.float32)
+    _need(kv_cache, "kv_cache", torch.uint8)
+    _need(block_table, "block_table", torch.int32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    B, Hq, D = q.shape
+    nb, bs, Hk, slot_bytes = kv_cache.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32)
+    need = kvq_decode_workspace_bytes(B, Hq, Hk, D, num_splits)
+    workspace = _workspace(workspace, need, q.device)
+    _check(lib().kvq_decode_tq(_ptr(q), _ptr(kv_cache), slot_bytes, value_bits, _ptr(block_table),
+                               block_table.shape[1], _ptr(seq_lens), float(attn_scale), num_splits,
+                               _ptr(workspace), workspace.numel(), _ptr(out), B, Hq, Hk, D, bs, nb,
+                               _stream(stream)),
+           "kvq_decode_tq")
+    return out
+
+
+def kvq_fwht128(x, y=None, row_scale=None, stream=None):
+    """fwht128_quant_fp8: x [rows, 128] bf16 -> (y [rows, 128] float8_e4m3fn, scale [rows, 1] fp32)."""
+    _need(x, "x", torch.bfloat16)
+    if x.dim() != 2 or x.shape[1] != 128:
+        raise ValueError("x must be [rows, 128]")
+    rows = x.shape[0]
+    if y is None:
+        y = torch.empty((rows, 128), dtype=torch.float8_e4m3fn, device=x.device)
+    if row_scale is None:
+        row_scale = torch.empty((rows, 1), dtype=torch.float32, device=x.device)
+    _need(y, "y")
+    _need(row_scale, "row_scale", torch.float32)
+    _check(lib().kvq_fwht128(_ptr(x), _ptr(y), _ptr(row_scale), rows, _stream(stream)), "kvq_fwht128")
+    return y, row_scale
+
+
+def kvq_device_error(stream=None):
+    """(status, flags): synchronizes the stream, reads and clears the device-side index flags."""
+    flags = ctypes.c_uint32(0)
+    st = lib().kvq_device_error(_stream(stream), ctypes.byref(flags))
+    return int(st), int(flags.value)

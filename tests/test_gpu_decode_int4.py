@@ -1,0 +1,131 @@
+"""kvq_decode_int4 on the GPU against the float64 oracle on the same (oracle-written) cache.
+
+Tolerance: |gpu - oracle| <= 2e-3 + 1e-2 |oracle| elementwise (fp32 accumulation against the
+float64 definition on the identical dequantized cache)."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import int4_cache
+from quantized_paged_kv_int4_gb300 import kvq, workloads
+
+from helpers import Int4Case, assert_close, run_int4
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("num_splits", [4, 0, 1, 3, 7])
+def test_tiny_config(num_splits):
+    """B=2, Hq=4, Hk=2, D=64, seq_lens {37, 100}: ragged last pages, 4 warps per kv head."""
+    c = Int4Case(workloads.tiny_int4())
+    got = run_int4(kvq, c.to_gpu(), c.scale, num_splits=num_splits).cpu().numpy()
+    assert_close(got, c.oracle(), what="tiny S=%d" % num_splits)
+
+
+@pytest.mark.parametrize("Hk,G,D", [(1, 1, 128), (1, 8, 128), (2, 3, 64), (4, 2, 128), (8, 4, 128),
+                                    (8, 8, 128), (16, 2, 64), (16, 5, 128), (8, 7, 64)])
+def test_head_layouts(Hk, G, D):
+    lens = [1, 15, 16, 17, 200, 513, 0, 33]
+    case = workloads.DecodeCase("heads", len(lens), Hk * G, Hk, D, lens, seed=Hk * 10 + G, outlier_channels=4)
+    c = Int4Case(case, num_blocks=sum(workloads.pages_needed(lens)) + 5)
+    g = c.to_gpu()
+    ref = c.oracle()
+    for S in (0, 5):
+        got = run_int4(kvq, g, c.scale, num_splits=S).cpu().numpy()
+        assert_close(got, ref, what="Hk=%d G=%d D=%d S=%d" % (Hk, G, D, S))
+        assert np.all(got[6] == 0.0)  # empty sequence
+
+
+def test_unrotated_cache_and_output_dtypes():
+    case = workloads.DecodeCase("norot", 3, 8, 2, 128, [77, 300, 5], seed=9)
+    c = Int4Case(case, signs=False)
+    g = c.to_gpu()
+    ref = c.oracle()
+    assert_close(run_int4(kvq, g, c.scale).cpu().numpy(), ref, what="f32")
+    for dt in (torch.bfloat16, torch.float16):
+        got = run_int4(kvq, g, c.scale, out_dtype=dt).float().cpu().numpy()
+        assert_close(got, ref, atol=2e-3 + 1e-2, rtol=1e-2, what=str(dt))
+
+
+def test_peaky_softmax():
+    """A 30x larger softmax scale makes the distribution sharp: tests the running max rescale."""
+    case = workloads.DecodeCase("peaky", 4, 32, 8, 128, [1000, 64, 4000, 17], seed=11, outlier_channels=4)
+    c = Int4Case(case, scale_mult=30.0)
+    got = run_int4(kvq, c.to_gpu(), c.scale).cpu().numpy()
+    assert_close(got, c.oracle(), what="peaky")
+
+
+def test_many_short_sequences_balanced():
+    """More sequences than CTAs: a CTA's page run crosses many sequence boundaries."""
+    rng = np.random.default_rng(12)
+    lens = rng.integers(0, 60, size=700).tolist()
+    case = workloads.DecodeCase("short", len(lens), 8, 2, 64, lens, seed=12)
+    c = Int4Case(case, random_cache=True)
+    got = run_int4(kvq, c.to_gpu(), c.scale).cpu().numpy()
+    idx = list(range(0, 700, 37)) + [699]
+    ref = c.oracle(batch_index=idx)
+    assert_close(got[idx], ref[idx], what="short seqs")
+
+
+def test_llama8b_decode_full_size_sampled():
+    """B=32, Hq=32, Hk=8, D=128, seq_lens ~ U[1024, 8192]: the benchmark's launch (heuristic
+    splits) on the full workload with a random cache; the oracle checks sampled sequences."""
+    case = workloads.llama8b_int4()
+    c = Int4Case(case, random_cache=True)
+    g = c.to_gpu()
+    got = run_int4(kvq, g, c.scale).cpu().numpy()
+    idx = [0, 13, 31]
+    ref = c.oracle(batch_index=idx)
+    assert_close(got[idx], ref[idx], what="llama8b")
+    assert np.all(np.isfinite(got))
+
+
+def test_llama8b_decode_oracle_written_cache_medium():
+    """Same shape family with the oracle writing the cache from K (4 outlier channels x10) and V."""
+    case = workloads.DecodeCase("llama_med", 6, 32, 8, 128, [1024, 1500, 2049, 777, 3000, 1], seed=1,
+                                outlier_channels=4)
+    c = Int4Case(case)
+    g = c.to_gpu()
+    ref = c.oracle()
+    for S in (0, 16):
+        assert_close(run_int4(kvq, g, c.scale, num_splits=S).cpu().numpy(), ref, what="S=%d" % S)
+
+
+def test_long_context_40gb_pool_sampled():
+    """B=4, Hq=64, Hk=8, D=128, 131072 positions each, 64 splits, pages scattered in a 40 GB pool."""
+    case = workloads.long_context_int4()
+    Hk, D = case.Hk, case.D
+    nb = case.pool_bytes // (16 * Hk * (D + 8))
+    bt, _ = workloads.paged_layout(case.seq_lens, case.seed, num_blocks=nb)
+    used = torch.unique(bt.flatten().to(torch.int64))
+    dev = "cuda"
+    kc = torch.empty((nb, 16, Hk, D // 2), dtype=torch.uint8, device=dev)
+    vc = torch.empty_like(kc)
+    ks = torch.empty((nb, 16, Hk), dtype=torch.float32, device=dev)
+    vs = torch.empty_like(ks)
+    kb, vb, kw, vw = workloads.random_int4_pages(used.numel(), Hk, D, case.seed)
+    u = used.to(dev)
+    kc[u] = kb.to(dev)
+    vc[u] = vb.to(dev)
+    ks[u] = kw.to(dev).view(torch.float32)
+    vs[u] = vw.to(dev).view(torch.float32)
+    q = workloads.query(case)
+    signs = workloads.rht_signs(D)
+    scale = 1.0 / math.sqrt(D)
+    lens = torch.tensor(case.seq_lens, dtype=torch.int32)
+    g = dict(q=q.to(dev), kc=kc, vc=vc, ks=ks, vs=vs, bt=bt.to(dev), lens=lens.to(dev), signs=signs.to(dev))
+    # oracle on one sequence, reading only its pages (mapped into a compact pool)
+    b = 2
+    small_bt = np.zeros_like(bt.numpy())
+    small_bt[b] = torch.searchsorted(used, bt[b].to(torch.int64)).numpy()
+    ref = int4_cache.decode_int4(workloads.to_numpy_f32(q), kb.numpy(), vb.numpy(),
+                                 kw.numpy().view(np.uint32), vw.numpy().view(np.uint32), small_bt,
+                                 np.asarray(case.seq_lens), signs.numpy(), scale, batch_index=[b])
+    for S in (64, 0):
+        got = run_int4(kvq, g, scale, num_splits=S).cpu().numpy()
+        assert_close(got[b], ref[b], what="long S=%d" % S)
+    del kc, vc, ks, vs
+    torch.cuda.empty_cache()

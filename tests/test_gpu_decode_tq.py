@@ -1,0 +1,42 @@
+"""kvq_decode_tq (FP8 keys, 4-bit / 3-bit values) on the GPU against the float64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+from quantized_paged_kv_int4_gb300 import kvq, workloads
+
+from helpers import TqCase, assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(c, num_splits=0):
+    out = kvq.kvq_decode_tq(c.q.cuda(), c.cache.cuda(), c.bits, c.bt.cuda(), c.lens.cuda(), c.scale,
+                            num_splits=num_splits)
+    st, flags = kvq.kvq_device_error()
+    assert st == 0 and flags == 0
+    return out.cpu().numpy()
+
+
+@pytest.mark.parametrize("bits", [4, 3])
+@pytest.mark.parametrize("Hk,G,D", [(8, 4, 128), (2, 2, 64), (1, 8, 128), (16, 1, 64)])
+def test_small_layouts(bits, Hk, G, D):
+    lens = [1, 16, 37, 300, 0, 129]
+    case = workloads.DecodeCase("tq", len(lens), Hk * G, Hk, D, lens, seed=bits + Hk + G)
+    c = TqCase(case, bits, num_blocks=sum(workloads.pages_needed(lens)) + 3)
+    ref = c.oracle()
+    for S in (0, 4):
+        got = _run(c, S)
+        assert_close(got, ref, what="bits=%d Hk=%d G=%d D=%d S=%d" % (bits, Hk, G, D, S))
+        assert np.all(got[4] == 0.0)
+
+
+@pytest.mark.parametrize("bits", [4, 3])
+def test_turboquant_full_size_sampled(bits):
+    """B=64, Hq=32, Hk=8, D=128, seq_len 4096: the full workload, oracle on sampled sequences."""
+    c = TqCase(workloads.turboquant_fp8(bits), bits)
+    got = _run(c)
+    idx = [0, 40, 63]
+    ref = c.oracle(batch_index=idx)
+    assert_close(got[idx], ref[idx], what="tq full bits=%d" % bits)
