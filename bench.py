@@ -237,7 +237,7 @@ def run_kvq(args, dist):
         nrep = 1  # 570 MB read per step: far beyond L2 by itself
     reps = [Int4Replica(case, 10 * dist.rank + r, dev, pool) for r in range(nrep)]
     S = case.num_splits
-    ws = torch.empty((kvq.kvq_decode_workspace_bytes(B, Hq, Hk, D, S),), dtype=torch.uint8, device=dev)
+    ws = torch.zeros((kvq.kvq_decode_workspace_bytes(B, Hq, Hk, D, S),), dtype=torch.uint8, device=dev)
 
     def write(r):
         kvq.kvq_write_int4(r.k_new, r.v_new, r.kc, r.vc, r.ks, r.vs, r.slots, signs, stream=stream)
@@ -377,7 +377,7 @@ def run_tq(args, dist, dev, stream):
     lens = torch.tensor(case.seq_lens, dtype=torch.int32, device=dev)
     q = torch.randn((B, Hq, D), device=dev, generator=g)
     out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
-    ws = torch.empty((kvq.kvq_decode_workspace_bytes(B, Hq, Hk, D, 0),), dtype=torch.uint8, device=dev)
+    ws = torch.zeros((kvq.kvq_decode_workspace_bytes(B, Hq, Hk, D, 0),), dtype=torch.uint8, device=dev)
     scale = 1.0 / math.sqrt(D)
 
     def decode(i):

@@ -12,14 +12,15 @@
 // NSTAGE-deep cp.async ring in shared memory: each lane copies exactly the bytes its MMA
 // fragments need (16 B of each of two K rows, 8 B of four V rows, one scale word), so the ring
 // needs no layout transform and no block-wide barrier. Both contractions run on the tensor
-// cores with exact operands:
-//   * S^T[16 tokens x 8 heads] = K[16 x D] . Q^T  (mma.m16n8k16, fp16): nibble n enters as the
-//     fp16 value 1024 + n (low nibble) or 1024 + 16 n (high nibble, with the matching q
-//     element pre-divided by 16), built with one LOP3 per pair; the 1024 offset is folded
-//     into a per-head bias;
-//   * O^T[D x 8 heads] += V^T[D x 16 tokens] . P_v^T with P_v in fp16 and the same nibble
-//     trick; the K dimension (tokens) and the D rows are permuted so that a lane's V bytes
-//     become A fragments with one PRMT.
+// cores (mma.m16n8k16, fp16 operands, fp32 accumulation) on exact operands: a nibble pair
+// masked into an fp16 pair with a zero exponent field IS the pair of fp16 subnormals n * 2^-24
+// (low nibble) or n * 2^-20 (high nibble), so one LOP3 turns 2 nibbles into MMA operands
+// without any offset; the power of two goes into the per-token scale, and the zero-point is
+// applied as the split-dot correction of the pages (sum q n - zp sum q; sum P_v v - sum P_v zp):
+//   * S^T[16 tokens x 8 heads] = K[16 x D] . Q^T  (q of a high-nibble dim pre-divided by 16);
+//   * O^T[D x 8 heads] += V^T[D x 16 tokens] . P_v^T with P_v = p * scale_v in fp16; the
+//     tokens (the K dimension) and the D rows are permuted so that a lane's V bytes become A
+//     fragments with one PRMT per pair of m-tiles.
 // The G query heads of a kv head share every K/V byte loaded (GQA), padded to the MMA's N = 8.
 
 #include "decode_common.cuh"
@@ -35,12 +36,14 @@ struct Int4Params {
   const uint8_t *k_cache, *v_cache;
   const uint32_t *k_scale, *v_scale;
   const int32_t *block_table;
-  const float *signs;
   float sm_log2;  // softmax scale (divided by D when rotating) times log2(e)
   int64_t num_blocks;
 };
 
-constexpr uint32_t kMagic = 0x64006400u;  // fp16 pair (1024, 1024)
+constexpr uint32_t kLo = 0x000F000Fu;  // low nibbles of bytes 0 and 2 -> fp16 subnormal pair n * 2^-24
+constexpr uint32_t kHi = 0x00F000F0u;  // high nibbles -> fp16 subnormal pair n * 2^-20
+constexpr float kTwo24 = 16777216.0f;
+constexpr float kTwo20 = 1048576.0f;
 
 template <int D>
 struct Int4Geom {
@@ -75,20 +78,24 @@ __device__ __forceinline__ void int4_piece(const Int4Params &p, uint8_t *ring, u
   int bids_cur = load_bids(0);
   int bids_next = load_bids(1);
 
-  // -------- query: q_rot = bf16(H(q * d1)) for the G heads of kv head h; fp16 B operands
+  // -------- query: q_rot = bf16(H(q * d1)) for the G heads of kv head h, as fp16 B operands
   {
     constexpr int J = D / 32;
     const __nv_bfloat16 *qb = p.q + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(h) * G) * D;
     __half *qh = reinterpret_cast<__half *>(qarea);
     float *qsum = reinterpret_cast<float *>(qarea + 8 * D * 2);
+    for (int n = G; n < 8; ++n) {  // padded MMA columns
 #pragma unroll
-    for (int n = 0; n < 8; ++n) {
+      for (int j = 0; j < J; ++j) qh[n * D + lane + 32 * j] = __float2half_rn(0.f);
+      if (lane == 0) qsum[n] = 0.f;
+    }
+    for (int n = 0; n < G; ++n) {
       float x[J];
 #pragma unroll
-      for (int j = 0; j < J; ++j) x[j] = n < G ? __bfloat162float(qb[n * D + lane + 32 * j]) : 0.f;
-      if (p.signs != nullptr && n < G) {
+      for (int j = 0; j < J; ++j) x[j] = __bfloat162float(qb[n * D + lane + 32 * j]);
+      if (p.s.signs != nullptr) {
 #pragma unroll
-        for (int j = 0; j < J; ++j) x[j] *= __ldg(p.signs + lane + 32 * j);
+        for (int j = 0; j < J; ++j) x[j] *= __ldg(p.s.signs + lane + 32 * j);
 #pragma unroll
         for (int mask = 1; mask < 32; mask <<= 1) {
 #pragma unroll
@@ -98,25 +105,22 @@ __device__ __forceinline__ void int4_piece(const Int4Params &p, uint8_t *ring, u
 #pragma unroll
         for (int j = 0; j < J; ++j) x[j] = bf16_round(x[j]);
       }
-      float raw = 0.f, eff = 0.f;
+      // odd dims meet high nibbles, which enter the MMA 16x larger: pre-divide q by 16 (exact)
+      float eff = 0.f;
 #pragma unroll
       for (int j = 0; j < J; ++j) {
         const int e = lane + 32 * j;
         const __half v = __float2half_rn((e & 1) ? x[j] * 0.0625f : x[j]);
         qh[n * D + e] = v;
-        const float f = __half2float(v);
-        raw += f;
-        eff += (e & 1) ? f * 16.f : f;
+        eff += (e & 1) ? __half2float(v) * 16.f : __half2float(v);
       }
-      raw = warp_sum(raw);
       eff = warp_sum(eff);
-      if (lane == 0) {
-        qsum[n] = eff;             // sum of the q values the products use (zero-point term)
-        qsum[8 + n] = 1024.f * raw;  // the fp16 offset of the nibble encoding
-      }
+      if (lane == 0) qsum[n] = eff * (1.0f / kTwo24);  // sum of the q the products use, in MMA units
     }
   }
   __syncwarp();
+  // B fragment of k-step ks = 2m + s: the dims a K word's nibbles occupy after the LOP3 split
+  // (word j = WPR * t + m: low nibbles 8j + 2s, 8j + 4 + 2s; high nibbles one dim up)
   uint32_t qf[Gm::KSTEPS][2];
   {
     const __half *qh = reinterpret_cast<const __half *>(qarea) + g * D;
@@ -129,12 +133,16 @@ __device__ __forceinline__ void int4_piece(const Int4Params &p, uint8_t *ring, u
   }
   const float *qsum = reinterpret_cast<const float *>(qarea + 8 * D * 2);
   const float qs0 = qsum[2 * t], qs1 = qsum[2 * t + 1];
-  const float bias0 = qsum[8 + 2 * t], bias1 = qsum[8 + 2 * t + 1];
+  const float sm24 = p.sm_log2 * kTwo24;  // the K operands carry a factor 2^-24
   __syncwarp();
 
   // -------- cp.async ring
   const uint32_t ring_s = smem_u32(ring);
   const long long row_stride = static_cast<long long>(Hk) * (D / 2);  // bytes between token rows
+  const long long page_bytes = kPage * row_stride;                     // one page of one pool
+  const uint8_t *kbase = p.k_cache + h * (D / 2) + g * row_stride + t * Gm::KCH;
+  const uint8_t *vbase = p.v_cache + h * (D / 2) + 2 * t * row_stride + g * Gm::VCH;
+  const uint32_t *sbase = (lane < 16 ? p.k_scale : p.v_scale) + h + (lane & 15) * Hk;
   auto issue = [&](int k) {
     const int kk = k & 31;
     if (k > 0 && kk == 0) {
@@ -146,23 +154,20 @@ __device__ __forceinline__ void int4_piece(const Int4Params &p, uint8_t *ring, u
     const bool ok = in && blk >= 0 && blk < p.num_blocks;
     if (in && !ok && lane == 0) atomicOr(&g_flags_decode_int4, ERR_BLOCK);
     const uint32_t st = ring_s + (k % NSTAGE) * Gm::STAGE;
-    const long long row0 = static_cast<long long>(ok ? blk : 0) * kPage * Hk + h;  // token 0 row
-    const uint8_t *kb = p.k_cache + row0 * (D / 2);
-    cp_async<Gm::KCH>(st + lane * Gm::KCH, kb + g * row_stride + t * Gm::KCH, ok);
-    cp_async<Gm::KCH>(st + (32 + lane) * Gm::KCH, kb + (g + 8) * row_stride + t * Gm::KCH, ok);
-    const uint8_t *vb = p.v_cache + row0 * (D / 2);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int tok = 2 * t + (i & 1) + 8 * (i >> 1);
-      cp_async<Gm::VCH>(st + Gm::KB + (i * 32 + lane) * Gm::VCH, vb + tok * row_stride + g * Gm::VCH, ok);
-    }
-    const uint32_t *sp = (lane < 16 ? p.k_scale : p.v_scale) + row0 + static_cast<long long>(lane & 15) * Hk;
-    cp_async<4>(st + Gm::KB + Gm::VB + lane * 4, sp, ok);
+    const long long pg = static_cast<long long>(ok ? blk : 0);
+    const uint8_t *kb = kbase + pg * page_bytes;
+    cp_async<Gm::KCH>(st + lane * Gm::KCH, kb, ok);
+    cp_async<Gm::KCH>(st + (32 + lane) * Gm::KCH, kb + 8 * row_stride, ok);
+    const uint8_t *vb = vbase + pg * page_bytes;
+    cp_async<Gm::VCH>(st + Gm::KB + lane * Gm::VCH, vb, ok);                          // token 2t
+    cp_async<Gm::VCH>(st + Gm::KB + (32 + lane) * Gm::VCH, vb + row_stride, ok);      // 2t + 1
+    cp_async<Gm::VCH>(st + Gm::KB + (64 + lane) * Gm::VCH, vb + 8 * row_stride, ok);  // 2t + 8
+    cp_async<Gm::VCH>(st + Gm::KB + (96 + lane) * Gm::VCH, vb + 9 * row_stride, ok);  // 2t + 9
+    cp_async<4>(st + Gm::KB + Gm::VB + lane * 4, sbase + pg * (kPage * Hk), ok);
     cp_async_commit();
   };
 
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float pz0 = 0.f, pz1 = 0.f, ps0 = 0.f, ps1 = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, pz0 = 0.f, pz1 = 0.f;
   float acc[Gm::MT][4];
 #pragma unroll
   for (int i = 0; i < Gm::MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
@@ -174,13 +179,15 @@ __device__ __forceinline__ void int4_piece(const Int4Params &p, uint8_t *ring, u
     issue(k + NSTAGE - 1);
     cp_async_wait<NSTAGE - 1>();
     __syncwarp();
-    const uint32_t st = ring_s + (k % NSTAGE) * Gm::STAGE;
+    const uint8_t *st = ring + (k % NSTAGE) * Gm::STAGE;
     const int nb = (first + k * WPH) * kPage;  // position of the page's row 0
     const bool ok0 = nb + g >= t0 && nb + g < t1;
     const bool ok1 = nb + g + 8 >= t0 && nb + g + 8 < t1;
 
-    // ---- scores
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- scores: S = (sum_d q_d n_d - zp sum_d q_d) * scale_k * sm (base 2)
+    const uint8_t *sb = st + Gm::KB + Gm::VB;
+    const uint32_t kw0 = lds32(sb + g * 4), kw1 = lds32(sb + (g + 8) * 4);
+    float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};  // two MMA chains
     {
       uint32_t wa[Gm::WPR], wb[Gm::WPR];
       if constexpr (Gm::WPR == 4) {
@@ -195,53 +202,48 @@ __device__ __forceinline__ void int4_piece(const Int4Params &p, uint8_t *ring, u
 #pragma unroll
       for (int m = 0; m < Gm::WPR; ++m) {
         const uint32_t xa = wa[m] >> 8, xb = wb[m] >> 8;
-        mma_f16_16816(c, and_or(wa[m], 0x000F000Fu, kMagic), and_or(wb[m], 0x000F000Fu, kMagic),
-                      and_or(wa[m], 0x00F000F0u, kMagic), and_or(wb[m], 0x00F000F0u, kMagic),
-                      qf[2 * m][0], qf[2 * m][1]);
-        mma_f16_16816(c, and_or(xa, 0x000F000Fu, kMagic), and_or(xb, 0x000F000Fu, kMagic),
-                      and_or(xa, 0x00F000F0u, kMagic), and_or(xb, 0x00F000F0u, kMagic),
-                      qf[2 * m + 1][0], qf[2 * m + 1][1]);
+        mma_f16_16816(c, wa[m] & kLo, wb[m] & kLo, wa[m] & kHi, wb[m] & kHi, qf[2 * m][0], qf[2 * m][1]);
+        mma_f16_16816(c2, xa & kLo, xb & kLo, xa & kHi, xb & kHi, qf[2 * m + 1][0], qf[2 * m + 1][1]);
       }
     }
-    const uint32_t sb = st + Gm::KB + Gm::VB;
-    const uint32_t kw0 = lds32(sb + g * 4), kw1 = lds32(sb + (g + 8) * 4);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] += c2[i];
     const uint32_t vw0 = lds32(sb + (16 + g) * 4), vw1 = lds32(sb + (24 + g) * 4);
-    const float ck0 = __uint_as_float(kw0 & ~0xFu) * p.sm_log2;
-    const float ck1 = __uint_as_float(kw1 & ~0xFu) * p.sm_log2;
+    const float ck0 = __uint_as_float(kw0 & ~0xFu) * sm24, ck1 = __uint_as_float(kw1 & ~0xFu) * sm24;
     const float zk0 = static_cast<float>(kw0 & 0xFu), zk1 = static_cast<float>(kw1 & 0xFu);
-    float s00 = ok0 ? (c[0] - bias0 - zk0 * qs0) * ck0 : -INFINITY;  // token g,   head 2t
-    float s01 = ok0 ? (c[1] - bias1 - zk0 * qs1) * ck0 : -INFINITY;  // token g,   head 2t+1
-    float s10 = ok1 ? (c[2] - bias0 - zk1 * qs0) * ck1 : -INFINITY;  // token g+8, head 2t
-    float s11 = ok1 ? (c[3] - bias1 - zk1 * qs1) * ck1 : -INFINITY;  // token g+8, head 2t+1
+    const float s00 = ok0 ? (c[0] - zk0 * qs0) * ck0 : -INFINITY;  // token g,   head 2t
+    const float s01 = ok0 ? (c[1] - zk0 * qs1) * ck0 : -INFINITY;  // token g,   head 2t+1
+    const float s10 = ok1 ? (c[2] - zk1 * qs0) * ck1 : -INFINITY;  // token g+8, head 2t
+    const float s11 = ok1 ? (c[3] - zk1 * qs1) * ck1 : -INFINITY;  // token g+8, head 2t+1
 
     // ---- online softmax (base 2)
     const float mx0 = fmaxf(m0, warp_max_g(fmaxf(s00, s10)));
     const float mx1 = fmaxf(m1, warp_max_g(fmaxf(s01, s11)));
     const float r0 = mx0 == -INFINITY ? 0.f : mx0, r1 = mx1 == -INFINITY ? 0.f : mx1;
-    const float al0 = exp2f(m0 - r0), al1 = exp2f(m1 - r1);
+    const float al0 = fast_exp2(m0 - r0), al1 = fast_exp2(m1 - r1);
     m0 = mx0;
     m1 = mx1;
-    const float p00 = exp2f(s00 - r0), p10 = exp2f(s10 - r0);
-    const float p01 = exp2f(s01 - r1), p11 = exp2f(s11 - r1);
+    const float p00 = fast_exp2(s00 - r0), p10 = fast_exp2(s10 - r0);
+    const float p01 = fast_exp2(s01 - r1), p11 = fast_exp2(s11 - r1);
     l0 = l0 * al0 + (p00 + p10);
     l1 = l1 * al1 + (p01 + p11);
 
-    // ---- P_v = p * scale_v (fp16), its sums for the offset and zero-point corrections
+    // ---- P_v = p * scale_v (fp16), and sum P_v * zp_v for the zero-point correction
     const float sv0 = __uint_as_float(vw0 & ~0xFu), sv1 = __uint_as_float(vw1 & ~0xFu);
     const float zv0 = static_cast<float>(vw0 & 0xFu), zv1 = static_cast<float>(vw1 & 0xFu);
     const __half2 X0 = __floats2half2_rn(ok0 ? p00 * sv0 : 0.f, ok1 ? p10 * sv1 : 0.f);
     const __half2 X1 = __floats2half2_rn(ok0 ? p01 * sv0 : 0.f, ok1 ? p11 * sv1 : 0.f);
     const float2 f0 = __half22float2(X0), f1 = __half22float2(X1);
-    ps0 = ps0 * al0 + (f0.x + f0.y);
-    ps1 = ps1 * al1 + (f1.x + f1.y);
     pz0 = pz0 * al0 + (f0.x * zv0 + f0.y * zv1);
     pz1 = pz1 * al1 + (f1.x * zv0 + f1.y * zv1);
+    if (!__all_sync(FULL, al0 == 1.f && al1 == 1.f)) {  // a running max moved: rescale
 #pragma unroll
-    for (int i = 0; i < Gm::MT; ++i) {
-      acc[i][0] *= al0;
-      acc[i][1] *= al1;
-      acc[i][2] *= al0;
-      acc[i][3] *= al1;
+      for (int i = 0; i < Gm::MT; ++i) {
+        acc[i][0] *= al0;
+        acc[i][1] *= al1;
+        acc[i][2] *= al0;
+        acc[i][3] *= al1;
+      }
     }
     // B fragment of P_v^T: this lane needs head g at tokens 2t, 2t+1 (b01), 2t+8, 2t+9 (b23)
     const int src0 = 8 * t + (g >> 1), src1 = src0 + 4;
@@ -273,11 +275,9 @@ __device__ __forceinline__ void int4_piece(const Int4Params &p, uint8_t *ring, u
           const uint32_t sel = hf ? 0x7632u : 0x5410u;
           const uint32_t x = __byte_perm(va[wi], vb[wi], sel), y = __byte_perm(vc[wi], vd[wi], sel);
           const int mt = 4 * wi + 2 * hf;
-          mma_f16_16816(acc[mt], and_or(x, 0x000F000Fu, kMagic), and_or(x, 0x00F000F0u, kMagic),
-                        and_or(y, 0x000F000Fu, kMagic), and_or(y, 0x00F000F0u, kMagic), b01, b23);
+          mma_f16_16816(acc[mt], x & kLo, x & kHi, y & kLo, y & kHi, b01, b23);
           const uint32_t x8 = x >> 8, y8 = y >> 8;
-          mma_f16_16816(acc[mt + 1], and_or(x8, 0x000F000Fu, kMagic), and_or(x8, 0x00F000F0u, kMagic),
-                        and_or(y8, 0x000F000Fu, kMagic), and_or(y8, 0x00F000F0u, kMagic), b01, b23);
+          mma_f16_16816(acc[mt + 1], x8 & kLo, x8 & kHi, y8 & kLo, y8 & kHi, b01, b23);
         }
       }
     }
@@ -286,22 +286,19 @@ __device__ __forceinline__ void int4_piece(const Int4Params &p, uint8_t *ring, u
   cp_async_wait<0>();
   __syncwarp();
 
-  // -------- epilogue: finish the corrections, normalise, store the partial
+  // -------- epilogue: undo the subnormal scaling, apply the zero-point term, normalise
   l0 = warp_sum_g(l0);
   l1 = warp_sum_g(l1);
-  ps0 = warp_sum_g(ps0);
-  ps1 = warp_sum_g(ps1);
   pz0 = warp_sum_g(pz0);
   pz1 = warp_sum_g(pz1);
   const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-  const float off0 = 1024.f * ps0, off1 = 1024.f * ps1;
   float o0[D / 8], o1[D / 8];
 #pragma unroll
   for (int mt = 0; mt < Gm::MT; ++mt) {
-    o0[2 * mt] = (acc[mt][0] - off0 - pz0) * inv0;
-    o1[2 * mt] = (acc[mt][1] - off1 - pz1) * inv1;
-    o0[2 * mt + 1] = ((acc[mt][2] - off0) * 0.0625f - pz0) * inv0;
-    o1[2 * mt + 1] = ((acc[mt][3] - off1) * 0.0625f - pz1) * inv1;
+    o0[2 * mt] = (acc[mt][0] * kTwo24 - pz0) * inv0;
+    o1[2 * mt] = (acc[mt][1] * kTwo24 - pz1) * inv1;
+    o0[2 * mt + 1] = (acc[mt][2] * kTwo20 - pz0) * inv0;
+    o1[2 * mt + 1] = (acc[mt][3] * kTwo20 - pz1) * inv1;
   }
   const float lse0 = l0 > 0.f ? m0 + log2f(l0) : -INFINITY;
   const float lse1 = l1 > 0.f ? m1 + log2f(l1) : -INFINITY;
@@ -318,7 +315,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const Int4Params p)
   const int hl = warp % p.s.heads_per_cta;
   const int sub = warp / p.s.heads_per_cta;
   const int h = blockIdx.y * p.s.heads_per_cta + hl;
-  for_each_piece(p.s, &g_flags_decode_int4, [&](int b, int t0, int t1, long long slot) {
+  for_each_piece<D>(p.s, &g_flags_decode_int4, [&](int b, int t0, int t1, long long slot) {
     int4_piece<D, NSTAGE>(p, ring, qarea, b, h, sub, t0, t1, slot);
   });
 }
@@ -340,8 +337,7 @@ bool take_flags_decode_int4(cudaStream_t stream, unsigned *host_word) {
 }
 
 template <int D>
-static kvq_status launch_int4(const Int4Params &p, const SplitPlan &plan, const MergeArgs &m,
-                              cudaStream_t s) {
+static kvq_status launch_int4(const Int4Params &p, const SplitPlan &plan, cudaStream_t s) {
   const size_t smem = int4_smem_bytes<D>();
   static bool attr_set = false;  // per process; the attribute is per function, not per device
   if (!attr_set) {
@@ -353,9 +349,6 @@ static kvq_status launch_int4(const Int4Params &p, const SplitPlan &plan, const 
   }
   const dim3 grid(plan.seg_ctas, plan.head_groups);
   decode_int4_kernel<D, kStagesInt4><<<grid, 256, smem, s>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
-  const long long rows = static_cast<long long>(p.s.B) * p.s.Hq;
-  merge_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(m);
   return launch_status();
 }
 
@@ -390,10 +383,10 @@ extern "C" kvq_status kvq_decode_int4(const void *q, const uint8_t *k_cache, con
       !aligned(out, 16) || !aligned(workspace, 16) || (rht_signs && !aligned(rht_signs, 16)))
     return KVQ_ERR_INVALID_ARG;
   if (max_blocks < 1) return KVQ_ERR_INVALID_ARG;
-  const size_t need = kvq::workspace_bytes(B, Hq, D, plan);
-  if (workspace_bytes < need) return KVQ_ERR_WORKSPACE;
+  if (workspace_bytes < kvq::workspace_bytes(B, Hq, D, plan)) return KVQ_ERR_WORKSPACE;
 
-  SplitArgs sa;
+  Int4Params p;
+  SplitArgs &sa = p.s;
   sa.seq_lens = seq_lens;
   sa.max_blocks = max_blocks;
   sa.num_splits = num_splits;
@@ -404,34 +397,19 @@ extern "C" kvq_status kvq_decode_int4(const void *q, const uint8_t *k_cache, con
   sa.heads_per_cta = plan.heads_per_cta;
   sa.warps_per_head = plan.warps_per_head;
   sa.slots = plan.slots;
-  const long long prows = plan.slots * plan.warps_per_head * Hq;
-  uint8_t *ws = static_cast<uint8_t *>(workspace);
-  sa.part_o = reinterpret_cast<float *>(ws);
-  size_t off = ((prows * D * sizeof(float)) + 255) / 256 * 256;
-  sa.part_lse = reinterpret_cast<float *>(ws + off);
-  off += ((prows * sizeof(float)) + 255) / 256 * 256;
-  sa.seg_first = reinterpret_cast<int32_t *>(ws + off);
-  off += ((B * sizeof(int32_t)) + 255) / 256 * 256;
-  sa.seg_last = reinterpret_cast<int32_t *>(ws + off);
-
-  Int4Params p;
-  p.s = sa;
+  workspace_carve(workspace, Hq, D, plan, &sa.part_o, &sa.part_lse, &sa.counters);
+  sa.signs = rht_signs;
+  sa.out = out;
+  sa.out_dtype = out_dtype;
   p.q = static_cast<const __nv_bfloat16 *>(q);
   p.k_cache = k_cache;
   p.v_cache = v_cache;
   p.k_scale = reinterpret_cast<const uint32_t *>(k_scale);
   p.v_scale = reinterpret_cast<const uint32_t *>(v_scale);
   p.block_table = block_table;
-  p.signs = rht_signs;
   const double sm = rht_signs ? static_cast<double>(softmax_scale) / D : softmax_scale;
   p.sm_log2 = static_cast<float>(sm * 1.4426950408889634);
   p.num_blocks = num_blocks;
-
-  MergeArgs m;
-  m.s = sa;
-  m.signs = rht_signs;
-  m.out = out;
-  m.out_dtype = out_dtype;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return D == 128 ? launch_int4<128>(p, plan, m, s) : launch_int4<64>(p, plan, m, s);
+  return D == 128 ? launch_int4<128>(p, plan, s) : launch_int4<64>(p, plan, s);
 }

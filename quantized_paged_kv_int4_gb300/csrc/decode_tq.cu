@@ -8,10 +8,12 @@
 // acc / l and lse per split, and the splits are merged by log-sum-exp (decode_common.cuh).
 //
 // GB300 design: the INT4 kernel's structure (one warp per kv head and run of pages, private
-// cp.async ring, mma.m16n8k16 for both contractions). Keys go to fp16 with the hardware
-// E4M3x2 -> f16x2 conversion (exact); q (fp32) is split into fp16 hi + lo parts, two MMAs per
-// k-step, so the score keeps ~22 bits. Values enter as exact integers (1024 + idx) with
-// P_v = p * scale in fp16, and sum_n p_n * zero_n is added in fp32.
+// cp.async ring, mma.m16n8k16 for both contractions, merge fused into the kernel). Keys go to
+// fp16 with the hardware E4M3x2 -> f16x2 conversion (exact); q (fp32) is split into fp16 hi + lo
+// parts, two MMAs per k-step, so the score keeps ~22 bits. Value indices enter as exact fp16
+// subnormals (the index bits masked into a zero-exponent fp16: idx * 2^-24, or idx * 2^-20 for a
+// high nibble) weighted by P_v = p * scale in fp16; the power of two is undone in the epilogue
+// and sum_n p_n * zero_n is added in fp32.
 
 #include "decode_common.cuh"
 #include "kvq_host.h"
@@ -30,7 +32,8 @@ struct TqParams {
   int64_t num_blocks;
 };
 
-constexpr uint32_t kMagicTq = 0x64006400u;
+constexpr uint32_t kLoTq = 0x000F000Fu;  // low nibbles -> fp16 subnormals idx * 2^-24
+constexpr uint32_t kHiTq = 0x00F000F0u;  // high nibbles -> idx * 2^-20
 
 template <int D, int VBITS>
 struct TqGeom {
@@ -76,7 +79,6 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
     constexpr int J = D / 32;
     const float *qb = p.q + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(h) * G) * D;
     __half *qh = reinterpret_cast<__half *>(qarea);
-#pragma unroll
     for (int n = 0; n < 8; ++n) {
 #pragma unroll
       for (int j = 0; j < J; ++j) {
@@ -105,10 +107,12 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
 
   const uint32_t ring_s = smem_u32(ring);
   const long long row_stride = static_cast<long long>(Hk) * SB;
-  // 3-bit: the lane's 2*D/16 value bits start at bit offset 3 * (D/8) * g of the value bytes
+  const long long page_bytes = kPage * row_stride;
+  // 3-bit: the lane's D/8 indices start at bit 3 * (D/8) * g of the value bytes
   constexpr int kV3Bytes = 3 * D / 64;  // bytes per lane (6 at D = 128, 3 at D = 64)
   const int v3_off = D + kV3Bytes * g;
   const int v3_al = v3_off & ~3;
+  const uint8_t *head = p.cache + static_cast<long long>(h) * SB;
   auto issue = [&](int k) {
     const int kk = k & 31;
     if (k > 0 && kk == 0) {
@@ -120,7 +124,7 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
     const bool ok = in && blk >= 0 && blk < p.num_blocks;
     if (in && !ok && lane == 0) atomicOr(&g_flags_decode_tq, ERR_BLOCK);
     const uint32_t st = ring_s + (k % NSTAGE) * Gm::STAGE;
-    const uint8_t *base = p.cache + (static_cast<long long>(ok ? blk : 0) * kPage * Hk + h) * SB;
+    const uint8_t *base = head + static_cast<long long>(ok ? blk : 0) * page_bytes;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
 #pragma unroll
@@ -146,7 +150,7 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
   };
 
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float pz0 = 0.f, pz1 = 0.f, ps0 = 0.f, ps1 = 0.f;
+  float pz0 = 0.f, pz1 = 0.f;
   float acc[Gm::MT][4];
 #pragma unroll
   for (int i = 0; i < Gm::MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
@@ -158,7 +162,7 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
     issue(k + NSTAGE - 1);
     cp_async_wait<NSTAGE - 1>();
     __syncwarp();
-    const uint32_t st = ring_s + (k % NSTAGE) * Gm::STAGE;
+    const uint8_t *st = ring + (k % NSTAGE) * Gm::STAGE;
     const int nb = (first + k * WPH) * kPage;
     const bool ok0 = nb + g >= t0 && nb + g < t1;
     const bool ok1 = nb + g + 8 >= t0 && nb + g + 8 < t1;
@@ -178,7 +182,7 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
         mma_f16_16816(c, a0, a1, a2, a3, qlo[ks][0], qlo[ks][1]);
       }
     }
-    const uint32_t sb = st + Gm::KB + Gm::VB;
+    const uint8_t *sb = st + Gm::KB + Gm::VB;
     const uint32_t sz0 = lds32(sb + g * 4), sz1 = lds32(sb + (g + 8) * 4);
     const float s00 = ok0 ? c[0] * p.sc_log2 : -INFINITY;
     const float s01 = ok0 ? c[1] * p.sc_log2 : -INFINITY;
@@ -188,28 +192,27 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
     const float mx0 = fmaxf(m0, warp_max_g(fmaxf(s00, s10)));
     const float mx1 = fmaxf(m1, warp_max_g(fmaxf(s01, s11)));
     const float r0 = mx0 == -INFINITY ? 0.f : mx0, r1 = mx1 == -INFINITY ? 0.f : mx1;
-    const float al0 = exp2f(m0 - r0), al1 = exp2f(m1 - r1);
+    const float al0 = fast_exp2(m0 - r0), al1 = fast_exp2(m1 - r1);
     m0 = mx0;
     m1 = mx1;
-    const float p00 = exp2f(s00 - r0), p10 = exp2f(s10 - r0);
-    const float p01 = exp2f(s01 - r1), p11 = exp2f(s11 - r1);
+    const float p00 = fast_exp2(s00 - r0), p10 = fast_exp2(s10 - r0);
+    const float p01 = fast_exp2(s01 - r1), p11 = fast_exp2(s11 - r1);
     l0 = l0 * al0 + (p00 + p10);
     l1 = l1 * al1 + (p01 + p11);
 
     const float2 szf0 = __half22float2(u32_as_h2(sz0)), szf1 = __half22float2(u32_as_h2(sz1));  // (scale, zero)
     const __half2 X0 = __floats2half2_rn(ok0 ? p00 * szf0.x : 0.f, ok1 ? p10 * szf1.x : 0.f);
     const __half2 X1 = __floats2half2_rn(ok0 ? p01 * szf0.x : 0.f, ok1 ? p11 * szf1.x : 0.f);
-    const float2 f0 = __half22float2(X0), f1 = __half22float2(X1);
-    ps0 = ps0 * al0 + (f0.x + f0.y);
-    ps1 = ps1 * al1 + (f1.x + f1.y);
     pz0 = pz0 * al0 + ((ok0 ? p00 * szf0.y : 0.f) + (ok1 ? p10 * szf1.y : 0.f));
     pz1 = pz1 * al1 + ((ok0 ? p01 * szf0.y : 0.f) + (ok1 ? p11 * szf1.y : 0.f));
+    if (!__all_sync(FULL, al0 == 1.f && al1 == 1.f)) {  // a running max moved: rescale
 #pragma unroll
-    for (int i = 0; i < Gm::MT; ++i) {
-      acc[i][0] *= al0;
-      acc[i][1] *= al1;
-      acc[i][2] *= al0;
-      acc[i][3] *= al1;
+      for (int i = 0; i < Gm::MT; ++i) {
+        acc[i][0] *= al0;
+        acc[i][1] *= al1;
+        acc[i][2] *= al0;
+        acc[i][3] *= al1;
+      }
     }
     const int src0 = 8 * t + (g >> 1), src1 = src0 + 4;
     const uint32_t x0 = h2_as_u32(X0), x1 = h2_as_u32(X1);
@@ -239,11 +242,9 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
           const uint32_t sel = hf ? 0x7632u : 0x5410u;
           const uint32_t x = __byte_perm(va[wi], vb[wi], sel), y = __byte_perm(vc[wi], vd[wi], sel);
           const int mt = 4 * wi + 2 * hf;
-          mma_f16_16816(acc[mt], and_or(x, 0x000F000Fu, kMagicTq), and_or(x, 0x00F000F0u, kMagicTq),
-                        and_or(y, 0x000F000Fu, kMagicTq), and_or(y, 0x00F000F0u, kMagicTq), b01, b23);
+          mma_f16_16816(acc[mt], x & kLoTq, x & kHiTq, y & kLoTq, y & kHiTq, b01, b23);
           const uint32_t x8 = x >> 8, y8 = y >> 8;
-          mma_f16_16816(acc[mt + 1], and_or(x8, 0x000F000Fu, kMagicTq), and_or(x8, 0x00F000F0u, kMagicTq),
-                        and_or(y8, 0x000F000Fu, kMagicTq), and_or(y8, 0x00F000F0u, kMagicTq), b01, b23);
+          mma_f16_16816(acc[mt + 1], x8 & kLoTq, x8 & kHiTq, y8 & kLoTq, y8 & kHiTq, b01, b23);
         }
       }
     } else {
@@ -265,7 +266,7 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
           for (int tp = 0; tp < 2; ++tp) {     // tokens (2t, 2t+1) then (2t+8, 2t+9)
             const uint32_t lo = static_cast<uint32_t>(w[2 * tp] >> bit) & 7u;
             const uint32_t hi = static_cast<uint32_t>(w[2 * tp + 1] >> bit) & 7u;
-            a[2 * tp + r] = lo | (hi << 16) | kMagicTq;
+            a[2 * tp + r] = lo | (hi << 16);  // fp16 subnormals idx * 2^-24
           }
         }
         mma_f16_16816(acc[mt], a[0], a[1], a[2], a[3], b01, b23);
@@ -278,20 +279,17 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
 
   l0 = warp_sum_g(l0);
   l1 = warp_sum_g(l1);
-  ps0 = warp_sum_g(ps0);
-  ps1 = warp_sum_g(ps1);
   pz0 = warp_sum_g(pz0);
   pz1 = warp_sum_g(pz1);
   const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-  const float off0 = 1024.f * ps0, off1 = 1024.f * ps1;
-  constexpr float hs = VBITS == 4 ? 0.0625f : 1.0f;  // high-nibble rows carry a factor 16
+  constexpr float hs = VBITS == 4 ? 1048576.f : 16777216.f;  // 2^20: high nibbles enter 16x larger
   float o0[D / 8], o1[D / 8];
 #pragma unroll
   for (int mt = 0; mt < Gm::MT; ++mt) {
-    o0[2 * mt] = (acc[mt][0] - off0 + pz0) * inv0;
-    o1[2 * mt] = (acc[mt][1] - off1 + pz1) * inv1;
-    o0[2 * mt + 1] = ((acc[mt][2] - off0) * hs + pz0) * inv0;
-    o1[2 * mt + 1] = ((acc[mt][3] - off1) * hs + pz1) * inv1;
+    o0[2 * mt] = (acc[mt][0] * 16777216.f + pz0) * inv0;
+    o1[2 * mt] = (acc[mt][1] * 16777216.f + pz1) * inv1;
+    o0[2 * mt + 1] = (acc[mt][2] * hs + pz0) * inv0;
+    o1[2 * mt + 1] = (acc[mt][3] * hs + pz1) * inv1;
   }
   const float lse0 = l0 > 0.f ? m0 + log2f(l0) : -INFINITY;
   const float lse1 = l1 > 0.f ? m1 + log2f(l1) : -INFINITY;
@@ -308,7 +306,7 @@ __global__ void __launch_bounds__(256, 2) decode_tq_kernel(const TqParams p) {
   const int hl = warp % p.s.heads_per_cta;
   const int sub = warp / p.s.heads_per_cta;
   const int h = blockIdx.y * p.s.heads_per_cta + hl;
-  for_each_piece(p.s, &g_flags_decode_tq, [&](int b, int t0, int t1, long long slot) {
+  for_each_piece<D>(p.s, &g_flags_decode_tq, [&](int b, int t0, int t1, long long slot) {
     tq_piece<D, VBITS, NSTAGE>(p, ring, qarea, b, h, sub, t0, t1, slot);
   });
 }
@@ -325,8 +323,7 @@ bool take_flags_decode_tq(cudaStream_t stream, unsigned *host_word) {
 }
 
 template <int D, int VBITS>
-static kvq_status launch_tq(const TqParams &p, const SplitPlan &plan, const MergeArgs &m,
-                            cudaStream_t s) {
+static kvq_status launch_tq(const TqParams &p, const SplitPlan &plan, cudaStream_t s) {
   using Gm = TqGeom<D, VBITS>;
   const size_t smem = 8 * static_cast<size_t>(kStagesTq * Gm::STAGE + Gm::QBYTES);
   static bool attr_set = false;
@@ -339,9 +336,6 @@ static kvq_status launch_tq(const TqParams &p, const SplitPlan &plan, const Merg
   }
   const dim3 grid(plan.seg_ctas, plan.head_groups);
   decode_tq_kernel<D, VBITS, kStagesTq><<<grid, 256, smem, s>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
-  const long long rows = static_cast<long long>(p.s.B) * p.s.Hq;
-  merge_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(m);
   return launch_status();
 }
 
@@ -374,7 +368,8 @@ extern "C" kvq_status kvq_decode_tq(const float *q, const uint8_t *kv_cache, int
   if (max_blocks < 1) return KVQ_ERR_INVALID_ARG;
   if (workspace_bytes < kvq::workspace_bytes(B, Hq, D, plan)) return KVQ_ERR_WORKSPACE;
 
-  SplitArgs sa;
+  TqParams p;
+  SplitArgs &sa = p.s;
   sa.seq_lens = seq_lens;
   sa.max_blocks = max_blocks;
   sa.num_splits = num_splits;
@@ -385,30 +380,17 @@ extern "C" kvq_status kvq_decode_tq(const float *q, const uint8_t *kv_cache, int
   sa.heads_per_cta = plan.heads_per_cta;
   sa.warps_per_head = plan.warps_per_head;
   sa.slots = plan.slots;
-  const long long prows = plan.slots * plan.warps_per_head * Hq;
-  uint8_t *ws = static_cast<uint8_t *>(workspace);
-  sa.part_o = reinterpret_cast<float *>(ws);
-  size_t off = ((prows * D * sizeof(float)) + 255) / 256 * 256;
-  sa.part_lse = reinterpret_cast<float *>(ws + off);
-  off += ((prows * sizeof(float)) + 255) / 256 * 256;
-  sa.seg_first = reinterpret_cast<int32_t *>(ws + off);
-  off += ((B * sizeof(int32_t)) + 255) / 256 * 256;
-  sa.seg_last = reinterpret_cast<int32_t *>(ws + off);
-
-  TqParams p;
-  p.s = sa;
+  workspace_carve(workspace, Hq, D, plan, &sa.part_o, &sa.part_lse, &sa.counters);
+  sa.signs = nullptr;
+  sa.out = out;
+  sa.out_dtype = KVQ_F32;
   p.q = q;
   p.cache = kv_cache;
   p.block_table = block_table;
   p.slot_bytes = slot_bytes;
   p.sc_log2 = static_cast<float>(static_cast<double>(attn_scale) * 1.4426950408889634);
   p.num_blocks = num_blocks;
-  MergeArgs m;
-  m.s = sa;
-  m.signs = nullptr;
-  m.out = out;
-  m.out_dtype = KVQ_F32;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (D == 128) return value_bits == 4 ? launch_tq<128, 4>(p, plan, m, s) : launch_tq<128, 3>(p, plan, m, s);
-  return value_bits == 4 ? launch_tq<64, 4>(p, plan, m, s) : launch_tq<64, 3>(p, plan, m, s);
+  if (D == 128) return value_bits == 4 ? launch_tq<128, 4>(p, plan, s) : launch_tq<128, 3>(p, plan, s);
+  return value_bits == 4 ? launch_tq<64, 4>(p, plan, s) : launch_tq<64, 3>(p, plan, s);
 }

@@ -33,6 +33,11 @@ struct SplitPlan {
   long long slots;     // partial-result slots (before the warps_per_head factor)
 };
 bool make_plan(int B, int Hk, int num_splits, SplitPlan *plan);
+// Workspace: partial outputs [slots * warps_per_head, Hq, D] fp32, their log-sum-exps
+// [slots * warps_per_head, Hq] fp32, then the merge tickets [B * head_groups] int32 (each region
+// 256-byte aligned). The tickets must be zero when a call starts; every call leaves them zero.
 size_t workspace_bytes(int B, int Hq, int D, const SplitPlan &plan);
+void workspace_carve(void *workspace, int Hq, int D, const SplitPlan &plan, float **part_o,
+                     float **part_lse, int32_t **counters);
 
 }  // namespace kvq

@@ -129,3 +129,21 @@ def test_long_context_40gb_pool_sampled():
         assert_close(got[b], ref[b], what="long S=%d" % S)
     del kc, vc, ks, vs
     torch.cuda.empty_cache()
+
+
+def test_workspace_reused_across_calls():
+    """One zero-filled workspace serves consecutive calls: the merge tickets reset themselves."""
+    case = workloads.DecodeCase("reuse", 5, 16, 4, 128, [700, 1, 0, 2000, 333], seed=21, outlier_channels=4)
+    c = Int4Case(case)
+    g = c.to_gpu()
+    ref = c.oracle()
+    for S in (0, 6):
+        ws = kvq.decode_workspace(case.B, case.Hq, case.Hk, case.D, S, device="cuda")
+        outs = []
+        for _ in range(3):
+            o = kvq.kvq_decode_int4(g["q"], g["kc"], g["vc"], g["ks"], g["vs"], g["bt"], g["lens"], g["signs"],
+                                    c.scale, workspace=ws, num_splits=S)
+            outs.append(o.cpu().numpy())
+        assert kvq.kvq_device_error() == (0, 0)
+        assert_close(outs[0], ref, what="reuse S=%d" % S)
+        assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
