@@ -89,8 +89,7 @@ KVQ_API kvq_status kvq_write_int4(const void *key, const void *value, int64_t k_
                           kvq_stream_t stream);
 
 /*
- * kvq_decode_workspace_bytes -- scratch size for kvq_decode_int4 / kvq_decode_tq (the workspace
- * must be zero-filled before its first use; see kvq_decode_int4).
+ * kvq_decode_workspace_bytes -- scratch size for kvq_decode_int4 / kvq_decode_tq.
  * num_splits > 0: every sequence is cut into num_splits ranges of ceil(L / num_splits) positions
  * (triton_turboquant_decode.py, _tq_decode_stage1). num_splits == 0: the library balances the
  * pages of the whole batch over a fixed number of CTAs derived from the CURRENT device's SM
@@ -115,11 +114,10 @@ KVQ_API size_t kvq_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hk, int
  *   k_cache...   as kvq_write_int4; block_size must be 16.
  *   block_table  int32 [B, max_blocks]; entries at or past page ceil(seq_lens[b]/16) are not read.
  *   seq_lens     int32 [B]; values are clamped to [0, 16*max_blocks] (a clamp raises the flag).
- *   workspace    >= kvq_decode_workspace_bytes(B, Hq, Hk, D, num_splits) bytes, 16-byte aligned,
- *                ZERO-FILLED before its first use (e.g. cudaMemsetAsync). It holds the per-split
- *                partial results and the tickets of the fused merge; every completed call leaves
- *                the tickets zero again, so one zero-fill per workspace suffices. Calls that share
- *                a workspace must be ordered on one stream.
+ *   workspace    >= kvq_decode_workspace_bytes(B, Hq, Hk, D, num_splits) bytes, 16-byte aligned;
+ *                holds the per-split partial results between the split kernel and the merge
+ *                kernel (both enqueued by this call). Contents need no initialisation and are
+ *                clobbered. Calls that share a workspace must be ordered on one stream.
  *   out          [B, Hq, D] of out_dtype (KVQ_BF16 / KVQ_F16 / KVQ_F32), contiguous, written in full.
  *   Supported: D in {64, 128}; Hq % Hk == 0 with Hq / Hk <= 8; Hk in {1, 2, 4, 8} or a multiple of 8.
  * Numerics: fp32 accumulation (tensor-core products of exact nibbles with fp16 operands);
@@ -149,7 +147,7 @@ KVQ_API kvq_status kvq_decode_int4(const void *q, const uint8_t *k_cache, const 
  *   q         fp32 [B, Hq, D] contiguous (already in the cache's rotated space), 16-byte aligned.
  *   kv_cache  uint8 [num_blocks, block_size(=16), Hk, slot_bytes], 16-byte aligned.
  *   out       fp32 [B, Hq, D] contiguous; rows with seq_lens[b] == 0 are zeros.
- *   workspace as kvq_decode_int4 (zero-filled before its first use).
+ *   workspace as kvq_decode_int4.
  *   value_bits 3 or 4; D 64 or 128; other arguments as kvq_decode_int4.
  */
 KVQ_API kvq_status kvq_decode_tq(const float *q, const uint8_t *kv_cache, int32_t slot_bytes,

@@ -53,18 +53,20 @@ static size_t round256(size_t n) { return (n + 255) / 256 * 256; }
 size_t workspace_bytes(int B, int Hq, int D, const SplitPlan &plan) {
   const size_t rows = static_cast<size_t>(plan.slots) * plan.warps_per_head * Hq;
   return round256(rows * D * sizeof(float)) + round256(rows * sizeof(float)) +
-         round256(static_cast<size_t>(B) * plan.head_groups * sizeof(int32_t));
+         2 * round256(static_cast<size_t>(B) * sizeof(int32_t));
 }
 
-void workspace_carve(void *workspace, int Hq, int D, const SplitPlan &plan, float **part_o,
-                     float **part_lse, int32_t **counters) {
+void workspace_carve(void *workspace, int B, int Hq, int D, const SplitPlan &plan, float **part_o,
+                     float **part_lse, int32_t **seg_first, int32_t **seg_last) {
   const size_t rows = static_cast<size_t>(plan.slots) * plan.warps_per_head * Hq;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   *part_o = reinterpret_cast<float *>(ws);
   ws += round256(rows * D * sizeof(float));
   *part_lse = reinterpret_cast<float *>(ws);
   ws += round256(rows * sizeof(float));
-  *counters = reinterpret_cast<int32_t *>(ws);
+  *seg_first = reinterpret_cast<int32_t *>(ws);
+  ws += round256(static_cast<size_t>(B) * sizeof(int32_t));
+  *seg_last = reinterpret_cast<int32_t *>(ws);
 }
 
 }  // namespace kvq

@@ -1,6 +1,5 @@
 // Split-KV plumbing shared by the INT4 and TurboQuant decode kernels: work partition,
-// partial-result layout, and the log-sum-exp merge (+ optional inverse rotation), fused into the
-// decode kernel as a "last CTA to finish a sequence merges it" epilogue.
+// partial-result layout, and the log-sum-exp merge (+ optional inverse rotation) kernel.
 //
 // Partition. A CTA covers the kv heads [blockIdx.y * heads_per_cta, +heads_per_cta) of one
 // contiguous piece of one or more sequences:
@@ -9,21 +8,19 @@
 //     triton_turboquant_decode.py, _tq_decode_stage1; partial slot = x;
 //   * balanced (num_splits = 0): the 16-token pages of the whole batch, concatenated in
 //     sequence order, are cut into gridDim.x runs whose lengths differ by at most one page
-//     (longer runs first, so the CTAs that touch a sequence are consecutive); CTA c walks its
-//     run and emits one partial per sequence piece, at slot c + b.
+//     (longer runs first, so the CTAs that touch a sequence are consecutive and non-empty);
+//     CTA c walks its run and emits one partial per sequence piece, at slot c + b.
+//     seg_first[b] / seg_last[b] record the first and last CTA that touched sequence b.
 // Inside a CTA, warp w serves kv head w % heads_per_cta and, when heads_per_cta < 8, every
 // warps_per_head-th page of the piece (warps_per_head = 8 / heads_per_cta). Every warp writes
 // its own partial (sub-slot w / heads_per_cta): o = acc / l and lse = m + log2(l) in the base-2
 // domain (scores are pre-multiplied by log2(e)); an empty warp writes lse = -inf.
 //
-// Merge. After a piece, the CTA publishes its partials (__threadfence) and takes a ticket on
-// the sequence's counter; the CTA that draws the last ticket (it never waits for anyone) resets
-// the counter and combines sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M) over all partials of
-// the sequence -- the stage-2 reduction that triton_turboquant_decode.py (_fwd_kernel_stage2) and
-// int4_per_token_head.py (reduce_segments) call but do not show -- then, for the INT4 cache,
-// applies H(o) * d1 / D (int4_per_token_head.py, unified_attention_int4: inverse single_rht
-// divided by head_size) and writes the output row. With the grid over head groups, the ticket
-// counts (sequence, head group) pairs and the merge covers the group's query heads.
+// Merge (a second kernel, launched as a programmatic dependent of the first so that its launch
+// overlaps the split kernel's tail): sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M) -- the stage-2
+// reduction that triton_turboquant_decode.py (_fwd_kernel_stage2) and int4_per_token_head.py
+// (reduce_segments) call but do not show; then, for the INT4 cache, H(o) * d1 / D
+// (int4_per_token_head.py, unified_attention_int4: inverse single_rht divided by head_size).
 #pragma once
 
 #include "kvq_device.cuh"
@@ -39,7 +36,8 @@ struct SplitArgs {
   long long slots;     // partial slots in the workspace (before the warps_per_head factor)
   float *part_o;       // [(slots * warps_per_head), Hq, D]
   float *part_lse;     // [(slots * warps_per_head), Hq]
-  int32_t *counters;   // [B * head_groups], zero between calls
+  int32_t *seg_first;  // [B] first / last CTA of each sequence (balanced only)
+  int32_t *seg_last;
   const float *signs;  // inverse rotation of the merged output when non-null
   void *out;           // [B, Hq, D] of out_dtype
   int32_t out_dtype;
@@ -78,145 +76,114 @@ __device__ __forceinline__ long long block_scan_256(long long v, long long *scra
   return v + before;
 }
 
+// Output rows: lane owns the D/32 consecutive dims [lane * D/32, (lane + 1) * D/32).
 template <int D>
 __device__ __forceinline__ void store_out(const SplitArgs &a, long long row, int lane, const float (&o)[D / 32]) {
-#pragma unroll
-  for (int j = 0; j < D / 32; ++j) {
-    const long long e = row * D + lane + 32 * j;
-    if (a.out_dtype == KVQ_F32)
-      static_cast<float *>(a.out)[e] = o[j];
-    else if (a.out_dtype == KVQ_BF16)
-      static_cast<__nv_bfloat16 *>(a.out)[e] = __float2bfloat16_rn(o[j]);
+  constexpr int V = D / 32;
+  const long long e = row * D + lane * V;
+  if (a.out_dtype == KVQ_F32) {
+    if constexpr (V == 4)
+      *reinterpret_cast<float4 *>(static_cast<float *>(a.out) + e) = make_float4(o[0], o[1], o[2], o[3]);
     else
-      static_cast<__half *>(a.out)[e] = __float2half_rn(o[j]);
+      *reinterpret_cast<float2 *>(static_cast<float *>(a.out) + e) = make_float2(o[0], o[1]);
+  } else if (a.out_dtype == KVQ_BF16) {
+#pragma unroll
+    for (int j = 0; j < V; j += 2)
+      *reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(a.out) + e + j) = __floats2bfloat162_rn(o[j], o[j + 1]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < V; j += 2)
+      *reinterpret_cast<__half2 *>(static_cast<__half *>(a.out) + e + j) = __floats2half2_rn(o[j], o[j + 1]);
   }
 }
 
 // Merge the partials of (b, hq) in slots [s_lo, s_hi) and write the output row (one warp).
-// Partials come from other CTAs: read through L2 (ld.global.cg), never a stale L1 line.
+// Up to 16 partial rows per round trip: their log-sum-exps and their vectors are all requested
+// before any is used, then combined online (running max M, weights 2^(lse - M)). Partials come
+// from the split kernel's CTAs: read through L2 (ld.global.cg).
 template <int D>
-__device__ void merge_row(const SplitArgs &a, int b, int hq, long long s_lo, long long s_hi, int lane) {
-  constexpr int J = D / 32;
+__device__ __forceinline__ void merge_row(const SplitArgs &a, int b, int hq, long long s_lo, long long s_hi, int lane) {
+  constexpr int V = D / 32, R = 16;
   const int W = a.warps_per_head;
   const long long n = (s_hi - s_lo) * W, r0 = s_lo * W;  // rows (s * W + w) are contiguous
-  const float *lse = a.part_lse + hq;
-  float M = -INFINITY;
-  for (long long i = lane; i < n; i += 32) M = fmaxf(M, __ldcg(lse + (r0 + i) * a.Hq));
+  float o[V];
 #pragma unroll
-  for (int mask = 16; mask >= 1; mask >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, mask));
-  float o[J];
+  for (int j = 0; j < V; ++j) o[j] = 0.f;
+  float M = -INFINITY, den = 0.f;
+  for (long long i0 = 0; i0 < n; i0 += R) {
+    const int cnt = static_cast<int>(min(static_cast<long long>(R), n - i0));
+    const float lse = lane < cnt ? __ldcg(a.part_lse + (r0 + i0 + lane) * a.Hq + hq) : -INFINITY;
+    float v[R][V];
 #pragma unroll
-  for (int j = 0; j < J; ++j) o[j] = 0.f;
-  float den = 0.f;
-  for (long long i0 = 0; i0 < n; i0 += 32) {
-    float wgt = 0.f;
-    if (i0 + lane < n) {
-      const float x = __ldcg(lse + (r0 + i0 + lane) * a.Hq);
-      wgt = x == -INFINITY ? 0.f : exp2f(x - M);
+    for (int k = 0; k < R; ++k) {
+      if (k < cnt) {
+        const float *src = a.part_o + ((r0 + i0 + k) * a.Hq + hq) * D + lane * V;
+        if constexpr (V == 4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
+          v[k][0] = x.x; v[k][1] = x.y; v[k][2] = x.z; v[k][3] = x.w;
+        } else {
+          const float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
+          v[k][0] = x.x; v[k][1] = x.y;
+        }
+      }
     }
-    den += wgt;
-    const int cnt = static_cast<int>(min(32LL, n - i0));
-#pragma unroll 4
-    for (int k = 0; k < cnt; ++k) {
-      const float wk = __shfl_sync(FULL, wgt, k);
-      const float *src = a.part_o + ((r0 + i0 + k) * a.Hq + hq) * D;
+    float cm = lse;
 #pragma unroll
-      for (int j = 0; j < J; ++j) o[j] = fmaf(wk, __ldcg(src + lane + 32 * j), o[j]);
+    for (int mask = 16; mask >= 1; mask >>= 1) cm = fmaxf(cm, __shfl_xor_sync(FULL, cm, mask));
+    const float nM = fmaxf(M, cm);
+    if (nM != -INFINITY) {
+      const float f = M == -INFINITY ? 0.f : exp2f(M - nM);
+#pragma unroll
+      for (int j = 0; j < V; ++j) o[j] *= f;
+      den *= f;
+      M = nM;
+    }
+    const float w = lse == -INFINITY ? 0.f : exp2f(lse - M);
+    float ws = w;
+#pragma unroll
+    for (int mask = 16; mask >= 1; mask >>= 1) ws += __shfl_xor_sync(FULL, ws, mask);
+    den += ws;
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+      if (k < cnt) {
+        const float wk = __shfl_sync(FULL, w, k);
+#pragma unroll
+        for (int j = 0; j < V; ++j) o[j] = fmaf(wk, v[k][j], o[j]);
+      }
     }
   }
-#pragma unroll
-  for (int mask = 16; mask >= 1; mask >>= 1) den += __shfl_xor_sync(FULL, den, mask);
   const float inv = den > 0.f ? 1.f / den : 0.f;
 #pragma unroll
-  for (int j = 0; j < J; ++j) o[j] *= inv;
+  for (int j = 0; j < V; ++j) o[j] *= inv;
   if (a.signs != nullptr) {
+    // element e = lane * V + j: stages h < V inside the lane, h = V .. D/2 across lanes
+    butterfly_local<V>(o);
 #pragma unroll
     for (int mask = 1; mask < 32; mask <<= 1) {
 #pragma unroll
-      for (int j = 0; j < J; ++j) o[j] = butterfly_xor(o[j], lane, mask);
+      for (int j = 0; j < V; ++j) o[j] = butterfly_xor(o[j], lane, mask);
     }
-    butterfly_local<J>(o);
 #pragma unroll
-    for (int j = 0; j < J; ++j) o[j] *= __ldg(a.signs + lane + 32 * j) * (1.0f / D);
+    for (int j = 0; j < V; ++j) o[j] *= __ldg(a.signs + lane * V + j) * (1.0f / D);
   }
   store_out<D>(a, static_cast<long long>(b) * a.Hq + hq, lane, o);
 }
 
-// Rows of the query heads this CTA's head group owns: [h0 * G, (h0 + heads_per_cta) * G).
-template <int D>
-__device__ void merge_sequence(const SplitArgs &a, int b, long long s_lo, long long s_hi) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q0 = blockIdx.y * a.heads_per_cta * a.G, nq = a.heads_per_cta * a.G;
-  s_lo = max(0LL, min(s_lo, a.slots));  // never index outside the workspace
-  s_hi = max(s_lo, min(s_hi, a.slots));
-  for (int i = warp; i < nq; i += 8) merge_row<D>(a, b, q0 + i, s_lo, s_hi, lane);
-}
-
-template <int D>
-__device__ void zero_sequence(const SplitArgs &a, int b) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q0 = blockIdx.y * a.heads_per_cta * a.G, nq = a.heads_per_cta * a.G;
-  float z[D / 32];
-#pragma unroll
-  for (int j = 0; j < D / 32; ++j) z[j] = 0.f;
-  for (int i = warp; i < nq; i += 8) store_out<D>(a, static_cast<long long>(b) * a.Hq + q0 + i, lane, z);
-}
-
-// After a piece of sequence b (slot range of the sequence [s_lo, s_hi), nseg CTAs in total):
-// publish, take a ticket, and merge if this CTA is the last of the sequence.
-template <int D>
-__device__ void arrive_and_merge(const SplitArgs &a, int b, long long s_lo, long long s_hi, int nseg) {
-  __shared__ int s_last;
-  __syncthreads();  // every warp of the CTA has written its partial
-  if (threadIdx.x == 0) {
-    int last = 1;
-    if (nseg > 1) {
-      int *ctr = a.counters + static_cast<long long>(b) * gridDim.y + blockIdx.y;
-      __threadfence();  // release: this CTA's partials before its ticket
-      last = atomicAdd(ctr, 1) == nseg - 1;
-      if (last) {
-        *ctr = 0;         // every other CTA of the sequence has taken its ticket
-        __threadfence();  // acquire: the other CTAs' partials after their tickets
-      }
-    }
-    s_last = last;
-  }
-  __syncthreads();
-  if (s_last) merge_sequence<D>(a, b, s_lo, s_hi);
-}
-
-// CTA index of global page x under the balanced cut of P pages into C runs (q = P / C,
-// r = P % C: runs 0..r-1 have q + 1 pages, the others q).
-__device__ __forceinline__ long long cta_of_page(long long x, long long q, long long r) {
-  const long long big = r * (q + 1);
-  return x < big ? x / (q + 1) : r + (x - big) / q;
-}
-
-// Calls seg(b, t0, t1, slot) for every sequence piece of this CTA (all threads, same order),
-// each followed by the fused merge; also writes the zero rows of empty sequences.
-template <int D, typename SegFn>
+// Calls seg(b, t0, t1, slot) for every sequence piece of this CTA (all threads, same order).
+template <typename SegFn>
 __device__ __forceinline__ void for_each_piece(const SplitArgs &a, unsigned *flags, SegFn &&seg) {
   if (a.num_splits > 0) {
-    const int S = a.num_splits;
-    const int b = blockIdx.x / S, s = blockIdx.x % S;
+    const int b = blockIdx.x / a.num_splits, s = blockIdx.x % a.num_splits;
     const int L = clamped_len(a, b, flags);
-    if (L == 0) {
-      if (s == 0) zero_sequence<D>(a, b);
-      return;
-    }
-    const int span = (L + S - 1) / S;
+    const int span = (L + a.num_splits - 1) / a.num_splits;
     const int t0 = s * span;
     const int t1 = min(t0 + span, L);
-    if (t0 >= t1) return;
-    seg(b, t0, t1, static_cast<long long>(blockIdx.x));
-    const int nseg = (L + span - 1) / span;
-    arrive_and_merge<D>(a, b, static_cast<long long>(b) * S, static_cast<long long>(b) * S + nseg, nseg);
+    if (t0 < t1) seg(b, t0, t1, static_cast<long long>(blockIdx.x));
     return;
   }
   __shared__ long long s_scan[8];
   __shared__ long long s_first_p;
   __shared__ int s_first_b;
-  const long long C = gridDim.x, c = blockIdx.x;
   long long P_tot = 0;
   for (int base = 0; base < a.B; base += 256) {
     const int b = base + threadIdx.x;
@@ -225,8 +192,7 @@ __device__ __forceinline__ void for_each_piece(const SplitArgs &a, unsigned *fla
     block_scan_256(np, s_scan, &chunk);
     P_tot += chunk;
   }
-  for (long long b = c; b < a.B; b += C)  // empty sequences: CTA b % C writes their zero rows
-    if (clamped_len(a, static_cast<int>(b), nullptr) == 0) zero_sequence<D>(a, static_cast<int>(b));
+  const long long C = gridDim.x, c = blockIdx.x;
   const long long q = P_tot / C, r = P_tot % C;
   const long long pb = c * q + min(c, r), pe = pb + q + (c < r ? 1 : 0);
   if (pb >= pe) return;
@@ -256,9 +222,11 @@ __device__ __forceinline__ void for_each_piece(const SplitArgs &a, unsigned *fla
       const long long lo = max(pb, P) - P, hi = min(pe, P + np) - P;
       const int t0 = static_cast<int>(lo * kPage);
       const int t1 = static_cast<int>(min(hi * kPage, static_cast<long long>(L)));
+      if (threadIdx.x == 0 && blockIdx.y == 0) {
+        if (P >= pb) a.seg_first[b] = static_cast<int>(c);
+        if (P + np <= pe) a.seg_last[b] = static_cast<int>(c);
+      }
       seg(b, t0, t1, c + b);
-      const long long c_first = cta_of_page(P, q, r), c_last = cta_of_page(P + np - 1, q, r);
-      arrive_and_merge<D>(a, b, c_first + b, c_last + b + 1, static_cast<int>(c_last - c_first + 1));
     }
     P += np;
     ++b;
@@ -286,6 +254,38 @@ __device__ __forceinline__ void store_partial(const SplitArgs &a, long long slot
     for (int i = 0; i < D / 32; ++i) dst[i] = make_float4(o1[4 * i], o1[4 * i + 1], o1[4 * i + 2], o1[4 * i + 3]);
     if (g == 0) a.part_lse[row + n1] = lse1;
   }
+}
+
+// One warp per output row (b, hq). Launched as a programmatic dependent of the split kernel:
+// griddepcontrol.wait holds it until that grid has finished and its writes are visible.
+template <int D>
+__global__ void __launch_bounds__(256) merge_kernel(const SplitArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int V = D / 32;
+  const int lane = threadIdx.x & 31;
+  const long long idx = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (idx >= static_cast<long long>(a.B) * a.Hq) return;
+  const int b = static_cast<int>(idx / a.Hq), hq = static_cast<int>(idx % a.Hq);
+  const int L = clamped_len(a, b, nullptr);  // the split kernel already flagged it
+  if (L == 0) {
+    float z[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) z[j] = 0.f;
+    store_out<D>(a, idx, lane, z);
+    return;
+  }
+  long long s_lo, s_hi;  // slot range [s_lo, s_hi)
+  if (a.num_splits > 0) {
+    const int span = (L + a.num_splits - 1) / a.num_splits;
+    s_lo = static_cast<long long>(b) * a.num_splits;
+    s_hi = s_lo + (L + span - 1) / span;
+  } else {
+    s_lo = static_cast<long long>(a.seg_first[b]) + b;
+    s_hi = static_cast<long long>(a.seg_last[b]) + b + 1;
+  }
+  s_lo = max(0LL, min(s_lo, a.slots));  // never index outside the workspace
+  s_hi = max(s_lo, min(s_hi, a.slots));
+  merge_row<D>(a, b, hq, s_lo, s_hi, lane);
 }
 
 }  // namespace kvq

@@ -6,7 +6,8 @@
 // zero-point applied through the split-dot correction
 //     S = (sum_d q_d n_d - zp * sum_d q_d) * scale_k * sm,
 // values enter the P.V product as P_v = p * scale_v with the correction - sum(P_v * zp_v), and
-// the per-split results are merged by log-sum-exp and rotated back (decode_common.cuh).
+// the per-split results are merged by log-sum-exp and rotated back (decode_common.cuh, a second
+// kernel launched as a programmatic dependent).
 //
 // GB300 design. One warp owns one (kv head, run of pages) and streams it through a private
 // NSTAGE-deep cp.async ring in shared memory: each lane copies exactly the bytes its MMA
@@ -308,6 +309,7 @@ __device__ __forceinline__ void int4_piece(const Int4Params &p, uint8_t *ring, u
 template <int D, int NSTAGE>
 __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const Int4Params p) {
   extern __shared__ __align__(16) uint8_t smem[];
+  asm volatile("griddepcontrol.launch_dependents;");  // let the merge kernel's launch begin early
   using Gm = Int4Geom<D>;
   const int warp = threadIdx.x >> 5;
   uint8_t *ring = smem + warp * (NSTAGE * Gm::STAGE + Gm::QBYTES);
@@ -315,7 +317,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const Int4Params p)
   const int hl = warp % p.s.heads_per_cta;
   const int sub = warp / p.s.heads_per_cta;
   const int h = blockIdx.y * p.s.heads_per_cta + hl;
-  for_each_piece<D>(p.s, &g_flags_decode_int4, [&](int b, int t0, int t1, long long slot) {
+  for_each_piece(p.s, &g_flags_decode_int4, [&](int b, int t0, int t1, long long slot) {
     int4_piece<D, NSTAGE>(p, ring, qarea, b, h, sub, t0, t1, slot);
   });
 }
@@ -349,6 +351,10 @@ static kvq_status launch_int4(const Int4Params &p, const SplitPlan &plan, cudaSt
   }
   const dim3 grid(plan.seg_ctas, plan.head_groups);
   decode_int4_kernel<D, kStagesInt4><<<grid, 256, smem, s>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  const long long rows = static_cast<long long>(p.s.B) * p.s.Hq;
+  if (launch_dependent(merge_kernel<D>, dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), s, p.s) != cudaSuccess)
+    return KVQ_ERR_CUDA;
   return launch_status();
 }
 
@@ -397,7 +403,7 @@ extern "C" kvq_status kvq_decode_int4(const void *q, const uint8_t *k_cache, con
   sa.heads_per_cta = plan.heads_per_cta;
   sa.warps_per_head = plan.warps_per_head;
   sa.slots = plan.slots;
-  workspace_carve(workspace, Hq, D, plan, &sa.part_o, &sa.part_lse, &sa.counters);
+  workspace_carve(workspace, B, Hq, D, plan, &sa.part_o, &sa.part_lse, &sa.seg_first, &sa.seg_last);
   sa.signs = rht_signs;
   sa.out = out;
   sa.out_dtype = out_dtype;

@@ -8,7 +8,7 @@
 // acc / l and lse per split, and the splits are merged by log-sum-exp (decode_common.cuh).
 //
 // GB300 design: the INT4 kernel's structure (one warp per kv head and run of pages, private
-// cp.async ring, mma.m16n8k16 for both contractions, merge fused into the kernel). Keys go to
+// cp.async ring, mma.m16n8k16 for both contractions, separate merge kernel). Keys go to
 // fp16 with the hardware E4M3x2 -> f16x2 conversion (exact); q (fp32) is split into fp16 hi + lo
 // parts, two MMAs per k-step, so the score keeps ~22 bits. Value indices enter as exact fp16
 // subnormals (the index bits masked into a zero-exponent fp16: idx * 2^-24, or idx * 2^-20 for a
@@ -299,6 +299,7 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
 template <int D, int VBITS, int NSTAGE>
 __global__ void __launch_bounds__(256, 2) decode_tq_kernel(const TqParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
+  asm volatile("griddepcontrol.launch_dependents;");  // let the merge kernel's launch begin early
   using Gm = TqGeom<D, VBITS>;
   const int warp = threadIdx.x >> 5;
   uint8_t *ring = smem + warp * (NSTAGE * Gm::STAGE + Gm::QBYTES);
@@ -306,7 +307,7 @@ __global__ void __launch_bounds__(256, 2) decode_tq_kernel(const TqParams p) {
   const int hl = warp % p.s.heads_per_cta;
   const int sub = warp / p.s.heads_per_cta;
   const int h = blockIdx.y * p.s.heads_per_cta + hl;
-  for_each_piece<D>(p.s, &g_flags_decode_tq, [&](int b, int t0, int t1, long long slot) {
+  for_each_piece(p.s, &g_flags_decode_tq, [&](int b, int t0, int t1, long long slot) {
     tq_piece<D, VBITS, NSTAGE>(p, ring, qarea, b, h, sub, t0, t1, slot);
   });
 }
@@ -336,6 +337,10 @@ static kvq_status launch_tq(const TqParams &p, const SplitPlan &plan, cudaStream
   }
   const dim3 grid(plan.seg_ctas, plan.head_groups);
   decode_tq_kernel<D, VBITS, kStagesTq><<<grid, 256, smem, s>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  const long long rows = static_cast<long long>(p.s.B) * p.s.Hq;
+  if (launch_dependent(merge_kernel<D>, dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), s, p.s) != cudaSuccess)
+    return KVQ_ERR_CUDA;
   return launch_status();
 }
 
@@ -380,7 +385,7 @@ extern "C" kvq_status kvq_decode_tq(const float *q, const uint8_t *kv_cache, int
   sa.heads_per_cta = plan.heads_per_cta;
   sa.warps_per_head = plan.warps_per_head;
   sa.slots = plan.slots;
-  workspace_carve(workspace, Hq, D, plan, &sa.part_o, &sa.part_lse, &sa.counters);
+  workspace_carve(workspace, B, Hq, D, plan, &sa.part_o, &sa.part_lse, &sa.seg_first, &sa.seg_last);
   sa.signs = nullptr;
   sa.out = out;
   sa.out_dtype = KVQ_F32;

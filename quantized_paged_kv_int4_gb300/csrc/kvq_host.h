@@ -34,10 +34,26 @@ struct SplitPlan {
 };
 bool make_plan(int B, int Hk, int num_splits, SplitPlan *plan);
 // Workspace: partial outputs [slots * warps_per_head, Hq, D] fp32, their log-sum-exps
-// [slots * warps_per_head, Hq] fp32, then the merge tickets [B * head_groups] int32 (each region
-// 256-byte aligned). The tickets must be zero when a call starts; every call leaves them zero.
+// [slots * warps_per_head, Hq] fp32, then seg_first / seg_last [B] int32 (each region 256-byte
+// aligned). Needs no initialisation.
 size_t workspace_bytes(int B, int Hq, int D, const SplitPlan &plan);
-void workspace_carve(void *workspace, int Hq, int D, const SplitPlan &plan, float **part_o,
-                     float **part_lse, int32_t **counters);
+void workspace_carve(void *workspace, int B, int Hq, int D, const SplitPlan &plan, float **part_o,
+                     float **part_lse, int32_t **seg_first, int32_t **seg_last);
+
+// Launch the log-sum-exp merge as a programmatic dependent of the kernel just enqueued on s.
+template <typename Args>
+cudaError_t launch_dependent(void (*kernel)(Args), dim3 grid, dim3 block, cudaStream_t s, const Args &a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
 
 }  // namespace kvq

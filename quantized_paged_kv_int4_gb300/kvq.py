@@ -133,16 +133,16 @@ def kvq_decode_workspace_bytes(B, Hq, Hk, D, num_splits=0):
 
 
 def decode_workspace(B, Hq, Hk, D, num_splits=0, device=None):
-    """A zero-filled workspace for kvq_decode_int4 / kvq_decode_tq (reusable across calls)."""
+    """A workspace for kvq_decode_int4 / kvq_decode_tq (reusable across calls on one stream)."""
     need = kvq_decode_workspace_bytes(B, Hq, Hk, D, num_splits)
     if need == 0:
         raise ValueError("unsupported decode shape")
-    return torch.zeros((need,), dtype=torch.uint8, device=device)
+    return torch.empty((need,), dtype=torch.uint8, device=device)
 
 
 def _workspace(workspace, need, device):
     if workspace is None:
-        return torch.zeros((max(need, 16),), dtype=torch.uint8, device=device)
+        return torch.empty((max(need, 16),), dtype=torch.uint8, device=device)
     _need(workspace, "workspace", torch.uint8)
     return workspace
 

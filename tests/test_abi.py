@@ -85,14 +85,14 @@ def test_decode_validation_without_gpu():
 
 def test_workspace_sizes_fixed_splits():
     # fixed splits need no device query: slots = B * S, 8 / Hk warps per head, Hq rows of D + lse,
-    # then one merge ticket per (sequence, head group)
+    # then the first / last CTA of each sequence
     n = kvq.kvq_decode_workspace_bytes(2, 4, 2, 64, 4)
     rows = 2 * 4 * 4 * 4
     r256 = lambda x: (x + 255) // 256 * 256
-    assert n == r256(rows * 64 * 4) + r256(rows * 4) + r256(2 * 4)
+    assert n == r256(rows * 64 * 4) + r256(rows * 4) + 2 * r256(2 * 4)
     n16 = kvq.kvq_decode_workspace_bytes(3, 32, 16, 128, 2)   # 2 head groups of 8 kv heads
     rows = 3 * 2 * 1 * 32
-    assert n16 == r256(rows * 128 * 4) + r256(rows * 4) + r256(3 * 2 * 4)
+    assert n16 == r256(rows * 128 * 4) + r256(rows * 4) + 2 * r256(3 * 4)
     assert kvq.kvq_decode_workspace_bytes(2, 4, 2, 80, 4) == 0
     assert kvq.kvq_decode_workspace_bytes(2, 4, 3, 64, 4) == 0
 

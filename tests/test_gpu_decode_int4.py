@@ -132,7 +132,7 @@ def test_long_context_40gb_pool_sampled():
 
 
 def test_workspace_reused_across_calls():
-    """One zero-filled workspace serves consecutive calls: the merge tickets reset themselves."""
+    """One workspace serves consecutive calls with identical results."""
     case = workloads.DecodeCase("reuse", 5, 16, 4, 128, [700, 1, 0, 2000, 333], seed=21, outlier_channels=4)
     c = Int4Case(case)
     g = c.to_gpu()
