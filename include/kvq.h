@@ -133,6 +133,39 @@ KVQ_API kvq_status kvq_decode_int4(const void *q, const uint8_t *k_cache, const 
                            kvq_stream_t stream);
 
 /*
+ * kvq_decode_int4_noalloc -- kvq_decode_int4 for callers that must not allocate device memory.
+ * The pages have no counterpart of this call; it exists for users of this library, not for the
+ * method.
+ *
+ * Some callers cannot call cudaMalloc or own a device buffer of their own: a plug-in inside a
+ * serving process whose allocator has already reserved all of HBM for its paged KV pool, a C
+ * caller with no access to the host framework's caching allocator, or a latency-critical path
+ * where an allocation's implicit device synchronization is not acceptable. This entry point
+ * takes the same arguments as kvq_decode_int4 except the workspace, which it replaces with a
+ * file-scope device array of KVQ_NOALLOC_SCRATCH_BYTES bytes inside the library (every GPU that
+ * loads the library holds that array until the process exits). It calls no allocating routine.
+ *
+ *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ *     with that device current); make that first call before any stream capture.
+ *   - A call whose scratch need, kvq_decode_workspace_bytes(B, Hq, Hk, D, num_splits), exceeds
+ *     KVQ_NOALLOC_SCRATCH_BYTES is rejected with KVQ_ERR_WORKSPACE before anything is launched.
+ *   - Every call on a device shares the one array and overwrites what the previous call left
+ *     there (nothing in it needs to start at zero). Calls that may overlap on the GPU -- on
+ *     different streams without ordering, or from several threads -- race on it and corrupt
+ *     each other's results: order them on one stream.
+ */
+#define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+KVQ_API kvq_status kvq_decode_int4_noalloc(const void *q, const uint8_t *k_cache,
+                                           const uint8_t *v_cache, const float *k_scale,
+                                           const float *v_scale, const int32_t *block_table,
+                                           int32_t max_blocks, const int32_t *seq_lens,
+                                           const float *rht_signs, float softmax_scale,
+                                           int32_t num_splits, void *out, kvq_dtype out_dtype,
+                                           int32_t B, int32_t Hq, int32_t Hk, int32_t D,
+                                           int32_t block_size, int64_t num_blocks,
+                                           kvq_stream_t stream);
+
+/*
  * kvq_decode_tq -- paged decode attention over the TurboQuant combined slot with FP8 keys.
  * Defined by triton_turboquant_decode.py, triton_turboquant_decode_attention and
  * _tq_decode_stage1 with KEY_FP8 = 1, followed by the split merge (_fwd_kernel_stage2).

@@ -24,6 +24,8 @@
 //     fragments with one PRMT per pair of m-tiles.
 // The G query heads of a kv head share every K/V byte loaded (GQA), padded to the MMA's N = 8.
 
+#include <mutex>
+
 #include "decode_common.cuh"
 #include "kvq_host.h"
 
@@ -418,4 +420,48 @@ extern "C" kvq_status kvq_decode_int4(const void *q, const uint8_t *k_cache, con
   p.num_blocks = num_blocks;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return D == 128 ? launch_int4<128>(p, plan, s) : launch_int4<64>(p, plan, s);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Allocation-free variant: the same decode with its scratch in a device array of this library.
+// ---------------------------------------------------------------------------------------------
+namespace kvq {
+
+// Scratch of kvq_decode_int4_noalloc: one array per GPU that loads the library, kept until exit.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
+
+// Device address of the array on the current device, looked up once per device. In host code
+// g_noalloc_scratch names a host-side stand-in, never a device address.
+static void *noalloc_scratch() {
+  static std::mutex mu;
+  static void *addr[64] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace kvq
+
+extern "C" kvq_status kvq_decode_int4_noalloc(const void *q, const uint8_t *k_cache,
+                                              const uint8_t *v_cache, const float *k_scale,
+                                              const float *v_scale, const int32_t *block_table,
+                                              int32_t max_blocks, const int32_t *seq_lens,
+                                              const float *rht_signs, float softmax_scale,
+                                              int32_t num_splits, void *out, kvq_dtype out_dtype,
+                                              int32_t B, int32_t Hq, int32_t Hk, int32_t D,
+                                              int32_t block_size, int64_t num_blocks,
+                                              kvq_stream_t stream) {
+  void *scratch = kvq::noalloc_scratch();
+  if (scratch == nullptr) return KVQ_ERR_CUDA;
+  // The workspace entry point validates everything and rejects a scratch need above the array
+  // size with KVQ_ERR_WORKSPACE before launching anything.
+  return kvq_decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, max_blocks, seq_lens,
+                         rht_signs, softmax_scale, num_splits, scratch, KVQ_NOALLOC_SCRATCH_BYTES,
+                         out, out_dtype, B, Hq, Hk, D, block_size, num_blocks, stream);
 }

@@ -24,7 +24,8 @@ KVQ_BF16, KVQ_F16, KVQ_F32 = 0, 1, 2
 
 # the C API's declared functions, in header order
 C_FUNCTIONS = ("kvq_status_string", "kvq_abi_version", "kvq_write_int4", "kvq_decode_workspace_bytes",
-               "kvq_decode_int4", "kvq_decode_tq", "kvq_fwht128", "kvq_device_error")
+               "kvq_decode_int4", "kvq_decode_int4_noalloc", "kvq_decode_tq", "kvq_fwht128", "kvq_device_error")
+KVQ_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lock = threading.Lock()
 _handle = None
@@ -38,6 +39,8 @@ _SIGS = {
     "kvq_decode_workspace_bytes": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32]),
     "kvq_decode_int4": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_f32, c_i32, c_p, c_sz,
                                        c_p, ctypes.c_int, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_p]),
+    "kvq_decode_int4_noalloc": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_f32, c_i32, c_p,
+                                               ctypes.c_int, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_p]),
     "kvq_decode_tq": (ctypes.c_int, [c_p, c_p, c_i32, c_i32, c_p, c_i32, c_p, c_f32, c_i32, c_p, c_sz, c_p,
                                      c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_p]),
     "kvq_fwht128": (ctypes.c_int, [c_p, c_p, c_p, c_i64, c_p]),
@@ -171,6 +174,31 @@ def kvq_decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens
                                  float(softmax_scale), num_splits, _ptr(workspace), workspace.numel(),
                                  _ptr(out), _out_code(out.dtype), B, Hq, Hk, D, bs, nb, _stream(stream)),
            "kvq_decode_int4")
+    return out
+
+
+def kvq_decode_int4_noalloc(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, rht_signs,
+                            softmax_scale, out, num_splits=0, stream=None):
+    """kvq_decode_int4 without a caller workspace: the library's own device scratch array is used
+    (KVQ_NOALLOC_SCRATCH_BYTES per GPU, shared by every call: order such calls on one stream).
+    For callers that cannot allocate device memory; `out` must be given. Returns out."""
+    _need(q, "q", torch.bfloat16)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.uint8)
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _need(t, n, torch.float32)
+    _need(block_table, "block_table", torch.int32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    _need(out, "out")
+    if rht_signs is not None:
+        _need(rht_signs, "rht_signs", torch.float32)
+    B, Hq, D = q.shape
+    nb, bs, Hk = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    _check(lib().kvq_decode_int4_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                         _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(rht_signs),
+                                         float(softmax_scale), num_splits, _ptr(out), _out_code(out.dtype),
+                                         B, Hq, Hk, D, bs, nb, _stream(stream)),
+           "kvq_decode_int4_noalloc")
     return out
 
 
