@@ -111,7 +111,8 @@ KVQ_API size_t kvq_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hk, int
  * Rows with seq_lens[b] == 0 are written as zeros.
  *
  *   q            bf16 [B, Hq, D] contiguous, 16-byte aligned.
- *   k_cache...   as kvq_write_int4; block_size must be 16.
+ *   k_cache...   as kvq_write_int4; block_size must be 16. The decode reads pages with TMA
+ *                tensor copies, so k_scale and v_scale must be 16-byte aligned here.
  *   block_table  int32 [B, max_blocks]; entries at or past page ceil(seq_lens[b]/16) are not read.
  *   seq_lens     int32 [B]; values are clamped to [0, 16*max_blocks] (a clamp raises the flag).
  *   workspace    >= kvq_decode_workspace_bytes(B, Hq, Hk, D, num_splits) bytes, 16-byte aligned;

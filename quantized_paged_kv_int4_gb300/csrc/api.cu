@@ -1,5 +1,8 @@
 // libkvq host glue: status strings, split planning and workspace sizing, device-flag readout.
 
+#include <cudaTypedefs.h>
+
+#include <cstring>
 #include <mutex>
 
 #include "kvq_host.h"
@@ -45,6 +48,91 @@ bool make_plan(int B, int Hk, int num_splits, SplitPlan *plan) {
     plan->seg_ctas = (2 * sms + plan->head_groups - 1) / plan->head_groups;
     plan->slots = static_cast<long long>(plan->seg_ctas) + B;
   }
+  return true;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool int4_tensor_maps(const void *k_cache, const void *v_cache, const void *k_scale, const void *v_scale,
+                      long long num_blocks, int Hk, int D, Int4Maps *maps) {
+  struct Entry {
+    const void *kc, *vc, *ks, *vs;
+    long long nb;
+    int hk, d;
+    Int4Maps maps;
+  };
+  static std::mutex mu;
+  static Entry cache[16];
+  static int n_cached = 0, next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_cached; ++i) {
+    const Entry &e = cache[i];
+    if (e.kc == k_cache && e.vc == v_cache && e.ks == k_scale && e.vs == v_scale && e.nb == num_blocks &&
+        e.hk == Hk && e.d == D) {
+      *maps = e.maps;
+      return true;
+    }
+  }
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_tiled();
+  if (enc == nullptr) return false;
+  Int4Maps m;
+  std::memset(&m, 0, sizeof(m));
+  const cuuint64_t rb = static_cast<cuuint64_t>(D / 2);
+  const cuuint64_t kv_dim[4] = {rb, static_cast<cuuint64_t>(Hk), 16, static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t kv_stride[3] = {rb, rb * Hk, rb * Hk * 16};
+  const cuuint32_t kv_box[4] = {static_cast<cuuint32_t>(rb), 1, 16, 1};
+  const cuuint32_t ones[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle sw = D == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  for (int i = 0; i < 2; ++i) {
+    if (enc(i ? &m.v : &m.k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(i ? v_cache : k_cache), kv_dim,
+            kv_stride, kv_box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  for (int i = 0; i < 2; ++i) {
+    CUtensorMap *dst = i ? &m.vs : &m.ks;
+    void *base = const_cast<void *>(i ? v_scale : k_scale);
+    CUresult r;
+    if (Hk % 4 == 0) {
+      const cuuint64_t dim[3] = {static_cast<cuuint64_t>(Hk), 16, static_cast<cuuint64_t>(num_blocks)};
+      const cuuint64_t stride[2] = {4ull * Hk, 64ull * Hk};
+      const cuuint32_t box[3] = {4, 16, 1};
+      r = enc(dst, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, base, dim, stride, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+      const cuuint64_t dim[2] = {16ull * Hk, static_cast<cuuint64_t>(num_blocks)};
+      const cuuint64_t stride[1] = {64ull * Hk};
+      const cuuint32_t box[2] = {static_cast<cuuint32_t>(16 * Hk), 1};
+      r = enc(dst, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, base, dim, stride, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) return false;
+  }
+  m.scale_heads = Hk % 4 == 0 ? 4 : Hk;
+  Entry &e = cache[next];
+  e.kc = k_cache;
+  e.vc = v_cache;
+  e.ks = k_scale;
+  e.vs = v_scale;
+  e.nb = num_blocks;
+  e.hk = Hk;
+  e.d = D;
+  e.maps = m;
+  next = (next + 1) % 16;
+  if (n_cached < 16) ++n_cached;
+  *maps = m;
   return true;
 }
 

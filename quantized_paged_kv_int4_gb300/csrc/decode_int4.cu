@@ -10,9 +10,11 @@
 // kernel launched as a programmatic dependent).
 //
 // GB300 design. One warp owns one (kv head, run of pages) and streams it through a private
-// NSTAGE-deep cp.async ring in shared memory: each lane copies exactly the bytes its MMA
-// fragments need (16 B of each of two K rows, 8 B of four V rows, one scale word), so the ring
-// needs no layout transform and no block-wide barrier. Both contractions run on the tensor
+// NSTAGE-deep ring in shared memory filled by TMA: per page, one lane issues four tensor loads
+// (this head's 16 K rows and 16 V rows, gathered from the page's [token][head] rows into a
+// [token] tile with the 64B/32B swizzle that makes the fragment reads conflict-free, and the
+// scale-word boxes) completing on the stage's mbarrier; waits are bounded and report a flag.
+// No block-wide barrier is needed. Both contractions run on the tensor
 // cores (mma.m16n8k16, fp16 operands, fp32 accumulation) on exact operands: a nibble pair
 // masked into an fp16 pair with a zero exponent field IS the pair of fp16 subnormals n * 2^-24
 // (low nibble) or n * 2^-20 (high nibble), so one LOP3 turns 2 nibbles into MMA operands
@@ -34,10 +36,9 @@ namespace kvq {
 __device__ unsigned g_flags_decode_int4 = 0;
 
 struct Int4Params {
+  Int4Maps maps;  // TMA descriptors of the K / V pools and their scale words (64-byte aligned)
   SplitArgs s;
   const __nv_bfloat16 *q;
-  const uint8_t *k_cache, *v_cache;
-  const uint32_t *k_scale, *v_scale;
   const int32_t *block_table;
   float sm_log2;  // softmax scale (divided by D when rotating) times log2(e)
   int64_t num_blocks;
@@ -50,20 +51,31 @@ constexpr float kTwo20 = 1048576.0f;
 
 template <int D>
 struct Int4Geom {
-  static constexpr int KCH = D / 8;    // K bytes per lane per row
-  static constexpr int VCH = D / 16;   // V bytes per lane per token
-  static constexpr int KB = 64 * KCH;  // K bytes per stage (2 rows x 32 lanes)
-  static constexpr int VB = 128 * VCH; // V bytes per stage (4 tokens x 32 lanes)
-  static constexpr int STAGE = KB + VB + 128;
-  static constexpr int WPR = D / 32;   // K words per lane per row
+  static constexpr int RB = D / 2;        // bytes per token row of one head
+  static constexpr int KCH = D / 8;       // K bytes per lane per row
+  static constexpr int VCH = D / 16;      // V bytes per lane per token
+  static constexpr int TILE = 16 * RB;    // one head's page of one pool (TMA box)
+  static constexpr int KVSTAGE = 2 * TILE < 1024 ? 1024 : 2 * TILE;  // K tile, V tile; 1024-aligned
+  static constexpr int SCSTAGE = 2 * 16 * 4 * 4;                     // K, V scale boxes (<= 4 heads)
+  static constexpr int WPR = D / 32;      // K words per lane per row
   static constexpr int KSTEPS = D / 16;
-  static constexpr int MT = D / 16;    // m-tiles of the PV product
+  static constexpr int MT = D / 16;       // m-tiles of the PV product
   static constexpr int QBYTES = 8 * D * 2 + 64;
 };
 
+// Per-warp TMA ring state, carried across the pieces of a CTA: pages issued / consumed so far
+// (stage = count % NSTAGE, phase parity = (count / NSTAGE) & 1) and a sticky abort bit.
+struct Ring {
+  uint8_t *kv;     // NSTAGE x KVSTAGE bytes, 1024-aligned
+  uint8_t *sc;     // NSTAGE x SCSTAGE bytes
+  uint32_t bars;   // shared address of NSTAGE mbarriers
+  uint32_t issued, consumed;
+  bool abort;
+};
+
 template <int D, int NSTAGE>
-__device__ __forceinline__ void int4_piece(const Int4Params &p, uint8_t *ring, uint8_t *qarea,
-                                           int b, int h, int sub, int t0, int t1, long long slot) {
+__device__ __forceinline__ void int4_piece(const Int4Params &p, Ring &rg, uint8_t *qarea, int b, int h,
+                                           int sub, int t0, int t1, long long slot) {
   using Gm = Int4Geom<D>;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -139,35 +151,52 @@ __device__ __forceinline__ void int4_piece(const Int4Params &p, uint8_t *ring, u
   const float sm24 = p.sm_log2 * kTwo24;  // the K operands carry a factor 2^-24
   __syncwarp();
 
-  // -------- cp.async ring
-  const uint32_t ring_s = smem_u32(ring);
-  const long long row_stride = static_cast<long long>(Hk) * (D / 2);  // bytes between token rows
-  const long long page_bytes = kPage * row_stride;                     // one page of one pool
-  const uint8_t *kbase = p.k_cache + h * (D / 2) + g * row_stride + t * Gm::KCH;
-  const uint8_t *vbase = p.v_cache + h * (D / 2) + 2 * t * row_stride + g * Gm::VCH;
-  const uint32_t *sbase = (lane < 16 ? p.k_scale : p.v_scale) + h + (lane & 15) * Hk;
+  // -------- TMA ring: per page, lane 0 loads this head's 16 K rows and 16 V rows (swizzled
+  // boxes) plus the scale-word boxes, all completing on the stage's mbarrier.
+  const int SH = p.maps.scale_heads;                 // heads per scale box
+  const int hh = SH == 4 ? (h & 3) : h;              // this head's column in the scale box
+  const int sc_h0 = SH == 4 ? (h & ~3) : 0;
+  constexpr uint32_t kTx = 2 * Gm::TILE;             // + the two scale boxes (below)
+  const uint32_t tx = kTx + 2 * 16 * SH * 4;
   auto issue = [&](int k) {
     const int kk = k & 31;
     if (k > 0 && kk == 0) {
       bids_cur = bids_next;
       bids_next = load_bids((k >> 5) + 1);
     }
-    const int blk = __shfl_sync(FULL, bids_cur, kk);
-    const bool in = k < n_my;
-    const bool ok = in && blk >= 0 && blk < p.num_blocks;
-    if (in && !ok && lane == 0) atomicOr(&g_flags_decode_int4, ERR_BLOCK);
-    const uint32_t st = ring_s + (k % NSTAGE) * Gm::STAGE;
-    const long long pg = static_cast<long long>(ok ? blk : 0);
-    const uint8_t *kb = kbase + pg * page_bytes;
-    cp_async<Gm::KCH>(st + lane * Gm::KCH, kb, ok);
-    cp_async<Gm::KCH>(st + (32 + lane) * Gm::KCH, kb + 8 * row_stride, ok);
-    const uint8_t *vb = vbase + pg * page_bytes;
-    cp_async<Gm::VCH>(st + Gm::KB + lane * Gm::VCH, vb, ok);                          // token 2t
-    cp_async<Gm::VCH>(st + Gm::KB + (32 + lane) * Gm::VCH, vb + row_stride, ok);      // 2t + 1
-    cp_async<Gm::VCH>(st + Gm::KB + (64 + lane) * Gm::VCH, vb + 8 * row_stride, ok);  // 2t + 8
-    cp_async<Gm::VCH>(st + Gm::KB + (96 + lane) * Gm::VCH, vb + 9 * row_stride, ok);  // 2t + 9
-    cp_async<4>(st + Gm::KB + Gm::VB + lane * 4, sbase + pg * (kPage * Hk), ok);
-    cp_async_commit();
+    const int blk_raw = __shfl_sync(FULL, bids_cur, kk);
+    if (k >= n_my) return;
+    const bool ok = blk_raw >= 0 && blk_raw < p.num_blocks;
+    const int blk = ok ? blk_raw : 0;  // out of range: flagged, page 0 read instead
+    const int stg = static_cast<int>(rg.issued % NSTAGE);
+    ++rg.issued;
+    if (lane == 0) {
+      if (!ok) atomicOr(&g_flags_decode_int4, ERR_BLOCK);
+      const uint32_t bar = rg.bars + 8 * stg;
+      const uint32_t kv = smem_u32(rg.kv + stg * Gm::KVSTAGE), sc = smem_u32(rg.sc + stg * Gm::SCSTAGE);
+      fence_proxy_async();
+      mbar_arrive_expect_tx(bar, tx);
+      tma_load_4d(kv, &p.maps.k, 0, h, 0, blk, bar);
+      tma_load_4d(kv + Gm::TILE, &p.maps.v, 0, h, 0, blk, bar);
+      if (SH == 4) {
+        tma_load_3d(sc, &p.maps.ks, sc_h0, 0, blk, bar);
+        tma_load_3d(sc + Gm::SCSTAGE / 2, &p.maps.vs, sc_h0, 0, blk, bar);
+      } else {
+        tma_load_2d(sc, &p.maps.ks, 0, blk, bar);
+        tma_load_2d(sc + Gm::SCSTAGE / 2, &p.maps.vs, 0, blk, bar);
+      }
+    }
+  };
+  // wait for the next page; on a timeout (a copy that never completes) raise the flag and abort
+  auto wait_next = [&]() -> bool {
+    const uint32_t stg = rg.consumed % NSTAGE, par = (rg.consumed / NSTAGE) & 1;
+    const bool ok = mbar_wait(rg.bars + 8 * stg, par);
+    if (!__all_sync(FULL, ok)) {
+      if (lane == 0) atomicOr(&g_flags_decode_int4, ERR_TIMEOUT);
+      rg.abort = true;
+      return false;
+    }
+    return true;
   };
 
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, pz0 = 0.f, pz1 = 0.f;
@@ -175,30 +204,33 @@ __device__ __forceinline__ void int4_piece(const Int4Params &p, uint8_t *ring, u
 #pragma unroll
   for (int i = 0; i < Gm::MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
+  if (rg.abort) return;
 #pragma unroll
   for (int k = 0; k < NSTAGE - 1; ++k) issue(k);
 
   for (int k = 0; k < n_my; ++k) {
     issue(k + NSTAGE - 1);
-    cp_async_wait<NSTAGE - 1>();
-    __syncwarp();
-    const uint8_t *st = ring + (k % NSTAGE) * Gm::STAGE;
+    const uint32_t stg = rg.consumed % NSTAGE;
+    if (!wait_next()) break;
+    ++rg.consumed;
+    const uint8_t *kt = rg.kv + stg * Gm::KVSTAGE, *vt = kt + Gm::TILE;
+    const uint32_t *sk = reinterpret_cast<const uint32_t *>(rg.sc + stg * Gm::SCSTAGE);
+    const uint32_t *sv = sk + Gm::SCSTAGE / 8;
     const int nb = (first + k * WPH) * kPage;  // position of the page's row 0
     const bool ok0 = nb + g >= t0 && nb + g < t1;
     const bool ok1 = nb + g + 8 >= t0 && nb + g + 8 < t1;
 
     // ---- scores: S = (sum_d q_d n_d - zp sum_d q_d) * scale_k * sm (base 2)
-    const uint8_t *sb = st + Gm::KB + Gm::VB;
-    const uint32_t kw0 = lds32(sb + g * 4), kw1 = lds32(sb + (g + 8) * 4);
+    const uint32_t kw0 = sk[g * SH + hh], kw1 = sk[(g + 8) * SH + hh];
     float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};  // two MMA chains
     {
       uint32_t wa[Gm::WPR], wb[Gm::WPR];
       if constexpr (Gm::WPR == 4) {
-        const uint4 a4 = lds128(st + lane * 16), b4 = lds128(st + (32 + lane) * 16);
+        const uint4 a4 = lds128(kt + swz<Gm::RB>(g, 16 * t)), b4 = lds128(kt + swz<Gm::RB>(g + 8, 16 * t));
         wa[0] = a4.x; wa[1] = a4.y; wa[2] = a4.z; wa[3] = a4.w;
         wb[0] = b4.x; wb[1] = b4.y; wb[2] = b4.z; wb[3] = b4.w;
       } else {
-        const uint2 a2 = lds64(st + lane * 8), b2 = lds64(st + (32 + lane) * 8);
+        const uint2 a2 = lds64(kt + swz<Gm::RB>(g, 8 * t)), b2 = lds64(kt + swz<Gm::RB>(g + 8, 8 * t));
         wa[0] = a2.x; wa[1] = a2.y;
         wb[0] = b2.x; wb[1] = b2.y;
       }
@@ -211,7 +243,7 @@ __device__ __forceinline__ void int4_piece(const Int4Params &p, uint8_t *ring, u
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) c[i] += c2[i];
-    const uint32_t vw0 = lds32(sb + (16 + g) * 4), vw1 = lds32(sb + (24 + g) * 4);
+    const uint32_t vw0 = sv[g * SH + hh], vw1 = sv[(g + 8) * SH + hh];
     const float ck0 = __uint_as_float(kw0 & ~0xFu) * sm24, ck1 = __uint_as_float(kw1 & ~0xFu) * sm24;
     const float zk0 = static_cast<float>(kw0 & 0xFu), zk1 = static_cast<float>(kw1 & 0xFu);
     const float s00 = ok0 ? (c[0] - zk0 * qs0) * ck0 : -INFINITY;  // token g,   head 2t
@@ -261,15 +293,15 @@ __device__ __forceinline__ void int4_piece(const Int4Params &p, uint8_t *ring, u
       constexpr int VW = Gm::VCH / 4;  // V words per token per lane (2 or 1)
       uint32_t va[VW], vb[VW], vc[VW], vd[VW];
       if constexpr (VW == 2) {
-        const uint2 A = lds64(st + Gm::KB + lane * 8), B2 = lds64(st + Gm::KB + (32 + lane) * 8);
-        const uint2 C = lds64(st + Gm::KB + (64 + lane) * 8), E = lds64(st + Gm::KB + (96 + lane) * 8);
+        const uint2 A = lds64(vt + swz<Gm::RB>(2 * t, 8 * g)), B2 = lds64(vt + swz<Gm::RB>(2 * t + 1, 8 * g));
+        const uint2 C = lds64(vt + swz<Gm::RB>(2 * t + 8, 8 * g)), E = lds64(vt + swz<Gm::RB>(2 * t + 9, 8 * g));
         va[0] = A.x; va[1] = A.y; vb[0] = B2.x; vb[1] = B2.y;
         vc[0] = C.x; vc[1] = C.y; vd[0] = E.x; vd[1] = E.y;
       } else {
-        va[0] = lds32(st + Gm::KB + lane * 4);
-        vb[0] = lds32(st + Gm::KB + (32 + lane) * 4);
-        vc[0] = lds32(st + Gm::KB + (64 + lane) * 4);
-        vd[0] = lds32(st + Gm::KB + (96 + lane) * 4);
+        va[0] = lds32(vt + swz<Gm::RB>(2 * t, 4 * g));
+        vb[0] = lds32(vt + swz<Gm::RB>(2 * t + 1, 4 * g));
+        vc[0] = lds32(vt + swz<Gm::RB>(2 * t + 8, 4 * g));
+        vd[0] = lds32(vt + swz<Gm::RB>(2 * t + 9, 4 * g));
       }
 #pragma unroll
       for (int wi = 0; wi < VW; ++wi) {
@@ -286,7 +318,12 @@ __device__ __forceinline__ void int4_piece(const Int4Params &p, uint8_t *ring, u
     }
     __syncwarp();
   }
-  cp_async_wait<0>();
+  if (rg.abort) {  // let every copy already issued land before the warp moves on or exits
+    while (rg.consumed < rg.issued) {
+      mbar_wait(rg.bars + 8 * (rg.consumed % NSTAGE), (rg.consumed / NSTAGE) & 1);
+      ++rg.consumed;
+    }
+  }
   __syncwarp();
 
   // -------- epilogue: undo the subnormal scaling, apply the zero-point term, normalise
@@ -309,18 +346,32 @@ __device__ __forceinline__ void int4_piece(const Int4Params &p, uint8_t *ring, u
 }
 
 template <int D, int NSTAGE>
-__global__ void __launch_bounds__(256, 2) decode_int4_kernel(const Int4Params p) {
-  extern __shared__ __align__(16) uint8_t smem[];
+__global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_constant__ Int4Params p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t s_bars[8][NSTAGE];
+  // the swizzled TMA tiles need 1024-byte alignment: round the dynamic base up (1 KB of slack)
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   asm volatile("griddepcontrol.launch_dependents;");  // let the merge kernel's launch begin early
   using Gm = Int4Geom<D>;
-  const int warp = threadIdx.x >> 5;
-  uint8_t *ring = smem + warp * (NSTAGE * Gm::STAGE + Gm::QBYTES);
-  uint8_t *qarea = ring + NSTAGE * Gm::STAGE;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // dynamic smem: [8 warps][NSTAGE][KVSTAGE] K/V tiles, then [8][NSTAGE][SCSTAGE], then [8][QBYTES]
+  Ring rg;
+  rg.kv = smem + warp * NSTAGE * Gm::KVSTAGE;
+  rg.sc = smem + 8 * NSTAGE * Gm::KVSTAGE + warp * NSTAGE * Gm::SCSTAGE;
+  uint8_t *qarea = smem + 8 * NSTAGE * (Gm::KVSTAGE + Gm::SCSTAGE) + warp * Gm::QBYTES;
+  rg.bars = smem_u32(&s_bars[warp][0]);
+  rg.issued = rg.consumed = 0;
+  rg.abort = false;
+  if (lane == 0) {
+    for (int i = 0; i < NSTAGE; ++i) mbar_init(rg.bars + 8 * i, 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
   const int hl = warp % p.s.heads_per_cta;
   const int sub = warp / p.s.heads_per_cta;
   const int h = blockIdx.y * p.s.heads_per_cta + hl;
   for_each_piece(p.s, &g_flags_decode_int4, [&](int b, int t0, int t1, long long slot) {
-    int4_piece<D, NSTAGE>(p, ring, qarea, b, h, sub, t0, t1, slot);
+    int4_piece<D, NSTAGE>(p, rg, qarea, b, h, sub, t0, t1, slot);
   });
 }
 
@@ -328,7 +379,8 @@ constexpr int kStagesInt4 = 4;
 
 template <int D>
 size_t int4_smem_bytes() {
-  return 8 * static_cast<size_t>(kStagesInt4 * Int4Geom<D>::STAGE + Int4Geom<D>::QBYTES);
+  using Gm = Int4Geom<D>;
+  return 8 * static_cast<size_t>(kStagesInt4 * (Gm::KVSTAGE + Gm::SCSTAGE) + Gm::QBYTES) + 1024;
 }
 
 bool take_flags_decode_int4(cudaStream_t stream, unsigned *host_word) {
@@ -386,8 +438,8 @@ extern "C" kvq_status kvq_decode_int4(const void *q, const uint8_t *k_cache, con
   if (!q || !k_cache || !v_cache || !k_scale || !v_scale || !block_table || !seq_lens || !out ||
       !workspace)
     return KVQ_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_scale, 4) ||
-      !aligned(v_scale, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_scale, 16) ||
+      !aligned(v_scale, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
       !aligned(out, 16) || !aligned(workspace, 16) || (rht_signs && !aligned(rht_signs, 16)))
     return KVQ_ERR_INVALID_ARG;
   if (max_blocks < 1) return KVQ_ERR_INVALID_ARG;
@@ -410,10 +462,7 @@ extern "C" kvq_status kvq_decode_int4(const void *q, const uint8_t *k_cache, con
   sa.out = out;
   sa.out_dtype = out_dtype;
   p.q = static_cast<const __nv_bfloat16 *>(q);
-  p.k_cache = k_cache;
-  p.v_cache = v_cache;
-  p.k_scale = reinterpret_cast<const uint32_t *>(k_scale);
-  p.v_scale = reinterpret_cast<const uint32_t *>(v_scale);
+  if (!int4_tensor_maps(k_cache, v_cache, k_scale, v_scale, num_blocks, Hk, D, &p.maps)) return KVQ_ERR_CUDA;
   p.block_table = block_table;
   const double sm = rht_signs ? static_cast<double>(softmax_scale) / D : softmax_scale;
   p.sm_log2 = static_cast<float>(sm * 1.4426950408889634);

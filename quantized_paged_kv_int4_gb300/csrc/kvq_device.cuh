@@ -5,6 +5,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
+#include <cuda.h>
 #include <stdint.h>
 
 #include "../../include/kvq.h"
@@ -15,7 +16,7 @@ constexpr unsigned FULL = 0xffffffffu;
 constexpr int kPage = 16;  // tokens per page: one MMA M-tile of the read kernels
 
 // Device-side error flags (kvq_device_error).
-enum : unsigned { ERR_BLOCK = 1u, ERR_SEQLEN = 2u, ERR_SLOT = 4u };
+enum : unsigned { ERR_BLOCK = 1u, ERR_SEQLEN = 2u, ERR_SLOT = 4u, ERR_TIMEOUT = 8u };
 
 // ---------------------------------------------------------------------------------------------
 // Exact fp32 building blocks (IEEE round-to-nearest, never contracted into an FMA).
@@ -108,6 +109,80 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// ---------------------------------------------------------------------------------------------
+// mbarrier + TMA (cp.async.bulk.tensor) helpers
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the phase with the given parity to complete, giving up after ~2 s of wall time
+// (a copy that never lands is a bug; the caller reports ERR_TIMEOUT instead of hanging).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t start = global_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - start > 2000000000ull) return false;
+  }
+}
+// Order this thread's earlier generic-proxy shared-memory accesses before later async-proxy
+// (TMA) writes to the same buffers.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            int c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+// Byte offset of (row, byte) inside a tile written by TMA with the 64B (rows of 64 bytes) or
+// 32B (rows of 32 bytes) swizzle: the 16-byte chunk index is XORed with address bits 7.. of the
+// row start. The tile base must be 1024-byte aligned.
+template <int ROW_BYTES>
+__device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t byte) {
+  constexpr uint32_t mask = ROW_BYTES / 16 - 1;  // 3 (64B swizzle) or 1 (32B swizzle)
+  const uint32_t o = row * ROW_BYTES;
+  return o + ((((byte >> 4) ^ (o >> 7)) & mask) << 4) + (byte & 15);
 }
 
 __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }

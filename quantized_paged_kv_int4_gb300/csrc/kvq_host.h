@@ -1,6 +1,7 @@
 // Host-side helpers shared by the libkvq translation units (not part of the public ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -39,6 +40,20 @@ bool make_plan(int B, int Hk, int num_splits, SplitPlan *plan);
 size_t workspace_bytes(int B, int Hq, int D, const SplitPlan &plan);
 void workspace_carve(void *workspace, int B, int Hq, int D, const SplitPlan &plan, float **part_o,
                      float **part_lse, int32_t **seg_first, int32_t **seg_last);
+
+// TMA descriptors of one INT4 cache (K, V pools and their scale words), see int4_tensor_maps.
+struct Int4Maps {
+  CUtensorMap k, v, ks, vs;
+  int scale_heads;  // heads per scale box: 4 (Hk % 4 == 0) or Hk (Hk < 4)
+};
+// Encode (or fetch from a small cache) the tensor maps of the pools:
+//   K / V  [num_blocks][16][Hk][D/2] bytes viewed as dims {D/2, Hk, 16, num_blocks}; box
+//          {D/2, 1, 16, 1} = one head's 16 token rows, 64B (D = 128) or 32B (D = 64) swizzle;
+//   scales [num_blocks][16][Hk] words: dims {Hk, 16, num_blocks} with box {4, 16, 1} when
+//          Hk % 4 == 0, else dims {16 * Hk, num_blocks} with box {16 * Hk, 1}.
+// Returns false if the driver entry point is unavailable or an encode fails.
+bool int4_tensor_maps(const void *k_cache, const void *v_cache, const void *k_scale, const void *v_scale,
+                      long long num_blocks, int Hk, int D, Int4Maps *maps);
 
 // Launch the log-sum-exp merge as a programmatic dependent of the kernel just enqueued on s.
 template <typename Args>

@@ -147,3 +147,23 @@ def test_workspace_reused_across_calls():
         assert kvq.kvq_device_error() == (0, 0)
         assert_close(outs[0], ref, what="reuse S=%d" % S)
         assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+
+
+@pytest.mark.parametrize("num_splits", [0, 3])
+def test_garbage_in_unwritten_rows_is_ignored(num_splits):
+    """Rows of a sequence's last page past its length were never written: NaN scale words and
+    arbitrary nibbles there must not reach the output."""
+    case = workloads.DecodeCase("garbage", 4, 16, 4, 128, [37, 16, 250, 1], seed=31, outlier_channels=4)
+    c = Int4Case(case)
+    ref = c.oracle()
+    nan_bits = np.uint32(0x7FC00000)
+    for b, L in enumerate(case.seq_lens):
+        page = int(c.bt[b, (L - 1) // 16])
+        for row in range(L % 16 if L % 16 else 16, 16):
+            c.ks[page, row] = nan_bits
+            c.vs[page, row] = nan_bits
+            c.kc[page, row] = 0xFF
+            c.vc[page, row] = 0x5A
+    got = run_int4(kvq, c.to_gpu(), c.scale, num_splits=num_splits).cpu().numpy()
+    assert np.all(np.isfinite(got))
+    assert_close(got, ref, what="garbage S=%d" % num_splits)
