@@ -89,10 +89,13 @@ bool int4_tensor_maps(const void *k_cache, const void *v_cache, const void *k_sc
   if (enc == nullptr) return false;
   Int4Maps m;
   std::memset(&m, 0, sizeof(m));
+  const int hpb = Hk < 8 ? Hk : 8;  // heads per box: one CTA's kv heads
   const cuuint64_t rb = static_cast<cuuint64_t>(D / 2);
-  const cuuint64_t kv_dim[4] = {rb, static_cast<cuuint64_t>(Hk), 16, static_cast<cuuint64_t>(num_blocks)};
-  const cuuint64_t kv_stride[3] = {rb, rb * Hk, rb * Hk * 16};
-  const cuuint32_t kv_box[4] = {static_cast<cuuint32_t>(rb), 1, 16, 1};
+  // dims {row bytes, token, head, page}: the token stride (Hk rows) is larger than the head
+  // stride, so a box lands in shared memory as [head][token][row]
+  const cuuint64_t kv_dim[4] = {rb, 16, static_cast<cuuint64_t>(Hk), static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t kv_stride[3] = {rb * Hk, rb, rb * Hk * 16};
+  const cuuint32_t kv_box[4] = {static_cast<cuuint32_t>(rb), 16, static_cast<cuuint32_t>(hpb), 1};
   const cuuint32_t ones[4] = {1, 1, 1, 1};
   const CUtensorMapSwizzle sw = D == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
   for (int i = 0; i < 2; ++i) {
@@ -105,13 +108,13 @@ bool int4_tensor_maps(const void *k_cache, const void *v_cache, const void *k_sc
     CUtensorMap *dst = i ? &m.vs : &m.ks;
     void *base = const_cast<void *>(i ? v_scale : k_scale);
     CUresult r;
-    if (Hk % 4 == 0) {
+    if (Hk > 8) {  // Hk a multiple of 8: a [16][8] box of words at the CTA's first head
       const cuuint64_t dim[3] = {static_cast<cuuint64_t>(Hk), 16, static_cast<cuuint64_t>(num_blocks)};
       const cuuint64_t stride[2] = {4ull * Hk, 64ull * Hk};
-      const cuuint32_t box[3] = {4, 16, 1};
+      const cuuint32_t box[3] = {8, 16, 1};
       r = enc(dst, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, base, dim, stride, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    } else {
+    } else {  // the page's whole [16][Hk] block of words
       const cuuint64_t dim[2] = {16ull * Hk, static_cast<cuuint64_t>(num_blocks)};
       const cuuint64_t stride[1] = {64ull * Hk};
       const cuuint32_t box[2] = {static_cast<cuuint32_t>(16 * Hk), 1};
@@ -120,7 +123,7 @@ bool int4_tensor_maps(const void *k_cache, const void *v_cache, const void *k_sc
     }
     if (r != CUDA_SUCCESS) return false;
   }
-  m.scale_heads = Hk % 4 == 0 ? 4 : Hk;
+  m.heads_per_box = hpb;
   Entry &e = cache[next];
   e.kc = k_cache;
   e.vc = v_cache;

@@ -9,17 +9,21 @@
 // the per-split results are merged by log-sum-exp and rotated back (decode_common.cuh, a second
 // kernel launched as a programmatic dependent).
 //
-// GB300 design. One warp owns one (kv head, run of pages) and streams it through a private
-// NSTAGE-deep ring in shared memory filled by TMA: per page, one lane issues four tensor loads
-// (this head's 16 K rows and 16 V rows, gathered from the page's [token][head] rows into a
-// [token] tile with the 64B/32B swizzle that makes the fragment reads conflict-free, and the
-// scale-word boxes) completing on the stage's mbarrier; waits are bounded and report a flag.
-// No block-wide barrier is needed. Both contractions run on the tensor
-// cores (mma.m16n8k16, fp16 operands, fp32 accumulation) on exact operands: a nibble pair
-// masked into an fp16 pair with a zero exponent field IS the pair of fp16 subnormals n * 2^-24
-// (low nibble) or n * 2^-20 (high nibble), so one LOP3 turns 2 nibbles into MMA operands
-// without any offset; the power of two goes into the per-token scale, and the zero-point is
-// applied as the split-dot correction of the pages (sum q n - zp sum q; sum P_v v - sum P_v zp):
+// GB300 design. A CTA owns HB = min(Hk, 8) kv heads and a run of pages (balanced split: an
+// equal share of all the batch's pages; fixed split: one piece of one sequence). It streams
+// the run through an NS-deep ring of stages in shared memory. A stage holds 8 (page, head)
+// tiles -- W = 8 / HB consecutive pages of the run, each with the CTA's HB heads -- loaded by
+// four TMA copies per page: one 4-D box of the K pool (HB heads x 16 tokens x D/2 bytes, stored
+// [head][token][row] with the 64B/32B swizzle that keeps the fragment reads conflict-free), the
+// same for V, and the page's two blocks of scale words. Warp w reads tile w of every stage
+// (head w % HB of page w / HB) and, when done with it, adds one to the stage's release counter;
+// the warp that brings it to 8 refills the stage with the pages NS stages ahead. So there is no
+// producer warp and no block-wide barrier after setup; waits on the stage barriers are bounded
+// and report a flag. Both contractions run on the tensor cores (mma.m16n8k16, fp16 operands,
+// fp32 accumulation) on exact operands: a nibble pair masked into an fp16 pair with a zero
+// exponent field IS the pair of fp16 subnormals n * 2^-24 (low nibble) or n * 2^-20 (high
+// nibble), so one LOP3 turns 2 nibbles into MMA operands; the power of two goes into the
+// per-token scale, and the zero-point is applied as the split-dot correction of the pages:
 //   * S^T[16 tokens x 8 heads] = K[16 x D] . Q^T  (q of a high-nibble dim pre-divided by 16);
 //   * O^T[D x 8 heads] += V^T[D x 16 tokens] . P_v^T with P_v = p * scale_v in fp16; the
 //     tokens (the K dimension) and the D rows are permuted so that a lane's V bytes become A
@@ -48,339 +52,623 @@ constexpr uint32_t kLo = 0x000F000Fu;  // low nibbles of bytes 0 and 2 -> fp16 s
 constexpr uint32_t kHi = 0x00F000F0u;  // high nibbles -> fp16 subnormal pair n * 2^-20
 constexpr float kTwo24 = 16777216.0f;
 constexpr float kTwo20 = 1048576.0f;
+// Slack of the lazy softmax maximum (base 2): weights stay below 2^kSlack = 8, so P_v = p * scale_v
+// stays finite in fp16 for V scale words below 8188 (per-token value ranges below ~1.2e5).
+constexpr float kSlack = 3.0f;
 
 template <int D>
 struct Int4Geom {
   static constexpr int RB = D / 2;        // bytes per token row of one head
-  static constexpr int KCH = D / 8;       // K bytes per lane per row
   static constexpr int VCH = D / 16;      // V bytes per lane per token
-  static constexpr int TILE = 16 * RB;    // one head's page of one pool (TMA box)
-  static constexpr int KVSTAGE = 2 * TILE < 1024 ? 1024 : 2 * TILE;  // K tile, V tile; 1024-aligned
-  static constexpr int SCSTAGE = 2 * 16 * 4 * 4;                     // K, V scale boxes (<= 4 heads)
+  static constexpr int TILE = 16 * RB;    // one (page, head) tile of one pool
+  static constexpr int VOFF = 8 * TILE;   // stage layout: 8 K tiles, 8 V tiles,
+  static constexpr int SOFF = 16 * TILE;  //   K scale blocks (<= 1 KB), V scale blocks (<= 1 KB)
+  static constexpr int SCPOOL = 1024;
+  static constexpr int STAGE = 16 * TILE + 2 * SCPOOL;  // a multiple of 1024
   static constexpr int WPR = D / 32;      // K words per lane per row
   static constexpr int KSTEPS = D / 16;
   static constexpr int MT = D / 16;       // m-tiles of the PV product
   static constexpr int QBYTES = 8 * D * 2 + 64;
 };
 
-// Per-warp TMA ring state, carried across the pieces of a CTA: pages issued / consumed so far
-// (stage = count % NSTAGE, phase parity = (count / NSTAGE) & 1) and a sticky abort bit.
-struct Ring {
-  uint8_t *kv;     // NSTAGE x KVSTAGE bytes, 1024-aligned
-  uint8_t *sc;     // NSTAGE x SCSTAGE bytes
-  uint32_t bars;   // shared address of NSTAGE mbarriers
-  uint32_t issued, consumed;
-  bool abort;
+// One sequence of the walk over a CTA's run: index b, global index of its page 0 (balanced
+// split) or 0 (fixed split), its page count and its clamped length.
+struct SeqCursor {
+  int b;
+  int np;
+  long long P;
+  int L;
 };
 
-template <int D, int NSTAGE>
-__device__ __forceinline__ void int4_piece(const Int4Params &p, Ring &rg, uint8_t *qarea, int b, int h,
-                                           int sub, int t0, int t1, long long slot) {
+__device__ __forceinline__ void seq_next(const SplitArgs &a, SeqCursor &c) {
+  do {
+    c.P += c.np;
+    ++c.b;
+    c.L = c.b < a.B ? clamped_len(a, c.b, nullptr) : 0;
+    c.np = (c.L + kPage - 1) / kPage;
+  } while (c.np == 0 && c.b < a.B);
+}
+
+// The CTA's run of pages (identical in all threads). Run page x is page base + x of the
+// concatenation of all sequences' pages (balanced) or page base + x of sequence first.b
+// (fixed split, token range [t0, t1)).
+struct PageRun {
+  long long base, end;  // run pages are base .. end - 1 (same numbering as SeqCursor::P)
+  int n;
+  bool fixed;
+  int t0, t1;
+  SeqCursor first;
+};
+
+__device__ __forceinline__ bool page_run(const SplitArgs &a, unsigned *flags, PageRun *run) {
+  if (a.num_splits > 0) {
+    const int b = blockIdx.x / a.num_splits, s = blockIdx.x % a.num_splits;
+    const int L = clamped_len(a, b, flags);
+    const int span = (L + a.num_splits - 1) / a.num_splits;
+    const int t0 = s * span, t1 = min(t0 + span, L);
+    if (t0 >= t1) return false;
+    run->fixed = true;
+    run->t0 = t0;
+    run->t1 = t1;
+    run->base = t0 / kPage;
+    run->n = (t1 - 1) / kPage - t0 / kPage + 1;
+    run->end = run->base + run->n;
+    run->first.b = b;
+    run->first.P = 0;
+    run->first.np = 0x3fffffff;  // never left
+    run->first.L = L;
+    return true;
+  }
+  __shared__ long long s_scan[8];
+  __shared__ long long s_first_p;
+  __shared__ int s_first_b;
+  long long P_tot = 0;
+  for (int base = 0; base < a.B; base += 256) {
+    const int b = base + threadIdx.x;
+    const long long np = b < a.B ? (clamped_len(a, b, flags) + kPage - 1) / kPage : 0;
+    long long chunk;
+    block_scan_256(np, s_scan, &chunk);
+    P_tot += chunk;
+  }
+  const long long C = gridDim.x, c = blockIdx.x;
+  const long long q = P_tot / C, r = P_tot % C;
+  const long long pb = c * q + min(c, r), pe = pb + q + (c < r ? 1 : 0);
+  if (pb >= pe) return false;
+  if (threadIdx.x == 0) s_first_b = -1;
+  __syncthreads();
+  long long running = 0;
+  for (int base = 0; base < a.B; base += 256) {
+    const int b = base + threadIdx.x;
+    const long long np = b < a.B ? (clamped_len(a, b, nullptr) + kPage - 1) / kPage : 0;
+    long long chunk;
+    const long long incl = block_scan_256(np, s_scan, &chunk) + running;
+    const long long excl = incl - np;
+    if (np > 0 && excl <= pb && pb < incl) {
+      s_first_b = b;
+      s_first_p = excl;
+    }
+    running += chunk;
+    __syncthreads();
+    if (s_first_b >= 0) break;
+  }
+  run->fixed = false;
+  run->base = pb;
+  run->end = pe;
+  run->n = static_cast<int>(pe - pb);
+  run->first.b = s_first_b;
+  run->first.P = s_first_p;
+  run->first.L = clamped_len(a, s_first_b, nullptr);
+  run->first.np = (run->first.L + kPage - 1) / kPage;
+  return true;
+}
+
+// Online-softmax state of one warp for one sequence piece.
+template <int D>
+struct PieceState {
+  float m0, m1, l0, l1, pz0, pz1;
+  float acc[D / 16][4];
+  __device__ __forceinline__ void reset() {
+    m0 = m1 = -INFINITY;
+    l0 = l1 = pz0 = pz1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  }
+};
+
+// q_rot = bf16(H(q * d1)) for the G heads of kv head h of sequence b, as the fp16 B fragments
+// of the score MMA (odd dims pre-divided by 16) and the per-head sums of the q the products use.
+template <int D>
+__device__ __forceinline__ void load_query(const Int4Params &p, uint8_t *qarea, int b, int h, int lane,
+                                           uint32_t (&qf)[D / 16][2], float &qs0, float &qs1) {
   using Gm = Int4Geom<D>;
-  const int lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int G = p.s.G, WPH = p.s.warps_per_head, Hk = p.s.Hk;
-
-  // -------- this warp's pages: first, first + WPH, ... <= last page of the piece
-  const int pg0 = t0 / kPage, pglast = (t1 - 1) / kPage;
-  const int first = pg0 + sub;
-  const int n_my = first <= pglast ? (pglast - first) / WPH + 1 : 0;
-  const int32_t *bt_row = p.block_table + static_cast<long long>(b) * p.s.max_blocks;
-  auto load_bids = [&](int batch) -> int {
-    const int k = batch * 32 + lane;
-    return k < n_my ? __ldg(bt_row + first + k * WPH) : 0;
-  };
-  int bids_cur = load_bids(0);
-  int bids_next = load_bids(1);
-
-  // -------- query: q_rot = bf16(H(q * d1)) for the G heads of kv head h, as fp16 B operands
-  {
-    constexpr int J = D / 32;
-    const __nv_bfloat16 *qb = p.q + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(h) * G) * D;
-    __half *qh = reinterpret_cast<__half *>(qarea);
-    float *qsum = reinterpret_cast<float *>(qarea + 8 * D * 2);
-    for (int n = G; n < 8; ++n) {  // padded MMA columns
+  constexpr int J = D / 32;
+  const int g = lane >> 2, t = lane & 3, G = p.s.G;
+  const __nv_bfloat16 *qb = p.q + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(h) * G) * D;
+  __half *qh = reinterpret_cast<__half *>(qarea);
+  float *qsum = reinterpret_cast<float *>(qarea + 8 * D * 2);
+  __syncwarp();
+  for (int n = G; n < 8; ++n) {  // padded MMA columns
 #pragma unroll
-      for (int j = 0; j < J; ++j) qh[n * D + lane + 32 * j] = __float2half_rn(0.f);
-      if (lane == 0) qsum[n] = 0.f;
-    }
-    for (int n = 0; n < G; ++n) {
-      float x[J];
+    for (int j = 0; j < J; ++j) qh[n * D + lane + 32 * j] = __float2half_rn(0.f);
+    if (lane == 0) qsum[n] = 0.f;
+  }
+  for (int n = 0; n < G; ++n) {
+    float x[J];
 #pragma unroll
-      for (int j = 0; j < J; ++j) x[j] = __bfloat162float(qb[n * D + lane + 32 * j]);
-      if (p.s.signs != nullptr) {
+    for (int j = 0; j < J; ++j) x[j] = __bfloat162float(qb[n * D + lane + 32 * j]);
+    if (p.s.signs != nullptr) {
 #pragma unroll
-        for (int j = 0; j < J; ++j) x[j] *= __ldg(p.s.signs + lane + 32 * j);
+      for (int j = 0; j < J; ++j) x[j] *= __ldg(p.s.signs + lane + 32 * j);
 #pragma unroll
-        for (int mask = 1; mask < 32; mask <<= 1) {
+      for (int mask = 1; mask < 32; mask <<= 1) {
 #pragma unroll
-          for (int j = 0; j < J; ++j) x[j] = butterfly_xor(x[j], lane, mask);
-        }
-        butterfly_local<J>(x);
-#pragma unroll
-        for (int j = 0; j < J; ++j) x[j] = bf16_round(x[j]);
+        for (int j = 0; j < J; ++j) x[j] = butterfly_xor(x[j], lane, mask);
       }
-      // odd dims meet high nibbles, which enter the MMA 16x larger: pre-divide q by 16 (exact)
-      float eff = 0.f;
+      butterfly_local<J>(x);
 #pragma unroll
-      for (int j = 0; j < J; ++j) {
-        const int e = lane + 32 * j;
-        const __half v = __float2half_rn((e & 1) ? x[j] * 0.0625f : x[j]);
-        qh[n * D + e] = v;
-        eff += (e & 1) ? __half2float(v) * 16.f : __half2float(v);
-      }
-      eff = warp_sum(eff);
-      if (lane == 0) qsum[n] = eff * (1.0f / kTwo24);  // sum of the q the products use, in MMA units
+      for (int j = 0; j < J; ++j) x[j] = bf16_round(x[j]);
     }
+    // odd dims meet high nibbles, which enter the MMA 16x larger: pre-divide q by 16 (exact)
+    float eff = 0.f;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int e = lane + 32 * j;
+      const __half v = __float2half_rn((e & 1) ? x[j] * 0.0625f : x[j]);
+      qh[n * D + e] = v;
+      eff += (e & 1) ? __half2float(v) * 16.f : __half2float(v);
+    }
+    eff = warp_sum(eff);
+    if (lane == 0) qsum[n] = eff * (1.0f / kTwo24);  // sum of the q the products use, in MMA units
   }
   __syncwarp();
   // B fragment of k-step ks = 2m + s: the dims a K word's nibbles occupy after the LOP3 split
   // (word j = WPR * t + m: low nibbles 8j + 2s, 8j + 4 + 2s; high nibbles one dim up)
-  uint32_t qf[Gm::KSTEPS][2];
-  {
-    const __half *qh = reinterpret_cast<const __half *>(qarea) + g * D;
+  const __half *qr = qh + g * D;
 #pragma unroll
-    for (int ks = 0; ks < Gm::KSTEPS; ++ks) {
-      const int j = Gm::WPR * t + (ks >> 1), s2 = 2 * (ks & 1);
-      qf[ks][0] = h2_as_u32(__halves2half2(qh[8 * j + s2], qh[8 * j + 4 + s2]));
-      qf[ks][1] = h2_as_u32(__halves2half2(qh[8 * j + 1 + s2], qh[8 * j + 5 + s2]));
-    }
+  for (int ks = 0; ks < Gm::KSTEPS; ++ks) {
+    const int j = Gm::WPR * t + (ks >> 1), s2 = 2 * (ks & 1);
+    qf[ks][0] = h2_as_u32(__halves2half2(qr[8 * j + s2], qr[8 * j + 4 + s2]));
+    qf[ks][1] = h2_as_u32(__halves2half2(qr[8 * j + 1 + s2], qr[8 * j + 5 + s2]));
   }
-  const float *qsum = reinterpret_cast<const float *>(qarea + 8 * D * 2);
-  const float qs0 = qsum[2 * t], qs1 = qsum[2 * t + 1];
-  const float sm24 = p.sm_log2 * kTwo24;  // the K operands carry a factor 2^-24
+  qs0 = qsum[2 * t];
+  qs1 = qsum[2 * t + 1];
   __syncwarp();
+}
 
-  // -------- TMA ring: per page, lane 0 loads this head's 16 K rows and 16 V rows (swizzled
-  // boxes) plus the scale-word boxes, all completing on the stage's mbarrier.
-  const int SH = p.maps.scale_heads;                 // heads per scale box
-  const int hh = SH == 4 ? (h & 3) : h;              // this head's column in the scale box
-  const int sc_h0 = SH == 4 ? (h & ~3) : 0;
-  constexpr uint32_t kTx = 2 * Gm::TILE;             // + the two scale boxes (below)
-  const uint32_t tx = kTx + 2 * 16 * SH * 4;
-  auto issue = [&](int k) {
-    const int kk = k & 31;
-    if (k > 0 && kk == 0) {
-      bids_cur = bids_next;
-      bids_next = load_bids((k >> 5) + 1);
-    }
-    const int blk_raw = __shfl_sync(FULL, bids_cur, kk);
-    if (k >= n_my) return;
-    const bool ok = blk_raw >= 0 && blk_raw < p.num_blocks;
-    const int blk = ok ? blk_raw : 0;  // out of range: flagged, page 0 read instead
-    const int stg = static_cast<int>(rg.issued % NSTAGE);
-    ++rg.issued;
-    if (lane == 0) {
-      if (!ok) atomicOr(&g_flags_decode_int4, ERR_BLOCK);
-      const uint32_t bar = rg.bars + 8 * stg;
-      const uint32_t kv = smem_u32(rg.kv + stg * Gm::KVSTAGE), sc = smem_u32(rg.sc + stg * Gm::SCSTAGE);
-      fence_proxy_async();
-      mbar_arrive_expect_tx(bar, tx);
-      tma_load_4d(kv, &p.maps.k, 0, h, 0, blk, bar);
-      tma_load_4d(kv + Gm::TILE, &p.maps.v, 0, h, 0, blk, bar);
-      if (SH == 4) {
-        tma_load_3d(sc, &p.maps.ks, sc_h0, 0, blk, bar);
-        tma_load_3d(sc + Gm::SCSTAGE / 2, &p.maps.vs, sc_h0, 0, blk, bar);
-      } else {
-        tma_load_2d(sc, &p.maps.ks, 0, blk, bar);
-        tma_load_2d(sc + Gm::SCSTAGE / 2, &p.maps.vs, 0, blk, bar);
-      }
-    }
-  };
-  // wait for the next page; on a timeout (a copy that never completes) raise the flag and abort
-  auto wait_next = [&]() -> bool {
-    const uint32_t stg = rg.consumed % NSTAGE, par = (rg.consumed / NSTAGE) & 1;
-    const bool ok = mbar_wait(rg.bars + 8 * stg, par);
-    if (!__all_sync(FULL, ok)) {
-      if (lane == 0) atomicOr(&g_flags_decode_int4, ERR_TIMEOUT);
-      rg.abort = true;
-      return false;
-    }
-    return true;
-  };
+// What a lane needs from one page after the score MMAs: its base-2 logits for tokens g, g+8 x
+// heads 2t, 2t+1, and the V scale / zero-point of tokens g, g+8.
+struct PageIn {
+  float s[4];  // (g, 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1)
+  float sv0, sv1, zv0, zv1;
+};
 
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, pz0 = 0.f, pz1 = 0.f;
-  float acc[Gm::MT][4];
-#pragma unroll
-  for (int i = 0; i < Gm::MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+// Shared-memory reads at 32-bit offsets from the dynamic buffer (the compiler folds constant
+// parts of an offset into the instruction).
+extern __shared__ __align__(16) uint8_t kvq_dsmem[];
+__device__ __forceinline__ uint4 ld_s128(uint32_t o) { return *reinterpret_cast<const uint4 *>(kvq_dsmem + o); }
+__device__ __forceinline__ uint2 ld_s64(uint32_t o) { return *reinterpret_cast<const uint2 *>(kvq_dsmem + o); }
+__device__ __forceinline__ uint32_t ld_s32(uint32_t o) { return *reinterpret_cast<const uint32_t *>(kvq_dsmem + o); }
 
-  if (rg.abort) return;
-#pragma unroll
-  for (int k = 0; k < NSTAGE - 1; ++k) issue(k);
+// This lane's fixed offsets inside a stage (stage-relative): K row g of its tile, V row 2t of its
+// tile, and its K scale word of token g. The other rows it reads sit at constant distances:
+// K row g+8 = +8 rows; V rows 2t+1, 2t+8, 2t+9 = +1, +8, +9 rows (the swizzle pattern repeats
+// every 8 rows and is the same for rows 2t and 2t+1); token g+8's word = +8 * HB words.
+template <int D>
+struct LaneOffsets {
+  uint32_t k, v, s;
+};
 
-  for (int k = 0; k < n_my; ++k) {
-    issue(k + NSTAGE - 1);
-    const uint32_t stg = rg.consumed % NSTAGE;
-    if (!wait_next()) break;
-    ++rg.consumed;
-    const uint8_t *kt = rg.kv + stg * Gm::KVSTAGE, *vt = kt + Gm::TILE;
-    const uint32_t *sk = reinterpret_cast<const uint32_t *>(rg.sc + stg * Gm::SCSTAGE);
-    const uint32_t *sv = sk + Gm::SCSTAGE / 8;
-    const int nb = (first + k * WPH) * kPage;  // position of the page's row 0
-    const bool ok0 = nb + g >= t0 && nb + g < t1;
-    const bool ok1 = nb + g + 8 >= t0 && nb + g + 8 < t1;
+template <int D, int W>
+__device__ __forceinline__ LaneOffsets<D> lane_offsets(int warp, int sub, int hl, int lane) {
+  using Gm = Int4Geom<D>;
+  constexpr int HB = 8 / W;
+  constexpr int SCP = 64 * HB < 128 ? 128 : 64 * HB;
+  const int g = lane >> 2, t = lane & 3;
+  LaneOffsets<D> o;
+  o.k = warp * Gm::TILE + swz<Gm::RB>(g, Gm::WPR * 4 * t);
+  o.v = Gm::VOFF + warp * Gm::TILE + swz<Gm::RB>(2 * t, (Gm::VCH) * g);
+  o.s = Gm::SOFF + sub * SCP + (g * HB + hl) * 4;
+  return o;
+}
 
-    // ---- scores: S = (sum_d q_d n_d - zp sum_d q_d) * scale_k * sm (base 2)
-    const uint32_t kw0 = sk[g * SH + hh], kw1 = sk[(g + 8) * SH + hh];
-    float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};  // two MMA chains
-    {
-      uint32_t wa[Gm::WPR], wb[Gm::WPR];
-      if constexpr (Gm::WPR == 4) {
-        const uint4 a4 = lds128(kt + swz<Gm::RB>(g, 16 * t)), b4 = lds128(kt + swz<Gm::RB>(g + 8, 16 * t));
-        wa[0] = a4.x; wa[1] = a4.y; wa[2] = a4.z; wa[3] = a4.w;
-        wb[0] = b4.x; wb[1] = b4.y; wb[2] = b4.z; wb[3] = b4.w;
-      } else {
-        const uint2 a2 = lds64(kt + swz<Gm::RB>(g, 8 * t)), b2 = lds64(kt + swz<Gm::RB>(g + 8, 8 * t));
-        wa[0] = a2.x; wa[1] = a2.y;
-        wb[0] = b2.x; wb[1] = b2.y;
-      }
-#pragma unroll
-      for (int m = 0; m < Gm::WPR; ++m) {
-        const uint32_t xa = wa[m] >> 8, xb = wb[m] >> 8;
-        mma_f16_16816(c, wa[m] & kLo, wb[m] & kLo, wa[m] & kHi, wb[m] & kHi, qf[2 * m][0], qf[2 * m][1]);
-        mma_f16_16816(c2, xa & kLo, xb & kLo, xa & kHi, xb & kHi, qf[2 * m + 1][0], qf[2 * m + 1][1]);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) c[i] += c2[i];
-    const uint32_t vw0 = sv[g * SH + hh], vw1 = sv[(g + 8) * SH + hh];
-    const float ck0 = __uint_as_float(kw0 & ~0xFu) * sm24, ck1 = __uint_as_float(kw1 & ~0xFu) * sm24;
-    const float zk0 = static_cast<float>(kw0 & 0xFu), zk1 = static_cast<float>(kw1 & 0xFu);
-    const float s00 = ok0 ? (c[0] - zk0 * qs0) * ck0 : -INFINITY;  // token g,   head 2t
-    const float s01 = ok0 ? (c[1] - zk0 * qs1) * ck0 : -INFINITY;  // token g,   head 2t+1
-    const float s10 = ok1 ? (c[2] - zk1 * qs0) * ck1 : -INFINITY;  // token g+8, head 2t
-    const float s11 = ok1 ? (c[3] - zk1 * qs1) * ck1 : -INFINITY;  // token g+8, head 2t+1
-
-    // ---- online softmax (base 2)
-    const float mx0 = fmaxf(m0, warp_max_g(fmaxf(s00, s10)));
-    const float mx1 = fmaxf(m1, warp_max_g(fmaxf(s01, s11)));
-    const float r0 = mx0 == -INFINITY ? 0.f : mx0, r1 = mx1 == -INFINITY ? 0.f : mx1;
-    const float al0 = fast_exp2(m0 - r0), al1 = fast_exp2(m1 - r1);
-    m0 = mx0;
-    m1 = mx1;
-    const float p00 = fast_exp2(s00 - r0), p10 = fast_exp2(s10 - r0);
-    const float p01 = fast_exp2(s01 - r1), p11 = fast_exp2(s11 - r1);
-    l0 = l0 * al0 + (p00 + p10);
-    l1 = l1 * al1 + (p01 + p11);
-
-    // ---- P_v = p * scale_v (fp16), and sum P_v * zp_v for the zero-point correction
-    const float sv0 = __uint_as_float(vw0 & ~0xFu), sv1 = __uint_as_float(vw1 & ~0xFu);
-    const float zv0 = static_cast<float>(vw0 & 0xFu), zv1 = static_cast<float>(vw1 & 0xFu);
-    const __half2 X0 = __floats2half2_rn(ok0 ? p00 * sv0 : 0.f, ok1 ? p10 * sv1 : 0.f);
-    const __half2 X1 = __floats2half2_rn(ok0 ? p01 * sv0 : 0.f, ok1 ? p11 * sv1 : 0.f);
-    const float2 f0 = __half22float2(X0), f1 = __half22float2(X1);
-    pz0 = pz0 * al0 + (f0.x * zv0 + f0.y * zv1);
-    pz1 = pz1 * al1 + (f1.x * zv0 + f1.y * zv1);
-    if (!__all_sync(FULL, al0 == 1.f && al1 == 1.f)) {  // a running max moved: rescale
-#pragma unroll
-      for (int i = 0; i < Gm::MT; ++i) {
-        acc[i][0] *= al0;
-        acc[i][1] *= al1;
-        acc[i][2] *= al0;
-        acc[i][3] *= al1;
-      }
-    }
-    // B fragment of P_v^T: this lane needs head g at tokens 2t, 2t+1 (b01), 2t+8, 2t+9 (b23)
-    const int src0 = 8 * t + (g >> 1), src1 = src0 + 4;
-    const uint32_t x0 = h2_as_u32(X0), x1 = h2_as_u32(X1);
-    const uint32_t y0 = __shfl_sync(FULL, x0, src0), y1 = __shfl_sync(FULL, x1, src0);
-    const uint32_t z0 = __shfl_sync(FULL, x0, src1), z1 = __shfl_sync(FULL, x1, src1);
-    const uint32_t ya = (g & 1) ? y1 : y0, za = (g & 1) ? z1 : z0;
-    const uint32_t b01 = __byte_perm(ya, za, 0x5410), b23 = __byte_perm(ya, za, 0x7632);
-
-    // ---- O^T += V^T . P_v^T
-    {
-      constexpr int VW = Gm::VCH / 4;  // V words per token per lane (2 or 1)
-      uint32_t va[VW], vb[VW], vc[VW], vd[VW];
-      if constexpr (VW == 2) {
-        const uint2 A = lds64(vt + swz<Gm::RB>(2 * t, 8 * g)), B2 = lds64(vt + swz<Gm::RB>(2 * t + 1, 8 * g));
-        const uint2 C = lds64(vt + swz<Gm::RB>(2 * t + 8, 8 * g)), E = lds64(vt + swz<Gm::RB>(2 * t + 9, 8 * g));
-        va[0] = A.x; va[1] = A.y; vb[0] = B2.x; vb[1] = B2.y;
-        vc[0] = C.x; vc[1] = C.y; vd[0] = E.x; vd[1] = E.y;
-      } else {
-        va[0] = lds32(vt + swz<Gm::RB>(2 * t, 4 * g));
-        vb[0] = lds32(vt + swz<Gm::RB>(2 * t + 1, 4 * g));
-        vc[0] = lds32(vt + swz<Gm::RB>(2 * t + 8, 4 * g));
-        vd[0] = lds32(vt + swz<Gm::RB>(2 * t + 9, 4 * g));
-      }
-#pragma unroll
-      for (int wi = 0; wi < VW; ++wi) {
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const uint32_t sel = hf ? 0x7632u : 0x5410u;
-          const uint32_t x = __byte_perm(va[wi], vb[wi], sel), y = __byte_perm(vc[wi], vd[wi], sel);
-          const int mt = 4 * wi + 2 * hf;
-          mma_f16_16816(acc[mt], x & kLo, x & kHi, y & kLo, y & kHi, b01, b23);
-          const uint32_t x8 = x >> 8, y8 = y >> 8;
-          mma_f16_16816(acc[mt + 1], x8 & kLo, x8 & kHi, y8 & kLo, y8 & kHi, b01, b23);
-        }
-      }
-    }
-    __syncwarp();
+// S = (sum_d q_d n_d - zp sum_d q_d) * scale_k * sm for one (page, head) tile at stage offset so.
+template <int D, int W>
+__device__ __forceinline__ void page_scores(PageIn &pg, uint32_t so, const LaneOffsets<D> &lo,
+                                            const uint32_t (&qf)[D / 16][2], float qs0, float qs1, float sm24) {
+  using Gm = Int4Geom<D>;
+  constexpr int HB = 8 / W;
+  float c[4] = {0.f, 0.f, 0.f, 0.f};
+  uint32_t wa[Gm::WPR], wb[Gm::WPR];
+  const uint32_t ko = so + lo.k, sk = so + lo.s;
+  if constexpr (Gm::WPR == 4) {
+    const uint4 a4 = ld_s128(ko), b4 = ld_s128(ko + 8 * Gm::RB);
+    wa[0] = a4.x; wa[1] = a4.y; wa[2] = a4.z; wa[3] = a4.w;
+    wb[0] = b4.x; wb[1] = b4.y; wb[2] = b4.z; wb[3] = b4.w;
+  } else {
+    const uint2 a2 = ld_s64(ko), b2 = ld_s64(ko + 8 * Gm::RB);
+    wa[0] = a2.x; wa[1] = a2.y;
+    wb[0] = b2.x; wb[1] = b2.y;
   }
-  if (rg.abort) {  // let every copy already issued land before the warp moves on or exits
-    while (rg.consumed < rg.issued) {
-      mbar_wait(rg.bars + 8 * (rg.consumed % NSTAGE), (rg.consumed / NSTAGE) & 1);
-      ++rg.consumed;
+  const uint32_t kw0 = ld_s32(sk), kw1 = ld_s32(sk + 32 * HB);
+  const uint32_t vw0 = ld_s32(sk + Gm::SCPOOL), vw1 = ld_s32(sk + Gm::SCPOOL + 32 * HB);
+#pragma unroll
+  for (int m = 0; m < Gm::WPR; ++m) {
+    const uint32_t xa = wa[m] >> 8, xb = wb[m] >> 8;
+    mma_f16_16816(c, wa[m] & kLo, wb[m] & kLo, wa[m] & kHi, wb[m] & kHi, qf[2 * m][0], qf[2 * m][1]);
+    mma_f16_16816(c, xa & kLo, xb & kLo, xa & kHi, xb & kHi, qf[2 * m + 1][0], qf[2 * m + 1][1]);
+  }
+  const float ck0 = __uint_as_float(kw0 & ~0xFu) * sm24, ck1 = __uint_as_float(kw1 & ~0xFu) * sm24;
+  const float zk0 = static_cast<float>(kw0 & 0xFu), zk1 = static_cast<float>(kw1 & 0xFu);
+  pg.s[0] = (c[0] - zk0 * qs0) * ck0;
+  pg.s[1] = (c[1] - zk0 * qs1) * ck0;
+  pg.s[2] = (c[2] - zk1 * qs0) * ck1;
+  pg.s[3] = (c[3] - zk1 * qs1) * ck1;
+  pg.sv0 = __uint_as_float(vw0 & ~0xFu);
+  pg.sv1 = __uint_as_float(vw1 & ~0xFu);
+  pg.zv0 = static_cast<float>(vw0 & 0xFu);
+  pg.zv1 = static_cast<float>(vw1 & 0xFu);
+}
+
+// O^T += V^T . P_v^T for one (page, head) tile at stage offset so; x0 / x1 = this lane's fp16
+// P_v pairs (tokens g, g+8) of heads 2t / 2t+1.
+template <int D>
+__device__ __forceinline__ void page_pv(float (&acc)[D / 16][4], uint32_t so, const LaneOffsets<D> &lo,
+                                        uint32_t x0, uint32_t x1, int lane) {
+  using Gm = Int4Geom<D>;
+  const int g = lane >> 2, t = lane & 3;
+  // B fragment of P_v^T: this lane needs head g at tokens 2t, 2t+1 (b01), 2t+8, 2t+9 (b23)
+  const int src0 = 8 * t + (g >> 1), src1 = src0 + 4;
+  const uint32_t y0 = __shfl_sync(FULL, x0, src0), y1 = __shfl_sync(FULL, x1, src0);
+  const uint32_t z0 = __shfl_sync(FULL, x0, src1), z1 = __shfl_sync(FULL, x1, src1);
+  const uint32_t ya = (g & 1) ? y1 : y0, za = (g & 1) ? z1 : z0;
+  const uint32_t b01 = __byte_perm(ya, za, 0x5410), b23 = __byte_perm(ya, za, 0x7632);
+  constexpr int VW = Gm::VCH / 4;  // V words per token per lane (2 or 1)
+  const uint32_t vo = so + lo.v;
+  uint32_t va[VW], vb[VW], vc[VW], vd[VW];
+  if constexpr (VW == 2) {
+    const uint2 A = ld_s64(vo), B2 = ld_s64(vo + Gm::RB);
+    const uint2 C = ld_s64(vo + 8 * Gm::RB), E = ld_s64(vo + 9 * Gm::RB);
+    va[0] = A.x; va[1] = A.y; vb[0] = B2.x; vb[1] = B2.y;
+    vc[0] = C.x; vc[1] = C.y; vd[0] = E.x; vd[1] = E.y;
+  } else {
+    va[0] = ld_s32(vo);
+    vb[0] = ld_s32(vo + Gm::RB);
+    vc[0] = ld_s32(vo + 8 * Gm::RB);
+    vd[0] = ld_s32(vo + 9 * Gm::RB);
+  }
+#pragma unroll
+  for (int wi = 0; wi < VW; ++wi) {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const uint32_t sel = hf ? 0x7632u : 0x5410u;
+      const uint32_t x = __byte_perm(va[wi], vb[wi], sel), y = __byte_perm(vc[wi], vd[wi], sel);
+      const int mt = 4 * wi + 2 * hf;
+      mma_f16_16816(acc[mt], x & kLo, x & kHi, y & kLo, y & kHi, b01, b23);
+      const uint32_t x8 = x >> 8, y8 = y >> 8;
+      mma_f16_16816(acc[mt + 1], x8 & kLo, x8 & kHi, y8 & kLo, y8 & kHi, b01, b23);
     }
   }
-  __syncwarp();
+}
 
-  // -------- epilogue: undo the subnormal scaling, apply the zero-point term, normalise
-  l0 = warp_sum_g(l0);
-  l1 = warp_sum_g(l1);
-  pz0 = warp_sum_g(pz0);
-  pz1 = warp_sum_g(pz1);
+// NP consecutive pages of this warp (stage offsets so[0..NP-1]) inside one piece: scores, one
+// online softmax step over their 16 * NP tokens, P.V. MASKED: some rows of the (single) page lie
+// outside [t0, t1) -- the ragged end of a sequence or a fixed split boundary -- and may hold
+// never-written scale words (NaN): they are selected away, never multiplied.
+template <int D, int W, int NP, bool MASKED>
+__device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&so)[2], const LaneOffsets<D> &lo,
+                                           const uint32_t (&qf)[D / 16][2], float qs0, float qs1, float sm24,
+                                           int lane, int nb, int t0, int t1) {
+  using Gm = Int4Geom<D>;
+  const int g = lane >> 2;
+  PageIn pg[NP];
+#pragma unroll
+  for (int i = 0; i < NP; ++i) page_scores<D, W>(pg[i], so[i], lo, qf, qs0, qs1, sm24);
+  bool ok0 = true, ok1 = true;
+  if (MASKED) {
+    ok0 = nb + g >= t0 && nb + g < t1;
+    ok1 = nb + g + 8 >= t0 && nb + g + 8 < t1;
+    pg[0].s[0] = ok0 ? pg[0].s[0] : -INFINITY;
+    pg[0].s[1] = ok0 ? pg[0].s[1] : -INFINITY;
+    pg[0].s[2] = ok1 ? pg[0].s[2] : -INFINITY;
+    pg[0].s[3] = ok1 ? pg[0].s[3] : -INFINITY;
+  }
+  // ---- online softmax (base 2) against a lazily raised reference maximum: the running sums are
+  // rescaled only when a new score exceeds the reference by more than kSlack, so the weights
+  // p = 2^(s - m) stay below 2^kSlack and most steps need no rescale at all
+  float ml0 = fmaxf(pg[0].s[0], pg[0].s[2]), ml1 = fmaxf(pg[0].s[1], pg[0].s[3]);
+#pragma unroll
+  for (int i = 1; i < NP; ++i) {
+    ml0 = fmaxf(ml0, fmaxf(pg[i].s[0], pg[i].s[2]));
+    ml1 = fmaxf(ml1, fmaxf(pg[i].s[1], pg[i].s[3]));
+  }
+  ml0 = warp_max_g(ml0);
+  ml1 = warp_max_g(ml1);
+  if (__any_sync(FULL, ml0 > st.m0 + kSlack || ml1 > st.m1 + kSlack)) {
+    const float n0 = fmaxf(st.m0, ml0), n1 = fmaxf(st.m1, ml1);
+    const float al0 = n0 == -INFINITY ? 1.f : fast_exp2(st.m0 - n0);
+    const float al1 = n1 == -INFINITY ? 1.f : fast_exp2(st.m1 - n1);
+    st.m0 = n0;
+    st.m1 = n1;
+    st.l0 *= al0;
+    st.l1 *= al1;
+    st.pz0 *= al0;
+    st.pz1 *= al1;
+#pragma unroll
+    for (int i = 0; i < Gm::MT; ++i) {
+      st.acc[i][0] *= al0;
+      st.acc[i][1] *= al1;
+      st.acc[i][2] *= al0;
+      st.acc[i][3] *= al1;
+    }
+  }
+  const float r0 = st.m0 == -INFINITY ? 0.f : st.m0, r1 = st.m1 == -INFINITY ? 0.f : st.m1;
+  uint32_t X0[NP], X1[NP];
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    const float p00 = fast_exp2(pg[i].s[0] - r0), p10 = fast_exp2(pg[i].s[2] - r0);
+    const float p01 = fast_exp2(pg[i].s[1] - r1), p11 = fast_exp2(pg[i].s[3] - r1);
+    st.l0 += p00 + p10;
+    st.l1 += p01 + p11;
+    // P_v = p * scale_v (fp16), and sum P_v * zp_v for the zero-point correction
+    float w00 = p00 * pg[i].sv0, w10 = p10 * pg[i].sv1, w01 = p01 * pg[i].sv0, w11 = p11 * pg[i].sv1;
+    if (MASKED) {
+      w00 = ok0 ? w00 : 0.f;
+      w01 = ok0 ? w01 : 0.f;
+      w10 = ok1 ? w10 : 0.f;
+      w11 = ok1 ? w11 : 0.f;
+    }
+    const __half2 h0 = __floats2half2_rn(w00, w10), h1 = __floats2half2_rn(w01, w11);
+    const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+    st.pz0 += f0.x * pg[i].zv0 + f0.y * pg[i].zv1;
+    st.pz1 += f1.x * pg[i].zv0 + f1.y * pg[i].zv1;
+    X0[i] = h2_as_u32(h0);
+    X1[i] = h2_as_u32(h1);
+  }
+  // ---- O^T += V^T . P_v^T
+#pragma unroll
+  for (int i = 0; i < NP; ++i) page_pv<D>(st.acc, so[i], lo, X0[i], X1[i], lane);
+}
+
+// Epilogue of one piece: undo the subnormal scaling, apply the zero-point term, normalise, and
+// write the warp's partial (an empty piece writes zeros with lse = -inf).
+template <int D>
+__device__ __forceinline__ void int4_finish(const SplitArgs &a, PieceState<D> &st, long long slot, int sub,
+                                            int h, int lane) {
+  using Gm = Int4Geom<D>;
+  const float l0 = warp_sum_g(st.l0), l1 = warp_sum_g(st.l1);
+  const float pz0 = warp_sum_g(st.pz0), pz1 = warp_sum_g(st.pz1);
   const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
   float o0[D / 8], o1[D / 8];
 #pragma unroll
   for (int mt = 0; mt < Gm::MT; ++mt) {
-    o0[2 * mt] = (acc[mt][0] * kTwo24 - pz0) * inv0;
-    o1[2 * mt] = (acc[mt][1] * kTwo24 - pz1) * inv1;
-    o0[2 * mt + 1] = (acc[mt][2] * kTwo20 - pz0) * inv0;
-    o1[2 * mt + 1] = (acc[mt][3] * kTwo20 - pz1) * inv1;
+    o0[2 * mt] = (st.acc[mt][0] * kTwo24 - pz0) * inv0;
+    o1[2 * mt] = (st.acc[mt][1] * kTwo24 - pz1) * inv1;
+    o0[2 * mt + 1] = (st.acc[mt][2] * kTwo20 - pz0) * inv0;
+    o1[2 * mt + 1] = (st.acc[mt][3] * kTwo20 - pz1) * inv1;
   }
-  const float lse0 = l0 > 0.f ? m0 + log2f(l0) : -INFINITY;
-  const float lse1 = l1 > 0.f ? m1 + log2f(l1) : -INFINITY;
-  store_partial<D>(p.s, slot, sub, h, lane, o0, o1, lse0, lse1);
+  const float lse0 = l0 > 0.f ? st.m0 + log2f(l0) : -INFINITY;
+  const float lse1 = l1 > 0.f ? st.m1 + log2f(l1) : -INFINITY;
+  store_partial<D>(a, slot, sub, h, lane, o0, o1, lse0, lse1);
 }
 
-template <int D, int NSTAGE>
+// W = warps per kv head (8 / heads per CTA). Stage k of the ring (slot k % NS) holds run pages
+// k * W .. k * W + W - 1 for the CTA's HB = 8 / W heads; warp w reads tile w of it.
+// Ring protocol: s_full[slot] completes when a stage's copies have landed (one arrival: the
+// expect_tx of the issuing lane 0, plus the copies' bytes); s_empty[slot] completes when all 256
+// threads have finished reading it (every thread arrives once). Warp 0 is also the producer: it
+// issued the first NS stages and refills a slot once its s_empty phase completes -- polling
+// without blocking between pages, and blocking only for a stage it needs itself.
+template <int D, int NS, int W>
 __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_constant__ Int4Params p) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t s_bars[8][NSTAGE];
-  // the swizzled TMA tiles need 1024-byte alignment: round the dynamic base up (1 KB of slack)
-  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  asm volatile("griddepcontrol.launch_dependents;");  // let the merge kernel's launch begin early
   using Gm = Int4Geom<D>;
+  constexpr int HB = 8 / W;
+  constexpr int SCP = 64 * HB < 128 ? 128 : 64 * HB;  // one page's scale block, 128-byte aligned slots
+  static_assert(NS >= 2 && NS * W <= 64, "the prologue reads at most two batches of block ids");
+  __shared__ __align__(8) uint64_t s_full[NS], s_empty[NS];
+  asm volatile("griddepcontrol.launch_dependents;");  // let the merge kernel's launch begin early
+  // stages start at the first 1024-byte aligned offset of the dynamic buffer (swizzled TMA tiles)
+  const uint32_t dbase = smem_u32(kvq_dsmem);
+  const uint32_t base = (1024u - (dbase & 1023u)) & 1023u;
+  const SplitArgs &a = p.s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // dynamic smem: [8 warps][NSTAGE][KVSTAGE] K/V tiles, then [8][NSTAGE][SCSTAGE], then [8][QBYTES]
-  Ring rg;
-  rg.kv = smem + warp * NSTAGE * Gm::KVSTAGE;
-  rg.sc = smem + 8 * NSTAGE * Gm::KVSTAGE + warp * NSTAGE * Gm::SCSTAGE;
-  uint8_t *qarea = smem + 8 * NSTAGE * (Gm::KVSTAGE + Gm::SCSTAGE) + warp * Gm::QBYTES;
-  rg.bars = smem_u32(&s_bars[warp][0]);
-  rg.issued = rg.consumed = 0;
-  rg.abort = false;
-  if (lane == 0) {
-    for (int i = 0; i < NSTAGE; ++i) mbar_init(rg.bars + 8 * i, 1);
+  const int hl = warp % HB, sub = warp / HB;
+  const int h0 = blockIdx.y * HB, h = h0 + hl;
+  const bool split_heads = a.Hk > 8;
+
+  PageRun run;
+  if (!page_run(a, &g_flags_decode_int4, &run)) return;  // uniform over the CTA
+  const int n_stages = (run.n + W - 1) / W;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(smem_u32(&s_full[i]), 1);
+      mbar_init(smem_u32(&s_empty[i]), 256);
+    }
     mbar_init_fence();
   }
-  __syncwarp();
-  const int hl = warp % p.s.heads_per_cta;
-  const int sub = warp / p.s.heads_per_cta;
-  const int h = blockIdx.y * p.s.heads_per_cta + hl;
-  for_each_piece(p.s, &g_flags_decode_int4, [&](int b, int t0, int t1, long long slot) {
-    int4_piece<D, NSTAGE>(p, rg, qarea, b, h, sub, t0, t1, slot);
-  });
+  __syncthreads();
+
+  // ---- producer state (warp 0): block ids, 32 run pages per batch, lane l of a batch register
+  // holding run page 32 * batch + l; each lane walks its own sequence cursor (monotone).
+  SeqCursor lc = run.first;
+  auto load_batch = [&](int k) -> int {
+    const int x = k * 32 + lane;
+    if (x >= run.n) return 0;
+    const long long X = run.base + x;
+    while (X >= lc.P + lc.np && lc.b < a.B) seq_next(a, lc);
+    return lc.b < a.B ? __ldg(p.block_table + static_cast<long long>(lc.b) * a.max_blocks + (X - lc.P)) : -1;
+  };
+  // Stage k into ring slot `slot`: lane i copies page k * W + i (expect_tx first, by lane 0).
+  auto issue = [&](int k, int slot, int bid) {  // warp-wide
+    const int x0 = k * W, npg = min(W, run.n - x0);
+    const uint32_t bar = smem_u32(&s_full[slot]);
+    const uint32_t stg = dbase + base + slot * Gm::STAGE;
+    const int raw = __shfl_sync(FULL, bid, (x0 + lane) & 31);
+    if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(npg * (2 * HB * Gm::TILE + 2 * 64 * HB)));
+    __syncwarp();
+    if (lane < npg) {
+      const bool ok = raw >= 0 && raw < p.num_blocks;
+      if (!ok) atomicOr(&g_flags_decode_int4, ERR_BLOCK);
+      const int blk = ok ? raw : 0;  // out of range: flagged, page 0 read instead
+      fence_proxy_async();  // the earlier reads of this slot come before the copies that refill it
+      tma_load_4d(stg + lane * HB * Gm::TILE, &p.maps.k, 0, 0, h0, blk, bar);
+      tma_load_4d(stg + Gm::VOFF + lane * HB * Gm::TILE, &p.maps.v, 0, 0, h0, blk, bar);
+      const uint32_t ks = stg + Gm::SOFF + lane * SCP, vs = ks + Gm::SCPOOL;
+      if (split_heads) {
+        tma_load_3d(ks, &p.maps.ks, h0, 0, blk, bar);
+        tma_load_3d(vs, &p.maps.vs, h0, 0, blk, bar);
+      } else {
+        tma_load_2d(ks, &p.maps.ks, 0, blk, bar);
+        tma_load_2d(vs, &p.maps.vs, 0, blk, bar);
+      }
+    }
+  };
+  int nxt = 0, nslot = 0, nrnd = 0;  // next stage to issue, its slot and round (warp 0)
+  int cb = 0, bid_cur = 0, bid_next = 0;
+  if (warp == 0) {
+    bid_cur = load_batch(0);
+    bid_next = load_batch(1);
+    for (; nxt < NS && nxt < n_stages; ++nxt) issue(nxt, nxt, ((nxt * W) >> 5) == 0 ? bid_cur : bid_next);
+    nslot = nxt == NS ? 0 : nxt;
+    nrnd = nxt == NS ? 1 : 0;
+  }
+  // Warp 0: issue the stages whose slot is free, in order; wait (bounded) for a slot only while
+  // the next stage is one this warp needs (<= need). False on a timeout.
+  auto produce = [&](int need) -> bool {
+    while (nxt < n_stages) {
+      const uint32_t eb = smem_u32(&s_empty[nslot]), par = static_cast<uint32_t>(nrnd - 1) & 1u;
+      if (nxt <= need) {
+        if (!__all_sync(FULL, mbar_wait(eb, par))) return false;
+      } else if (!__all_sync(FULL, mbar_test_wait(eb, par))) {
+        break;
+      }
+      if (((nxt * W) >> 5) > cb) {  // next batch of block ids (loaded a batch ahead)
+        ++cb;
+        bid_cur = bid_next;
+        bid_next = load_batch(cb + 1);
+      }
+      issue(nxt, nslot, bid_cur);
+      ++nxt;
+      if (++nslot == NS) {
+        nslot = 0;
+        ++nrnd;
+      }
+    }
+    return true;
+  };
+
+  // ---- consumer side: warp w takes run page k * W + sub of every stage k
+  uint8_t *qarea = kvq_dsmem + base + NS * Gm::STAGE + warp * Gm::QBYTES;
+  const LaneOffsets<D> lo = lane_offsets<D, W>(warp, sub, hl, lane);
+  SeqCursor cur = run.first;
+  PieceState<D> st;
+  st.reset();
+  uint32_t qf[Gm::KSTEPS][2];
+  float qs0 = 0.f, qs1 = 0.f;
+  bool have_q = false, abort = false;
+  const float sm24 = p.sm_log2 * kTwo24;  // the K operands carry a factor 2^-24
+  // the current piece in run coordinates: its pages are run pages < pe_x, run page x is page
+  // x + off of sequence cur.b, and its tokens are [t0, t1)
+  int pe_x = 0, off = 0, t0 = 0, t1 = 0;
+  auto bounds = [&]() {
+    off = static_cast<int>(run.base - cur.P);
+    if (run.fixed) {
+      pe_x = run.n;
+      t0 = run.t0;
+      t1 = run.t1;
+    } else {
+      pe_x = static_cast<int>(min(static_cast<long long>(run.n), cur.P + cur.np - run.base));
+      t0 = static_cast<int>((max(run.base, cur.P) - cur.P) * kPage);
+      t1 = static_cast<int>(min((min(run.end, cur.P + cur.np) - cur.P) * kPage, static_cast<long long>(cur.L)));
+    }
+  };
+  bounds();
+  auto finish_piece = [&]() {
+    const long long slot = run.fixed ? static_cast<long long>(blockIdx.x) : blockIdx.x + static_cast<long long>(cur.b);
+    int4_finish<D>(a, st, slot, sub, h, lane);
+    if (!run.fixed && warp == 0 && lane == 0 && blockIdx.y == 0) {
+      if (cur.P >= run.base) a.seg_first[cur.b] = static_cast<int>(blockIdx.x);
+      if (cur.P + cur.np <= run.end) a.seg_last[cur.b] = static_cast<int>(blockIdx.x);
+    }
+    st.reset();
+    have_q = false;
+  };
+  // wait for stage k (in `slot`, round rnd); on a timeout (a copy that never completes) raise
+  // the flag, let the copies already issued land (bounded), and report failure
+  auto wait_stage = [&](int k, int slot, int rnd) -> bool {
+    const uint32_t fb = smem_u32(&s_full[slot]);
+    if (__all_sync(FULL, mbar_try_wait(fb, rnd & 1))) return true;
+    if (__all_sync(FULL, mbar_wait(fb, rnd & 1))) return true;
+    if (lane == 0) atomicOr(&g_flags_decode_int4, ERR_TIMEOUT);
+    for (int i = k; i < k + NS && i < n_stages; ++i)
+      mbar_wait(smem_u32(&s_full[i % NS]), (i / NS) & 1, 100000000ull);
+    return false;
+  };
+
+  int j = 0, sj = 0, rj = 0;  // stage j lives in slot sj = j % NS, round rj = j / NS
+  while (j < n_stages) {
+    const int x = j * W + sub;
+    if (x >= run.n) break;
+    if (x >= pe_x) {  // pieces this warp is done with (or has no page of)
+      while (run.base + x >= cur.P + cur.np && cur.b < a.B) {
+        finish_piece();
+        seq_next(a, cur);
+      }
+      if (cur.b >= a.B) break;  // cannot happen: the run lies inside the batch's pages
+      bounds();
+    }
+    if (!have_q) {
+      load_query<D>(p, qarea, cur.b, h, lane, qf, qs0, qs1);
+      have_q = true;
+    }
+    const int nb = (x + off) * kPage;  // position of the page's row 0 in its sequence
+    const int sj1 = sj + 1 == NS ? 0 : sj + 1, rj1 = sj + 1 == NS ? rj + 1 : rj;
+    const uint32_t so[2] = {base + sj * Gm::STAGE, base + sj1 * Gm::STAGE};
+    const bool pair = nb >= t0 && nb + (W + 1) * kPage <= t1 && x + W < pe_x;  // two full pages of the piece
+    if (warp == 0 && !produce(pair ? j + 1 : j)) {
+      abort = true;
+      if (lane == 0) atomicOr(&g_flags_decode_int4, ERR_TIMEOUT);
+      break;
+    }
+    if (pair) {
+      if (!wait_stage(j, sj, rj) || !wait_stage(j + 1, sj1, rj1)) {
+        abort = true;
+        break;
+      }
+      int4_pages<D, W, 2, false>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1);
+      mbar_arrive(smem_u32(&s_empty[sj]));
+      mbar_arrive(smem_u32(&s_empty[sj1]));
+      j += 2;
+      sj = sj1 + 1 == NS ? 0 : sj1 + 1;
+      rj = sj1 + 1 == NS ? rj1 + 1 : rj1;
+    } else {
+      if (!wait_stage(j, sj, rj)) {
+        abort = true;
+        break;
+      }
+      int4_pages<D, W, 1, true>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1);
+      mbar_arrive(smem_u32(&s_empty[sj]));
+      j += 1;
+      sj = sj1;
+      rj = rj1;
+    }
+    if (warp == 0) produce(-1);  // refill what this warp just freed, if the others are done too
+  }
+  if (cur.b < a.B) finish_piece();
+  if (!run.fixed && !abort) {
+    while (cur.P + cur.np < run.end && cur.b < a.B - 1) {  // later pieces of the run without a page of this warp
+      seq_next(a, cur);
+      if (cur.b >= a.B) break;
+      finish_piece();
+    }
+  }
 }
 
-constexpr int kStagesInt4 = 4;
+constexpr int kStagesInt4 = 5;
 
 template <int D>
 size_t int4_smem_bytes() {
   using Gm = Int4Geom<D>;
-  return 8 * static_cast<size_t>(kStagesInt4 * (Gm::KVSTAGE + Gm::SCSTAGE) + Gm::QBYTES) + 1024;
+  return static_cast<size_t>(kStagesInt4) * Gm::STAGE + 8 * Gm::QBYTES + 1024;
 }
 
 bool take_flags_decode_int4(cudaStream_t stream, unsigned *host_word) {
@@ -392,24 +680,35 @@ bool take_flags_decode_int4(cudaStream_t stream, unsigned *host_word) {
                                  cudaMemcpyHostToDevice, stream) == cudaSuccess;
 }
 
-template <int D>
-static kvq_status launch_int4(const Int4Params &p, const SplitPlan &plan, cudaStream_t s) {
+template <int D, int W>
+static kvq_status launch_int4_w(const Int4Params &p, const SplitPlan &plan, cudaStream_t s) {
   const size_t smem = int4_smem_bytes<D>();
   static bool attr_set = false;  // per process; the attribute is per function, not per device
   if (!attr_set) {
-    if (cudaFuncSetAttribute(decode_int4_kernel<D, kStagesInt4>,
+    if (cudaFuncSetAttribute(decode_int4_kernel<D, kStagesInt4, W>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return KVQ_ERR_CUDA;
     attr_set = true;
   }
   const dim3 grid(plan.seg_ctas, plan.head_groups);
-  decode_int4_kernel<D, kStagesInt4><<<grid, 256, smem, s>>>(p);
+  decode_int4_kernel<D, kStagesInt4, W><<<grid, 256, smem, s>>>(p);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   const long long rows = static_cast<long long>(p.s.B) * p.s.Hq;
   if (launch_dependent(merge_kernel<D>, dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), s, p.s) != cudaSuccess)
     return KVQ_ERR_CUDA;
   return launch_status();
+}
+
+template <int D>
+static kvq_status launch_int4(const Int4Params &p, const SplitPlan &plan, cudaStream_t s) {
+  switch (plan.warps_per_head) {
+    case 1: return launch_int4_w<D, 1>(p, plan, s);
+    case 2: return launch_int4_w<D, 2>(p, plan, s);
+    case 4: return launch_int4_w<D, 4>(p, plan, s);
+    case 8: return launch_int4_w<D, 8>(p, plan, s);
+    default: return KVQ_ERR_UNSUPPORTED;
+  }
 }
 
 }  // namespace kvq

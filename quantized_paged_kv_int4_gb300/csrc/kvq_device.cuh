@@ -132,20 +132,56 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
+// Non-blocking probe: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Arrive once on the barrier (release semantics: this thread's earlier accesses come first).
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// try_wait that may suspend the thread (up to hint_ns) until the phase completes, instead of
+// returning at once: a waiting warp then takes no issue slots from the others.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
 }
-// Wait for the phase with the given parity to complete, giving up after ~2 s of wall time
-// (a copy that never lands is a bug; the caller reports ERR_TIMEOUT instead of hanging).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete, giving up after limit_ns of wall time
+// (~2 s by default: a copy that never lands is a bug; the caller reports ERR_TIMEOUT instead of
+// hanging).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t start = global_ns();
   for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - start > 2000000000ull) return false;
+    if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
+    if (global_ns() - start > limit_ns) return false;
   }
+}
+// Shared-memory counter increment with acquire-release semantics at CTA scope; returns the old
+// value. Used to find the last of a CTA's warps to finish reading a buffer.
+__device__ __forceinline__ unsigned atom_add_acq_rel_cta(unsigned *p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(v)
+               : "memory");
+  return old;
 }
 // Order this thread's earlier generic-proxy shared-memory accesses before later async-proxy
 // (TMA) writes to the same buffers.

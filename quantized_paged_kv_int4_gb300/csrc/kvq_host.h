@@ -44,13 +44,14 @@ void workspace_carve(void *workspace, int B, int Hq, int D, const SplitPlan &pla
 // TMA descriptors of one INT4 cache (K, V pools and their scale words), see int4_tensor_maps.
 struct Int4Maps {
   CUtensorMap k, v, ks, vs;
-  int scale_heads;  // heads per scale box: 4 (Hk % 4 == 0) or Hk (Hk < 4)
+  int heads_per_box;  // kv heads one box covers: min(Hk, 8)
 };
-// Encode (or fetch from a small cache) the tensor maps of the pools:
-//   K / V  [num_blocks][16][Hk][D/2] bytes viewed as dims {D/2, Hk, 16, num_blocks}; box
-//          {D/2, 1, 16, 1} = one head's 16 token rows, 64B (D = 128) or 32B (D = 64) swizzle;
-//   scales [num_blocks][16][Hk] words: dims {Hk, 16, num_blocks} with box {4, 16, 1} when
-//          Hk % 4 == 0, else dims {16 * Hk, num_blocks} with box {16 * Hk, 1}.
+// Encode (or fetch from a small cache) the tensor maps of the pools, with HB = min(Hk, 8):
+//   K / V  [num_blocks][16][Hk][D/2] bytes viewed as dims {D/2, 16, Hk, num_blocks} (token
+//          stride Hk * D/2, head stride D/2); box {D/2, 16, HB, 1} = HB heads' 16 token rows
+//          of one page, stored [head][token][row] with the 64B (D = 128) or 32B (D = 64) swizzle;
+//   scales [num_blocks][16][Hk] words: Hk <= 8: dims {16 * Hk, num_blocks}, box {16 * Hk, 1}
+//          (the page's whole block); Hk > 8: dims {Hk, 16, num_blocks}, box {8, 16, 1}.
 // Returns false if the driver entry point is unavailable or an encode fails.
 bool int4_tensor_maps(const void *k_cache, const void *v_cache, const void *k_scale, const void *v_scale,
                       long long num_blocks, int Hk, int D, Int4Maps *maps);
