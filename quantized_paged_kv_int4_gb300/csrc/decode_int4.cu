@@ -122,6 +122,30 @@ __device__ __forceinline__ bool page_run(const SplitArgs &a, unsigned *flags, Pa
   __shared__ long long s_scan[8];
   __shared__ long long s_first_p;
   __shared__ int s_first_b;
+  const long long C = gridDim.x, c = blockIdx.x;
+  if (a.B <= 256) {  // one scan finds both the total and the sequence holding the run's first page
+    const int b = threadIdx.x;
+    const long long np = b < a.B ? (clamped_len(a, b, flags) + kPage - 1) / kPage : 0;
+    long long P_tot;
+    const long long incl = block_scan_256(np, s_scan, &P_tot);
+    const long long q = P_tot / C, r = P_tot % C;
+    const long long pb = c * q + min(c, r), pe = pb + q + (c < r ? 1 : 0);
+    if (pb >= pe) return false;
+    if (np > 0 && incl - np <= pb && pb < incl) {
+      s_first_b = b;
+      s_first_p = incl - np;
+    }
+    __syncthreads();
+    run->fixed = false;
+    run->base = pb;
+    run->end = pe;
+    run->n = static_cast<int>(pe - pb);
+    run->first.b = s_first_b;
+    run->first.P = s_first_p;
+    run->first.L = clamped_len(a, s_first_b, nullptr);
+    run->first.np = (run->first.L + kPage - 1) / kPage;
+    return true;
+  }
   long long P_tot = 0;
   for (int base = 0; base < a.B; base += 256) {
     const int b = base + threadIdx.x;
@@ -130,7 +154,6 @@ __device__ __forceinline__ bool page_run(const SplitArgs &a, unsigned *flags, Pa
     block_scan_256(np, s_scan, &chunk);
     P_tot += chunk;
   }
-  const long long C = gridDim.x, c = blockIdx.x;
   const long long q = P_tot / C, r = P_tot % C;
   const long long pb = c * q + min(c, r), pe = pb + q + (c < r ? 1 : 0);
   if (pb >= pe) return false;
@@ -463,7 +486,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   using Gm = Int4Geom<D>;
   constexpr int HB = 8 / W;
   constexpr int SCP = 64 * HB < 128 ? 128 : 64 * HB;  // one page's scale block, 128-byte aligned slots
-  static_assert(NS >= 2 && NS * W <= 64, "the prologue reads at most two batches of block ids");
+  static_assert(NS >= 2 && NS * W <= 64, "refills read at most two batches of block ids ahead");
   __shared__ __align__(8) uint64_t s_full[NS], s_empty[NS];
   asm volatile("griddepcontrol.launch_dependents;");  // let the merge kernel's launch begin early
   // stages start at the first 1024-byte aligned offset of the dynamic buffer (swizzled TMA tiles)
@@ -527,9 +550,12 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   if (warp == 0) {
     bid_cur = load_batch(0);
     bid_next = load_batch(1);
-    for (; nxt < NS && nxt < n_stages; ++nxt) issue(nxt, nxt, ((nxt * W) >> 5) == 0 ? bid_cur : bid_next);
-    nslot = nxt == NS ? 0 : nxt;
-    nrnd = nxt == NS ? 1 : 0;
+    // Only the first two stages now: at launch every CTA requests its first stages at once and
+    // DRAM serves them interleaved, so a shorter first request lands sooner; the other slots
+    // are filled as soon as this warp has its first stage (produce after the first wait).
+    for (; nxt < 2 && nxt < n_stages; ++nxt) issue(nxt, nxt, bid_cur);
+    nslot = nxt;
+    nrnd = 0;
   }
   // Warp 0: issue the stages whose slot is free, in order; wait (bounded) for a slot only while
   // the next stage is one this warp needs (<= need). False on a timeout.
@@ -624,7 +650,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     const int sj1 = sj + 1 == NS ? 0 : sj + 1, rj1 = sj + 1 == NS ? rj + 1 : rj;
     const uint32_t so[2] = {base + sj * Gm::STAGE, base + sj1 * Gm::STAGE};
     const bool pair = nb >= t0 && nb + (W + 1) * kPage <= t1 && x + W < pe_x;  // two full pages of the piece
-    if (warp == 0 && !produce(pair ? j + 1 : j)) {
+    if (warp == 0 && nxt <= (pair ? j + 1 : j) && !produce(pair ? j + 1 : j)) {
       abort = true;
       if (lane == 0) atomicOr(&g_flags_decode_int4, ERR_TIMEOUT);
       break;
@@ -634,6 +660,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
         abort = true;
         break;
       }
+      if (warp == 0) produce(-1);  // the slots freed meanwhile (at the start: the unused ones)
       int4_pages<D, W, 2, false>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1);
       mbar_arrive(smem_u32(&s_empty[sj]));
       mbar_arrive(smem_u32(&s_empty[sj1]));
@@ -645,6 +672,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
         abort = true;
         break;
       }
+      if (warp == 0) produce(-1);  // the slots freed meanwhile (at the start: the unused ones)
       int4_pages<D, W, 1, true>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1);
       mbar_arrive(smem_u32(&s_empty[sj]));
       j += 1;
@@ -663,7 +691,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   }
 }
 
-constexpr int kStagesInt4 = 5;
+constexpr int kStagesInt4 = 4;
 
 template <int D>
 size_t int4_smem_bytes() {
