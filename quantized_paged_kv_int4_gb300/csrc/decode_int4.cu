@@ -200,48 +200,89 @@ struct PieceState {
 
 // q_rot = bf16(H(q * d1)) for the G heads of kv head h of sequence b, as the fp16 B fragments
 // of the score MMA (odd dims pre-divided by 16) and the per-head sums of the q the products use.
+// Start copying the G raw query rows of (sequence b, kv head h) -- contiguous, G * D bf16 -- into
+// this warp's area (16-byte cp.async per lane); load_query waits for them.
+template <int D>
+__device__ __forceinline__ void fetch_query(const Int4Params &p, uint8_t *qarea, int b, int h, int lane) {
+  const int G = p.s.G;
+  const uint8_t *src = reinterpret_cast<const uint8_t *>(
+      p.q + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(h) * G) * D);
+  const uint32_t dst = smem_u32(qarea);
+  for (int c = lane; c < G * D / 8; c += 32) cp_async<16>(dst + 16 * c, src + 16 * c, true);
+  cp_async_commit();
+}
+
 template <int D>
 __device__ __forceinline__ void load_query(const Int4Params &p, uint8_t *qarea, int b, int h, int lane,
-                                           uint32_t (&qf)[D / 16][2], float &qs0, float &qs1) {
+                                           uint32_t (&qf)[D / 16][2], float &qs0, float &qs1, bool fetched) {
   using Gm = Int4Geom<D>;
   constexpr int J = D / 32;
   const int g = lane >> 2, t = lane & 3, G = p.s.G;
-  const __nv_bfloat16 *qb = p.q + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(h) * G) * D;
   __half *qh = reinterpret_cast<__half *>(qarea);
   float *qsum = reinterpret_cast<float *>(qarea + 8 * D * 2);
+  // The raw rows land in this warp's area (fetch_query, issued early when possible); each head is
+  // then rotated and converted in place (a lane rewrites exactly the elements it read).
   __syncwarp();
+  if (!fetched) fetch_query<D>(p, qarea, b, h, lane);
+  cp_async_wait<0>();
+  float sg[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) sg[j] = p.s.signs != nullptr ? __ldg(p.s.signs + lane + 32 * j) : 1.f;
+  __syncwarp();
+  const __nv_bfloat16 *qraw = reinterpret_cast<const __nv_bfloat16 *>(qarea);
+  // four heads at a time, interleaved: their shuffle chains overlap instead of running back to back
+  for (int n0 = 0; n0 < G; n0 += 4) {
+    float x[4][J];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int j = 0; j < J; ++j)
+        x[i][j] = n0 + i < G ? __bfloat162float(qraw[(n0 + i) * D + lane + 32 * j]) * sg[j] : 0.f;
+    }
+    if (p.s.signs != nullptr) {
+#pragma unroll
+      for (int mask = 1; mask < 32; mask <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+          for (int j = 0; j < J; ++j) x[i][j] = butterfly_xor(x[i][j], lane, mask);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        butterfly_local<J>(x[i]);
+#pragma unroll
+        for (int j = 0; j < J; ++j) x[i][j] = bf16_round(x[i][j]);
+      }
+    }
+    // odd dims meet high nibbles, which enter the MMA 16x larger: pre-divide q by 16 (exact)
+    float eff[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      eff[i] = 0.f;
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const int e = lane + 32 * j;
+        const __half v = __float2half_rn((e & 1) ? x[i][j] * 0.0625f : x[i][j]);
+        if (n0 + i < G) qh[(n0 + i) * D + e] = v;
+        eff[i] += (e & 1) ? __half2float(v) * 16.f : __half2float(v);
+      }
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) eff[i] += __shfl_xor_sync(FULL, eff[i], m);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (n0 + i < G) qsum[n0 + i] = eff[i] * (1.0f / kTwo24);  // sum of the q the products use
+    }
+  }
   for (int n = G; n < 8; ++n) {  // padded MMA columns
 #pragma unroll
     for (int j = 0; j < J; ++j) qh[n * D + lane + 32 * j] = __float2half_rn(0.f);
     if (lane == 0) qsum[n] = 0.f;
-  }
-  for (int n = 0; n < G; ++n) {
-    float x[J];
-#pragma unroll
-    for (int j = 0; j < J; ++j) x[j] = __bfloat162float(qb[n * D + lane + 32 * j]);
-    if (p.s.signs != nullptr) {
-#pragma unroll
-      for (int j = 0; j < J; ++j) x[j] *= __ldg(p.s.signs + lane + 32 * j);
-#pragma unroll
-      for (int mask = 1; mask < 32; mask <<= 1) {
-#pragma unroll
-        for (int j = 0; j < J; ++j) x[j] = butterfly_xor(x[j], lane, mask);
-      }
-      butterfly_local<J>(x);
-#pragma unroll
-      for (int j = 0; j < J; ++j) x[j] = bf16_round(x[j]);
-    }
-    // odd dims meet high nibbles, which enter the MMA 16x larger: pre-divide q by 16 (exact)
-    float eff = 0.f;
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const int e = lane + 32 * j;
-      const __half v = __float2half_rn((e & 1) ? x[j] * 0.0625f : x[j]);
-      qh[n * D + e] = v;
-      eff += (e & 1) ? __half2float(v) * 16.f : __half2float(v);
-    }
-    eff = warp_sum(eff);
-    if (lane == 0) qsum[n] = eff * (1.0f / kTwo24);  // sum of the q the products use, in MMA units
   }
   __syncwarp();
   // B fragment of k-step ks = 2m + s: the dims a K word's nibbles occupy after the LOP3 split
@@ -545,6 +586,19 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
       }
     }
   };
+  // the first piece's query rows go out before any page copy, so they do not queue behind the
+  // launch-time burst of page copies
+  uint8_t *qarea = kvq_dsmem + base + NS * Gm::STAGE + warp * Gm::QBYTES;
+  int q_prefetched = -1;  // sequence whose query rows fetch_query has started
+  if (sub < run.n) {
+    SeqCursor c0 = run.first;
+    const long long X0 = run.base + sub;
+    while (X0 >= c0.P + c0.np && c0.b < a.B) seq_next(a, c0);
+    if (c0.b < a.B) {
+      fetch_query<D>(p, qarea, c0.b, h, lane);
+      q_prefetched = c0.b;
+    }
+  }
   int nxt = 0, nslot = 0, nrnd = 0;  // next stage to issue, its slot and round (warp 0)
   int cb = 0, bid_cur = 0, bid_next = 0;
   if (warp == 0) {
@@ -583,7 +637,6 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   };
 
   // ---- consumer side: warp w takes run page k * W + sub of every stage k
-  uint8_t *qarea = kvq_dsmem + base + NS * Gm::STAGE + warp * Gm::QBYTES;
   const LaneOffsets<D> lo = lane_offsets<D, W>(warp, sub, hl, lane);
   SeqCursor cur = run.first;
   PieceState<D> st;
@@ -643,7 +696,8 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
       bounds();
     }
     if (!have_q) {
-      load_query<D>(p, qarea, cur.b, h, lane, qf, qs0, qs1);
+      load_query<D>(p, qarea, cur.b, h, lane, qf, qs0, qs1, q_prefetched == cur.b);
+      q_prefetched = -1;
       have_q = true;
     }
     const int nb = (x + off) * kPage;  // position of the page's row 0 in its sequence

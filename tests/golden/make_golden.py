@@ -81,6 +81,7 @@ def fwht_fixture(rng):
     x[1] *= F32(1e-3)       # small row: the 1e-4 absmax floor is not reached, scale < 1
     x[2] = F32(0.0)         # all-zero row: absmax floored at 1e-4
     x[3, 7] = F32(3000.0)   # outlier row
+    x = formats.bf16_round(x)  # the kernel's input is bf16: keep every fixture row bf16-exact
     y, s = fwht_fp8.fwht128_quant_fp8(x)
     return {"x_bf16_as_f32": hexs(x), "y_e4m3": hexs(y), "row_scale_f32": hexs(s)}
 

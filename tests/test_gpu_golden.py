@@ -63,7 +63,7 @@ def test_fwht_matches_fixture():
     x = _bf16(_arr(f["x_bf16_as_f32"], F32, (4, 128))).cuda()
     y, s = kvq.kvq_fwht128(x)
     torch.cuda.synchronize()
-    assert y.cpu().numpy().tobytes().hex() == f["y_e4m3"]
+    assert y.view(torch.uint8).cpu().numpy().tobytes().hex() == f["y_e4m3"]
     assert s.cpu().numpy().tobytes().hex() == f["row_scale_f32"]
 
 
