@@ -223,7 +223,10 @@ __device__ __forceinline__ void load_query(const Int4Params &p, uint8_t *qarea, 
   // The raw rows land in this warp's area (fetch_query, issued early when possible); each head is
   // then rotated and converted in place (a lane rewrites exactly the elements it read).
   __syncwarp();
-  if (!fetched) fetch_query<D>(p, qarea, b, h, lane);
+  if (!fetched) {
+    cp_async_wait<0>();  // a prefetch of another sequence's rows may still be landing here
+    fetch_query<D>(p, qarea, b, h, lane);
+  }
   cp_async_wait<0>();
   float sg[J];
 #pragma unroll
@@ -698,6 +701,14 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     if (!have_q) {
       load_query<D>(p, qarea, cur.b, h, lane, qf, qs0, qs1, q_prefetched == cur.b);
       q_prefetched = -1;
+      if (pe_x < run.n && !run.fixed) {  // the run goes on into another sequence: fetch its query now
+        SeqCursor nx = cur;
+        seq_next(a, nx);
+        if (nx.b < a.B) {
+          fetch_query<D>(p, qarea, nx.b, h, lane);
+          q_prefetched = nx.b;
+        }
+      }
       have_q = true;
     }
     const int nb = (x + off) * kPage;  // position of the page's row 0 in its sequence
