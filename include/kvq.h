@@ -197,7 +197,7 @@ KVQ_API kvq_status kvq_decode_tq(const float *q, const uint8_t *kv_cache, int32_
  *   x = bf16(FWHT128(row) * fp32(0.08838834764831845));  a = max(max |x|, 1e-4)
  *   s = smallest power of two >= a * fp32(1/448);   y = e4m3_rne(clamp(x / s, -448, 448))
  *   x         bf16 [rows, 128] contiguous, 16-byte aligned.
- *   y_e4m3    uint8 [rows, 128] (E4M3FN codes), 8-byte aligned.    row_scale  fp32 [rows] (s).
+ *   y_e4m3    uint8 [rows, 128] (E4M3FN codes), 16-byte aligned.    row_scale  fp32 [rows] (s).
  * Bit-exact.
  */
 KVQ_API kvq_status kvq_fwht128(const void *x, uint8_t *y_e4m3, float *row_scale, int64_t rows,

@@ -6,67 +6,95 @@
 // product absmax * fp32(1/448)), y = clamp(x / scale, +-448) stored as E4M3FN (round to nearest
 // even). The rotated row never leaves registers.
 //
-// Mapping: a half-warp per 128-wide row, 8 elements (16 bytes) per lane; one warp = 2 rows.
+// Mapping: 8 lanes per 128-wide row, 16 elements per lane; one warp = 4 rows.
 
 #include "kvq_device.cuh"
 #include "kvq_host.h"
 
 namespace kvq {
 
+// Row r of a warp (4 rows per warp) is viewed as 8 x 16: lane l8 of the row holds elements
+// 16 l8 .. 16 l8 + 15. Stages h = 1 .. 8 run in the lane; for h = 16, 32, 64 the warp transposes
+// its rows through shared memory (lane l8 then holds columns 2 l8, 2 l8 + 1 of all 8 row-blocks),
+// runs them in registers and transposes back -- the pages' stage order throughout.
+constexpr int kFwRow = 16 + 4;          // padded 16-element block (words)
+constexpr int kFwVec = 8 * kFwRow + 16; // padded row: the 4 rows of a warp in two bank halves
+
 __global__ void __launch_bounds__(256) fwht128_fp8_kernel(const __nv_bfloat16 *__restrict__ x,
                                                           uint8_t *__restrict__ y,
                                                           float *__restrict__ row_scale,
                                                           long long rows) {
-  const int lane = threadIdx.x & 31;
-  const int l16 = lane & 15;
-  const long long row = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * 2 + (lane >> 4);
+  __shared__ __align__(16) float s_buf[8][4 * kFwVec];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rw = lane >> 3, l8 = lane & 7;
+  const long long row = (static_cast<long long>(blockIdx.x) * 8 + warp) * 4 + rw;
   const bool live = row < rows;
-  float v[8];
-  {
-    uint4 raw = make_uint4(0, 0, 0, 0);
-    if (live) raw = __ldg(reinterpret_cast<const uint4 *>(x + row * 128) + l16);
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint4 raw = live ? __ldg(reinterpret_cast<const uint4 *>(x + row * 128 + 16 * l8) + i) : make_uint4(0, 0, 0, 0);
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[2 * i] = __uint_as_float(w[i] << 16);
-      v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    for (int k = 0; k < 4; ++k) {
+      v[8 * i + 2 * k] = __uint_as_float(w[k] << 16);
+      v[8 * i + 2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
     }
   }
-  butterfly_local<8>(v);  // h = 1, 2, 4
+  butterfly_local<16>(v);  // h = 1, 2, 4, 8
+  float *buf = &s_buf[warp][rw * kFwVec];
 #pragma unroll
-  for (int m = 1; m < 16; m <<= 1) {  // h = 8, 16, 32, 64
+  for (int i = 0; i < 4; ++i)
+    *reinterpret_cast<float4 *>(buf + l8 * kFwRow + 4 * i) = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  __syncwarp();
+  float c0[8], c1[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = butterfly_xor(v[j], l16, m);
+  for (int r = 0; r < 8; ++r) {
+    const float2 f = *reinterpret_cast<const float2 *>(buf + r * kFwRow + 2 * l8);
+    c0[r] = f.x;
+    c1[r] = f.y;
   }
+  butterfly_local<8>(c0);  // h = 16, 32, 64
+  butterfly_local<8>(c1);
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < 8; ++r) *reinterpret_cast<float2 *>(buf + r * kFwRow + 2 * l8) = make_float2(c0[r], c1[r]);
+  __syncwarp();
   const float kInvSqrt128 = 0x1.6a09e6p-4f;  // 0.08838834764831845 rounded to fp32
   float amax = 0.f;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    v[j] = bf16_round(__fmul_rn(v[j], kInvSqrt128));
-    amax = fmaxf(amax, fabsf(v[j]));
+  for (int i = 0; i < 4; ++i) {
+    const float4 f = *reinterpret_cast<const float4 *>(buf + l8 * kFwRow + 4 * i);
+    v[4 * i] = bf16_round(__fmul_rn(f.x, kInvSqrt128));
+    v[4 * i + 1] = bf16_round(__fmul_rn(f.y, kInvSqrt128));
+    v[4 * i + 2] = bf16_round(__fmul_rn(f.z, kInvSqrt128));
+    v[4 * i + 3] = bf16_round(__fmul_rn(f.w, kInvSqrt128));
   }
 #pragma unroll
-  for (int m = 1; m < 16; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, m));
+  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, m));
   amax = fmaxf(amax, 1e-4f);
   const float kInv448 = 0x1.24924ap-9f;  // 1/448 rounded to fp32
   const uint32_t mb = __float_as_uint(__fmul_rn(amax, kInv448));
   // smallest power of two >= m: m itself when its mantissa is zero, else the next binade
-  const float s = (mb & 0x007FFFFFu) ? __uint_as_float((mb & 0x7F800000u) + 0x00800000u)
-                                     : __uint_as_float(mb);
-  uint32_t lo = 0, hi = 0;
+  const uint32_t sb = (mb & 0x007FFFFFu) ? (mb & 0x7F800000u) + 0x00800000u : mb;
+  const float s = __uint_as_float(sb);
+  // x / s == x * (1/s) exactly while s is a power of two below 2^127 (1/s is then one too); an
+  // infinite input row (s = inf) keeps the division
+  const bool by_inv = sb < 0x7F000000u;
+  const float inv = __uint_as_float(0x7F000000u - (by_inv ? sb : 0x3F800000u));
+  auto q8 = [&](float x) { return fminf(fmaxf(by_inv ? __fmul_rn(x, inv) : __fdiv_rn(x, s), -448.f), 448.f); };
+  uint32_t out[4];
 #pragma unroll
-  for (int j = 0; j < 8; j += 2) {
-    const float a = fminf(fmaxf(__fdiv_rn(v[j], s), -448.f), 448.f);
-    const float b = fminf(fmaxf(__fdiv_rn(v[j + 1], s), -448.f), 448.f);
-    const uint32_t pair = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-    if (j < 4)
-      lo |= pair << (8 * j);
-    else
-      hi |= pair << (8 * (j - 4));
+  for (int k = 0; k < 4; ++k) {
+    const float a = q8(v[4 * k]), b = q8(v[4 * k + 1]), c = q8(v[4 * k + 2]), d = q8(v[4 * k + 3]);
+    const uint32_t p0 = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t p1 = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    out[k] = p0 | (p1 << 16);
   }
   if (live) {
-    reinterpret_cast<uint2 *>(y + row * 128)[l16] = make_uint2(lo, hi);
-    if (l16 == 0) row_scale[row] = s;
+    reinterpret_cast<uint4 *>(y + row * 128)[l8] = make_uint4(out[0], out[1], out[2], out[3]);
+    if (l8 == 0) row_scale[row] = s;
   }
 }
 
@@ -78,9 +106,9 @@ extern "C" kvq_status kvq_fwht128(const void *x, uint8_t *y_e4m3, float *row_sca
                                   kvq_stream_t stream) {
   if (rows < 0) return KVQ_ERR_INVALID_ARG;
   if (rows == 0) return KVQ_OK;
-  if (!x || !y_e4m3 || !row_scale || !aligned(x, 16) || !aligned(y_e4m3, 8) || !aligned(row_scale, 4))
+  if (!x || !y_e4m3 || !row_scale || !aligned(x, 16) || !aligned(y_e4m3, 16) || !aligned(row_scale, 4))
     return KVQ_ERR_INVALID_ARG;
-  const long long blocks = (rows + 15) / 16;
+  const long long blocks = (rows + 31) / 32;
   if (blocks > 0x7fffffffLL) return KVQ_ERR_UNSUPPORTED;
   fwht128_fp8_kernel<<<static_cast<unsigned>(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       static_cast<const __nv_bfloat16 *>(x), y_e4m3, row_scale, rows);
