@@ -78,7 +78,8 @@ KVQ_API int32_t kvq_abi_version(void);
  *   k_scale, v_scale  fp32 words [num_blocks, block_size, Hk], 4-byte aligned.
  *   slot_mapping      int64 [T]; entries < 0 are skipped; entries >= num_blocks*block_size are
  *                     skipped and flagged. Two tokens with the same slot race (caller error).
- *   rht_signs         fp32 [D] of +1/-1, or NULL for no rotation.
+ *   rht_signs         fp32 [D] of +1/-1, or NULL for no rotation; 16-byte aligned. Only each
+ *                     entry's sign bit is read (the flip x * (+-1) is exact).
  *   D                 64 or 128.
  */
 KVQ_API kvq_status kvq_write_int4(const void *key, const void *value, int64_t k_stride_t,

@@ -30,12 +30,39 @@ struct WriteParams {
   const float *signs;
   int32_t T, Hk, block_size;
   int64_t num_blocks;
+  uint32_t pairs;               // T * Hk (< 2^31)
+  uint32_t hk_magic, hk_shift;  // pair / Hk == (umulhi(pair, hk_magic) + pair) >> hk_shift
 };
 
-// clamp(round_half_away(x), 0, 15) for the x = fp32 value the pages round (see above)
-__device__ __forceinline__ uint32_t nibble_of(float x) {
-  const float w = fminf(fmaxf(__fadd_rn(x, 0.5f), 0.f), 15.5f);
-  return __float_as_uint(__fadd_rz(w, 8388608.0f)) & 0xFu;
+// Bits of the code clamp(rha(u), 0, 15) for the fp32 value u the pages round, as 0x49000000 | code.
+// w = fl(u + 0.5) scaled by 2^-4 is one fused multiply-add (u * 2^-4 is exact, so its single
+// rounding is that of u + 0.5), saturated to [0, 1] (NaN -> 0); adding 2^19 toward zero leaves
+// trunc(16 w) in the low bits (the ulp at 2^19 is 2^-4), and an integer min caps it at 15. Equal to
+// trunc(clamp(fl(u + 0.5), 0, 15.5)), which is clamp(rha(u), 0, 15) for every u.
+__device__ __forceinline__ uint32_t code_bits(float u) {
+  const float w = __saturatef(__fmaf_rn(u, 0.0625f, 0.03125f));
+  return min(__float_as_uint(__fadd_rz(w, 524288.0f)), 0x4900000Fu);
+}
+
+// Eight code words (element 2i in the low nibble of byte i) -> one packed word. lo + (hi << 4)
+// puts a finished byte in bits 0..7 (the constant upper bits land above it); byte_perm gathers.
+__device__ __forceinline__ uint32_t pack_codes(const uint32_t (&c)[8]) {
+  const uint32_t b0 = c[0] + (c[1] << 4), b1 = c[2] + (c[3] << 4);
+  const uint32_t b2 = c[4] + (c[5] << 4), b3 = c[6] + (c[7] << 4);
+  return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
+}
+
+__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t w) {
+  __nv_bfloat162 r;
+  memcpy(&r, &w, 4);
+  return r;
+}
+
+__device__ __forceinline__ uint32_t bf2_bits(float lo, float hi) {
+  const __nv_bfloat162 r = __float22bfloat162_rn(make_float2(lo, hi));
+  uint32_t w;
+  memcpy(&w, &r, 4);
+  return w;
 }
 
 template <int D>
@@ -46,126 +73,185 @@ struct WriteGeom {
   static constexpr int VEC = 8 * ROW + 16; // padded vector: the 4 vectors of a warp in two bank halves
 };
 
+// One lane's share of a (token, head) vector: E bf16 values as E/2 words (element 2i low).
 template <int D>
-__global__ void __launch_bounds__(256) write_int4_kernel(const WriteParams p) {
+struct WriteUnit {
+  uint32_t w[D / 16];
+  long long slot;
+  int t, h;
+  bool in_range;
+};
+
+// Tile = 16 (token, kv head) pairs; warp w takes pairs 2w, 2w + 1, lanes 8v .. 8v + 7 vector v
+// (K of pair 0, V of pair 0, K of pair 1, V of pair 1).
+template <int D>
+__device__ __forceinline__ void load_unit(const WriteParams &p, long long tile, int warp, int v, int l8,
+                                          WriteUnit<D> &u) {
+  constexpr int E = D / 8;
+  const uint32_t pair = static_cast<uint32_t>(tile) * 16u + warp * 2 + (v >> 1);
+  u.in_range = pair < p.pairs;
+  const uint32_t t = (__umulhi(pair, p.hk_magic) + pair) >> p.hk_shift;
+  u.t = u.in_range ? static_cast<int>(t) : 0;
+  u.h = u.in_range ? static_cast<int>(pair - t * static_cast<uint32_t>(p.Hk)) : 0;
+  u.slot = u.in_range ? __ldg(p.slot_mapping + u.t) : -1;
+  const __nv_bfloat16 *src = ((v & 1) ? p.value + u.t * p.v_stride_t + u.h * p.v_stride_h
+                                      : p.key + u.t * p.k_stride_t + u.h * p.k_stride_h) + l8 * E;
+#pragma unroll
+  for (int i = 0; i < E / 8; ++i) {
+    // loaded whatever the slot says (a skipped token's row is read but not stored), so the load
+    // does not wait for slot_mapping
+    const uint4 raw = u.in_range ? __ldg(reinterpret_cast<const uint4 *>(src) + i) : make_uint4(0, 0, 0, 0);
+    u.w[4 * i] = raw.x;
+    u.w[4 * i + 1] = raw.y;
+    u.w[4 * i + 2] = raw.z;
+    u.w[4 * i + 3] = raw.w;
+  }
+}
+
+template <int D, bool ROT>
+__global__ void __launch_bounds__(256, 4) write_int4_kernel(const WriteParams p, long long tiles) {
   using Wg = WriteGeom<D>;
-  constexpr int E = Wg::E, CPL = Wg::CPL;
+  constexpr int E = Wg::E, CPL = Wg::CPL, NW = E / 2;
   __shared__ __align__(16) float s_buf[8][4 * Wg::VEC];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int v = lane >> 3, l8 = lane & 7;  // vector of the warp (K/V of pair 0, K/V of pair 1), row
+  const int v = lane >> 3, l8 = lane & 7;
   const bool is_v = v & 1;
-  const long long pair = static_cast<long long>(blockIdx.x) * 16 + warp * 2 + (v >> 1);
-  const bool in_range = pair < static_cast<long long>(p.T) * p.Hk;
-  bool valid = in_range;
-  const int t = valid ? static_cast<int>(pair / p.Hk) : 0;
-  const int h = valid ? static_cast<int>(pair % p.Hk) : 0;
-  const long long slot = valid ? __ldg(p.slot_mapping + t) : -1;
-  if (valid && slot >= p.num_blocks * p.block_size) {
-    if (l8 == 0 && !is_v) atomicOr(&g_flags_write, ERR_SLOT);
-    valid = false;
-  }
-  valid = valid && slot >= 0;  // padding tokens store nothing
-
-  float x[E];
-  {
-    const __nv_bfloat16 *src = (is_v ? p.value + t * p.v_stride_t + h * p.v_stride_h
-                                     : p.key + t * p.k_stride_t + h * p.k_stride_h) + l8 * E;
-#pragma unroll
-    for (int i = 0; i < E / 8; ++i) {
-      // loaded whatever the slot says (a skipped token's row is read but not stored), so the
-      // load does not wait for slot_mapping
-      const uint4 raw = in_range ? __ldg(reinterpret_cast<const uint4 *>(src) + i) : make_uint4(0, 0, 0, 0);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        x[8 * i + 2 * k] = __uint_as_float(w[k] << 16);
-        x[8 * i + 2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-      }
-    }
-  }
-
   float *buf = &s_buf[warp][v * Wg::VEC];
-  if (p.signs != nullptr) {
-    // H (x * d1): exact sign flip, then stages h = 1 .. E/2 inside the lane's row
+
+  // x * d1 with d1 = +-1 is an exact sign flip: XOR the bf16 sign bits of the lane's words
+  uint32_t sgn[NW];
+#pragma unroll
+  for (int i = 0; i < NW; ++i) sgn[i] = 0;
+  if constexpr (ROT) {
     const float4 *sg = reinterpret_cast<const float4 *>(p.signs + l8 * E);
 #pragma unroll
     for (int i = 0; i < E / 4; ++i) {
-      const float4 s = __ldg(sg + i);
-      x[4 * i] *= s.x;
-      x[4 * i + 1] *= s.y;
-      x[4 * i + 2] *= s.z;
-      x[4 * i + 3] *= s.w;
+      const float4 sv = __ldg(sg + i);
+      sgn[2 * i] = ((__float_as_uint(sv.x) >> 16) & 0x8000u) | (__float_as_uint(sv.y) & 0x80000000u);
+      sgn[2 * i + 1] = ((__float_as_uint(sv.z) >> 16) & 0x8000u) | (__float_as_uint(sv.w) & 0x80000000u);
     }
-    butterfly_local<E>(x);
-    // stages h = E, 2E, 4E pair rows r and r ^ 1, 2, 4: transpose, butterfly over rows, back
+  }
+
+  WriteUnit<D> cur;
+  long long tile = blockIdx.x;
+  if (tile < tiles) load_unit<D>(p, tile, warp, v, l8, cur);
+  for (; tile < tiles; tile += gridDim.x) {
+    WriteUnit<D> nxt;
+    const long long nt = tile + gridDim.x;
+    if (nt < tiles) load_unit<D>(p, nt, warp, v, l8, nxt);
+
+    bool valid = cur.in_range;
+    if (valid && cur.slot >= p.num_blocks * p.block_size) {
+      if (l8 == 0 && !is_v) atomicOr(&g_flags_write, ERR_SLOT);
+      valid = false;
+    }
+    valid = valid && cur.slot >= 0;  // padding tokens store nothing
+
+    uint32_t wb[NW];  // the vector as bf16 pairs after the rotation and its bf16 cast
+    if constexpr (ROT) {
+      float x[E];
 #pragma unroll
-    for (int i = 0; i < E / 4; ++i)
-      *reinterpret_cast<float4 *>(buf + l8 * Wg::ROW + 4 * i) = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
-    __syncwarp();
-    float c[CPL][8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      if constexpr (CPL == 2) {
-        const float2 f = *reinterpret_cast<const float2 *>(buf + r * Wg::ROW + 2 * l8);
-        c[0][r] = f.x;
-        c[1][r] = f.y;
-      } else {
-        c[0][r] = buf[r * Wg::ROW + l8];
+      for (int i = 0; i < NW; ++i) {
+        const uint32_t w = cur.w[i] ^ sgn[i];
+        x[2 * i] = __uint_as_float(w << 16);
+        x[2 * i + 1] = __uint_as_float(w & 0xffff0000u);
       }
+      butterfly_local<E>(x);  // h = 1 .. E/2 inside the lane's row
+      // stages h = E, 2E, 4E pair rows r and r ^ 1, 2, 4: transpose, butterfly over rows, back
+      __syncwarp();  // the previous tile's reads of buf are done
+#pragma unroll
+      for (int i = 0; i < E / 4; ++i)
+        *reinterpret_cast<float4 *>(buf + l8 * Wg::ROW + 4 * i) = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+      __syncwarp();
+      float c[CPL][8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if constexpr (CPL == 2) {
+          const float2 f = *reinterpret_cast<const float2 *>(buf + r * Wg::ROW + 2 * l8);
+          c[0][r] = f.x;
+          c[1][r] = f.y;
+        } else {
+          c[0][r] = buf[r * Wg::ROW + l8];
+        }
+      }
+#pragma unroll
+      for (int cc = 0; cc < CPL; ++cc) butterfly_local<8>(c[cc]);
+      __syncwarp();
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if constexpr (CPL == 2)
+          *reinterpret_cast<float2 *>(buf + r * Wg::ROW + 2 * l8) = make_float2(c[0][r], c[1][r]);
+        else
+          buf[r * Wg::ROW + l8] = c[0][r];
+      }
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < E / 4; ++i) {
+        const float4 f = *reinterpret_cast<const float4 *>(buf + l8 * Wg::ROW + 4 * i);
+        wb[2 * i] = bf2_bits(f.x, f.y);
+        wb[2 * i + 1] = bf2_bits(f.z, f.w);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < NW; ++i) wb[i] = cur.w[i];
     }
+
+    // min / max over the vector: bf16 pairs in the lane (exact), then fp32 across the 8 lanes
+    __nv_bfloat162 mn2 = as_bf2(wb[0]), mx2 = mn2;
 #pragma unroll
-    for (int cc = 0; cc < CPL; ++cc) butterfly_local<8>(c[cc]);
-    __syncwarp();
+    for (int i = 1; i < NW; ++i) {
+      mn2 = __hmin2(mn2, as_bf2(wb[i]));
+      mx2 = __hmax2(mx2, as_bf2(wb[i]));
+    }
+    float mn = fminf(__low2float(mn2), __high2float(mn2));
+    float mx = fmaxf(__low2float(mx2), __high2float(mx2));
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      if constexpr (CPL == 2)
-        *reinterpret_cast<float2 *>(buf + r * Wg::ROW + 2 * l8) = make_float2(c[0][r], c[1][r]);
+    for (int m = 1; m < 8; m <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(FULL, mn, m));
+      mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, m));
+    }
+    const float scale = fmaxf(__fdiv_rn(__fsub_rn(mx, mn), 15.0f), 1e-6f);
+    const uint32_t zpi = code_bits(__fdiv_rn(-mn, scale)) & 0xFu;
+    const float zp = static_cast<float>(zpi);
+    const float inv = __fdiv_rn(1.0f, scale);
+
+    uint32_t packed[E / 8];
+#pragma unroll
+    for (int i = 0; i < E / 8; ++i) {
+      uint32_t c[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t w = wb[4 * i + k];
+        c[2 * k] = code_bits(__fadd_rn(__fmul_rn(__uint_as_float(w << 16), inv), zp));
+        c[2 * k + 1] = code_bits(__fadd_rn(__fmul_rn(__uint_as_float(w & 0xffff0000u), inv), zp));
+      }
+      packed[i] = pack_codes(c);
+    }
+    if (valid) {
+      // [num_blocks][block_size][Hk] flattened: (slot / bs * bs + slot % bs) * Hk + h
+      const long long row = cur.slot * p.Hk + cur.h;
+      uint8_t *dst = (is_v ? p.v_cache : p.k_cache) + row * (D / 2) + l8 * (E / 2);
+      if constexpr (E == 16)
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
       else
-        buf[r * Wg::ROW + l8] = c[0][r];
+        *reinterpret_cast<uint32_t *>(dst) = packed[0];
+      if (l8 == 0) (is_v ? p.v_scale : p.k_scale)[row] = (__float_as_uint(scale) & 0xFFFFFFF0u) | zpi;
     }
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < E / 4; ++i) {
-      const float4 f = *reinterpret_cast<const float4 *>(buf + l8 * Wg::ROW + 4 * i);
-      x[4 * i] = bf16_round(f.x);
-      x[4 * i + 1] = bf16_round(f.y);
-      x[4 * i + 2] = bf16_round(f.z);
-      x[4 * i + 3] = bf16_round(f.w);
-    }
+    if (nt < tiles) cur = nxt;
   }
+}
 
-  float mn = x[0], mx = x[0];
-#pragma unroll
-  for (int j = 1; j < E; ++j) {
-    mn = fminf(mn, x[j]);
-    mx = fmaxf(mx, x[j]);
+template <int D, bool ROT>
+unsigned write_grid(long long tiles) {
+  static int per_sm = 0;  // resident CTAs per SM, from the occupancy calculator
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, write_int4_kernel<D, ROT>, 256, 0) != cudaSuccess || n < 1)
+      n = 1;
+    per_sm = n;
   }
-#pragma unroll
-  for (int m = 1; m < 8; m <<= 1) {
-    mn = fminf(mn, __shfl_xor_sync(FULL, mn, m));
-    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, m));
-  }
-  const float scale = fmaxf(__fdiv_rn(__fsub_rn(mx, mn), 15.0f), 1e-6f);
-  const uint32_t zpi = nibble_of(__fdiv_rn(-mn, scale));
-  const float zp = static_cast<float>(zpi);
-  const float inv = __fdiv_rn(1.0f, scale);
-
-  uint32_t packed[E / 8];
-#pragma unroll
-  for (int i = 0; i < E / 8; ++i) {
-    uint32_t wd = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) wd |= nibble_of(__fadd_rn(__fmul_rn(x[8 * i + k], inv), zp)) << (4 * k);
-    packed[i] = wd;
-  }
-  if (!valid) return;
-  const long long row = ((slot / p.block_size) * p.block_size + slot % p.block_size) * p.Hk + h;
-  uint8_t *dst = (is_v ? p.v_cache : p.k_cache) + row * (D / 2) + l8 * (E / 2);
-  if constexpr (E == 16)
-    *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
-  else
-    *reinterpret_cast<uint32_t *>(dst) = packed[0];
-  if (l8 == 0) (is_v ? p.v_scale : p.k_scale)[row] = (__float_as_uint(scale) & 0xFFFFFFF0u) | zpi;
+  const long long cap = static_cast<long long>(sm_count() > 0 ? sm_count() : 1) * per_sm;
+  return static_cast<unsigned>(tiles < cap ? tiles : cap);
 }
 
 bool take_flags_write(cudaStream_t stream, unsigned *host_word) {
@@ -221,11 +307,27 @@ extern "C" kvq_status kvq_write_int4(const void *key, const void *value, int64_t
   p.num_blocks = num_blocks;
 
   const long long pairs = static_cast<long long>(T) * Hk;
-  const unsigned grid = static_cast<unsigned>((pairs + 15) / 16);
+  if (pairs >= (1LL << 31)) return KVQ_ERR_UNSUPPORTED;
+  p.pairs = static_cast<uint32_t>(pairs);
+  // division by the invariant Hk (Granlund and Montgomery, "Division by invariant integers using
+  // multiplication", round-up variant): l = ceil(log2 Hk), m = floor(2^32 (2^l - Hk) / Hk) + 1;
+  // exact for every pair < 2^31, where umulhi(pair, m) + pair stays below 2^32
+  uint32_t l = 0;
+  while ((1LL << l) < Hk) ++l;
+  p.hk_shift = l;
+  p.hk_magic = static_cast<uint32_t>((((1ULL << 32) * ((1ULL << l) - static_cast<uint64_t>(Hk))) / Hk) + 1);
+  const long long tiles = (pairs + 15) / 16;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (D == 128)
-    write_int4_kernel<128><<<grid, 256, 0, s>>>(p);
-  else
-    write_int4_kernel<64><<<grid, 256, 0, s>>>(p);
+  if (D == 128) {
+    if (rht_signs)
+      write_int4_kernel<128, true><<<write_grid<128, true>(tiles), 256, 0, s>>>(p, tiles);
+    else
+      write_int4_kernel<128, false><<<write_grid<128, false>(tiles), 256, 0, s>>>(p, tiles);
+  } else {
+    if (rht_signs)
+      write_int4_kernel<64, true><<<write_grid<64, true>(tiles), 256, 0, s>>>(p, tiles);
+    else
+      write_int4_kernel<64, false><<<write_grid<64, false>(tiles), 256, 0, s>>>(p, tiles);
+  }
   return launch_status();
 }

@@ -79,3 +79,18 @@ def test_empty_and_all_skipped():
     e = torch.empty((0, 2, 64), dtype=torch.bfloat16, device="cuda")
     kvq.kvq_write_int4(e, e, kc, kc, sc, sc, torch.empty((0,), dtype=torch.int64, device="cuda"))
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("Hk,D,T", [(1, 64, 777), (3, 128, 777), (5, 64, 1001), (12, 128, 2049)])
+def test_head_counts_and_ragged_tiles(Hk, D, T):
+    """Head counts that are not powers of two (the kernel splits a pair index into token and head
+    by a multiply-shift) and pair counts that leave a ragged last tile of 16 pairs."""
+    k, v, slots, nb = workloads.write_case(T=T, Hk=Hk, D=D, hole_frac=0.1, seed=Hk)
+    _write_both(k, v, slots, nb, Hk, D, workloads.rht_signs(D))
+
+
+def test_many_tiles_per_cta():
+    """More 16-pair tiles than resident CTAs: every CTA walks several tiles with the next one's
+    rows fetched ahead (65536 tokens x 3 heads = 12288 tiles)."""
+    k, v, slots, nb = workloads.write_case(T=65536, Hk=3, D=64, hole_frac=0.02, seed=11)
+    _write_both(k, v, slots, nb, 3, 64, None)

@@ -2,10 +2,11 @@
 
 int4_per_token_head.py, _reshape_cache_int4_kernel rounds half away from zero (where(u >= 0,
 int(u + 0.5), int(u - 0.5)) in fp32) and clamps to [0, 15]. The kernel instead computes
-trunc(clamp(fl(u + 0.5), 0, 15.5)), taking the truncation as the low bits of the fp32 sum
-value + 2^23 under round-toward-zero. These tests run that formula in numpy over every fp32 u in
-[0.25, 17) (where the rounding of u + 0.5 and the clamp matter), random values elsewhere and the
-special values, against oracle.int4_cache.round_half_away."""
+w = saturate(fma(u, 2^-4, 2^-5)) -- fl(u + 0.5) / 16, since the product is exact and the fused
+add rounds once -- then adds 2^19 under round-toward-zero (the ulp at 2^19 is 2^-4, so the low
+bits hold trunc(16 w)) and takes an integer min with 15. These tests run that formula in numpy over
+every fp32 u in [0.25, 17) (where the rounding of u + 0.5 and the clamp matter), random values
+elsewhere and the special values, against oracle.int4_cache.round_half_away."""
 
 import numpy as np
 
@@ -16,14 +17,14 @@ F32 = np.float32
 
 def _kernel_formula(u):
     u = np.asarray(u, dtype=F32)
-    with np.errstate(invalid="ignore"):
-        w = (u + F32(0.5)).astype(F32)                      # fl(u + 0.5), round to nearest
-        w = np.where(np.isnan(w), F32(0.0), np.maximum(w, F32(0.0)))  # fmaxf(NaN, 0) = 0
-        w = np.minimum(w, F32(15.5)).astype(F32)
-    # w + 2^23 with round-toward-zero: exact in float64, then truncated to the fp32 grid (ulp 1)
-    s = np.floor(w.astype(np.float64) + 8388608.0)
-    bits = s.astype(F32).view(np.uint32)
-    return (bits & np.uint32(0xF)).astype(np.int64)
+    with np.errstate(invalid="ignore", over="ignore"):
+        # fma(u, 1/16, 1/32): the exact value rounded once to fp32 (float64 holds u/16 + 1/32 exactly
+        # wherever the result is not simply 1/32)
+        w = (u.astype(np.float64) * 0.0625 + 0.03125).astype(F32)
+        w = np.where(np.isnan(w), F32(0.0), np.clip(w, F32(0.0), F32(1.0)))  # .sat: NaN -> 0
+    # w + 2^19 with round-toward-zero lands on the grid of step 2^-4: the field above 2^19 is trunc(16 w)
+    field = np.floor((w.astype(np.float64) + 524288.0) * 16.0) - 8388608.0
+    return np.minimum(field, 15.0).astype(np.int64)
 
 
 def _oracle(u):
