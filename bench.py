@@ -282,7 +282,8 @@ def run_kvq(args, dist):
                   % (nrep, kv_bytes / 1e6)) if nrep > 1 else "single %.0f MB cache read per step (> L2)" % (kv_bytes / 1e6),
            "decode_bytes_per_step": dec_bytes, "kv_cache_bytes_per_step": kv_bytes, "write_bytes_per_step": wr_bytes}
     kernels = 3  # write, split-KV decode, merge
-    return finish(args, dist, res, dec_bytes, cfg, e2e, kernels, "decode_int4",
+    tag = "decode_int4" if wl == "llama3_8b_int4" else "decode_int4_long_context"
+    return finish(args, dist, res, dec_bytes, cfg, e2e, kernels, tag,
                   ["quantized_paged_kv_int4_gb300/csrc/decode_int4.cu",
                    "quantized_paged_kv_int4_gb300/csrc/decode_common.cuh",
                    "quantized_paged_kv_int4_gb300/csrc/kvq_device.cuh"], "f32")

@@ -54,7 +54,10 @@ __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two_bytes) {
   return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
 }
 
-template <int D, int VBITS, int NSTAGE>
+// PACKQ (G <= 4): the q hi parts of the G heads fill MMA columns 0..3 and the lo parts columns
+// 4..7, so one MMA per k-step yields both halves of every score (added across lanes t, t ^ 2);
+// otherwise hi and lo take one MMA each.
+template <int D, int VBITS, int NSTAGE, bool PACKQ>
 __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8_t *qarea, int b,
                                          int h, int sub, int t0, int t1, long long slot) {
   using Gm = TqGeom<D, VBITS>;
@@ -83,15 +86,21 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
 #pragma unroll
       for (int j = 0; j < J; ++j) {
         const int e = lane + 32 * j;
-        const float x = n < G ? qb[n * D + e] : 0.f;
+        const int head = PACKQ ? (n & 3) : n;
+        const float x = head < G ? qb[head * D + e] : 0.f;
         const __half hi = __float2half_rn(x);
-        qh[n * D + e] = hi;
-        qh[8 * D + n * D + e] = __float2half_rn(x - __half2float(hi));
+        const __half lo = __float2half_rn(x - __half2float(hi));
+        if constexpr (PACKQ) {
+          qh[n * D + e] = n < 4 ? hi : lo;
+        } else {
+          qh[n * D + e] = hi;
+          qh[8 * D + n * D + e] = lo;
+        }
       }
     }
   }
   __syncwarp();
-  uint32_t qhi[Gm::KSTEPS][2], qlo[Gm::KSTEPS][2];
+  uint32_t qhi[Gm::KSTEPS][2], qlo[PACKQ ? 1 : Gm::KSTEPS][2];
   {
     const __half *qh = reinterpret_cast<const __half *>(qarea) + g * D + t * Gm::KCH;
 #pragma unroll
@@ -99,8 +108,10 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
       const __half *r = qh + 4 * ks;
       qhi[ks][0] = h2_as_u32(__halves2half2(r[0], r[1]));
       qhi[ks][1] = h2_as_u32(__halves2half2(r[2], r[3]));
-      qlo[ks][0] = h2_as_u32(__halves2half2(r[8 * D + 0], r[8 * D + 1]));
-      qlo[ks][1] = h2_as_u32(__halves2half2(r[8 * D + 2], r[8 * D + 3]));
+      if constexpr (!PACKQ) {
+        qlo[ks][0] = h2_as_u32(__halves2half2(r[8 * D + 0], r[8 * D + 1]));
+        qlo[ks][1] = h2_as_u32(__halves2half2(r[8 * D + 2], r[8 * D + 3]));
+      }
     }
   }
   __syncwarp();
@@ -178,9 +189,17 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
         const int ks = 4 * ch + i;
         const uint32_t a0 = e4m3x2_to_h2(wa[i] & 0xffffu), a2 = e4m3x2_to_h2(wa[i] >> 16);
         const uint32_t a1 = e4m3x2_to_h2(wb[i] & 0xffffu), a3 = e4m3x2_to_h2(wb[i] >> 16);
-        mma_f16_16816(c, a0, a1, a2, a3, qhi[ks][0], qhi[ks][1]);
-        mma_f16_16816(c, a0, a1, a2, a3, qlo[ks][0], qlo[ks][1]);
+        if constexpr (PACKQ) {
+          mma_f16_16816(c, a0, a1, a2, a3, qhi[ks][0], qhi[ks][1]);
+        } else {
+          mma_f16_16816(c, a0, a1, a2, a3, qhi[ks][0], qhi[ks][1]);
+          mma_f16_16816(c, a0, a1, a2, a3, qlo[ks][0], qlo[ks][1]);
+        }
       }
+    }
+    if constexpr (PACKQ) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[i] += __shfl_xor_sync(FULL, c[i], 2);  // hi (t < 2) + lo (t >= 2)
     }
     const uint8_t *sb = st + Gm::KB + Gm::VB;
     const uint32_t sz0 = lds32(sb + g * 4), sz1 = lds32(sb + (g + 8) * 4);
@@ -296,7 +315,7 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
   store_partial<D>(p.s, slot, sub, h, lane, o0, o1, lse0, lse1);
 }
 
-template <int D, int VBITS, int NSTAGE>
+template <int D, int VBITS, int NSTAGE, bool PACKQ>
 __global__ void __launch_bounds__(256, 2) decode_tq_kernel(const TqParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   asm volatile("griddepcontrol.launch_dependents;");  // let the merge kernel's launch begin early
@@ -308,7 +327,7 @@ __global__ void __launch_bounds__(256, 2) decode_tq_kernel(const TqParams p) {
   const int sub = warp / p.s.heads_per_cta;
   const int h = blockIdx.y * p.s.heads_per_cta + hl;
   for_each_piece(p.s, &g_flags_decode_tq, [&](int b, int t0, int t1, long long slot) {
-    tq_piece<D, VBITS, NSTAGE>(p, ring, qarea, b, h, sub, t0, t1, slot);
+    tq_piece<D, VBITS, NSTAGE, PACKQ>(p, ring, qarea, b, h, sub, t0, t1, slot);
   });
 }
 
@@ -323,20 +342,20 @@ bool take_flags_decode_tq(cudaStream_t stream, unsigned *host_word) {
                                  cudaMemcpyHostToDevice, stream) == cudaSuccess;
 }
 
-template <int D, int VBITS>
+template <int D, int VBITS, bool PACKQ>
 static kvq_status launch_tq(const TqParams &p, const SplitPlan &plan, cudaStream_t s) {
   using Gm = TqGeom<D, VBITS>;
   const size_t smem = 8 * static_cast<size_t>(kStagesTq * Gm::STAGE + Gm::QBYTES);
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(decode_tq_kernel<D, VBITS, kStagesTq>,
+    if (cudaFuncSetAttribute(decode_tq_kernel<D, VBITS, kStagesTq, PACKQ>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return KVQ_ERR_CUDA;
     attr_set = true;
   }
   const dim3 grid(plan.seg_ctas, plan.head_groups);
-  decode_tq_kernel<D, VBITS, kStagesTq><<<grid, 256, smem, s>>>(p);
+  decode_tq_kernel<D, VBITS, kStagesTq, PACKQ><<<grid, 256, smem, s>>>(p);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   const long long rows = static_cast<long long>(p.s.B) * p.s.Hq;
   if (launch_dependent(merge_kernel<D>, dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), s, p.s) != cudaSuccess)
@@ -396,6 +415,13 @@ extern "C" kvq_status kvq_decode_tq(const float *q, const uint8_t *kv_cache, int
   p.sc_log2 = static_cast<float>(static_cast<double>(attn_scale) * 1.4426950408889634);
   p.num_blocks = num_blocks;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (D == 128) return value_bits == 4 ? launch_tq<128, 4>(p, plan, s) : launch_tq<128, 3>(p, plan, s);
-  return value_bits == 4 ? launch_tq<64, 4>(p, plan, s) : launch_tq<64, 3>(p, plan, s);
+  // packed q columns: faster for 3-bit values (127 vs 131 us on the 64 x 4096 workload), slower
+  // for 4-bit ones (131 vs 126 us), measured on GB300
+  const bool packq = sa.G <= 4 && value_bits == 3;
+  if (D == 128) {
+    if (value_bits == 4) return packq ? launch_tq<128, 4, true>(p, plan, s) : launch_tq<128, 4, false>(p, plan, s);
+    return packq ? launch_tq<128, 3, true>(p, plan, s) : launch_tq<128, 3, false>(p, plan, s);
+  }
+  if (value_bits == 4) return packq ? launch_tq<64, 4, true>(p, plan, s) : launch_tq<64, 4, false>(p, plan, s);
+  return packq ? launch_tq<64, 3, true>(p, plan, s) : launch_tq<64, 3, false>(p, plan, s);
 }
