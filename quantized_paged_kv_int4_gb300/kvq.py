@@ -61,6 +61,9 @@ def library_path():
 def lib():
     """The loaded libkvq (built in-tree on first use if it is missing or stale)."""
     global _handle
+    h = _handle
+    if h is not None:
+        return h
     with _lock:
         if _handle is None:
             path = _build.build()
@@ -87,12 +90,11 @@ def _check(status, where):
 
 
 def _ptr(t):
-    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+    return t.data_ptr() if t is not None else None
 
 
 def _stream(stream):
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    return (torch.cuda.current_stream() if stream is None else stream).cuda_stream
 
 
 def _need(t, name, dtype=None, contiguous=True):
@@ -143,8 +145,10 @@ def decode_workspace(B, Hq, Hk, D, num_splits=0, device=None):
     return torch.empty((need,), dtype=torch.uint8, device=device)
 
 
-def _workspace(workspace, need, device):
+def _workspace(workspace, B, Hq, Hk, D, num_splits, device):
+    """The caller's workspace (its size is checked by the library), or a new one of the needed size."""
     if workspace is None:
+        need = kvq_decode_workspace_bytes(B, Hq, Hk, D, num_splits)
         return torch.empty((max(need, 16),), dtype=torch.uint8, device=device)
     _need(workspace, "workspace", torch.uint8)
     return workspace
@@ -167,8 +171,7 @@ def kvq_decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens
     if out is None:
         out = torch.empty((B, Hq, D), dtype=out_dtype or torch.float32, device=q.device)
     _need(out, "out")
-    need = kvq_decode_workspace_bytes(B, Hq, Hk, D, num_splits)
-    workspace = _workspace(workspace, need, q.device)
+    workspace = _workspace(workspace, B, Hq, Hk, D, num_splits, q.device)
     _check(lib().kvq_decode_int4(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                                  _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(rht_signs),
                                  float(softmax_scale), num_splits, _ptr(workspace), workspace.numel(),
@@ -214,8 +217,7 @@ def kvq_decode_tq(q, kv_cache, value_bits, block_table, seq_lens, attn_scale, ou
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
     _need(out, "out", torch.float32)
-    need = kvq_decode_workspace_bytes(B, Hq, Hk, D, num_splits)
-    workspace = _workspace(workspace, need, q.device)
+    workspace = _workspace(workspace, B, Hq, Hk, D, num_splits, q.device)
     _check(lib().kvq_decode_tq(_ptr(q), _ptr(kv_cache), slot_bytes, value_bits, _ptr(block_table),
                                block_table.shape[1], _ptr(seq_lens), float(attn_scale), num_splits,
                                _ptr(workspace), workspace.numel(), _ptr(out), B, Hq, Hk, D, bs, nb,
