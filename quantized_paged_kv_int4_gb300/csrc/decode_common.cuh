@@ -33,6 +33,7 @@ struct SplitArgs {
   int32_t num_splits;  // 0 = balanced
   int32_t B, Hq, Hk, G;
   int32_t heads_per_cta, warps_per_head;
+  int32_t seg_ctas;    // the split kernel's gridDim.x
   long long slots;     // partial slots in the workspace (before the warps_per_head factor)
   float *part_o;       // [(slots * warps_per_head), Hq, D]
   float *part_lse;     // [(slots * warps_per_head), Hq]
@@ -100,9 +101,11 @@ __device__ __forceinline__ void store_out(const SplitArgs &a, long long row, int
 // Merge the partials of (b, hq) in slots [s_lo, s_hi) and write the output row (one warp).
 // Up to 16 partial rows per round trip: their log-sum-exps and their vectors are all requested
 // before any is used, then combined online (running max M, weights 2^(lse - M)). Partials come
-// from the split kernel's CTAs: read through L2 (ld.global.cg).
+// from the split kernel's CTAs: read through L2 (ld.global.cg). sg: this lane's rotation signs
+// (used when a.signs is set).
 template <int D>
-__device__ __forceinline__ void merge_row(const SplitArgs &a, int b, int hq, long long s_lo, long long s_hi, int lane) {
+__device__ __forceinline__ void merge_row(const SplitArgs &a, int b, int hq, long long s_lo, long long s_hi, int lane,
+                                          const float (&sg)[D / 32]) {
   constexpr int V = D / 32, R = 16;
   const int W = a.warps_per_head;
   const long long n = (s_hi - s_lo) * W, r0 = s_lo * W;  // rows (s * W + w) are contiguous
@@ -164,7 +167,7 @@ __device__ __forceinline__ void merge_row(const SplitArgs &a, int b, int hq, lon
       for (int j = 0; j < V; ++j) o[j] = butterfly_xor(o[j], lane, mask);
     }
 #pragma unroll
-    for (int j = 0; j < V; ++j) o[j] *= __ldg(a.signs + lane * V + j) * (1.0f / D);
+    for (int j = 0; j < V; ++j) o[j] *= sg[j] * (1.0f / D);
   }
   store_out<D>(a, static_cast<long long>(b) * a.Hq + hq, lane, o);
 }
@@ -256,17 +259,55 @@ __device__ __forceinline__ void store_partial(const SplitArgs &a, long long slot
   }
 }
 
+// The CTA of the balanced split that holds page X of the concatenated pages: runs are
+// [c q + min(c, r), ...) with q = P_tot / C, r = P_tot % C (the first r runs one page longer).
+__device__ __forceinline__ long long run_of_page(long long X, long long q, long long r) {
+  return X < r * (q + 1) ? X / (q + 1) : r + (X - r * (q + 1)) / q;
+}
+
 // One warp per output row (b, hq). Launched as a programmatic dependent of the split kernel:
-// griddepcontrol.wait holds it until that grid has finished and its writes are visible.
+// everything that does not depend on its results -- lengths, slot ranges (recomputed from the
+// partition for B <= 256, else read from seg_first / seg_last), the rotation signs -- is done
+// before griddepcontrol.wait, which holds the kernel until that grid has finished and its writes
+// are visible; after it, one round trip for the partials.
 template <int D>
 __global__ void __launch_bounds__(256) merge_kernel(const SplitArgs a) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int V = D / 32;
+  __shared__ long long s_scan[8];
+  __shared__ long long s_first_page[256];
   const int lane = threadIdx.x & 31;
   const long long idx = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (idx >= static_cast<long long>(a.B) * a.Hq) return;
-  const int b = static_cast<int>(idx / a.Hq), hq = static_cast<int>(idx % a.Hq);
-  const int L = clamped_len(a, b, nullptr);  // the split kernel already flagged it
+  const bool live = idx < static_cast<long long>(a.B) * a.Hq;
+  const int b = live ? static_cast<int>(idx / a.Hq) : 0, hq = live ? static_cast<int>(idx % a.Hq) : 0;
+  const bool scan = a.num_splits == 0 && a.B <= 256;  // uniform over the grid
+  long long P_tot = 0;
+  if (scan) {
+    const int t = threadIdx.x;
+    const long long np = t < a.B ? (clamped_len(a, t, nullptr) + kPage - 1) / kPage : 0;
+    const long long incl = block_scan_256(np, s_scan, &P_tot);
+    s_first_page[t] = incl - np;
+    __syncthreads();
+  }
+  float sg[V];
+#pragma unroll
+  for (int j = 0; j < V; ++j) sg[j] = a.signs != nullptr ? __ldg(a.signs + lane * V + j) : 0.f;
+  const int L = live ? clamped_len(a, b, nullptr) : 0;  // the split kernel already flagged it
+  long long s_lo = 0, s_hi = 0;                           // slot range [s_lo, s_hi)
+  bool ranged = false;
+  if (L > 0 && a.num_splits > 0) {
+    const int span = (L + a.num_splits - 1) / a.num_splits;
+    s_lo = static_cast<long long>(b) * a.num_splits;
+    s_hi = s_lo + (L + span - 1) / span;
+    ranged = true;
+  } else if (L > 0 && scan) {
+    const long long C = a.seg_ctas, q = P_tot / C, r = P_tot % C;
+    const long long P0 = s_first_page[b], np = (L + kPage - 1) / kPage;
+    s_lo = run_of_page(P0, q, r) + b;
+    s_hi = run_of_page(P0 + np - 1, q, r) + b + 1;
+    ranged = true;
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (!live) return;
   if (L == 0) {
     float z[V];
 #pragma unroll
@@ -274,18 +315,13 @@ __global__ void __launch_bounds__(256) merge_kernel(const SplitArgs a) {
     store_out<D>(a, idx, lane, z);
     return;
   }
-  long long s_lo, s_hi;  // slot range [s_lo, s_hi)
-  if (a.num_splits > 0) {
-    const int span = (L + a.num_splits - 1) / a.num_splits;
-    s_lo = static_cast<long long>(b) * a.num_splits;
-    s_hi = s_lo + (L + span - 1) / span;
-  } else {
+  if (!ranged) {
     s_lo = static_cast<long long>(a.seg_first[b]) + b;
     s_hi = static_cast<long long>(a.seg_last[b]) + b + 1;
   }
   s_lo = max(0LL, min(s_lo, a.slots));  // never index outside the workspace
   s_hi = max(s_lo, min(s_hi, a.slots));
-  merge_row<D>(a, b, hq, s_lo, s_hi, lane);
+  merge_row<D>(a, b, hq, s_lo, s_hi, lane, sg);
 }
 
 }  // namespace kvq

@@ -848,6 +848,7 @@ extern "C" kvq_status kvq_decode_int4(const void *q, const uint8_t *k_cache, con
   sa.G = Hq / Hk;
   sa.heads_per_cta = plan.heads_per_cta;
   sa.warps_per_head = plan.warps_per_head;
+  sa.seg_ctas = plan.seg_ctas;
   sa.slots = plan.slots;
   workspace_carve(workspace, B, Hq, D, plan, &sa.part_o, &sa.part_lse, &sa.seg_first, &sa.seg_last);
   sa.signs = rht_signs;
