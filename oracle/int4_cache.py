@@ -140,10 +140,24 @@ def gather_rows(pool, bt_row, L):
     return pool[np.asarray(bt_row, dtype=np.int64)[n // bs], n % bs]
 
 
-def _head_attention(q_rows, K, V, sm):
-    """float64 softmax(sm * q.k) v for q_rows [G, D], K/V [L, D]; returns ([G, D], lse [G])."""
+def _head_attention(q_rows, K, V, sm, pos=None, qpos=None, softcap=0.0, slopes=None, keep=None):
+    """float64 softmax(S) v for q_rows [G, D], K/V [n, D]; returns ([G, D], lse [G]).
+
+    S = sm * q.k, then, in the order of unified_attention_int4's tile loop: the soft cap
+    S = softcap * tanh(S / softcap) when softcap > 0 (USE_SOFTCAP), the key mask (keep), and the
+    ALiBi bias S += slope_g * (pos - qpos) (USE_ALIBI_SLOPES; pos = key positions, qpos = the
+    query's position). A fully masked range returns o = 0, lse = -inf.
+    """
     s = sm * (q_rows[:, None, :] * K[None, :, :]).sum(axis=-1)
+    if softcap > 0:
+        s = softcap * np.tanh(s / softcap)
+    if keep is not None:
+        s = np.where(keep[None, :], s, -np.inf)
+    if slopes is not None:
+        s = s + np.asarray(slopes, np.float64)[:, None] * (np.asarray(pos, np.float64) - qpos)[None, :]
     m = s.max(axis=1, keepdims=True)
+    if not np.all(np.isfinite(m)):
+        return np.zeros((q_rows.shape[0], V.shape[1])), np.full(q_rows.shape[0], -np.inf)
     e = np.exp(s - m)
     l = e.sum(axis=1, keepdims=True)
     o = (e[:, :, None] * V[None, :, :]).sum(axis=1) / l
@@ -151,16 +165,24 @@ def _head_attention(q_rows, K, V, sm):
 
 
 def decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
-                signs, softmax_scale, num_splits=None, batch_index=None):
+                signs, softmax_scale, num_splits=None, batch_index=None,
+                window=0, softcap=0.0, sinks=None, alibi_slopes=None):
     """Paged decode attention over the INT4 cache (unified_attention_int4 semantics).
 
     q: [B, Hq, D] float32 holding bf16 values. Returns float64 [B, Hq, D] (rows of
-    empty sequences are zero). With num_splits=S the keys of each sequence are cut
-    into S ranges of ceil(L / S) positions (triton_turboquant_decode.py,
+    empty sequences are zero). With num_splits=S the kept keys of each sequence are cut
+    into S ranges of ceil(n / S) positions (triton_turboquant_decode.py,
     _tq_decode_stage1 split range), each range is attended separately and the
     partial results are combined by the log-sum-exp merge (lse_merge); without it
     one softmax covers the whole sequence. batch_index restricts the work to some
     sequences (other rows are left zero).
+
+    Score modifiers (unified_attention_int4 flags; the query is the token at position L - 1):
+      window > 0      SLIDING_WINDOW: keys at positions n with (L - 1) - n < window are kept;
+      softcap > 0     USE_SOFTCAP: S = softcap * tanh(S / softcap) on the scaled score;
+      alibi_slopes    USE_ALIBI_SLOPES: [Hq] slopes, S += slope * (n - (L - 1));
+      sinks           USE_SINKS: [Hq] logits that join each head's softmax denominator with no
+                      value (the softmax state starts at M = sink, L = 1).
     """
     q = np.asarray(q, dtype=np.float32)
     B, Hq, D = q.shape
@@ -174,21 +196,29 @@ def decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
         L = int(seq_lens[b])
         if L == 0:
             continue
+        lo = max(0, L - window) if window > 0 else 0   # first kept key
         K = dequant_int4(gather_rows(k_cache, block_table[b], L), gather_rows(k_scale, block_table[b], L))
         V = dequant_int4(gather_rows(v_cache, block_table[b], L), gather_rows(v_scale, block_table[b], L))
+        pos = np.arange(L)
+        keep = pos >= lo
         for h in range(Hk):
             qg = q_rot[b, h * G:(h + 1) * G]
+            sl = None if alibi_slopes is None else np.asarray(alibi_slopes, np.float64)[h * G:(h + 1) * G]
+            kw = dict(qpos=L - 1, softcap=softcap, slopes=sl)
             if num_splits is None:
-                o, _ = _head_attention(qg, K[:, h], V[:, h], sm)
+                o, lse = _head_attention(qg, K[:, h], V[:, h], sm, pos=pos, keep=keep, **kw)
+                parts = [(o, lse)]
             else:
                 parts = []
-                span = -(-L // num_splits)
+                span = -(-(L - lo) // num_splits)
                 for s in range(num_splits):
-                    lo, hi = s * span, min((s + 1) * span, L)
-                    if lo >= hi:
+                    a, e = lo + s * span, min(lo + (s + 1) * span, L)
+                    if a >= e:
                         continue
-                    parts.append(_head_attention(qg, K[lo:hi, h], V[lo:hi, h], sm))
-                o = lse_merge([p[0] for p in parts], [p[1] for p in parts])
+                    parts.append(_head_attention(qg, K[a:e, h], V[a:e, h], sm, pos=pos[a:e], **kw))
+            if sinks is not None:
+                parts.append((np.zeros((G, D)), np.asarray(sinks, np.float64)[h * G:(h + 1) * G]))
+            o = parts[0][0] if len(parts) == 1 else lse_merge([p[0] for p in parts], [p[1] for p in parts])
             if signs is not None:
                 o = rht_inverse_f64(o, signs) / D
             out[b, h * G:(h + 1) * G] = o
