@@ -135,6 +135,41 @@ KVQ_API kvq_status kvq_decode_int4(const void *q, const uint8_t *k_cache, const 
                            kvq_stream_t stream);
 
 /*
+ * kvq_score_mods / kvq_decode_int4_mods -- kvq_decode_int4 with the score modifiers of
+ * unified_attention_int4 (int4_per_token_head.py): SLIDING_WINDOW, USE_SOFTCAP, USE_ALIBI_SLOPES
+ * and USE_SINKS, in the tile loop's order. With L = seq_lens[b] and the query at position L - 1:
+ *   S_n = sm * q_rot . k_n                                  (as kvq_decode_int4)
+ *   S_n = softcap * tanh(S_n / softcap)                     softcap > 0
+ *   key n is read only if (L - 1) - n < sliding_window      sliding_window > 0 (0: every key)
+ *   S_n += alibi_slopes[hq] * (n - (L - 1))                 alibi_slopes != NULL
+ *   o = sum_n e^{S_n} v_n / (e^{sinks[hq]} + sum_n e^{S_n}) sinks != NULL (else without the sink)
+ * The window also limits what is read: pages that hold no key of the window are skipped.
+ *
+ *   mods                NULL: exactly kvq_decode_int4. Otherwise host memory read during the call.
+ *   mods->sliding_window  >= 0 keys (the query's own position counts).
+ *   mods->softcap         >= 0, finite (natural-log units of S, like softmax_scale).
+ *   mods->sinks           fp32 [Hq] device array (4-byte aligned) or NULL.
+ *   mods->alibi_slopes    fp32 [Hq] device array (4-byte aligned) or NULL.
+ * Invalid fields return KVQ_ERR_INVALID_ARG. Other arguments, numerics and errors: as
+ * kvq_decode_int4.
+ */
+typedef struct kvq_score_mods {
+  int32_t sliding_window;
+  float softcap;
+  const float *sinks;
+  const float *alibi_slopes;
+} kvq_score_mods;
+
+KVQ_API kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                const float *k_scale, const float *v_scale,
+                                const int32_t *block_table, int32_t max_blocks,
+                                const int32_t *seq_lens, const float *rht_signs, float softmax_scale,
+                                int32_t num_splits, void *workspace, size_t workspace_bytes,
+                                void *out, kvq_dtype out_dtype, int32_t B, int32_t Hq, int32_t Hk,
+                                int32_t D, int32_t block_size, int64_t num_blocks,
+                                const kvq_score_mods *mods, kvq_stream_t stream);
+
+/*
  * kvq_decode_int4_noalloc -- kvq_decode_int4 for callers that must not allocate device memory.
  * The pages have no counterpart of this call; it exists for users of this library, not for the
  * method.

@@ -40,6 +40,8 @@ struct SplitArgs {
   int32_t *seg_first;  // [B] first / last CTA of each sequence (balanced only)
   int32_t *seg_last;
   const float *signs;  // inverse rotation of the merged output when non-null
+  int32_t window;      // sliding window: keys at positions >= L - window (0 = all keys)
+  const float *sinks;  // [Hq] sink logits joining each head's softmax denominator, or null
   void *out;           // [B, Hq, D] of out_dtype
   int32_t out_dtype;
 };
@@ -52,6 +54,23 @@ __device__ __forceinline__ int clamped_len(const SplitArgs &a, int b, unsigned *
     L = cap;
   }
   return L < 0 ? 0 : L;
+}
+
+// The keys of sequence b that a decode reads: positions [lo, L), lo = max(0, L - window) under a
+// sliding window (unified_attention_int4, SLIDING_WINDOW), on the sequence's pages f .. f + np - 1.
+struct SeqSpan {
+  int L, lo, f, np;
+};
+
+// WIN = false: the caller's kernel runs without a window (a.window == 0), all keys are read.
+template <bool WIN = true>
+__device__ __forceinline__ SeqSpan seq_span(const SplitArgs &a, int b, unsigned *flags) {
+  SeqSpan s;
+  s.L = clamped_len(a, b, flags);
+  s.lo = WIN && a.window > 0 && s.L > a.window ? s.L - a.window : 0;
+  s.f = s.lo / kPage;
+  s.np = s.L > 0 ? (s.L - 1) / kPage - s.f + 1 : 0;
+  return s;
 }
 
 // Block-wide inclusive scan of one int64 per thread (256 threads); returns the inclusive
@@ -102,10 +121,11 @@ __device__ __forceinline__ void store_out(const SplitArgs &a, long long row, int
 // Up to 16 partial rows per round trip: their log-sum-exps and their vectors are all requested
 // before any is used, then combined online (running max M, weights 2^(lse - M)). Partials come
 // from the split kernel's CTAs: read through L2 (ld.global.cg). sg: this lane's rotation signs
-// (used when a.signs is set).
+// (used when a.signs is set); sink2: the head's sink logit in base 2 (-inf: none), a partial with
+// lse = sink2 and a zero vector.
 template <int D>
 __device__ __forceinline__ void merge_row(const SplitArgs &a, int b, int hq, long long s_lo, long long s_hi, int lane,
-                                          const float (&sg)[D / 32]) {
+                                          const float (&sg)[D / 32], float sink2) {
   constexpr int V = D / 32, R = 16;
   const int W = a.warps_per_head;
   const long long n = (s_hi - s_lo) * W, r0 = s_lo * W;  // rows (s * W + w) are contiguous
@@ -154,6 +174,14 @@ __device__ __forceinline__ void merge_row(const SplitArgs &a, int b, int hq, lon
         for (int j = 0; j < V; ++j) o[j] = fmaf(wk, v[k][j], o[j]);
       }
     }
+  }
+  if (sink2 > -INFINITY) {  // USE_SINKS: one more term of the denominator, nothing in the sum
+    const float nM = fmaxf(M, sink2);
+    const float f = M == -INFINITY ? 0.f : exp2f(M - nM);
+#pragma unroll
+    for (int j = 0; j < V; ++j) o[j] *= f;
+    den = den * f + exp2f(sink2 - nM);
+    M = nM;
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
 #pragma unroll
@@ -283,7 +311,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const SplitArgs a) {
   long long P_tot = 0;
   if (scan) {
     const int t = threadIdx.x;
-    const long long np = t < a.B ? (clamped_len(a, t, nullptr) + kPage - 1) / kPage : 0;
+    const long long np = t < a.B ? seq_span(a, t, nullptr).np : 0;
     const long long incl = block_scan_256(np, s_scan, &P_tot);
     s_first_page[t] = incl - np;
     __syncthreads();
@@ -291,17 +319,19 @@ __global__ void __launch_bounds__(256) merge_kernel(const SplitArgs a) {
   float sg[V];
 #pragma unroll
   for (int j = 0; j < V; ++j) sg[j] = a.signs != nullptr ? __ldg(a.signs + lane * V + j) : 0.f;
-  const int L = live ? clamped_len(a, b, nullptr) : 0;  // the split kernel already flagged it
+  const float sink2 = live && a.sinks != nullptr ? __ldg(a.sinks + hq) * 1.4426950408889634f : -INFINITY;
+  const SeqSpan sp = live ? seq_span(a, b, nullptr) : SeqSpan{0, 0, 0, 0};  // the split kernel already flagged it
+  const int L = sp.L;
   long long s_lo = 0, s_hi = 0;                           // slot range [s_lo, s_hi)
   bool ranged = false;
   if (L > 0 && a.num_splits > 0) {
-    const int span = (L + a.num_splits - 1) / a.num_splits;
+    const int n = L - sp.lo, span = (n + a.num_splits - 1) / a.num_splits;
     s_lo = static_cast<long long>(b) * a.num_splits;
-    s_hi = s_lo + (L + span - 1) / span;
+    s_hi = s_lo + (n + span - 1) / span;
     ranged = true;
   } else if (L > 0 && scan) {
     const long long C = a.seg_ctas, q = P_tot / C, r = P_tot % C;
-    const long long P0 = s_first_page[b], np = (L + kPage - 1) / kPage;
+    const long long P0 = s_first_page[b], np = sp.np;
     s_lo = run_of_page(P0, q, r) + b;
     s_hi = run_of_page(P0 + np - 1, q, r) + b + 1;
     ranged = true;
@@ -321,7 +351,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const SplitArgs a) {
   }
   s_lo = max(0LL, min(s_lo, a.slots));  // never index outside the workspace
   s_hi = max(s_lo, min(s_hi, a.slots));
-  merge_row<D>(a, b, hq, s_lo, s_hi, lane, sg);
+  merge_row<D>(a, b, hq, s_lo, s_hi, lane, sg, sink2);
 }
 
 }  // namespace kvq

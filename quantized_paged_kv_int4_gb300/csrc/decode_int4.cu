@@ -46,6 +46,9 @@ struct Int4Params {
   const int32_t *block_table;
   float sm_log2;  // softmax scale (divided by D when rotating) times log2(e)
   int64_t num_blocks;
+  float softcap2;       // USE_SOFTCAP: the cap in base-2 units (cap * log2 e), 0 = off
+  float inv_softcap2;
+  const float *alibi;   // USE_ALIBI_SLOPES: [Hq] slopes, or null
 };
 
 constexpr uint32_t kLo = 0x000F000Fu;  // low nibbles of bytes 0 and 2 -> fp16 subnormal pair n * 2^-24
@@ -71,21 +74,28 @@ struct Int4Geom {
   static constexpr int QBYTES = 8 * D * 2 + 64;
 };
 
-// One sequence of the walk over a CTA's run: index b, global index of its page 0 (balanced
-// split) or 0 (fixed split), its page count and its clamped length.
+// One sequence of the walk over a CTA's run: index b, global index of its first read page
+// (balanced split) or 0 (fixed split), its read page count, its clamped length, its first read
+// key lo and the sequence page f holding it (balanced split; 0 in a fixed split, whose page
+// numbers are the sequence's own).
 struct SeqCursor {
   int b;
   int np;
   long long P;
   int L;
+  int lo, f;
 };
 
+template <bool WIN>
 __device__ __forceinline__ void seq_next(const SplitArgs &a, SeqCursor &c) {
   do {
     c.P += c.np;
     ++c.b;
-    c.L = c.b < a.B ? clamped_len(a, c.b, nullptr) : 0;
-    c.np = (c.L + kPage - 1) / kPage;
+    const SeqSpan sp = c.b < a.B ? seq_span<WIN>(a, c.b, nullptr) : SeqSpan{0, 0, 0, 0};
+    c.L = sp.L;
+    c.lo = sp.lo;
+    c.f = sp.f;
+    c.np = sp.np;
   } while (c.np == 0 && c.b < a.B);
 }
 
@@ -100,12 +110,14 @@ struct PageRun {
   SeqCursor first;
 };
 
+template <bool WIN>
 __device__ __forceinline__ bool page_run(const SplitArgs &a, unsigned *flags, PageRun *run) {
   if (a.num_splits > 0) {
     const int b = blockIdx.x / a.num_splits, s = blockIdx.x % a.num_splits;
-    const int L = clamped_len(a, b, flags);
-    const int span = (L + a.num_splits - 1) / a.num_splits;
-    const int t0 = s * span, t1 = min(t0 + span, L);
+    const SeqSpan sp = seq_span<WIN>(a, b, flags);
+    const int L = sp.L;
+    const int span = (L - sp.lo + a.num_splits - 1) / a.num_splits;
+    const int t0 = sp.lo + s * span, t1 = min(t0 + span, L);
     if (t0 >= t1) return false;
     run->fixed = true;
     run->t0 = t0;
@@ -117,6 +129,8 @@ __device__ __forceinline__ bool page_run(const SplitArgs &a, unsigned *flags, Pa
     run->first.P = 0;
     run->first.np = 0x3fffffff;  // never left
     run->first.L = L;
+    run->first.lo = sp.lo;
+    run->first.f = 0;
     return true;
   }
   __shared__ long long s_scan[8];
@@ -125,7 +139,7 @@ __device__ __forceinline__ bool page_run(const SplitArgs &a, unsigned *flags, Pa
   const long long C = gridDim.x, c = blockIdx.x;
   if (a.B <= 256) {  // one scan finds both the total and the sequence holding the run's first page
     const int b = threadIdx.x;
-    const long long np = b < a.B ? (clamped_len(a, b, flags) + kPage - 1) / kPage : 0;
+    const long long np = b < a.B ? seq_span<WIN>(a, b, flags).np : 0;
     long long P_tot;
     const long long incl = block_scan_256(np, s_scan, &P_tot);
     const long long q = P_tot / C, r = P_tot % C;
@@ -142,14 +156,17 @@ __device__ __forceinline__ bool page_run(const SplitArgs &a, unsigned *flags, Pa
     run->n = static_cast<int>(pe - pb);
     run->first.b = s_first_b;
     run->first.P = s_first_p;
-    run->first.L = clamped_len(a, s_first_b, nullptr);
-    run->first.np = (run->first.L + kPage - 1) / kPage;
+    const SeqSpan sp = seq_span<WIN>(a, s_first_b, nullptr);
+    run->first.L = sp.L;
+    run->first.lo = sp.lo;
+    run->first.f = sp.f;
+    run->first.np = sp.np;
     return true;
   }
   long long P_tot = 0;
   for (int base = 0; base < a.B; base += 256) {
     const int b = base + threadIdx.x;
-    const long long np = b < a.B ? (clamped_len(a, b, flags) + kPage - 1) / kPage : 0;
+    const long long np = b < a.B ? seq_span<WIN>(a, b, flags).np : 0;
     long long chunk;
     block_scan_256(np, s_scan, &chunk);
     P_tot += chunk;
@@ -162,7 +179,7 @@ __device__ __forceinline__ bool page_run(const SplitArgs &a, unsigned *flags, Pa
   long long running = 0;
   for (int base = 0; base < a.B; base += 256) {
     const int b = base + threadIdx.x;
-    const long long np = b < a.B ? (clamped_len(a, b, nullptr) + kPage - 1) / kPage : 0;
+    const long long np = b < a.B ? seq_span<WIN>(a, b, nullptr).np : 0;
     long long chunk;
     const long long incl = block_scan_256(np, s_scan, &chunk) + running;
     const long long excl = incl - np;
@@ -180,8 +197,11 @@ __device__ __forceinline__ bool page_run(const SplitArgs &a, unsigned *flags, Pa
   run->n = static_cast<int>(pe - pb);
   run->first.b = s_first_b;
   run->first.P = s_first_p;
-  run->first.L = clamped_len(a, s_first_b, nullptr);
-  run->first.np = (run->first.L + kPage - 1) / kPage;
+  const SeqSpan sp = seq_span<WIN>(a, s_first_b, nullptr);
+  run->first.L = sp.L;
+  run->first.lo = sp.lo;
+  run->first.f = sp.f;
+  run->first.np = sp.np;
   return true;
 }
 
@@ -417,19 +437,45 @@ __device__ __forceinline__ void page_pv(float (&acc)[D / 16][4], uint32_t so, co
   }
 }
 
+// Score modifiers of one warp (unified_attention_int4's USE_SOFTCAP and USE_ALIBI_SLOPES), in
+// base-2 units: S = cap2 tanh(S / cap2), then S += slope2 * (n - qpos) for the lane's two head
+// columns; qpos = L - 1, the query's position.
+struct ScoreMods {
+  float cap2, inv_cap2, sl0, sl1;
+  int qpos;
+  bool cap, alibi;
+};
+
 // NP consecutive pages of this warp (stage offsets so[0..NP-1]) inside one piece: scores, one
 // online softmax step over their 16 * NP tokens, P.V. MASKED: some rows of the (single) page lie
-// outside [t0, t1) -- the ragged end of a sequence or a fixed split boundary -- and may hold
-// never-written scale words (NaN): they are selected away, never multiplied.
-template <int D, int W, int NP, bool MASKED>
+// outside [t0, t1) -- the ragged end of a sequence, a fixed split boundary or the start of a
+// sliding window -- and may hold never-written scale words (NaN): they are selected away, never
+// multiplied. MODS: apply the score modifiers md (page i's row 0 is at position nb + 16 W i).
+template <int D, int W, int NP, bool MASKED, bool MODS>
 __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&so)[2], const LaneOffsets<D> &lo,
                                            const uint32_t (&qf)[D / 16][2], float qs0, float qs1, float sm24,
-                                           int lane, int nb, int t0, int t1) {
+                                           int lane, int nb, int t0, int t1, const ScoreMods &md) {
   using Gm = Int4Geom<D>;
   const int g = lane >> 2;
   PageIn pg[NP];
 #pragma unroll
   for (int i = 0; i < NP; ++i) page_scores<D, W>(pg[i], so[i], lo, qf, qs0, qs1, sm24);
+  if constexpr (MODS) {
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      if (md.cap) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) pg[i].s[j] = md.cap2 * tanhf(pg[i].s[j] * md.inv_cap2);
+      }
+      if (md.alibi) {
+        const float d0 = static_cast<float>(nb + i * W * kPage + g - md.qpos), d1 = d0 + 8.f;
+        pg[i].s[0] = fmaf(md.sl0, d0, pg[i].s[0]);
+        pg[i].s[1] = fmaf(md.sl1, d0, pg[i].s[1]);
+        pg[i].s[2] = fmaf(md.sl0, d1, pg[i].s[2]);
+        pg[i].s[3] = fmaf(md.sl1, d1, pg[i].s[3]);
+      }
+    }
+  }
   bool ok0 = true, ok1 = true;
   if (MASKED) {
     ok0 = nb + g >= t0 && nb + g < t1;
@@ -525,7 +571,7 @@ __device__ __forceinline__ void int4_finish(const SplitArgs &a, PieceState<D> &s
 // threads have finished reading it (every thread arrives once). Warp 0 is also the producer: it
 // issued the first NS stages and refills a slot once its s_empty phase completes -- polling
 // without blocking between pages, and blocking only for a stage it needs itself.
-template <int D, int NS, int W>
+template <int D, int NS, int W, bool MODS>
 __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_constant__ Int4Params p) {
   using Gm = Int4Geom<D>;
   constexpr int HB = 8 / W;
@@ -543,7 +589,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   const bool split_heads = a.Hk > 8;
 
   PageRun run;
-  if (!page_run(a, &g_flags_decode_int4, &run)) return;  // uniform over the CTA
+  if (!page_run<MODS>(a, &g_flags_decode_int4, &run)) return;  // uniform over the CTA
   const int n_stages = (run.n + W - 1) / W;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -561,8 +607,8 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     const int x = k * 32 + lane;
     if (x >= run.n) return 0;
     const long long X = run.base + x;
-    while (X >= lc.P + lc.np && lc.b < a.B) seq_next(a, lc);
-    return lc.b < a.B ? __ldg(p.block_table + static_cast<long long>(lc.b) * a.max_blocks + (X - lc.P)) : -1;
+    while (X >= lc.P + lc.np && lc.b < a.B) seq_next<MODS>(a, lc);
+    return lc.b < a.B ? __ldg(p.block_table + static_cast<long long>(lc.b) * a.max_blocks + (X - lc.P + lc.f)) : -1;
   };
   // Stage k into ring slot `slot`: lane i copies page k * W + i (expect_tx first, by lane 0).
   auto issue = [&](int k, int slot, int bid) {  // warp-wide
@@ -596,7 +642,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   if (sub < run.n) {
     SeqCursor c0 = run.first;
     const long long X0 = run.base + sub;
-    while (X0 >= c0.P + c0.np && c0.b < a.B) seq_next(a, c0);
+    while (X0 >= c0.P + c0.np && c0.b < a.B) seq_next<MODS>(a, c0);
     if (c0.b < a.B) {
       fetch_query<D>(p, qarea, c0.b, h, lane);
       q_prefetched = c0.b;
@@ -648,22 +694,34 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   float qs0 = 0.f, qs1 = 0.f;
   bool have_q = false, abort = false;
   const float sm24 = p.sm_log2 * kTwo24;  // the K operands carry a factor 2^-24
+  ScoreMods md{};
+  if constexpr (MODS) {
+    const int c0 = 2 * (lane & 3), G = a.G;
+    const float lg2e = 1.4426950408889634f;
+    md.cap = p.softcap2 > 0.f;
+    md.cap2 = p.softcap2;
+    md.inv_cap2 = p.inv_softcap2;
+    md.alibi = p.alibi != nullptr;
+    md.sl0 = md.alibi && c0 < G ? __ldg(p.alibi + h * G + c0) * lg2e : 0.f;
+    md.sl1 = md.alibi && c0 + 1 < G ? __ldg(p.alibi + h * G + c0 + 1) * lg2e : 0.f;
+  }
   // the current piece in run coordinates: its pages are run pages < pe_x, run page x is page
   // x + off of sequence cur.b, and its tokens are [t0, t1)
   int pe_x = 0, off = 0, t0 = 0, t1 = 0;
   auto bounds = [&]() {
-    off = static_cast<int>(run.base - cur.P);
+    off = static_cast<int>(run.base - cur.P) + cur.f;
     if (run.fixed) {
       pe_x = run.n;
       t0 = run.t0;
       t1 = run.t1;
     } else {
       pe_x = static_cast<int>(min(static_cast<long long>(run.n), cur.P + cur.np - run.base));
-      t0 = static_cast<int>((max(run.base, cur.P) - cur.P) * kPage);
-      t1 = static_cast<int>(min((min(run.end, cur.P + cur.np) - cur.P) * kPage, static_cast<long long>(cur.L)));
+      t0 = max(cur.lo, static_cast<int>((max(run.base, cur.P) - cur.P + cur.f) * kPage));
+      t1 = static_cast<int>(min((min(run.end, cur.P + cur.np) - cur.P + cur.f) * kPage, static_cast<long long>(cur.L)));
     }
   };
   bounds();
+  md.qpos = cur.L - 1;
   auto finish_piece = [&]() {
     const long long slot = run.fixed ? static_cast<long long>(blockIdx.x) : blockIdx.x + static_cast<long long>(cur.b);
     int4_finish<D>(a, st, slot, sub, h, lane);
@@ -693,17 +751,18 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     if (x >= pe_x) {  // pieces this warp is done with (or has no page of)
       while (run.base + x >= cur.P + cur.np && cur.b < a.B) {
         finish_piece();
-        seq_next(a, cur);
+        seq_next<MODS>(a, cur);
       }
       if (cur.b >= a.B) break;  // cannot happen: the run lies inside the batch's pages
       bounds();
+      md.qpos = cur.L - 1;
     }
     if (!have_q) {
       load_query<D>(p, qarea, cur.b, h, lane, qf, qs0, qs1, q_prefetched == cur.b);
       q_prefetched = -1;
       if (pe_x < run.n && !run.fixed) {  // the run goes on into another sequence: fetch its query now
         SeqCursor nx = cur;
-        seq_next(a, nx);
+        seq_next<MODS>(a, nx);
         if (nx.b < a.B) {
           fetch_query<D>(p, qarea, nx.b, h, lane);
           q_prefetched = nx.b;
@@ -726,7 +785,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
         break;
       }
       if (warp == 0) produce(-1);  // the slots freed meanwhile (at the start: the unused ones)
-      int4_pages<D, W, 2, false>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1);
+      int4_pages<D, W, 2, false, MODS>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, md);
       mbar_arrive(smem_u32(&s_empty[sj]));
       mbar_arrive(smem_u32(&s_empty[sj1]));
       j += 2;
@@ -738,7 +797,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
         break;
       }
       if (warp == 0) produce(-1);  // the slots freed meanwhile (at the start: the unused ones)
-      int4_pages<D, W, 1, true>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1);
+      int4_pages<D, W, 1, true, MODS>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, md);
       mbar_arrive(smem_u32(&s_empty[sj]));
       j += 1;
       sj = sj1;
@@ -749,7 +808,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   if (cur.b < a.B) finish_piece();
   if (!run.fixed && !abort) {
     while (cur.P + cur.np < run.end && cur.b < a.B - 1) {  // later pieces of the run without a page of this warp
-      seq_next(a, cur);
+      seq_next<MODS>(a, cur);
       if (cur.b >= a.B) break;
       finish_piece();
     }
@@ -773,19 +832,19 @@ bool take_flags_decode_int4(cudaStream_t stream, unsigned *host_word) {
                                  cudaMemcpyHostToDevice, stream) == cudaSuccess;
 }
 
-template <int D, int W>
+template <int D, int W, bool MODS>
 static kvq_status launch_int4_w(const Int4Params &p, const SplitPlan &plan, cudaStream_t s) {
   const size_t smem = int4_smem_bytes<D>();
   static bool attr_set = false;  // per process; the attribute is per function, not per device
   if (!attr_set) {
-    if (cudaFuncSetAttribute(decode_int4_kernel<D, kStagesInt4, W>,
+    if (cudaFuncSetAttribute(decode_int4_kernel<D, kStagesInt4, W, MODS>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return KVQ_ERR_CUDA;
     attr_set = true;
   }
   const dim3 grid(plan.seg_ctas, plan.head_groups);
-  decode_int4_kernel<D, kStagesInt4, W><<<grid, 256, smem, s>>>(p);
+  decode_int4_kernel<D, kStagesInt4, W, MODS><<<grid, 256, smem, s>>>(p);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   const long long rows = static_cast<long long>(p.s.B) * p.s.Hq;
   if (launch_dependent(merge_kernel<D>, dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), s, p.s) != cudaSuccess)
@@ -793,13 +852,13 @@ static kvq_status launch_int4_w(const Int4Params &p, const SplitPlan &plan, cuda
   return launch_status();
 }
 
-template <int D>
+template <int D, bool MODS>
 static kvq_status launch_int4(const Int4Params &p, const SplitPlan &plan, cudaStream_t s) {
   switch (plan.warps_per_head) {
-    case 1: return launch_int4_w<D, 1>(p, plan, s);
-    case 2: return launch_int4_w<D, 2>(p, plan, s);
-    case 4: return launch_int4_w<D, 4>(p, plan, s);
-    case 8: return launch_int4_w<D, 8>(p, plan, s);
+    case 1: return launch_int4_w<D, 1, MODS>(p, plan, s);
+    case 2: return launch_int4_w<D, 2, MODS>(p, plan, s);
+    case 4: return launch_int4_w<D, 4, MODS>(p, plan, s);
+    case 8: return launch_int4_w<D, 8, MODS>(p, plan, s);
     default: return KVQ_ERR_UNSUPPORTED;
   }
 }
@@ -808,15 +867,20 @@ static kvq_status launch_int4(const Int4Params &p, const SplitPlan &plan, cudaSt
 
 using namespace kvq;
 
-extern "C" kvq_status kvq_decode_int4(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
-                                      const float *k_scale, const float *v_scale,
-                                      const int32_t *block_table, int32_t max_blocks,
-                                      const int32_t *seq_lens, const float *rht_signs,
-                                      float softmax_scale, int32_t num_splits, void *workspace,
-                                      size_t workspace_bytes, void *out, kvq_dtype out_dtype,
-                                      int32_t B, int32_t Hq, int32_t Hk, int32_t D,
-                                      int32_t block_size, int64_t num_blocks, kvq_stream_t stream) {
+extern "C" kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                           const float *k_scale, const float *v_scale,
+                                           const int32_t *block_table, int32_t max_blocks,
+                                           const int32_t *seq_lens, const float *rht_signs,
+                                           float softmax_scale, int32_t num_splits, void *workspace,
+                                           size_t workspace_bytes, void *out, kvq_dtype out_dtype,
+                                           int32_t B, int32_t Hq, int32_t Hk, int32_t D,
+                                           int32_t block_size, int64_t num_blocks,
+                                           const kvq_score_mods *mods, kvq_stream_t stream) {
   if (B < 0 || Hq < 1 || Hk < 1 || max_blocks < 0 || num_splits < 0 || num_blocks < 1)
+    return KVQ_ERR_INVALID_ARG;
+  if (mods && (mods->sliding_window < 0 || !(mods->softcap >= 0.f) || !(mods->softcap < INFINITY) ||
+               (mods->sinks && !aligned(mods->sinks, 4)) ||
+               (mods->alibi_slopes && !aligned(mods->alibi_slopes, 4))))
     return KVQ_ERR_INVALID_ARG;
   if (Hq % Hk != 0) return KVQ_ERR_INVALID_ARG;
   if (out_dtype != KVQ_BF16 && out_dtype != KVQ_F16 && out_dtype != KVQ_F32) return KVQ_ERR_INVALID_ARG;
@@ -854,14 +918,35 @@ extern "C" kvq_status kvq_decode_int4(const void *q, const uint8_t *k_cache, con
   sa.signs = rht_signs;
   sa.out = out;
   sa.out_dtype = out_dtype;
+  sa.window = mods ? mods->sliding_window : 0;
+  sa.sinks = mods ? mods->sinks : nullptr;
   p.q = static_cast<const __nv_bfloat16 *>(q);
   if (!int4_tensor_maps(k_cache, v_cache, k_scale, v_scale, num_blocks, Hk, D, &p.maps)) return KVQ_ERR_CUDA;
   p.block_table = block_table;
   const double sm = rht_signs ? static_cast<double>(softmax_scale) / D : softmax_scale;
   p.sm_log2 = static_cast<float>(sm * 1.4426950408889634);
   p.num_blocks = num_blocks;
+  const double cap2 = mods ? static_cast<double>(mods->softcap) * 1.4426950408889634 : 0.0;
+  p.softcap2 = static_cast<float>(cap2);
+  p.inv_softcap2 = cap2 > 0.0 ? static_cast<float>(1.0 / cap2) : 0.f;
+  p.alibi = mods ? mods->alibi_slopes : nullptr;
+  const bool score_mods = p.softcap2 > 0.f || p.alibi != nullptr || sa.window > 0;  // sinks: merge only
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return D == 128 ? launch_int4<128>(p, plan, s) : launch_int4<64>(p, plan, s);
+  if (D == 128) return score_mods ? launch_int4<128, true>(p, plan, s) : launch_int4<128, false>(p, plan, s);
+  return score_mods ? launch_int4<64, true>(p, plan, s) : launch_int4<64, false>(p, plan, s);
+}
+
+extern "C" kvq_status kvq_decode_int4(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                      const float *k_scale, const float *v_scale,
+                                      const int32_t *block_table, int32_t max_blocks,
+                                      const int32_t *seq_lens, const float *rht_signs,
+                                      float softmax_scale, int32_t num_splits, void *workspace,
+                                      size_t workspace_bytes, void *out, kvq_dtype out_dtype,
+                                      int32_t B, int32_t Hq, int32_t Hk, int32_t D,
+                                      int32_t block_size, int64_t num_blocks, kvq_stream_t stream) {
+  return kvq_decode_int4_mods(q, k_cache, v_cache, k_scale, v_scale, block_table, max_blocks, seq_lens,
+                              rht_signs, softmax_scale, num_splits, workspace, workspace_bytes, out,
+                              out_dtype, B, Hq, Hk, D, block_size, num_blocks, nullptr, stream);
 }
 
 // ---------------------------------------------------------------------------------------------

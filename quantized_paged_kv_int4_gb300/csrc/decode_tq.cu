@@ -407,6 +407,8 @@ extern "C" kvq_status kvq_decode_tq(const float *q, const uint8_t *kv_cache, int
   sa.slots = plan.slots;
   workspace_carve(workspace, B, Hq, D, plan, &sa.part_o, &sa.part_lse, &sa.seg_first, &sa.seg_last);
   sa.signs = nullptr;
+  sa.window = 0;
+  sa.sinks = nullptr;
   sa.out = out;
   sa.out_dtype = KVQ_F32;
   p.q = q;

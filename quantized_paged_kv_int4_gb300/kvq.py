@@ -24,13 +24,21 @@ KVQ_BF16, KVQ_F16, KVQ_F32 = 0, 1, 2
 
 # the C API's declared functions, in header order
 C_FUNCTIONS = ("kvq_status_string", "kvq_abi_version", "kvq_write_int4", "kvq_decode_workspace_bytes",
-               "kvq_decode_int4", "kvq_decode_int4_noalloc", "kvq_decode_tq", "kvq_fwht128", "kvq_device_error")
+               "kvq_decode_int4", "kvq_decode_int4_mods", "kvq_decode_int4_noalloc", "kvq_decode_tq",
+               "kvq_fwht128", "kvq_device_error")
 KVQ_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lock = threading.Lock()
 _handle = None
 
 c_i32, c_i64, c_sz, c_p, c_f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
+
+
+class ScoreMods(ctypes.Structure):
+    """kvq_score_mods (include/kvq.h)."""
+    _fields_ = [("sliding_window", c_i32), ("softcap", c_f32), ("sinks", c_p), ("alibi_slopes", c_p)]
+
+
 _SIGS = {
     "kvq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kvq_abi_version": (c_i32, []),
@@ -39,6 +47,9 @@ _SIGS = {
     "kvq_decode_workspace_bytes": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32]),
     "kvq_decode_int4": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_f32, c_i32, c_p, c_sz,
                                        c_p, ctypes.c_int, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_p]),
+    "kvq_decode_int4_mods": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_f32, c_i32, c_p, c_sz,
+                                            c_p, ctypes.c_int, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64,
+                                            ctypes.POINTER(ScoreMods), c_p]),
     "kvq_decode_int4_noalloc": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_f32, c_i32, c_p,
                                                ctypes.c_int, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_p]),
     "kvq_decode_tq": (ctypes.c_int, [c_p, c_p, c_i32, c_i32, c_p, c_i32, c_p, c_f32, c_i32, c_p, c_sz, c_p,
@@ -155,8 +166,12 @@ def _workspace(workspace, B, Hq, Hk, D, num_splits, device):
 
 
 def kvq_decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, rht_signs, softmax_scale,
-                    out=None, workspace=None, num_splits=0, out_dtype=None, stream=None):
-    """unified_attention_int4 (decode): q [B, Hq, D] bf16 -> out [B, Hq, D]. Returns out."""
+                    out=None, workspace=None, num_splits=0, out_dtype=None, stream=None,
+                    sliding_window=0, softcap=0.0, sinks=None, alibi_slopes=None):
+    """unified_attention_int4 (decode): q [B, Hq, D] bf16 -> out [B, Hq, D]. Returns out.
+
+    sliding_window / softcap / sinks ([Hq] fp32) / alibi_slopes ([Hq] fp32): the score modifiers
+    (kvq_decode_int4_mods); all off by default."""
     _need(q, "q", torch.bfloat16)
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
         _need(t, n, torch.uint8)
@@ -172,6 +187,20 @@ def kvq_decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens
         out = torch.empty((B, Hq, D), dtype=out_dtype or torch.float32, device=q.device)
     _need(out, "out")
     workspace = _workspace(workspace, B, Hq, Hk, D, num_splits, q.device)
+    if sliding_window or softcap or sinks is not None or alibi_slopes is not None:
+        for t, n in ((sinks, "sinks"), (alibi_slopes, "alibi_slopes")):
+            if t is not None:
+                _need(t, n, torch.float32)
+                if t.numel() != Hq:
+                    raise ValueError("%s must have Hq = %d entries" % (n, Hq))
+        mods = ScoreMods(int(sliding_window), float(softcap), _ptr(sinks), _ptr(alibi_slopes))
+        _check(lib().kvq_decode_int4_mods(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                          _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(rht_signs),
+                                          float(softmax_scale), num_splits, _ptr(workspace), workspace.numel(),
+                                          _ptr(out), _out_code(out.dtype), B, Hq, Hk, D, bs, nb, ctypes.byref(mods),
+                                          _stream(stream)),
+               "kvq_decode_int4_mods")
+        return out
     _check(lib().kvq_decode_int4(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                                  _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(rht_signs),
                                  float(softmax_scale), num_splits, _ptr(workspace), workspace.numel(),

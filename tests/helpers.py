@@ -56,11 +56,11 @@ class Int4Case:
         self.q = workloads.query(case)
         self.lens = torch.tensor(case.seq_lens, dtype=torch.int32)
 
-    def oracle(self, batch_index=None, num_splits=None):
+    def oracle(self, batch_index=None, num_splits=None, **mods):
         return int4_cache.decode_int4(
             workloads.to_numpy_f32(self.q), self.kc, self.vc, self.ks, self.vs, self.bt.numpy(),
             np.asarray(self.case.seq_lens), None if self.signs is None else self.signs.numpy(),
-            self.scale, num_splits=num_splits, batch_index=batch_index)
+            self.scale, num_splits=num_splits, batch_index=batch_index, **mods)
 
     def to_gpu(self, dev="cuda"):
         g = {}
@@ -75,9 +75,9 @@ class Int4Case:
         return g
 
 
-def run_int4(kvq, g, scale, num_splits=0, out_dtype=torch.float32):
+def run_int4(kvq, g, scale, num_splits=0, out_dtype=torch.float32, **mods):
     out = kvq.kvq_decode_int4(g["q"], g["kc"], g["vc"], g["ks"], g["vs"], g["bt"], g["lens"], g["signs"],
-                              scale, num_splits=num_splits, out_dtype=out_dtype)
+                              scale, num_splits=num_splits, out_dtype=out_dtype, **mods)
     st, flags = kvq.kvq_device_error()
     assert st == 0 and flags == 0, (st, flags)
     return out

@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings_and_version():
-    assert kvq.kvq_abi_version() == 1
+    assert kvq.kvq_abi_version() == 2
     for code in range(6):
         assert kvq.kvq_status_string(code).startswith("KVQ_")
     assert "UNKNOWN" in kvq.kvq_status_string(77)
@@ -81,6 +81,29 @@ def test_decode_validation_without_gpu():
     assert _decode(out=20) == kvq.KVQ_ERR_INVALID_ARG          # misaligned output
     assert _decode(od=7) == kvq.KVQ_ERR_INVALID_ARG
     assert _decode(wsb=10) == kvq.KVQ_ERR_WORKSPACE
+
+
+def _decode_mods(mods, **kw):
+    a = dict(q=16, kc=16, vc=16, ks=16, vs=16, bt=16, mb=4, sl=16, signs=None, scale=0.1, S=4, ws=16,
+             wsb=1 << 30, out=16, od=kvq.KVQ_F32, B=2, Hq=4, Hk=2, D=64, bs=16, nb=10, stream=None)
+    a.update(kw)
+    return kvq.lib().kvq_decode_int4_mods(a["q"], a["kc"], a["vc"], a["ks"], a["vs"], a["bt"], a["mb"], a["sl"],
+                                          a["signs"], a["scale"], a["S"], a["ws"], a["wsb"], a["out"], a["od"],
+                                          a["B"], a["Hq"], a["Hk"], a["D"], a["bs"], a["nb"],
+                                          None if mods is None else ctypes.byref(mods), a["stream"])
+
+
+def test_decode_mods_validation_without_gpu():
+    M = kvq.ScoreMods
+    assert _decode_mods(None, B=0) == kvq.KVQ_OK
+    assert _decode_mods(M(0, 0.0, None, None), B=0) == kvq.KVQ_OK
+    assert _decode_mods(M(-1, 0.0, None, None)) == kvq.KVQ_ERR_INVALID_ARG       # negative window
+    assert _decode_mods(M(0, -1.0, None, None)) == kvq.KVQ_ERR_INVALID_ARG       # negative cap
+    assert _decode_mods(M(0, float("inf"), None, None)) == kvq.KVQ_ERR_INVALID_ARG
+    assert _decode_mods(M(0, float("nan"), None, None)) == kvq.KVQ_ERR_INVALID_ARG
+    assert _decode_mods(M(0, 0.0, 18, None)) == kvq.KVQ_ERR_INVALID_ARG          # misaligned sinks
+    assert _decode_mods(M(0, 0.0, None, 18)) == kvq.KVQ_ERR_INVALID_ARG          # misaligned slopes
+    assert _decode_mods(M(8, 30.0, 16, 16), wsb=10) == kvq.KVQ_ERR_WORKSPACE      # then the usual checks
 
 
 def test_workspace_sizes_fixed_splits():
