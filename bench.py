@@ -50,8 +50,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--workload", default="llama3_8b_int4",
-                    choices=["llama3_8b_int4", "long_context_int4", "turboquant_fp8_v4", "turboquant_fp8_v3",
-                             "write_fwht"])
+                    choices=["llama3_8b_int4", "llama3_8b_int4_mods", "long_context_int4", "turboquant_fp8_v4",
+                             "turboquant_fp8_v3", "write_fwht"])
     ap.add_argument("--replicas", type=int, default=4)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -176,9 +176,15 @@ def ncu_traffic(kernel_tag, source_files):
 # ----------------------------------------------------------------------------------------------
 # workloads
 # ----------------------------------------------------------------------------------------------
-def int4_decode_bytes(lens, Hq, Hk, D, out_bytes=2):
-    kv = sum(L * Hk * (D + 8) for L in lens)
-    bt = sum(-(-L // 16) * 4 for L in lens)
+def int4_decode_bytes(lens, Hq, Hk, D, out_bytes=2, window=0):
+    """Algorithmic bytes of one decode call: the keys read (the last `window` of each sequence
+    under a sliding window) at D + 8 bytes per (token, kv head), their block-table entries, q,
+    out and seq_lens."""
+    kv, bt = 0, 0
+    for L in lens:
+        lo = max(0, L - window) if window > 0 else 0
+        kv += (L - lo) * Hk * (D + 8)
+        bt += ((L - 1) // 16 - lo // 16 + 1) * 4 if L > 0 else 0
     return kv + bt + len(lens) * Hq * D * (2 + out_bytes) + 4 * len(lens), kv
 
 
@@ -227,10 +233,15 @@ def run_kvq(args, dist):
         return run_write_fwht(args, dist, dev, stream)
     if wl.startswith("turboquant"):
         return run_tq(args, dist, dev, stream)
-    case = workloads.llama8b_int4() if wl == "llama3_8b_int4" else workloads.long_context_int4()
+    case = workloads.long_context_int4() if wl == "long_context_int4" else workloads.llama8b_int4()
     B, Hq, Hk, D = case.B, case.Hq, case.Hk, case.D
     signs = workloads.rht_signs(D).to(dev)
     scale = 1.0 / math.sqrt(D)
+    mods = {}
+    if wl == "llama3_8b_int4_mods":  # every score modifier at once: 4096-key window, cap 30, ALiBi, sinks
+        mods = dict(sliding_window=4096, softcap=30.0,
+                    alibi_slopes=(2.0 ** (-8.0 * (torch.arange(Hq, dtype=torch.float32) + 1) / Hq)).to(dev),
+                    sinks=(torch.randn((Hq,), generator=torch.Generator().manual_seed(5)) * 2.0).to(dev))
     pool = None
     nrep = args.replicas
     if wl == "long_context_int4":
@@ -245,7 +256,7 @@ def run_kvq(args, dist):
 
     def decode(r):
         kvq.kvq_decode_int4(r.q, r.kc, r.vc, r.ks, r.vs, r.bt, r.lens, signs, scale, out=r.out, workspace=ws,
-                            num_splits=S, stream=stream)
+                            num_splits=S, stream=stream, **mods)
 
     with torch.cuda.stream(stream):
         for r in reps:  # eager warm-up (also sets kernel attributes before capture)
@@ -264,7 +275,8 @@ def run_kvq(args, dist):
         gw.append(a)
         gd.append(b)
 
-    dec_bytes, kv_bytes = int4_decode_bytes(case.seq_lens, Hq, Hk, D)
+    dec_bytes, kv_bytes = int4_decode_bytes(case.seq_lens, Hq, Hk, D, window=mods.get("sliding_window", 0))
+    dec_bytes += 8 * Hq if mods else 0  # sinks and slopes
     wr_bytes = B * Hk * (2 * D * 2 + 2 * (D // 2 + 4)) + 8 * B
     res = timed_steps(args, dist, stream, lambda i: gw[i % nrep].replay(), lambda i: gd[i % nrep].replay(),
                       dev.index)
@@ -272,18 +284,22 @@ def run_kvq(args, dist):
     assert st == 0, flags
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not mods:
         e2e = e2e_int4(args, reps[0], case, signs, scale, ws, S, dev, stream, dec_bytes)
     cfg = {"workload": wl, "B": B, "Hq": Hq, "Hk": Hk, "D": D, "block_size": 16,
-           "seq_lens": "U[1024,8192] seed 0, sum %d" % sum(case.seq_lens) if wl == "llama3_8b_int4"
+           "seq_lens": "U[1024,8192] seed 0, sum %d" % sum(case.seq_lens) if wl != "long_context_int4"
            else "131072 x 4, pages scattered in a %.0f GB pool" % (case.pool_bytes / 1e9),
            "num_splits": "heuristic (balanced)" if S == 0 else S, "rht": True, "out_dtype": "bf16",
            "step": "kvq_write_int4 (B new tokens) + kvq_decode_int4",
-           "l2": ("%d rotating cache replicas of %.0f MB (> 126 MB L2): no L2 reuse across steps"
-                  % (nrep, kv_bytes / 1e6)) if nrep > 1 else "single %.0f MB cache read per step (> L2)" % (kv_bytes / 1e6),
+           "l2": ("%d rotating cache replicas, %.0f MB read from each per step (%d x %.0f MB > 126 MB L2): "
+                  "no L2 reuse across steps" % (nrep, kv_bytes / 1e6, nrep, kv_bytes / 1e6)) if nrep > 1
+           else "single %.0f MB cache read per step (> L2)" % (kv_bytes / 1e6),
            "decode_bytes_per_step": dec_bytes, "kv_cache_bytes_per_step": kv_bytes, "write_bytes_per_step": wr_bytes}
+    if mods:
+        cfg["score_mods"] = "sliding_window 4096 (keys read: %d of %d), softcap 30, ALiBi slopes 2^(-8(h+1)/Hq), sinks" % (
+            kv_bytes // (Hk * (D + 8)), sum(case.seq_lens))
     kernels = 3  # write, split-KV decode, merge
-    tag = "decode_int4" if wl == "llama3_8b_int4" else "decode_int4_long_context"
+    tag = {"llama3_8b_int4": "decode_int4", "long_context_int4": "decode_int4_long_context"}.get(wl, "decode_int4_mods")
     return finish(args, dist, res, dec_bytes, cfg, e2e, kernels, tag,
                   ["quantized_paged_kv_int4_gb300/csrc/decode_int4.cu",
                    "quantized_paged_kv_int4_gb300/csrc/decode_common.cuh",

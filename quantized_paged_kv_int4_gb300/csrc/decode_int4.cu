@@ -437,13 +437,20 @@ __device__ __forceinline__ void page_pv(float (&acc)[D / 16][4], uint32_t so, co
   }
 }
 
+// tanh(y) = 1 - 2 / (e^(2y) + 1) with the hardware base-2 exponential; |y| is limited to 10
+// (tanh(10) rounds to 1 in fp32). The absolute error (a few 1e-7) is what the soft cap passes on.
+__device__ __forceinline__ float tanh_fast(float y) {
+  const float e = fast_exp2(fminf(fmaxf(y, -10.f), 10.f) * 2.8853900817779268f);  // e^(2y)
+  return 1.f - __fdividef(2.f, e + 1.f);
+}
+
 // Score modifiers of one warp (unified_attention_int4's USE_SOFTCAP and USE_ALIBI_SLOPES), in
-// base-2 units: S = cap2 tanh(S / cap2), then S += slope2 * (n - qpos) for the lane's two head
-// columns; qpos = L - 1, the query's position.
+// base-2 units: S = cap2 tanh(S / cap2) (cap2 and its inverse stay in the kernel parameters),
+// then S += slope2 * (n - qpos) for the lane's two head columns; qpos = L - 1, the query's
+// position.
 struct ScoreMods {
-  float cap2, inv_cap2, sl0, sl1;
+  float sl0, sl1;
   int qpos;
-  bool cap, alibi;
 };
 
 // NP consecutive pages of this warp (stage offsets so[0..NP-1]) inside one piece: scores, one
@@ -454,7 +461,8 @@ struct ScoreMods {
 template <int D, int W, int NP, bool MASKED, bool MODS>
 __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&so)[2], const LaneOffsets<D> &lo,
                                            const uint32_t (&qf)[D / 16][2], float qs0, float qs1, float sm24,
-                                           int lane, int nb, int t0, int t1, const ScoreMods &md) {
+                                           int lane, int nb, int t0, int t1, const Int4Params &p,
+                                           const ScoreMods &md) {
   using Gm = Int4Geom<D>;
   const int g = lane >> 2;
   PageIn pg[NP];
@@ -463,11 +471,11 @@ __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&s
   if constexpr (MODS) {
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
-      if (md.cap) {
+      if (p.softcap2 > 0.f) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) pg[i].s[j] = md.cap2 * tanhf(pg[i].s[j] * md.inv_cap2);
+        for (int j = 0; j < 4; ++j) pg[i].s[j] = p.softcap2 * tanh_fast(pg[i].s[j] * p.inv_softcap2);
       }
-      if (md.alibi) {
+      if (p.alibi != nullptr) {
         const float d0 = static_cast<float>(nb + i * W * kPage + g - md.qpos), d1 = d0 + 8.f;
         pg[i].s[0] = fmaf(md.sl0, d0, pg[i].s[0]);
         pg[i].s[1] = fmaf(md.sl1, d0, pg[i].s[1]);
@@ -698,12 +706,8 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   if constexpr (MODS) {
     const int c0 = 2 * (lane & 3), G = a.G;
     const float lg2e = 1.4426950408889634f;
-    md.cap = p.softcap2 > 0.f;
-    md.cap2 = p.softcap2;
-    md.inv_cap2 = p.inv_softcap2;
-    md.alibi = p.alibi != nullptr;
-    md.sl0 = md.alibi && c0 < G ? __ldg(p.alibi + h * G + c0) * lg2e : 0.f;
-    md.sl1 = md.alibi && c0 + 1 < G ? __ldg(p.alibi + h * G + c0 + 1) * lg2e : 0.f;
+    md.sl0 = p.alibi != nullptr && c0 < G ? __ldg(p.alibi + h * G + c0) * lg2e : 0.f;
+    md.sl1 = p.alibi != nullptr && c0 + 1 < G ? __ldg(p.alibi + h * G + c0 + 1) * lg2e : 0.f;
   }
   // the current piece in run coordinates: its pages are run pages < pe_x, run page x is page
   // x + off of sequence cur.b, and its tokens are [t0, t1)
@@ -785,7 +789,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
         break;
       }
       if (warp == 0) produce(-1);  // the slots freed meanwhile (at the start: the unused ones)
-      int4_pages<D, W, 2, false, MODS>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, md);
+      int4_pages<D, W, 2, false, MODS>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, p, md);
       mbar_arrive(smem_u32(&s_empty[sj]));
       mbar_arrive(smem_u32(&s_empty[sj1]));
       j += 2;
@@ -797,7 +801,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
         break;
       }
       if (warp == 0) produce(-1);  // the slots freed meanwhile (at the start: the unused ones)
-      int4_pages<D, W, 1, true, MODS>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, md);
+      int4_pages<D, W, 1, true, MODS>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, p, md);
       mbar_arrive(smem_u32(&s_empty[sj]));
       j += 1;
       sj = sj1;
