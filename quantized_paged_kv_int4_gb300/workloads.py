@@ -81,6 +81,13 @@ def turboquant_fp8(value_bits=4, seed=0):
                       num_splits=0, seed=seed, extra={"value_bits": value_bits})
 
 
+def turboquant_mse(key_bits=3, value_bits=4, seed=0):
+    """B=64, Hq=32, Hk=8, D=128, seq_len 4096, MSE keys (key_bits-bit centroid indices + fp16
+    norm) + 4-bit (or 3-bit) values."""
+    return DecodeCase("turboquant_mse_k%dv%d" % (key_bits, value_bits), 64, 32, 8, 128, [4096] * 64,
+                      num_splits=0, seed=seed, extra={"key_bits": key_bits, "value_bits": value_bits})
+
+
 # ----------------------------------------------------------------------------
 # paged layout
 # ----------------------------------------------------------------------------
@@ -278,3 +285,62 @@ def to_numpy_f32(t):
 
 def as_u32(t):
     return np.ascontiguousarray(t.detach().to("cpu").view(torch.int32).numpy().view(np.uint32))
+
+
+# ----------------------------------------------------------------------------
+# TurboQuant MSE-key slots (synthetic codebook, rotation and cache bytes)
+# ----------------------------------------------------------------------------
+
+
+def turboquant_mse_layout(D, key_bits, value_bits):
+    """(mse_bytes, key_packed_size, slot_bytes): key_bits-bit indices, the fp16 norm right after
+    them (no QJL bytes), the values from key_packed_size = mse_bytes + 2, then fp16 scale and
+    zero; the slot padded to a multiple of 16 bytes."""
+    mse = -(-D * key_bits // 8)
+    kps = mse + 2
+    raw = kps + (-(-D * value_bits // 8)) + 4
+    return mse, kps, -(-raw // 16) * 16
+
+
+def mse_codebook(key_bits, D):
+    """A synthetic centroid table [2^key_bits] float32: the N(0, 1/D) quantiles at the bin
+    midpoints (j + 1/2) / 2^key_bits (no trained codebook is on the pages)."""
+    n = 1 << key_bits
+    p = (torch.arange(n, dtype=torch.float64) + 0.5) / n
+    return (torch.special.ndtri(p) / np.sqrt(D)).to(torch.float32)
+
+
+def random_rotation(D, seed):
+    """A seeded random orthogonal [D, D] float32 matrix (QR of a Gaussian draw, signs fixed)."""
+    a = torch.randn((D, D), generator=_gen(seed, 10), dtype=torch.float64)
+    qm, r = torch.linalg.qr(a)
+    return (qm * torch.sign(torch.diagonal(r))[None, :]).to(torch.float32)
+
+
+def _pack_lsb_stream(idx, bits, nbytes):
+    """[..., D] indices -> [..., nbytes] LSB-first bit stream (index d at bit bits * d)."""
+    out = torch.zeros(idx.shape[:-1] + (nbytes,), dtype=torch.int64)
+    for d in range(idx.shape[-1]):
+        bit = bits * d
+        out[..., bit // 8] |= (idx[..., d] << (bit % 8)) & 0xFF
+        if bit % 8 + bits > 8:
+            out[..., bit // 8 + 1] |= idx[..., d] >> (8 - bit % 8)
+    return out.to(torch.uint8)
+
+
+def random_turboquant_mse_slots(n_slots_shape, D, key_bits, value_bits, seed):
+    """Synthetic MSE-key slots [..., slot_bytes] uint8: uniform random key indices, fp16 norms
+    |N(0, 1)| * sqrt(D) / 2 + 1, values as random_turboquant_slots (min/max grid)."""
+    shape = tuple(n_slots_shape)
+    mse, kps, sb = turboquant_mse_layout(D, key_bits, value_bits)
+    idx = torch.randint(0, 1 << key_bits, shape + (D,), generator=_gen(seed, 2), dtype=torch.int64)
+    norms = (torch.randn(shape, generator=_gen(seed, 11), dtype=torch.float32).abs() * (np.sqrt(D) / 2) + 1.0)
+    nb = norms.to(torch.float16).view(torch.int16).to(torch.int64) & 0xFFFF
+    fp8 = random_turboquant_slots(shape, D, value_bits, seed)          # reuse its value bytes
+    vlen = -(-D * value_bits // 8) + 4
+    out = torch.zeros(shape + (sb,), dtype=torch.uint8)
+    out[..., :mse] = _pack_lsb_stream(idx, key_bits, mse)
+    out[..., mse] = (nb & 0xFF).to(torch.uint8)
+    out[..., mse + 1] = (nb >> 8).to(torch.uint8)
+    out[..., kps:kps + vlen] = fp8[..., D:D + vlen]
+    return out
