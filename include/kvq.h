@@ -228,6 +228,43 @@ KVQ_API kvq_status kvq_decode_tq(const float *q, const uint8_t *kv_cache, int32_
                          int64_t num_blocks, kvq_stream_t stream);
 
 /*
+ * kvq_decode_tq_mse -- TurboQuant decode with MSE keys. Defined by triton_turboquant_decode.py,
+ * _tq_decode_stage1 with KEY_FP8 = 0 (NORM_CORRECTION optional) and
+ * triton_turboquant_decode_attention with key_fp8 = False.
+ *
+ *   q_rot = q @ rotation^T                                    (fp32, computed by the call)
+ *   per key n (slot of kv head hq / (Hq/Hk)): idx_d = key_bits-bit field d of the LSB-first
+ *     stream at byte 0 (bits key_bits*d ..), c_d = centroids[idx_d];
+ *     with norm_correction: c = c / sqrt(sum_d c_d^2 + 1e-16);
+ *     norm = fp16 at byte MSE_BYTES = ceil(D * key_bits / 8);
+ *     S_n = attn_scale * norm * (q_rot . c)
+ *   values from byte key_packed_size: value_bits-bit indices (as kvq_decode_tq), fp16 scale and
+ *   zero right after the ceil(D * value_bits / 8) value bytes; v = idx * scale + zero
+ *   out[b][hq] = sum_n softmax_n(S_n) v_n  (fp32; zero rows for seq_lens[b] == 0)
+ *
+ *   q             fp32 [B, Hq, D] (the original query), 16-byte aligned.
+ *   rotation      fp32 [D, D] (Pi), 16-byte aligned.   centroids  fp32 [2^key_bits].
+ *   kv_cache      uint8 [num_blocks, 16, Hk, slot_bytes]; slot_bytes a multiple of 16, at most 512,
+ *                 >= key_packed_size + ceil(D * value_bits / 8) + 4.
+ *   key_bits, value_bits  3 or 4.   key_packed_size  even, >= MSE_BYTES + 2.
+ *   workspace     >= kvq_decode_tq_mse_workspace_bytes(...) bytes, 256-byte aligned (holds q_rot
+ *                 and the split partials); contents need no initialisation.
+ *   Supported: D in {64, 128}; Hq / Hk <= 8; block_size 16. Errors as kvq_decode_tq.
+ * Numerics: centroids and q_rot enter the tensor cores as fp16 hi + lo pairs (three products per
+ * step, ~22 bits), fp32 accumulation; within 2e-3 abs / 1e-2 rel of the float64 definition.
+ */
+KVQ_API size_t kvq_decode_tq_mse_workspace_bytes(int32_t B, int32_t Hq, int32_t Hk, int32_t D,
+                                         int32_t num_splits);
+
+KVQ_API kvq_status kvq_decode_tq_mse(const float *q, const float *rotation, const float *centroids,
+                             const uint8_t *kv_cache, int32_t slot_bytes, int32_t key_bits,
+                             int32_t key_packed_size, int32_t value_bits, int32_t norm_correction,
+                             const int32_t *block_table, int32_t max_blocks, const int32_t *seq_lens,
+                             float attn_scale, int32_t num_splits, void *workspace,
+                             size_t workspace_bytes, float *out, int32_t B, int32_t Hq, int32_t Hk,
+                             int32_t D, int32_t block_size, int64_t num_blocks, kvq_stream_t stream);
+
+/*
  * kvq_fwht128 -- fused normalised Walsh-Hadamard-128 rotation + per-row power-of-two FP8 quant.
  * Defined by kpool_compress.py, fwht128_quant_fp8 and _fwht_quant_kernel.
  *   x = bf16(FWHT128(row) * fp32(0.08838834764831845));  a = max(max |x|, 1e-4)

@@ -1,0 +1,501 @@
+// kvq_decode_tq_mse: split-KV paged decode attention over the TurboQuant combined slot with MSE
+// keys (key_bits-bit centroid indices + an fp16 norm) and 4-bit or 3-bit uniform values.
+//
+// Follows triton_turboquant_decode.py, _tq_decode_stage1 with KEY_FP8 = 0 and
+// triton_turboquant_decode_attention with key_fp8 = False: q_rot = q @ Pi^T (the launcher's
+// GEMM; here rotate_q_kernel, fp32), per key the LSB-first index stream from byte 0 of the slot,
+// the centroid gather c_d = centroids[idx_d], with NORM_CORRECTION c / sqrt(sum c^2 + 1e-16), the
+// fp16 norm at byte MSE_BYTES, score = ATTN_SCALE * norm * (q_rot . c); the values start at byte
+// key_packed_size (KPS) and dequantize as idx * scale + zero like the FP8-key layout; the splits
+// are merged by log-sum-exp (decode_common.cuh).
+//
+// GB300 design: the FP8-key kernel's structure (one warp per kv head and run of pages, private
+// cp.async ring, mma.m16n8k16 for both contractions), with whole slots staged: KPS is usually not
+// a multiple of 4 (MSE_BYTES + 2), so each stage row is the slot's bytes and the fields are read
+// from shared memory at any byte offset (aligned words + funnel shifts). A centroid goes to the
+// tensor cores as an fp16 pair hi + lo (one 32-bit table word per centroid in shared memory, so a
+// gather is one conflict-free load); q as fp16 hi + lo as in the FP8 path; three MMAs per k-step
+// (hi.hi, hi.lo, lo.hi) keep ~22 bits of the product.
+
+#include "decode_common.cuh"
+#include "kvq_host.h"
+
+namespace kvq {
+
+__device__ unsigned g_flags_decode_tq_mse = 0;
+
+struct TqMseParams {
+  SplitArgs s;
+  const float *q_rot;      // [B, Hq, D] fp32 (written by rotate_q_kernel into the workspace)
+  const uint8_t *cache;
+  const int32_t *block_table;
+  const float *centroids;  // [2^key_bits]
+  int32_t slot_bytes, kps, norm_correction;
+  float sc_log2;           // attn_scale * log2(e)
+  int64_t num_blocks;
+};
+
+constexpr uint32_t kLoMse = 0x000F000Fu;
+constexpr uint32_t kHiMse = 0x00F000F0u;
+
+template <int D, int KB, int VB>
+struct MseGeom {
+  static constexpr int MSE = (D * KB + 7) / 8;      // MSE_BYTES
+  static constexpr int KCH = D / 4;                 // dims per lane (t) in the score MMA's k order
+  static constexpr int KW = (KCH * KB + 31) / 32;   // index words per lane and row
+  static constexpr int VDB = (D * VB + 7) / 8;
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int MT = D / 16;
+  static constexpr int QBYTES = 2 * 8 * D * 2;      // fp16 hi and lo
+  static constexpr int TABLE = 64 + 64;             // 16 (hi | lo) words, 16 fp32 squares
+};
+
+// Stage row stride for slot_bytes SB: a multiple of 16 (cp.async destination) whose word stride
+// is 4 mod 8 (rows g and g + 8 of a fragment fall in different banks).
+__host__ __device__ inline int mse_row_stride(int SB) {
+  int rs = (SB + 15) / 16 * 16;
+  while (((rs / 4) & 7) != 4) rs += 16;
+  return rs;
+}
+
+// 32 bits of a shared-memory row starting at any byte offset o (two aligned words, funnel shift)
+__device__ __forceinline__ uint32_t lds32_at(const uint8_t *row, int o) {
+  const uint32_t *w = reinterpret_cast<const uint32_t *>(row + (o & ~3));
+  return __funnelshift_r(w[0], w[1], 8 * (o & 3));
+}
+
+__device__ __forceinline__ uint32_t lds16_at(const uint8_t *row, int o) {
+  return *reinterpret_cast<const uint16_t *>(row + o);  // o even
+}
+
+// q_rot[r][d] = sum_e q[r][e] * Pi[d][e] (fp32) for 32 rows per CTA, one output dim per thread.
+template <int D>
+__global__ void __launch_bounds__(D) rotate_q_kernel(const float *__restrict__ q, const float *__restrict__ Pi,
+                                                     float *__restrict__ q_rot, long long rows) {
+  constexpr int R = 32;
+  __shared__ __align__(16) float s_q[R][D];
+  const long long r0 = static_cast<long long>(blockIdx.x) * R;
+  const int d = threadIdx.x;
+  for (int i = d; i < R * D; i += D) {
+    const long long r = r0 + i / D;
+    s_q[i / D][i % D] = r < rows ? q[r * D + i % D] : 0.f;
+  }
+  __syncthreads();
+  float acc[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) acc[r] = 0.f;
+  const float4 *pr = reinterpret_cast<const float4 *>(Pi + static_cast<long long>(d) * D);
+  for (int e4 = 0; e4 < D / 4; ++e4) {
+    const float4 pv = __ldg(pr + e4);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const float4 qv = *reinterpret_cast<const float4 *>(&s_q[r][4 * e4]);
+      acc[r] = fmaf(qv.x, pv.x, acc[r]);
+      acc[r] = fmaf(qv.y, pv.y, acc[r]);
+      acc[r] = fmaf(qv.z, pv.z, acc[r]);
+      acc[r] = fmaf(qv.w, pv.w, acc[r]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+    if (r0 + r < rows) q_rot[(r0 + r) * D + d] = acc[r];
+}
+
+template <int D, int KB, int VB, int NSTAGE>
+__device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring, uint8_t *qarea,
+                                             const uint32_t *table, const float *sq, int RS, int b, int h,
+                                             int sub, int t0, int t1, long long slot) {
+  using Gm = MseGeom<D, KB, VB>;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int G = p.s.G, WPH = p.s.warps_per_head, Hk = p.s.Hk;
+  const int SB = p.slot_bytes, KPS = p.kps;
+  const int STAGE = kPage * RS;
+
+  const int pg0 = t0 / kPage, pglast = (t1 - 1) / kPage;
+  const int first = pg0 + sub;
+  const int n_my = first <= pglast ? (pglast - first) / WPH + 1 : 0;
+  const int32_t *bt_row = p.block_table + static_cast<long long>(b) * p.s.max_blocks;
+  auto load_bids = [&](int batch) -> int {
+    const int k = batch * 32 + lane;
+    return k < n_my ? __ldg(bt_row + first + k * WPH) : 0;
+  };
+  int bids_cur = load_bids(0);
+  int bids_next = load_bids(1);
+
+  // -------- q_rot -> fp16 hi / lo parts in shared memory, then B fragments
+  {
+    constexpr int J = D / 32;
+    const float *qb = p.q_rot + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(h) * G) * D;
+    __half *qh = reinterpret_cast<__half *>(qarea);
+    for (int n = 0; n < 8; ++n) {
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const int e = lane + 32 * j;
+        const float x = n < G ? qb[n * D + e] : 0.f;
+        const __half hi = __float2half_rn(x);
+        qh[n * D + e] = hi;
+        qh[8 * D + n * D + e] = __float2half_rn(x - __half2float(hi));
+      }
+    }
+  }
+  __syncwarp();
+  uint32_t qhi[Gm::KSTEPS][2], qlo[Gm::KSTEPS][2];
+  {
+    const __half *qh = reinterpret_cast<const __half *>(qarea) + g * D + t * Gm::KCH;
+#pragma unroll
+    for (int ks = 0; ks < Gm::KSTEPS; ++ks) {
+      const __half *r = qh + 4 * ks;
+      qhi[ks][0] = h2_as_u32(__halves2half2(r[0], r[1]));
+      qhi[ks][1] = h2_as_u32(__halves2half2(r[2], r[3]));
+      qlo[ks][0] = h2_as_u32(__halves2half2(r[8 * D + 0], r[8 * D + 1]));
+      qlo[ks][1] = h2_as_u32(__halves2half2(r[8 * D + 2], r[8 * D + 3]));
+    }
+  }
+  __syncwarp();
+
+  const uint32_t ring_s = smem_u32(ring);
+  const long long row_stride = static_cast<long long>(Hk) * SB;
+  const long long page_bytes = kPage * row_stride;
+  const uint8_t *head = p.cache + static_cast<long long>(h) * SB;
+  const int chunks = SB / 16;  // 16-byte pieces of one slot
+  auto issue = [&](int k) {
+    const int kk = k & 31;
+    if (k > 0 && kk == 0) {
+      bids_cur = bids_next;
+      bids_next = load_bids((k >> 5) + 1);
+    }
+    const int blk = __shfl_sync(FULL, bids_cur, kk);
+    const bool in = k < n_my;
+    const bool ok = in && blk >= 0 && blk < p.num_blocks;
+    if (in && !ok && lane == 0) atomicOr(&g_flags_decode_tq_mse, ERR_BLOCK);
+    const uint32_t st = ring_s + (k % NSTAGE) * STAGE;
+    const uint8_t *base = head + static_cast<long long>(ok ? blk : 0) * page_bytes;
+    for (int i = lane; i < kPage * chunks; i += 32) {
+      const int r = i / chunks, c = i - r * chunks;
+      cp_async<16>(st + r * RS + 16 * c, base + r * row_stride + 16 * c, ok);
+    }
+    cp_async_commit();
+  };
+
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float pz0 = 0.f, pz1 = 0.f;
+  float acc[Gm::MT][4];
+#pragma unroll
+  for (int i = 0; i < Gm::MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+#pragma unroll
+  for (int k = 0; k < NSTAGE - 1; ++k) issue(k);
+
+  for (int k = 0; k < n_my; ++k) {
+    issue(k + NSTAGE - 1);
+    cp_async_wait<NSTAGE - 1>();
+    __syncwarp();
+    const uint8_t *st = ring + (k % NSTAGE) * STAGE;
+    const int nb = (first + k * WPH) * kPage;
+    const bool ok0 = nb + g >= t0 && nb + g < t1;
+    const bool ok1 = nb + g + 8 >= t0 && nb + g + 8 < t1;
+    const uint8_t *row0 = st + g * RS, *row1 = st + (g + 8) * RS;
+
+    // ---- scores: the lane's KCH dims of rows g, g + 8 as centroid hi / lo fp16 pairs
+    uint32_t w0[Gm::KW + 1], w1[Gm::KW + 1];
+#pragma unroll
+    for (int i = 0; i < Gm::KW; ++i) {
+      w0[i] = lds32_at(row0, t * (Gm::KCH * KB / 8) + 4 * i);
+      w1[i] = lds32_at(row1, t * (Gm::KCH * KB / 8) + 4 * i);
+    }
+    w0[Gm::KW] = w1[Gm::KW] = 0u;
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    float ss0 = 0.f, ss1 = 0.f;  // sum of c^2 over the lane's dims (NORM_CORRECTION)
+#pragma unroll
+    for (int ks = 0; ks < Gm::KSTEPS; ++ks) {
+      uint32_t e0[4], e1[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int bit = (4 * ks + j) * KB, wi = bit >> 5, sh = bit & 31;
+        const uint32_t i0 = __funnelshift_r(w0[wi], w0[wi + 1], sh) & ((1u << KB) - 1);
+        const uint32_t i1 = __funnelshift_r(w1[wi], w1[wi + 1], sh) & ((1u << KB) - 1);
+        e0[j] = table[i0];
+        e1[j] = table[i1];
+        if (p.norm_correction) {
+          ss0 += sq[i0];
+          ss1 += sq[i1];
+        }
+      }
+      const uint32_t h00 = __byte_perm(e0[0], e0[1], 0x5410), h02 = __byte_perm(e0[2], e0[3], 0x5410);
+      const uint32_t h10 = __byte_perm(e1[0], e1[1], 0x5410), h12 = __byte_perm(e1[2], e1[3], 0x5410);
+      const uint32_t l00 = __byte_perm(e0[0], e0[1], 0x7632), l02 = __byte_perm(e0[2], e0[3], 0x7632);
+      const uint32_t l10 = __byte_perm(e1[0], e1[1], 0x7632), l12 = __byte_perm(e1[2], e1[3], 0x7632);
+      mma_f16_16816(c, h00, h10, h02, h12, qhi[ks][0], qhi[ks][1]);
+      mma_f16_16816(c, h00, h10, h02, h12, qlo[ks][0], qlo[ks][1]);
+      mma_f16_16816(c, l00, l10, l02, l12, qhi[ks][0], qhi[ks][1]);
+    }
+    // per-token factor: attn_scale * log2(e) * norm (/ |c| under NORM_CORRECTION)
+    float f0 = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16_at(row0, Gm::MSE)))) * p.sc_log2;
+    float f1 = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16_at(row1, Gm::MSE)))) * p.sc_log2;
+    if (p.norm_correction) {
+      ss0 += __shfl_xor_sync(FULL, ss0, 1);
+      ss0 += __shfl_xor_sync(FULL, ss0, 2);
+      ss1 += __shfl_xor_sync(FULL, ss1, 1);
+      ss1 += __shfl_xor_sync(FULL, ss1, 2);
+      f0 *= rsqrtf(ss0 + 1e-16f);
+      f1 *= rsqrtf(ss1 + 1e-16f);
+    }
+    const float s00 = ok0 ? c[0] * f0 : -INFINITY;
+    const float s01 = ok0 ? c[1] * f0 : -INFINITY;
+    const float s10 = ok1 ? c[2] * f1 : -INFINITY;
+    const float s11 = ok1 ? c[3] * f1 : -INFINITY;
+
+    const float mx0 = fmaxf(m0, warp_max_g(fmaxf(s00, s10)));
+    const float mx1 = fmaxf(m1, warp_max_g(fmaxf(s01, s11)));
+    const float r0 = mx0 == -INFINITY ? 0.f : mx0, r1 = mx1 == -INFINITY ? 0.f : mx1;
+    const float al0 = fast_exp2(m0 - r0), al1 = fast_exp2(m1 - r1);
+    m0 = mx0;
+    m1 = mx1;
+    const float p00 = fast_exp2(s00 - r0), p10 = fast_exp2(s10 - r0);
+    const float p01 = fast_exp2(s01 - r1), p11 = fast_exp2(s11 - r1);
+    l0 = l0 * al0 + (p00 + p10);
+    l1 = l1 * al1 + (p01 + p11);
+
+    // value scale and zero of tokens g, g + 8 (fp16 pair at KPS + VDB)
+    const uint32_t sz0 = lds32_at(row0, KPS + Gm::VDB), sz1 = lds32_at(row1, KPS + Gm::VDB);
+    const float2 szf0 = __half22float2(u32_as_h2(sz0)), szf1 = __half22float2(u32_as_h2(sz1));
+    const __half2 X0 = __floats2half2_rn(ok0 ? p00 * szf0.x : 0.f, ok1 ? p10 * szf1.x : 0.f);
+    const __half2 X1 = __floats2half2_rn(ok0 ? p01 * szf0.x : 0.f, ok1 ? p11 * szf1.x : 0.f);
+    pz0 = pz0 * al0 + ((ok0 ? p00 * szf0.y : 0.f) + (ok1 ? p10 * szf1.y : 0.f));
+    pz1 = pz1 * al1 + ((ok0 ? p01 * szf0.y : 0.f) + (ok1 ? p11 * szf1.y : 0.f));
+    if (!__all_sync(FULL, al0 == 1.f && al1 == 1.f)) {  // a running max moved: rescale
+#pragma unroll
+      for (int i = 0; i < Gm::MT; ++i) {
+        acc[i][0] *= al0;
+        acc[i][1] *= al1;
+        acc[i][2] *= al0;
+        acc[i][3] *= al1;
+      }
+    }
+    const int src0 = 8 * t + (g >> 1), src1 = src0 + 4;
+    const uint32_t x0 = h2_as_u32(X0), x1 = h2_as_u32(X1);
+    const uint32_t y0 = __shfl_sync(FULL, x0, src0), y1 = __shfl_sync(FULL, x1, src0);
+    const uint32_t z0 = __shfl_sync(FULL, x0, src1), z1 = __shfl_sync(FULL, x1, src1);
+    const uint32_t ya = (g & 1) ? y1 : y0, za = (g & 1) ? z1 : z0;
+    const uint32_t b01 = __byte_perm(ya, za, 0x5410), b23 = __byte_perm(ya, za, 0x7632);
+
+    // ---- O^T += V^T . P_v^T over tokens 2t, 2t+1, 2t+8, 2t+9 (rows of this stage)
+    const uint8_t *ra = st + (2 * t) * RS, *rb = ra + RS, *rc = ra + 8 * RS, *rd = ra + 9 * RS;
+    if constexpr (VB == 4) {
+      constexpr int VW = D / 64;  // value words per lane per token (dims 8 g .. of D / 8 per lane)
+#pragma unroll
+      for (int wi = 0; wi < VW; ++wi) {
+        const int o = KPS + g * (D / 16) + 4 * wi;
+        const uint32_t va = lds32_at(ra, o), vb = lds32_at(rb, o), vc = lds32_at(rc, o), vd = lds32_at(rd, o);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const uint32_t sel = hf ? 0x7632u : 0x5410u;
+          const uint32_t x = __byte_perm(va, vb, sel), y = __byte_perm(vc, vd, sel);
+          const int mt = 4 * wi + 2 * hf;
+          mma_f16_16816(acc[mt], x & kLoMse, x & kHiMse, y & kLoMse, y & kHiMse, b01, b23);
+          const uint32_t x8 = x >> 8, y8 = y >> 8;
+          mma_f16_16816(acc[mt + 1], x8 & kLoMse, x8 & kHiMse, y8 & kLoMse, y8 & kHiMse, b01, b23);
+        }
+      }
+    } else {
+      // 3-bit: the lane's D/8 indices per token, LSB first, from bit 3 (D/8) g of the value data
+      constexpr int kV3Bytes = 3 * D / 64;
+      const int off = KPS + kV3Bytes * g;
+      unsigned long long w[4];
+      const uint8_t *rows[4] = {ra, rb, rc, rd};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = lds32_at(rows[i], off), hi = lds32_at(rows[i], off + 4);
+        w[i] = (static_cast<unsigned long long>(hi) << 32) | lo;
+      }
+#pragma unroll
+      for (int mt = 0; mt < Gm::MT; ++mt) {
+        uint32_t a[4];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int bit = 3 * (2 * mt + r);
+#pragma unroll
+          for (int tp = 0; tp < 2; ++tp) {
+            const uint32_t lo = static_cast<uint32_t>(w[2 * tp] >> bit) & 7u;
+            const uint32_t hi = static_cast<uint32_t>(w[2 * tp + 1] >> bit) & 7u;
+            a[2 * tp + r] = lo | (hi << 16);
+          }
+        }
+        mma_f16_16816(acc[mt], a[0], a[1], a[2], a[3], b01, b23);
+      }
+    }
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+  __syncwarp();
+
+  l0 = warp_sum_g(l0);
+  l1 = warp_sum_g(l1);
+  pz0 = warp_sum_g(pz0);
+  pz1 = warp_sum_g(pz1);
+  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+  constexpr float hs = VB == 4 ? 1048576.f : 16777216.f;  // 2^20: high nibbles enter 16x larger
+  float o0[D / 8], o1[D / 8];
+#pragma unroll
+  for (int mt = 0; mt < Gm::MT; ++mt) {
+    o0[2 * mt] = (acc[mt][0] * 16777216.f + pz0) * inv0;
+    o1[2 * mt] = (acc[mt][1] * 16777216.f + pz1) * inv1;
+    o0[2 * mt + 1] = (acc[mt][2] * hs + pz0) * inv0;
+    o1[2 * mt + 1] = (acc[mt][3] * hs + pz1) * inv1;
+  }
+  const float lse0 = l0 > 0.f ? m0 + log2f(l0) : -INFINITY;
+  const float lse1 = l1 > 0.f ? m1 + log2f(l1) : -INFINITY;
+  store_partial<D>(p.s, slot, sub, h, lane, o0, o1, lse0, lse1);
+}
+
+template <int D, int KB, int VB, int NSTAGE>
+__global__ void __launch_bounds__(256, 2) decode_tq_mse_kernel(const TqMseParams p, int RS) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  asm volatile("griddepcontrol.launch_dependents;");  // let the merge kernel's launch begin early
+  using Gm = MseGeom<D, KB, VB>;
+  const int warp = threadIdx.x >> 5;
+  // the centroid table: word j = fp16 hi | fp16 lo << 16 of centroid j, then the fp32 squares
+  uint32_t *table = reinterpret_cast<uint32_t *>(smem);
+  float *sq = reinterpret_cast<float *>(smem + 64);
+  if (threadIdx.x < (1 << KB)) {
+    const float cv = __ldg(p.centroids + threadIdx.x);
+    const __half hi = __float2half_rn(cv);
+    const __half lo = __float2half_rn(cv - __half2float(hi));
+    table[threadIdx.x] = static_cast<uint32_t>(__half_as_ushort(hi)) |
+                         (static_cast<uint32_t>(__half_as_ushort(lo)) << 16);
+    sq[threadIdx.x] = cv * cv;
+  }
+  __syncthreads();
+  uint8_t *ring = smem + Gm::TABLE + warp * (NSTAGE * kPage * RS + Gm::QBYTES);
+  uint8_t *qarea = ring + NSTAGE * kPage * RS;
+  const int hl = warp % p.s.heads_per_cta;
+  const int sub = warp / p.s.heads_per_cta;
+  const int h = blockIdx.y * p.s.heads_per_cta + hl;
+  for_each_piece(p.s, &g_flags_decode_tq_mse, [&](int b, int t0, int t1, long long slot) {
+    tq_mse_piece<D, KB, VB, NSTAGE>(p, ring, qarea, table, sq, RS, b, h, sub, t0, t1, slot);
+  });
+}
+
+constexpr int kStagesMse = 3;
+
+bool take_flags_decode_tq_mse(cudaStream_t stream, unsigned *host_word) {
+  static const unsigned zero = 0;
+  if (cudaMemcpyFromSymbolAsync(host_word, g_flags_decode_tq_mse, sizeof(unsigned), 0,
+                                cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return false;
+  return cudaMemcpyToSymbolAsync(g_flags_decode_tq_mse, &zero, sizeof(unsigned), 0,
+                                 cudaMemcpyHostToDevice, stream) == cudaSuccess;
+}
+
+template <int D, int KB, int VB>
+static kvq_status launch_tq_mse(const TqMseParams &p, const SplitPlan &plan, const float *q, const float *Pi,
+                                float *q_rot, cudaStream_t s) {
+  using Gm = MseGeom<D, KB, VB>;
+  const int RS = mse_row_stride(p.slot_bytes);
+  const size_t smem = Gm::TABLE + 8 * static_cast<size_t>(kStagesMse * kPage * RS + Gm::QBYTES);
+  if (smem > 227 * 1024) return KVQ_ERR_UNSUPPORTED;
+  static size_t attr_bytes = 0;  // the largest dynamic size set so far for this instantiation
+  if (smem > attr_bytes) {
+    if (cudaFuncSetAttribute(decode_tq_mse_kernel<D, KB, VB, kStagesMse>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+    attr_bytes = smem;
+  }
+  const long long rows = static_cast<long long>(p.s.B) * p.s.Hq;
+  rotate_q_kernel<D><<<static_cast<unsigned>((rows + 31) / 32), D, 0, s>>>(q, Pi, q_rot, rows);
+  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  const dim3 grid(plan.seg_ctas, plan.head_groups);
+  decode_tq_mse_kernel<D, KB, VB, kStagesMse><<<grid, 256, smem, s>>>(p, RS);
+  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  if (launch_dependent(merge_kernel<D>, dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), s, p.s) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  return launch_status();
+}
+
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" size_t kvq_decode_tq_mse_workspace_bytes(int32_t B, int32_t Hq, int32_t Hk, int32_t D,
+                                                    int32_t num_splits) {
+  if (B < 0 || Hq < 1 || Hk < 1 || Hq % Hk || (D != 64 && D != 128)) return 0;
+  SplitPlan plan;
+  if (!make_plan(B, Hk, num_splits, &plan)) return 0;
+  const size_t qbytes = (static_cast<size_t>(B) * Hq * D * sizeof(float) + 255) / 256 * 256;
+  return qbytes + workspace_bytes(B, Hq, D, plan);
+}
+
+extern "C" kvq_status kvq_decode_tq_mse(const float *q, const float *rotation, const float *centroids,
+                                        const uint8_t *kv_cache, int32_t slot_bytes, int32_t key_bits,
+                                        int32_t key_packed_size, int32_t value_bits, int32_t norm_correction,
+                                        const int32_t *block_table, int32_t max_blocks, const int32_t *seq_lens,
+                                        float attn_scale, int32_t num_splits, void *workspace,
+                                        size_t workspace_bytes_, float *out, int32_t B, int32_t Hq, int32_t Hk,
+                                        int32_t D, int32_t block_size, int64_t num_blocks,
+                                        kvq_stream_t stream) {
+  if (B < 0 || Hq < 1 || Hk < 1 || max_blocks < 0 || num_splits < 0 || num_blocks < 1)
+    return KVQ_ERR_INVALID_ARG;
+  if (Hq % Hk != 0) return KVQ_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return KVQ_ERR_UNSUPPORTED;
+  if ((key_bits != 3 && key_bits != 4) || (value_bits != 3 && value_bits != 4)) return KVQ_ERR_UNSUPPORTED;
+  if (block_size != kPage || Hq / Hk > 8) return KVQ_ERR_UNSUPPORTED;
+  const int mse = (D * key_bits + 7) / 8, vdb = (D * value_bits + 7) / 8;
+  if (key_packed_size < mse + 2 || key_packed_size % 2 != 0) return KVQ_ERR_INVALID_ARG;
+  if (slot_bytes % 16 != 0 || slot_bytes < key_packed_size + vdb + 4 || slot_bytes > 512) return KVQ_ERR_INVALID_ARG;
+  if (!(attn_scale > 0.f) || !(attn_scale < INFINITY)) return KVQ_ERR_INVALID_ARG;
+  SplitPlan plan;
+  if (!make_plan(B, Hk, num_splits, &plan)) return KVQ_ERR_UNSUPPORTED;
+  if (B == 0) return KVQ_OK;
+  if (!q || !rotation || !centroids || !kv_cache || !block_table || !seq_lens || !out || !workspace)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(rotation, 16) || !aligned(centroids, 4) || !aligned(kv_cache, 16) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(out, 16) || !aligned(workspace, 256))
+    return KVQ_ERR_INVALID_ARG;
+  if (max_blocks < 1) return KVQ_ERR_INVALID_ARG;
+  if (workspace_bytes_ < kvq_decode_tq_mse_workspace_bytes(B, Hq, Hk, D, num_splits)) return KVQ_ERR_WORKSPACE;
+
+  float *q_rot = static_cast<float *>(workspace);
+  void *rest = static_cast<uint8_t *>(workspace) + (static_cast<size_t>(B) * Hq * D * sizeof(float) + 255) / 256 * 256;
+  TqMseParams p;
+  SplitArgs &sa = p.s;
+  sa.seq_lens = seq_lens;
+  sa.max_blocks = max_blocks;
+  sa.num_splits = num_splits;
+  sa.B = B;
+  sa.Hq = Hq;
+  sa.Hk = Hk;
+  sa.G = Hq / Hk;
+  sa.heads_per_cta = plan.heads_per_cta;
+  sa.warps_per_head = plan.warps_per_head;
+  sa.seg_ctas = plan.seg_ctas;
+  sa.slots = plan.slots;
+  workspace_carve(rest, B, Hq, D, plan, &sa.part_o, &sa.part_lse, &sa.seg_first, &sa.seg_last);
+  sa.signs = nullptr;
+  sa.window = 0;
+  sa.sinks = nullptr;
+  sa.out = out;
+  sa.out_dtype = KVQ_F32;
+  p.q_rot = q_rot;
+  p.cache = kv_cache;
+  p.block_table = block_table;
+  p.centroids = centroids;
+  p.slot_bytes = slot_bytes;
+  p.kps = key_packed_size;
+  p.norm_correction = norm_correction != 0;
+  p.sc_log2 = static_cast<float>(static_cast<double>(attn_scale) * 1.4426950408889634);
+  p.num_blocks = num_blocks;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+#define KVQ_MSE_CASE(DD, KK, VV) \
+  if (D == DD && key_bits == KK && value_bits == VV) return launch_tq_mse<DD, KK, VV>(p, plan, q, rotation, q_rot, s);
+  KVQ_MSE_CASE(128, 3, 4)
+  KVQ_MSE_CASE(128, 4, 4)
+  KVQ_MSE_CASE(128, 3, 3)
+  KVQ_MSE_CASE(128, 4, 3)
+  KVQ_MSE_CASE(64, 3, 4)
+  KVQ_MSE_CASE(64, 4, 4)
+  KVQ_MSE_CASE(64, 3, 3)
+  KVQ_MSE_CASE(64, 4, 3)
+#undef KVQ_MSE_CASE
+  return KVQ_ERR_UNSUPPORTED;
+}

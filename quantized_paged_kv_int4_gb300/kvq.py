@@ -25,7 +25,7 @@ KVQ_BF16, KVQ_F16, KVQ_F32 = 0, 1, 2
 # the C API's declared functions, in header order
 C_FUNCTIONS = ("kvq_status_string", "kvq_abi_version", "kvq_write_int4", "kvq_decode_workspace_bytes",
                "kvq_decode_int4", "kvq_decode_int4_mods", "kvq_decode_int4_noalloc", "kvq_decode_tq",
-               "kvq_fwht128", "kvq_device_error")
+               "kvq_decode_tq_mse_workspace_bytes", "kvq_decode_tq_mse", "kvq_fwht128", "kvq_device_error")
 KVQ_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lock = threading.Lock()
@@ -54,6 +54,10 @@ _SIGS = {
                                                ctypes.c_int, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_p]),
     "kvq_decode_tq": (ctypes.c_int, [c_p, c_p, c_i32, c_i32, c_p, c_i32, c_p, c_f32, c_i32, c_p, c_sz, c_p,
                                      c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_p]),
+    "kvq_decode_tq_mse_workspace_bytes": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32]),
+    "kvq_decode_tq_mse": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_i32, c_i32, c_i32, c_i32, c_i32, c_p, c_i32, c_p,
+                                         c_f32, c_i32, c_p, c_sz, c_p, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64,
+                                         c_p]),
     "kvq_fwht128": (ctypes.c_int, [c_p, c_p, c_p, c_i64, c_p]),
     "kvq_device_error": (ctypes.c_int, [c_p, ctypes.POINTER(ctypes.c_uint32)]),
 }
@@ -252,6 +256,39 @@ def kvq_decode_tq(q, kv_cache, value_bits, block_table, seq_lens, attn_scale, ou
                                _ptr(workspace), workspace.numel(), _ptr(out), B, Hq, Hk, D, bs, nb,
                                _stream(stream)),
            "kvq_decode_tq")
+    return out
+
+
+def kvq_decode_tq_mse_workspace_bytes(B, Hq, Hk, D, num_splits=0):
+    return int(lib().kvq_decode_tq_mse_workspace_bytes(B, Hq, Hk, D, num_splits))
+
+
+def kvq_decode_tq_mse(q, rotation, centroids, kv_cache, key_bits, key_packed_size, value_bits, block_table,
+                      seq_lens, attn_scale, norm_correction=False, out=None, workspace=None, num_splits=0,
+                      stream=None):
+    """TurboQuant decode with MSE keys: q [B, Hq, D] fp32 (original query), rotation [D, D] fp32 (Pi),
+    centroids [2^key_bits] fp32, kv_cache [nb, 16, Hk, slot_bytes] uint8."""
+    _need(q, "q", torch.float32)
+    _need(rotation, "rotation", torch.float32)
+    _need(centroids, "centroids", torch.float32)
+    _need(kv_cache, "kv_cache", torch.uint8)
+    _need(block_table, "block_table", torch.int32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    B, Hq, D = q.shape
+    nb, bs, Hk, slot_bytes = kv_cache.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32)
+    if workspace is None:
+        workspace = torch.empty((max(kvq_decode_tq_mse_workspace_bytes(B, Hq, Hk, D, num_splits), 16),),
+                                dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", torch.uint8)
+    _check(lib().kvq_decode_tq_mse(_ptr(q), _ptr(rotation), _ptr(centroids), _ptr(kv_cache), slot_bytes, key_bits,
+                                   key_packed_size, value_bits, int(bool(norm_correction)), _ptr(block_table),
+                                   block_table.shape[1], _ptr(seq_lens), float(attn_scale), num_splits,
+                                   _ptr(workspace), workspace.numel(), _ptr(out), B, Hq, Hk, D, bs, nb,
+                                   _stream(stream)),
+           "kvq_decode_tq_mse")
     return out
 
 

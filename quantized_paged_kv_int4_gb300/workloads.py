@@ -314,7 +314,7 @@ def random_rotation(D, seed):
     """A seeded random orthogonal [D, D] float32 matrix (QR of a Gaussian draw, signs fixed)."""
     a = torch.randn((D, D), generator=_gen(seed, 10), dtype=torch.float64)
     qm, r = torch.linalg.qr(a)
-    return (qm * torch.sign(torch.diagonal(r))[None, :]).to(torch.float32)
+    return (qm * torch.sign(torch.diagonal(r))[None, :]).to(torch.float32).contiguous()
 
 
 def _pack_lsb_stream(idx, bits, nbytes):

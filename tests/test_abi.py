@@ -140,6 +140,31 @@ def test_tq_and_fwht_validation_without_gpu():
     assert L.kvq_fwht128(16, 16, 16, -1, None) == kvq.KVQ_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("name", ["kvq_write_int4", "kvq_decode_int4", "kvq_decode_tq", "kvq_fwht128"])
+def test_tq_mse_validation_without_gpu():
+    L = kvq.lib()
+    # q, Pi, centroids, cache, slot 128, key 3, kps 50, value 4, norm corr, bt, mb, lens, scale, S, ws, wsb,
+    # out, B, Hq, Hk, D, bs, nb, stream
+    args = [16, 16, 16, 16, 128, 3, 50, 4, 0, 16, 4, 16, ctypes.c_float(0.1), 4, 256, 1 << 30, 16, 2, 4, 2, 128,
+            16, 10, None]
+    def call(**kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return L.kvq_decode_tq_mse(*a)
+    assert call(a17=0) == kvq.KVQ_OK                          # B = 0
+    assert call(a5=5) == kvq.KVQ_ERR_UNSUPPORTED              # key bits
+    assert call(a7=8) == kvq.KVQ_ERR_UNSUPPORTED              # value bits
+    assert call(a6=49) == kvq.KVQ_ERR_INVALID_ARG             # kps odd / below MSE_BYTES + 2
+    assert call(a6=48) == kvq.KVQ_ERR_INVALID_ARG
+    assert call(a4=112) == kvq.KVQ_ERR_INVALID_ARG            # slot too small for the 4-bit values
+    assert call(a4=130) == kvq.KVQ_ERR_INVALID_ARG            # not a multiple of 16
+    assert call(a14=272) == kvq.KVQ_ERR_INVALID_ARG           # workspace not 256-byte aligned
+    assert call(a15=100) == kvq.KVQ_ERR_WORKSPACE
+    n = kvq.kvq_decode_tq_mse_workspace_bytes(2, 4, 2, 128, 4)
+    assert n == kvq.kvq_decode_workspace_bytes(2, 4, 2, 128, 4) + 2 * 4 * 128 * 4
+
+
+@pytest.mark.parametrize("name", ["kvq_write_int4", "kvq_decode_int4", "kvq_decode_tq", "kvq_decode_tq_mse",
+                                  "kvq_fwht128"])
 def test_python_binding_names_match_the_c_api(name):
     assert callable(getattr(kvq, name))
