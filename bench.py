@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--workload", default="llama3_8b_int4",
                     choices=["llama3_8b_int4", "llama3_8b_int4_mods", "long_context_int4", "turboquant_fp8_v4",
-                             "turboquant_fp8_v3", "write_fwht"])
+                             "turboquant_fp8_v3", "turboquant_mse_k3v4", "write_fwht"])
     ap.add_argument("--replicas", type=int, default=4)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -231,6 +231,8 @@ def run_kvq(args, dist):
     wl = args.workload
     if wl == "write_fwht":
         return run_write_fwht(args, dist, dev, stream)
+    if wl.startswith("turboquant_mse"):
+        return run_tq_mse(args, dist, dev, stream)
     if wl.startswith("turboquant"):
         return run_tq(args, dist, dev, stream)
     case = workloads.long_context_int4() if wl == "long_context_int4" else workloads.llama8b_int4()
@@ -434,6 +436,53 @@ def run_tq(args, dist, dev, stream):
                    "quantized_paged_kv_int4_gb300/csrc/kvq_device.cuh"], "f32")
 
 
+def run_tq_mse(args, dist, dev, stream):
+    kb, vb = 3, 4
+    case = workloads.turboquant_mse(kb, vb)
+    B, Hq, Hk, D = case.B, case.Hq, case.Hk, case.D
+    mse, kps, sb = workloads.turboquant_mse_layout(D, kb, vb)
+    bt, nb = workloads.paged_layout(case.seq_lens, 10 * dist.rank, num_blocks=None)
+    g = torch.Generator(device=dev)
+    g.manual_seed(4000 + dist.rank)
+    cache = torch.randint(0, 256, (nb, 16, Hk, sb), dtype=torch.uint8, device=dev, generator=g)
+    two = lambda x: torch.full((nb, 16, Hk), x, dtype=torch.float16, device=dev).view(torch.uint8).view(nb, 16, Hk, 2)
+    cache[..., mse:mse + 2] = two(4.0)                       # key norms
+    vdb = -(-D * vb // 8)
+    cache[..., kps + vdb:kps + vdb + 2] = two(0.05)          # value scale
+    cache[..., kps + vdb + 2:kps + vdb + 4] = 0              # value zero
+    bt = bt.to(dev)
+    lens = torch.tensor(case.seq_lens, dtype=torch.int32, device=dev)
+    q = torch.randn((B, Hq, D), device=dev, generator=g)
+    Pi = workloads.random_rotation(D, 1).to(dev)
+    cb = workloads.mse_codebook(kb, D).to(dev)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    ws = torch.zeros((kvq.kvq_decode_tq_mse_workspace_bytes(B, Hq, Hk, D, 0),), dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(D)
+
+    def decode(i):
+        kvq.kvq_decode_tq_mse(q, Pi, cb, cache, kb, kps, vb, bt, lens, scale, out=out, workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        decode(0)
+    stream.synchronize()
+    st, flags = kvq.kvq_device_error(stream)
+    assert st == 0, flags
+    gd = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gd, stream=stream):
+        decode(0)
+    res = timed_steps(args, dist, stream, lambda i: None, lambda i: gd.replay(), dev.index)
+    kvb = sum(case.seq_lens) * Hk * sb
+    byt = kvb + sum(-(-L // 16) * 4 for L in case.seq_lens) + B * Hq * D * 8 + D * D * 4 + (1 << kb) * 4
+    cfg = {"workload": args.workload, "B": B, "Hq": Hq, "Hk": Hk, "D": D, "block_size": 16, "seq_len": 4096,
+           "slot_bytes": sb, "key": "MSE %d-bit centroid indices + fp16 norm (key_packed_size %d)" % (kb, kps),
+           "value_bits": vb, "num_splits": "heuristic (balanced)",
+           "l2": "single %.0f MB cache read per step (> L2)" % (kvb / 1e6), "decode_bytes_per_step": byt}
+    return finish(args, dist, res, byt, cfg, None, 3, "decode_tq_mse_k%dv%d" % (kb, vb),
+                  ["quantized_paged_kv_int4_gb300/csrc/decode_tq_mse.cu",
+                   "quantized_paged_kv_int4_gb300/csrc/decode_common.cuh",
+                   "quantized_paged_kv_int4_gb300/csrc/kvq_device.cuh"], "f32")
+
+
 def run_write_fwht(args, dist, dev, stream):
     nrep = 4
     reps = []
@@ -504,7 +553,9 @@ def finish(args, dist, res, step_bytes, cfg, e2e, kernels_per_step, dom_tag, dom
                      else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes_per_launch": dom_b,
                      "avg_launch_us": round(dom_ms * 1e3, 3),
-                     "note": "launch = the whole library call (split-KV kernel + LSE merge kernel)"
+                     "note": ("launch = the whole library call (q rotation, split-KV kernel, LSE merge kernel)"
+                              if dom_tag.startswith("decode_tq_mse") else
+                              "launch = the whole library call (split-KV kernel + LSE merge kernel)")
                      if dom_tag.startswith("decode") else "launch = one write kernel"},
     }
     if e2e is not None:
