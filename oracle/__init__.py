@@ -16,8 +16,9 @@ Modules
   int4_cache   RHT + INT4 quantize + nibble pack + page scatter, dequant, decode
   turboquant   decode over the FP8-key / 3-4-bit-value combined slot layout
   fwht_fp8     fused normalised FWHT-128 + power-of-two absmax FP8 quantizer
+  kpool        pooled softmax-weighted key -> Hadamard-128 -> FP8 -> paged write (kpool_compress.py)
 
 Every function is pinned by tests that do not re-use it (see tests/test_oracle_*.py).
 """
 
-from . import formats, hadamard, int4_cache, turboquant, fwht_fp8  # noqa: F401
+from . import formats, hadamard, int4_cache, turboquant, fwht_fp8, kpool  # noqa: F401
