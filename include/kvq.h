@@ -265,6 +265,36 @@ KVQ_API kvq_status kvq_decode_tq_mse(const float *q, const float *rotation, cons
                              int32_t D, int32_t block_size, int64_t num_blocks, kvq_stream_t stream);
 
 /*
+ * kvq_kpool_write -- kpool compress-and-write: one FP8 cache entry per pool of pool_size tokens.
+ * Defined by kpool_compress.py, _kpool_softmax_rotate_write_cache_kernel and
+ * kpool_compress_and_write_cache (write_cache = True, return_compressed = False).
+ *
+ * For pool p with write_mask[p] (every pool when write_mask == NULL), per dimension d (fp32, each
+ * operation rounded to nearest):
+ *   z_s = slot_score[p][s][d] + ape[s][d];  M = max_s z_s;  w_s = exp(z_s - M)
+ *   x_d = bf16(sum_s slot_k[p][s][d] * w_s / sum_s w_s)            (sums in slot order)
+ *   y = bf16(H_128(x) * fp32(1/sqrt(128)));  a = max(max |y|, 1e-4)
+ *   scale = smallest power of two >= a * fp32(1/448) (round_scale), else a * fp32(1/448)
+ *   codes = E4M3FN(clamp(y / scale, -448, 448))
+ *   page = loc[p] / page_size, row = loc[p] % page_size of kv_cache:
+ *     bytes [row * 128, +128) of the page = codes; fp32 at byte page_size * 128 + 4 * row = scale.
+ * exp is the library's fp32 exponential (within 1 ulp; results below 2^-125 are 0), so the codes
+ * are reproducible bit for bit. Bytes of other pages and rows are not touched.
+ *
+ *   kv_cache    uint8 [num_blocks, page_size, 132], 16-byte aligned; page_size a multiple of 4.
+ *   slot_k      bf16 [n_pools, pool_size, 128], contiguous, 16-byte aligned.
+ *   slot_score  fp32 [n_pools, pool_size, 128], contiguous, 16-byte aligned.
+ *   ape         fp32 [pool_size, 128], contiguous, 16-byte aligned.
+ *   loc         int64 [n_pools]; a location outside [0, num_blocks * page_size) is skipped and flagged.
+ *   write_mask  bool (one byte) [n_pools] or NULL.
+ *   head_dim    must be 128 (KVQ_ERR_UNSUPPORTED otherwise). n_pools == 0 is a no-op.
+ */
+KVQ_API kvq_status kvq_kpool_write(uint8_t *kv_cache, const void *slot_k, const float *slot_score,
+                           const float *ape, const int64_t *loc, const uint8_t *write_mask,
+                           int64_t n_pools, int32_t pool_size, int32_t head_dim, int32_t page_size,
+                           int64_t num_blocks, int32_t round_scale, kvq_stream_t stream);
+
+/*
  * kvq_fwht128 -- fused normalised Walsh-Hadamard-128 rotation + per-row power-of-two FP8 quant.
  * Defined by kpool_compress.py, fwht128_quant_fp8 and _fwht_quant_kernel.
  *   x = bf16(FWHT128(row) * fp32(0.08838834764831845));  a = max(max |x|, 1e-4)

@@ -188,12 +188,13 @@ extern "C" size_t kvq_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hk, 
 
 extern "C" kvq_status kvq_device_error(kvq_stream_t stream, uint32_t *flags) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  unsigned words[4] = {0, 0, 0, 0};
+  unsigned words[5] = {0, 0, 0, 0, 0};
   if (!take_flags_write(s, &words[0]) || !take_flags_decode_int4(s, &words[1]) ||
-      !take_flags_decode_tq(s, &words[2]) || !take_flags_decode_tq_mse(s, &words[3]))
+      !take_flags_decode_tq(s, &words[2]) || !take_flags_decode_tq_mse(s, &words[3]) ||
+      !take_flags_kpool(s, &words[4]))
     return KVQ_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return KVQ_ERR_CUDA;
-  const uint32_t all = words[0] | words[1] | words[2] | words[3];
+  const uint32_t all = words[0] | words[1] | words[2] | words[3] | words[4];
   if (flags) *flags = all;
   return all ? KVQ_ERR_OUT_OF_RANGE : KVQ_OK;
 }

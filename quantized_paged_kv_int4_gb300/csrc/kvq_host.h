@@ -25,6 +25,7 @@ bool take_flags_write(cudaStream_t stream, unsigned *host_word);
 bool take_flags_decode_int4(cudaStream_t stream, unsigned *host_word);
 bool take_flags_decode_tq(cudaStream_t stream, unsigned *host_word);
 bool take_flags_decode_tq_mse(cudaStream_t stream, unsigned *host_word);
+bool take_flags_kpool(cudaStream_t stream, unsigned *host_word);
 
 // Split-partition geometry shared by workspace sizing and the launches.
 struct SplitPlan {

@@ -25,7 +25,8 @@ KVQ_BF16, KVQ_F16, KVQ_F32 = 0, 1, 2
 # the C API's declared functions, in header order
 C_FUNCTIONS = ("kvq_status_string", "kvq_abi_version", "kvq_write_int4", "kvq_decode_workspace_bytes",
                "kvq_decode_int4", "kvq_decode_int4_mods", "kvq_decode_int4_noalloc", "kvq_decode_tq",
-               "kvq_decode_tq_mse_workspace_bytes", "kvq_decode_tq_mse", "kvq_fwht128", "kvq_device_error")
+               "kvq_decode_tq_mse_workspace_bytes", "kvq_decode_tq_mse", "kvq_kpool_write", "kvq_fwht128",
+               "kvq_device_error")
 KVQ_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lock = threading.Lock()
@@ -58,6 +59,7 @@ _SIGS = {
     "kvq_decode_tq_mse": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_i32, c_i32, c_i32, c_i32, c_i32, c_p, c_i32, c_p,
                                          c_f32, c_i32, c_p, c_sz, c_p, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64,
                                          c_p]),
+    "kvq_kpool_write": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_p, c_p, c_i64, c_i32, c_i32, c_i32, c_i64, c_i32, c_p]),
     "kvq_fwht128": (ctypes.c_int, [c_p, c_p, c_p, c_i64, c_p]),
     "kvq_device_error": (ctypes.c_int, [c_p, ctypes.POINTER(ctypes.c_uint32)]),
 }
@@ -290,6 +292,27 @@ def kvq_decode_tq_mse(q, rotation, centroids, kv_cache, key_bits, key_packed_siz
                                    _stream(stream)),
            "kvq_decode_tq_mse")
     return out
+
+
+def kvq_kpool_write(kv_cache, slot_k, slot_score, ape, loc, write_mask=None, round_scale=True, stream=None):
+    """kpool_compress_and_write_cache: kv_cache [num_blocks, page_size, 132] uint8 written in place;
+    slot_k [n, pool, 128] bf16, slot_score [n, pool, 128] fp32, ape [pool, 128] fp32, loc [n] int64."""
+    _need(kv_cache, "kv_cache", torch.uint8)
+    _need(slot_k, "slot_k", torch.bfloat16)
+    _need(slot_score, "slot_score", torch.float32)
+    _need(ape, "ape", torch.float32)
+    _need(loc, "loc", torch.int64)
+    if write_mask is not None:
+        _need(write_mask, "write_mask", torch.bool)
+    n, pool, hd = slot_k.shape
+    if tuple(slot_score.shape) != (n, pool, hd) or tuple(ape.shape) != (pool, hd) or loc.numel() != n:
+        raise ValueError("slot_score / ape / loc shapes do not match slot_k")
+    nb, ps, row = kv_cache.shape
+    if row != hd + 4:
+        raise ValueError("kv_cache rows must be head_dim + 4 bytes")
+    _check(lib().kvq_kpool_write(_ptr(kv_cache), _ptr(slot_k), _ptr(slot_score), _ptr(ape), _ptr(loc),
+                                 _ptr(write_mask), n, pool, hd, ps, nb, int(bool(round_scale)), _stream(stream)),
+           "kvq_kpool_write")
 
 
 def kvq_fwht128(x, y=None, row_scale=None, stream=None):

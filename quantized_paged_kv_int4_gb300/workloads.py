@@ -344,3 +344,20 @@ def random_turboquant_mse_slots(n_slots_shape, D, key_bits, value_bits, seed):
     out[..., mse + 1] = (nb >> 8).to(torch.uint8)
     out[..., kps:kps + vlen] = fp8[..., D:D + vlen]
     return out
+
+
+# ----------------------------------------------------------------------------
+# kpool compress-and-write inputs
+# ----------------------------------------------------------------------------
+
+
+def kpool_case(n_pools=16384, pool_size=4, page_size=64, seed=0, extra_blocks=4):
+    """(slot_k bf16 [n, pool, 128], slot_score fp32 [n, pool, 128], ape fp32 [pool, 128], loc int64 [n],
+    num_blocks): N(0, 1) keys, N(0, 4) scores, N(0, 1/4) position biases, locations a random
+    permutation of the pool's slots."""
+    num_blocks = -(-n_pools // page_size) + extra_blocks
+    slot_k = torch.randn((n_pools, pool_size, 128), generator=_gen(seed, 2)).to(torch.bfloat16)
+    slot_score = torch.randn((n_pools, pool_size, 128), generator=_gen(seed, 12)) * 2.0
+    ape = torch.randn((pool_size, 128), generator=_gen(seed, 13)) * 0.5
+    loc = torch.randperm(num_blocks * page_size, generator=_gen(seed, 6))[:n_pools].to(torch.int64)
+    return slot_k, slot_score, ape, loc, num_blocks

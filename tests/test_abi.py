@@ -164,7 +164,24 @@ def test_tq_mse_validation_without_gpu():
     assert n == kvq.kvq_decode_workspace_bytes(2, 4, 2, 128, 4) + 2 * 4 * 128 * 4
 
 
+def test_kpool_validation_without_gpu():
+    L = kvq.lib()
+    args = [16, 16, 16, 16, 16, None, 8, 4, 128, 16, 10, 1, None]
+    def call(**kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return L.kvq_kpool_write(*a)
+    assert call(a6=0) == kvq.KVQ_OK                        # no pools
+    assert call(a8=64) == kvq.KVQ_ERR_UNSUPPORTED          # head_dim
+    assert call(a9=6) == kvq.KVQ_ERR_UNSUPPORTED           # page_size not a multiple of 4
+    assert call(a7=0) == kvq.KVQ_ERR_INVALID_ARG           # pool_size
+    assert call(a1=None) == kvq.KVQ_ERR_INVALID_ARG
+    assert call(a2=20) == kvq.KVQ_ERR_INVALID_ARG          # misaligned scores
+    assert call(a4=12) == kvq.KVQ_ERR_INVALID_ARG          # misaligned loc
+
+
 @pytest.mark.parametrize("name", ["kvq_write_int4", "kvq_decode_int4", "kvq_decode_tq", "kvq_decode_tq_mse",
-                                  "kvq_fwht128"])
+                                  "kvq_kpool_write", "kvq_fwht128"])
 def test_python_binding_names_match_the_c_api(name):
     assert callable(getattr(kvq, name))
