@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--workload", default="llama3_8b_int4",
                     choices=["llama3_8b_int4", "llama3_8b_int4_mods", "long_context_int4", "turboquant_fp8_v4",
-                             "turboquant_fp8_v3", "turboquant_mse_k3v4", "write_fwht"])
+                             "turboquant_fp8_v3", "turboquant_mse_k3v4", "write_fwht", "kpool_write"])
     ap.add_argument("--replicas", type=int, default=4)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -231,6 +231,8 @@ def run_kvq(args, dist):
     wl = args.workload
     if wl == "write_fwht":
         return run_write_fwht(args, dist, dev, stream)
+    if wl == "kpool_write":
+        return run_kpool(args, dist, dev, stream)
     if wl.startswith("turboquant_mse"):
         return run_tq_mse(args, dist, dev, stream)
     if wl.startswith("turboquant"):
@@ -483,6 +485,41 @@ def run_tq_mse(args, dist, dev, stream):
                    "quantized_paged_kv_int4_gb300/csrc/kvq_device.cuh"], "f32")
 
 
+def run_kpool(args, dist, dev, stream):
+    """kpool compress-and-write: 16384 pools of 4 tokens (65536 tokens), pages of 64, four input
+    replicas (4 x 50 MB > L2)."""
+    n, pool, ps = 16384, 4, 64
+    reps = []
+    for r in range(4):
+        slot_k, score, ape, loc, nb = workloads.kpool_case(n, pool, ps, seed=10 * dist.rank + r)
+        reps.append([t.to(dev) for t in (slot_k, score, ape, loc)] +
+                    [torch.zeros((nb, ps, 132), dtype=torch.uint8, device=dev)])
+
+    def step(i):
+        k, sc, ap, lc, cache = reps[i % 4]
+        kvq.kvq_kpool_write(cache, k, sc, ap, lc, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(4):
+            step(i)
+    stream.synchronize()
+    st, flags = kvq.kvq_device_error(stream)
+    assert st == 0, flags
+    graphs = []
+    for i in range(4):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(i)
+        graphs.append(g)
+    res = timed_steps(args, dist, stream, lambda i: None, lambda i: graphs[i % 4].replay(), dev.index)
+    byt = n * pool * 128 * (2 + 4) + pool * 128 * 4 + n * 8 + n * 132
+    cfg = {"workload": "kpool_write", "n_pools": n, "pool_size": pool, "page_size": ps, "head_dim": 128,
+           "round_scale": True, "l2": "4 rotating input replicas (4 x %.0f MB > 126 MB L2)" % (byt / 1e6),
+           "kpool_bytes_per_step": byt}
+    return finish(args, dist, res, byt, cfg, None, 1, "kpool_write", ["quantized_paged_kv_int4_gb300/csrc/kpool.cu",
+                  "quantized_paged_kv_int4_gb300/csrc/kvq_device.cuh"], "f32")
+
+
 def run_write_fwht(args, dist, dev, stream):
     nrep = 4
     reps = []
@@ -556,7 +593,7 @@ def finish(args, dist, res, step_bytes, cfg, e2e, kernels_per_step, dom_tag, dom
                      "note": ("launch = the whole library call (q rotation, split-KV kernel, LSE merge kernel)"
                               if dom_tag.startswith("decode_tq_mse") else
                               "launch = the whole library call (split-KV kernel + LSE merge kernel)")
-                     if dom_tag.startswith("decode") else "launch = one write kernel"},
+                     if dom_tag.startswith("decode") else "launch = one %s kernel" % dom_tag},
     }
     if e2e is not None:
         e_s = dist.max(e2e["seconds_per_step"])
