@@ -95,3 +95,70 @@ def kpool_compress_write(kv_cache, slot_k, slot_score, ape, loc, write_mask=None
         flat[page, off * 128:(off + 1) * 128] = codes[p]
         flat[page, ps * 128 + 4 * off:ps * 128 + 4 * off + 4] = np.frombuffer(scales[p].tobytes(), np.uint8)
     return codes, scales
+
+
+# ----------------------------------------------------------------------------------------------
+# tail ring: prefill seeding and the batched decode-step update
+# ----------------------------------------------------------------------------------------------
+
+
+def seed_tail(tail, key, gate_score, tslot, kpool):
+    """kpool_compress.py, _kpool_tail_seed_kernel. tail: [num_blocks, 2, ring, 128] float32 holding
+    bf16 values (half 0 keys, half 1 scores), written in place; key / gate_score [n, 128] (bf16
+    values); tslot [n] int (block * ring + pos % ring, < 0 = padding). Token i is copied iff it is
+    one of its request's last kpool tokens: the token kpool ahead is past the batch, padding, or
+    in another tail block."""
+    ring = tail.shape[2]
+    n = len(tslot)
+    for i in range(n):
+        t = int(tslot[i])
+        if t < 0:
+            continue
+        blk = t // ring
+        ahead = int(tslot[i + kpool]) if i + kpool < n else -1
+        if ahead >= 0 and ahead // ring == blk:
+            continue
+        tail[blk, 0, t % ring] = key[i]
+        tail[blk, 1, t % ring] = gate_score[i]
+
+
+def decode_update(kv_cache, tail, tail_slot, key, slot_score, ape, slot_mapping, positions, pool_size,
+                  round_scale=True):
+    """kpool_compress.py, _kpool_decode_update_batched_kernel: per request, its next_n tokens in
+    order. Token (r, t) with pos = positions[r, t] >= 0:
+      * if slot_mapping[r, t] >= 0 and pos % pool_size == pool_size - 1, the pool ending at pos is
+        compressed -- its earlier slots from the tail ring (phys = (pos - slot + j) % ring), its
+        last one the current key / score -- with the pooled softmax + Hadamard + FP8 of
+        kpool_compress_write and written at slot_mapping[r, t];
+      * then, if tail_slot[r, t] >= 0, the current key and score are stashed at ring position
+        pos % ring of block tail_slot[r, t] // ring.
+    tail: [num_blocks, 2, ring, 128] float32 (bf16 values), kv_cache: uint8 [nb, page_size, 132],
+    both written in place."""
+    ring = tail.shape[2]
+    R, T = positions.shape
+    nb, ps, _ = kv_cache.shape
+    flat = kv_cache.reshape(nb, ps * 132)
+    ape = np.asarray(ape, F32)
+    for r in range(R):
+        for t in range(T):
+            pos = int(positions[r, t])
+            loc = int(slot_mapping[r, t])
+            ts = int(tail_slot[r, t])
+            blk = max(ts, 0) // ring
+            slot = max(pos, 0) % pool_size
+            if loc >= 0 and pos >= 0 and slot == pool_size - 1:
+                start = pos - slot
+                ks = np.empty((1, pool_size, 128), F32)
+                ss = np.empty((1, pool_size, 128), F32)
+                for j in range(pool_size):
+                    phys = (start + j) % ring
+                    cur = j == slot
+                    ks[0, j] = key[r, t] if cur else tail[blk, 0, phys]
+                    ss[0, j] = slot_score[r, t] if cur else tail[blk, 1, phys]
+                codes, scales = quantize_rows(pool_keys(ks, ss, ape), round_scale)
+                page, off = divmod(loc, ps)
+                flat[page, off * 128:(off + 1) * 128] = codes[0]
+                flat[page, ps * 128 + 4 * off:ps * 128 + 4 * off + 4] = np.frombuffer(scales[0].tobytes(), np.uint8)
+            if pos >= 0 and ts >= 0:
+                tail[blk, 0, pos % ring] = key[r, t]
+                tail[blk, 1, pos % ring] = slot_score[r, t]

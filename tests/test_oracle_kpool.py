@@ -100,3 +100,89 @@ def test_scatter_to_pages_and_write_mask():
         else:
             assert np.all(got_k == 0xA5) and np.all(got_s == 0xA5)
     assert (flat != 0xA5).sum() == 5 * (128 + 4)   # nothing else touched
+
+
+# ---- tail ring (prefill seeding + batched decode update) --------------------------------------
+
+def _stream(R=3, pool=4, ring=8, next_n=3, seed=7):
+    """R requests with prompts of different lengths, then decode steps of next_n tokens each."""
+    rng = np.random.default_rng(seed)
+    prompt = [10, 4, 13][:R]
+    total = [31, 27, 30][:R]
+    keys = [_bf16(rng, (total[r], 128)) for r in range(R)]
+    scores = [formats.bf16_round(rng.standard_normal((total[r], 128)).astype(F32) * 2) for r in range(R)]
+    ape = rng.standard_normal((pool, 128)).astype(F32) * 0.5
+    n_slots = 64 * 16
+    perm = rng.permutation(n_slots)
+    pool_loc = {}
+    for r in range(R):
+        for q in range(total[r] // pool):
+            pool_loc[(r, q)] = int(perm[len(pool_loc)])
+    return prompt, total, keys, scores, ape, pool_loc, pool, ring, next_n
+
+
+def test_decode_update_reproduces_direct_pool_compression():
+    """Seeding the prompts' tails, then feeding the rest next_n tokens at a time through the ring,
+    writes every pool completed during decode exactly as compressing that pool directly."""
+    prompt, total, keys, scores, ape, pool_loc, pool, ring, next_n = _stream()
+    R = len(prompt)
+    tail = np.full((R + 2, 2, ring, 128), np.nan, F32)   # tail block r + 1 (block 0 unused)
+    # prefill: all prompt tokens of the batch, flattened
+    tk, ts, tsl = [], [], []
+    for r in range(R):
+        for pos in range(prompt[r]):
+            tk.append(keys[r][pos]); ts.append(scores[r][pos]); tsl.append((r + 1) * ring + pos % ring)
+    tsl.append(-1)  # padding
+    tk.append(np.zeros(128, F32)); ts.append(np.zeros(128, F32))
+    kpool.seed_tail(tail, np.array(tk), np.array(ts), np.array(tsl), pool)
+    cache = np.zeros((64, 16, 132), np.uint8)
+    cur = list(prompt)
+    while any(cur[r] < total[r] for r in range(R)):
+        K = np.zeros((R, next_n, 128), F32); S = np.zeros_like(K)
+        P = np.full((R, next_n), -1, np.int64); L = np.full((R, next_n), -1, np.int64)
+        TS = np.full((R, next_n), -1, np.int64)
+        for r in range(R):
+            for t in range(next_n):
+                pos = cur[r] + t
+                if pos >= total[r]:
+                    continue
+                K[r, t], S[r, t], P[r, t] = keys[r][pos], scores[r][pos], pos
+                TS[r, t] = (r + 1) * ring + pos % ring
+                if pos % pool == pool - 1:
+                    L[r, t] = pool_loc[(r, pos // pool)]
+        kpool.decode_update(cache, tail, TS, K, S, ape, L, P, pool)
+        cur = [min(c + next_n, total[r]) for r, c in enumerate(cur)]
+    flat = cache.reshape(64, 16 * 132)
+    checked = 0
+    for (r, q), loc in pool_loc.items():
+        if (q + 1) * pool - 1 < prompt[r]:
+            continue  # completed in the prompt: written by the prefill compress, not here
+        codes, scales = kpool.quantize_rows(kpool.pool_keys(keys[r][None, q * pool:(q + 1) * pool],
+                                                            scores[r][None, q * pool:(q + 1) * pool], ape))
+        page, off = divmod(loc, 16)
+        assert np.array_equal(flat[page, off * 128:(off + 1) * 128], codes[0])
+        assert flat[page, 16 * 128 + 4 * off:16 * 128 + 4 * off + 4].tobytes() == scales[0].tobytes()
+        checked += 1
+    assert checked >= 12
+
+
+def test_seed_tail_copies_only_each_requests_last_kpool_tokens():
+    rng = np.random.default_rng(8)
+    ring, kpool_n = 8, 4
+    lens = [6, 3, 9]
+    tsl, owner = [], []
+    for r, n in enumerate(lens):
+        for pos in range(n):
+            tsl.append(r * ring + pos % ring); owner.append((r, pos))
+    tsl += [-1, -1]
+    owner += [None, None]
+    key = rng.standard_normal((len(tsl), 128)).astype(F32)
+    score = rng.standard_normal((len(tsl), 128)).astype(F32)
+    tail = np.full((3, 2, ring, 128), 7.0, F32)
+    kpool.seed_tail(tail, key, score, np.array(tsl), kpool_n)
+    expect = np.full_like(tail, 7.0)
+    for i, o in enumerate(owner):
+        if o is not None and o[1] >= lens[o[0]] - kpool_n:
+            expect[o[0], 0, o[1] % ring] = key[i]
+            expect[o[0], 1, o[1] % ring] = score[i]
+    assert np.array_equal(tail, expect)
