@@ -295,6 +295,45 @@ KVQ_API kvq_status kvq_kpool_write(uint8_t *kv_cache, const void *slot_k, const 
                            int64_t num_blocks, int32_t round_scale, kvq_stream_t stream);
 
 /*
+ * kvq_kpool_seed_tail / kvq_kpool_decode_update -- the kpool tail ring. Defined by kpool_compress.py,
+ * _kpool_tail_seed_kernel / kpool_seed_tail_cache and _kpool_decode_update_batched_kernel /
+ * kpool_decode_update_and_maybe_write_cache_batched.
+ *
+ * The tail cache is bf16 [tail_blocks][2][ring][128] addressed through tail_block_stride and
+ * tail_half_stride (elements; the tail may alias a padded cache): half 0 keys, half 1 gate scores.
+ *
+ * Seed (prefill): token i (key / gate_score rows i, bf16 [n_tokens, 128]) with tslot[i] >= 0 is one
+ *   of its request's last kpool tokens iff tslot[i + kpool] is past the batch, negative, or in
+ *   another block (tslot / ring); such a token is copied to ring position tslot[i] % ring of block
+ *   tslot[i] / ring.
+ * Decode update: one request at a time is independent; within a request its next_n tokens run in
+ *   order. For token (r, t) with pos = positions[r][t] >= 0:
+ *     if slot_mapping[r][t] >= 0 and pos % pool_size == pool_size - 1: the pool ending at pos is
+ *       compressed exactly as kvq_kpool_write does (its earlier slots from ring positions
+ *       (pos - pool_size + 1 + j) % ring of block tail_slot[r][t] / ring, its last slot the current
+ *       key and score, both bf16 here) and written at slot_mapping[r][t] of kv_cache;
+ *     then, if tail_slot[r][t] >= 0, the current key and score are stored at ring position pos % ring.
+ *   key, slot_score  bf16 [R, next_n, 128] with element strides (b, t) multiples of 4, last dim
+ *                    contiguous; ape fp32 [pool_size, 128]; tail_slot_mapping, slot_mapping,
+ *                    positions int32 [R, next_n] contiguous. ring >= pool_size, ring % pool_size == 0.
+ *   kv_cache, page_size, num_blocks, round_scale: as kvq_kpool_write.
+ * Block ids >= tail_blocks and locations outside the cache are skipped and flagged.
+ */
+KVQ_API kvq_status kvq_kpool_seed_tail(void *tail, int64_t tail_block_stride, int64_t tail_half_stride,
+                               int32_t ring, int64_t tail_blocks, const void *key, const void *gate_score,
+                               const int32_t *tslot, int64_t n_tokens, int32_t kpool, int32_t head_dim,
+                               kvq_stream_t stream);
+
+KVQ_API kvq_status kvq_kpool_decode_update(uint8_t *kv_cache, int32_t page_size, int64_t num_blocks, void *tail,
+                                   int64_t tail_block_stride, int64_t tail_half_stride, int32_t ring,
+                                   int64_t tail_blocks, const int32_t *tail_slot_mapping, const void *key,
+                                   int64_t key_stride_b, int64_t key_stride_t, const void *slot_score,
+                                   int64_t score_stride_b, int64_t score_stride_t, const float *ape,
+                                   const int32_t *slot_mapping, const int32_t *positions,
+                                   int32_t num_requests, int32_t next_n, int32_t pool_size, int32_t head_dim,
+                                   int32_t round_scale, kvq_stream_t stream);
+
+/*
  * kvq_fwht128 -- fused normalised Walsh-Hadamard-128 rotation + per-row power-of-two FP8 quant.
  * Defined by kpool_compress.py, fwht128_quant_fp8 and _fwht_quant_kernel.
  *   x = bf16(FWHT128(row) * fp32(0.08838834764831845));  a = max(max |x|, 1e-4)

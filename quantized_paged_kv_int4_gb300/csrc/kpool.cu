@@ -191,6 +191,182 @@ __global__ void __launch_bounds__(256) kpool_write_kernel(const KpoolParams p, l
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Tail ring: prefill seeding and the batched decode-step update (kpool_compress.py,
+// _kpool_tail_seed_kernel and _kpool_decode_update_batched_kernel). The tail cache is bf16
+// [blocks][2][ring][128] addressed through its block and half strides (it may alias a padded
+// cache); half 0 holds keys, half 1 gate scores.
+// ---------------------------------------------------------------------------------------------
+
+struct TailArgs {
+  __nv_bfloat16 *tail;
+  long long block_stride, half_stride;  // elements
+  int ring;
+  long long blocks;
+};
+
+// One warp per token; lane l copies key / score elements 4l .. 4l + 3 (8 bytes each).
+__global__ void __launch_bounds__(256) kpool_seed_tail_kernel(const TailArgs ta, const __nv_bfloat16 *__restrict__ key,
+                                                              const __nv_bfloat16 *__restrict__ score,
+                                                              const int32_t *__restrict__ tslot, long long n,
+                                                              int kpool) {
+  const long long i = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (i >= n) return;
+  const long long t = tslot[i];
+  if (t < 0) return;
+  const long long blk = t / ta.ring;
+  const long long ahead = i + kpool < n ? tslot[i + kpool] : -1;
+  if (ahead >= 0 && ahead / ta.ring == blk) return;  // not among the request's last kpool tokens
+  if (blk >= ta.blocks) {
+    if (lane == 0) atomicOr(&g_flags_kpool, ERR_SLOT);
+    return;
+  }
+  __nv_bfloat16 *dst = ta.tail + blk * ta.block_stride + (t % ta.ring) * 128 + 4 * lane;
+  *reinterpret_cast<uint2 *>(dst) = __ldg(reinterpret_cast<const uint2 *>(key + i * 128) + lane);
+  *reinterpret_cast<uint2 *>(dst + ta.half_stride) = __ldg(reinterpret_cast<const uint2 *>(score + i * 128) + lane);
+}
+
+struct DecodeUpdateArgs {
+  uint8_t *cache;
+  int page_size;
+  long long num_blocks;
+  const int32_t *tail_slot, *slot_mapping, *positions;  // [R, next_n]
+  const __nv_bfloat16 *key, *score;
+  long long key_sb, key_st, score_sb, score_st;         // strides (elements)
+  const float *ape;                                     // [pool, 128]
+  int R, next_n, pool;
+  bool round_scale;
+};
+
+__device__ __forceinline__ void load_bf16x4(const __nv_bfloat16 *p, float (&v)[4]) {
+  const uint2 w = *reinterpret_cast<const uint2 *>(p);
+  v[0] = __uint_as_float(w.x << 16);
+  v[1] = __uint_as_float(w.x & 0xffff0000u);
+  v[2] = __uint_as_float(w.y << 16);
+  v[3] = __uint_as_float(w.y & 0xffff0000u);
+}
+
+// One warp per request, its next_n tokens in order; lane l owns dimensions 4l .. 4l + 3. A pool
+// completion reads ring entries that earlier tokens of this warp stashed -- each lane its own
+// dimensions, so program order makes them visible.
+__global__ void __launch_bounds__(256) kpool_decode_update_kernel(const DecodeUpdateArgs a, const TailArgs ta) {
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= a.R) return;
+  for (int t = 0; t < a.next_n; ++t) {
+    const long long idx = static_cast<long long>(r) * a.next_n + t;
+    const long long loc = a.slot_mapping[idx];
+    const int pos = a.positions[idx];
+    const long long ts = a.tail_slot[idx];
+    const int safe_pos = max(pos, 0);
+    const int slot = safe_pos % a.pool;
+    const long long blk = max(ts, 0LL) / ta.ring;
+    const bool blk_ok = blk < ta.blocks;
+    float key[4], sc[4];
+    load_bf16x4(a.key + r * a.key_sb + t * a.key_st + 4 * lane, key);
+    load_bf16x4(a.score + r * a.score_sb + t * a.score_st + 4 * lane, sc);
+    const __nv_bfloat16 *ring_k = ta.tail + (blk_ok ? blk : 0) * ta.block_stride + 4 * lane;
+    const __nv_bfloat16 *ring_s = ring_k + ta.half_stride;
+
+    if (loc >= 0 && pos >= 0 && slot == a.pool - 1) {
+      if (!blk_ok || loc >= a.num_blocks * a.page_size) {
+        if (lane == 0) atomicOr(&g_flags_kpool, ERR_SLOT);
+      } else {
+        const int start = safe_pos - slot;
+        float M[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        for (int j = 0; j < a.pool; ++j) {
+          float z[4];
+          if (j == slot) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) z[e] = sc[e];
+          } else {
+            load_bf16x4(ring_s + ((start + j) % ta.ring) * 128, z);
+          }
+          const float4 ap = __ldg(reinterpret_cast<const float4 *>(a.ape + j * 128 + 4 * lane));
+          M[0] = fmaxf(M[0], __fadd_rn(z[0], ap.x));
+          M[1] = fmaxf(M[1], __fadd_rn(z[1], ap.y));
+          M[2] = fmaxf(M[2], __fadd_rn(z[2], ap.z));
+          M[3] = fmaxf(M[3], __fadd_rn(z[3], ap.w));
+        }
+        float den[4] = {0.f, 0.f, 0.f, 0.f}, acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < a.pool; ++j) {
+          float z[4], k[4];
+          if (j == slot) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              z[e] = sc[e];
+              k[e] = key[e];
+            }
+          } else {
+            const int phys = (start + j) % ta.ring;
+            load_bf16x4(ring_s + phys * 128, z);
+            load_bf16x4(ring_k + phys * 128, k);
+          }
+          const float4 ap = __ldg(reinterpret_cast<const float4 *>(a.ape + j * 128 + 4 * lane));
+          const float zz[4] = {__fadd_rn(z[0], ap.x), __fadd_rn(z[1], ap.y), __fadd_rn(z[2], ap.z), __fadd_rn(z[3], ap.w)};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float w = exp_pool(__fsub_rn(zz[e], M[e]));
+            den[e] = __fadd_rn(den[e], w);
+            acc[e] = __fadd_rn(acc[e], __fmul_rn(k[e], w));
+          }
+        }
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = bf16_round(__fdiv_rn(acc[e], den[e]));
+        // Hadamard-128: stages h = 1, 2 in the lane, h = 4 .. 64 across lanes (partner lane ^ h/4)
+        butterfly_local<4>(v);
+#pragma unroll
+        for (int mask = 1; mask < 32; mask <<= 1) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[e] = butterfly_xor(v[e], lane, mask);
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[e] = bf16_round(__fmul_rn(v[e], 0x1.6a09e6p-4f));
+          amax = fmaxf(amax, fabsf(v[e]));
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, m));
+        amax = fmaxf(amax, 1e-4f);
+        const float m448 = __fmul_rn(amax, 0x1.24924ap-9f);
+        float s;
+        if (a.round_scale) {
+          const uint32_t mb = __float_as_uint(m448);
+          const uint32_t sb = (mb & 0x007FFFFFu) ? (mb & 0x7F800000u) + 0x00800000u : mb;
+          s = __uint_as_float(sb);
+          const float inv = __uint_as_float(0x7F000000u - sb);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[e] = __fmul_rn(v[e], inv);
+        } else {
+          s = m448;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[e] = __fdiv_rn(v[e], s);
+        }
+        const uint32_t c01 = __nv_cvt_float2_to_fp8x2(make_float2(v[0], v[1]), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t c23 = __nv_cvt_float2_to_fp8x2(make_float2(v[2], v[3]), __NV_SATFINITE, __NV_E4M3);
+        const long long page = loc / a.page_size, off = loc - page * a.page_size;
+        uint8_t *pg = a.cache + page * a.page_size * 132;
+        reinterpret_cast<uint32_t *>(pg + off * 128)[lane] = c01 | (c23 << 16);
+        if (lane == 0) reinterpret_cast<float *>(pg + a.page_size * 128)[off] = s;
+      }
+    }
+    // stash the current token after any completion read
+    if (pos >= 0 && ts >= 0) {
+      if (!blk_ok) {
+        if (lane == 0) atomicOr(&g_flags_kpool, ERR_SLOT);
+      } else {
+        __nv_bfloat16 *dk = ta.tail + blk * ta.block_stride + (pos % ta.ring) * 128 + 4 * lane;
+        *reinterpret_cast<uint2 *>(dk) = *reinterpret_cast<const uint2 *>(a.key + r * a.key_sb + t * a.key_st + 4 * lane);
+        *reinterpret_cast<uint2 *>(dk + ta.half_stride) =
+            *reinterpret_cast<const uint2 *>(a.score + r * a.score_sb + t * a.score_st + 4 * lane);
+      }
+    }
+  }
+}
+
 bool take_flags_kpool(cudaStream_t stream, unsigned *host_word) {
   static const unsigned zero = 0;
   if (cudaMemcpyFromSymbolAsync(host_word, g_flags_kpool, sizeof(unsigned), 0, cudaMemcpyDeviceToHost,
@@ -238,5 +414,69 @@ extern "C" kvq_status kvq_kpool_write(uint8_t *kv_cache, const void *slot_k, con
   const long long cap = static_cast<long long>(sm_count() > 0 ? sm_count() : 1) * per_sm;
   kpool_write_kernel<<<static_cast<unsigned>(tiles < cap ? tiles : cap), 256, 0,
                        reinterpret_cast<cudaStream_t>(stream)>>>(p, tiles);
+  return launch_status();
+}
+
+extern "C" kvq_status kvq_kpool_seed_tail(void *tail, int64_t tail_block_stride, int64_t tail_half_stride,
+                                          int32_t ring, int64_t tail_blocks, const void *key,
+                                          const void *gate_score, const int32_t *tslot, int64_t n_tokens,
+                                          int32_t kpool, int32_t head_dim, kvq_stream_t stream) {
+  if (n_tokens < 0 || ring < 1 || tail_blocks < 1 || kpool < 1) return KVQ_ERR_INVALID_ARG;
+  if (head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  if (n_tokens == 0) return KVQ_OK;
+  if (!tail || !key || !gate_score || !tslot) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(tail, 8) || !aligned(key, 8) || !aligned(gate_score, 8) || !aligned(tslot, 4) ||
+      tail_block_stride % 4 || tail_half_stride % 4 || tail_block_stride < 2LL * ring * 128 ||
+      tail_half_stride < static_cast<long long>(ring) * 128)
+    return KVQ_ERR_INVALID_ARG;
+  TailArgs ta{static_cast<__nv_bfloat16 *>(tail), tail_block_stride, tail_half_stride, ring, tail_blocks};
+  kpool_seed_tail_kernel<<<static_cast<unsigned>((n_tokens + 7) / 8), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      ta, static_cast<const __nv_bfloat16 *>(key), static_cast<const __nv_bfloat16 *>(gate_score), tslot, n_tokens,
+      kpool);
+  return launch_status();
+}
+
+extern "C" kvq_status kvq_kpool_decode_update(uint8_t *kv_cache, int32_t page_size, int64_t num_blocks, void *tail,
+                                              int64_t tail_block_stride, int64_t tail_half_stride, int32_t ring,
+                                              int64_t tail_blocks, const int32_t *tail_slot_mapping, const void *key,
+                                              int64_t key_stride_b, int64_t key_stride_t, const void *slot_score,
+                                              int64_t score_stride_b, int64_t score_stride_t, const float *ape,
+                                              const int32_t *slot_mapping, const int32_t *positions,
+                                              int32_t num_requests, int32_t next_n, int32_t pool_size,
+                                              int32_t head_dim, int32_t round_scale, kvq_stream_t stream) {
+  if (num_requests < 0 || next_n < 0 || pool_size < 1 || page_size < 1 || num_blocks < 1 || tail_blocks < 1)
+    return KVQ_ERR_INVALID_ARG;
+  if (head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  if (ring < pool_size || ring % pool_size != 0) return KVQ_ERR_INVALID_ARG;
+  if (page_size % 4 != 0) return KVQ_ERR_UNSUPPORTED;
+  if (num_requests == 0 || next_n == 0) return KVQ_OK;
+  if (!kv_cache || !tail || !tail_slot_mapping || !key || !slot_score || !ape || !slot_mapping || !positions)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned(kv_cache, 16) || !aligned(tail, 8) || !aligned(key, 8) || !aligned(slot_score, 8) ||
+      !aligned(ape, 16) || !aligned(tail_slot_mapping, 4) || !aligned(slot_mapping, 4) || !aligned(positions, 4) ||
+      key_stride_b % 4 || key_stride_t % 4 || score_stride_b % 4 || score_stride_t % 4 || tail_block_stride % 4 ||
+      tail_half_stride % 4 || tail_block_stride < 2LL * ring * 128 || tail_half_stride < static_cast<long long>(ring) * 128)
+    return KVQ_ERR_INVALID_ARG;
+  DecodeUpdateArgs a;
+  a.cache = kv_cache;
+  a.page_size = page_size;
+  a.num_blocks = num_blocks;
+  a.tail_slot = tail_slot_mapping;
+  a.slot_mapping = slot_mapping;
+  a.positions = positions;
+  a.key = static_cast<const __nv_bfloat16 *>(key);
+  a.score = static_cast<const __nv_bfloat16 *>(slot_score);
+  a.key_sb = key_stride_b;
+  a.key_st = key_stride_t;
+  a.score_sb = score_stride_b;
+  a.score_st = score_stride_t;
+  a.ape = ape;
+  a.R = num_requests;
+  a.next_n = next_n;
+  a.pool = pool_size;
+  a.round_scale = round_scale != 0;
+  TailArgs ta{static_cast<__nv_bfloat16 *>(tail), tail_block_stride, tail_half_stride, ring, tail_blocks};
+  kpool_decode_update_kernel<<<static_cast<unsigned>((num_requests + 7) / 8), 256, 0,
+                               reinterpret_cast<cudaStream_t>(stream)>>>(a, ta);
   return launch_status();
 }

@@ -25,8 +25,8 @@ KVQ_BF16, KVQ_F16, KVQ_F32 = 0, 1, 2
 # the C API's declared functions, in header order
 C_FUNCTIONS = ("kvq_status_string", "kvq_abi_version", "kvq_write_int4", "kvq_decode_workspace_bytes",
                "kvq_decode_int4", "kvq_decode_int4_mods", "kvq_decode_int4_noalloc", "kvq_decode_tq",
-               "kvq_decode_tq_mse_workspace_bytes", "kvq_decode_tq_mse", "kvq_kpool_write", "kvq_fwht128",
-               "kvq_device_error")
+               "kvq_decode_tq_mse_workspace_bytes", "kvq_decode_tq_mse", "kvq_kpool_write",
+               "kvq_kpool_seed_tail", "kvq_kpool_decode_update", "kvq_fwht128", "kvq_device_error")
 KVQ_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lock = threading.Lock()
@@ -60,6 +60,10 @@ _SIGS = {
                                          c_f32, c_i32, c_p, c_sz, c_p, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64,
                                          c_p]),
     "kvq_kpool_write": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_p, c_p, c_i64, c_i32, c_i32, c_i32, c_i64, c_i32, c_p]),
+    "kvq_kpool_seed_tail": (ctypes.c_int, [c_p, c_i64, c_i64, c_i32, c_i64, c_p, c_p, c_p, c_i64, c_i32, c_i32, c_p]),
+    "kvq_kpool_decode_update": (ctypes.c_int, [c_p, c_i32, c_i64, c_p, c_i64, c_i64, c_i32, c_i64, c_p, c_p, c_i64,
+                                               c_i64, c_p, c_i64, c_i64, c_p, c_p, c_p, c_i32, c_i32, c_i32, c_i32,
+                                               c_i32, c_p]),
     "kvq_fwht128": (ctypes.c_int, [c_p, c_p, c_p, c_i64, c_p]),
     "kvq_device_error": (ctypes.c_int, [c_p, ctypes.POINTER(ctypes.c_uint32)]),
 }
@@ -313,6 +317,53 @@ def kvq_kpool_write(kv_cache, slot_k, slot_score, ape, loc, write_mask=None, rou
     _check(lib().kvq_kpool_write(_ptr(kv_cache), _ptr(slot_k), _ptr(slot_score), _ptr(ape), _ptr(loc),
                                  _ptr(write_mask), n, pool, hd, ps, nb, int(bool(round_scale)), _stream(stream)),
            "kvq_kpool_write")
+
+
+def _tail_geometry(tail):
+    """(block stride, half stride, ring, blocks) of a bf16 tail cache [blocks, 2, ring, 128] view."""
+    if not isinstance(tail, torch.Tensor) or not tail.is_cuda or tail.dtype != torch.bfloat16 or tail.dim() != 4:
+        raise TypeError("tail must be a CUDA bf16 tensor [blocks, 2, ring, 128]")
+    if tail.shape[1] != 2 or tail.shape[3] != 128 or tail.stride(3) != 1 or tail.stride(2) != 128:
+        raise ValueError("tail must be [blocks, 2, ring, 128] with contiguous rows")
+    return tail.stride(0), tail.stride(1), tail.shape[2], tail.shape[0]
+
+
+def kvq_kpool_seed_tail(tail, key, gate_score, tslot, kpool, stream=None):
+    """kpool_seed_tail_cache: tail bf16 [blocks, 2, ring, 128] (a view; strides are honoured),
+    key / gate_score bf16 [n, 128], tslot int32 [n]."""
+    bs, hs, ring, nblk = _tail_geometry(tail)
+    _need(key, "key", torch.bfloat16)
+    _need(gate_score, "gate_score", torch.bfloat16)
+    _need(tslot, "tslot", torch.int32)
+    n = tslot.numel()
+    if tuple(key.shape) != (n, 128) or tuple(gate_score.shape) != (n, 128):
+        raise ValueError("key / gate_score must be [n, 128]")
+    _check(lib().kvq_kpool_seed_tail(_ptr(tail), bs, hs, ring, nblk, _ptr(key), _ptr(gate_score), _ptr(tslot), n,
+                                     kpool, 128, _stream(stream)), "kvq_kpool_seed_tail")
+
+
+def kvq_kpool_decode_update(kv_cache, tail, tail_slot_mapping, key, slot_score, ape, slot_mapping, positions,
+                            pool_size, round_scale=True, stream=None):
+    """kpool_decode_update_and_maybe_write_cache_batched: key / slot_score bf16 [R, next_n, 128];
+    tail_slot_mapping / slot_mapping / positions int32 [R, next_n]; ape fp32 [pool, 128]."""
+    bs, hs, ring, nblk = _tail_geometry(tail)
+    _need(kv_cache, "kv_cache", torch.uint8)
+    for t, n in ((key, "key"), (slot_score, "slot_score")):
+        _need(t, n, torch.bfloat16, contiguous=False)
+        if t.dim() != 3 or t.shape[2] != 128 or t.stride(2) != 1:
+            raise ValueError("%s must be [R, next_n, 128] with a contiguous last dim" % n)
+    _need(ape, "ape", torch.float32)
+    for t, n in ((tail_slot_mapping, "tail_slot_mapping"), (slot_mapping, "slot_mapping"), (positions, "positions")):
+        _need(t, n, torch.int32)
+        if tuple(t.shape) != tuple(key.shape[:2]):
+            raise ValueError("%s must be [R, next_n]" % n)
+    R, next_n = key.shape[0], key.shape[1]
+    nb, ps, row = kv_cache.shape
+    _check(lib().kvq_kpool_decode_update(_ptr(kv_cache), ps, nb, _ptr(tail), bs, hs, ring, nblk, _ptr(tail_slot_mapping),
+                                         _ptr(key), key.stride(0), key.stride(1), _ptr(slot_score), slot_score.stride(0),
+                                         slot_score.stride(1), _ptr(ape), _ptr(slot_mapping), _ptr(positions), R, next_n,
+                                         pool_size, 128, int(bool(round_scale)), _stream(stream)),
+           "kvq_kpool_decode_update")
 
 
 def kvq_fwht128(x, y=None, row_scale=None, stream=None):

@@ -181,7 +181,30 @@ def test_kpool_validation_without_gpu():
     assert call(a4=12) == kvq.KVQ_ERR_INVALID_ARG          # misaligned loc
 
 
+def test_kpool_tail_validation_without_gpu():
+    L = kvq.lib()
+    # tail, block stride, half stride, ring, blocks, key, score, tslot, n, kpool, head_dim, stream
+    seed = [16, 2 * 8 * 128, 8 * 128, 8, 4, 16, 16, 16, 5, 4, 128, None]
+    def call(args, **kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return a
+    assert L.kvq_kpool_seed_tail(*call(seed, a8=0)) == kvq.KVQ_OK
+    assert L.kvq_kpool_seed_tail(*call(seed, a10=64)) == kvq.KVQ_ERR_UNSUPPORTED
+    assert L.kvq_kpool_seed_tail(*call(seed, a1=100)) == kvq.KVQ_ERR_INVALID_ARG     # block stride too small
+    assert L.kvq_kpool_seed_tail(*call(seed, a0=18)) == kvq.KVQ_ERR_INVALID_ARG      # misaligned tail
+    upd = [16, 16, 10, 16, 2 * 8 * 128, 8 * 128, 8, 4, 16, 16, 3 * 128, 128, 16, 3 * 128, 128, 16, 16, 16, 2, 3, 4,
+           128, 1, None]
+    assert L.kvq_kpool_decode_update(*call(upd, a18=0)) == kvq.KVQ_OK                # no requests
+    assert L.kvq_kpool_decode_update(*call(upd, a6=6)) == kvq.KVQ_ERR_INVALID_ARG    # ring % pool
+    assert L.kvq_kpool_decode_update(*call(upd, a6=2)) == kvq.KVQ_ERR_INVALID_ARG    # ring < pool
+    assert L.kvq_kpool_decode_update(*call(upd, a21=64)) == kvq.KVQ_ERR_UNSUPPORTED
+    assert L.kvq_kpool_decode_update(*call(upd, a10=130)) == kvq.KVQ_ERR_INVALID_ARG  # key stride
+
+
 @pytest.mark.parametrize("name", ["kvq_write_int4", "kvq_decode_int4", "kvq_decode_tq", "kvq_decode_tq_mse",
-                                  "kvq_kpool_write", "kvq_fwht128"])
+                                  "kvq_kpool_write", "kvq_kpool_seed_tail", "kvq_kpool_decode_update",
+                                  "kvq_fwht128"])
 def test_python_binding_names_match_the_c_api(name):
     assert callable(getattr(kvq, name))

@@ -63,3 +63,89 @@ def test_full_size_16384_pools():
     got, ref, st, flags = _both(16384, 4, 64, seed=0)
     assert st == 0 and flags == 0
     assert np.array_equal(got, ref)
+
+
+# ---- tail ring ----------------------------------------------------------------------------------
+
+def _bf16_np(t):
+    return t.float().cpu().numpy()
+
+
+def _tail_views(blocks, ring, pad_blocks=0):
+    """A bf16 tail [blocks, 2, ring, 128] inside a larger buffer (padded block stride), NaN-filled."""
+    big = torch.full((blocks, 2 * ring * 128 + pad_blocks * 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    tail = big[:, :2 * ring * 128].view(blocks, 2, ring, 128)
+    return big, tail
+
+
+def test_seed_tail_bit_exact():
+    rng = np.random.default_rng(21)
+    ring, kp = 8, 4
+    lens = [6, 3, 9, 1, 12]
+    tsl = []
+    for r, n in enumerate(lens):
+        tsl += [r * ring + p % ring for p in range(n)]
+    tsl += [-1, -1, -1]
+    n = len(tsl)
+    key = torch.from_numpy(rng.standard_normal((n, 128)).astype(np.float32)).to(torch.bfloat16)
+    score = torch.from_numpy(rng.standard_normal((n, 128)).astype(np.float32)).to(torch.bfloat16)
+    big, tail = _tail_views(len(lens), ring, pad_blocks=3)
+    ref = _bf16_np(tail)
+    kpool.seed_tail(ref, key.float().numpy(), score.float().numpy(), np.array(tsl), kp)
+    kvq.kvq_kpool_seed_tail(tail, key.cuda(), score.cuda(), torch.tensor(tsl, dtype=torch.int32, device="cuda"), kp)
+    st, flags = kvq.kvq_device_error()
+    assert st == 0 and flags == 0
+    got = _bf16_np(tail)
+    assert np.array_equal(np.isnan(got), np.isnan(ref)) and np.array_equal(np.nan_to_num(got), np.nan_to_num(ref))
+
+
+@pytest.mark.parametrize("next_n,round_scale", [(1, True), (3, True), (4, False)])
+def test_decode_update_stream_bit_exact(next_n, round_scale):
+    """Prompts seeded into the ring, then decode steps of next_n tokens per request: every cache
+    byte and every ring entry equal the oracle's after each step."""
+    rng = np.random.default_rng(30 + next_n)
+    pool, ring, ps = 4, 8, 16
+    prompt, total = [10, 4, 13, 7], [31, 27, 30, 19]
+    R = len(prompt)
+    keys = [torch.from_numpy(rng.standard_normal((total[r], 128)).astype(np.float32)).to(torch.bfloat16) for r in range(R)]
+    scores = [torch.from_numpy(rng.standard_normal((total[r], 128)).astype(np.float32) * 2).to(torch.bfloat16)
+              for r in range(R)]
+    ape = torch.from_numpy(rng.standard_normal((pool, 128)).astype(np.float32) * 0.5)
+    perm = rng.permutation(64 * ps)
+    pool_loc, k = {}, 0
+    for r in range(R):
+        for q in range(total[r] // pool):
+            pool_loc[(r, q)] = int(perm[k]); k += 1
+    big, tail = _tail_views(R + 1, ring, pad_blocks=1)
+    ref_tail = _bf16_np(tail)
+    cache = torch.zeros((64, ps, 132), dtype=torch.uint8, device="cuda")
+    ref_cache = np.zeros((64, ps, 132), np.uint8)
+    tk = torch.cat([keys[r][:prompt[r]] for r in range(R)])
+    tsc = torch.cat([scores[r][:prompt[r]] for r in range(R)])
+    tsl = [(r + 1) * ring + p % ring for r in range(R) for p in range(prompt[r])]
+    kpool.seed_tail(ref_tail, tk.float().numpy(), tsc.float().numpy(), np.array(tsl), pool)
+    kvq.kvq_kpool_seed_tail(tail, tk.cuda(), tsc.cuda(), torch.tensor(tsl, dtype=torch.int32, device="cuda"), pool)
+    cur = list(prompt)
+    while any(cur[r] < total[r] for r in range(R)):
+        K = torch.zeros((R, next_n, 128), dtype=torch.bfloat16); S = torch.zeros_like(K)
+        P = torch.full((R, next_n), -1, dtype=torch.int32); L = torch.full_like(P, -1); TS = torch.full_like(P, -1)
+        for r in range(R):
+            for t in range(next_n):
+                pos = cur[r] + t
+                if pos >= total[r]:
+                    continue
+                K[r, t], S[r, t], P[r, t] = keys[r][pos], scores[r][pos], pos
+                TS[r, t] = (r + 1) * ring + pos % ring
+                if pos % pool == pool - 1:
+                    L[r, t] = pool_loc[(r, pos // pool)]
+        kpool.decode_update(ref_cache, ref_tail, TS.numpy(), K.float().numpy(), S.float().numpy(), ape.numpy(),
+                            L.numpy(), P.numpy(), pool, round_scale)
+        kvq.kvq_kpool_decode_update(cache, tail, TS.cuda(), K.cuda(), S.cuda(), ape.cuda(), L.cuda(), P.cuda(), pool,
+                                    round_scale=round_scale)
+        st, flags = kvq.kvq_device_error()
+        assert st == 0 and flags == 0
+        assert np.array_equal(cache.cpu().numpy(), ref_cache)
+        got = _bf16_np(tail)
+        assert np.array_equal(np.isnan(got), np.isnan(ref_tail))
+        assert np.array_equal(np.nan_to_num(got), np.nan_to_num(ref_tail))
+        cur = [min(c + next_n, total[r]) for r, c in enumerate(cur)]
