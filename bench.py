@@ -51,7 +51,8 @@ def parse():
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--workload", default="llama3_8b_int4",
                     choices=["llama3_8b_int4", "llama3_8b_int4_mods", "long_context_int4", "turboquant_fp8_v4",
-                             "turboquant_fp8_v3", "turboquant_mse_k3v4", "write_fwht", "kpool_write"])
+                             "turboquant_fp8_v3", "turboquant_mse_k3v4", "write_fwht", "kpool_write",
+                             "kpool_decode_update"])
     ap.add_argument("--replicas", type=int, default=4)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -233,6 +234,8 @@ def run_kvq(args, dist):
         return run_write_fwht(args, dist, dev, stream)
     if wl == "kpool_write":
         return run_kpool(args, dist, dev, stream)
+    if wl == "kpool_decode_update":
+        return run_kpool_update(args, dist, dev, stream)
     if wl.startswith("turboquant_mse"):
         return run_tq_mse(args, dist, dev, stream)
     if wl.startswith("turboquant"):
@@ -518,6 +521,44 @@ def run_kpool(args, dist, dev, stream):
            "kpool_bytes_per_step": byt}
     return finish(args, dist, res, byt, cfg, None, 1, "kpool_write", ["quantized_paged_kv_int4_gb300/csrc/kpool.cu",
                   "quantized_paged_kv_int4_gb300/csrc/kvq_device.cuh"], "f32")
+
+
+def run_kpool_update(args, dist, dev, stream):
+    """Batched kpool decode update (spec verify): 1024 requests x next_n = 4 tokens, pools of 4 (each
+    request completes one pool per step), ring 8, pages of 64."""
+    R, nn, pool, ring, ps = 1024, 4, 4, 8, 64
+    g = torch.Generator().manual_seed(50 + dist.rank)
+    key = torch.randn((R, nn, 128), generator=g).to(torch.bfloat16).to(dev)
+    score = (torch.randn((R, nn, 128), generator=g) * 2).to(torch.bfloat16).to(dev)
+    ape = (torch.randn((pool, 128), generator=g) * 0.5).to(dev)
+    tail = (torch.randn((R, 2, ring, 128), generator=g)).to(torch.bfloat16).to(dev)
+    nb = R // ps + 4
+    cache = torch.zeros((nb, ps, 132), dtype=torch.uint8, device=dev)
+    pos = (torch.arange(nn, dtype=torch.int32)[None, :] + 100).repeat(R, 1)          # positions 100..103
+    ts = (torch.arange(R, dtype=torch.int32)[:, None] * ring + pos % ring).to(torch.int32)
+    loc = torch.where(pos % pool == pool - 1, torch.randperm(nb * ps, generator=g)[:R, None].to(torch.int32),
+                      torch.full_like(pos, -1))
+    pos, ts, loc = pos.to(dev), ts.to(dev), loc.to(dev)
+
+    def step(i):
+        kvq.kvq_kpool_decode_update(cache, tail, ts, key, score, ape, loc, pos, pool, stream=stream)
+
+    with torch.cuda.stream(stream):
+        step(0)
+    stream.synchronize()
+    st, flags = kvq.kvq_device_error(stream)
+    assert st == 0, flags
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        step(0)
+    res = timed_steps(args, dist, stream, lambda i: None, lambda i: gr.replay(), dev.index)
+    byt = R * nn * 128 * 2 * 2 + R * (pool - 1) * 128 * 2 * 2 + R * nn * 128 * 2 * 2 + R * 132 + 3 * R * nn * 4
+    cfg = {"workload": "kpool_decode_update", "requests": R, "next_n": nn, "pool_size": pool, "ring": ring,
+           "page_size": ps, "l2": "inputs %.1f MB (L2-resident; a launch-latency-bound step)" % (byt / 1e6),
+           "kpool_update_bytes_per_step": byt}
+    return finish(args, dist, res, byt, cfg, None, 1, "kpool_decode_update",
+                  ["quantized_paged_kv_int4_gb300/csrc/kpool.cu", "quantized_paged_kv_int4_gb300/csrc/kvq_device.cuh"],
+                  "f32")
 
 
 def run_write_fwht(args, dist, dev, stream):
