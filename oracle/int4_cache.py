@@ -166,7 +166,7 @@ def _head_attention(q_rows, K, V, sm, pos=None, qpos=None, softcap=0.0, slopes=N
 
 def decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
                 signs, softmax_scale, num_splits=None, batch_index=None,
-                window=0, softcap=0.0, sinks=None, alibi_slopes=None):
+                window=0, softcap=0.0, sinks=None, alibi_slopes=None, q_len=1):
     """Paged decode attention over the INT4 cache (unified_attention_int4 semantics).
 
     q: [B, Hq, D] float32 holding bf16 values. Returns float64 [B, Hq, D] (rows of
@@ -183,7 +183,30 @@ def decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
       alibi_slopes    USE_ALIBI_SLOPES: [Hq] slopes, S += slope * (n - (L - 1));
       sinks           USE_SINKS: [Hq] logits that join each head's softmax denominator with no
                       value (the softmax state starts at M = sink, L = 1).
+
+    Multi-token decode (q_len = Q > 1, the speculative-verify case of unified_attention_int4):
+    q is [B * Q, Hq, D], query token i of sequence b (row b * Q + i) sits at position L - Q + i and
+    attends causally to keys n <= L - Q + i; the output has q's row layout. Sequences need
+    L >= Q. (With Q > 1 only the soft cap and sinks are combined with it here.)
     """
+    if q_len > 1:
+        q = np.asarray(q, dtype=np.float32)
+        BQ, Hq, D = q.shape
+        assert BQ % q_len == 0 and window == 0 and alibi_slopes is None
+        B = BQ // q_len
+        out = np.zeros((BQ, Hq, D), dtype=np.float64)
+        rows = range(B) if batch_index is None else batch_index
+        for b in rows:
+            L = int(seq_lens[b])
+            for i in range(q_len):
+                Li = L - q_len + i + 1   # keys 0 .. L - Q + i
+                if Li <= 0:
+                    continue
+                out[b * q_len + i] = decode_int4(q[b * q_len + i][None], k_cache, v_cache, k_scale, v_scale,
+                                                 np.asarray(block_table)[b][None], np.array([Li]), signs,
+                                                 softmax_scale, num_splits=num_splits, softcap=softcap,
+                                                 sinks=sinks)[0]
+        return out
     q = np.asarray(q, dtype=np.float32)
     B, Hq, D = q.shape
     Hk = k_cache.shape[2]

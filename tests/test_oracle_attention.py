@@ -154,3 +154,32 @@ def test_unrotated_exactly_representable_cache_is_textbook_attention():
         o = torch.nn.functional.scaled_dot_product_attention(Q, K, V, scale=0.2)[0, :, 0, :].numpy()
         assert np.max(np.abs(got[b] - o)) < 1e-12
         off += L
+
+
+@pytest.mark.parametrize("Q", [2, 4])
+def test_multi_token_decode_matches_causal_sdpa(Q):
+    """Q query tokens per sequence at positions L - Q .. L - 1, each attending causally: float64 SDPA
+    with an explicit boolean causal mask on the dequantized cache."""
+    case = workloads.DecodeCase("mtok", 3, 4 * Q, 2, 64, [5, 40, 17], seed=40 + Q)
+    c = _build(case)
+    B, Hq, D = 3, 4, 64
+    G = Hq // 2
+    rng = np.random.default_rng(Q)
+    q = int4_cache.bf16_round(rng.standard_normal((B * Q, Hq, D)).astype(np.float32))
+    scale = 1.0 / np.sqrt(D)
+    got = int4_cache.decode_int4(q, c["kc"], c["vc"], c["ks"], c["vs"], c["bt"], c["lens"], c["signs"], scale,
+                                 q_len=Q)
+    q_rot = int4_cache.rotate_to_bf16(q, c["signs"])
+    for b, L in enumerate(c["lens"]):
+        Kt = np.zeros((L, 2, D)); Vt = np.zeros((L, 2, D))
+        for n in range(L):
+            page, row = c["bt"][b, n // 16], n % 16
+            Kt[n] = _unrotate(int4_cache.dequant_int4(c["kc"][page, row], c["ks"][page, row]), c["signs"], D)
+            Vt[n] = _unrotate(int4_cache.dequant_int4(c["vc"][page, row], c["vs"][page, row]), c["signs"], D)
+        Qm = torch.from_numpy(np.stack([_unrotate(q_rot[b * Q + i], c["signs"], D) for i in range(Q)], axis=1))  # [Hq, Q, D]
+        K = torch.from_numpy(np.repeat(Kt.transpose(1, 0, 2), G, axis=0))
+        V = torch.from_numpy(np.repeat(Vt.transpose(1, 0, 2), G, axis=0))
+        allowed = torch.from_numpy(np.arange(L)[None, :] <= (L - Q + np.arange(Q))[:, None])  # [Q, L]
+        o = torch.nn.functional.scaled_dot_product_attention(Qm, K, V, attn_mask=allowed, scale=scale)  # [Hq, Q, D]
+        for i in range(Q):
+            assert np.max(np.abs(got[b * Q + i] - o[:, i].numpy())) < 1e-12
