@@ -150,6 +150,12 @@ KVQ_API kvq_status kvq_decode_int4(const void *q, const uint8_t *k_cache, const 
  *   mods->softcap         >= 0, finite (natural-log units of S, like softmax_scale).
  *   mods->sinks           fp32 [Hq] device array (4-byte aligned) or NULL.
  *   mods->alibi_slopes    fp32 [Hq] device array (4-byte aligned) or NULL.
+ *   mods->q_len           query tokens per sequence (0 or 1: one). Multi-token decode (the
+ *                         speculative-verify case): q and out are [B * q_len, Hq, D], row
+ *                         b * q_len + i the query at position L - q_len + i, attending causally
+ *                         to keys n <= L - q_len + i (a query with no key gets a zero row). Needs
+ *                         (Hq / Hk) * q_len <= 8 and no window or ALiBi (KVQ_ERR_UNSUPPORTED);
+ *                         the workspace is kvq_decode_workspace_bytes(B, q_len * Hq, Hk, D, S).
  * Invalid fields return KVQ_ERR_INVALID_ARG. Other arguments, numerics and errors: as
  * kvq_decode_int4.
  */
@@ -158,6 +164,7 @@ typedef struct kvq_score_mods {
   float softcap;
   const float *sinks;
   const float *alibi_slopes;
+  int32_t q_len;
 } kvq_score_mods;
 
 KVQ_API kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,

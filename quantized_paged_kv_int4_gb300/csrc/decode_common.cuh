@@ -31,7 +31,8 @@ struct SplitArgs {
   const int32_t *seq_lens;
   int32_t max_blocks;
   int32_t num_splits;  // 0 = balanced
-  int32_t B, Hq, Hk, G;
+  int32_t B, Hq, Hk, G;  // Hq: output rows per sequence (Q tokens x heads); G: heads per kv head
+  int32_t Q;             // query tokens per sequence (multi-token decode; 1 otherwise)
   int32_t heads_per_cta, warps_per_head;
   int32_t seg_ctas;    // the split kernel's gridDim.x
   long long slots;     // partial slots in the workspace (before the warps_per_head factor)
@@ -271,19 +272,23 @@ __device__ __forceinline__ void store_partial(const SplitArgs &a, long long slot
                                               int lane, const float (&o0)[D / 8],
                                               const float (&o1)[D / 8], float lse0, float lse1) {
   const int g = lane >> 2, t = lane & 3;
-  const long long row = (slot * a.warps_per_head + sub) * a.Hq + static_cast<long long>(h) * a.G;
-  const int n0 = 2 * t, n1 = 2 * t + 1;
-  if (n0 < a.G) {
-    float4 *dst = reinterpret_cast<float4 *>(a.part_o + (row + n0) * D + g * (D / 8));
+  const long long row = (slot * a.warps_per_head + sub) * a.Hq;
+  const int n0 = 2 * t, n1 = 2 * t + 1, heads = a.Hq / a.Q;
+  // MMA column n = query token n / G, head h * G + n % G of it
+  auto row_of = [&](int n) { return row + (n / a.G) * heads + static_cast<long long>(h) * a.G + n % a.G; };
+  if (n0 < a.G * a.Q) {
+    const long long r0 = row_of(n0);
+    float4 *dst = reinterpret_cast<float4 *>(a.part_o + r0 * D + g * (D / 8));
 #pragma unroll
     for (int i = 0; i < D / 32; ++i) dst[i] = make_float4(o0[4 * i], o0[4 * i + 1], o0[4 * i + 2], o0[4 * i + 3]);
-    if (g == 0) a.part_lse[row + n0] = lse0;
+    if (g == 0) a.part_lse[r0] = lse0;
   }
-  if (n1 < a.G) {
-    float4 *dst = reinterpret_cast<float4 *>(a.part_o + (row + n1) * D + g * (D / 8));
+  if (n1 < a.G * a.Q) {
+    const long long r1 = row_of(n1);
+    float4 *dst = reinterpret_cast<float4 *>(a.part_o + r1 * D + g * (D / 8));
 #pragma unroll
     for (int i = 0; i < D / 32; ++i) dst[i] = make_float4(o1[4 * i], o1[4 * i + 1], o1[4 * i + 2], o1[4 * i + 3]);
-    if (g == 0) a.part_lse[row + n1] = lse1;
+    if (g == 0) a.part_lse[r1] = lse1;
   }
 }
 
@@ -319,7 +324,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const SplitArgs a) {
   float sg[V];
 #pragma unroll
   for (int j = 0; j < V; ++j) sg[j] = a.signs != nullptr ? __ldg(a.signs + lane * V + j) : 0.f;
-  const float sink2 = live && a.sinks != nullptr ? __ldg(a.sinks + hq) * 1.4426950408889634f : -INFINITY;
+  const float sink2 = live && a.sinks != nullptr ? __ldg(a.sinks + hq % (a.Hq / a.Q)) * 1.4426950408889634f : -INFINITY;
   const SeqSpan sp = live ? seq_span(a, b, nullptr) : SeqSpan{0, 0, 0, 0};  // the split kernel already flagged it
   const int L = sp.L;
   long long s_lo = 0, s_hi = 0;                           // slot range [s_lo, s_hi)

@@ -220,15 +220,19 @@ struct PieceState {
 
 // q_rot = bf16(H(q * d1)) for the G heads of kv head h of sequence b, as the fp16 B fragments
 // of the score MMA (odd dims pre-divided by 16) and the per-head sums of the q the products use.
-// Start copying the G raw query rows of (sequence b, kv head h) -- contiguous, G * D bf16 -- into
-// this warp's area (16-byte cp.async per lane); load_query waits for them.
+// Start copying the G * Q raw query rows of (sequence b, kv head h) -- for each of the Q query
+// tokens G contiguous rows, G * D bf16 -- into this warp's area (16-byte cp.async per lane), row
+// i * G + g for token i, head h * G + g; load_query waits for them.
 template <int D>
 __device__ __forceinline__ void fetch_query(const Int4Params &p, uint8_t *qarea, int b, int h, int lane) {
-  const int G = p.s.G;
-  const uint8_t *src = reinterpret_cast<const uint8_t *>(
-      p.q + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(h) * G) * D);
+  const int G = p.s.G, per = G * D / 8, heads = p.s.Hq / p.s.Q;
   const uint32_t dst = smem_u32(qarea);
-  for (int c = lane; c < G * D / 8; c += 32) cp_async<16>(dst + 16 * c, src + 16 * c, true);
+  for (int c = lane; c < p.s.Q * per; c += 32) {
+    const int i = c / per, w = c - i * per;
+    const uint8_t *src = reinterpret_cast<const uint8_t *>(
+        p.q + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(i) * heads + static_cast<long long>(h) * G) * D);
+    cp_async<16>(dst + 16 * c, src + 16 * w, true);
+  }
   cp_async_commit();
 }
 
@@ -237,7 +241,7 @@ __device__ __forceinline__ void load_query(const Int4Params &p, uint8_t *qarea, 
                                            uint32_t (&qf)[D / 16][2], float &qs0, float &qs1, bool fetched) {
   using Gm = Int4Geom<D>;
   constexpr int J = D / 32;
-  const int g = lane >> 2, t = lane & 3, G = p.s.G;
+  const int g = lane >> 2, t = lane & 3, G = p.s.G * p.s.Q;  // MMA columns in use
   __half *qh = reinterpret_cast<__half *>(qarea);
   float *qsum = reinterpret_cast<float *>(qarea + 8 * D * 2);
   // The raw rows land in this warp's area (fetch_query, issued early when possible); each head is
@@ -457,12 +461,14 @@ struct ScoreMods {
 // online softmax step over their 16 * NP tokens, P.V. MASKED: some rows of the (single) page lie
 // outside [t0, t1) -- the ragged end of a sequence, a fixed split boundary or the start of a
 // sliding window -- and may hold never-written scale words (NaN): they are selected away, never
-// multiplied. MODS: apply the score modifiers md (page i's row 0 is at position nb + 16 W i).
+// multiplied; in multi-token decode a column's keys also stop at its causal limit (lim0 / lim1
+// for the lane's columns 2t / 2t + 1, exclusive). MODS: apply the score modifiers md (page i's
+// row 0 is at position nb + 16 W i).
 template <int D, int W, int NP, bool MASKED, bool MODS>
 __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&so)[2], const LaneOffsets<D> &lo,
                                            const uint32_t (&qf)[D / 16][2], float qs0, float qs1, float sm24,
-                                           int lane, int nb, int t0, int t1, const Int4Params &p,
-                                           const ScoreMods &md) {
+                                           int lane, int nb, int t0, int t1, int lim0, int lim1,
+                                           const Int4Params &p, const ScoreMods &md) {
   using Gm = Int4Geom<D>;
   const int g = lane >> 2;
   PageIn pg[NP];
@@ -484,14 +490,18 @@ __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&s
       }
     }
   }
-  bool ok0 = true, ok1 = true;
+  bool ok00 = true, ok01 = true, ok10 = true, ok11 = true;  // (token g / g + 8, column 2t / 2t + 1)
   if (MASKED) {
-    ok0 = nb + g >= t0 && nb + g < t1;
-    ok1 = nb + g + 8 >= t0 && nb + g + 8 < t1;
-    pg[0].s[0] = ok0 ? pg[0].s[0] : -INFINITY;
-    pg[0].s[1] = ok0 ? pg[0].s[1] : -INFINITY;
-    pg[0].s[2] = ok1 ? pg[0].s[2] : -INFINITY;
-    pg[0].s[3] = ok1 ? pg[0].s[3] : -INFINITY;
+    const bool ok0 = nb + g >= t0 && nb + g < t1;
+    const bool ok1 = nb + g + 8 >= t0 && nb + g + 8 < t1;
+    ok00 = ok0 && nb + g < lim0;
+    ok01 = ok0 && nb + g < lim1;
+    ok10 = ok1 && nb + g + 8 < lim0;
+    ok11 = ok1 && nb + g + 8 < lim1;
+    pg[0].s[0] = ok00 ? pg[0].s[0] : -INFINITY;
+    pg[0].s[1] = ok01 ? pg[0].s[1] : -INFINITY;
+    pg[0].s[2] = ok10 ? pg[0].s[2] : -INFINITY;
+    pg[0].s[3] = ok11 ? pg[0].s[3] : -INFINITY;
   }
   // ---- online softmax (base 2) against a lazily raised reference maximum: the running sums are
   // rescaled only when a new score exceeds the reference by more than kSlack, so the weights
@@ -533,10 +543,10 @@ __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&s
     // P_v = p * scale_v (fp16), and sum P_v * zp_v for the zero-point correction
     float w00 = p00 * pg[i].sv0, w10 = p10 * pg[i].sv1, w01 = p01 * pg[i].sv0, w11 = p11 * pg[i].sv1;
     if (MASKED) {
-      w00 = ok0 ? w00 : 0.f;
-      w01 = ok0 ? w01 : 0.f;
-      w10 = ok1 ? w10 : 0.f;
-      w11 = ok1 ? w11 : 0.f;
+      w00 = ok00 ? w00 : 0.f;
+      w01 = ok01 ? w01 : 0.f;
+      w10 = ok10 ? w10 : 0.f;
+      w11 = ok11 ? w11 : 0.f;
     }
     const __half2 h0 = __floats2half2_rn(w00, w10), h1 = __floats2half2_rn(w01, w11);
     const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
@@ -777,7 +787,9 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     const int nb = (x + off) * kPage;  // position of the page's row 0 in its sequence
     const int sj1 = sj + 1 == NS ? 0 : sj + 1, rj1 = sj + 1 == NS ? rj + 1 : rj;
     const uint32_t so[2] = {base + sj * Gm::STAGE, base + sj1 * Gm::STAGE};
-    const bool pair = nb >= t0 && nb + (W + 1) * kPage <= t1 && x + W < pe_x;  // two full pages of the piece
+    // two full pages of the piece, both below every column's causal limit
+    const bool pair = nb >= t0 && nb + (W + 1) * kPage <= min(t1, cur.L - a.Q + 1) && x + W < pe_x;
+    const int lim0 = cur.L - a.Q + 1 + (2 * (lane & 3)) / a.G, lim1 = cur.L - a.Q + 1 + (2 * (lane & 3) + 1) / a.G;
     if (warp == 0 && nxt <= (pair ? j + 1 : j) && !produce(pair ? j + 1 : j)) {
       abort = true;
       if (lane == 0) atomicOr(&g_flags_decode_int4, ERR_TIMEOUT);
@@ -789,7 +801,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
         break;
       }
       if (warp == 0) produce(-1);  // the slots freed meanwhile (at the start: the unused ones)
-      int4_pages<D, W, 2, false, MODS>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, p, md);
+      int4_pages<D, W, 2, false, MODS>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, lim0, lim1, p, md);
       mbar_arrive(smem_u32(&s_empty[sj]));
       mbar_arrive(smem_u32(&s_empty[sj1]));
       j += 2;
@@ -801,7 +813,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
         break;
       }
       if (warp == 0) produce(-1);  // the slots freed meanwhile (at the start: the unused ones)
-      int4_pages<D, W, 1, true, MODS>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, p, md);
+      int4_pages<D, W, 1, true, MODS>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, lim0, lim1, p, md);
       mbar_arrive(smem_u32(&s_empty[sj]));
       j += 1;
       sj = sj1;
@@ -884,8 +896,11 @@ extern "C" kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache
     return KVQ_ERR_INVALID_ARG;
   if (mods && (mods->sliding_window < 0 || !(mods->softcap >= 0.f) || !(mods->softcap < INFINITY) ||
                (mods->sinks && !aligned(mods->sinks, 4)) ||
-               (mods->alibi_slopes && !aligned(mods->alibi_slopes, 4))))
+               (mods->alibi_slopes && !aligned(mods->alibi_slopes, 4)) || mods->q_len < 0))
     return KVQ_ERR_INVALID_ARG;
+  const int Q = mods && mods->q_len > 1 ? mods->q_len : 1;  // query tokens per sequence
+  if (Q > 1 && (Hk < 1 || Hq % Hk != 0 || (Hq / Hk) * Q > 8 || mods->sliding_window > 0 || mods->alibi_slopes))
+    return KVQ_ERR_UNSUPPORTED;  // G * Q MMA columns; window and ALiBi are single-token here
   if (Hq % Hk != 0) return KVQ_ERR_INVALID_ARG;
   if (out_dtype != KVQ_BF16 && out_dtype != KVQ_F16 && out_dtype != KVQ_F32) return KVQ_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return KVQ_ERR_UNSUPPORTED;
@@ -903,7 +918,7 @@ extern "C" kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache
       !aligned(out, 16) || !aligned(workspace, 16) || (rht_signs && !aligned(rht_signs, 16)))
     return KVQ_ERR_INVALID_ARG;
   if (max_blocks < 1) return KVQ_ERR_INVALID_ARG;
-  if (workspace_bytes < kvq::workspace_bytes(B, Hq, D, plan)) return KVQ_ERR_WORKSPACE;
+  if (workspace_bytes < kvq::workspace_bytes(B, Q * Hq, D, plan)) return KVQ_ERR_WORKSPACE;
 
   Int4Params p;
   SplitArgs &sa = p.s;
@@ -911,14 +926,15 @@ extern "C" kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache
   sa.max_blocks = max_blocks;
   sa.num_splits = num_splits;
   sa.B = B;
-  sa.Hq = Hq;
+  sa.Hq = Q * Hq;  // output rows per sequence
+  sa.Q = Q;
   sa.Hk = Hk;
   sa.G = Hq / Hk;
   sa.heads_per_cta = plan.heads_per_cta;
   sa.warps_per_head = plan.warps_per_head;
   sa.seg_ctas = plan.seg_ctas;
   sa.slots = plan.slots;
-  workspace_carve(workspace, B, Hq, D, plan, &sa.part_o, &sa.part_lse, &sa.seg_first, &sa.seg_last);
+  workspace_carve(workspace, B, Q * Hq, D, plan, &sa.part_o, &sa.part_lse, &sa.seg_first, &sa.seg_last);
   sa.signs = rht_signs;
   sa.out = out;
   sa.out_dtype = out_dtype;

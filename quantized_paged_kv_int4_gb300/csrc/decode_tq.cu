@@ -401,6 +401,7 @@ extern "C" kvq_status kvq_decode_tq(const float *q, const uint8_t *kv_cache, int
   sa.Hq = Hq;
   sa.Hk = Hk;
   sa.G = Hq / Hk;
+  sa.Q = 1;
   sa.heads_per_cta = plan.heads_per_cta;
   sa.warps_per_head = plan.warps_per_head;
   sa.seg_ctas = plan.seg_ctas;

@@ -466,6 +466,7 @@ extern "C" kvq_status kvq_decode_tq_mse(const float *q, const float *rotation, c
   sa.Hq = Hq;
   sa.Hk = Hk;
   sa.G = Hq / Hk;
+  sa.Q = 1;
   sa.heads_per_cta = plan.heads_per_cta;
   sa.warps_per_head = plan.warps_per_head;
   sa.seg_ctas = plan.seg_ctas;

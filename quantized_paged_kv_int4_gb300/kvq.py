@@ -37,7 +37,8 @@ c_i32, c_i64, c_sz, c_p, c_f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
 
 class ScoreMods(ctypes.Structure):
     """kvq_score_mods (include/kvq.h)."""
-    _fields_ = [("sliding_window", c_i32), ("softcap", c_f32), ("sinks", c_p), ("alibi_slopes", c_p)]
+    _fields_ = [("sliding_window", c_i32), ("softcap", c_f32), ("sinks", c_p), ("alibi_slopes", c_p),
+                ("q_len", c_i32)]
 
 
 _SIGS = {
@@ -177,11 +178,11 @@ def _workspace(workspace, B, Hq, Hk, D, num_splits, device):
 
 def kvq_decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, rht_signs, softmax_scale,
                     out=None, workspace=None, num_splits=0, out_dtype=None, stream=None,
-                    sliding_window=0, softcap=0.0, sinks=None, alibi_slopes=None):
-    """unified_attention_int4 (decode): q [B, Hq, D] bf16 -> out [B, Hq, D]. Returns out.
+                    sliding_window=0, softcap=0.0, sinks=None, alibi_slopes=None, q_len=1):
+    """unified_attention_int4 (decode): q [B * q_len, Hq, D] bf16 -> out [B * q_len, Hq, D]. Returns out.
 
     sliding_window / softcap / sinks ([Hq] fp32) / alibi_slopes ([Hq] fp32): the score modifiers
-    (kvq_decode_int4_mods); all off by default."""
+    (kvq_decode_int4_mods); all off by default. q_len > 1: multi-token (causal) decode."""
     _need(q, "q", torch.bfloat16)
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
         _need(t, n, torch.uint8)
@@ -191,19 +192,22 @@ def kvq_decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens
     _need(seq_lens, "seq_lens", torch.int32)
     if rht_signs is not None:
         _need(rht_signs, "rht_signs", torch.float32)
-    B, Hq, D = q.shape
+    BQ, Hq, D = q.shape
+    if q_len < 1 or BQ % q_len:
+        raise ValueError("q must hold q_len rows per sequence")
+    B = BQ // q_len
     nb, bs, Hk = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
     if out is None:
-        out = torch.empty((B, Hq, D), dtype=out_dtype or torch.float32, device=q.device)
+        out = torch.empty((BQ, Hq, D), dtype=out_dtype or torch.float32, device=q.device)
     _need(out, "out")
-    workspace = _workspace(workspace, B, Hq, Hk, D, num_splits, q.device)
-    if sliding_window or softcap or sinks is not None or alibi_slopes is not None:
+    workspace = _workspace(workspace, B, q_len * Hq, Hk, D, num_splits, q.device)
+    if sliding_window or softcap or sinks is not None or alibi_slopes is not None or q_len > 1:
         for t, n in ((sinks, "sinks"), (alibi_slopes, "alibi_slopes")):
             if t is not None:
                 _need(t, n, torch.float32)
                 if t.numel() != Hq:
                     raise ValueError("%s must have Hq = %d entries" % (n, Hq))
-        mods = ScoreMods(int(sliding_window), float(softcap), _ptr(sinks), _ptr(alibi_slopes))
+        mods = ScoreMods(int(sliding_window), float(softcap), _ptr(sinks), _ptr(alibi_slopes), int(q_len))
         _check(lib().kvq_decode_int4_mods(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                                           _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(rht_signs),
                                           float(softmax_scale), num_splits, _ptr(workspace), workspace.numel(),
