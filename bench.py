@@ -50,7 +50,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--workload", default="llama3_8b_int4",
-                    choices=["llama3_8b_int4", "llama3_8b_int4_mods", "long_context_int4", "turboquant_fp8_v4",
+                    choices=["llama3_8b_int4", "llama3_8b_int4_mods", "llama3_8b_int4_q2", "long_context_int4",
+                             "turboquant_fp8_v4",
                              "turboquant_fp8_v3", "turboquant_mse_k3v4", "write_fwht", "kpool_write",
                              "kpool_decode_update"])
     ap.add_argument("--replicas", type=int, default=4)
@@ -261,6 +262,15 @@ def run_kvq(args, dist):
     def write(r):
         kvq.kvq_write_int4(r.k_new, r.v_new, r.kc, r.vc, r.ks, r.vs, r.slots, signs, stream=stream)
 
+    Q = 2 if wl == "llama3_8b_int4_q2" else 1  # speculative verify: two query tokens per sequence
+    if Q > 1:
+        mods = dict(q_len=Q)
+        gq = torch.Generator().manual_seed(77)
+        for r in reps:
+            r.q = torch.randn((B * Q, Hq, D), generator=gq).to(torch.bfloat16).to(dev)
+            r.out = torch.empty((B * Q, Hq, D), dtype=torch.bfloat16, device=dev)
+        ws = torch.zeros((kvq.kvq_decode_workspace_bytes(B, Q * Hq, Hk, D, S),), dtype=torch.uint8, device=dev)
+
     def decode(r):
         kvq.kvq_decode_int4(r.q, r.kc, r.vc, r.ks, r.vs, r.bt, r.lens, signs, scale, out=r.out, workspace=ws,
                             num_splits=S, stream=stream, **mods)
@@ -282,8 +292,8 @@ def run_kvq(args, dist):
         gw.append(a)
         gd.append(b)
 
-    dec_bytes, kv_bytes = int4_decode_bytes(case.seq_lens, Hq, Hk, D, window=mods.get("sliding_window", 0))
-    dec_bytes += 8 * Hq if mods else 0  # sinks and slopes
+    dec_bytes, kv_bytes = int4_decode_bytes(case.seq_lens, Q * Hq, Hk, D, window=mods.get("sliding_window", 0))
+    dec_bytes += 8 * Hq if "sinks" in mods else 0  # sinks and slopes
     wr_bytes = B * Hk * (2 * D * 2 + 2 * (D // 2 + 4)) + 8 * B
     res = timed_steps(args, dist, stream, lambda i: gw[i % nrep].replay(), lambda i: gd[i % nrep].replay(),
                       dev.index)
@@ -291,7 +301,7 @@ def run_kvq(args, dist):
     assert st == 0, flags
 
     e2e = None
-    if not args.no_e2e and not mods:
+    if not args.no_e2e and not mods and Q == 1:
         e2e = e2e_int4(args, reps[0], case, signs, scale, ws, S, dev, stream, dec_bytes)
     cfg = {"workload": wl, "B": B, "Hq": Hq, "Hk": Hk, "D": D, "block_size": 16,
            "seq_lens": "U[1024,8192] seed 0, sum %d" % sum(case.seq_lens) if wl != "long_context_int4"
@@ -302,11 +312,14 @@ def run_kvq(args, dist):
                   "no L2 reuse across steps" % (nrep, kv_bytes / 1e6, nrep, kv_bytes / 1e6)) if nrep > 1
            else "single %.0f MB cache read per step (> L2)" % (kv_bytes / 1e6),
            "decode_bytes_per_step": dec_bytes, "kv_cache_bytes_per_step": kv_bytes, "write_bytes_per_step": wr_bytes}
-    if mods:
+    if Q > 1:
+        cfg["q_len"] = "%d query tokens per sequence (causal; keys read once for both)" % Q
+    if "sinks" in mods:
         cfg["score_mods"] = "sliding_window 4096 (keys read: %d of %d), softcap 30, ALiBi slopes 2^(-8(h+1)/Hq), sinks" % (
             kv_bytes // (Hk * (D + 8)), sum(case.seq_lens))
     kernels = 3  # write, split-KV decode, merge
-    tag = {"llama3_8b_int4": "decode_int4", "long_context_int4": "decode_int4_long_context"}.get(wl, "decode_int4_mods")
+    tag = {"llama3_8b_int4": "decode_int4", "long_context_int4": "decode_int4_long_context",
+           "llama3_8b_int4_q2": "decode_int4_q2"}.get(wl, "decode_int4_mods")
     return finish(args, dist, res, dec_bytes, cfg, e2e, kernels, tag,
                   ["quantized_paged_kv_int4_gb300/csrc/decode_int4.cu",
                    "quantized_paged_kv_int4_gb300/csrc/decode_common.cuh",

@@ -267,23 +267,27 @@ __device__ __forceinline__ void for_each_piece(const SplitArgs &a, unsigned *fla
 
 // Writes one warp's partial: thread (g, t) holds, for heads 2t and 2t + 1, the D/8 consecutive
 // dims [g * D/8, (g+1) * D/8) in o0 / o1; lse in base 2.
-template <int D>
+// MULTI: a.Q may exceed 1 (multi-token decode); otherwise column n is head h * G + n.
+template <int D, bool MULTI = false>
 __device__ __forceinline__ void store_partial(const SplitArgs &a, long long slot, int sub, int h,
                                               int lane, const float (&o0)[D / 8],
                                               const float (&o1)[D / 8], float lse0, float lse1) {
   const int g = lane >> 2, t = lane & 3;
   const long long row = (slot * a.warps_per_head + sub) * a.Hq;
-  const int n0 = 2 * t, n1 = 2 * t + 1, heads = a.Hq / a.Q;
+  const int n0 = 2 * t, n1 = 2 * t + 1, ncol = MULTI ? a.G * a.Q : a.G;
   // MMA column n = query token n / G, head h * G + n % G of it
-  auto row_of = [&](int n) { return row + (n / a.G) * heads + static_cast<long long>(h) * a.G + n % a.G; };
-  if (n0 < a.G * a.Q) {
+  auto row_of = [&](int n) {
+    return !MULTI || a.Q == 1 ? row + static_cast<long long>(h) * a.G + n
+                              : row + (n / a.G) * (a.Hq / a.Q) + static_cast<long long>(h) * a.G + n % a.G;
+  };
+  if (n0 < ncol) {
     const long long r0 = row_of(n0);
     float4 *dst = reinterpret_cast<float4 *>(a.part_o + r0 * D + g * (D / 8));
 #pragma unroll
     for (int i = 0; i < D / 32; ++i) dst[i] = make_float4(o0[4 * i], o0[4 * i + 1], o0[4 * i + 2], o0[4 * i + 3]);
     if (g == 0) a.part_lse[r0] = lse0;
   }
-  if (n1 < a.G * a.Q) {
+  if (n1 < ncol) {
     const long long r1 = row_of(n1);
     float4 *dst = reinterpret_cast<float4 *>(a.part_o + r1 * D + g * (D / 8));
 #pragma unroll

@@ -223,10 +223,17 @@ struct PieceState {
 // Start copying the G * Q raw query rows of (sequence b, kv head h) -- for each of the Q query
 // tokens G contiguous rows, G * D bf16 -- into this warp's area (16-byte cp.async per lane), row
 // i * G + g for token i, head h * G + g; load_query waits for them.
-template <int D>
+template <int D, bool MTOK>
 __device__ __forceinline__ void fetch_query(const Int4Params &p, uint8_t *qarea, int b, int h, int lane) {
   const int G = p.s.G, per = G * D / 8, heads = p.s.Hq / p.s.Q;
   const uint32_t dst = smem_u32(qarea);
+  if (!MTOK || p.s.Q == 1) {  // one token: G contiguous rows
+    const uint8_t *src = reinterpret_cast<const uint8_t *>(
+        p.q + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(h) * G) * D);
+    for (int c = lane; c < per; c += 32) cp_async<16>(dst + 16 * c, src + 16 * c, true);
+    cp_async_commit();
+    return;
+  }
   for (int c = lane; c < p.s.Q * per; c += 32) {
     const int i = c / per, w = c - i * per;
     const uint8_t *src = reinterpret_cast<const uint8_t *>(
@@ -236,12 +243,12 @@ __device__ __forceinline__ void fetch_query(const Int4Params &p, uint8_t *qarea,
   cp_async_commit();
 }
 
-template <int D>
+template <int D, bool MTOK>
 __device__ __forceinline__ void load_query(const Int4Params &p, uint8_t *qarea, int b, int h, int lane,
                                            uint32_t (&qf)[D / 16][2], float &qs0, float &qs1, bool fetched) {
   using Gm = Int4Geom<D>;
   constexpr int J = D / 32;
-  const int g = lane >> 2, t = lane & 3, G = p.s.G * p.s.Q;  // MMA columns in use
+  const int g = lane >> 2, t = lane & 3, G = MTOK ? p.s.G * p.s.Q : p.s.G;  // MMA columns in use
   __half *qh = reinterpret_cast<__half *>(qarea);
   float *qsum = reinterpret_cast<float *>(qarea + 8 * D * 2);
   // The raw rows land in this warp's area (fetch_query, issued early when possible); each head is
@@ -249,7 +256,7 @@ __device__ __forceinline__ void load_query(const Int4Params &p, uint8_t *qarea, 
   __syncwarp();
   if (!fetched) {
     cp_async_wait<0>();  // a prefetch of another sequence's rows may still be landing here
-    fetch_query<D>(p, qarea, b, h, lane);
+    fetch_query<D, MTOK>(p, qarea, b, h, lane);
   }
   cp_async_wait<0>();
   float sg[J];
@@ -464,7 +471,7 @@ struct ScoreMods {
 // multiplied; in multi-token decode a column's keys also stop at its causal limit (lim0 / lim1
 // for the lane's columns 2t / 2t + 1, exclusive). MODS: apply the score modifiers md (page i's
 // row 0 is at position nb + 16 W i).
-template <int D, int W, int NP, bool MASKED, bool MODS>
+template <int D, int W, int NP, bool MASKED, bool MODS, bool MTOK>
 __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&so)[2], const LaneOffsets<D> &lo,
                                            const uint32_t (&qf)[D / 16][2], float qs0, float qs1, float sm24,
                                            int lane, int nb, int t0, int t1, int lim0, int lim1,
@@ -494,10 +501,14 @@ __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&s
   if (MASKED) {
     const bool ok0 = nb + g >= t0 && nb + g < t1;
     const bool ok1 = nb + g + 8 >= t0 && nb + g + 8 < t1;
-    ok00 = ok0 && nb + g < lim0;
-    ok01 = ok0 && nb + g < lim1;
-    ok10 = ok1 && nb + g + 8 < lim0;
-    ok11 = ok1 && nb + g + 8 < lim1;
+    ok00 = ok01 = ok0;
+    ok10 = ok11 = ok1;
+    if constexpr (MTOK) {  // multi-token decode: each column's causal limit
+      ok00 = ok00 && nb + g < lim0;
+      ok01 = ok01 && nb + g < lim1;
+      ok10 = ok10 && nb + g + 8 < lim0;
+      ok11 = ok11 && nb + g + 8 < lim1;
+    }
     pg[0].s[0] = ok00 ? pg[0].s[0] : -INFINITY;
     pg[0].s[1] = ok01 ? pg[0].s[1] : -INFINITY;
     pg[0].s[2] = ok10 ? pg[0].s[2] : -INFINITY;
@@ -562,7 +573,7 @@ __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&s
 
 // Epilogue of one piece: undo the subnormal scaling, apply the zero-point term, normalise, and
 // write the warp's partial (an empty piece writes zeros with lse = -inf).
-template <int D>
+template <int D, bool MTOK>
 __device__ __forceinline__ void int4_finish(const SplitArgs &a, PieceState<D> &st, long long slot, int sub,
                                             int h, int lane) {
   using Gm = Int4Geom<D>;
@@ -579,7 +590,7 @@ __device__ __forceinline__ void int4_finish(const SplitArgs &a, PieceState<D> &s
   }
   const float lse0 = l0 > 0.f ? st.m0 + log2f(l0) : -INFINITY;
   const float lse1 = l1 > 0.f ? st.m1 + log2f(l1) : -INFINITY;
-  store_partial<D>(a, slot, sub, h, lane, o0, o1, lse0, lse1);
+  store_partial<D, MTOK>(a, slot, sub, h, lane, o0, o1, lse0, lse1);
 }
 
 // W = warps per kv head (8 / heads per CTA). Stage k of the ring (slot k % NS) holds run pages
@@ -589,8 +600,11 @@ __device__ __forceinline__ void int4_finish(const SplitArgs &a, PieceState<D> &s
 // threads have finished reading it (every thread arrives once). Warp 0 is also the producer: it
 // issued the first NS stages and refills a slot once its s_empty phase completes -- polling
 // without blocking between pages, and blocking only for a stage it needs itself.
-template <int D, int NS, int W, bool MODS>
+// VAR 0: plain; 1: score modifiers (window, soft cap, ALiBi; multi-token decode allowed);
+// 2: multi-token decode only.
+template <int D, int NS, int W, int VAR>
 __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_constant__ Int4Params p) {
+  constexpr bool MODS = VAR == 1, MTOK = VAR != 0;
   using Gm = Int4Geom<D>;
   constexpr int HB = 8 / W;
   constexpr int SCP = 64 * HB < 128 ? 128 : 64 * HB;  // one page's scale block, 128-byte aligned slots
@@ -662,7 +676,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     const long long X0 = run.base + sub;
     while (X0 >= c0.P + c0.np && c0.b < a.B) seq_next<MODS>(a, c0);
     if (c0.b < a.B) {
-      fetch_query<D>(p, qarea, c0.b, h, lane);
+      fetch_query<D, MTOK>(p, qarea, c0.b, h, lane);
       q_prefetched = c0.b;
     }
   }
@@ -738,7 +752,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   md.qpos = cur.L - 1;
   auto finish_piece = [&]() {
     const long long slot = run.fixed ? static_cast<long long>(blockIdx.x) : blockIdx.x + static_cast<long long>(cur.b);
-    int4_finish<D>(a, st, slot, sub, h, lane);
+    int4_finish<D, MTOK>(a, st, slot, sub, h, lane);
     if (!run.fixed && warp == 0 && lane == 0 && blockIdx.y == 0) {
       if (cur.P >= run.base) a.seg_first[cur.b] = static_cast<int>(blockIdx.x);
       if (cur.P + cur.np <= run.end) a.seg_last[cur.b] = static_cast<int>(blockIdx.x);
@@ -772,13 +786,13 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
       md.qpos = cur.L - 1;
     }
     if (!have_q) {
-      load_query<D>(p, qarea, cur.b, h, lane, qf, qs0, qs1, q_prefetched == cur.b);
+      load_query<D, MTOK>(p, qarea, cur.b, h, lane, qf, qs0, qs1, q_prefetched == cur.b);
       q_prefetched = -1;
       if (pe_x < run.n && !run.fixed) {  // the run goes on into another sequence: fetch its query now
         SeqCursor nx = cur;
         seq_next<MODS>(a, nx);
         if (nx.b < a.B) {
-          fetch_query<D>(p, qarea, nx.b, h, lane);
+          fetch_query<D, MTOK>(p, qarea, nx.b, h, lane);
           q_prefetched = nx.b;
         }
       }
@@ -787,9 +801,12 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     const int nb = (x + off) * kPage;  // position of the page's row 0 in its sequence
     const int sj1 = sj + 1 == NS ? 0 : sj + 1, rj1 = sj + 1 == NS ? rj + 1 : rj;
     const uint32_t so[2] = {base + sj * Gm::STAGE, base + sj1 * Gm::STAGE};
-    // two full pages of the piece, both below every column's causal limit
-    const bool pair = nb >= t0 && nb + (W + 1) * kPage <= min(t1, cur.L - a.Q + 1) && x + W < pe_x;
-    const int lim0 = cur.L - a.Q + 1 + (2 * (lane & 3)) / a.G, lim1 = cur.L - a.Q + 1 + (2 * (lane & 3) + 1) / a.G;
+    // two full pages of the piece, both below every column's causal limit (multi-token decode
+    // runs in the modifier kernel; elsewhere Q = 1 and the limit is the sequence end)
+    const int tpair = MTOK ? min(t1, cur.L - a.Q + 1) : t1;
+    const bool pair = nb >= t0 && nb + (W + 1) * kPage <= tpair && x + W < pe_x;
+    const int lim0 = MTOK ? cur.L - a.Q + 1 + (2 * (lane & 3)) / a.G : 0;
+    const int lim1 = MTOK ? cur.L - a.Q + 1 + (2 * (lane & 3) + 1) / a.G : 0;
     if (warp == 0 && nxt <= (pair ? j + 1 : j) && !produce(pair ? j + 1 : j)) {
       abort = true;
       if (lane == 0) atomicOr(&g_flags_decode_int4, ERR_TIMEOUT);
@@ -801,7 +818,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
         break;
       }
       if (warp == 0) produce(-1);  // the slots freed meanwhile (at the start: the unused ones)
-      int4_pages<D, W, 2, false, MODS>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, lim0, lim1, p, md);
+      int4_pages<D, W, 2, false, MODS, MTOK>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, lim0, lim1, p, md);
       mbar_arrive(smem_u32(&s_empty[sj]));
       mbar_arrive(smem_u32(&s_empty[sj1]));
       j += 2;
@@ -813,7 +830,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
         break;
       }
       if (warp == 0) produce(-1);  // the slots freed meanwhile (at the start: the unused ones)
-      int4_pages<D, W, 1, true, MODS>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, lim0, lim1, p, md);
+      int4_pages<D, W, 1, true, MODS, MTOK>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, lim0, lim1, p, md);
       mbar_arrive(smem_u32(&s_empty[sj]));
       j += 1;
       sj = sj1;
@@ -848,19 +865,19 @@ bool take_flags_decode_int4(cudaStream_t stream, unsigned *host_word) {
                                  cudaMemcpyHostToDevice, stream) == cudaSuccess;
 }
 
-template <int D, int W, bool MODS>
+template <int D, int W, int VAR>
 static kvq_status launch_int4_w(const Int4Params &p, const SplitPlan &plan, cudaStream_t s) {
   const size_t smem = int4_smem_bytes<D>();
   static bool attr_set = false;  // per process; the attribute is per function, not per device
   if (!attr_set) {
-    if (cudaFuncSetAttribute(decode_int4_kernel<D, kStagesInt4, W, MODS>,
+    if (cudaFuncSetAttribute(decode_int4_kernel<D, kStagesInt4, W, VAR>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return KVQ_ERR_CUDA;
     attr_set = true;
   }
   const dim3 grid(plan.seg_ctas, plan.head_groups);
-  decode_int4_kernel<D, kStagesInt4, W, MODS><<<grid, 256, smem, s>>>(p);
+  decode_int4_kernel<D, kStagesInt4, W, VAR><<<grid, 256, smem, s>>>(p);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   const long long rows = static_cast<long long>(p.s.B) * p.s.Hq;
   if (launch_dependent(merge_kernel<D>, dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), s, p.s) != cudaSuccess)
@@ -868,13 +885,13 @@ static kvq_status launch_int4_w(const Int4Params &p, const SplitPlan &plan, cuda
   return launch_status();
 }
 
-template <int D, bool MODS>
+template <int D, int VAR>
 static kvq_status launch_int4(const Int4Params &p, const SplitPlan &plan, cudaStream_t s) {
   switch (plan.warps_per_head) {
-    case 1: return launch_int4_w<D, 1, MODS>(p, plan, s);
-    case 2: return launch_int4_w<D, 2, MODS>(p, plan, s);
-    case 4: return launch_int4_w<D, 4, MODS>(p, plan, s);
-    case 8: return launch_int4_w<D, 8, MODS>(p, plan, s);
+    case 1: return launch_int4_w<D, 1, VAR>(p, plan, s);
+    case 2: return launch_int4_w<D, 2, VAR>(p, plan, s);
+    case 4: return launch_int4_w<D, 4, VAR>(p, plan, s);
+    case 8: return launch_int4_w<D, 8, VAR>(p, plan, s);
     default: return KVQ_ERR_UNSUPPORTED;
   }
 }
@@ -950,10 +967,13 @@ extern "C" kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache
   p.softcap2 = static_cast<float>(cap2);
   p.inv_softcap2 = cap2 > 0.0 ? static_cast<float>(1.0 / cap2) : 0.f;
   p.alibi = mods ? mods->alibi_slopes : nullptr;
-  const bool score_mods = p.softcap2 > 0.f || p.alibi != nullptr || sa.window > 0;  // sinks: merge only
+  // sinks act in the merge only; window, soft cap and ALiBi need the modifier kernel (which also
+  // takes multi-token decode); multi-token decode alone has its own
+  const int var = (p.softcap2 > 0.f || p.alibi != nullptr || sa.window > 0) ? 1 : (Q > 1 ? 2 : 0);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (D == 128) return score_mods ? launch_int4<128, true>(p, plan, s) : launch_int4<128, false>(p, plan, s);
-  return score_mods ? launch_int4<64, true>(p, plan, s) : launch_int4<64, false>(p, plan, s);
+  if (D == 128)
+    return var == 0 ? launch_int4<128, 0>(p, plan, s) : var == 1 ? launch_int4<128, 1>(p, plan, s) : launch_int4<128, 2>(p, plan, s);
+  return var == 0 ? launch_int4<64, 0>(p, plan, s) : var == 1 ? launch_int4<64, 1>(p, plan, s) : launch_int4<64, 2>(p, plan, s);
 }
 
 extern "C" kvq_status kvq_decode_int4(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
