@@ -68,11 +68,14 @@ __device__ __forceinline__ uint32_t lds16_at(const uint8_t *row, int o) {
   return *reinterpret_cast<const uint16_t *>(row + o);  // o even
 }
 
-// q_rot[r][d] = sum_e q[r][e] * Pi[d][e] (fp32) for 32 rows per CTA, one output dim per thread.
+// q_rot[r][d] = sum_e q[r][e] * Pi[d][e] (fp32) for R = 8 rows per CTA (enough CTAs to fill the
+// GPU for a decode batch), one output dim per thread.
+constexpr int kRotRows = 8;
+
 template <int D>
 __global__ void __launch_bounds__(D) rotate_q_kernel(const float *__restrict__ q, const float *__restrict__ Pi,
                                                      float *__restrict__ q_rot, long long rows) {
-  constexpr int R = 32;
+  constexpr int R = kRotRows;
   __shared__ __align__(16) float s_q[R][D];
   const long long r0 = static_cast<long long>(blockIdx.x) * R;
   const int d = threadIdx.x;
@@ -403,7 +406,7 @@ static kvq_status launch_tq_mse(const TqMseParams &p, const SplitPlan &plan, con
     attr_bytes = smem;
   }
   const long long rows = static_cast<long long>(p.s.B) * p.s.Hq;
-  rotate_q_kernel<D><<<static_cast<unsigned>((rows + 31) / 32), D, 0, s>>>(q, Pi, q_rot, rows);
+  rotate_q_kernel<D><<<static_cast<unsigned>((rows + kRotRows - 1) / kRotRows), D, 0, s>>>(q, Pi, q_rot, rows);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   const dim3 grid(plan.seg_ctas, plan.head_groups);
   decode_tq_mse_kernel<D, KB, VB, kStagesMse><<<grid, 256, smem, s>>>(p, RS);
