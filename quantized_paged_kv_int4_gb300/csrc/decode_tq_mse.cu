@@ -12,10 +12,10 @@
 // GB300 design: the FP8-key kernel's structure (one warp per kv head and run of pages, private
 // cp.async ring, mma.m16n8k16 for both contractions), with whole slots staged: KPS is usually not
 // a multiple of 4 (MSE_BYTES + 2), so each stage row is the slot's bytes and the fields are read
-// from shared memory at any byte offset (aligned words + funnel shifts). A centroid goes to the
-// tensor cores as an fp16 pair hi + lo (one 32-bit table word per centroid in shared memory, so a
-// gather is one conflict-free load); q as fp16 hi + lo as in the FP8 path; three MMAs per k-step
-// (hi.hi, hi.lo, lo.hi) keep ~22 bits of the product.
+// from shared memory at any byte offset (aligned words + funnel shifts). Centroids go to the
+// tensor cores as fp16 hi + lo parts: a pair table in shared memory maps two adjacent indices to
+// the hi pair and the lo pair of an A-fragment register in one 8-byte load; q as fp16 hi + lo as
+// in the FP8 path; three MMAs per k-step (hi.hi, hi.lo, lo.hi) keep ~22 bits of the product.
 
 #include "decode_common.cuh"
 #include "kvq_host.h"
@@ -47,7 +47,10 @@ struct MseGeom {
   static constexpr int KSTEPS = D / 16;
   static constexpr int MT = D / 16;
   static constexpr int QBYTES = 2 * 8 * D * 2;      // fp16 hi and lo
-  static constexpr int TABLE = 64 + 64;             // 16 (hi | lo) words, 16 fp32 squares
+  static constexpr int NPAIR = 1 << (2 * KB);       // index pairs
+  // pair table: entry (i0 | i1 << KB) = {fp16 hi(c_i0) | hi(c_i1) << 16, lo(c_i0) | lo(c_i1) << 16},
+  // then the fp32 sums c_i0^2 + c_i1^2 (NORM_CORRECTION)
+  static constexpr int TABLE = NPAIR * 8 + NPAIR * 4;
 };
 
 // Stage row stride for slot_bytes SB: a multiple of 16 (cp.async destination) whose word stride
@@ -106,7 +109,7 @@ __global__ void __launch_bounds__(D) rotate_q_kernel(const float *__restrict__ q
 
 template <int D, int KB, int VB, int NSTAGE>
 __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring, uint8_t *qarea,
-                                             const uint32_t *table, const float *sq, int RS, int b, int h,
+                                             const uint2 *table, const float *sq, int RS, int b, int h,
                                              int sub, int t0, int t1, long long slot) {
   using Gm = MseGeom<D, KB, VB>;
   const int lane = threadIdx.x & 31;
@@ -212,12 +215,12 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
     float ss0 = 0.f, ss1 = 0.f;  // sum of c^2 over the lane's dims (NORM_CORRECTION)
 #pragma unroll
     for (int ks = 0; ks < Gm::KSTEPS; ++ks) {
-      uint32_t e0[4], e1[4];
+      uint2 e0[2], e1[2];  // elements (4 ks + 2 j, + 1) of rows g, g + 8: one pair-table entry each
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int bit = (4 * ks + j) * KB, wi = bit >> 5, sh = bit & 31;
-        const uint32_t i0 = __funnelshift_r(w0[wi], w0[wi + 1], sh) & ((1u << KB) - 1);
-        const uint32_t i1 = __funnelshift_r(w1[wi], w1[wi + 1], sh) & ((1u << KB) - 1);
+      for (int j = 0; j < 2; ++j) {
+        const int bit = (4 * ks + 2 * j) * KB, wi = bit >> 5, sh = bit & 31;
+        const uint32_t i0 = __funnelshift_r(w0[wi], w0[wi + 1], sh) & ((1u << (2 * KB)) - 1);
+        const uint32_t i1 = __funnelshift_r(w1[wi], w1[wi + 1], sh) & ((1u << (2 * KB)) - 1);
         e0[j] = table[i0];
         e1[j] = table[i1];
         if (p.norm_correction) {
@@ -225,13 +228,9 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
           ss1 += sq[i1];
         }
       }
-      const uint32_t h00 = __byte_perm(e0[0], e0[1], 0x5410), h02 = __byte_perm(e0[2], e0[3], 0x5410);
-      const uint32_t h10 = __byte_perm(e1[0], e1[1], 0x5410), h12 = __byte_perm(e1[2], e1[3], 0x5410);
-      const uint32_t l00 = __byte_perm(e0[0], e0[1], 0x7632), l02 = __byte_perm(e0[2], e0[3], 0x7632);
-      const uint32_t l10 = __byte_perm(e1[0], e1[1], 0x7632), l12 = __byte_perm(e1[2], e1[3], 0x7632);
-      mma_f16_16816(c, h00, h10, h02, h12, qhi[ks][0], qhi[ks][1]);
-      mma_f16_16816(c, h00, h10, h02, h12, qlo[ks][0], qlo[ks][1]);
-      mma_f16_16816(c, l00, l10, l02, l12, qhi[ks][0], qhi[ks][1]);
+      mma_f16_16816(c, e0[0].x, e1[0].x, e0[1].x, e1[1].x, qhi[ks][0], qhi[ks][1]);
+      mma_f16_16816(c, e0[0].x, e1[0].x, e0[1].x, e1[1].x, qlo[ks][0], qlo[ks][1]);
+      mma_f16_16816(c, e0[0].y, e1[0].y, e0[1].y, e1[1].y, qhi[ks][0], qhi[ks][1]);
     }
     // per-token factor: attn_scale * log2(e) * norm (/ |c| under NORM_CORRECTION)
     float f0 = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16_at(row0, Gm::MSE)))) * p.sc_log2;
@@ -358,16 +357,16 @@ __global__ void __launch_bounds__(256, 2) decode_tq_mse_kernel(const TqMseParams
   asm volatile("griddepcontrol.launch_dependents;");  // let the merge kernel's launch begin early
   using Gm = MseGeom<D, KB, VB>;
   const int warp = threadIdx.x >> 5;
-  // the centroid table: word j = fp16 hi | fp16 lo << 16 of centroid j, then the fp32 squares
-  uint32_t *table = reinterpret_cast<uint32_t *>(smem);
-  float *sq = reinterpret_cast<float *>(smem + 64);
-  if (threadIdx.x < (1 << KB)) {
-    const float cv = __ldg(p.centroids + threadIdx.x);
-    const __half hi = __float2half_rn(cv);
-    const __half lo = __float2half_rn(cv - __half2float(hi));
-    table[threadIdx.x] = static_cast<uint32_t>(__half_as_ushort(hi)) |
-                         (static_cast<uint32_t>(__half_as_ushort(lo)) << 16);
-    sq[threadIdx.x] = cv * cv;
+  // the pair table (MseGeom::TABLE): centroids split into fp16 hi + lo, two per entry
+  uint2 *table = reinterpret_cast<uint2 *>(smem);
+  float *sq = reinterpret_cast<float *>(smem + Gm::NPAIR * 8);
+  for (int e = threadIdx.x; e < Gm::NPAIR; e += 256) {
+    const float c0 = __ldg(p.centroids + (e & ((1 << KB) - 1))), c1 = __ldg(p.centroids + (e >> KB));
+    const __half h0 = __float2half_rn(c0), h1 = __float2half_rn(c1);
+    const __half l0 = __float2half_rn(c0 - __half2float(h0)), l1 = __float2half_rn(c1 - __half2float(h1));
+    table[e] = make_uint2(static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16),
+                          static_cast<uint32_t>(__half_as_ushort(l0)) | (static_cast<uint32_t>(__half_as_ushort(l1)) << 16));
+    sq[e] = c0 * c0 + c1 * c1;
   }
   __syncthreads();
   uint8_t *ring = smem + Gm::TABLE + warp * (NSTAGE * kPage * RS + Gm::QBYTES);
