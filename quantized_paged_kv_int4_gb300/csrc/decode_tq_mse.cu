@@ -107,6 +107,16 @@ __global__ void __launch_bounds__(D) rotate_q_kernel(const float *__restrict__ q
     if (r0 + r < rows) q_rot[(r0 + r) * D + d] = acc[r];
 }
 
+// byte offset into the pair table (8-byte entries) of the 2 KB-bit field at bit `bit` (a
+// compile-time constant) of the index words w: the field shifted to bit 3 and masked
+template <int KB>
+__device__ __forceinline__ uint32_t pair_offset(const uint32_t *w, int bit) {
+  constexpr uint32_t mask = ((1u << (2 * KB)) - 1) << 3;
+  const int wi = bit >> 5, sh = bit & 31;
+  if (sh >= 3) return __funnelshift_r(w[wi], w[wi + 1], sh - 3) & mask;
+  return (w[wi] << (3 - sh)) & mask;
+}
+
 template <int D, int KB, int VB, int NSTAGE>
 __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring, uint8_t *qarea,
                                              const uint2 *table, const float *sq, int RS, int b, int h,
@@ -117,6 +127,7 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
   const int G = p.s.G, WPH = p.s.warps_per_head, Hk = p.s.Hk;
   const int SB = p.slot_bytes, KPS = p.kps;
   const int STAGE = kPage * RS;
+  const uint8_t *tb = reinterpret_cast<const uint8_t *>(table);
 
   const int pg0 = t0 / kPage, pglast = (t1 - 1) / kPage;
   const int first = pg0 + sub;
@@ -165,6 +176,9 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
   const long long page_bytes = kPage * row_stride;
   const uint8_t *head = p.cache + static_cast<long long>(h) * SB;
   const int chunks = SB / 16;  // 16-byte pieces of one slot
+  // piece i = lane + 32 n of a page is row i / chunks, piece i % chunks: stepped without division
+  const int r_l = lane / chunks, c_l = lane - r_l * chunks;
+  const int dr = 32 / chunks, dc = 32 - dr * chunks;
   auto issue = [&](int k) {
     const int kk = k & 31;
     if (k > 0 && kk == 0) {
@@ -177,9 +191,14 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
     if (in && !ok && lane == 0) atomicOr(&g_flags_decode_tq_mse, ERR_BLOCK);
     const uint32_t st = ring_s + (k % NSTAGE) * STAGE;
     const uint8_t *base = head + static_cast<long long>(ok ? blk : 0) * page_bytes;
-    for (int i = lane; i < kPage * chunks; i += 32) {
-      const int r = i / chunks, c = i - r * chunks;
+    for (int r = r_l, c = c_l; r < kPage;) {
       cp_async<16>(st + r * RS + 16 * c, base + r * row_stride + 16 * c, ok);
+      r += dr;
+      c += dc;
+      if (c >= chunks) {
+        c -= chunks;
+        ++r;
+      }
     }
     cp_async_commit();
   };
@@ -218,14 +237,13 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
       uint2 e0[2], e1[2];  // elements (4 ks + 2 j, + 1) of rows g, g + 8: one pair-table entry each
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int bit = (4 * ks + 2 * j) * KB, wi = bit >> 5, sh = bit & 31;
-        const uint32_t i0 = __funnelshift_r(w0[wi], w0[wi + 1], sh) & ((1u << (2 * KB)) - 1);
-        const uint32_t i1 = __funnelshift_r(w1[wi], w1[wi + 1], sh) & ((1u << (2 * KB)) - 1);
-        e0[j] = table[i0];
-        e1[j] = table[i1];
+        const int bit = (4 * ks + 2 * j) * KB;
+        const uint32_t o0 = pair_offset<KB>(w0, bit), o1 = pair_offset<KB>(w1, bit);
+        e0[j] = *reinterpret_cast<const uint2 *>(tb + o0);
+        e1[j] = *reinterpret_cast<const uint2 *>(tb + o1);
         if (p.norm_correction) {
-          ss0 += sq[i0];
-          ss1 += sq[i1];
+          ss0 += sq[o0 >> 3];
+          ss1 += sq[o1 >> 3];
         }
       }
       mma_f16_16816(c, e0[0].x, e1[0].x, e0[1].x, e1[1].x, qhi[ks][0], qhi[ks][1]);
