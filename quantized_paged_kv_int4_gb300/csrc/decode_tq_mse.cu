@@ -49,8 +49,12 @@ struct MseGeom {
   static constexpr int QBYTES = 2 * 8 * D * 2;      // fp16 hi and lo
   static constexpr int NPAIR = 1 << (2 * KB);       // index pairs
   // pair table: entry (i0 | i1 << KB) = {fp16 hi(c_i0) | hi(c_i1) << 16, lo(c_i0) | lo(c_i1) << 16},
-  // then the fp32 sums c_i0^2 + c_i1^2 (NORM_CORRECTION)
-  static constexpr int TABLE = NPAIR * 8 + NPAIR * 4;
+  // in COPIES copies side by side (entry e of copy c at byte 8 (e COPIES + c): lane l reads copy
+  // l % COPIES, so lanes of a half-warp with different copies never share a bank), then the fp32
+  // sums c_i0^2 + c_i1^2 (NORM_CORRECTION)
+  static constexpr int COPIES = KB == 3 ? 16 : 4;   // 8 KB either way
+  static constexpr int PSH = 3 + (KB == 3 ? 4 : 2); // entry index -> byte offset shift
+  static constexpr int TABLE = NPAIR * 8 * COPIES + NPAIR * 4;
 };
 
 // Stage row stride for slot_bytes SB: a multiple of 16 (cp.async destination) whose word stride
@@ -65,6 +69,21 @@ __host__ __device__ inline int mse_row_stride(int SB) {
 __device__ __forceinline__ uint32_t lds32_at(const uint8_t *row, int o) {
   const uint32_t *w = reinterpret_cast<const uint32_t *>(row + (o & ~3));
   return __funnelshift_r(w[0], w[1], 8 * (o & 3));
+}
+
+// N consecutive 32-bit values of a shared-memory row starting at any byte offset o (N + 1 aligned
+// words, N funnel shifts)
+template <int N>
+__device__ __forceinline__ void lds_words_at(const uint8_t *row, int o, uint32_t (&out)[N]) {
+  const uint32_t *w = reinterpret_cast<const uint32_t *>(row + (o & ~3));
+  const int sh = 8 * (o & 3);
+  uint32_t prev = w[0];
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const uint32_t next = w[i + 1];
+    out[i] = __funnelshift_r(prev, next, sh);
+    prev = next;
+  }
 }
 
 __device__ __forceinline__ uint32_t lds16_at(const uint8_t *row, int o) {
@@ -107,14 +126,14 @@ __global__ void __launch_bounds__(D) rotate_q_kernel(const float *__restrict__ q
     if (r0 + r < rows) q_rot[(r0 + r) * D + d] = acc[r];
 }
 
-// byte offset into the pair table (8-byte entries) of the 2 KB-bit field at bit `bit` (a
-// compile-time constant) of the index words w: the field shifted to bit 3 and masked
-template <int KB>
+// the 2 KB-bit field at bit `bit` (a compile-time constant) of the index words w, shifted to bit
+// PSH and masked: the byte offset of its pair-table entry in copy 0
+template <int KB, int PSH>
 __device__ __forceinline__ uint32_t pair_offset(const uint32_t *w, int bit) {
-  constexpr uint32_t mask = ((1u << (2 * KB)) - 1) << 3;
+  constexpr uint32_t mask = ((1u << (2 * KB)) - 1) << PSH;
   const int wi = bit >> 5, sh = bit & 31;
-  if (sh >= 3) return __funnelshift_r(w[wi], w[wi + 1], sh - 3) & mask;
-  return (w[wi] << (3 - sh)) & mask;
+  if (sh >= PSH) return __funnelshift_r(w[wi], w[wi + 1], sh - PSH) & mask;
+  return (w[wi] << (PSH - sh)) & mask;
 }
 
 template <int D, int KB, int VB, int NSTAGE>
@@ -128,6 +147,7 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
   const int SB = p.slot_bytes, KPS = p.kps;
   const int STAGE = kPage * RS;
   const uint8_t *tb = reinterpret_cast<const uint8_t *>(table);
+  const uint32_t copy_off = (lane & (Gm::COPIES - 1)) << 3;
 
   const int pg0 = t0 / kPage, pglast = (t1 - 1) / kPage;
   const int first = pg0 + sub;
@@ -224,10 +244,15 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
 
     // ---- scores: the lane's KCH dims of rows g, g + 8 as centroid hi / lo fp16 pairs
     uint32_t w0[Gm::KW + 1], w1[Gm::KW + 1];
+    {
+      uint32_t x0[Gm::KW], x1[Gm::KW];
+      lds_words_at(row0, t * (Gm::KCH * KB / 8), x0);
+      lds_words_at(row1, t * (Gm::KCH * KB / 8), x1);
 #pragma unroll
-    for (int i = 0; i < Gm::KW; ++i) {
-      w0[i] = lds32_at(row0, t * (Gm::KCH * KB / 8) + 4 * i);
-      w1[i] = lds32_at(row1, t * (Gm::KCH * KB / 8) + 4 * i);
+      for (int i = 0; i < Gm::KW; ++i) {
+        w0[i] = x0[i];
+        w1[i] = x1[i];
+      }
     }
     w0[Gm::KW] = w1[Gm::KW] = 0u;
     float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -238,12 +263,12 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int bit = (4 * ks + 2 * j) * KB;
-        const uint32_t o0 = pair_offset<KB>(w0, bit), o1 = pair_offset<KB>(w1, bit);
-        e0[j] = *reinterpret_cast<const uint2 *>(tb + o0);
-        e1[j] = *reinterpret_cast<const uint2 *>(tb + o1);
+        const uint32_t o0 = pair_offset<KB, Gm::PSH>(w0, bit), o1 = pair_offset<KB, Gm::PSH>(w1, bit);
+        e0[j] = *reinterpret_cast<const uint2 *>(tb + (o0 | copy_off));
+        e1[j] = *reinterpret_cast<const uint2 *>(tb + (o1 | copy_off));
         if (p.norm_correction) {
-          ss0 += sq[o0 >> 3];
-          ss1 += sq[o1 >> 3];
+          ss0 += sq[o0 >> Gm::PSH];
+          ss1 += sq[o1 >> Gm::PSH];
         }
       }
       mma_f16_16816(c, e0[0].x, e1[0].x, e0[1].x, e1[1].x, qhi[ks][0], qhi[ks][1]);
@@ -304,10 +329,15 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
     const uint8_t *ra = st + (2 * t) * RS, *rb = ra + RS, *rc = ra + 8 * RS, *rd = ra + 9 * RS;
     if constexpr (VB == 4) {
       constexpr int VW = D / 64;  // value words per lane per token (dims 8 g .. of D / 8 per lane)
+      uint32_t wa[VW], wb[VW], wc[VW], wd[VW];
+      const int o = KPS + g * (D / 16);
+      lds_words_at(ra, o, wa);
+      lds_words_at(rb, o, wb);
+      lds_words_at(rc, o, wc);
+      lds_words_at(rd, o, wd);
 #pragma unroll
       for (int wi = 0; wi < VW; ++wi) {
-        const int o = KPS + g * (D / 16) + 4 * wi;
-        const uint32_t va = lds32_at(ra, o), vb = lds32_at(rb, o), vc = lds32_at(rc, o), vd = lds32_at(rd, o);
+        const uint32_t va = wa[wi], vb = wb[wi], vc = wc[wi], vd = wd[wi];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           const uint32_t sel = hf ? 0x7632u : 0x5410u;
@@ -326,8 +356,9 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
       const uint8_t *rows[4] = {ra, rb, rc, rd};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint32_t lo = lds32_at(rows[i], off), hi = lds32_at(rows[i], off + 4);
-        w[i] = (static_cast<unsigned long long>(hi) << 32) | lo;
+        uint32_t x[2];
+        lds_words_at(rows[i], off, x);
+        w[i] = (static_cast<unsigned long long>(x[1]) << 32) | x[0];
       }
 #pragma unroll
       for (int mt = 0; mt < Gm::MT; ++mt) {
@@ -377,14 +408,15 @@ __global__ void __launch_bounds__(256, 2) decode_tq_mse_kernel(const TqMseParams
   const int warp = threadIdx.x >> 5;
   // the pair table (MseGeom::TABLE): centroids split into fp16 hi + lo, two per entry
   uint2 *table = reinterpret_cast<uint2 *>(smem);
-  float *sq = reinterpret_cast<float *>(smem + Gm::NPAIR * 8);
-  for (int e = threadIdx.x; e < Gm::NPAIR; e += 256) {
+  float *sq = reinterpret_cast<float *>(smem + Gm::NPAIR * 8 * Gm::COPIES);
+  for (int i = threadIdx.x; i < Gm::NPAIR * Gm::COPIES; i += 256) {
+    const int e = i / Gm::COPIES;
     const float c0 = __ldg(p.centroids + (e & ((1 << KB) - 1))), c1 = __ldg(p.centroids + (e >> KB));
     const __half h0 = __float2half_rn(c0), h1 = __float2half_rn(c1);
     const __half l0 = __float2half_rn(c0 - __half2float(h0)), l1 = __float2half_rn(c1 - __half2float(h1));
-    table[e] = make_uint2(static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16),
+    table[i] = make_uint2(static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16),
                           static_cast<uint32_t>(__half_as_ushort(l0)) | (static_cast<uint32_t>(__half_as_ushort(l1)) << 16));
-    sq[e] = c0 * c0 + c1 * c1;
+    if (i % Gm::COPIES == 0) sq[e] = c0 * c0 + c1 * c1;
   }
   __syncthreads();
   uint8_t *ring = smem + Gm::TABLE + warp * (NSTAGE * kPage * RS + Gm::QBYTES);
