@@ -136,7 +136,10 @@ __device__ __forceinline__ uint32_t pair_offset(const uint32_t *w, int bit) {
   return (w[wi] << (PSH - sh)) & mask;
 }
 
-template <int D, int KB, int VB, int NSTAGE>
+// PACKQ (G <= 4): the q hi parts of the G heads fill MMA columns 0..3 and the lo parts columns
+// 4..7, so two MMAs per k-step (centroid hi, centroid lo) cover all four products and a
+// shuffle adds column n + 4 into column n; columns 4..7 then repeat heads 0..3 and are dropped.
+template <int D, int KB, int VB, int NSTAGE, bool PACKQ>
 __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring, uint8_t *qarea,
                                              const uint2 *table, const float *sq, int RS, int b, int h,
                                              int sub, int t0, int t1, long long slot) {
@@ -169,15 +172,21 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
 #pragma unroll
       for (int j = 0; j < J; ++j) {
         const int e = lane + 32 * j;
-        const float x = n < G ? qb[n * D + e] : 0.f;
+        const int head = PACKQ ? (n & 3) : n;
+        const float x = head < G ? qb[head * D + e] : 0.f;
         const __half hi = __float2half_rn(x);
-        qh[n * D + e] = hi;
-        qh[8 * D + n * D + e] = __float2half_rn(x - __half2float(hi));
+        const __half lo = __float2half_rn(x - __half2float(hi));
+        if constexpr (PACKQ) {
+          qh[n * D + e] = n < 4 ? hi : lo;
+        } else {
+          qh[n * D + e] = hi;
+          qh[8 * D + n * D + e] = lo;
+        }
       }
     }
   }
   __syncwarp();
-  uint32_t qhi[Gm::KSTEPS][2], qlo[Gm::KSTEPS][2];
+  uint32_t qhi[Gm::KSTEPS][2], qlo[PACKQ ? 1 : Gm::KSTEPS][2];
   {
     const __half *qh = reinterpret_cast<const __half *>(qarea) + g * D + t * Gm::KCH;
 #pragma unroll
@@ -185,8 +194,10 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
       const __half *r = qh + 4 * ks;
       qhi[ks][0] = h2_as_u32(__halves2half2(r[0], r[1]));
       qhi[ks][1] = h2_as_u32(__halves2half2(r[2], r[3]));
-      qlo[ks][0] = h2_as_u32(__halves2half2(r[8 * D + 0], r[8 * D + 1]));
-      qlo[ks][1] = h2_as_u32(__halves2half2(r[8 * D + 2], r[8 * D + 3]));
+      if constexpr (!PACKQ) {
+        qlo[ks][0] = h2_as_u32(__halves2half2(r[8 * D + 0], r[8 * D + 1]));
+        qlo[ks][1] = h2_as_u32(__halves2half2(r[8 * D + 2], r[8 * D + 3]));
+      }
     }
   }
   __syncwarp();
@@ -272,8 +283,12 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
         }
       }
       mma_f16_16816(c, e0[0].x, e1[0].x, e0[1].x, e1[1].x, qhi[ks][0], qhi[ks][1]);
-      mma_f16_16816(c, e0[0].x, e1[0].x, e0[1].x, e1[1].x, qlo[ks][0], qlo[ks][1]);
+      if constexpr (!PACKQ) mma_f16_16816(c, e0[0].x, e1[0].x, e0[1].x, e1[1].x, qlo[ks][0], qlo[ks][1]);
       mma_f16_16816(c, e0[0].y, e1[0].y, e0[1].y, e1[1].y, qhi[ks][0], qhi[ks][1]);
+    }
+    if constexpr (PACKQ) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[i] += __shfl_xor_sync(FULL, c[i], 2);  // hi (t < 2) + lo (t >= 2)
     }
     // per-token factor: attn_scale * log2(e) * norm (/ |c| under NORM_CORRECTION)
     float f0 = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16_at(row0, Gm::MSE)))) * p.sc_log2;
@@ -400,7 +415,7 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
   store_partial<D>(p.s, slot, sub, h, lane, o0, o1, lse0, lse1);
 }
 
-template <int D, int KB, int VB, int NSTAGE>
+template <int D, int KB, int VB, int NSTAGE, bool PACKQ>
 __global__ void __launch_bounds__(256, 2) decode_tq_mse_kernel(const TqMseParams p, int RS) {
   extern __shared__ __align__(16) uint8_t smem[];
   asm volatile("griddepcontrol.launch_dependents;");  // let the merge kernel's launch begin early
@@ -425,7 +440,7 @@ __global__ void __launch_bounds__(256, 2) decode_tq_mse_kernel(const TqMseParams
   const int sub = warp / p.s.heads_per_cta;
   const int h = blockIdx.y * p.s.heads_per_cta + hl;
   for_each_piece(p.s, &g_flags_decode_tq_mse, [&](int b, int t0, int t1, long long slot) {
-    tq_mse_piece<D, KB, VB, NSTAGE>(p, ring, qarea, table, sq, RS, b, h, sub, t0, t1, slot);
+    tq_mse_piece<D, KB, VB, NSTAGE, PACKQ>(p, ring, qarea, table, sq, RS, b, h, sub, t0, t1, slot);
   });
 }
 
@@ -440,7 +455,7 @@ bool take_flags_decode_tq_mse(cudaStream_t stream, unsigned *host_word) {
                                  cudaMemcpyHostToDevice, stream) == cudaSuccess;
 }
 
-template <int D, int KB, int VB>
+template <int D, int KB, int VB, bool PACKQ>
 static kvq_status launch_tq_mse(const TqMseParams &p, const SplitPlan &plan, const float *q, const float *Pi,
                                 float *q_rot, cudaStream_t s) {
   using Gm = MseGeom<D, KB, VB>;
@@ -449,7 +464,7 @@ static kvq_status launch_tq_mse(const TqMseParams &p, const SplitPlan &plan, con
   if (smem > 227 * 1024) return KVQ_ERR_UNSUPPORTED;
   static size_t attr_bytes = 0;  // the largest dynamic size set so far for this instantiation
   if (smem > attr_bytes) {
-    if (cudaFuncSetAttribute(decode_tq_mse_kernel<D, KB, VB, kStagesMse>,
+    if (cudaFuncSetAttribute(decode_tq_mse_kernel<D, KB, VB, kStagesMse, PACKQ>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
       return KVQ_ERR_CUDA;
     attr_bytes = smem;
@@ -458,7 +473,7 @@ static kvq_status launch_tq_mse(const TqMseParams &p, const SplitPlan &plan, con
   rotate_q_kernel<D><<<static_cast<unsigned>((rows + kRotRows - 1) / kRotRows), D, 0, s>>>(q, Pi, q_rot, rows);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   const dim3 grid(plan.seg_ctas, plan.head_groups);
-  decode_tq_mse_kernel<D, KB, VB, kStagesMse><<<grid, 256, smem, s>>>(p, RS);
+  decode_tq_mse_kernel<D, KB, VB, kStagesMse, PACKQ><<<grid, 256, smem, s>>>(p, RS);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   if (launch_dependent(merge_kernel<D>, dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), s, p.s) != cudaSuccess)
     return KVQ_ERR_CUDA;
@@ -539,8 +554,11 @@ extern "C" kvq_status kvq_decode_tq_mse(const float *q, const float *rotation, c
   p.sc_log2 = static_cast<float>(static_cast<double>(attn_scale) * 1.4426950408889634);
   p.num_blocks = num_blocks;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-#define KVQ_MSE_CASE(DD, KK, VV) \
-  if (D == DD && key_bits == KK && value_bits == VV) return launch_tq_mse<DD, KK, VV>(p, plan, q, rotation, q_rot, s);
+  const bool packq = sa.G <= 4;
+#define KVQ_MSE_CASE(DD, KK, VV)                                                                     \
+  if (D == DD && key_bits == KK && value_bits == VV)                                                 \
+    return packq ? launch_tq_mse<DD, KK, VV, true>(p, plan, q, rotation, q_rot, s)                   \
+                 : launch_tq_mse<DD, KK, VV, false>(p, plan, q, rotation, q_rot, s);
   KVQ_MSE_CASE(128, 3, 4)
   KVQ_MSE_CASE(128, 4, 4)
   KVQ_MSE_CASE(128, 3, 3)
