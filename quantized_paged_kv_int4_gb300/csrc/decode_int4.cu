@@ -16,10 +16,10 @@
 // four TMA copies per page: one 4-D box of the K pool (HB heads x 16 tokens x D/2 bytes, stored
 // [head][token][row] with the 64B/32B swizzle that keeps the fragment reads conflict-free), the
 // same for V, and the page's two blocks of scale words. Warp w reads tile w of every stage
-// (head w % HB of page w / HB) and, when done with it, adds one to the stage's release counter;
-// the warp that brings it to 8 refills the stage with the pages NS stages ahead. So there is no
-// producer warp and no block-wide barrier after setup; waits on the stage barriers are bounded
-// and report a flag. Both contractions run on the tensor cores (mma.m16n8k16, fp16 operands,
+// (head w % HB of page w / HB) and, when done with it, arrives on the stage's empty barrier;
+// warp 0, a consumer like the others, also refills each stage once that barrier completes
+// (polled between its pages, so there is no dedicated producer warp and no block-wide barrier
+// after setup). Waits on the stage barriers are bounded and report a flag. Both contractions run on the tensor cores (mma.m16n8k16, fp16 operands,
 // fp32 accumulation) on exact operands: a nibble pair masked into an fp16 pair with a zero
 // exponent field IS the pair of fp16 subnormals n * 2^-24 (low nibble) or n * 2^-20 (high
 // nibble), so one LOP3 turns 2 nibbles into MMA operands; the power of two goes into the
