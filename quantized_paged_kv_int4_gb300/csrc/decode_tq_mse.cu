@@ -137,8 +137,9 @@ __device__ __forceinline__ uint32_t pair_offset(const uint32_t *w, int bit) {
 }
 
 // PACKQ (G <= 4): the q hi parts of the G heads fill MMA columns 0..3 and the lo parts columns
-// 4..7, so two MMAs per k-step (centroid hi, centroid lo) cover all four products and a
-// shuffle adds column n + 4 into column n; columns 4..7 then repeat heads 0..3 and are dropped.
+// 4..7, and the MMA rows are 8 tokens' centroid hi parts (rows 0..7) and lo parts (rows 8..15),
+// so one MMA per 8 tokens and k-step covers all four products; rows g and g + 8 are added, and a
+// shuffle adds column n + 4 into column n (columns 4..7 then repeat heads 0..3 and are dropped).
 template <int D, int KB, int VB, int NSTAGE, bool PACKQ>
 __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring, uint8_t *qarea,
                                              const uint2 *table, const float *sq, int RS, int b, int h,
@@ -206,10 +207,12 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
   const long long row_stride = static_cast<long long>(Hk) * SB;
   const long long page_bytes = kPage * row_stride;
   const uint8_t *head = p.cache + static_cast<long long>(h) * SB;
-  const int chunks = SB / 16;  // 16-byte pieces of one slot
-  // piece i = lane + 32 n of a page is row i / chunks, piece i % chunks: stepped without division
-  const int r_l = lane / chunks, c_l = lane - r_l * chunks;
-  const int dr = 32 / chunks, dc = 32 - dr * chunks;
+  // lanes 2r and 2r + 1 copy slot row r of a page: its even and odd 16-byte pieces, so each
+  // further piece of a lane is 32 bytes on in both memories
+  const int chunks = SB / 16;
+  const int n_cp = (chunks - (lane & 1) + 1) >> 1;
+  const long long src_lane = (lane >> 1) * row_stride + 16 * (lane & 1);
+  const uint32_t dst_lane = (lane >> 1) * RS + 16 * (lane & 1);
   auto issue = [&](int k) {
     const int kk = k & 31;
     if (k > 0 && kk == 0) {
@@ -221,16 +224,9 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
     const bool ok = in && blk >= 0 && blk < p.num_blocks;
     if (in && !ok && lane == 0) atomicOr(&g_flags_decode_tq_mse, ERR_BLOCK);
     const uint32_t st = ring_s + (k % NSTAGE) * STAGE;
-    const uint8_t *base = head + static_cast<long long>(ok ? blk : 0) * page_bytes;
-    for (int r = r_l, c = c_l; r < kPage;) {
-      cp_async<16>(st + r * RS + 16 * c, base + r * row_stride + 16 * c, ok);
-      r += dr;
-      c += dc;
-      if (c >= chunks) {
-        c -= chunks;
-        ++r;
-      }
-    }
+    const uint8_t *src = head + static_cast<long long>(ok ? blk : 0) * page_bytes + src_lane;
+    const uint32_t dst = st + dst_lane;
+    for (int i = 0; i < n_cp; ++i) cp_async<16>(dst + 32 * i, src + 32 * i, ok);
     cp_async_commit();
   };
 
@@ -267,6 +263,7 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
     }
     w0[Gm::KW] = w1[Gm::KW] = 0u;
     float c[4] = {0.f, 0.f, 0.f, 0.f};
+    float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};  // PACKQ: tokens g, g + 8
     float ss0 = 0.f, ss1 = 0.f;  // sum of c^2 over the lane's dims (NORM_CORRECTION)
 #pragma unroll
     for (int ks = 0; ks < Gm::KSTEPS; ++ks) {
@@ -282,13 +279,24 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
           ss1 += sq[o1 >> Gm::PSH];
         }
       }
-      mma_f16_16816(c, e0[0].x, e1[0].x, e0[1].x, e1[1].x, qhi[ks][0], qhi[ks][1]);
-      if constexpr (!PACKQ) mma_f16_16816(c, e0[0].x, e1[0].x, e0[1].x, e1[1].x, qlo[ks][0], qlo[ks][1]);
-      mma_f16_16816(c, e0[0].y, e1[0].y, e0[1].y, e1[1].y, qhi[ks][0], qhi[ks][1]);
+      if constexpr (PACKQ) {
+        // MMA rows = 8 tokens x (centroid hi, centroid lo): a pair-table entry is exactly the
+        // (row g, row g + 8) half of an A fragment, so the loads feed the MMAs directly
+        mma_f16_16816(ca, e0[0].x, e0[0].y, e0[1].x, e0[1].y, qhi[ks][0], qhi[ks][1]);
+        mma_f16_16816(cb, e1[0].x, e1[0].y, e1[1].x, e1[1].y, qhi[ks][0], qhi[ks][1]);
+      } else {
+        mma_f16_16816(c, e0[0].x, e1[0].x, e0[1].x, e1[1].x, qhi[ks][0], qhi[ks][1]);
+        mma_f16_16816(c, e0[0].x, e1[0].x, e0[1].x, e1[1].x, qlo[ks][0], qlo[ks][1]);
+        mma_f16_16816(c, e0[0].y, e1[0].y, e0[1].y, e1[1].y, qhi[ks][0], qhi[ks][1]);
+      }
     }
     if constexpr (PACKQ) {
+      c[0] = ca[0] + ca[2];  // token g: centroid hi + lo rows
+      c[1] = ca[1] + ca[3];
+      c[2] = cb[0] + cb[2];  // token g + 8
+      c[3] = cb[1] + cb[3];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) c[i] += __shfl_xor_sync(FULL, c[i], 2);  // hi (t < 2) + lo (t >= 2)
+      for (int i = 0; i < 4; ++i) c[i] += __shfl_xor_sync(FULL, c[i], 2);  // q hi (t < 2) + q lo (t >= 2)
     }
     // per-token factor: attn_scale * log2(e) * norm (/ |c| under NORM_CORRECTION)
     float f0 = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16_at(row0, Gm::MSE)))) * p.sc_log2;
