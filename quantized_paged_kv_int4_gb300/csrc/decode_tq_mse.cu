@@ -97,6 +97,7 @@ constexpr int kRotRows = 8;
 template <int D>
 __global__ void __launch_bounds__(D) rotate_q_kernel(const float *__restrict__ q, const float *__restrict__ Pi,
                                                      float *__restrict__ q_rot, long long rows) {
+  asm volatile("griddepcontrol.launch_dependents;");  // the decode kernel may start its prologue
   constexpr int R = kRotRows;
   __shared__ __align__(16) float s_q[R][D];
   const long long r0 = static_cast<long long>(blockIdx.x) * R;
@@ -164,7 +165,46 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
   int bids_cur = load_bids(0);
   int bids_next = load_bids(1);
 
-  // -------- q_rot -> fp16 hi / lo parts in shared memory, then B fragments
+  const uint32_t ring_s = smem_u32(ring);
+  const long long row_stride = static_cast<long long>(Hk) * SB;
+  const long long page_bytes = kPage * row_stride;
+  const uint8_t *head = p.cache + static_cast<long long>(h) * SB;
+  // lanes 2r and 2r + 1 copy slot row r of a page: its even and odd 16-byte pieces, so each
+  // further piece of a lane is 32 bytes on in both memories
+  const int chunks = SB / 16;
+  const int n_cp = (chunks - (lane & 1) + 1) >> 1;
+  const long long src_lane = (lane >> 1) * row_stride + 16 * (lane & 1);
+  const uint32_t dst_lane = (lane >> 1) * RS + 16 * (lane & 1);
+  auto issue = [&](int k) {
+    const int kk = k & 31;
+    if (k > 0 && kk == 0) {
+      bids_cur = bids_next;
+      bids_next = load_bids((k >> 5) + 1);
+    }
+    const int blk = __shfl_sync(FULL, bids_cur, kk);
+    const bool in = k < n_my;
+    const bool ok = in && blk >= 0 && blk < p.num_blocks;
+    if (in && !ok && lane == 0) atomicOr(&g_flags_decode_tq_mse, ERR_BLOCK);
+    const uint32_t st = ring_s + (k % NSTAGE) * STAGE;
+    const uint8_t *src = head + static_cast<long long>(ok ? blk : 0) * page_bytes + src_lane;
+    const uint32_t dst = st + dst_lane;
+    for (int i = 0; i < n_cp; ++i) cp_async<16>(dst + 32 * i, src + 32 * i, ok);
+    cp_async_commit();
+  };
+
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float pz0 = 0.f, pz1 = 0.f;
+  float acc[Gm::MT][4];
+#pragma unroll
+  for (int i = 0; i < Gm::MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+#pragma unroll
+  for (int k = 0; k < NSTAGE - 1; ++k) issue(k);
+
+  // -------- q_rot -> fp16 hi / lo parts in shared memory, then B fragments. The first page
+  // copies are already on their way; q_rot is written by the rotation kernel this one may
+  // overlap (a programmatic dependent launch), so wait for that grid first.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   {
     constexpr int J = D / 32;
     const float *qb = p.q_rot + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(h) * G) * D;
@@ -203,41 +243,6 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
   }
   __syncwarp();
 
-  const uint32_t ring_s = smem_u32(ring);
-  const long long row_stride = static_cast<long long>(Hk) * SB;
-  const long long page_bytes = kPage * row_stride;
-  const uint8_t *head = p.cache + static_cast<long long>(h) * SB;
-  // lanes 2r and 2r + 1 copy slot row r of a page: its even and odd 16-byte pieces, so each
-  // further piece of a lane is 32 bytes on in both memories
-  const int chunks = SB / 16;
-  const int n_cp = (chunks - (lane & 1) + 1) >> 1;
-  const long long src_lane = (lane >> 1) * row_stride + 16 * (lane & 1);
-  const uint32_t dst_lane = (lane >> 1) * RS + 16 * (lane & 1);
-  auto issue = [&](int k) {
-    const int kk = k & 31;
-    if (k > 0 && kk == 0) {
-      bids_cur = bids_next;
-      bids_next = load_bids((k >> 5) + 1);
-    }
-    const int blk = __shfl_sync(FULL, bids_cur, kk);
-    const bool in = k < n_my;
-    const bool ok = in && blk >= 0 && blk < p.num_blocks;
-    if (in && !ok && lane == 0) atomicOr(&g_flags_decode_tq_mse, ERR_BLOCK);
-    const uint32_t st = ring_s + (k % NSTAGE) * STAGE;
-    const uint8_t *src = head + static_cast<long long>(ok ? blk : 0) * page_bytes + src_lane;
-    const uint32_t dst = st + dst_lane;
-    for (int i = 0; i < n_cp; ++i) cp_async<16>(dst + 32 * i, src + 32 * i, ok);
-    cp_async_commit();
-  };
-
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float pz0 = 0.f, pz1 = 0.f;
-  float acc[Gm::MT][4];
-#pragma unroll
-  for (int i = 0; i < Gm::MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-
-#pragma unroll
-  for (int k = 0; k < NSTAGE - 1; ++k) issue(k);
 
   for (int k = 0; k < n_my; ++k) {
     issue(k + NSTAGE - 1);
@@ -481,8 +486,20 @@ static kvq_status launch_tq_mse(const TqMseParams &p, const SplitPlan &plan, con
   rotate_q_kernel<D><<<static_cast<unsigned>((rows + kRotRows - 1) / kRotRows), D, 0, s>>>(q, Pi, q_rot, rows);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   const dim3 grid(plan.seg_ctas, plan.head_groups);
-  decode_tq_mse_kernel<D, KB, VB, kStagesMse, PACKQ><<<grid, 256, smem, s>>>(p, RS);
-  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, decode_tq_mse_kernel<D, KB, VB, kStagesMse, PACKQ>, p, RS) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+  }
   if (launch_dependent(merge_kernel<D>, dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), s, p.s) != cudaSuccess)
     return KVQ_ERR_CUDA;
   return launch_status();
