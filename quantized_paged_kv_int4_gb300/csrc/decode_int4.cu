@@ -868,14 +868,9 @@ bool take_flags_decode_int4(cudaStream_t stream, unsigned *host_word) {
 template <int D, int W, int VAR>
 static kvq_status launch_int4_w(const Int4Params &p, const SplitPlan &plan, cudaStream_t s) {
   const size_t smem = int4_smem_bytes<D>();
-  static bool attr_set = false;  // per process; the attribute is per function, not per device
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(decode_int4_kernel<D, kStagesInt4, W, VAR>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-    attr_set = true;
-  }
+  static size_t attr_done[kMaxDevices] = {};
+  if (ensure_dynamic_smem(decode_int4_kernel<D, kStagesInt4, W, VAR>, smem, attr_done) != cudaSuccess)
+    return KVQ_ERR_CUDA;
   const dim3 grid(plan.seg_ctas, plan.head_groups);
   decode_int4_kernel<D, kStagesInt4, W, VAR><<<grid, 256, smem, s>>>(p);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;

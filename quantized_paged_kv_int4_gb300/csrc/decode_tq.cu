@@ -346,14 +346,9 @@ template <int D, int VBITS, bool PACKQ>
 static kvq_status launch_tq(const TqParams &p, const SplitPlan &plan, cudaStream_t s) {
   using Gm = TqGeom<D, VBITS>;
   const size_t smem = 8 * static_cast<size_t>(kStagesTq * Gm::STAGE + Gm::QBYTES);
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(decode_tq_kernel<D, VBITS, kStagesTq, PACKQ>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-    attr_set = true;
-  }
+  static size_t attr_done[kMaxDevices] = {};
+  if (ensure_dynamic_smem(decode_tq_kernel<D, VBITS, kStagesTq, PACKQ>, smem, attr_done) != cudaSuccess)
+    return KVQ_ERR_CUDA;
   const dim3 grid(plan.seg_ctas, plan.head_groups);
   decode_tq_kernel<D, VBITS, kStagesTq, PACKQ><<<grid, 256, smem, s>>>(p);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;

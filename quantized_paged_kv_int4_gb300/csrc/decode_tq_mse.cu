@@ -475,13 +475,9 @@ static kvq_status launch_tq_mse(const TqMseParams &p, const SplitPlan &plan, con
   const int RS = mse_row_stride(p.slot_bytes);
   const size_t smem = Gm::TABLE + 8 * static_cast<size_t>(kStagesMse * kPage * RS + Gm::QBYTES);
   if (smem > 227 * 1024) return KVQ_ERR_UNSUPPORTED;
-  static size_t attr_bytes = 0;  // the largest dynamic size set so far for this instantiation
-  if (smem > attr_bytes) {
-    if (cudaFuncSetAttribute(decode_tq_mse_kernel<D, KB, VB, kStagesMse, PACKQ>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-    attr_bytes = smem;
-  }
+  static size_t attr_done[kMaxDevices] = {};  // the size depends on slot_bytes: the largest set so far
+  if (ensure_dynamic_smem(decode_tq_mse_kernel<D, KB, VB, kStagesMse, PACKQ>, smem, attr_done) != cudaSuccess)
+    return KVQ_ERR_CUDA;
   const long long rows = static_cast<long long>(p.s.B) * p.s.Hq;
   rotate_q_kernel<D><<<static_cast<unsigned>((rows + kRotRows - 1) / kRotRows), D, 0, s>>>(q, Pi, q_rot, rows);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;

@@ -58,6 +58,23 @@ struct Int4Maps {
 bool int4_tensor_maps(const void *k_cache, const void *v_cache, const void *k_scale, const void *v_scale,
                       long long num_blocks, int Hk, int D, Int4Maps *maps);
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current device. The attribute
+// lives with the function in each device's context, so it is set once per (instantiation,
+// device): `done[dev]` holds the largest size set there so far (devices past kMaxDevices set it
+// on every call).
+constexpr int kMaxDevices = 64;
+template <typename Kernel>
+cudaError_t ensure_dynamic_smem(Kernel *kernel, size_t bytes, size_t (&done)[kMaxDevices]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached && done[dev] >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess && cached) done[dev] = bytes;
+  return e;
+}
+
 // Launch the log-sum-exp merge as a programmatic dependent of the kernel just enqueued on s.
 template <typename Args>
 cudaError_t launch_dependent(void (*kernel)(Args), dim3 grid, dim3 block, cudaStream_t s, const Args &a) {
