@@ -166,7 +166,7 @@ def _head_attention(q_rows, K, V, sm, pos=None, qpos=None, softcap=0.0, slopes=N
 
 def decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
                 signs, softmax_scale, num_splits=None, batch_index=None,
-                window=0, softcap=0.0, sinks=None, alibi_slopes=None, q_len=1):
+                window=0, softcap=0.0, sinks=None, alibi_slopes=None, q_len=1, return_lse=False):
     """Paged decode attention over the INT4 cache (unified_attention_int4 semantics).
 
     q: [B, Hq, D] float32 holding bf16 values. Returns float64 [B, Hq, D] (rows of
@@ -188,6 +188,11 @@ def decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
     q is [B * Q, Hq, D], query token i of sequence b (row b * Q + i) sits at position L - Q + i and
     attends causally to keys n <= L - Q + i; the output has q's row layout. Sequences need
     L >= Q. (With Q > 1 only the soft cap and sinks are combined with it here.)
+
+    return_lse: also return the log-sum-exp of each row's scores, ln(sum_n e^{S_n}) (plus e^{sink}
+    with sinks; -inf for a row with no key), float64 [rows, Hq] -- what
+    triton_turboquant_decode_attention returns in lse_buf next to the output, so that a caller
+    can merge this result with attention over other keys.
     """
     if q_len > 1:
         q = np.asarray(q, dtype=np.float32)
@@ -195,6 +200,9 @@ def decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
         assert BQ % q_len == 0 and window == 0 and alibi_slopes is None
         B = BQ // q_len
         out = np.zeros((BQ, Hq, D), dtype=np.float64)
+        lse = np.full((BQ, Hq), -np.inf)
+        if sinks is not None:
+            lse[:] = np.asarray(sinks, np.float64)[None, :]   # a row with no key: the sink alone
         rows = range(B) if batch_index is None else batch_index
         for b in rows:
             L = int(seq_lens[b])
@@ -202,11 +210,12 @@ def decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
                 Li = L - q_len + i + 1   # keys 0 .. L - Q + i
                 if Li <= 0:
                     continue
-                out[b * q_len + i] = decode_int4(q[b * q_len + i][None], k_cache, v_cache, k_scale, v_scale,
-                                                 np.asarray(block_table)[b][None], np.array([Li]), signs,
-                                                 softmax_scale, num_splits=num_splits, softcap=softcap,
-                                                 sinks=sinks)[0]
-        return out
+                o, l = decode_int4(q[b * q_len + i][None], k_cache, v_cache, k_scale, v_scale,
+                                   np.asarray(block_table)[b][None], np.array([Li]), signs,
+                                   softmax_scale, num_splits=num_splits, softcap=softcap,
+                                   sinks=sinks, return_lse=True)
+                out[b * q_len + i], lse[b * q_len + i] = o[0], l[0]
+        return (out, lse) if return_lse else out
     q = np.asarray(q, dtype=np.float32)
     B, Hq, D = q.shape
     Hk = k_cache.shape[2]
@@ -214,6 +223,9 @@ def decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
     q_rot = rotate_to_bf16(q, signs).astype(np.float64)
     sm = softmax_scale / D if signs is not None else softmax_scale
     out = np.zeros((B, Hq, D), dtype=np.float64)
+    lse_out = np.full((B, Hq), -np.inf)
+    if sinks is not None:
+        lse_out[:] = np.asarray(sinks, np.float64)[None, :]   # a row with no key: the sink alone
     rows = range(B) if batch_index is None else batch_index
     for b in rows:
         L = int(seq_lens[b])
@@ -241,15 +253,20 @@ def decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
                     parts.append(_head_attention(qg, K[a:e, h], V[a:e, h], sm, pos=pos[a:e], **kw))
             if sinks is not None:
                 parts.append((np.zeros((G, D)), np.asarray(sinks, np.float64)[h * G:(h + 1) * G]))
-            o = parts[0][0] if len(parts) == 1 else lse_merge([p[0] for p in parts], [p[1] for p in parts])
+            if len(parts) == 1:
+                o, lse = parts[0]
+            else:
+                o, lse = lse_merge([p[0] for p in parts], [p[1] for p in parts], return_lse=True)
             if signs is not None:
                 o = rht_inverse_f64(o, signs) / D
             out[b, h * G:(h + 1) * G] = o
-    return out
+            lse_out[b, h * G:(h + 1) * G] = lse
+    return (out, lse_out) if return_lse else out
 
 
-def lse_merge(outs, lses):
-    """Combine per-split (o_s, lse_s): sum_s e^(lse_s - M) o_s / sum_s e^(lse_s - M).
+def lse_merge(outs, lses, return_lse=False):
+    """Combine per-split (o_s, lse_s): sum_s e^(lse_s - M) o_s / sum_s e^(lse_s - M), and (with
+    return_lse) the merged log-sum-exp M + ln sum_s e^(lse_s - M).
 
     The stage-2 reduction itself is not on the pages (triton_turboquant_decode.py
     imports _fwd_kernel_stage2; int4_per_token_head.py imports reduce_segments);
@@ -260,4 +277,5 @@ def lse_merge(outs, lses):
     outs = np.stack([np.asarray(x, dtype=np.float64) for x in outs])     # [S, G, D]
     M = lses.max(axis=0)
     w = np.exp(lses - M)
-    return (w[:, :, None] * outs).sum(axis=0) / w.sum(axis=0)[:, None]
+    o = (w[:, :, None] * outs).sum(axis=0) / w.sum(axis=0)[:, None]
+    return (o, M + np.log(w.sum(axis=0))) if return_lse else o

@@ -82,10 +82,13 @@ def dequant_slots(slots, D, value_bits):
     return k, v
 
 
-def decode_tq(q, kv_cache, value_bits, block_table, seq_lens, attn_scale, batch_index=None):
+def decode_tq(q, kv_cache, value_bits, block_table, seq_lens, attn_scale, batch_index=None,
+              return_lse=False):
     """q: [B, Hq, D] float32; kv_cache: [num_blocks, block_size, Hk, slot_bytes] uint8.
 
-    Returns float64 [B, Hq, D]; rows of empty sequences are zero.
+    Returns float64 [B, Hq, D]; rows of empty sequences are zero. return_lse: also the
+    log-sum-exp ln(sum_n e^{score_n}) of each row, float64 [B, Hq] (-inf for an empty row), the
+    lse_buf that triton_turboquant_decode_attention returns next to the output.
     """
     q = np.asarray(q, dtype=np.float64)
     B, Hq, D = q.shape
@@ -93,6 +96,7 @@ def decode_tq(q, kv_cache, value_bits, block_table, seq_lens, attn_scale, batch_
     G = Hq // Hk
     bs = kv_cache.shape[1]
     out = np.zeros((B, Hq, D), dtype=np.float64)
+    lse = np.full((B, Hq), -np.inf)
     rows = range(B) if batch_index is None else batch_index
     for b in rows:
         L = int(seq_lens[b])
@@ -106,7 +110,8 @@ def decode_tq(q, kv_cache, value_bits, block_table, seq_lens, attn_scale, batch_
             s = attn_scale * (q[b, hq][None, :] * K[:, h, :]).sum(axis=-1)
             e = np.exp(s - s.max())
             out[b, hq] = (e[:, None] * V[:, h, :]).sum(axis=0) / e.sum()
-    return out
+            lse[b, hq] = s.max() + np.log(e.sum())
+    return (out, lse) if return_lse else out
 
 
 # ----------------------------------------------------------------------------------------------

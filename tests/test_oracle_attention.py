@@ -183,3 +183,60 @@ def test_multi_token_decode_matches_causal_sdpa(Q):
         o = torch.nn.functional.scaled_dot_product_attention(Qm, K, V, attn_mask=allowed, scale=scale)  # [Hq, Q, D]
         for i in range(Q):
             assert np.max(np.abs(got[b * Q + i] - o[:, i].numpy())) < 1e-12
+
+
+# ---------------------------------------------------------------------------------------------
+# The merged log-sum-exp (return_lse): closed forms and split invariance
+# ---------------------------------------------------------------------------------------------
+def test_lse_of_a_zero_query_is_the_log_of_the_length():
+    """Every score is 0, so ln(sum_n e^0) = ln L exactly; with a sink s: ln(L + e^s); an empty row:
+    -inf without a sink, s with one."""
+    case = workloads.DecodeCase("zl", 3, 4, 2, 64, [33, 0, 5], seed=21)
+    c = _build(case)
+    c["q"][:] = 0.0
+    _, lse = _run(c, 0.3, return_lse=True)
+    assert np.allclose(lse[0], np.log(33.0), rtol=0, atol=1e-12) and np.allclose(lse[2], np.log(5.0), atol=1e-12)
+    assert np.all(lse[1] == -np.inf)
+    sinks = np.array([0.5, -1.0, 2.0, 0.0])
+    for S in (None, 3):
+        _, lse = _run(c, 0.3, return_lse=True, sinks=sinks, num_splits=S)
+        assert np.allclose(lse[0], np.log(33.0 + np.exp(sinks)), atol=1e-12)
+        assert np.allclose(lse[1], sinks, atol=0)
+
+
+def test_lse_of_identical_keys_grows_by_log_length():
+    """L copies of one key: lse(L) - lse(1) = ln L (each copy adds the same e^S)."""
+    case = workloads.DecodeCase("same", 1, 2, 1, 64, [40], seed=22)
+    k, v = workloads.kv_vectors(case, 40)
+    k[:] = k[0]
+    c = _build(case, k=k, v=v)
+    _, lse40 = _run(c, 0.5, return_lse=True)
+    c["lens"] = np.array([1])
+    _, lse1 = _run(c, 0.5, return_lse=True)
+    assert np.max(np.abs(lse40 - lse1 - np.log(40.0))) < 1e-12
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 7, 64])
+def test_lse_of_split_merge_equals_single_pass(S):
+    case = workloads.tiny_int4(seed=23)
+    c = _build(case, num_blocks=12)
+    o1, l1 = _run(c, 0.125, return_lse=True)
+    oS, lS = _run(c, 0.125, return_lse=True, num_splits=S)
+    assert np.max(np.abs(lS - l1)) < 1e-12 and np.max(np.abs(oS - o1)) < 1e-12
+
+
+def test_lse_multi_token_rows_are_their_prefix_lse():
+    """Query token i of a Q-token row sees keys 0 .. L - Q + i: its lse is the single-token lse
+    over that prefix."""
+    case = workloads.DecodeCase("mt", 2, 4, 2, 64, [30, 45], seed=24)
+    c = _build(case)
+    Q = 3
+    q = np.repeat(c["q"], Q, axis=0)
+    _, lse = int4_cache.decode_int4(q, c["kc"], c["vc"], c["ks"], c["vs"], c["bt"], c["lens"], c["signs"], 0.2,
+                                    q_len=Q, return_lse=True)
+    for b in range(2):
+        for i in range(Q):
+            Li = c["lens"][b] - Q + i + 1
+            _, one = int4_cache.decode_int4(c["q"][b][None], c["kc"], c["vc"], c["ks"], c["vs"], c["bt"][b][None],
+                                            np.array([Li]), c["signs"], 0.2, return_lse=True)
+            assert np.max(np.abs(lse[b * Q + i] - one[0])) < 1e-12

@@ -151,3 +151,14 @@ def test_mse_identity_rotation_zero_query_is_uniform_mean():
         n = np.arange(L)
         V = turboquant.dequant_values(c["cache"][c["bt"][b][n // 16], n % 16], c["D"], 4, c["kps"])
         assert np.max(np.abs(got[b] - np.repeat(V.mean(axis=0), c["G"], axis=0))) < 1e-12
+
+
+def test_tq_lse_of_a_zero_query_is_the_log_of_the_length():
+    """Every score is 0: lse = ln L exactly; an empty row is -inf."""
+    case = workloads.DecodeCase("tql", 3, 4, 2, 64, [20, 0, 7], seed=25)
+    bt, nb = workloads.paged_layout(case.seq_lens, case.seed)
+    cache = workloads.random_turboquant_slots((nb, 16, 2), 64, 4, case.seed).numpy()
+    q = np.zeros((3, 4, 64), np.float32)
+    _, lse = turboquant.decode_tq(q, cache, 4, bt.numpy(), np.array(case.seq_lens), 0.125, return_lse=True)
+    assert np.allclose(lse[0], np.log(20.0), atol=1e-12) and np.allclose(lse[2], np.log(7.0), atol=1e-12)
+    assert np.all(lse[1] == -np.inf)
