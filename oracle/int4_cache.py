@@ -166,7 +166,8 @@ def _head_attention(q_rows, K, V, sm, pos=None, qpos=None, softcap=0.0, slopes=N
 
 def decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
                 signs, softmax_scale, num_splits=None, batch_index=None,
-                window=0, softcap=0.0, sinks=None, alibi_slopes=None, q_len=1, return_lse=False):
+                window=0, softcap=0.0, sinks=None, alibi_slopes=None, q_len=1, return_lse=False,
+                query_start_loc=None):
     """Paged decode attention over the INT4 cache (unified_attention_int4 semantics).
 
     q: [B, Hq, D] float32 holding bf16 values. Returns float64 [B, Hq, D] (rows of
@@ -184,37 +185,44 @@ def decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
       sinks           USE_SINKS: [Hq] logits that join each head's softmax denominator with no
                       value (the softmax state starts at M = sink, L = 1).
 
-    Multi-token decode (q_len = Q > 1, the speculative-verify case of unified_attention_int4):
-    q is [B * Q, Hq, D], query token i of sequence b (row b * Q + i) sits at position L - Q + i and
-    attends causally to keys n <= L - Q + i; the output has q's row layout. Sequences need
-    L >= Q. (With Q > 1 only the soft cap and sinks are combined with it here.)
+    Multi-token decode (unified_attention_int4 with max_seqlen_q > 1): sequence b has q_b query
+    tokens, rows query_start_loc[b] .. query_start_loc[b + 1] - 1 of q (the varlen cu_seqlens_q
+    layout; q_len = Q > 1 without it means q_b = Q for every b, rows b * Q + i). Query token i of
+    sequence b sits at position L - q_b + i and attends causally to keys n <= L - q_b + i, every
+    score modifier taken relative to its own position; the output has q's row layout. Sequences
+    need L >= q_b.
 
     return_lse: also return the log-sum-exp of each row's scores, ln(sum_n e^{S_n}) (plus e^{sink}
     with sinks; -inf for a row with no key), float64 [rows, Hq] -- what
     triton_turboquant_decode_attention returns in lse_buf next to the output, so that a caller
     can merge this result with attention over other keys.
     """
-    if q_len > 1:
+    if q_len > 1 or query_start_loc is not None:
         q = np.asarray(q, dtype=np.float32)
         BQ, Hq, D = q.shape
-        assert BQ % q_len == 0 and window == 0 and alibi_slopes is None
-        B = BQ // q_len
+        if query_start_loc is None:
+            assert BQ % q_len == 0
+            qsl = np.arange(0, BQ + 1, q_len)
+        else:
+            qsl = np.asarray(query_start_loc, dtype=np.int64)
+        B = len(qsl) - 1
         out = np.zeros((BQ, Hq, D), dtype=np.float64)
         lse = np.full((BQ, Hq), -np.inf)
         if sinks is not None:
             lse[:] = np.asarray(sinks, np.float64)[None, :]   # a row with no key: the sink alone
         rows = range(B) if batch_index is None else batch_index
         for b in rows:
-            L = int(seq_lens[b])
-            for i in range(q_len):
-                Li = L - q_len + i + 1   # keys 0 .. L - Q + i
+            L, qb = int(seq_lens[b]), int(qsl[b + 1] - qsl[b])
+            for i in range(qb):
+                r = int(qsl[b]) + i
+                Li = L - qb + i + 1   # keys 0 .. L - q_b + i: the query at position Li - 1
                 if Li <= 0:
                     continue
-                o, l = decode_int4(q[b * q_len + i][None], k_cache, v_cache, k_scale, v_scale,
+                o, l = decode_int4(q[r][None], k_cache, v_cache, k_scale, v_scale,
                                    np.asarray(block_table)[b][None], np.array([Li]), signs,
-                                   softmax_scale, num_splits=num_splits, softcap=softcap,
-                                   sinks=sinks, return_lse=True)
-                out[b * q_len + i], lse[b * q_len + i] = o[0], l[0]
+                                   softmax_scale, num_splits=num_splits, window=window, softcap=softcap,
+                                   sinks=sinks, alibi_slopes=alibi_slopes, return_lse=True)
+                out[r], lse[r] = o[0], l[0]
         return (out, lse) if return_lse else out
     q = np.asarray(q, dtype=np.float32)
     B, Hq, D = q.shape

@@ -240,3 +240,57 @@ def test_lse_multi_token_rows_are_their_prefix_lse():
             _, one = int4_cache.decode_int4(c["q"][b][None], c["kc"], c["vc"], c["ks"], c["vs"], c["bt"][b][None],
                                             np.array([Li]), c["signs"], 0.2, return_lse=True)
             assert np.max(np.abs(lse[b * Q + i] - one[0])) < 1e-12
+
+
+@pytest.mark.parametrize("window", [0, 6])
+def test_ragged_multi_query_with_window_and_alibi_matches_masked_sdpa(window):
+    """Ragged query counts (query_start_loc, the varlen cu_seqlens_q layout): sequence b's q_b tokens
+    sit at positions L - q_b .. L - 1; token at position p sees keys n <= p (and p - n < window),
+    with the ALiBi bias slope * (n - p). Expected: float64 SDPA with that additive float mask."""
+    lens = [9, 40, 17, 3]
+    counts = [3, 0, 5, 1]
+    case = workloads.DecodeCase("rag", 4, 4, 2, 64, lens, seed=50 + window)
+    c = _build(case)
+    Hq, D, G = 4, 64, 2
+    qsl = np.concatenate([[0], np.cumsum(counts)])
+    rng = np.random.default_rng(window)
+    q = int4_cache.bf16_round(rng.standard_normal((qsl[-1], Hq, D)).astype(np.float32))
+    slopes = np.array([0.5, 0.25, 0.125, 0.0625])
+    scale = 1.0 / np.sqrt(D)
+    got = int4_cache.decode_int4(q, c["kc"], c["vc"], c["ks"], c["vs"], c["bt"], c["lens"], c["signs"], scale,
+                                 query_start_loc=qsl, window=window, alibi_slopes=slopes)
+    q_rot = int4_cache.rotate_to_bf16(q, c["signs"])
+    for b, L in enumerate(lens):
+        qb = counts[b]
+        if qb == 0:
+            continue
+        Kt = np.zeros((L, 2, D)); Vt = np.zeros((L, 2, D))
+        for n in range(L):
+            page, row = c["bt"][b, n // 16], n % 16
+            Kt[n] = _unrotate(int4_cache.dequant_int4(c["kc"][page, row], c["ks"][page, row]), c["signs"], D)
+            Vt[n] = _unrotate(int4_cache.dequant_int4(c["vc"][page, row], c["vs"][page, row]), c["signs"], D)
+        rows = range(qsl[b], qsl[b + 1])
+        Qm = torch.from_numpy(np.stack([_unrotate(q_rot[r], c["signs"], D) for r in rows], axis=1))  # [Hq, qb, D]
+        K = torch.from_numpy(np.repeat(Kt.transpose(1, 0, 2), G, axis=0))
+        V = torch.from_numpy(np.repeat(Vt.transpose(1, 0, 2), G, axis=0))
+        pos = L - qb + np.arange(qb)                       # query positions
+        n = np.arange(L)
+        keep = n[None, :] <= pos[:, None]
+        if window:
+            keep &= (pos[:, None] - n[None, :]) < window
+        bias = slopes[:, None, None] * (n[None, None, :] - pos[None, :, None])   # [Hq, qb, L]
+        mask = torch.from_numpy(np.where(keep[None], bias, -np.inf))
+        o = torch.nn.functional.scaled_dot_product_attention(Qm, K, V, attn_mask=mask, scale=scale)
+        for i, r in enumerate(rows):
+            assert np.max(np.abs(got[r] - o[:, i].numpy())) < 1e-12
+
+
+def test_uniform_query_counts_equal_the_q_len_layout():
+    case = workloads.DecodeCase("u", 3, 4, 2, 64, [20, 33, 7], seed=55)
+    c = _build(case)
+    rng = np.random.default_rng(3)
+    q = int4_cache.bf16_round(rng.standard_normal((9, 4, 64)).astype(np.float32))
+    a = int4_cache.decode_int4(q, c["kc"], c["vc"], c["ks"], c["vs"], c["bt"], c["lens"], c["signs"], 0.1, q_len=3)
+    b = int4_cache.decode_int4(q, c["kc"], c["vc"], c["ks"], c["vs"], c["bt"], c["lens"], c["signs"], 0.1,
+                               query_start_loc=np.array([0, 3, 6, 9]))
+    assert np.array_equal(a, b)
