@@ -56,7 +56,7 @@ typedef enum { KVQ_BF16 = 0, KVQ_F16 = 1, KVQ_F32 = 2 } kvq_dtype;
 /* Static, human-readable name of a status. Never NULL. */
 KVQ_API const char *kvq_status_string(kvq_status status);
 
-/* ABI revision of this header (bumped on any signature change). */
+/* ABI revision of this header (bumped on any signature or struct change). */
 KVQ_API int32_t kvq_abi_version(void);
 
 /*
@@ -153,9 +153,24 @@ KVQ_API kvq_status kvq_decode_int4(const void *q, const uint8_t *k_cache, const 
  *   mods->q_len           query tokens per sequence (0 or 1: one). Multi-token decode (the
  *                         speculative-verify case): q and out are [B * q_len, Hq, D], row
  *                         b * q_len + i the query at position L - q_len + i, attending causally
- *                         to keys n <= L - q_len + i (a query with no key gets a zero row). Needs
- *                         (Hq / Hk) * q_len <= 8 and no window or ALiBi (KVQ_ERR_UNSUPPORTED);
- *                         the workspace is kvq_decode_workspace_bytes(B, q_len * Hq, Hk, D, S).
+ *                         to keys n <= L - q_len + i (a query with no key gets a zero row).
+ *   mods->query_start_loc int32 [B + 1] device array (4-byte aligned) or NULL: ragged multi-token
+ *                         decode (unified_attention_int4's cu_seqlens_q). Sequence b has
+ *                         q_b = query_start_loc[b + 1] - query_start_loc[b] query tokens (0 allowed),
+ *                         rows query_start_loc[b] .. of q and out ([total_q, Hq, D]); token i sits at
+ *                         position L - q_b + i and attends causally to keys n <= L - q_b + i. A row
+ *                         range outside [0, total_q) is skipped and raises flag 2. Overrides q_len.
+ *   mods->total_q         rows of q and out with query_start_loc (>= 0); ignored otherwise.
+ *                         In multi-token decode every modifier applies per query token, relative to
+ *                         its own position (window, ALiBi); the tokens of a sequence are served in
+ *                         blocks of 8 / (Hq / Hk) that read the sequence's keys once per block, and
+ *                         the workspace is kvq_decode_int4_mods_workspace_bytes(...).
+ *   mods->lse_out         fp32 [rows, Hq] device array (4-byte aligned; rows as out) or NULL. When
+ *                         set, each row's log-sum-exp ln(e^{sinks[hq]} + sum_n e^{S_n}) (without
+ *                         the sink term when sinks == NULL; -inf for a row with no key and no
+ *                         sink) is written next to out, so that the caller can merge this result
+ *                         with attention over other keys (the lse_buf of
+ *                         triton_turboquant_decode.py, triton_turboquant_decode_attention).
  * Invalid fields return KVQ_ERR_INVALID_ARG. Other arguments, numerics and errors: as
  * kvq_decode_int4.
  */
@@ -165,7 +180,15 @@ typedef struct kvq_score_mods {
   const float *sinks;
   const float *alibi_slopes;
   int32_t q_len;
+  float *lse_out;
+  const int32_t *query_start_loc;
+  int32_t total_q;
 } kvq_score_mods;
+
+/* Workspace bytes of kvq_decode_int4_mods with these mods (any multi-token layout); equal to
+   kvq_decode_workspace_bytes when mods is NULL or single-token. 0 for invalid sizes. */
+KVQ_API size_t kvq_decode_int4_mods_workspace_bytes(int32_t B, int32_t Hq, int32_t Hk, int32_t D,
+                                                    int32_t num_splits, const kvq_score_mods *mods);
 
 KVQ_API kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
                                 const float *k_scale, const float *v_scale,
@@ -190,7 +213,9 @@ KVQ_API kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache, c
  * loads the library holds that array until the process exits). It calls no allocating routine.
  *
  *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
- *     with that device current); make that first call before any stream capture.
+ *     with that device current); make that first call before any stream capture. The address
+ *     is kept for the life of the process: after a cudaDeviceReset (or any teardown of the
+ *     device's primary context) this entry point must not be called again in that process.
  *   - A call whose scratch need, kvq_decode_workspace_bytes(B, Hq, Hk, D, num_splits), exceeds
  *     KVQ_NOALLOC_SCRATCH_BYTES is rejected with KVQ_ERR_WORKSPACE before anything is launched.
  *   - Every call on a device shares the one array and overwrites what the previous call left
@@ -233,6 +258,20 @@ KVQ_API kvq_status kvq_decode_tq(const float *q, const uint8_t *kv_cache, int32_
                          void *workspace, size_t workspace_bytes, float *out, int32_t B,
                          int32_t Hq, int32_t Hk, int32_t D, int32_t block_size,
                          int64_t num_blocks, kvq_stream_t stream);
+
+/*
+ * kvq_decode_tq_lse -- kvq_decode_tq that also returns each row's log-sum-exp, as
+ * triton_turboquant_decode_attention returns lse_buf next to the output:
+ *   lse_out[b][hq] = ln(sum_n e^{score_n})     (-inf for seq_lens[b] == 0)
+ *   lse_out   fp32 [B, Hq] device array, 4-byte aligned, or NULL (then exactly kvq_decode_tq).
+ * Everything else as kvq_decode_tq.
+ */
+KVQ_API kvq_status kvq_decode_tq_lse(const float *q, const uint8_t *kv_cache, int32_t slot_bytes,
+                             int32_t value_bits, const int32_t *block_table, int32_t max_blocks,
+                             const int32_t *seq_lens, float attn_scale, int32_t num_splits,
+                             void *workspace, size_t workspace_bytes, float *out, float *lse_out,
+                             int32_t B, int32_t Hq, int32_t Hk, int32_t D, int32_t block_size,
+                             int64_t num_blocks, kvq_stream_t stream);
 
 /*
  * kvq_decode_tq_mse -- TurboQuant decode with MSE keys. Defined by triton_turboquant_decode.py,
@@ -353,10 +392,27 @@ KVQ_API kvq_status kvq_fwht128(const void *x, uint8_t *y_e4m3, float *row_scale,
                        kvq_stream_t stream);
 
 /*
+ * kvq_debug_set_wait -- for tests of the error path only (no counterpart on the pages).
+ * Every wait of the INT4 decode kernel on a page copy is bounded; when one runs out the kernel
+ * raises flag 8, lets the copies it has issued land, writes what it has and returns, so the
+ * context stays usable. This call makes that path reachable on purpose, without any fault:
+ *   wait_limit_ns   the limit of every such wait from now on in this process (0: the default, 2 s).
+ *   withhold_stage  >= 0: the NEXT kvq_decode_int4 / kvq_decode_int4_mods call (that one call only)
+ *                   does not issue the copies of that ring stage in its first CTA, so the wait on
+ *                   it runs out after wait_limit_ns (plus ~0.1 s for the bounded drain) and flag 8
+ *                   is raised; that call's results are not valid. -1: none.
+ * Returns KVQ_ERR_INVALID_ARG for withhold_stage < -1.
+ */
+KVQ_API kvq_status kvq_debug_set_wait(uint64_t wait_limit_ns, int32_t withhold_stage);
+
+/*
  * kvq_device_error -- synchronize `stream`, then read and clear the sticky device-side flags
  * of every libkvq kernel on the current device. *flags (may be NULL) receives their bitwise OR:
  *   1 block-table entry outside [0, num_blocks)   2 seq_len above 16 * max_blocks (clamped)
- *   4 slot_mapping entry beyond the pool
+ *   4 slot_mapping entry beyond the pool             8 a bounded wait on a page copy ran out
+ *   16 a decode input outside the supported range: a query element beyond ~2^100 in magnitude
+ *      (q, or q_rot for MSE keys, or a centroid), or a softmax weight beyond fp32 (value scales
+ *      near fp32's maximum); the rows concerned may hold inf/NaN
  * Returns KVQ_OK when no flag was set, KVQ_ERR_OUT_OF_RANGE otherwise, KVQ_ERR_CUDA if the
  * synchronization or the read failed.
  */

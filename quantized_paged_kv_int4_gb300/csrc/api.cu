@@ -176,7 +176,7 @@ extern "C" const char *kvq_status_string(kvq_status s) {
   return "KVQ_ERR_UNKNOWN";
 }
 
-extern "C" int32_t kvq_abi_version(void) { return 3; }
+extern "C" int32_t kvq_abi_version(void) { return 4; }
 
 extern "C" size_t kvq_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hk, int32_t D,
                                              int32_t num_splits) {

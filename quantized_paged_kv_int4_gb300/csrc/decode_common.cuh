@@ -21,6 +21,8 @@
 // reduction that triton_turboquant_decode.py (_fwd_kernel_stage2) and int4_per_token_head.py
 // (reduce_segments) call but do not show; then, for the INT4 cache, H(o) * d1 / D
 // (int4_per_token_head.py, unified_attention_int4: inverse single_rht divided by head_size).
+// On request the merged log-sum-exp (M + log2 sum_s 2^(lse_s - M)) ln 2 of each row is written too
+// (the lse_buf of triton_turboquant_decode.py, triton_turboquant_decode_attention).
 #pragma once
 
 #include "kvq_device.cuh"
@@ -33,6 +35,10 @@ struct SplitArgs {
   int32_t num_splits;  // 0 = balanced
   int32_t B, Hq, Hk, G;  // Hq: output rows per sequence (Q tokens x heads); G: heads per kv head
   int32_t Q;             // query tokens per sequence (multi-token decode; 1 otherwise)
+  // Multi-token decode: the "sequences" are virtual -- vseq[v] = {block-table row, key end L (the
+  // last query token's position + 1), first query / output row, query tokens (<= Q)}; Q is then
+  // the largest block of query tokens one pass serves (8 / G). Null: sequence b is itself.
+  const int4 *vseq;
   int32_t heads_per_cta, warps_per_head;
   int32_t seg_ctas;    // the split kernel's gridDim.x
   long long slots;     // partial slots in the workspace (before the warps_per_head factor)
@@ -45,9 +51,57 @@ struct SplitArgs {
   const float *sinks;  // [Hq] sink logits joining each head's softmax denominator, or null
   void *out;           // [B, Hq, D] of out_dtype
   int32_t out_dtype;
+  float *lse_out;      // [B, Hq] merged log-sum-exp (natural log) of every row's scores, or null
 };
 
+// ---------------------------------------------------------------------------------------------
+// Range of the fp16 tensor-core operands (all decode kernels).
+//
+// Queries: the fp16 query operand is the query times 2^-k, k chosen per (piece, kv head) from the
+// largest |q| so that no element can reach 2^15; 2^k goes into the score scale. The shift is a
+// power of two, so every element keeps its value exactly.
+//
+// Weights: softmax is invariant to the reference it is taken against, so each query column keeps
+// a reference m that is not the running maximum of its scores but a value chosen for the fp16
+// P.V operands P_v = 2^(S - m) * s_v (s_v the token's value scale): l = sum 2^(S - m),
+// acc = sum P_v (...), o = acc / l and lse = m + log2 l hold for any m. A step moves m (upwards
+// only, rescaling l and acc by 2^(m_old - m_new)) when one of its weights passes kWeightHi or a
+// score passes m + kScoreCap; the new m puts the step's largest P_v into [1, 2), and never below
+// the step's largest score - kScoreCap (so 2^(S - m) <= 2^64 and l cannot overflow). Then no
+// weight overflows fp16, and a token whose weight is within 2^-29 of the largest seen keeps a
+// normal fp16 weight, for value scales of any magnitude.
+// ---------------------------------------------------------------------------------------------
+constexpr float kWeightHi = 32768.f;
+constexpr float kScoreCap = 64.f;
+
+// Starting point of a column's new reference: the step's largest score ms for a column with no
+// keys yet (ref = -inf), else the old reference raised to at least ms - kScoreCap.
+__device__ __forceinline__ float ref_base(float ref, float ms) {
+  return ref == -INFINITY ? ms : fmaxf(ref, ms - kScoreCap);
+}
+// The new reference, given the column's largest P_v wb against `base`: base + floor(log2 wb),
+// at least ms - kScoreCap. A weight beyond fp32 raises ERR_RANGE.
+__device__ __forceinline__ float ref_new(float base, float ms, float wb, unsigned *flags) {
+  int k = 0;
+  if (wb > 0.f) {
+    if (!(wb < INFINITY)) atomicOr(flags, ERR_RANGE);
+    k = min(ilog2f(wb), 127);
+  }
+  return fmaxf(base + static_cast<float>(k), ms - kScoreCap);
+}
+
+// k of the query shift for a largest element maxabs whose products may grow by up to 2^extra
+// (the unnormalised Hadamard rotation: extra = log2 D): every |q| * 2^extra * 2^-k stays below
+// 2^15. k is kept within [-100, 100]; a clamp at the top (|q| beyond ~2^100) raises ERR_RANGE.
+// flags may be null (no report).
+__device__ __forceinline__ int query_shift(float maxabs, int extra, unsigned *flags) {
+  const int k = ilog2f(maxabs) + 1 + extra - 15;
+  if ((k > 100 || !(maxabs < INFINITY)) && flags != nullptr) atomicOr(flags, ERR_RANGE);
+  return max(-100, min(100, k));
+}
+
 __device__ __forceinline__ int clamped_len(const SplitArgs &a, int b, unsigned *flags) {
+  if (a.vseq != nullptr) return a.vseq[b].y;  // clamped (and flagged) when the list was built
   int L = __ldg(a.seq_lens + b);
   const int cap = a.max_blocks * kPage;
   if (L > cap) {
@@ -58,7 +112,8 @@ __device__ __forceinline__ int clamped_len(const SplitArgs &a, int b, unsigned *
 }
 
 // The keys of sequence b that a decode reads: positions [lo, L), lo = max(0, L - window) under a
-// sliding window (unified_attention_int4, SLIDING_WINDOW), on the sequence's pages f .. f + np - 1.
+// sliding window (unified_attention_int4, SLIDING_WINDOW) -- for nq query tokens the first one's
+// window, max(0, L - nq + 1 - window) -- on the sequence's pages f .. f + np - 1.
 struct SeqSpan {
   int L, lo, f, np;
 };
@@ -68,7 +123,8 @@ template <bool WIN = true>
 __device__ __forceinline__ SeqSpan seq_span(const SplitArgs &a, int b, unsigned *flags) {
   SeqSpan s;
   s.L = clamped_len(a, b, flags);
-  s.lo = WIN && a.window > 0 && s.L > a.window ? s.L - a.window : 0;
+  const int nq = a.vseq != nullptr ? a.vseq[b].w : 1;
+  s.lo = WIN && a.window > 0 ? max(0, s.L - nq + 1 - a.window) : 0;
   s.f = s.lo / kPage;
   s.np = s.L > 0 ? (s.L - 1) / kPage - s.f + 1 : 0;
   return s;
@@ -125,8 +181,8 @@ __device__ __forceinline__ void store_out(const SplitArgs &a, long long row, int
 // (used when a.signs is set); sink2: the head's sink logit in base 2 (-inf: none), a partial with
 // lse = sink2 and a zero vector.
 template <int D>
-__device__ __forceinline__ void merge_row(const SplitArgs &a, int b, int hq, long long s_lo, long long s_hi, int lane,
-                                          const float (&sg)[D / 32], float sink2) {
+__device__ __forceinline__ void merge_row(const SplitArgs &a, int b, int hq, long long orow, long long s_lo,
+                                          long long s_hi, int lane, const float (&sg)[D / 32], float sink2) {
   constexpr int V = D / 32, R = 16;
   const int W = a.warps_per_head;
   const long long n = (s_hi - s_lo) * W, r0 = s_lo * W;  // rows (s * W + w) are contiguous
@@ -187,6 +243,8 @@ __device__ __forceinline__ void merge_row(const SplitArgs &a, int b, int hq, lon
   const float inv = den > 0.f ? 1.f / den : 0.f;
 #pragma unroll
   for (int j = 0; j < V; ++j) o[j] *= inv;
+  if (a.lse_out != nullptr && lane == 0)  // ln(sum of e^S) = (M + log2 den) ln 2
+    a.lse_out[orow] = den > 0.f ? (M + log2f(den)) * 0.6931471805599453f : -INFINITY;
   if (a.signs != nullptr) {
     // element e = lane * V + j: stages h < V inside the lane, h = V .. D/2 across lanes
     butterfly_local<V>(o);
@@ -198,7 +256,7 @@ __device__ __forceinline__ void merge_row(const SplitArgs &a, int b, int hq, lon
 #pragma unroll
     for (int j = 0; j < V; ++j) o[j] *= sg[j] * (1.0f / D);
   }
-  store_out<D>(a, static_cast<long long>(b) * a.Hq + hq, lane, o);
+  store_out<D>(a, orow, lane, o);
 }
 
 // Calls seg(b, t0, t1, slot) for every sequence piece of this CTA (all threads, same order).
@@ -330,6 +388,16 @@ __global__ void __launch_bounds__(256) merge_kernel(const SplitArgs a) {
   for (int j = 0; j < V; ++j) sg[j] = a.signs != nullptr ? __ldg(a.signs + lane * V + j) : 0.f;
   const float sink2 = live && a.sinks != nullptr ? __ldg(a.sinks + hq % (a.Hq / a.Q)) * 1.4426950408889634f : -INFINITY;
   const SeqSpan sp = live ? seq_span(a, b, nullptr) : SeqSpan{0, 0, 0, 0};  // the split kernel already flagged it
+  // the output row: row (b, hq) itself, or for a virtual sequence query token hq / heads of its
+  // block (rows past its tokens belong to no query)
+  long long orow = idx;
+  bool owns = live;
+  if (a.vseq != nullptr && live) {
+    const int heads = a.Hq / a.Q, i = hq / heads;
+    const int4 vs = a.vseq[b];
+    owns = i < vs.w;
+    orow = (static_cast<long long>(vs.z) + i) * heads + hq % heads;
+  }
   const int L = sp.L;
   long long s_lo = 0, s_hi = 0;                           // slot range [s_lo, s_hi)
   bool ranged = false;
@@ -346,12 +414,14 @@ __global__ void __launch_bounds__(256) merge_kernel(const SplitArgs a) {
     ranged = true;
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (!live) return;
+  if (!owns) return;
   if (L == 0) {
     float z[V];
 #pragma unroll
     for (int j = 0; j < V; ++j) z[j] = 0.f;
-    store_out<D>(a, idx, lane, z);
+    store_out<D>(a, orow, lane, z);
+    if (a.lse_out != nullptr && lane == 0)  // no key: the sink alone, if any
+      a.lse_out[orow] = sink2 > -INFINITY ? sink2 * 0.6931471805599453f : -INFINITY;
     return;
   }
   if (!ranged) {
@@ -360,7 +430,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const SplitArgs a) {
   }
   s_lo = max(0LL, min(s_lo, a.slots));  // never index outside the workspace
   s_hi = max(s_lo, min(s_hi, a.slots));
-  merge_row<D>(a, b, hq, s_lo, s_hi, lane, sg, sink2);
+  merge_row<D>(a, b, hq, orow, s_lo, s_hi, lane, sg, sink2);
 }
 
 }  // namespace kvq

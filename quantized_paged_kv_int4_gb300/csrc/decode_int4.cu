@@ -25,11 +25,15 @@
 // nibble), so one LOP3 turns 2 nibbles into MMA operands; the power of two goes into the
 // per-token scale, and the zero-point is applied as the split-dot correction of the pages:
 //   * S^T[16 tokens x 8 heads] = K[16 x D] . Q^T  (q of a high-nibble dim pre-divided by 16);
-//   * O^T[D x 8 heads] += V^T[D x 16 tokens] . P_v^T with P_v = p * scale_v in fp16; the
-//     tokens (the K dimension) and the D rows are permuted so that a lane's V bytes become A
-//     fragments with one PRMT per pair of m-tiles.
+//   * O^T[D x 8 heads] += V^T[D x 16 tokens] . P_v^T with P_v = 2^(S - m) * scale_v in fp16, m a
+//     per-column softmax reference kept so that P_v stays inside fp16 for any value scale
+//     (decode_common.cuh); the tokens (the K dimension) and the D rows are permuted so that a
+//     lane's V bytes become A fragments with one PRMT per pair of m-tiles.
+// q enters as fp16 times a per-(piece, kv head) power of two 2^-k (so no element can overflow),
+// and 2^k joins the score scale.
 // The G query heads of a kv head share every K/V byte loaded (GQA), padded to the MMA's N = 8.
 
+#include <atomic>
 #include <mutex>
 
 #include "decode_common.cuh"
@@ -49,15 +53,14 @@ struct Int4Params {
   float softcap2;       // USE_SOFTCAP: the cap in base-2 units (cap * log2 e), 0 = off
   float inv_softcap2;
   const float *alibi;   // USE_ALIBI_SLOPES: [Hq] slopes, or null
+  unsigned long long wait_ns;  // limit of every bounded wait on a stage barrier
+  int32_t withhold;     // error-path tests only: CTA (0, 0) never issues stage `withhold` (-1: none)
 };
 
 constexpr uint32_t kLo = 0x000F000Fu;  // low nibbles of bytes 0 and 2 -> fp16 subnormal pair n * 2^-24
 constexpr uint32_t kHi = 0x00F000F0u;  // high nibbles -> fp16 subnormal pair n * 2^-20
 constexpr float kTwo24 = 16777216.0f;
 constexpr float kTwo20 = 1048576.0f;
-// Slack of the lazy softmax maximum (base 2): weights stay below 2^kSlack = 8, so P_v = p * scale_v
-// stays finite in fp16 for V scale words below 8188 (per-token value ranges below ~1.2e5).
-constexpr float kSlack = 3.0f;
 
 template <int D>
 struct Int4Geom {
@@ -205,7 +208,8 @@ __device__ __forceinline__ bool page_run(const SplitArgs &a, unsigned *flags, Pa
   return true;
 }
 
-// Online-softmax state of one warp for one sequence piece.
+// Online-softmax state of one warp for one sequence piece: per query column (2t, 2t + 1) the
+// softmax reference m (decode_common.cuh), the weight sum l and the zero-point sum pz = sum P_v zp_v.
 template <int D>
 struct PieceState {
   float m0, m1, l0, l1, pz0, pz1;
@@ -225,27 +229,35 @@ struct PieceState {
 // i * G + g for token i, head h * G + g; load_query waits for them.
 template <int D, bool MTOK>
 __device__ __forceinline__ void fetch_query(const Int4Params &p, uint8_t *qarea, int b, int h, int lane) {
-  const int G = p.s.G, per = G * D / 8, heads = p.s.Hq / p.s.Q;
+  const int G = p.s.G, per = G * D / 8;
   const uint32_t dst = smem_u32(qarea);
-  if (!MTOK || p.s.Q == 1) {  // one token: G contiguous rows
+  if (!MTOK || p.s.vseq == nullptr) {  // one token: G contiguous rows
     const uint8_t *src = reinterpret_cast<const uint8_t *>(
         p.q + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(h) * G) * D);
     for (int c = lane; c < per; c += 32) cp_async<16>(dst + 16 * c, src + 16 * c, true);
     cp_async_commit();
     return;
   }
+  // a virtual sequence: its nq query tokens are q rows row0 .. row0 + nq - 1; the rows of the
+  // block's other (Q - nq) tokens are zero-filled
+  const int heads = p.s.Hq / p.s.Q;
+  const int4 vs = p.s.vseq[b];
   for (int c = lane; c < p.s.Q * per; c += 32) {
     const int i = c / per, w = c - i * per;
-    const uint8_t *src = reinterpret_cast<const uint8_t *>(
-        p.q + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(i) * heads + static_cast<long long>(h) * G) * D);
-    cp_async<16>(dst + 16 * c, src + 16 * w, true);
+    const bool ok = i < vs.w;
+    const uint8_t *src = ok ? reinterpret_cast<const uint8_t *>(
+                                  p.q + ((static_cast<long long>(vs.z) + i) * heads + static_cast<long long>(h) * G) * D) + 16 * w
+                            : reinterpret_cast<const uint8_t *>(p.q);
+    cp_async<16>(dst + 16 * c, src, ok);
   }
   cp_async_commit();
 }
 
+// qmul receives 2^k, the power of two the fp16 operands were divided by (query_shift).
 template <int D, bool MTOK>
 __device__ __forceinline__ void load_query(const Int4Params &p, uint8_t *qarea, int b, int h, int lane,
-                                           uint32_t (&qf)[D / 16][2], float &qs0, float &qs1, bool fetched) {
+                                           uint32_t (&qf)[D / 16][2], float &qs0, float &qs1, float &qmul,
+                                           bool fetched) {
   using Gm = Int4Geom<D>;
   constexpr int J = D / 32;
   const int g = lane >> 2, t = lane & 3, G = MTOK ? p.s.G * p.s.Q : p.s.G;  // MMA columns in use
@@ -264,6 +276,23 @@ __device__ __forceinline__ void load_query(const Int4Params &p, uint8_t *qarea, 
   for (int j = 0; j < J; ++j) sg[j] = p.s.signs != nullptr ? __ldg(p.s.signs + lane + 32 * j) : 1.f;
   __syncwarp();
   const __nv_bfloat16 *qraw = reinterpret_cast<const __nv_bfloat16 *>(qarea);
+  // |H(q d1)| <= D max |q|: the shift that keeps every operand below 2^15 (exact)
+  uint32_t qbits = 0;  // the largest |q| as bf16 bits (sign cleared: ordered like the values)
+  {
+    const uint32_t *qw = reinterpret_cast<const uint32_t *>(qarea);
+#pragma unroll
+    for (int i = 0; i < 8 * D / 64; ++i) {
+      const int wi = lane + 32 * i;  // word wi holds dims 2 wi, 2 wi + 1 of the raw rows
+      if (wi < G * D / 2) {
+        const uint32_t v = qw[wi] & 0x7FFF7FFFu;
+        qbits = max(qbits, max(v & 0xFFFFu, v >> 16));
+      }
+    }
+  }
+  const float qmax = warp_max(__uint_as_float(qbits << 16));
+  const int qk = query_shift(qmax, p.s.signs != nullptr ? (D == 128 ? 7 : 6) : 0, &g_flags_decode_int4);
+  qmul = pow2i(qk);
+  const float qdiv = pow2i(-qk), qdiv16 = pow2i(-qk - 4);
   // four heads at a time, interleaved: their shuffle chains overlap instead of running back to back
   for (int n0 = 0; n0 < G; n0 += 4) {
     float x[4][J];
@@ -289,7 +318,8 @@ __device__ __forceinline__ void load_query(const Int4Params &p, uint8_t *qarea, 
         for (int j = 0; j < J; ++j) x[i][j] = bf16_round(x[i][j]);
       }
     }
-    // odd dims meet high nibbles, which enter the MMA 16x larger: pre-divide q by 16 (exact)
+    // odd dims meet high nibbles, which enter the MMA 16x larger: pre-divide q by 16 (exact);
+    // the operands (and their sums) are in units of 2^k
     float eff[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -297,7 +327,7 @@ __device__ __forceinline__ void load_query(const Int4Params &p, uint8_t *qarea, 
 #pragma unroll
       for (int j = 0; j < J; ++j) {
         const int e = lane + 32 * j;
-        const __half v = __float2half_rn((e & 1) ? x[i][j] * 0.0625f : x[i][j]);
+        const __half v = __float2half_rn(x[i][j] * ((e & 1) ? qdiv16 : qdiv));
         if (n0 + i < G) qh[(n0 + i) * D + e] = v;
         eff[i] += (e & 1) ? __half2float(v) * 16.f : __half2float(v);
       }
@@ -457,25 +487,25 @@ __device__ __forceinline__ float tanh_fast(float y) {
 
 // Score modifiers of one warp (unified_attention_int4's USE_SOFTCAP and USE_ALIBI_SLOPES), in
 // base-2 units: S = cap2 tanh(S / cap2) (cap2 and its inverse stay in the kernel parameters),
-// then S += slope2 * (n - qpos) for the lane's two head columns; qpos = L - 1, the query's
-// position.
+// then S += slope2 * (n - qpos) for the lane's two columns, qpos the position of the column's
+// query token.
 struct ScoreMods {
   float sl0, sl1;
-  int qpos;
+  int qp0, qp1;
 };
 
 // NP consecutive pages of this warp (stage offsets so[0..NP-1]) inside one piece: scores, one
 // online softmax step over their 16 * NP tokens, P.V. MASKED: some rows of the (single) page lie
 // outside [t0, t1) -- the ragged end of a sequence, a fixed split boundary or the start of a
 // sliding window -- and may hold never-written scale words (NaN): they are selected away, never
-// multiplied; in multi-token decode a column's keys also stop at its causal limit (lim0 / lim1
-// for the lane's columns 2t / 2t + 1, exclusive). MODS: apply the score modifiers md (page i's
-// row 0 is at position nb + 16 W i).
+// multiplied; in multi-token decode a column's keys are also limited to its own query token's
+// range [lw0, lim0) / [lw1, lim1) for the lane's columns 2t / 2t + 1 (causal limit, window).
+// MODS: apply the score modifiers md (page i's row 0 is at position nb + 16 W i).
 template <int D, int W, int NP, bool MASKED, bool MODS, bool MTOK>
 __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&so)[2], const LaneOffsets<D> &lo,
                                            const uint32_t (&qf)[D / 16][2], float qs0, float qs1, float sm24,
-                                           int lane, int nb, int t0, int t1, int lim0, int lim1,
-                                           const Int4Params &p, const ScoreMods &md) {
+                                           int lane, int nb, int t0, int t1, int lim0, int lim1, int lw0,
+                                           int lw1, const Int4Params &p, const ScoreMods &md) {
   using Gm = Int4Geom<D>;
   const int g = lane >> 2;
   PageIn pg[NP];
@@ -489,11 +519,12 @@ __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&s
         for (int j = 0; j < 4; ++j) pg[i].s[j] = p.softcap2 * tanh_fast(pg[i].s[j] * p.inv_softcap2);
       }
       if (p.alibi != nullptr) {
-        const float d0 = static_cast<float>(nb + i * W * kPage + g - md.qpos), d1 = d0 + 8.f;
-        pg[i].s[0] = fmaf(md.sl0, d0, pg[i].s[0]);
-        pg[i].s[1] = fmaf(md.sl1, d0, pg[i].s[1]);
-        pg[i].s[2] = fmaf(md.sl0, d1, pg[i].s[2]);
-        pg[i].s[3] = fmaf(md.sl1, d1, pg[i].s[3]);
+        const int n = nb + i * W * kPage + g;  // token g's position (token g + 8: n + 8)
+        const float e0 = static_cast<float>(n - md.qp0), e1 = static_cast<float>(n - md.qp1);
+        pg[i].s[0] = fmaf(md.sl0, e0, pg[i].s[0]);
+        pg[i].s[1] = fmaf(md.sl1, e1, pg[i].s[1]);
+        pg[i].s[2] = fmaf(md.sl0, e0 + 8.f, pg[i].s[2]);
+        pg[i].s[3] = fmaf(md.sl1, e1 + 8.f, pg[i].s[3]);
       }
     }
   }
@@ -503,32 +534,73 @@ __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&s
     const bool ok1 = nb + g + 8 >= t0 && nb + g + 8 < t1;
     ok00 = ok01 = ok0;
     ok10 = ok11 = ok1;
-    if constexpr (MTOK) {  // multi-token decode: each column's causal limit
-      ok00 = ok00 && nb + g < lim0;
-      ok01 = ok01 && nb + g < lim1;
-      ok10 = ok10 && nb + g + 8 < lim0;
-      ok11 = ok11 && nb + g + 8 < lim1;
+    if constexpr (MTOK) {  // multi-token decode: each column's own key range
+      ok00 = ok00 && nb + g < lim0 && nb + g >= lw0;
+      ok01 = ok01 && nb + g < lim1 && nb + g >= lw1;
+      ok10 = ok10 && nb + g + 8 < lim0 && nb + g + 8 >= lw0;
+      ok11 = ok11 && nb + g + 8 < lim1 && nb + g + 8 >= lw1;
     }
     pg[0].s[0] = ok00 ? pg[0].s[0] : -INFINITY;
     pg[0].s[1] = ok01 ? pg[0].s[1] : -INFINITY;
     pg[0].s[2] = ok10 ? pg[0].s[2] : -INFINITY;
     pg[0].s[3] = ok11 ? pg[0].s[3] : -INFINITY;
   }
-  // ---- online softmax (base 2) against a lazily raised reference maximum: the running sums are
-  // rescaled only when a new score exceeds the reference by more than kSlack, so the weights
-  // p = 2^(s - m) stay below 2^kSlack and most steps need no rescale at all
+  // ---- online softmax (base 2): weights p = 2^(S - m) and P.V operands w = p * scale_v against
+  // each column's reference m (decode_common.cuh); one warp vote finds a step in which a score
+  // passes m + kScoreCap or a weight passes kWeightHi, and only then (rarely) are the columns'
+  // maxima reduced, their references raised and the running sums rescaled.
+  uint32_t X0[NP], X1[NP];  // this lane's fp16 P_v pairs (tokens g, g+8) of columns 2t, 2t+1
+  float ls0, ls1, wm0, wm1;  // the step's weight sums and largest P_v per column
+  auto weights = [&](float q0, float q1) {
+    ls0 = ls1 = wm0 = wm1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      const float p00 = fast_exp2(pg[i].s[0] - q0), p10 = fast_exp2(pg[i].s[2] - q0);
+      const float p01 = fast_exp2(pg[i].s[1] - q1), p11 = fast_exp2(pg[i].s[3] - q1);
+      ls0 += p00 + p10;
+      ls1 += p01 + p11;
+      float w00 = p00 * pg[i].sv0, w10 = p10 * pg[i].sv1, w01 = p01 * pg[i].sv0, w11 = p11 * pg[i].sv1;
+      if (MASKED) {  // never-written rows may hold NaN scale words: select them away
+        w00 = ok00 ? w00 : 0.f;
+        w01 = ok01 ? w01 : 0.f;
+        w10 = ok10 ? w10 : 0.f;
+        w11 = ok11 ? w11 : 0.f;
+      }
+      wm0 = fmaxf(wm0, fmaxf(w00, w10));
+      wm1 = fmaxf(wm1, fmaxf(w01, w11));
+      X0[i] = h2_as_u32(__floats2half2_rn(w00, w10));
+      X1[i] = h2_as_u32(__floats2half2_rn(w01, w11));
+    }
+  };
+  weights(st.m0 == -INFINITY ? 0.f : st.m0, st.m1 == -INFINITY ? 0.f : st.m1);
   float ml0 = fmaxf(pg[0].s[0], pg[0].s[2]), ml1 = fmaxf(pg[0].s[1], pg[0].s[3]);
 #pragma unroll
   for (int i = 1; i < NP; ++i) {
     ml0 = fmaxf(ml0, fmaxf(pg[i].s[0], pg[i].s[2]));
     ml1 = fmaxf(ml1, fmaxf(pg[i].s[1], pg[i].s[3]));
   }
-  ml0 = warp_max_g(ml0);
-  ml1 = warp_max_g(ml1);
-  if (__any_sync(FULL, ml0 > st.m0 + kSlack || ml1 > st.m1 + kSlack)) {
-    const float n0 = fmaxf(st.m0, ml0), n1 = fmaxf(st.m1, ml1);
-    const float al0 = n0 == -INFINITY ? 1.f : fast_exp2(st.m0 - n0);
-    const float al1 = n1 == -INFINITY ? 1.f : fast_exp2(st.m1 - n1);
+  if (__any_sync(FULL, ml0 > st.m0 + kScoreCap || ml1 > st.m1 + kScoreCap || fmaxf(wm0, wm1) > kWeightHi)) {
+    // every lane takes part in every reduction (no shuffle inside a conditional expression)
+    const float ms0 = warp_max_g(ml0), ms1 = warp_max_g(ml1);
+    const float wc0 = warp_max_g(wm0), wc1 = warp_max_g(wm1);
+    const bool tr0 = ms0 > st.m0 + kScoreCap || wc0 > kWeightHi;
+    const bool tr1 = ms1 > st.m1 + kScoreCap || wc1 > kWeightHi;
+    const float b0 = tr0 ? ref_base(st.m0, ms0) : st.m0, b1 = tr1 ? ref_base(st.m1, ms1) : st.m1;
+    const float q0 = b0 == -INFINITY ? 0.f : b0, q1 = b1 == -INFINITY ? 0.f : b1;
+    float x0 = 0.f, x1 = 0.f;  // the largest P_v per column against the bases
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      const float a00 = fast_exp2(pg[i].s[0] - q0) * pg[i].sv0, a10 = fast_exp2(pg[i].s[2] - q0) * pg[i].sv1;
+      const float a01 = fast_exp2(pg[i].s[1] - q1) * pg[i].sv0, a11 = fast_exp2(pg[i].s[3] - q1) * pg[i].sv1;
+      x0 = fmaxf(x0, fmaxf(ok00 ? a00 : 0.f, ok10 ? a10 : 0.f));
+      x1 = fmaxf(x1, fmaxf(ok01 ? a01 : 0.f, ok11 ? a11 : 0.f));
+    }
+    x0 = warp_max_g(x0);
+    x1 = warp_max_g(x1);
+    const float n0 = tr0 ? ref_new(b0, ms0, x0, &g_flags_decode_int4) : st.m0;
+    const float n1 = tr1 ? ref_new(b1, ms1, x1, &g_flags_decode_int4) : st.m1;
+    const float al0 = tr0 ? fast_exp2(st.m0 - n0) : 1.f;  // 0 for a column that had no keys yet
+    const float al1 = tr1 ? fast_exp2(st.m1 - n1) : 1.f;
     st.m0 = n0;
     st.m1 = n1;
     st.l0 *= al0;
@@ -542,29 +614,16 @@ __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&s
       st.acc[i][2] *= al0;
       st.acc[i][3] *= al1;
     }
+    weights(n0 == -INFINITY ? 0.f : n0, n1 == -INFINITY ? 0.f : n1);
+    if (fmaxf(wm0, wm1) > kWeightHi) atomicOr(&g_flags_decode_int4, ERR_RANGE);
   }
-  const float r0 = st.m0 == -INFINITY ? 0.f : st.m0, r1 = st.m1 == -INFINITY ? 0.f : st.m1;
-  uint32_t X0[NP], X1[NP];
+  st.l0 += ls0;
+  st.l1 += ls1;
 #pragma unroll
-  for (int i = 0; i < NP; ++i) {
-    const float p00 = fast_exp2(pg[i].s[0] - r0), p10 = fast_exp2(pg[i].s[2] - r0);
-    const float p01 = fast_exp2(pg[i].s[1] - r1), p11 = fast_exp2(pg[i].s[3] - r1);
-    st.l0 += p00 + p10;
-    st.l1 += p01 + p11;
-    // P_v = p * scale_v (fp16), and sum P_v * zp_v for the zero-point correction
-    float w00 = p00 * pg[i].sv0, w10 = p10 * pg[i].sv1, w01 = p01 * pg[i].sv0, w11 = p11 * pg[i].sv1;
-    if (MASKED) {
-      w00 = ok00 ? w00 : 0.f;
-      w01 = ok01 ? w01 : 0.f;
-      w10 = ok10 ? w10 : 0.f;
-      w11 = ok11 ? w11 : 0.f;
-    }
-    const __half2 h0 = __floats2half2_rn(w00, w10), h1 = __floats2half2_rn(w01, w11);
-    const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+  for (int i = 0; i < NP; ++i) {  // sum P_v * zp_v (the fp16 P_v the products use)
+    const float2 f0 = __half22float2(u32_as_h2(X0[i])), f1 = __half22float2(u32_as_h2(X1[i]));
     st.pz0 += f0.x * pg[i].zv0 + f0.y * pg[i].zv1;
     st.pz1 += f1.x * pg[i].zv0 + f1.y * pg[i].zv1;
-    X0[i] = h2_as_u32(h0);
-    X1[i] = h2_as_u32(h1);
   }
   // ---- O^T += V^T . P_v^T
 #pragma unroll
@@ -640,10 +699,13 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     if (x >= run.n) return 0;
     const long long X = run.base + x;
     while (X >= lc.P + lc.np && lc.b < a.B) seq_next<MODS>(a, lc);
-    return lc.b < a.B ? __ldg(p.block_table + static_cast<long long>(lc.b) * a.max_blocks + (X - lc.P + lc.f)) : -1;
+    if (lc.b >= a.B) return -1;
+    const long long row = a.vseq != nullptr ? a.vseq[lc.b].x : lc.b;  // a virtual sequence: its sequence's row
+    return __ldg(p.block_table + row * a.max_blocks + (X - lc.P + lc.f));
   };
   // Stage k into ring slot `slot`: lane i copies page k * W + i (expect_tx first, by lane 0).
   auto issue = [&](int k, int slot, int bid) {  // warp-wide
+    if (k == p.withhold && blockIdx.x == 0 && blockIdx.y == 0) return;  // its full barrier never completes
     const int x0 = k * W, npg = min(W, run.n - x0);
     const uint32_t bar = smem_u32(&s_full[slot]);
     const uint32_t stg = dbase + base + slot * Gm::STAGE;
@@ -698,7 +760,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     while (nxt < n_stages) {
       const uint32_t eb = smem_u32(&s_empty[nslot]), par = static_cast<uint32_t>(nrnd - 1) & 1u;
       if (nxt <= need) {
-        if (!__all_sync(FULL, mbar_wait(eb, par))) return false;
+        if (!__all_sync(FULL, mbar_wait(eb, par, p.wait_ns))) return false;
       } else if (!__all_sync(FULL, mbar_test_wait(eb, par))) {
         break;
       }
@@ -725,14 +787,30 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   uint32_t qf[Gm::KSTEPS][2];
   float qs0 = 0.f, qs1 = 0.f;
   bool have_q = false, abort = false;
-  const float sm24 = p.sm_log2 * kTwo24;  // the K operands carry a factor 2^-24
+  float sm24 = 0.f;  // score scale of the piece: sm * log2 e * 2^24 (K operands) * 2^k (q shift)
   ScoreMods md{};
-  if constexpr (MODS) {
+  if constexpr (MODS) {  // MMA column n is query token n / G, head h G + n % G of it
     const int c0 = 2 * (lane & 3), G = a.G;
     const float lg2e = 1.4426950408889634f;
-    md.sl0 = p.alibi != nullptr && c0 < G ? __ldg(p.alibi + h * G + c0) * lg2e : 0.f;
-    md.sl1 = p.alibi != nullptr && c0 + 1 < G ? __ldg(p.alibi + h * G + c0 + 1) * lg2e : 0.f;
+    md.sl0 = p.alibi != nullptr && c0 < G * a.Q ? __ldg(p.alibi + h * G + c0 % G) * lg2e : 0.f;
+    md.sl1 = p.alibi != nullptr && c0 + 1 < G * a.Q ? __ldg(p.alibi + h * G + (c0 + 1) % G) * lg2e : 0.f;
   }
+  // per piece: the lane's columns' key ranges [lw, lim) and the first query token's limit limf
+  // (pages below it, and at or above the last token's window start lwl, need no masks). Columns
+  // past the block's query tokens repeat its last token (their rows are never read).
+  int lim0 = 0, lim1 = 0, lw0 = 0, lw1 = 0, limf = 0, lwl = 0;
+  auto columns = [&]() {
+    const int nq = a.vseq != nullptr ? a.vseq[cur.b].w : 1;
+    const int k0 = min((2 * (lane & 3)) / a.G, nq - 1), k1 = min((2 * (lane & 3) + 1) / a.G, nq - 1);
+    md.qp0 = cur.L - nq + k0;
+    md.qp1 = cur.L - nq + k1;
+    lim0 = md.qp0 + 1;
+    lim1 = md.qp1 + 1;
+    lw0 = a.window > 0 ? max(0, md.qp0 + 1 - a.window) : 0;
+    lw1 = a.window > 0 ? max(0, md.qp1 + 1 - a.window) : 0;
+    limf = cur.L - nq + 1;
+    lwl = a.window > 0 ? max(0, cur.L - a.window) : 0;
+  };
   // the current piece in run coordinates: its pages are run pages < pe_x, run page x is page
   // x + off of sequence cur.b, and its tokens are [t0, t1)
   int pe_x = 0, off = 0, t0 = 0, t1 = 0;
@@ -749,7 +827,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     }
   };
   bounds();
-  md.qpos = cur.L - 1;
+  columns();
   auto finish_piece = [&]() {
     const long long slot = run.fixed ? static_cast<long long>(blockIdx.x) : blockIdx.x + static_cast<long long>(cur.b);
     int4_finish<D, MTOK>(a, st, slot, sub, h, lane);
@@ -765,7 +843,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   auto wait_stage = [&](int k, int slot, int rnd) -> bool {
     const uint32_t fb = smem_u32(&s_full[slot]);
     if (__all_sync(FULL, mbar_try_wait(fb, rnd & 1))) return true;
-    if (__all_sync(FULL, mbar_wait(fb, rnd & 1))) return true;
+    if (__all_sync(FULL, mbar_wait(fb, rnd & 1, p.wait_ns))) return true;
     if (lane == 0) atomicOr(&g_flags_decode_int4, ERR_TIMEOUT);
     for (int i = k; i < k + NS && i < n_stages; ++i)
       mbar_wait(smem_u32(&s_full[i % NS]), (i / NS) & 1, 100000000ull);
@@ -783,10 +861,12 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
       }
       if (cur.b >= a.B) break;  // cannot happen: the run lies inside the batch's pages
       bounds();
-      md.qpos = cur.L - 1;
+      columns();
     }
     if (!have_q) {
-      load_query<D, MTOK>(p, qarea, cur.b, h, lane, qf, qs0, qs1, q_prefetched == cur.b);
+      float qmul;
+      load_query<D, MTOK>(p, qarea, cur.b, h, lane, qf, qs0, qs1, qmul, q_prefetched == cur.b);
+      sm24 = p.sm_log2 * kTwo24 * qmul;
       q_prefetched = -1;
       if (pe_x < run.n && !run.fixed) {  // the run goes on into another sequence: fetch its query now
         SeqCursor nx = cur;
@@ -801,12 +881,9 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     const int nb = (x + off) * kPage;  // position of the page's row 0 in its sequence
     const int sj1 = sj + 1 == NS ? 0 : sj + 1, rj1 = sj + 1 == NS ? rj + 1 : rj;
     const uint32_t so[2] = {base + sj * Gm::STAGE, base + sj1 * Gm::STAGE};
-    // two full pages of the piece, both below every column's causal limit (multi-token decode
-    // runs in the modifier kernel; elsewhere Q = 1 and the limit is the sequence end)
-    const int tpair = MTOK ? min(t1, cur.L - a.Q + 1) : t1;
-    const bool pair = nb >= t0 && nb + (W + 1) * kPage <= tpair && x + W < pe_x;
-    const int lim0 = MTOK ? cur.L - a.Q + 1 + (2 * (lane & 3)) / a.G : 0;
-    const int lim1 = MTOK ? cur.L - a.Q + 1 + (2 * (lane & 3) + 1) / a.G : 0;
+    // two full pages of the piece inside every column's key range (one query token: the piece)
+    const int tpair = MTOK ? min(t1, limf) : t1;
+    const bool pair = nb >= (MTOK ? max(t0, lwl) : t0) && nb + (W + 1) * kPage <= tpair && x + W < pe_x;
     if (warp == 0 && nxt <= (pair ? j + 1 : j) && !produce(pair ? j + 1 : j)) {
       abort = true;
       if (lane == 0) atomicOr(&g_flags_decode_int4, ERR_TIMEOUT);
@@ -818,7 +895,8 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
         break;
       }
       if (warp == 0) produce(-1);  // the slots freed meanwhile (at the start: the unused ones)
-      int4_pages<D, W, 2, false, MODS, MTOK>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, lim0, lim1, p, md);
+      int4_pages<D, W, 2, false, MODS, MTOK>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, lim0, lim1, lw0,
+                                             lw1, p, md);
       mbar_arrive(smem_u32(&s_empty[sj]));
       mbar_arrive(smem_u32(&s_empty[sj1]));
       j += 2;
@@ -830,7 +908,8 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
         break;
       }
       if (warp == 0) produce(-1);  // the slots freed meanwhile (at the start: the unused ones)
-      int4_pages<D, W, 1, true, MODS, MTOK>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, lim0, lim1, p, md);
+      int4_pages<D, W, 1, true, MODS, MTOK>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, lim0, lim1, lw0,
+                                            lw1, p, md);
       mbar_arrive(smem_u32(&s_empty[sj]));
       j += 1;
       sj = sj1;
@@ -895,6 +974,107 @@ static kvq_status launch_int4(const Int4Params &p, const SplitPlan &plan, cudaSt
 
 using namespace kvq;
 
+namespace kvq {
+// Error-path test settings (kvq_debug_set_wait): the wait limit of the decode kernels' bounded
+// waits, and a stage whose copies the next INT4 decode call withholds (one call only).
+static std::atomic<unsigned long long> g_wait_ns{2000000000ull};
+static std::atomic<int> g_withhold{-1};
+}  // namespace kvq
+
+extern "C" kvq_status kvq_debug_set_wait(uint64_t wait_limit_ns, int32_t withhold_stage) {
+  if (withhold_stage < -1) return KVQ_ERR_INVALID_ARG;
+  kvq::g_wait_ns.store(wait_limit_ns == 0 ? 2000000000ull : wait_limit_ns);
+  kvq::g_withhold.store(withhold_stage);
+  return KVQ_OK;
+}
+
+namespace kvq {
+
+// Multi-token decode (unified_attention_int4 with max_seqlen_q > 1): the query tokens of every
+// sequence are cut into blocks of up to QB = 8 / G tokens -- the MMA's 8 columns, G heads per
+// token -- and each block is a virtual sequence whose keys end at its last token's position + 1.
+// vseq[v] = {sequence b (its block-table row), that key end, the block's first q / out row, its
+// tokens}; entries past the last block are empty (key end 0). One CTA, sequences 256 at a time.
+__global__ void __launch_bounds__(256) build_vseq_kernel(const int32_t *qsl, int q_uniform, const int32_t *seq_lens,
+                                                         int B, int QB, int max_blocks, int total_q, int4 *vseq,
+                                                         int vmax) {
+  __shared__ long long s_scan[8];
+  long long running = 0;
+  for (int base = 0; base < B; base += 256) {
+    const int b = base + threadIdx.x;
+    int qb = 0, r0 = 0, L = 0;
+    if (b < B) {
+      if (qsl != nullptr) {
+        r0 = __ldg(qsl + b);
+        const int r1 = __ldg(qsl + b + 1);
+        qb = r1 - r0;
+        if (r0 < 0 || qb < 0 || r1 > total_q) {  // query rows outside q: skipped, flagged
+          atomicOr(&g_flags_decode_int4, ERR_SEQLEN);
+          qb = 0;
+        }
+      } else {
+        r0 = b * q_uniform;
+        qb = q_uniform;
+      }
+      L = __ldg(seq_lens + b);
+      if (L > max_blocks * kPage) {
+        atomicOr(&g_flags_decode_int4, ERR_SEQLEN);
+        L = max_blocks * kPage;
+      }
+      L = max(L, 0);
+    }
+    const long long nv = (qb + QB - 1) / QB;
+    long long chunk;
+    const long long off = block_scan_256(nv, s_scan, &chunk) + running - nv;
+    for (int k = 0; k < nv; ++k) {
+      const int i0 = k * QB, nq = min(QB, qb - i0);
+      if (off + k < vmax) vseq[off + k] = make_int4(b, max(0, L - qb + i0 + nq), r0 + i0, nq);
+    }
+    running += chunk;
+  }
+  for (long long v = running + threadIdx.x; v < vmax; v += 256) vseq[v] = make_int4(0, 0, 0, 0);
+}
+
+// Geometry of a decode call: multi-token or not, tokens per block QB, (virtual) sequences.
+struct CallGeom {
+  bool mtok;
+  int QB;
+  long long nseq;
+};
+static bool call_geom(int B, int Hq, int Hk, const kvq_score_mods *mods, CallGeom *g) {
+  g->mtok = mods != nullptr && (mods->q_len > 1 || mods->query_start_loc != nullptr);
+  g->QB = 1;
+  g->nseq = B;
+  if (!g->mtok) return true;
+  if (Hk < 1 || Hq % Hk != 0 || Hq / Hk > 8) return false;
+  g->QB = 8 / (Hq / Hk);
+  if (mods->query_start_loc != nullptr) {
+    if (mods->total_q < 0) return false;
+    g->nseq = static_cast<long long>(B) + (mods->total_q + g->QB - 1) / g->QB;  // sum of ceil(q_b / QB)
+  } else {
+    g->nseq = static_cast<long long>(B) * ((mods->q_len + g->QB - 1) / g->QB);
+  }
+  return g->nseq <= 0x7fffffffLL;
+}
+static size_t mods_workspace_bytes(int B, int Hq, int Hk, int D, int num_splits, const kvq_score_mods *mods,
+                                   SplitPlan *plan, CallGeom *g) {
+  if (!call_geom(B, Hq, Hk, mods, g)) return 0;
+  if (!make_plan(static_cast<int>(g->nseq), Hk, num_splits, plan)) return 0;
+  const size_t ws = workspace_bytes(static_cast<int>(g->nseq), g->QB * Hq, D, *plan);
+  return g->mtok ? ws + (static_cast<size_t>(g->nseq) * sizeof(int4) + 255) / 256 * 256 : ws;
+}
+
+}  // namespace kvq
+
+extern "C" size_t kvq_decode_int4_mods_workspace_bytes(int32_t B, int32_t Hq, int32_t Hk, int32_t D,
+                                                       int32_t num_splits, const kvq_score_mods *mods) {
+  if (B < 0 || Hq < 1 || Hk < 1 || Hq % Hk || (D != 64 && D != 128) || num_splits < 0) return 0;
+  if (mods && (mods->q_len < 0 || (mods->query_start_loc && mods->total_q < 0))) return 0;
+  SplitPlan plan;
+  CallGeom g;
+  return mods_workspace_bytes(B, Hq, Hk, D, num_splits, mods, &plan, &g);
+}
+
 extern "C" kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
                                            const float *k_scale, const float *v_scale,
                                            const int32_t *block_table, int32_t max_blocks,
@@ -908,11 +1088,10 @@ extern "C" kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache
     return KVQ_ERR_INVALID_ARG;
   if (mods && (mods->sliding_window < 0 || !(mods->softcap >= 0.f) || !(mods->softcap < INFINITY) ||
                (mods->sinks && !aligned(mods->sinks, 4)) ||
-               (mods->alibi_slopes && !aligned(mods->alibi_slopes, 4)) || mods->q_len < 0))
+               (mods->alibi_slopes && !aligned(mods->alibi_slopes, 4)) || mods->q_len < 0 ||
+               (mods->lse_out && !aligned(mods->lse_out, 4)) ||
+               (mods->query_start_loc && (!aligned(mods->query_start_loc, 4) || mods->total_q < 0))))
     return KVQ_ERR_INVALID_ARG;
-  const int Q = mods && mods->q_len > 1 ? mods->q_len : 1;  // query tokens per sequence
-  if (Q > 1 && (Hk < 1 || Hq % Hk != 0 || (Hq / Hk) * Q > 8 || mods->sliding_window > 0 || mods->alibi_slopes))
-    return KVQ_ERR_UNSUPPORTED;  // G * Q MMA columns; window and ALiBi are single-token here
   if (Hq % Hk != 0) return KVQ_ERR_INVALID_ARG;
   if (out_dtype != KVQ_BF16 && out_dtype != KVQ_F16 && out_dtype != KVQ_F32) return KVQ_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return KVQ_ERR_UNSUPPORTED;
@@ -920,8 +1099,12 @@ extern "C" kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache
   if (Hq / Hk > 8) return KVQ_ERR_UNSUPPORTED;
   if (!(softmax_scale > 0.f) || !(softmax_scale < INFINITY)) return KVQ_ERR_INVALID_ARG;
   SplitPlan plan;
-  if (!make_plan(B, Hk, num_splits, &plan)) return KVQ_ERR_UNSUPPORTED;
-  if (B == 0) return KVQ_OK;
+  CallGeom cg;
+  if (!call_geom(B, Hq, Hk, mods, &cg) || !make_plan(static_cast<int>(cg.nseq), Hk, num_splits, &plan))
+    return KVQ_ERR_UNSUPPORTED;
+  if (B == 0 || cg.nseq == 0) return KVQ_OK;
+  const size_t need = mods_workspace_bytes(B, Hq, Hk, D, num_splits, mods, &plan, &cg);
+  if (need == 0) return KVQ_ERR_UNSUPPORTED;
   if (!q || !k_cache || !v_cache || !k_scale || !v_scale || !block_table || !seq_lens || !out ||
       !workspace)
     return KVQ_ERR_INVALID_ARG;
@@ -930,28 +1113,34 @@ extern "C" kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache
       !aligned(out, 16) || !aligned(workspace, 16) || (rht_signs && !aligned(rht_signs, 16)))
     return KVQ_ERR_INVALID_ARG;
   if (max_blocks < 1) return KVQ_ERR_INVALID_ARG;
-  if (workspace_bytes < kvq::workspace_bytes(B, Q * Hq, D, plan)) return KVQ_ERR_WORKSPACE;
+  if (workspace_bytes < need) return KVQ_ERR_WORKSPACE;
 
   Int4Params p;
   SplitArgs &sa = p.s;
+  const int nseq = static_cast<int>(cg.nseq);
   sa.seq_lens = seq_lens;
   sa.max_blocks = max_blocks;
   sa.num_splits = num_splits;
-  sa.B = B;
-  sa.Hq = Q * Hq;  // output rows per sequence
-  sa.Q = Q;
+  sa.B = nseq;
+  sa.Hq = cg.QB * Hq;  // output rows per (virtual) sequence
+  sa.Q = cg.QB;
   sa.Hk = Hk;
   sa.G = Hq / Hk;
   sa.heads_per_cta = plan.heads_per_cta;
   sa.warps_per_head = plan.warps_per_head;
   sa.seg_ctas = plan.seg_ctas;
   sa.slots = plan.slots;
-  workspace_carve(workspace, B, Q * Hq, D, plan, &sa.part_o, &sa.part_lse, &sa.seg_first, &sa.seg_last);
+  workspace_carve(workspace, nseq, cg.QB * Hq, D, plan, &sa.part_o, &sa.part_lse, &sa.seg_first, &sa.seg_last);
+  int4 *vseq = cg.mtok ? reinterpret_cast<int4 *>(static_cast<uint8_t *>(workspace) +
+                                                  kvq::workspace_bytes(nseq, cg.QB * Hq, D, plan))
+                       : nullptr;
+  sa.vseq = vseq;
   sa.signs = rht_signs;
   sa.out = out;
   sa.out_dtype = out_dtype;
   sa.window = mods ? mods->sliding_window : 0;
   sa.sinks = mods ? mods->sinks : nullptr;
+  sa.lse_out = mods ? mods->lse_out : nullptr;
   p.q = static_cast<const __nv_bfloat16 *>(q);
   if (!int4_tensor_maps(k_cache, v_cache, k_scale, v_scale, num_blocks, Hk, D, &p.maps)) return KVQ_ERR_CUDA;
   p.block_table = block_table;
@@ -962,10 +1151,17 @@ extern "C" kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache
   p.softcap2 = static_cast<float>(cap2);
   p.inv_softcap2 = cap2 > 0.0 ? static_cast<float>(1.0 / cap2) : 0.f;
   p.alibi = mods ? mods->alibi_slopes : nullptr;
+  p.wait_ns = g_wait_ns.load();
+  p.withhold = g_withhold.exchange(-1);  // one call only
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cg.mtok) {  // the virtual sequences, in stream order before the split kernel
+    build_vseq_kernel<<<1, 256, 0, s>>>(mods->query_start_loc, mods->query_start_loc ? 0 : mods->q_len, seq_lens, B,
+                                        cg.QB, max_blocks, mods->total_q, vseq, nseq);
+    if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  }
   // sinks act in the merge only; window, soft cap and ALiBi need the modifier kernel (which also
   // takes multi-token decode); multi-token decode alone has its own
-  const int var = (p.softcap2 > 0.f || p.alibi != nullptr || sa.window > 0) ? 1 : (Q > 1 ? 2 : 0);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int var = (p.softcap2 > 0.f || p.alibi != nullptr || sa.window > 0) ? 1 : (cg.mtok ? 2 : 0);
   if (D == 128)
     return var == 0 ? launch_int4<128, 0>(p, plan, s) : var == 1 ? launch_int4<128, 1>(p, plan, s) : launch_int4<128, 2>(p, plan, s);
   return var == 0 ? launch_int4<64, 0>(p, plan, s) : var == 1 ? launch_int4<64, 1>(p, plan, s) : launch_int4<64, 2>(p, plan, s);
@@ -1019,6 +1215,10 @@ extern "C" kvq_status kvq_decode_int4_noalloc(const void *q, const uint8_t *k_ca
                                               int32_t B, int32_t Hq, int32_t Hk, int32_t D,
                                               int32_t block_size, int64_t num_blocks,
                                               kvq_stream_t stream) {
+  if (B == 0)  // empty work: a successful no-op, as for the workspace entry point
+    return kvq_decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, max_blocks, seq_lens,
+                           rht_signs, softmax_scale, num_splits, nullptr, 0, out, out_dtype, B, Hq, Hk, D,
+                           block_size, num_blocks, stream);
   void *scratch = kvq::noalloc_scratch();
   if (scratch == nullptr) return KVQ_ERR_CUDA;
   // The workspace entry point validates everything and rejects a scratch need above the array

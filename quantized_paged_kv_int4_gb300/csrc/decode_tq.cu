@@ -9,11 +9,13 @@
 //
 // GB300 design: the INT4 kernel's structure (one warp per kv head and run of pages, private
 // cp.async ring, mma.m16n8k16 for both contractions, separate merge kernel). Keys go to
-// fp16 with the hardware E4M3x2 -> f16x2 conversion (exact); q (fp32) is split into fp16 hi + lo
-// parts, two MMAs per k-step, so the score keeps ~22 bits. Value indices enter as exact fp16
-// subnormals (the index bits masked into a zero-exponent fp16: idx * 2^-24, or idx * 2^-20 for a
-// high nibble) weighted by P_v = p * scale in fp16; the power of two is undone in the epilogue
-// and sum_n p_n * zero_n is added in fp32.
+// fp16 with the hardware E4M3x2 -> f16x2 conversion (exact); q (fp32, shifted by a power of two
+// into the fp16 range, decode_common.cuh) is split into fp16 hi + lo parts, two MMAs per k-step,
+// so the score keeps ~22 bits. Value indices enter as exact fp16 subnormals (the index bits
+// masked into a zero-exponent fp16: idx * 2^-24, or idx * 2^-20 for a high nibble) weighted by
+// P_v = 2^(S - m) * scale in fp16 against a per-column softmax reference m that keeps P_v inside
+// fp16 (decode_common.cuh); the power of two is undone in the epilogue and sum_n p_n * zero_n is
+// added in fp32.
 
 #include "decode_common.cuh"
 #include "kvq_host.h"
@@ -77,17 +79,26 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
   int bids_cur = load_bids(0);
   int bids_next = load_bids(1);
 
-  // -------- query -> fp16 hi / lo parts in shared memory, then B fragments
+  // -------- query -> fp16 hi / lo parts (of q * 2^-k) in shared memory, then B fragments
+  float sc2;  // score scale of the piece: attn_scale * log2 e * 2^k
   {
     constexpr int J = D / 32;
     const float *qb = p.q + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(h) * G) * D;
+    float qmax = 0.f;
+    for (int n = 0; n < G; ++n) {
+#pragma unroll
+      for (int j = 0; j < J; ++j) qmax = fmaxf(qmax, fabsf(qb[n * D + lane + 32 * j]));
+    }
+    const int qk = query_shift(warp_max(qmax), 0, &g_flags_decode_tq);
+    const float qdiv = pow2i(-qk);
+    sc2 = p.sc_log2 * pow2i(qk);
     __half *qh = reinterpret_cast<__half *>(qarea);
     for (int n = 0; n < 8; ++n) {
 #pragma unroll
       for (int j = 0; j < J; ++j) {
         const int e = lane + 32 * j;
         const int head = PACKQ ? (n & 3) : n;
-        const float x = head < G ? qb[head * D + e] : 0.f;
+        const float x = head < G ? qb[head * D + e] * qdiv : 0.f;
         const __half hi = __float2half_rn(x);
         const __half lo = __float2half_rn(x - __half2float(hi));
         if constexpr (PACKQ) {
@@ -203,28 +214,46 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
     }
     const uint8_t *sb = st + Gm::KB + Gm::VB;
     const uint32_t sz0 = lds32(sb + g * 4), sz1 = lds32(sb + (g + 8) * 4);
-    const float s00 = ok0 ? c[0] * p.sc_log2 : -INFINITY;
-    const float s01 = ok0 ? c[1] * p.sc_log2 : -INFINITY;
-    const float s10 = ok1 ? c[2] * p.sc_log2 : -INFINITY;
-    const float s11 = ok1 ? c[3] * p.sc_log2 : -INFINITY;
-
-    const float mx0 = fmaxf(m0, warp_max_g(fmaxf(s00, s10)));
-    const float mx1 = fmaxf(m1, warp_max_g(fmaxf(s01, s11)));
-    const float r0 = mx0 == -INFINITY ? 0.f : mx0, r1 = mx1 == -INFINITY ? 0.f : mx1;
-    const float al0 = fast_exp2(m0 - r0), al1 = fast_exp2(m1 - r1);
-    m0 = mx0;
-    m1 = mx1;
-    const float p00 = fast_exp2(s00 - r0), p10 = fast_exp2(s10 - r0);
-    const float p01 = fast_exp2(s01 - r1), p11 = fast_exp2(s11 - r1);
-    l0 = l0 * al0 + (p00 + p10);
-    l1 = l1 * al1 + (p01 + p11);
-
+    const float s00 = ok0 ? c[0] * sc2 : -INFINITY;
+    const float s01 = ok0 ? c[1] * sc2 : -INFINITY;
+    const float s10 = ok1 ? c[2] * sc2 : -INFINITY;
+    const float s11 = ok1 ? c[3] * sc2 : -INFINITY;
     const float2 szf0 = __half22float2(u32_as_h2(sz0)), szf1 = __half22float2(u32_as_h2(sz1));  // (scale, zero)
-    const __half2 X0 = __floats2half2_rn(ok0 ? p00 * szf0.x : 0.f, ok1 ? p10 * szf1.x : 0.f);
-    const __half2 X1 = __floats2half2_rn(ok0 ? p01 * szf0.x : 0.f, ok1 ? p11 * szf1.x : 0.f);
-    pz0 = pz0 * al0 + ((ok0 ? p00 * szf0.y : 0.f) + (ok1 ? p10 * szf1.y : 0.f));
-    pz1 = pz1 * al1 + ((ok0 ? p01 * szf0.y : 0.f) + (ok1 ? p11 * szf1.y : 0.f));
-    if (!__all_sync(FULL, al0 == 1.f && al1 == 1.f)) {  // a running max moved: rescale
+
+    // online softmax against the columns' references (decode_common.cuh): p = 2^(S - m), P_v =
+    // p * scale; a warp vote finds the rare step that must raise a reference
+    float p00, p01, p10, p11, w00, w01, w10, w11;
+    auto weights = [&](float q0, float q1) {
+      p00 = fast_exp2(s00 - q0);
+      p10 = fast_exp2(s10 - q0);
+      p01 = fast_exp2(s01 - q1);
+      p11 = fast_exp2(s11 - q1);
+      w00 = ok0 ? p00 * szf0.x : 0.f;
+      w01 = ok0 ? p01 * szf0.x : 0.f;
+      w10 = ok1 ? p10 * szf1.x : 0.f;
+      w11 = ok1 ? p11 * szf1.x : 0.f;
+    };
+    weights(m0 == -INFINITY ? 0.f : m0, m1 == -INFINITY ? 0.f : m1);
+    const float ml0 = fmaxf(s00, s10), ml1 = fmaxf(s01, s11);
+    if (__any_sync(FULL, ml0 > m0 + kScoreCap || ml1 > m1 + kScoreCap ||
+                             fmaxf(fmaxf(w00, w10), fmaxf(w01, w11)) > kWeightHi)) {
+      // every lane takes part in every reduction (no shuffle inside a conditional expression)
+      const float ms0 = warp_max_g(ml0), ms1 = warp_max_g(ml1);
+      const float wc0 = warp_max_g(fmaxf(w00, w10)), wc1 = warp_max_g(fmaxf(w01, w11));
+      const bool tr0 = ms0 > m0 + kScoreCap || wc0 > kWeightHi;
+      const bool tr1 = ms1 > m1 + kScoreCap || wc1 > kWeightHi;
+      const float b0 = tr0 ? ref_base(m0, ms0) : m0, b1 = tr1 ? ref_base(m1, ms1) : m1;
+      weights(b0 == -INFINITY ? 0.f : b0, b1 == -INFINITY ? 0.f : b1);
+      const float x0 = warp_max_g(fmaxf(w00, w10)), x1 = warp_max_g(fmaxf(w01, w11));
+      const float n0 = tr0 ? ref_new(b0, ms0, x0, &g_flags_decode_tq) : m0;
+      const float n1 = tr1 ? ref_new(b1, ms1, x1, &g_flags_decode_tq) : m1;
+      const float al0 = tr0 ? fast_exp2(m0 - n0) : 1.f, al1 = tr1 ? fast_exp2(m1 - n1) : 1.f;
+      m0 = n0;
+      m1 = n1;
+      l0 *= al0;
+      l1 *= al1;
+      pz0 *= al0;
+      pz1 *= al1;
 #pragma unroll
       for (int i = 0; i < Gm::MT; ++i) {
         acc[i][0] *= al0;
@@ -232,7 +261,15 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
         acc[i][2] *= al0;
         acc[i][3] *= al1;
       }
+      weights(n0 == -INFINITY ? 0.f : n0, n1 == -INFINITY ? 0.f : n1);
+      if (fmaxf(fmaxf(w00, w10), fmaxf(w01, w11)) > kWeightHi) atomicOr(&g_flags_decode_tq, ERR_RANGE);
     }
+    l0 += p00 + p10;
+    l1 += p01 + p11;
+    pz0 += (ok0 ? p00 * szf0.y : 0.f) + (ok1 ? p10 * szf1.y : 0.f);
+    pz1 += (ok0 ? p01 * szf0.y : 0.f) + (ok1 ? p11 * szf1.y : 0.f);
+    const __half2 X0 = __floats2half2_rn(w00, w10);
+    const __half2 X1 = __floats2half2_rn(w01, w11);
     const int src0 = 8 * t + (g >> 1), src1 = src0 + 4;
     const uint32_t x0 = h2_as_u32(X0), x1 = h2_as_u32(X1);
     const uint32_t y0 = __shfl_sync(FULL, x0, src0), y1 = __shfl_sync(FULL, x1, src0);
@@ -362,12 +399,13 @@ static kvq_status launch_tq(const TqParams &p, const SplitPlan &plan, cudaStream
 
 using namespace kvq;
 
-extern "C" kvq_status kvq_decode_tq(const float *q, const uint8_t *kv_cache, int32_t slot_bytes,
-                                    int32_t value_bits, const int32_t *block_table,
-                                    int32_t max_blocks, const int32_t *seq_lens, float attn_scale,
-                                    int32_t num_splits, void *workspace, size_t workspace_bytes,
-                                    float *out, int32_t B, int32_t Hq, int32_t Hk, int32_t D,
-                                    int32_t block_size, int64_t num_blocks, kvq_stream_t stream) {
+extern "C" kvq_status kvq_decode_tq_lse(const float *q, const uint8_t *kv_cache, int32_t slot_bytes,
+                                        int32_t value_bits, const int32_t *block_table,
+                                        int32_t max_blocks, const int32_t *seq_lens, float attn_scale,
+                                        int32_t num_splits, void *workspace, size_t workspace_bytes,
+                                        float *out, float *lse_out, int32_t B, int32_t Hq, int32_t Hk,
+                                        int32_t D, int32_t block_size, int64_t num_blocks,
+                                        kvq_stream_t stream) {
   if (B < 0 || Hq < 1 || Hk < 1 || max_blocks < 0 || num_splits < 0 || num_blocks < 1)
     return KVQ_ERR_INVALID_ARG;
   if (Hq % Hk != 0) return KVQ_ERR_INVALID_ARG;
@@ -382,7 +420,7 @@ extern "C" kvq_status kvq_decode_tq(const float *q, const uint8_t *kv_cache, int
   if (B == 0) return KVQ_OK;
   if (!q || !kv_cache || !block_table || !seq_lens || !out || !workspace) return KVQ_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(block_table, 4) ||
-      !aligned(seq_lens, 4) || !aligned(out, 16) || !aligned(workspace, 16))
+      !aligned(seq_lens, 4) || !aligned(out, 16) || !aligned(workspace, 16) || !aligned(lse_out, 4))
     return KVQ_ERR_INVALID_ARG;
   if (max_blocks < 1) return KVQ_ERR_INVALID_ARG;
   if (workspace_bytes < kvq::workspace_bytes(B, Hq, D, plan)) return KVQ_ERR_WORKSPACE;
@@ -405,6 +443,8 @@ extern "C" kvq_status kvq_decode_tq(const float *q, const uint8_t *kv_cache, int
   sa.signs = nullptr;
   sa.window = 0;
   sa.sinks = nullptr;
+  sa.vseq = nullptr;
+  sa.lse_out = lse_out;
   sa.out = out;
   sa.out_dtype = KVQ_F32;
   p.q = q;
@@ -423,4 +463,15 @@ extern "C" kvq_status kvq_decode_tq(const float *q, const uint8_t *kv_cache, int
   }
   if (value_bits == 4) return packq ? launch_tq<64, 4, true>(p, plan, s) : launch_tq<64, 4, false>(p, plan, s);
   return packq ? launch_tq<64, 3, true>(p, plan, s) : launch_tq<64, 3, false>(p, plan, s);
+}
+
+extern "C" kvq_status kvq_decode_tq(const float *q, const uint8_t *kv_cache, int32_t slot_bytes,
+                                    int32_t value_bits, const int32_t *block_table,
+                                    int32_t max_blocks, const int32_t *seq_lens, float attn_scale,
+                                    int32_t num_splits, void *workspace, size_t workspace_bytes,
+                                    float *out, int32_t B, int32_t Hq, int32_t Hk, int32_t D,
+                                    int32_t block_size, int64_t num_blocks, kvq_stream_t stream) {
+  return kvq_decode_tq_lse(q, kv_cache, slot_bytes, value_bits, block_table, max_blocks, seq_lens, attn_scale,
+                           num_splits, workspace, workspace_bytes, out, nullptr, B, Hq, Hk, D, block_size,
+                           num_blocks, stream);
 }

@@ -141,10 +141,11 @@ __device__ __forceinline__ uint32_t pair_offset(const uint32_t *w, int bit) {
 // 4..7, and the MMA rows are 8 tokens' centroid hi parts (rows 0..7) and lo parts (rows 8..15),
 // so one MMA per 8 tokens and k-step covers all four products; rows g and g + 8 are added, and a
 // shuffle adds column n + 4 into column n (columns 4..7 then repeat heads 0..3 and are dropped).
+// ctab: the power of two the table's centroids were divided by (2^kc, decode_tq_mse_kernel).
 template <int D, int KB, int VB, int NSTAGE, bool PACKQ>
 __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring, uint8_t *qarea,
-                                             const uint2 *table, const float *sq, int RS, int b, int h,
-                                             int sub, int t0, int t1, long long slot) {
+                                             const uint2 *table, const float *sq, float ctab, int RS, int b,
+                                             int h, int sub, int t0, int t1, long long slot) {
   using Gm = MseGeom<D, KB, VB>;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -205,16 +206,25 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
   // copies are already on their way; q_rot is written by the rotation kernel this one may
   // overlap (a programmatic dependent launch), so wait for that grid first.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  float sc2;  // score scale of the piece: attn_scale * log2 e * 2^k (q shift) * 2^kc (table shift)
   {
     constexpr int J = D / 32;
     const float *qb = p.q_rot + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(h) * G) * D;
+    float qmax = 0.f;
+    for (int n = 0; n < G; ++n) {
+#pragma unroll
+      for (int j = 0; j < J; ++j) qmax = fmaxf(qmax, fabsf(qb[n * D + lane + 32 * j]));
+    }
+    const int qk = query_shift(warp_max(qmax), 0, &g_flags_decode_tq_mse);
+    const float qdiv = pow2i(-qk);
+    sc2 = p.sc_log2 * pow2i(qk) * ctab;
     __half *qh = reinterpret_cast<__half *>(qarea);
     for (int n = 0; n < 8; ++n) {
 #pragma unroll
       for (int j = 0; j < J; ++j) {
         const int e = lane + 32 * j;
         const int head = PACKQ ? (n & 3) : n;
-        const float x = head < G ? qb[head * D + e] : 0.f;
+        const float x = head < G ? qb[head * D + e] * qdiv : 0.f;
         const __half hi = __float2half_rn(x);
         const __half lo = __float2half_rn(x - __half2float(hi));
         if constexpr (PACKQ) {
@@ -304,8 +314,8 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
       for (int i = 0; i < 4; ++i) c[i] += __shfl_xor_sync(FULL, c[i], 2);  // q hi (t < 2) + q lo (t >= 2)
     }
     // per-token factor: attn_scale * log2(e) * norm (/ |c| under NORM_CORRECTION)
-    float f0 = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16_at(row0, Gm::MSE)))) * p.sc_log2;
-    float f1 = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16_at(row1, Gm::MSE)))) * p.sc_log2;
+    float f0 = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16_at(row0, Gm::MSE)))) * sc2;
+    float f1 = __half2float(__ushort_as_half(static_cast<unsigned short>(lds16_at(row1, Gm::MSE)))) * sc2;
     if (p.norm_correction) {
       ss0 += __shfl_xor_sync(FULL, ss0, 1);
       ss0 += __shfl_xor_sync(FULL, ss0, 2);
@@ -319,25 +329,44 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
     const float s10 = ok1 ? c[2] * f1 : -INFINITY;
     const float s11 = ok1 ? c[3] * f1 : -INFINITY;
 
-    const float mx0 = fmaxf(m0, warp_max_g(fmaxf(s00, s10)));
-    const float mx1 = fmaxf(m1, warp_max_g(fmaxf(s01, s11)));
-    const float r0 = mx0 == -INFINITY ? 0.f : mx0, r1 = mx1 == -INFINITY ? 0.f : mx1;
-    const float al0 = fast_exp2(m0 - r0), al1 = fast_exp2(m1 - r1);
-    m0 = mx0;
-    m1 = mx1;
-    const float p00 = fast_exp2(s00 - r0), p10 = fast_exp2(s10 - r0);
-    const float p01 = fast_exp2(s01 - r1), p11 = fast_exp2(s11 - r1);
-    l0 = l0 * al0 + (p00 + p10);
-    l1 = l1 * al1 + (p01 + p11);
-
     // value scale and zero of tokens g, g + 8 (fp16 pair at KPS + VDB)
     const uint32_t sz0 = lds32_at(row0, KPS + Gm::VDB), sz1 = lds32_at(row1, KPS + Gm::VDB);
     const float2 szf0 = __half22float2(u32_as_h2(sz0)), szf1 = __half22float2(u32_as_h2(sz1));
-    const __half2 X0 = __floats2half2_rn(ok0 ? p00 * szf0.x : 0.f, ok1 ? p10 * szf1.x : 0.f);
-    const __half2 X1 = __floats2half2_rn(ok0 ? p01 * szf0.x : 0.f, ok1 ? p11 * szf1.x : 0.f);
-    pz0 = pz0 * al0 + ((ok0 ? p00 * szf0.y : 0.f) + (ok1 ? p10 * szf1.y : 0.f));
-    pz1 = pz1 * al1 + ((ok0 ? p01 * szf0.y : 0.f) + (ok1 ? p11 * szf1.y : 0.f));
-    if (!__all_sync(FULL, al0 == 1.f && al1 == 1.f)) {  // a running max moved: rescale
+
+    // online softmax against the columns' references (decode_common.cuh): p = 2^(S - m), P_v =
+    // p * scale; a warp vote finds the rare step that must raise a reference
+    float p00, p01, p10, p11, w00, w01, w10, w11;
+    auto weights = [&](float q0, float q1) {
+      p00 = fast_exp2(s00 - q0);
+      p10 = fast_exp2(s10 - q0);
+      p01 = fast_exp2(s01 - q1);
+      p11 = fast_exp2(s11 - q1);
+      w00 = ok0 ? p00 * szf0.x : 0.f;
+      w01 = ok0 ? p01 * szf0.x : 0.f;
+      w10 = ok1 ? p10 * szf1.x : 0.f;
+      w11 = ok1 ? p11 * szf1.x : 0.f;
+    };
+    weights(m0 == -INFINITY ? 0.f : m0, m1 == -INFINITY ? 0.f : m1);
+    const float ml0 = fmaxf(s00, s10), ml1 = fmaxf(s01, s11);
+    if (__any_sync(FULL, ml0 > m0 + kScoreCap || ml1 > m1 + kScoreCap ||
+                             fmaxf(fmaxf(w00, w10), fmaxf(w01, w11)) > kWeightHi)) {
+      // every lane takes part in every reduction (no shuffle inside a conditional expression)
+      const float ms0 = warp_max_g(ml0), ms1 = warp_max_g(ml1);
+      const float wc0 = warp_max_g(fmaxf(w00, w10)), wc1 = warp_max_g(fmaxf(w01, w11));
+      const bool tr0 = ms0 > m0 + kScoreCap || wc0 > kWeightHi;
+      const bool tr1 = ms1 > m1 + kScoreCap || wc1 > kWeightHi;
+      const float b0 = tr0 ? ref_base(m0, ms0) : m0, b1 = tr1 ? ref_base(m1, ms1) : m1;
+      weights(b0 == -INFINITY ? 0.f : b0, b1 == -INFINITY ? 0.f : b1);
+      const float x0 = warp_max_g(fmaxf(w00, w10)), x1 = warp_max_g(fmaxf(w01, w11));
+      const float n0 = tr0 ? ref_new(b0, ms0, x0, &g_flags_decode_tq_mse) : m0;
+      const float n1 = tr1 ? ref_new(b1, ms1, x1, &g_flags_decode_tq_mse) : m1;
+      const float al0 = tr0 ? fast_exp2(m0 - n0) : 1.f, al1 = tr1 ? fast_exp2(m1 - n1) : 1.f;
+      m0 = n0;
+      m1 = n1;
+      l0 *= al0;
+      l1 *= al1;
+      pz0 *= al0;
+      pz1 *= al1;
 #pragma unroll
       for (int i = 0; i < Gm::MT; ++i) {
         acc[i][0] *= al0;
@@ -345,7 +374,15 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
         acc[i][2] *= al0;
         acc[i][3] *= al1;
       }
+      weights(n0 == -INFINITY ? 0.f : n0, n1 == -INFINITY ? 0.f : n1);
+      if (fmaxf(fmaxf(w00, w10), fmaxf(w01, w11)) > kWeightHi) atomicOr(&g_flags_decode_tq_mse, ERR_RANGE);
     }
+    l0 += p00 + p10;
+    l1 += p01 + p11;
+    pz0 += (ok0 ? p00 * szf0.y : 0.f) + (ok1 ? p10 * szf1.y : 0.f);
+    pz1 += (ok0 ? p01 * szf0.y : 0.f) + (ok1 ? p11 * szf1.y : 0.f);
+    const __half2 X0 = __floats2half2_rn(w00, w10);
+    const __half2 X1 = __floats2half2_rn(w01, w11);
     const int src0 = 8 * t + (g >> 1), src1 = src0 + 4;
     const uint32_t x0 = h2_as_u32(X0), x1 = h2_as_u32(X1);
     const uint32_t y0 = __shfl_sync(FULL, x0, src0), y1 = __shfl_sync(FULL, x1, src0);
@@ -434,14 +471,21 @@ __global__ void __launch_bounds__(256, 2) decode_tq_mse_kernel(const TqMseParams
   asm volatile("griddepcontrol.launch_dependents;");  // let the merge kernel's launch begin early
   using Gm = MseGeom<D, KB, VB>;
   const int warp = threadIdx.x >> 5;
-  // the pair table (MseGeom::TABLE): centroids split into fp16 hi + lo, two per entry
+  // the pair table (MseGeom::TABLE): centroids times 2^-kc (kc from the largest |centroid|, so no
+  // entry can reach 2^15) split into fp16 hi + lo, two per entry
   uint2 *table = reinterpret_cast<uint2 *>(smem);
   float *sq = reinterpret_cast<float *>(smem + Gm::NPAIR * 8 * Gm::COPIES);
+  float cmax = 0.f;
+#pragma unroll
+  for (int i = 0; i < (1 << KB); ++i) cmax = fmaxf(cmax, fabsf(__ldg(p.centroids + i)));
+  const int kc = query_shift(cmax, 0, threadIdx.x == 0 ? &g_flags_decode_tq_mse : nullptr);
+  const float cdiv = pow2i(-kc);
   for (int i = threadIdx.x; i < Gm::NPAIR * Gm::COPIES; i += 256) {
     const int e = i / Gm::COPIES;
     const float c0 = __ldg(p.centroids + (e & ((1 << KB) - 1))), c1 = __ldg(p.centroids + (e >> KB));
-    const __half h0 = __float2half_rn(c0), h1 = __float2half_rn(c1);
-    const __half l0 = __float2half_rn(c0 - __half2float(h0)), l1 = __float2half_rn(c1 - __half2float(h1));
+    const float d0 = c0 * cdiv, d1 = c1 * cdiv;
+    const __half h0 = __float2half_rn(d0), h1 = __float2half_rn(d1);
+    const __half l0 = __float2half_rn(d0 - __half2float(h0)), l1 = __float2half_rn(d1 - __half2float(h1));
     table[i] = make_uint2(static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16),
                           static_cast<uint32_t>(__half_as_ushort(l0)) | (static_cast<uint32_t>(__half_as_ushort(l1)) << 16));
     if (i % Gm::COPIES == 0) sq[e] = c0 * c0 + c1 * c1;
@@ -453,7 +497,7 @@ __global__ void __launch_bounds__(256, 2) decode_tq_mse_kernel(const TqMseParams
   const int sub = warp / p.s.heads_per_cta;
   const int h = blockIdx.y * p.s.heads_per_cta + hl;
   for_each_piece(p.s, &g_flags_decode_tq_mse, [&](int b, int t0, int t1, long long slot) {
-    tq_mse_piece<D, KB, VB, NSTAGE, PACKQ>(p, ring, qarea, table, sq, RS, b, h, sub, t0, t1, slot);
+    tq_mse_piece<D, KB, VB, NSTAGE, PACKQ>(p, ring, qarea, table, sq, pow2i(kc), RS, b, h, sub, t0, t1, slot);
   });
 }
 
@@ -563,6 +607,8 @@ extern "C" kvq_status kvq_decode_tq_mse(const float *q, const float *rotation, c
   sa.signs = nullptr;
   sa.window = 0;
   sa.sinks = nullptr;
+  sa.vseq = nullptr;
+  sa.lse_out = nullptr;
   sa.out = out;
   sa.out_dtype = KVQ_F32;
   p.q_rot = q_rot;

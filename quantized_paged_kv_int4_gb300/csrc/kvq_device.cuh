@@ -16,7 +16,13 @@ constexpr unsigned FULL = 0xffffffffu;
 constexpr int kPage = 16;  // tokens per page: one MMA M-tile of the read kernels
 
 // Device-side error flags (kvq_device_error).
-enum : unsigned { ERR_BLOCK = 1u, ERR_SEQLEN = 2u, ERR_SLOT = 4u, ERR_TIMEOUT = 8u };
+enum : unsigned { ERR_BLOCK = 1u, ERR_SEQLEN = 2u, ERR_SLOT = 4u, ERR_TIMEOUT = 8u, ERR_RANGE = 16u };
+
+// 2^k for an integer k in [-126, 127], exact.
+__device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }
+// floor(log2 x) of a finite x > 0 from its exponent field (-127 for zero and subnormals, 128
+// for inf / NaN).
+__device__ __forceinline__ int ilog2f(float x) { return ((__float_as_uint(x) >> 23) & 0xFF) - 127; }
 
 // ---------------------------------------------------------------------------------------------
 // Exact fp32 building blocks (IEEE round-to-nearest, never contracted into an FMA).
@@ -234,6 +240,11 @@ __device__ __forceinline__ float warp_sum_g(float v) {
   v += __shfl_xor_sync(FULL, v, 4);
   v += __shfl_xor_sync(FULL, v, 8);
   v += __shfl_xor_sync(FULL, v, 16);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, m));
   return v;
 }
 __device__ __forceinline__ float warp_sum(float v) {

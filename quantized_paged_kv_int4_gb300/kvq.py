@@ -24,9 +24,11 @@ KVQ_BF16, KVQ_F16, KVQ_F32 = 0, 1, 2
 
 # the C API's declared functions, in header order
 C_FUNCTIONS = ("kvq_status_string", "kvq_abi_version", "kvq_write_int4", "kvq_decode_workspace_bytes",
-               "kvq_decode_int4", "kvq_decode_int4_mods", "kvq_decode_int4_noalloc", "kvq_decode_tq",
-               "kvq_decode_tq_mse_workspace_bytes", "kvq_decode_tq_mse", "kvq_kpool_write",
-               "kvq_kpool_seed_tail", "kvq_kpool_decode_update", "kvq_fwht128", "kvq_device_error")
+               "kvq_decode_int4", "kvq_decode_int4_mods", "kvq_decode_int4_mods_workspace_bytes",
+               "kvq_decode_int4_noalloc", "kvq_decode_tq",
+               "kvq_decode_tq_lse", "kvq_decode_tq_mse_workspace_bytes", "kvq_decode_tq_mse", "kvq_kpool_write",
+               "kvq_kpool_seed_tail", "kvq_kpool_decode_update", "kvq_fwht128", "kvq_debug_set_wait",
+               "kvq_device_error")
 KVQ_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lock = threading.Lock()
@@ -38,7 +40,7 @@ c_i32, c_i64, c_sz, c_p, c_f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
 class ScoreMods(ctypes.Structure):
     """kvq_score_mods (include/kvq.h)."""
     _fields_ = [("sliding_window", c_i32), ("softcap", c_f32), ("sinks", c_p), ("alibi_slopes", c_p),
-                ("q_len", c_i32)]
+                ("q_len", c_i32), ("lse_out", c_p), ("query_start_loc", c_p), ("total_q", c_i32)]
 
 
 _SIGS = {
@@ -52,10 +54,13 @@ _SIGS = {
     "kvq_decode_int4_mods": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_f32, c_i32, c_p, c_sz,
                                             c_p, ctypes.c_int, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64,
                                             ctypes.POINTER(ScoreMods), c_p]),
+    "kvq_decode_int4_mods_workspace_bytes": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(ScoreMods)]),
     "kvq_decode_int4_noalloc": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_f32, c_i32, c_p,
                                                ctypes.c_int, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_p]),
     "kvq_decode_tq": (ctypes.c_int, [c_p, c_p, c_i32, c_i32, c_p, c_i32, c_p, c_f32, c_i32, c_p, c_sz, c_p,
                                      c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_p]),
+    "kvq_decode_tq_lse": (ctypes.c_int, [c_p, c_p, c_i32, c_i32, c_p, c_i32, c_p, c_f32, c_i32, c_p, c_sz, c_p,
+                                         c_p, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64, c_p]),
     "kvq_decode_tq_mse_workspace_bytes": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32]),
     "kvq_decode_tq_mse": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_i32, c_i32, c_i32, c_i32, c_i32, c_p, c_i32, c_p,
                                          c_f32, c_i32, c_p, c_sz, c_p, c_i32, c_i32, c_i32, c_i32, c_i32, c_i64,
@@ -66,6 +71,7 @@ _SIGS = {
                                                c_i64, c_p, c_i64, c_i64, c_p, c_p, c_p, c_i32, c_i32, c_i32, c_i32,
                                                c_i32, c_p]),
     "kvq_fwht128": (ctypes.c_int, [c_p, c_p, c_p, c_i64, c_p]),
+    "kvq_debug_set_wait": (ctypes.c_int, [ctypes.c_uint64, c_i32]),
     "kvq_device_error": (ctypes.c_int, [c_p, ctypes.POINTER(ctypes.c_uint32)]),
 }
 
@@ -128,8 +134,37 @@ def _need(t, name, dtype=None, contiguous=True):
         raise ValueError("%s must be contiguous" % name)
 
 
+_OUT_CODES = {torch.bfloat16: KVQ_BF16, torch.float16: KVQ_F16, torch.float32: KVQ_F32}
+
+
 def _out_code(dtype):
-    return {torch.bfloat16: KVQ_BF16, torch.float16: KVQ_F16, torch.float32: KVQ_F32}[dtype]
+    if dtype not in _OUT_CODES:
+        raise TypeError("out must be bfloat16, float16 or float32, got %s" % dtype)
+    return _OUT_CODES[dtype]
+
+
+def _check_int4_decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, q_len=1,
+                            ragged=False):
+    """Shape agreement of an INT4 decode call: q / out [B * q_len, Hq, D] (ragged: [total_q, Hq, D]),
+    caches [nb, bs, Hk, D/2], scales [nb, bs, Hk], block_table [B, max_blocks], seq_lens [B]."""
+    if q.dim() != 3:
+        raise ValueError("q must be [B, Hq, D]")
+    BQ, Hq, D = q.shape
+    if k_cache.dim() != 4 or tuple(v_cache.shape) != tuple(k_cache.shape) or k_cache.shape[3] * 2 != D:
+        raise ValueError("k_cache / v_cache must both be [num_blocks, block_size, Hk, D/2]")
+    nb, bs, Hk = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        if tuple(t.shape) != (nb, bs, Hk):
+            raise ValueError("%s must be [num_blocks, block_size, Hk] = %s" % (n, (nb, bs, Hk)))
+    B = block_table.shape[0] if ragged else BQ // q_len
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [B, max_blocks] with B = %d" % B)
+    if seq_lens.dim() != 1 or seq_lens.numel() != B:
+        raise ValueError("seq_lens must have B = %d entries" % B)
+    if out is not None:
+        if tuple(out.shape) != tuple(q.shape):
+            raise ValueError("out must have q's shape %s, got %s" % (tuple(q.shape), tuple(out.shape)))
+        _out_code(out.dtype)
 
 
 def kvq_write_int4(key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, rht_signs=None, stream=None):
@@ -176,13 +211,21 @@ def _workspace(workspace, B, Hq, Hk, D, num_splits, device):
     return workspace
 
 
+def kvq_decode_int4_mods_workspace_bytes(B, Hq, Hk, D, num_splits=0, mods=None):
+    return int(lib().kvq_decode_int4_mods_workspace_bytes(B, Hq, Hk, D, num_splits,
+                                                          None if mods is None else ctypes.byref(mods)))
+
+
 def kvq_decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, rht_signs, softmax_scale,
                     out=None, workspace=None, num_splits=0, out_dtype=None, stream=None,
-                    sliding_window=0, softcap=0.0, sinks=None, alibi_slopes=None, q_len=1):
+                    sliding_window=0, softcap=0.0, sinks=None, alibi_slopes=None, q_len=1, lse_out=None,
+                    query_start_loc=None):
     """unified_attention_int4 (decode): q [B * q_len, Hq, D] bf16 -> out [B * q_len, Hq, D]. Returns out.
 
     sliding_window / softcap / sinks ([Hq] fp32) / alibi_slopes ([Hq] fp32): the score modifiers
-    (kvq_decode_int4_mods); all off by default. q_len > 1: multi-token (causal) decode."""
+    (kvq_decode_int4_mods); all off by default. q_len > 1: multi-token (causal) decode;
+    query_start_loc (int32 [B + 1], the varlen cu_seqlens_q): ragged multi-token decode with q and
+    out [total_q, Hq, D]. lse_out: an fp32 [rows, Hq] tensor that receives each row's log-sum-exp."""
     _need(q, "q", torch.bfloat16)
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
         _need(t, n, torch.uint8)
@@ -193,21 +236,41 @@ def kvq_decode_int4(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens
     if rht_signs is not None:
         _need(rht_signs, "rht_signs", torch.float32)
     BQ, Hq, D = q.shape
-    if q_len < 1 or BQ % q_len:
-        raise ValueError("q must hold q_len rows per sequence")
-    B = BQ // q_len
+    ragged = query_start_loc is not None
+    if ragged:
+        _need(query_start_loc, "query_start_loc", torch.int32)
+        B = block_table.shape[0]
+        if query_start_loc.numel() != B + 1:
+            raise ValueError("query_start_loc must have B + 1 = %d entries" % (B + 1))
+    else:
+        if q_len < 1 or BQ % q_len:
+            raise ValueError("q must hold q_len rows per sequence")
+        B = BQ // q_len
+    _check_int4_decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, q_len, ragged)
     nb, bs, Hk = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
     if out is None:
         out = torch.empty((BQ, Hq, D), dtype=out_dtype or torch.float32, device=q.device)
     _need(out, "out")
-    workspace = _workspace(workspace, B, q_len * Hq, Hk, D, num_splits, q.device)
-    if sliding_window or softcap or sinks is not None or alibi_slopes is not None or q_len > 1:
+    mq = ragged or q_len > 1
+    if workspace is None and mq:
+        probe = ScoreMods(0, 0.0, None, None, int(q_len), None, _ptr(query_start_loc), int(BQ))
+        need = kvq_decode_int4_mods_workspace_bytes(B, Hq, Hk, D, num_splits, probe)
+        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=q.device)
+    else:
+        workspace = _workspace(workspace, B, Hq, Hk, D, num_splits, q.device)
+    if lse_out is not None:
+        _need(lse_out, "lse_out", torch.float32)
+        if tuple(lse_out.shape) != (BQ, Hq):
+            raise ValueError("lse_out must be [%d, %d]" % (BQ, Hq))
+    if (sliding_window or softcap or sinks is not None or alibi_slopes is not None or mq
+            or lse_out is not None):
         for t, n in ((sinks, "sinks"), (alibi_slopes, "alibi_slopes")):
             if t is not None:
                 _need(t, n, torch.float32)
                 if t.numel() != Hq:
                     raise ValueError("%s must have Hq = %d entries" % (n, Hq))
-        mods = ScoreMods(int(sliding_window), float(softcap), _ptr(sinks), _ptr(alibi_slopes), int(q_len))
+        mods = ScoreMods(int(sliding_window), float(softcap), _ptr(sinks), _ptr(alibi_slopes), int(q_len),
+                         _ptr(lse_out), _ptr(query_start_loc), int(BQ))
         _check(lib().kvq_decode_int4_mods(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                                           _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(rht_signs),
                                           float(softmax_scale), num_splits, _ptr(workspace), workspace.numel(),
@@ -238,6 +301,7 @@ def kvq_decode_int4_noalloc(q, k_cache, v_cache, k_scale, v_scale, block_table, 
     _need(out, "out")
     if rht_signs is not None:
         _need(rht_signs, "rht_signs", torch.float32)
+    _check_int4_decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out)
     B, Hq, D = q.shape
     nb, bs, Hk = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
     _check(lib().kvq_decode_int4_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
@@ -249,8 +313,9 @@ def kvq_decode_int4_noalloc(q, k_cache, v_cache, k_scale, v_scale, block_table, 
 
 
 def kvq_decode_tq(q, kv_cache, value_bits, block_table, seq_lens, attn_scale, out=None, workspace=None,
-                  num_splits=0, stream=None):
-    """TurboQuant FP8-key decode: q [B, Hq, D] fp32, kv_cache [nb, 16, Hk, slot_bytes] uint8."""
+                  num_splits=0, stream=None, lse_out=None):
+    """TurboQuant FP8-key decode: q [B, Hq, D] fp32, kv_cache [nb, 16, Hk, slot_bytes] uint8.
+    lse_out: an fp32 [B, Hq] tensor that receives each row's log-sum-exp (kvq_decode_tq_lse), or None."""
     _need(q, "q", torch.float32)
     _need(kv_cache, "kv_cache", torch.uint8)
     _need(block_table, "block_table", torch.int32)
@@ -261,6 +326,16 @@ def kvq_decode_tq(q, kv_cache, value_bits, block_table, seq_lens, attn_scale, ou
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
     _need(out, "out", torch.float32)
     workspace = _workspace(workspace, B, Hq, Hk, D, num_splits, q.device)
+    if lse_out is not None:
+        _need(lse_out, "lse_out", torch.float32)
+        if tuple(lse_out.shape) != (B, Hq):
+            raise ValueError("lse_out must be [%d, %d]" % (B, Hq))
+        _check(lib().kvq_decode_tq_lse(_ptr(q), _ptr(kv_cache), slot_bytes, value_bits, _ptr(block_table),
+                                       block_table.shape[1], _ptr(seq_lens), float(attn_scale), num_splits,
+                                       _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse_out), B, Hq, Hk,
+                                       D, bs, nb, _stream(stream)),
+               "kvq_decode_tq_lse")
+        return out
     _check(lib().kvq_decode_tq(_ptr(q), _ptr(kv_cache), slot_bytes, value_bits, _ptr(block_table),
                                block_table.shape[1], _ptr(seq_lens), float(attn_scale), num_splits,
                                _ptr(workspace), workspace.numel(), _ptr(out), B, Hq, Hk, D, bs, nb,
@@ -386,8 +461,96 @@ def kvq_fwht128(x, y=None, row_scale=None, stream=None):
     return y, row_scale
 
 
+def kvq_debug_set_wait(wait_limit_ns=0, withhold_stage=-1):
+    """Error-path tests only: the decode's bounded-wait limit (0: default) and a ring stage the next
+    INT4 decode call withholds in its first CTA (kvq_debug_set_wait in include/kvq.h)."""
+    _check(lib().kvq_debug_set_wait(int(wait_limit_ns), int(withhold_stage)), "kvq_debug_set_wait")
+
+
 def kvq_device_error(stream=None):
     """(status, flags): synchronizes the stream, reads and clears the device-side index flags."""
     flags = ctypes.c_uint32(0)
     st = lib().kvq_device_error(_stream(stream), ctypes.byref(flags))
     return int(st), int(flags.value)
+
+
+# ----------------------------------------------------------------------------------------------
+# Prepared calls: the tensors that stay the same from step to step (caches, scales, block table,
+# lengths, rotation signs, workspace) are checked once and their pointers packed once; each call
+# checks and passes only the per-step tensors. For serving loops whose buffers live across steps.
+# ----------------------------------------------------------------------------------------------
+class Int4Writer:
+    """kvq_write_int4 into fixed caches: writer(key, value, slot_mapping[, stream])."""
+
+    def __init__(self, k_cache, v_cache, k_scale, v_scale, rht_signs=None):
+        for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+            _need(t, n, torch.uint8)
+        for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+            _need(t, n, torch.float32)
+        if rht_signs is not None:
+            _need(rht_signs, "rht_signs", torch.float32)
+        nb, bs, Hk, half = k_cache.shape
+        if tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(k_scale.shape) != (nb, bs, Hk) or \
+                tuple(v_scale.shape) != (nb, bs, Hk):
+            raise ValueError("cache / scale shapes disagree")
+        self.kv_shape = (Hk, 2 * half)
+        self._keep = (k_cache, v_cache, k_scale, v_scale, rht_signs)
+        self._fn = lib().kvq_write_int4
+        self._caches = (k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(), v_scale.data_ptr())
+        self._tail = (_ptr(rht_signs),)
+        self._dims = (Hk, 2 * half, bs, nb)
+
+    def __call__(self, key, value, slot_mapping, stream=None):
+        if key.dtype != torch.bfloat16 or value.dtype != torch.bfloat16 or not key.is_cuda or not value.is_cuda:
+            raise TypeError("key / value must be CUDA bf16 tensors")
+        if key.shape[1:] != self.kv_shape or value.shape != key.shape or key.stride(-1) != 1 or value.stride(-1) != 1:
+            raise ValueError("key / value must be [T, %d, %d] with a contiguous last dim" % self.kv_shape)
+        if slot_mapping.dtype != torch.int64 or not slot_mapping.is_cuda or not slot_mapping.is_contiguous() or \
+                slot_mapping.numel() != key.shape[0]:
+            raise ValueError("slot_mapping must be a contiguous CUDA int64 [T] tensor")
+        Hk, D, bs, nb = self._dims
+        _check(self._fn(key.data_ptr(), value.data_ptr(), key.stride(0), key.stride(1), value.stride(0),
+                        value.stride(1), *self._caches, slot_mapping.data_ptr(), *self._tail, key.shape[0], Hk, D,
+                        bs, nb, _stream(stream)), "kvq_write_int4")
+
+
+class Int4Decoder:
+    """kvq_decode_int4 over fixed caches, block table, lengths and workspace:
+    decoder(q, out[, stream]) with q [B, Hq, D] bf16 and out [B, Hq, D] (bf16 / f16 / f32).
+    The block table's and lengths' contents may change between calls; their buffers may not."""
+
+    def __init__(self, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, rht_signs, softmax_scale, Hq,
+                 num_splits=0, workspace=None):
+        for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+            _need(t, n, torch.uint8)
+        for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+            _need(t, n, torch.float32)
+        _need(block_table, "block_table", torch.int32)
+        _need(seq_lens, "seq_lens", torch.int32)
+        if rht_signs is not None:
+            _need(rht_signs, "rht_signs", torch.float32)
+        nb, bs, Hk, half = k_cache.shape
+        D = 2 * half
+        B = block_table.shape[0]
+        if tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(k_scale.shape) != (nb, bs, Hk) or \
+                tuple(v_scale.shape) != (nb, bs, Hk) or seq_lens.numel() != B or block_table.dim() != 2:
+            raise ValueError("cache / scale / table shapes disagree")
+        if workspace is None:
+            workspace = decode_workspace(B, Hq, Hk, D, num_splits, device=k_cache.device)
+        _need(workspace, "workspace", torch.uint8)
+        self.q_shape = (B, Hq, D)
+        self._keep = (k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, rht_signs, workspace)
+        self._fn = lib().kvq_decode_int4
+        self._head = (k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(), v_scale.data_ptr(),
+                      block_table.data_ptr(), block_table.shape[1], seq_lens.data_ptr(), _ptr(rht_signs),
+                      float(softmax_scale), int(num_splits), workspace.data_ptr(), workspace.numel())
+        self._dims = (B, Hq, Hk, D, bs, nb)
+
+    def __call__(self, q, out, stream=None):
+        if q.dtype != torch.bfloat16 or not q.is_cuda or not q.is_contiguous() or tuple(q.shape) != self.q_shape:
+            raise ValueError("q must be a contiguous CUDA bf16 tensor of shape %s" % (self.q_shape,))
+        if not out.is_cuda or not out.is_contiguous() or tuple(out.shape) != self.q_shape:
+            raise ValueError("out must be a contiguous CUDA tensor of shape %s" % (self.q_shape,))
+        _check(self._fn(q.data_ptr(), *self._head, out.data_ptr(), _out_code(out.dtype), *self._dims,
+                        _stream(stream)), "kvq_decode_int4")
+        return out
