@@ -30,7 +30,7 @@ class Int4Case:
     """An INT4 decode case whose cache the ORACLE wrote (from seeded K / V), or random bytes."""
 
     def __init__(self, case, signs=True, num_blocks=None, random_cache=False, scale_mult=1.0,
-                 unused_fill=0):
+                 unused_fill=0, kv_transform=None):
         self.case = case
         D, Hk = case.D, case.Hk
         self.bt, self.nb = workloads.paged_layout(case.seq_lens, case.seed, num_blocks=num_blocks,
@@ -46,6 +46,8 @@ class Int4Case:
         else:
             _, _, slots = workloads.all_token_slots(self.bt, case.seq_lens)
             k, v = workloads.kv_vectors(case, slots.numel())
+            if kv_transform is not None:  # (k, v) bf16 [T, Hk, D] -> (k, v) before the write
+                k, v = kv_transform(k, v)
             self.kc = np.zeros((nb, 16, Hk, D // 2), np.uint8)
             self.vc = np.zeros_like(self.kc)
             self.ks = np.zeros((nb, 16, Hk), np.uint32)
@@ -75,6 +77,11 @@ class Int4Case:
         return g
 
 
+def assert_close_scaled(gpu, ref, unit, what=""):
+    """The attention tolerance on data of magnitude `unit`: (gpu / unit) against (ref / unit)."""
+    return assert_close(np.asarray(gpu, np.float64) / unit, np.asarray(ref, np.float64) / unit, what=what)
+
+
 def run_int4(kvq, g, scale, num_splits=0, out_dtype=torch.float32, **mods):
     out = kvq.kvq_decode_int4(g["q"], g["kc"], g["vc"], g["ks"], g["vs"], g["bt"], g["lens"], g["signs"],
                               scale, num_splits=num_splits, out_dtype=out_dtype, **mods)
@@ -96,3 +103,43 @@ class TqCase:
     def oracle(self, batch_index=None):
         return turboquant.decode_tq(self.q.numpy(), self.cache.numpy(), self.bits, self.bt.numpy(),
                                     np.asarray(self.case.seq_lens), self.scale, batch_index=batch_index)
+
+
+class MseCase:
+    def __init__(self, case, key_bits, value_bits, num_blocks=None, kps_pad=0):
+        self.case, self.kb, self.vb = case, key_bits, value_bits
+        D, Hk = case.D, case.Hk
+        mse, kps, sb = workloads.turboquant_mse_layout(D, key_bits, value_bits)
+        if kps_pad:  # a larger key_packed_size (padding after the norm)
+            kps += kps_pad
+            sb = -(-(kps + (-(-D * value_bits // 8)) + 4) // 16) * 16
+        self.kps, self.sb = kps, sb
+        self.bt, self.nb = workloads.paged_layout(case.seq_lens, case.seed, num_blocks=num_blocks)
+        base = workloads.random_turboquant_mse_slots((self.nb, 16, Hk), D, key_bits, value_bits, case.seed)
+        if kps_pad:  # move the value fields behind the padded key part
+            m0, k0, s0 = workloads.turboquant_mse_layout(D, key_bits, value_bits)
+            cache = torch.zeros((self.nb, 16, Hk, sb), dtype=torch.uint8)
+            cache[..., :k0] = base[..., :k0]
+            vlen = -(-D * value_bits // 8) + 4
+            cache[..., kps:kps + vlen] = base[..., k0:k0 + vlen]
+            base = cache
+        self.cache = base
+        self.q = workloads.query(case, dtype=torch.float32)
+        self.Pi = workloads.random_rotation(D, case.seed)
+        self.cb = workloads.mse_codebook(key_bits, D)
+        self.lens = torch.tensor(case.seq_lens, dtype=torch.int32)
+        self.scale = 1.0 / np.sqrt(D)
+
+    def gpu(self, norm_correction, num_splits=0):
+        from quantized_paged_kv_int4_gb300 import kvq
+        out = kvq.kvq_decode_tq_mse(self.q.cuda(), self.Pi.cuda(), self.cb.cuda(), self.cache.cuda(), self.kb,
+                                    self.kps, self.vb, self.bt.cuda(), self.lens.cuda(), self.scale,
+                                    norm_correction=norm_correction, num_splits=num_splits)
+        st, flags = kvq.kvq_device_error()
+        assert st == 0 and flags == 0, (st, flags)
+        return out.cpu().numpy()
+
+    def oracle(self, norm_correction, batch_index=None):
+        return turboquant.decode_tq_mse(self.q.numpy(), self.cache.numpy(), self.kb, self.kps, self.vb,
+                                        self.cb.numpy(), norm_correction, self.Pi.numpy(), self.bt.numpy(),
+                                        np.asarray(self.case.seq_lens), self.scale, batch_index=batch_index)

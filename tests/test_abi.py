@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings_and_version():
-    assert kvq.kvq_abi_version() == 3
+    assert kvq.kvq_abi_version() == 4
     for code in range(6):
         assert kvq.kvq_status_string(code).startswith("KVQ_")
     assert "UNKNOWN" in kvq.kvq_status_string(77)
@@ -104,6 +104,8 @@ def test_decode_mods_validation_without_gpu():
     assert _decode_mods(M(0, 0.0, 18, None)) == kvq.KVQ_ERR_INVALID_ARG          # misaligned sinks
     assert _decode_mods(M(0, 0.0, None, 18)) == kvq.KVQ_ERR_INVALID_ARG          # misaligned slopes
     assert _decode_mods(M(8, 30.0, 16, 16), wsb=10) == kvq.KVQ_ERR_WORKSPACE      # then the usual checks
+    assert _decode_mods(M(0, 0.0, None, None, 1, 18)) == kvq.KVQ_ERR_INVALID_ARG  # misaligned lse_out
+    assert _decode_mods(M(0, 0.0, None, None, 1, 16), B=0) == kvq.KVQ_OK
 
 
 def test_workspace_sizes_fixed_splits():
@@ -135,6 +137,13 @@ def test_tq_and_fwht_validation_without_gpu():
     bad = list(args)
     bad[12] = 0
     assert L.kvq_decode_tq(*bad) == kvq.KVQ_OK                    # B = 0
+    lse = list(args[:12]) + [18] + list(args[12:])
+    assert L.kvq_decode_tq_lse(*lse) == kvq.KVQ_ERR_INVALID_ARG   # misaligned lse_out
+    lse[3] = 5
+    assert L.kvq_decode_tq_lse(*lse) == kvq.KVQ_ERR_UNSUPPORTED   # the usual checks come first (value bits)
+    lse = list(args[:12]) + [None] + list(args[12:])
+    lse[13] = 0
+    assert L.kvq_decode_tq_lse(*lse) == kvq.KVQ_OK                # B = 0
     assert L.kvq_fwht128(16, 16, 16, 0, None) == kvq.KVQ_OK
     assert L.kvq_fwht128(18, 16, 16, 5, None) == kvq.KVQ_ERR_INVALID_ARG
     assert L.kvq_fwht128(16, 16, 16, -1, None) == kvq.KVQ_ERR_INVALID_ARG
@@ -208,3 +217,9 @@ def test_kpool_tail_validation_without_gpu():
                                   "kvq_fwht128"])
 def test_python_binding_names_match_the_c_api(name):
     assert callable(getattr(kvq, name))
+
+
+def test_debug_wait_setting_without_gpu():
+    L = kvq.lib()
+    assert L.kvq_debug_set_wait(0, -2) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_debug_set_wait(0, -1) == kvq.KVQ_OK      # the defaults

@@ -167,3 +167,32 @@ def test_garbage_in_unwritten_rows_is_ignored(num_splits):
     got = run_int4(kvq, c.to_gpu(), c.scale, num_splits=num_splits).cpu().numpy()
     assert np.all(np.isfinite(got))
     assert_close(got, ref, what="garbage S=%d" % num_splits)
+
+
+def test_prepared_writer_and_decoder_match_the_oracle():
+    """Int4Writer / Int4Decoder (buffers checked once, per-step tensors per call) write the same
+    bytes and decode the same rows as the oracle; wrong per-call shapes are rejected before launch."""
+    case = workloads.DecodeCase("prep", 4, 32, 8, 128, [100, 1, 2049, 700], seed=71, outlier_channels=4)
+    c = Int4Case(case)
+    g = c.to_gpu()
+    dec = kvq.Int4Decoder(g["kc"], g["vc"], g["ks"], g["vs"], g["bt"], g["lens"], g["signs"], c.scale, case.Hq)
+    out = torch.empty((4, 32, 128), dtype=torch.float32, device="cuda")
+    for _ in range(2):
+        dec(g["q"], out)
+        assert kvq.kvq_device_error() == (0, 0)
+        assert_close(out.cpu().numpy(), c.oracle(), what="prepared decoder")
+    with pytest.raises(ValueError):
+        dec(g["q"][:2], out)
+    with pytest.raises(ValueError):
+        dec(g["q"], out[:, :16])
+    k, v, slots, nb = workloads.write_case(T=300, Hk=8, D=128, seed=3)
+    kc = torch.zeros((nb, 16, 8, 64), dtype=torch.uint8, device="cuda")
+    caches = [kc, torch.zeros_like(kc), torch.zeros((nb, 16, 8), device="cuda"), torch.zeros((nb, 16, 8), device="cuda")]
+    ref = [t.clone() for t in caches]
+    signs = workloads.rht_signs(128).cuda()
+    kvq.Int4Writer(*caches, signs)(k.cuda(), v.cuda(), slots.cuda())
+    kvq.kvq_write_int4(k.cuda(), v.cuda(), *ref, slots.cuda(), signs)
+    for a, b in zip(caches, ref):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    with pytest.raises(ValueError):
+        kvq.Int4Writer(*caches, signs)(k.cuda()[:, :4], v.cuda()[:, :4], slots.cuda())

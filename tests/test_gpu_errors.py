@@ -65,3 +65,24 @@ def test_invalid_arguments_raise():
         kvq.kvq_decode_int4(g["q"], g["kc"], g["vc"], g["ks"], g["vs"], g["bt"], g["lens"], g["signs"], c.scale,
                             workspace=torch.empty((16,), dtype=torch.uint8, device="cuda"))
     assert e.value.status == kvq.KVQ_ERR_WORKSPACE
+
+
+def test_a_wait_that_runs_out_is_reported_and_the_gpu_stays_usable():
+    """The bounded-wait path: the next call withholds one ring stage's page copies in its first CTA
+    (kvq_debug_set_wait), so that CTA's waits on it run out after 5 ms; the call still returns,
+    flag 8 is raised, and the following call on the same context is exact again."""
+    lens = [1200, 700, 2000]
+    case = workloads.DecodeCase("timeout", len(lens), 32, 8, 128, lens, seed=61, outlier_channels=4)
+    c = Int4Case(case)
+    g = c.to_gpu()
+    try:
+        kvq.kvq_debug_set_wait(5_000_000, 2)  # the first CTA (sequence 0, split 0) has 38 pages = 38 stages
+        kvq.kvq_decode_int4(g["q"], g["kc"], g["vc"], g["ks"], g["vs"], g["bt"], g["lens"], g["signs"], c.scale,
+                            num_splits=2)
+        st, flags = kvq.kvq_device_error()
+        assert st == kvq.KVQ_ERR_OUT_OF_RANGE and flags == 8, (st, flags)
+    finally:
+        kvq.kvq_debug_set_wait(0, -1)
+    from helpers import assert_close
+    for S in (2, 0):
+        assert_close(run_int4(kvq, g, c.scale, num_splits=S).cpu().numpy(), c.oracle(), what="after the timeout")

@@ -65,6 +65,36 @@ def test_full_size_16384_pools():
     assert np.array_equal(got, ref)
 
 
+def _code_order(c):
+    """E4M3FN codes as signed integers ordered like their values (adjacent values differ by 1)."""
+    c = np.asarray(c, np.int64)
+    return np.where(c & 0x80, -(c & 0x7F), c & 0x7F)
+
+
+def test_codes_are_within_one_step_of_a_correctly_rounded_exp():
+    """The bit-exact checks above use the oracle's written-out fp32 exponential, the same operation
+    sequence as the kernel's (the page does not show tl.exp). Against an independent fp32 exp --
+    the float64 exponential rounded once (oracle/kpool.py, exp_f32_rounded) -- the kernel's codes
+    may differ only where a pooled value sits on a bf16 rounding boundary: each such code by one
+    E4M3 step, in at most 1e-4 of all codes, with the same power-of-two scale on every row."""
+    n, pool, ps = 16384, 4, 64
+    slot_k, score, ape, loc, nb = workloads.kpool_case(n, pool, ps, seed=0)
+    g = torch.zeros((nb, ps, 132), dtype=torch.uint8, device="cuda")
+    kvq.kvq_kpool_write(g, slot_k.cuda(), score.cuda(), ape.cuda(), loc.cuda())
+    assert kvq.kvq_device_error() == (0, 0)
+    got = g.cpu().numpy().reshape(nb, ps * 132)
+    x = kpool.pool_keys(slot_k.float().numpy(), score.numpy(), ape.numpy(), exp=kpool.exp_f32_rounded)
+    codes, scales = kpool.quantize_rows(x)
+    page, row = np.divmod(loc.numpy(), ps)
+    gpu_codes = np.stack([got[p, r * 128:(r + 1) * 128] for p, r in zip(page, row)])
+    gpu_scales = np.array([got[p, ps * 128 + 4 * r:ps * 128 + 4 * r + 4].view(np.float32)[0]
+                           for p, r in zip(page, row)])
+    assert np.array_equal(gpu_scales, scales)
+    step = np.abs(_code_order(gpu_codes) - _code_order(codes))
+    assert step.max() <= 1
+    assert (step > 0).mean() <= 1e-4, (step > 0).sum()
+
+
 # ---- tail ring ----------------------------------------------------------------------------------
 
 def _bf16_np(t):

@@ -3,10 +3,12 @@
 Such callers (for example a plug-in inside a serving process whose allocator already owns all of
 HBM, or a C caller without the host framework's allocator) get the library's own device scratch
 array instead of passing a workspace. These tests call that entry point through the C ABI and
-check it against the workspace entry point, on two calls in a row (the second call finds the
-first call's leftovers in the shared array). The file is named to be collected last, so a run
-that stops at the first failure has already run every other test; it also passes on its own in a
-fresh process, where its first call is the one that looks up the array's device address.
+check it against the float64 oracle and against the workspace entry point, on two calls in a row
+(the second call finds the first call's leftovers in the shared array). The large balanced-split
+case runs first, so the tiny fixed-split case that follows also starts on another layout's
+leftovers. The file is named to be collected last, so a run that stops at the first failure has
+already run every other test; it also passes on its own in a fresh process, where its first call
+is the one that looks up the array's device address.
 """
 
 import ctypes
@@ -35,23 +37,44 @@ def _noalloc(g, scale, out, num_splits, dims):
         kvq.KVQ_F32, B, Hq, Hk, D, 16, nb, stream)
 
 
-@pytest.mark.parametrize("case,num_splits", [
-    (workloads.tiny_int4(), 4),
+CASES = [  # the large balanced-split case first, then the tiny fixed-split one on its leftovers
     (workloads.DecodeCase("noalloc", 6, 32, 8, 128, [1024, 1500, 2049, 0, 3000, 1], seed=5,
                           outlier_channels=4), 0),
-])
-def test_noalloc_matches_the_workspace_entry_point_twice(case, num_splits):
-    c = Int4Case(case)
+    (workloads.tiny_int4(), 4),
+]
+
+
+def test_noalloc_matches_the_oracle_twice_per_case():
+    for case, num_splits in CASES:
+        c = Int4Case(case)
+        g = c.to_gpu()
+        ref = c.oracle()
+        ws = kvq.kvq_decode_int4(g["q"], g["kc"], g["vc"], g["ks"], g["vs"], g["bt"], g["lens"], g["signs"],
+                                 c.scale, num_splits=num_splits).cpu().numpy()
+        dims = (case.B, case.Hq, case.Hk, case.D, c.nb)
+        for _ in range(2):
+            out = torch.full((case.B, case.Hq, case.D), float("nan"), dtype=torch.float32, device="cuda")
+            assert _noalloc(g, c.scale, out, num_splits, dims) == kvq.KVQ_OK
+            torch.cuda.synchronize()
+            got = out.cpu().numpy()
+            assert_close(got, ref, what="noalloc vs oracle S=%d" % num_splits)
+            assert_close(got, ws, what="noalloc vs workspace entry point S=%d" % num_splits)
+        assert kvq.kvq_device_error() == (0, 0)
+
+
+def test_noalloc_python_wrapper_and_its_checks():
+    c = Int4Case(workloads.tiny_int4())
     g = c.to_gpu()
-    ref = kvq.kvq_decode_int4(g["q"], g["kc"], g["vc"], g["ks"], g["vs"], g["bt"], g["lens"], g["signs"],
-                              c.scale, num_splits=num_splits).cpu().numpy()
-    dims = (case.B, case.Hq, case.Hk, case.D, c.nb)
-    for _ in range(2):
-        out = torch.full((case.B, case.Hq, case.D), float("nan"), dtype=torch.float32, device="cuda")
-        assert _noalloc(g, c.scale, out, num_splits, dims) == kvq.KVQ_OK
-        torch.cuda.synchronize()
-        assert_close(out.cpu().numpy(), ref, what="noalloc S=%d" % num_splits)
-    assert kvq.kvq_device_error() == (0, 0)
+    out = torch.empty((c.case.B, c.case.Hq, c.case.D), dtype=torch.float32, device="cuda")
+    kvq.kvq_decode_int4_noalloc(g["q"], g["kc"], g["vc"], g["ks"], g["vs"], g["bt"], g["lens"], g["signs"],
+                                c.scale, out, num_splits=4)
+    assert_close(out.cpu().numpy(), c.oracle(), what="noalloc wrapper")
+    with pytest.raises(ValueError):  # an output smaller than q is rejected before any launch
+        kvq.kvq_decode_int4_noalloc(g["q"], g["kc"], g["vc"], g["ks"], g["vs"], g["bt"], g["lens"], g["signs"],
+                                    c.scale, out[:1])
+    with pytest.raises(TypeError):
+        kvq.kvq_decode_int4_noalloc(g["q"], g["kc"], g["vc"], g["ks"], g["vs"], g["bt"], g["lens"], g["signs"],
+                                    c.scale, out.to(torch.int32))
 
 
 def test_noalloc_rejects_a_scratch_need_above_the_array():
