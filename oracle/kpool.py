@@ -54,15 +54,24 @@ def exp_f32(x):
     return np.where(n <= F32(-126.0), F32(0.0), out).astype(F32)
 
 
-def pool_keys(slot_k, slot_score, ape):
-    """Steps 1-3 without the mask: [n_pools, 128] fp32 holding bf16 values."""
+def exp_f32_rounded(x):
+    """exp(x) rounded once to fp32 from the float64 exponential (within half an fp32 ulp but for
+    rare double-rounding ties): an fp32 exponential independent of exp_f32's operation sequence,
+    the checker for the choice of exp (the page does not show tl.exp's)."""
+    with np.errstate(under="ignore"):
+        return np.exp(np.asarray(x, dtype=F32).astype(np.float64)).astype(F32)
+
+
+def pool_keys(slot_k, slot_score, ape, exp=exp_f32):
+    """Steps 1-3 without the mask: [n_pools, 128] fp32 holding bf16 values (exp: the fp32
+    exponential used for w_s)."""
     k = np.asarray(slot_k, dtype=F32)
     z = (np.asarray(slot_score, dtype=F32) + np.asarray(ape, dtype=F32)[None]).astype(F32)
     M = z.max(axis=1)
     den = np.zeros_like(M)
     acc = np.zeros_like(M)
     for s in range(k.shape[1]):  # slot order, as the page's static loop
-        w = exp_f32((z[:, s] - M).astype(F32))
+        w = exp((z[:, s] - M).astype(F32))
         den = (den + w).astype(F32)
         acc = (acc + (k[:, s] * w).astype(F32)).astype(F32)
     return bf16_round((acc / den).astype(F32))
@@ -78,11 +87,12 @@ def quantize_rows(x, round_scale=True):
     return f32_to_e4m3fn(q), s.astype(F32)
 
 
-def kpool_compress_write(kv_cache, slot_k, slot_score, ape, loc, write_mask=None, round_scale=True):
+def kpool_compress_write(kv_cache, slot_k, slot_score, ape, loc, write_mask=None, round_scale=True,
+                         exp=exp_f32):
     """kv_cache: uint8 [num_blocks, page_size, 128 + 4] written in place; returns (codes, scales)
     of every pool (masked pools quantize a zero vector and are not written)."""
     n = np.asarray(slot_k).shape[0]
-    x = pool_keys(slot_k, slot_score, ape)
+    x = pool_keys(slot_k, slot_score, ape, exp=exp)
     if write_mask is not None:
         x = np.where(np.asarray(write_mask, bool)[:, None], x, F32(0.0)).astype(F32)
     codes, scales = quantize_rows(x, round_scale)
