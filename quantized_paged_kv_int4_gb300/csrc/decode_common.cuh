@@ -326,7 +326,7 @@ __device__ __forceinline__ void for_each_piece(const SplitArgs &a, unsigned *fla
 // Writes one warp's partial: thread (g, t) holds, for heads 2t and 2t + 1, the D/8 consecutive
 // dims [g * D/8, (g+1) * D/8) in o0 / o1; lse in base 2.
 // MULTI: a.Q may exceed 1 (multi-token decode); otherwise column n is head h * G + n.
-template <int D, bool MULTI = false>
+template <int D, bool MULTI = false, bool STRIDED = false>
 __device__ __forceinline__ void store_partial(const SplitArgs &a, long long slot, int sub, int h,
                                               int lane, const float (&o0)[D / 8],
                                               const float (&o1)[D / 8], float lse0, float lse1) {
@@ -340,16 +340,20 @@ __device__ __forceinline__ void store_partial(const SplitArgs &a, long long slot
   };
   if (n0 < ncol) {
     const long long r0 = row_of(n0);
-    float4 *dst = reinterpret_cast<float4 *>(a.part_o + r0 * D + g * (D / 8));
+    float *base = a.part_o + r0 * D;
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) dst[i] = make_float4(o0[4 * i], o0[4 * i + 1], o0[4 * i + 2], o0[4 * i + 3]);
+    for (int i = 0; i < D / 32; ++i)  // STRIDED: float4 i holds dims 32 i + 4 g ..; else dims g D/8 + 4 i ..
+      *reinterpret_cast<float4 *>(base + (STRIDED ? 32 * i + 4 * g : g * (D / 8) + 4 * i)) =
+          make_float4(o0[4 * i], o0[4 * i + 1], o0[4 * i + 2], o0[4 * i + 3]);
     if (g == 0) a.part_lse[r0] = lse0;
   }
   if (n1 < ncol) {
     const long long r1 = row_of(n1);
-    float4 *dst = reinterpret_cast<float4 *>(a.part_o + r1 * D + g * (D / 8));
+    float *base = a.part_o + r1 * D;
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) dst[i] = make_float4(o1[4 * i], o1[4 * i + 1], o1[4 * i + 2], o1[4 * i + 3]);
+    for (int i = 0; i < D / 32; ++i)  // STRIDED: float4 i holds dims 32 i + 4 g ..; else dims g D/8 + 4 i ..
+      *reinterpret_cast<float4 *>(base + (STRIDED ? 32 * i + 4 * g : g * (D / 8) + 4 * i)) =
+          make_float4(o1[4 * i], o1[4 * i + 1], o1[4 * i + 2], o1[4 * i + 3]);
     if (g == 0) a.part_lse[r1] = lse1;
   }
 }

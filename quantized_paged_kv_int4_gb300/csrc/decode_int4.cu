@@ -16,10 +16,10 @@
 // four TMA copies per page: one 4-D box of the K pool (HB heads x 16 tokens x D/2 bytes, stored
 // [head][token][row] with the 64B/32B swizzle that keeps the fragment reads conflict-free), the
 // same for V, and the page's two blocks of scale words. Warp w reads tile w of every stage
-// (head w % HB of page w / HB) and, when done with it, arrives on the stage's empty barrier;
-// warp 0, a consumer like the others, also refills each stage once that barrier completes
-// (polled between its pages, so there is no dedicated producer warp and no block-wide barrier
-// after setup). Waits on the stage barriers are bounded and report a flag. Both contractions run on the tensor cores (mma.m16n8k16, fp16 operands,
+// (head w % HB of page w / HB); the last of the 8 warps to finish with a stage refills its slot
+// at once (a shared counter), so no warp waits for another to notice a free slot and there is
+// no producer warp and no block-wide barrier after setup. Waits on the stage barriers are
+// bounded and report a flag. Both contractions run on the tensor cores (mma.m16n8k16, fp16 operands,
 // fp32 accumulation) on exact operands: a nibble pair masked into an fp16 pair with a zero
 // exponent field IS the pair of fp16 subnormals n * 2^-24 (low nibble) or n * 2^-20 (high
 // nibble), so one LOP3 turns 2 nibbles into MMA operands; the power of two goes into the
@@ -384,6 +384,7 @@ __device__ __forceinline__ uint32_t ld_s32(uint32_t o) { return *reinterpret_cas
 template <int D>
 struct LaneOffsets {
   uint32_t k, v, s;
+  uint32_t vm[D / 64];  // shared address (minus the stage offset) of this lane's ldmatrix row, per load
 };
 
 template <int D, int W>
@@ -396,6 +397,12 @@ __device__ __forceinline__ LaneOffsets<D> lane_offsets(int warp, int sub, int hl
   o.k = warp * Gm::TILE + swz<Gm::RB>(g, Gm::WPR * 4 * t);
   o.v = Gm::VOFF + warp * Gm::TILE + swz<Gm::RB>(2 * t, (Gm::VCH) * g);
   o.s = Gm::SOFF + sub * SCP + (g * HB + hl) * 4;
+  // ldmatrix.x4.trans load i: lanes 8m .. 8m + 7 address the 8 token rows of matrix m = (token
+  // half m & 1, 16-byte chunk 2i + (m >> 1)) of the warp's V tile
+  const int mi = lane >> 3, tok = (lane & 7) + 8 * (mi & 1);
+#pragma unroll
+  for (int i = 0; i < D / 64; ++i)
+    o.vm[i] = smem_u32(kvq_dsmem) + Gm::VOFF + warp * Gm::TILE + swz<Gm::RB>(tok, 16 * (2 * i + (mi >> 1)));
   return o;
 }
 
@@ -450,27 +457,18 @@ __device__ __forceinline__ void page_pv(float (&acc)[D / 16][4], uint32_t so, co
   const uint32_t z0 = __shfl_sync(FULL, x0, src1), z1 = __shfl_sync(FULL, x1, src1);
   const uint32_t ya = (g & 1) ? y1 : y0, za = (g & 1) ? z1 : z0;
   const uint32_t b01 = __byte_perm(ya, za, 0x5410), b23 = __byte_perm(ya, za, 0x7632);
-  constexpr int VW = Gm::VCH / 4;  // V words per token per lane (2 or 1)
-  const uint32_t vo = so + lo.v;
-  uint32_t va[VW], vb[VW], vc[VW], vd[VW];
-  if constexpr (VW == 2) {
-    const uint2 A = ld_s64(vo), B2 = ld_s64(vo + Gm::RB);
-    const uint2 C = ld_s64(vo + 8 * Gm::RB), E = ld_s64(vo + 9 * Gm::RB);
-    va[0] = A.x; va[1] = A.y; vb[0] = B2.x; vb[1] = B2.y;
-    vc[0] = C.x; vc[1] = C.y; vd[0] = E.x; vd[1] = E.y;
-  } else {
-    va[0] = ld_s32(vo);
-    vb[0] = ld_s32(vo + Gm::RB);
-    vc[0] = ld_s32(vo + 8 * Gm::RB);
-    vd[0] = ld_s32(vo + 9 * Gm::RB);
-  }
+  // V^T fragments: ldmatrix.trans gives this lane word 8q + g of tokens (2t, 2t+1) [x] and
+  // (2t+8, 2t+9) [y]; its low / high nibbles of byte 0 (then byte 1) are A rows g / g + 8
 #pragma unroll
-  for (int wi = 0; wi < VW; ++wi) {
+  for (int i = 0; i < D / 64; ++i) {
+    uint32_t r[4];
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(lo.vm[i] + so));
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const uint32_t sel = hf ? 0x7632u : 0x5410u;
-      const uint32_t x = __byte_perm(va[wi], vb[wi], sel), y = __byte_perm(vc[wi], vd[wi], sel);
-      const int mt = 4 * wi + 2 * hf;
+    for (int e = 0; e < 2; ++e) {
+      const uint32_t x = r[2 * e], y = r[2 * e + 1];
+      const int mt = 2 * (2 * i + e);
       mma_f16_16816(acc[mt], x & kLo, x & kHi, y & kLo, y & kHi, b01, b23);
       const uint32_t x8 = x >> 8, y8 = y >> 8;
       mma_f16_16816(acc[mt + 1], x8 & kLo, x8 & kHi, y8 & kLo, y8 & kHi, b01, b23);
@@ -649,16 +647,17 @@ __device__ __forceinline__ void int4_finish(const SplitArgs &a, PieceState<D> &s
   }
   const float lse0 = l0 > 0.f ? st.m0 + log2f(l0) : -INFINITY;
   const float lse1 = l1 > 0.f ? st.m1 + log2f(l1) : -INFINITY;
-  store_partial<D, MTOK>(a, slot, sub, h, lane, o0, o1, lse0, lse1);
+  store_partial<D, MTOK, true>(a, slot, sub, h, lane, o0, o1, lse0, lse1);
 }
 
 // W = warps per kv head (8 / heads per CTA). Stage k of the ring (slot k % NS) holds run pages
 // k * W .. k * W + W - 1 for the CTA's HB = 8 / W heads; warp w reads tile w of it.
 // Ring protocol: s_full[slot] completes when a stage's copies have landed (one arrival: the
-// expect_tx of the issuing lane 0, plus the copies' bytes); s_empty[slot] completes when all 256
-// threads have finished reading it (every thread arrives once). Warp 0 is also the producer: it
-// issued the first NS stages and refills a slot once its s_empty phase completes -- polling
-// without blocking between pages, and blocking only for a stage it needs itself.
+// expect_tx of the issuing lane 0, plus the copies' bytes). Every warp done with a stage adds 1 to
+// s_done[slot] (acquire-release); the warp whose addition completes a multiple of 8 is the last
+// reader and issues stage k + NS into the slot. Warp 0 issues the first stages and keeps the
+// CTA's block ids in a shared ring two batches of 32 pages ahead of its own position (a refill
+// is at most NS * W <= 32 pages ahead of the slowest warp).
 // VAR 0: plain; 1: score modifiers (window, soft cap, ALiBi; multi-token decode allowed);
 // 2: multi-token decode only.
 template <int D, int NS, int W, int VAR>
@@ -667,8 +666,10 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   using Gm = Int4Geom<D>;
   constexpr int HB = 8 / W;
   constexpr int SCP = 64 * HB < 128 ? 128 : 64 * HB;  // one page's scale block, 128-byte aligned slots
-  static_assert(NS >= 2 && NS * W <= 64, "refills read at most two batches of block ids ahead");
-  __shared__ __align__(8) uint64_t s_full[NS], s_empty[NS];
+  static_assert(NS >= 2 && NS * W <= 32, "refills read at most two batches of block ids ahead");
+  __shared__ __align__(8) uint64_t s_full[NS];
+  __shared__ unsigned s_done[NS];   // warps done with each slot, counted up forever (mod 8 = this round)
+  __shared__ int s_bids[128];       // block ids of run pages: batch c (32 pages) at (c % 4) * 32
   asm volatile("griddepcontrol.launch_dependents;");  // let the merge kernel's launch begin early
   // stages start at the first 1024-byte aligned offset of the dynamic buffer (swizzled TMA tiles)
   const uint32_t dbase = smem_u32(kvq_dsmem);
@@ -685,11 +686,10 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&s_full[i]), 1);
-      mbar_init(smem_u32(&s_empty[i]), 256);
+      s_done[i] = 0;
     }
     mbar_init_fence();
   }
-  __syncthreads();
 
   // ---- producer state (warp 0): block ids, 32 run pages per batch, lane l of a batch register
   // holding run page 32 * batch + l; each lane walks its own sequence cursor (monotone).
@@ -703,13 +703,17 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     const long long row = a.vseq != nullptr ? a.vseq[lc.b].x : lc.b;  // a virtual sequence: its sequence's row
     return __ldg(p.block_table + row * a.max_blocks + (X - lc.P + lc.f));
   };
+  auto store_batch = [&](int c) {  // warp 0: block ids of batch c into the shared ring
+    if (c * 32 < run.n) s_bids[(c & 3) * 32 + lane] = load_batch(c);
+  };
   // Stage k into ring slot `slot`: lane i copies page k * W + i (expect_tx first, by lane 0).
-  auto issue = [&](int k, int slot, int bid) {  // warp-wide
+  auto issue = [&](int k, int slot) {  // warp-wide
     if (k == p.withhold && blockIdx.x == 0 && blockIdx.y == 0) return;  // its full barrier never completes
     const int x0 = k * W, npg = min(W, run.n - x0);
     const uint32_t bar = smem_u32(&s_full[slot]);
     const uint32_t stg = dbase + base + slot * Gm::STAGE;
-    const int raw = __shfl_sync(FULL, bid, (x0 + lane) & 31);
+    const int xi = x0 + (lane < npg ? lane : 0);
+    const int raw = s_bids[((xi >> 5) & 3) * 32 + (xi & 31)];
     if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(npg * (2 * HB * Gm::TILE + 2 * 64 * HB)));
     __syncwarp();
     if (lane < npg) {
@@ -742,41 +746,26 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
       q_prefetched = c0.b;
     }
   }
-  int nxt = 0, nslot = 0, nrnd = 0;  // next stage to issue, its slot and round (warp 0)
-  int cb = 0, bid_cur = 0, bid_next = 0;
+  int cb = 0;        // warp 0: the batch of block ids its consumption has reached
+  bool rest = false;  // warp 0: stages 2 .. NS - 1 issued
   if (warp == 0) {
-    bid_cur = load_batch(0);
-    bid_next = load_batch(1);
+    store_batch(0);
+    store_batch(1);
+    __syncwarp();
     // Only the first two stages now: at launch every CTA requests its first stages at once and
     // DRAM serves them interleaved, so a shorter first request lands sooner; the other slots
-    // are filled as soon as this warp has its first stage (produce after the first wait).
-    for (; nxt < 2 && nxt < n_stages; ++nxt) issue(nxt, nxt, bid_cur);
-    nslot = nxt;
-    nrnd = 0;
+    // are filled once this warp has its first stage.
+    for (int k = 0; k < 2 && k < n_stages; ++k) issue(k, k);
   }
-  // Warp 0: issue the stages whose slot is free, in order; wait (bounded) for a slot only while
-  // the next stage is one this warp needs (<= need). False on a timeout.
-  auto produce = [&](int need) -> bool {
-    while (nxt < n_stages) {
-      const uint32_t eb = smem_u32(&s_empty[nslot]), par = static_cast<uint32_t>(nrnd - 1) & 1u;
-      if (nxt <= need) {
-        if (!__all_sync(FULL, mbar_wait(eb, par, p.wait_ns))) return false;
-      } else if (!__all_sync(FULL, mbar_test_wait(eb, par))) {
-        break;
-      }
-      if (((nxt * W) >> 5) > cb) {  // next batch of block ids (loaded a batch ahead)
-        ++cb;
-        bid_cur = bid_next;
-        bid_next = load_batch(cb + 1);
-      }
-      issue(nxt, nslot, bid_cur);
-      ++nxt;
-      if (++nslot == NS) {
-        nslot = 0;
-        ++nrnd;
-      }
-    }
-    return true;
+  __syncthreads();  // barrier init and the first block ids, before any other warp can refill
+  // A slot is refilled by the last warp done with it (the shared counter's old value is 7 mod 8):
+  // no warp waits for another to notice the slot is free.
+  auto release = [&](int k, int slot) {
+    __syncwarp();
+    unsigned old = 0;
+    if (lane == 0) old = atom_add_acq_rel_cta(&s_done[slot], 1u);
+    old = __shfl_sync(FULL, old, 0);
+    if ((old & 7u) == 7u && k + NS < n_stages) issue(k + NS, slot);
   };
 
   // ---- consumer side: warp w takes run page k * W + sub of every stage k
@@ -884,21 +873,23 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     // two full pages of the piece inside every column's key range (one query token: the piece)
     const int tpair = MTOK ? min(t1, limf) : t1;
     const bool pair = nb >= (MTOK ? max(t0, lwl) : t0) && nb + (W + 1) * kPage <= tpair && x + W < pe_x;
-    if (warp == 0 && nxt <= (pair ? j + 1 : j) && !produce(pair ? j + 1 : j)) {
-      abort = true;
-      if (lane == 0) atomicOr(&g_flags_decode_int4, ERR_TIMEOUT);
-      break;
+    if (warp == 0 && ((j * W) >> 5) >= cb) {  // entering a new batch of block ids: load the one two ahead
+      cb = ((j * W) >> 5) + 1;
+      store_batch(cb + 1);
     }
     if (pair) {
       if (!wait_stage(j, sj, rj) || !wait_stage(j + 1, sj1, rj1)) {
         abort = true;
         break;
       }
-      if (warp == 0) produce(-1);  // the slots freed meanwhile (at the start: the unused ones)
+      if (warp == 0 && !rest) {  // the slots never used yet
+        rest = true;
+        for (int k = 2; k < NS && k < n_stages; ++k) issue(k, k);
+      }
       int4_pages<D, W, 2, false, MODS, MTOK>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, lim0, lim1, lw0,
                                              lw1, p, md);
-      mbar_arrive(smem_u32(&s_empty[sj]));
-      mbar_arrive(smem_u32(&s_empty[sj1]));
+      release(j, sj);
+      release(j + 1, sj1);
       j += 2;
       sj = sj1 + 1 == NS ? 0 : sj1 + 1;
       rj = sj1 + 1 == NS ? rj1 + 1 : rj1;
@@ -907,15 +898,17 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
         abort = true;
         break;
       }
-      if (warp == 0) produce(-1);  // the slots freed meanwhile (at the start: the unused ones)
+      if (warp == 0 && !rest) {
+        rest = true;
+        for (int k = 2; k < NS && k < n_stages; ++k) issue(k, k);
+      }
       int4_pages<D, W, 1, true, MODS, MTOK>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, lim0, lim1, lw0,
                                             lw1, p, md);
-      mbar_arrive(smem_u32(&s_empty[sj]));
+      release(j, sj);
       j += 1;
       sj = sj1;
       rj = rj1;
     }
-    if (warp == 0) produce(-1);  // refill what this warp just freed, if the others are done too
   }
   if (cur.b < a.B) finish_piece();
   if (!run.fixed && !abort) {

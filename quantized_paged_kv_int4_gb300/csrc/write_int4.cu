@@ -65,6 +65,60 @@ __device__ __forceinline__ uint32_t bf2_bits(float lo, float hi) {
   return w;
 }
 
+// Packed fp32 pairs (Blackwell f32x2 ALU): each component rounded exactly like the scalar op.
+__device__ __forceinline__ unsigned long long f2pack(float a, float b) {
+  return static_cast<unsigned long long>(__float_as_uint(a)) | (static_cast<unsigned long long>(__float_as_uint(b)) << 32);
+}
+__device__ __forceinline__ void f2unpack(unsigned long long v, float &a, float &b) {
+  a = __uint_as_float(static_cast<uint32_t>(v));
+  b = __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long sub2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// butterfly stages h = 1 .. N/2 over N consecutive elements: h = 1 scalar, h >= 2 on pairs (j, j + 1)
+template <int N>
+__device__ __forceinline__ void butterfly_local2(float (&x)[N]) {
+#pragma unroll
+  for (int j = 0; j < N; j += 2) {
+    const float a = x[j], b = x[j + 1];
+    x[j] = __fadd_rn(a, b);
+    x[j + 1] = __fsub_rn(a, b);
+  }
+#pragma unroll
+  for (int h = 2; h < N; h <<= 1) {
+#pragma unroll
+    for (int j = 0; j < N; j += 2) {
+      if (!(j & h)) {
+        const unsigned long long a = f2pack(x[j], x[j + 1]), b = f2pack(x[j + h], x[j + h + 1]);
+        f2unpack(add2(a, b), x[j], x[j + 1]);
+        f2unpack(sub2(a, b), x[j + h], x[j + h + 1]);
+      }
+    }
+  }
+}
+// the same stages over rows of two columns at once: element r of column c is x[c][r]
+__device__ __forceinline__ void butterfly_cols2(float (&x)[2][8]) {
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      if (!(r & h)) {
+        const unsigned long long a = f2pack(x[0][r], x[1][r]), b = f2pack(x[0][r + h], x[1][r + h]);
+        f2unpack(add2(a, b), x[0][r], x[1][r]);
+        f2unpack(sub2(a, b), x[0][r + h], x[1][r + h]);
+      }
+    }
+  }
+}
+
 template <int D>
 struct WriteGeom {
   static constexpr int E = D / 8;          // elements per lane (one row of the 8 x E vector view)
@@ -156,7 +210,7 @@ __global__ void __launch_bounds__(256, 4) write_int4_kernel(const WriteParams p,
         x[2 * i] = __uint_as_float(w << 16);
         x[2 * i + 1] = __uint_as_float(w & 0xffff0000u);
       }
-      butterfly_local<E>(x);  // h = 1 .. E/2 inside the lane's row
+      butterfly_local2<E>(x);  // h = 1 .. E/2 inside the lane's row
       // stages h = E, 2E, 4E pair rows r and r ^ 1, 2, 4: transpose, butterfly over rows, back
       __syncwarp();  // the previous tile's reads of buf are done
 #pragma unroll
@@ -174,8 +228,12 @@ __global__ void __launch_bounds__(256, 4) write_int4_kernel(const WriteParams p,
           c[0][r] = buf[r * Wg::ROW + l8];
         }
       }
+      if constexpr (CPL == 2) {
+        butterfly_cols2(c);
+      } else {
 #pragma unroll
-      for (int cc = 0; cc < CPL; ++cc) butterfly_local<8>(c[cc]);
+        for (int cc = 0; cc < CPL; ++cc) butterfly_local<8>(c[cc]);
+      }
       __syncwarp();
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
