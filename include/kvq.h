@@ -117,8 +117,9 @@ KVQ_API size_t kvq_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hk, int
  *   block_table  int32 [B, max_blocks]; entries at or past page ceil(seq_lens[b]/16) are not read.
  *   seq_lens     int32 [B]; values are clamped to [0, 16*max_blocks] (a clamp raises the flag).
  *   workspace    >= kvq_decode_workspace_bytes(B, Hq, Hk, D, num_splits) bytes, 16-byte aligned;
- *                holds the per-split partial results between the split kernel and the merge
- *                kernel (both enqueued by this call). Contents need no initialisation and are
+ *                holds the rotated query's MMA fragments (written by a pre-kernel) and the
+ *                per-split partial results between the split kernel and the merge kernel (all
+ *                three enqueued by this call). Contents need no initialisation and are
  *                clobbered. Calls that share a workspace must be ordered on one stream.
  *   out          [B, Hq, D] of out_dtype (KVQ_BF16 / KVQ_F16 / KVQ_F32), contiguous, written in full.
  *   Supported: D in {64, 128}; Hq % Hk == 0 with Hq / Hk <= 8; Hk in {1, 2, 4, 8} or a multiple of 8.

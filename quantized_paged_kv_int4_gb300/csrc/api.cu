@@ -139,7 +139,6 @@ bool int4_tensor_maps(const void *k_cache, const void *v_cache, const void *k_sc
   return true;
 }
 
-static size_t round256(size_t n) { return (n + 255) / 256 * 256; }
 
 size_t workspace_bytes(int B, int Hq, int D, const SplitPlan &plan) {
   const size_t rows = static_cast<size_t>(plan.slots) * plan.warps_per_head * Hq;
@@ -183,7 +182,7 @@ extern "C" size_t kvq_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hk, 
   if (B < 0 || Hq < 1 || Hk < 1 || Hq % Hk || (D != 64 && D != 128)) return 0;
   SplitPlan plan;
   if (!make_plan(B, Hk, num_splits, &plan)) return 0;
-  return workspace_bytes(B, Hq, D, plan);
+  return workspace_bytes(B, Hq, D, plan) + qfrag_bytes(B, Hk, D);  // the INT4 call's query fragments
 }
 
 extern "C" kvq_status kvq_device_error(kvq_stream_t stream, uint32_t *flags) {

@@ -29,8 +29,11 @@
 //     per-column softmax reference kept so that P_v stays inside fp16 for any value scale
 //     (decode_common.cuh); the tokens (the K dimension) and the D rows are permuted so that a
 //     lane's V bytes become A fragments with one PRMT per pair of m-tiles.
-// q enters as fp16 times a per-(piece, kv head) power of two 2^-k (so no element can overflow),
-// and 2^k joins the score scale.
+// q enters as fp16 times a per-(sequence, kv head) power of two 2^-k (so no element can overflow),
+// and 2^k joins the score scale. In single-token calls a pre-kernel rotates q and builds these
+// fragments once per (sequence, kv head); the split kernel, its programmatic dependent, sets up
+// its run and issues its first page copies meanwhile and then copies the fragments (2.4 KB) at
+// each piece start. Multi-token calls rotate in the split kernel.
 // The G query heads of a kv head share every K/V byte loaded (GQA), padded to the MMA's N = 8.
 
 #include <atomic>
@@ -53,6 +56,8 @@ struct Int4Params {
   float softcap2;       // USE_SOFTCAP: the cap in base-2 units (cap * log2 e), 0 = off
   float inv_softcap2;
   const float *alibi;   // USE_ALIBI_SLOPES: [Hq] slopes, or null
+  uint32_t *qfrag;      // single-token calls: the query fragments of rotate_q_int4_kernel
+                        // [B][Hk][QWORDS][32 lanes]; null in multi-token calls
   unsigned long long wait_ns;  // limit of every bounded wait on a stage barrier
   int32_t withhold;     // error-path tests only: CTA (0, 0) never issues stage `withhold` (-1: none)
 };
@@ -74,7 +79,8 @@ struct Int4Geom {
   static constexpr int WPR = D / 32;      // K words per lane per row
   static constexpr int KSTEPS = D / 16;
   static constexpr int MT = D / 16;       // m-tiles of the PV product
-  static constexpr int QBYTES = 8 * D * 2 + 64;
+  static constexpr int QWORDS = 2 * (D / 16) + 3;   // query words per lane: qf, qs0, qs1, qmul
+  static constexpr int QBYTES = (8 * D * 2 + 64) > QWORDS * 128 ? (8 * D * 2 + 64) : QWORDS * 128;
 };
 
 // One sequence of the walk over a CTA's run: index b, global index of its first read page
@@ -361,6 +367,70 @@ __device__ __forceinline__ void load_query(const Int4Params &p, uint8_t *qarea, 
   qs0 = qsum[2 * t];
   qs1 = qsum[2 * t + 1];
   __syncwarp();
+}
+
+// The query fragments of (sequence b, kv head h) written by rotate_q_int4_kernel: QWORDS words per
+// lane, word w of lane l at ((b Hk + h) QWORDS + w) 32 + l -- copied into the warp's query area
+// (16-byte cp.async), then read by each lane.
+template <int D>
+__device__ __forceinline__ void fetch_frag(const Int4Params &p, uint8_t *qarea, int b, int h, int lane) {
+  using Gm = Int4Geom<D>;
+  const uint8_t *src = reinterpret_cast<const uint8_t *>(
+      p.qfrag + (static_cast<long long>(b) * p.s.Hk + h) * Gm::QWORDS * 32);
+  const uint32_t dst = smem_u32(qarea);
+  for (int c = lane; c < Gm::QWORDS * 8; c += 32) cp_async<16>(dst + 16 * c, src + 16 * c, true);
+  cp_async_commit();
+}
+template <int D>
+__device__ __forceinline__ void load_frag(const Int4Params &p, uint8_t *qarea, int b, int h, int lane,
+                                          uint32_t (&qf)[D / 16][2], float &qs0, float &qs1, float &qmul,
+                                          bool fetched) {
+  using Gm = Int4Geom<D>;
+  __syncwarp();
+  if (!fetched) {
+    cp_async_wait<0>();
+    fetch_frag<D>(p, qarea, b, h, lane);
+  }
+  cp_async_wait<0>();
+  __syncwarp();
+  const uint32_t *w = reinterpret_cast<const uint32_t *>(qarea);
+#pragma unroll
+  for (int k = 0; k < D / 16; ++k) {
+    qf[k][0] = w[(2 * k) * 32 + lane];
+    qf[k][1] = w[(2 * k + 1) * 32 + lane];
+  }
+  qs0 = __uint_as_float(w[(Gm::QWORDS - 3) * 32 + lane]);
+  qs1 = __uint_as_float(w[(Gm::QWORDS - 2) * 32 + lane]);
+  qmul = __uint_as_float(w[(Gm::QWORDS - 1) * 32 + lane]);
+  __syncwarp();
+}
+
+// Single-token decode: one warp per (sequence, kv head) rotates the query and builds its fp16 MMA
+// fragments (load_query) once, for every CTA that walks the sequence; the split kernel is launched
+// as its programmatic dependent, so the split kernel's setup and first page copies overlap this
+// kernel, and a piece change inside a CTA's run costs a 2.4 KB copy instead of a rotation.
+template <int D>
+__global__ void __launch_bounds__(256) rotate_q_int4_kernel(const __grid_constant__ Int4Params p) {
+  using Gm = Int4Geom<D>;
+  extern __shared__ __align__(16) uint8_t qsm[];
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long gw = static_cast<long long>(blockIdx.x) * 8 + warp;
+  if (gw >= static_cast<long long>(p.s.B) * p.s.Hk) return;
+  const int b = static_cast<int>(gw / p.s.Hk), h = static_cast<int>(gw % p.s.Hk);
+  uint8_t *qarea = qsm + warp * Gm::QBYTES;
+  uint32_t qf[D / 16][2];
+  float qs0, qs1, qmul;
+  load_query<D, false>(p, qarea, b, h, lane, qf, qs0, qs1, qmul, false);
+  uint32_t *dst = p.qfrag + gw * Gm::QWORDS * 32 + lane;
+#pragma unroll
+  for (int k = 0; k < D / 16; ++k) {
+    dst[(2 * k) * 32] = qf[k][0];
+    dst[(2 * k + 1) * 32] = qf[k][1];
+  }
+  dst[(Gm::QWORDS - 3) * 32] = __float_as_uint(qs0);
+  dst[(Gm::QWORDS - 2) * 32] = __float_as_uint(qs1);
+  dst[(Gm::QWORDS - 1) * 32] = __float_as_uint(qmul);
 }
 
 // What a lane needs from one page after the score MMAs: its base-2 logits for tokens g, g+8 x
@@ -742,7 +812,12 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     const long long X0 = run.base + sub;
     while (X0 >= c0.P + c0.np && c0.b < a.B) seq_next<MODS>(a, c0);
     if (c0.b < a.B) {
-      fetch_query<D, MTOK>(p, qarea, c0.b, h, lane);
+      if (!MTOK && p.qfrag != nullptr) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // the fragments of the pre-kernel
+        fetch_frag<D>(p, qarea, c0.b, h, lane);
+      } else {
+        fetch_query<D, MTOK>(p, qarea, c0.b, h, lane);
+      }
       q_prefetched = c0.b;
     }
   }
@@ -854,14 +929,24 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     }
     if (!have_q) {
       float qmul;
-      load_query<D, MTOK>(p, qarea, cur.b, h, lane, qf, qs0, qs1, qmul, q_prefetched == cur.b);
+      if (!MTOK && p.qfrag != nullptr) {
+        if (q_prefetched != cur.b) asm volatile("griddepcontrol.wait;" ::: "memory");
+        load_frag<D>(p, qarea, cur.b, h, lane, qf, qs0, qs1, qmul, q_prefetched == cur.b);
+      } else {
+        load_query<D, MTOK>(p, qarea, cur.b, h, lane, qf, qs0, qs1, qmul, q_prefetched == cur.b);
+      }
       sm24 = p.sm_log2 * kTwo24 * qmul;
       q_prefetched = -1;
       if (pe_x < run.n && !run.fixed) {  // the run goes on into another sequence: fetch its query now
         SeqCursor nx = cur;
         seq_next<MODS>(a, nx);
         if (nx.b < a.B) {
-          fetch_query<D, MTOK>(p, qarea, nx.b, h, lane);
+          if (!MTOK && p.qfrag != nullptr) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            fetch_frag<D>(p, qarea, nx.b, h, lane);
+          } else {
+            fetch_query<D, MTOK>(p, qarea, nx.b, h, lane);
+          }
           q_prefetched = nx.b;
         }
       }
@@ -944,8 +1029,16 @@ static kvq_status launch_int4_w(const Int4Params &p, const SplitPlan &plan, cuda
   if (ensure_dynamic_smem(decode_int4_kernel<D, kStagesInt4, W, VAR>, smem, attr_done) != cudaSuccess)
     return KVQ_ERR_CUDA;
   const dim3 grid(plan.seg_ctas, plan.head_groups);
-  decode_int4_kernel<D, kStagesInt4, W, VAR><<<grid, 256, smem, s>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  if (VAR == 0 && p.qfrag != nullptr) {  // single token: query pre-rotation, then the split kernel
+    const long long warps = static_cast<long long>(p.s.B) * p.s.Hk;
+    rotate_q_int4_kernel<D><<<static_cast<unsigned>((warps + 7) / 8), 256, 8 * Int4Geom<D>::QBYTES, s>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+    if (launch_dependent(decode_int4_kernel<D, kStagesInt4, W, VAR>, grid, dim3(256), s, p, smem) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+  } else {
+    decode_int4_kernel<D, kStagesInt4, W, VAR><<<grid, 256, smem, s>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  }
   const long long rows = static_cast<long long>(p.s.B) * p.s.Hq;
   if (launch_dependent(merge_kernel<D>, dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), s, p.s) != cudaSuccess)
     return KVQ_ERR_CUDA;
@@ -1054,7 +1147,7 @@ static size_t mods_workspace_bytes(int B, int Hq, int Hk, int D, int num_splits,
   if (!call_geom(B, Hq, Hk, mods, g)) return 0;
   if (!make_plan(static_cast<int>(g->nseq), Hk, num_splits, plan)) return 0;
   const size_t ws = workspace_bytes(static_cast<int>(g->nseq), g->QB * Hq, D, *plan);
-  return g->mtok ? ws + (static_cast<size_t>(g->nseq) * sizeof(int4) + 255) / 256 * 256 : ws;
+  return ws + (g->mtok ? round256(static_cast<size_t>(g->nseq) * sizeof(int4)) : qfrag_bytes(B, Hk, D));
 }
 
 }  // namespace kvq
@@ -1127,6 +1220,9 @@ extern "C" kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache
   int4 *vseq = cg.mtok ? reinterpret_cast<int4 *>(static_cast<uint8_t *>(workspace) +
                                                   kvq::workspace_bytes(nseq, cg.QB * Hq, D, plan))
                        : nullptr;
+  p.qfrag = cg.mtok ? nullptr
+                     : reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) +
+                                                    kvq::workspace_bytes(nseq, cg.QB * Hq, D, plan));
   sa.vseq = vseq;
   sa.signs = rht_signs;
   sa.out = out;

@@ -40,6 +40,12 @@ bool make_plan(int B, int Hk, int num_splits, SplitPlan *plan);
 // [slots * warps_per_head, Hq] fp32, then seg_first / seg_last [B] int32 (each region 256-byte
 // aligned). Needs no initialisation.
 size_t workspace_bytes(int B, int Hq, int D, const SplitPlan &plan);
+inline size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+// Single-token INT4 decode: the rotated query's MMA fragments, (2 D/16 + 3) words per lane of one
+// warp per (sequence, kv head), after the split workspace.
+inline size_t qfrag_bytes(int B, int Hk, int D) {
+  return round256(static_cast<size_t>(B) * Hk * (2 * (D / 16) + 3) * 32 * sizeof(uint32_t));
+}
 void workspace_carve(void *workspace, int B, int Hq, int D, const SplitPlan &plan, float **part_o,
                      float **part_lse, int32_t **seg_first, int32_t **seg_last);
 
@@ -75,13 +81,16 @@ cudaError_t ensure_dynamic_smem(Kernel *kernel, size_t bytes, size_t (&done)[kMa
   return e;
 }
 
-// Launch the log-sum-exp merge as a programmatic dependent of the kernel just enqueued on s.
+// Launch `kernel` as a programmatic dependent of the kernel just enqueued on s (it may start once
+// that kernel has executed griddepcontrol.launch_dependents, and must execute griddepcontrol.wait
+// before reading anything that kernel writes).
 template <typename Args>
-cudaError_t launch_dependent(void (*kernel)(Args), dim3 grid, dim3 block, cudaStream_t s, const Args &a) {
+cudaError_t launch_dependent(void (*kernel)(Args), dim3 grid, dim3 block, cudaStream_t s, const Args &a,
+                             size_t dynamic_smem = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = dynamic_smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -110,14 +110,16 @@ def test_decode_mods_validation_without_gpu():
 
 def test_workspace_sizes_fixed_splits():
     # fixed splits need no device query: slots = B * S, 8 / Hk warps per head, Hq rows of D + lse,
-    # then the first / last CTA of each sequence
+    # then the first / last CTA of each sequence, then the single-token INT4 call's rotated query
+    # fragments (2 D/16 + 3 words for each of 32 lanes per (sequence, kv head))
     n = kvq.kvq_decode_workspace_bytes(2, 4, 2, 64, 4)
     rows = 2 * 4 * 4 * 4
     r256 = lambda x: (x + 255) // 256 * 256
-    assert n == r256(rows * 64 * 4) + r256(rows * 4) + 2 * r256(2 * 4)
+    frag = lambda B, Hk, D: r256(B * Hk * (2 * (D // 16) + 3) * 32 * 4)
+    assert n == r256(rows * 64 * 4) + r256(rows * 4) + 2 * r256(2 * 4) + frag(2, 2, 64)
     n16 = kvq.kvq_decode_workspace_bytes(3, 32, 16, 128, 2)   # 2 head groups of 8 kv heads
     rows = 3 * 2 * 1 * 32
-    assert n16 == r256(rows * 128 * 4) + r256(rows * 4) + 2 * r256(3 * 4)
+    assert n16 == r256(rows * 128 * 4) + r256(rows * 4) + 2 * r256(3 * 4) + frag(3, 16, 128)
     assert kvq.kvq_decode_workspace_bytes(2, 4, 2, 80, 4) == 0
     assert kvq.kvq_decode_workspace_bytes(2, 4, 3, 64, 4) == 0
 
@@ -170,7 +172,8 @@ def test_tq_mse_validation_without_gpu():
     assert call(a14=272) == kvq.KVQ_ERR_INVALID_ARG           # workspace not 256-byte aligned
     assert call(a15=100) == kvq.KVQ_ERR_WORKSPACE
     n = kvq.kvq_decode_tq_mse_workspace_bytes(2, 4, 2, 128, 4)
-    assert n == kvq.kvq_decode_workspace_bytes(2, 4, 2, 128, 4) + 2 * 4 * 128 * 4
+    int4_frag = 2 * 2 * (2 * (128 // 16) + 3) * 32 * 4  # the INT4 call's query fragments (not used here)
+    assert n == kvq.kvq_decode_workspace_bytes(2, 4, 2, 128, 4) - int4_frag + 2 * 4 * 128 * 4
 
 
 def test_kpool_validation_without_gpu():
