@@ -476,15 +476,13 @@ __device__ __forceinline__ LaneOffsets<D> lane_offsets(int warp, int sub, int hl
   return o;
 }
 
-// S = (sum_d q_d n_d - zp sum_d q_d) * scale_k * sm for one (page, head) tile at stage offset so.
-template <int D, int W>
-__device__ __forceinline__ void page_scores(PageIn &pg, uint32_t so, const LaneOffsets<D> &lo,
-                                            const uint32_t (&qf)[D / 16][2], float qs0, float qs1, float sm24) {
+// c += sum_d q_d n_d (the score MMAs, all 8 columns) for the (page, head) tile at stage offset so.
+template <int D>
+__device__ __forceinline__ void score_mma(float (&c)[4], uint32_t so, const LaneOffsets<D> &lo,
+                                          const uint32_t (&qf)[D / 16][2]) {
   using Gm = Int4Geom<D>;
-  constexpr int HB = 8 / W;
-  float c[4] = {0.f, 0.f, 0.f, 0.f};
   uint32_t wa[Gm::WPR], wb[Gm::WPR];
-  const uint32_t ko = so + lo.k, sk = so + lo.s;
+  const uint32_t ko = so + lo.k;
   if constexpr (Gm::WPR == 4) {
     const uint4 a4 = ld_s128(ko), b4 = ld_s128(ko + 8 * Gm::RB);
     wa[0] = a4.x; wa[1] = a4.y; wa[2] = a4.z; wa[3] = a4.w;
@@ -494,14 +492,22 @@ __device__ __forceinline__ void page_scores(PageIn &pg, uint32_t so, const LaneO
     wa[0] = a2.x; wa[1] = a2.y;
     wb[0] = b2.x; wb[1] = b2.y;
   }
-  const uint32_t kw0 = ld_s32(sk), kw1 = ld_s32(sk + 32 * HB);
-  const uint32_t vw0 = ld_s32(sk + Gm::SCPOOL), vw1 = ld_s32(sk + Gm::SCPOOL + 32 * HB);
 #pragma unroll
   for (int m = 0; m < Gm::WPR; ++m) {
     const uint32_t xa = wa[m] >> 8, xb = wb[m] >> 8;
     mma_f16_16816(c, wa[m] & kLo, wb[m] & kLo, wa[m] & kHi, wb[m] & kHi, qf[2 * m][0], qf[2 * m][1]);
     mma_f16_16816(c, xa & kLo, xb & kLo, xa & kHi, xb & kHi, qf[2 * m + 1][0], qf[2 * m + 1][1]);
   }
+}
+
+// S = (sum_d q_d n_d - zp sum_d q_d) * scale_k * sm from the MMA sums c of tokens g, g + 8, and
+// their V scales / zero-points; sk = the stage offset of token g's K scale word (this lane's page).
+template <int D, int HB>
+__device__ __forceinline__ void score_epilogue(PageIn &pg, const float (&c)[4], uint32_t sk, float qs0, float qs1,
+                                               float sm24) {
+  using Gm = Int4Geom<D>;
+  const uint32_t kw0 = ld_s32(sk), kw1 = ld_s32(sk + 32 * HB);
+  const uint32_t vw0 = ld_s32(sk + Gm::SCPOOL), vw1 = ld_s32(sk + Gm::SCPOOL + 32 * HB);
   const float ck0 = __uint_as_float(kw0 & ~0xFu) * sm24, ck1 = __uint_as_float(kw1 & ~0xFu) * sm24;
   const float zk0 = static_cast<float>(kw0 & 0xFu), zk1 = static_cast<float>(kw1 & 0xFu);
   pg.s[0] = (c[0] - zk0 * qs0) * ck0;
@@ -514,19 +520,33 @@ __device__ __forceinline__ void page_scores(PageIn &pg, uint32_t so, const LaneO
   pg.zv1 = static_cast<float>(vw1 & 0xFu);
 }
 
+// S = (sum_d q_d n_d - zp sum_d q_d) * scale_k * sm for one (page, head) tile at stage offset so.
+template <int D, int W>
+__device__ __forceinline__ void page_scores(PageIn &pg, uint32_t so, const LaneOffsets<D> &lo,
+                                            const uint32_t (&qf)[D / 16][2], float qs0, float qs1, float sm24) {
+  float c[4] = {0.f, 0.f, 0.f, 0.f};
+  score_mma<D>(c, so, lo, qf);
+  score_epilogue<D, 8 / W>(pg, c, so + lo.s, qs0, qs1, sm24);
+}
+
 // O^T += V^T . P_v^T for one (page, head) tile at stage offset so; x0 / x1 = this lane's fp16
 // P_v pairs (tokens g, g+8) of heads 2t / 2t+1.
-template <int D>
-__device__ __forceinline__ void page_pv(float (&acc)[D / 16][4], uint32_t so, const LaneOffsets<D> &lo,
-                                        uint32_t x0, uint32_t x1, int lane) {
-  using Gm = Int4Geom<D>;
+// B fragment of P_v^T from the lanes' P_v pairs: this lane needs MMA column g at tokens 2t, 2t+1
+// (b01) and 2t+8, 2t+9 (b23).
+__device__ __forceinline__ void pv_bfrag(uint32_t x0, uint32_t x1, int lane, uint32_t &b01, uint32_t &b23) {
   const int g = lane >> 2, t = lane & 3;
-  // B fragment of P_v^T: this lane needs head g at tokens 2t, 2t+1 (b01), 2t+8, 2t+9 (b23)
   const int src0 = 8 * t + (g >> 1), src1 = src0 + 4;
   const uint32_t y0 = __shfl_sync(FULL, x0, src0), y1 = __shfl_sync(FULL, x1, src0);
   const uint32_t z0 = __shfl_sync(FULL, x0, src1), z1 = __shfl_sync(FULL, x1, src1);
   const uint32_t ya = (g & 1) ? y1 : y0, za = (g & 1) ? z1 : z0;
-  const uint32_t b01 = __byte_perm(ya, za, 0x5410), b23 = __byte_perm(ya, za, 0x7632);
+  b01 = __byte_perm(ya, za, 0x5410);
+  b23 = __byte_perm(ya, za, 0x7632);
+}
+
+// O^T += V^T . P_v^T for the (page, head) tile at stage offset so, given the B fragment.
+template <int D>
+__device__ __forceinline__ void pv_mma(float (&acc)[D / 16][4], uint32_t so, const LaneOffsets<D> &lo,
+                                       uint32_t b01, uint32_t b23) {
   // V^T fragments: ldmatrix.trans gives this lane word 8q + g of tokens (2t, 2t+1) [x] and
   // (2t+8, 2t+9) [y]; its low / high nibbles of byte 0 (then byte 1) are A rows g / g + 8
 #pragma unroll
@@ -546,6 +566,14 @@ __device__ __forceinline__ void page_pv(float (&acc)[D / 16][4], uint32_t so, co
   }
 }
 
+template <int D>
+__device__ __forceinline__ void page_pv(float (&acc)[D / 16][4], uint32_t so, const LaneOffsets<D> &lo,
+                                        uint32_t x0, uint32_t x1, int lane) {
+  uint32_t b01, b23;
+  pv_bfrag(x0, x1, lane, b01, b23);
+  pv_mma<D>(acc, so, lo, b01, b23);
+}
+
 // tanh(y) = 1 - 2 / (e^(2y) + 1) with the hardware base-2 exponential; |y| is limited to 10
 // (tanh(10) rounds to 1 in fp32). The absolute error (a few 1e-7) is what the soft cap passes on.
 __device__ __forceinline__ float tanh_fast(float y) {
@@ -563,22 +591,42 @@ struct ScoreMods {
 };
 
 // NP consecutive pages of this warp (stage offsets so[0..NP-1]) inside one piece: scores, one
-// online softmax step over their 16 * NP tokens, P.V. MASKED: some rows of the (single) page lie
+// online softmax step over their 16 * NP tokens, P.V.
+// COMB (single-token decode with G <= 4 heads per kv head): the MMA's 8 columns carry the G heads
+// twice (columns n and n + 4 hold head n), and a pair of pages is split over them -- columns 0..3
+// score the first page, columns 4..7 the second -- so each lane's softmax handles 4 live scores
+// instead of 8 of which half are padding. Columns 0..3 and 4..7 are two independent softmax
+// streams over the piece's pages (a single page, MASKED, goes to columns 0..3 only), combined by
+// comb_merge at the end of the piece. MASKED: some rows of the (single) page lie
 // outside [t0, t1) -- the ragged end of a sequence, a fixed split boundary or the start of a
 // sliding window -- and may hold never-written scale words (NaN): they are selected away, never
 // multiplied; in multi-token decode a column's keys are also limited to its own query token's
 // range [lw0, lim0) / [lw1, lim1) for the lane's columns 2t / 2t + 1 (causal limit, window).
 // MODS: apply the score modifiers md (page i's row 0 is at position nb + 16 W i).
-template <int D, int W, int NP, bool MASKED, bool MODS, bool MTOK>
+template <int D, int W, int NP, bool MASKED, bool MODS, bool MTOK, bool COMB>
 __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&so)[2], const LaneOffsets<D> &lo,
                                            const uint32_t (&qf)[D / 16][2], float qs0, float qs1, float sm24,
                                            int lane, int nb, int t0, int t1, int lim0, int lim1, int lw0,
                                            int lw1, const Int4Params &p, const ScoreMods &md) {
   using Gm = Int4Geom<D>;
+  static_assert(!COMB || (!MODS && !MTOK), "combined columns: plain single-token decode only");
+  constexpr bool PAIRED = COMB && NP == 2;  // two pages over the two column halves
+  constexpr int NQ = PAIRED ? 1 : NP;       // pages of softmax operands per lane
   const int g = lane >> 2;
-  PageIn pg[NP];
+  const bool hi_half = (lane & 3) >= 2;  // this lane's columns are 4..7
+  PageIn pg[NQ];
+  if constexpr (PAIRED) {
+    float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
+    score_mma<D>(ca, so[0], lo, qf);
+    score_mma<D>(cb, so[1], lo, qf);
+    float c[4];
 #pragma unroll
-  for (int i = 0; i < NP; ++i) page_scores<D, W>(pg[i], so[i], lo, qf, qs0, qs1, sm24);
+    for (int j = 0; j < 4; ++j) c[j] = hi_half ? cb[j] : ca[j];
+    score_epilogue<D, 8 / W>(pg[0], c, (hi_half ? so[1] : so[0]) + lo.s, qs0, qs1, sm24);
+  } else {
+#pragma unroll
+    for (int i = 0; i < NP; ++i) page_scores<D, W>(pg[i], so[i], lo, qf, qs0, qs1, sm24);
+  }
   if constexpr (MODS) {
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
@@ -608,6 +656,12 @@ __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&s
       ok10 = ok10 && nb + g + 8 < lim0 && nb + g + 8 >= lw0;
       ok11 = ok11 && nb + g + 8 < lim1 && nb + g + 8 >= lw1;
     }
+    if constexpr (COMB) {  // a single page belongs to columns 0..3
+      ok00 = ok00 && !hi_half;
+      ok01 = ok01 && !hi_half;
+      ok10 = ok10 && !hi_half;
+      ok11 = ok11 && !hi_half;
+    }
     pg[0].s[0] = ok00 ? pg[0].s[0] : -INFINITY;
     pg[0].s[1] = ok01 ? pg[0].s[1] : -INFINITY;
     pg[0].s[2] = ok10 ? pg[0].s[2] : -INFINITY;
@@ -617,12 +671,12 @@ __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&s
   // each column's reference m (decode_common.cuh); one warp vote finds a step in which a score
   // passes m + kScoreCap or a weight passes kWeightHi, and only then (rarely) are the columns'
   // maxima reduced, their references raised and the running sums rescaled.
-  uint32_t X0[NP], X1[NP];  // this lane's fp16 P_v pairs (tokens g, g+8) of columns 2t, 2t+1
+  uint32_t X0[NQ], X1[NQ];  // this lane's fp16 P_v pairs (tokens g, g+8) of columns 2t, 2t+1
   float ls0, ls1, wm0, wm1;  // the step's weight sums and largest P_v per column
   auto weights = [&](float q0, float q1) {
     ls0 = ls1 = wm0 = wm1 = 0.f;
 #pragma unroll
-    for (int i = 0; i < NP; ++i) {
+    for (int i = 0; i < NQ; ++i) {
       const float p00 = fast_exp2(pg[i].s[0] - q0), p10 = fast_exp2(pg[i].s[2] - q0);
       const float p01 = fast_exp2(pg[i].s[1] - q1), p11 = fast_exp2(pg[i].s[3] - q1);
       ls0 += p00 + p10;
@@ -643,7 +697,7 @@ __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&s
   weights(st.m0 == -INFINITY ? 0.f : st.m0, st.m1 == -INFINITY ? 0.f : st.m1);
   float ml0 = fmaxf(pg[0].s[0], pg[0].s[2]), ml1 = fmaxf(pg[0].s[1], pg[0].s[3]);
 #pragma unroll
-  for (int i = 1; i < NP; ++i) {
+  for (int i = 1; i < NQ; ++i) {
     ml0 = fmaxf(ml0, fmaxf(pg[i].s[0], pg[i].s[2]));
     ml1 = fmaxf(ml1, fmaxf(pg[i].s[1], pg[i].s[3]));
   }
@@ -657,7 +711,7 @@ __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&s
     const float q0 = b0 == -INFINITY ? 0.f : b0, q1 = b1 == -INFINITY ? 0.f : b1;
     float x0 = 0.f, x1 = 0.f;  // the largest P_v per column against the bases
 #pragma unroll
-    for (int i = 0; i < NP; ++i) {
+    for (int i = 0; i < NQ; ++i) {
       const float a00 = fast_exp2(pg[i].s[0] - q0) * pg[i].sv0, a10 = fast_exp2(pg[i].s[2] - q0) * pg[i].sv1;
       const float a01 = fast_exp2(pg[i].s[1] - q1) * pg[i].sv0, a11 = fast_exp2(pg[i].s[3] - q1) * pg[i].sv1;
       x0 = fmaxf(x0, fmaxf(ok00 ? a00 : 0.f, ok10 ? a10 : 0.f));
@@ -688,22 +742,55 @@ __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&s
   st.l0 += ls0;
   st.l1 += ls1;
 #pragma unroll
-  for (int i = 0; i < NP; ++i) {  // sum P_v * zp_v (the fp16 P_v the products use)
+  for (int i = 0; i < NQ; ++i) {  // sum P_v * zp_v (the fp16 P_v the products use)
     const float2 f0 = __half22float2(u32_as_h2(X0[i])), f1 = __half22float2(u32_as_h2(X1[i]));
     st.pz0 += f0.x * pg[i].zv0 + f0.y * pg[i].zv1;
     st.pz1 += f1.x * pg[i].zv0 + f1.y * pg[i].zv1;
   }
   // ---- O^T += V^T . P_v^T
+  if constexpr (PAIRED) {  // columns 0..3 take the first page's V, columns 4..7 the second's
+    uint32_t b01, b23;
+    pv_bfrag(X0[0], X1[0], lane, b01, b23);
+    const bool lo_col = g < 4;  // this lane supplies MMA column g of the B fragment
+    pv_mma<D>(st.acc, so[0], lo, lo_col ? b01 : 0u, lo_col ? b23 : 0u);
+    pv_mma<D>(st.acc, so[1], lo, lo_col ? 0u : b01, lo_col ? 0u : b23);
+  } else {
 #pragma unroll
-  for (int i = 0; i < NP; ++i) page_pv<D>(st.acc, so[i], lo, X0[i], X1[i], lane);
+    for (int i = 0; i < NP; ++i) page_pv<D>(st.acc, so[i], lo, X0[i], X1[i], lane);
+  }
 }
 
 // Epilogue of one piece: undo the subnormal scaling, apply the zero-point term, normalise, and
 // write the warp's partial (an empty piece writes zeros with lse = -inf).
-template <int D, bool MTOK>
+// COMB: fold the softmax stream of columns 4..7 into columns 0..3 (lanes t and t ^ 2 hold the
+// same heads): each side is rescaled from its reference to the larger one (a side with no keys,
+// reference -inf, contributes nothing).
+template <int D>
+__device__ __forceinline__ void comb_merge(PieceState<D> &st) {
+  auto fold = [&](float &m, float &l, float &pz, int j0, int j1) {
+    const float mo = __shfl_xor_sync(FULL, m, 2), lo = __shfl_xor_sync(FULL, l, 2);
+    const float pzo = __shfl_xor_sync(FULL, pz, 2);
+    const float mn = fmaxf(m, mo);
+    const float a = m == -INFINITY ? 0.f : fast_exp2(m - mn), ao = mo == -INFINITY ? 0.f : fast_exp2(mo - mn);
+    m = mn;
+    l = l * a + lo * ao;
+    pz = pz * a + pzo * ao;
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+      const float x0 = __shfl_xor_sync(FULL, st.acc[i][j0], 2), x1 = __shfl_xor_sync(FULL, st.acc[i][j1], 2);
+      st.acc[i][j0] = st.acc[i][j0] * a + x0 * ao;
+      st.acc[i][j1] = st.acc[i][j1] * a + x1 * ao;
+    }
+  };
+  fold(st.m0, st.l0, st.pz0, 0, 2);  // column 2t: acc[.][0] (row g), acc[.][2] (row g + 8)
+  fold(st.m1, st.l1, st.pz1, 1, 3);  // column 2t + 1
+}
+
+template <int D, bool MTOK, bool COMB>
 __device__ __forceinline__ void int4_finish(const SplitArgs &a, PieceState<D> &st, long long slot, int sub,
                                             int h, int lane) {
   using Gm = Int4Geom<D>;
+  if constexpr (COMB) comb_merge<D>(st);
   const float l0 = warp_sum_g(st.l0), l1 = warp_sum_g(st.l1);
   const float pz0 = warp_sum_g(st.pz0), pz1 = warp_sum_g(st.pz1);
   const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
@@ -729,10 +816,10 @@ __device__ __forceinline__ void int4_finish(const SplitArgs &a, PieceState<D> &s
 // CTA's block ids in a shared ring two batches of 32 pages ahead of its own position (a refill
 // is at most NS * W <= 32 pages ahead of the slowest warp).
 // VAR 0: plain; 1: score modifiers (window, soft cap, ALiBi; multi-token decode allowed);
-// 2: multi-token decode only.
+// 2: multi-token decode only; 3: plain with combined columns (G <= 4, see int4_pages).
 template <int D, int NS, int W, int VAR>
 __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_constant__ Int4Params p) {
-  constexpr bool MODS = VAR == 1, MTOK = VAR != 0;
+  constexpr bool MODS = VAR == 1, MTOK = VAR == 1 || VAR == 2, COMB = VAR == 3;
   using Gm = Int4Geom<D>;
   constexpr int HB = 8 / W;
   constexpr int SCP = 64 * HB < 128 ? 128 : 64 * HB;  // one page's scale block, 128-byte aligned slots
@@ -894,7 +981,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   columns();
   auto finish_piece = [&]() {
     const long long slot = run.fixed ? static_cast<long long>(blockIdx.x) : blockIdx.x + static_cast<long long>(cur.b);
-    int4_finish<D, MTOK>(a, st, slot, sub, h, lane);
+    int4_finish<D, MTOK, COMB>(a, st, slot, sub, h, lane);
     if (!run.fixed && warp == 0 && lane == 0 && blockIdx.y == 0) {
       if (cur.P >= run.base) a.seg_first[cur.b] = static_cast<int>(blockIdx.x);
       if (cur.P + cur.np <= run.end) a.seg_last[cur.b] = static_cast<int>(blockIdx.x);
@@ -936,6 +1023,18 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
         load_query<D, MTOK>(p, qarea, cur.b, h, lane, qf, qs0, qs1, qmul, q_prefetched == cur.b);
       }
       sm24 = p.sm_log2 * kTwo24 * qmul;
+      if constexpr (COMB) {  // columns 4..7 repeat columns 0..3 (lane l + 16 holds column n + 4)
+#pragma unroll
+        for (int k = 0; k < Gm::KSTEPS; ++k) {
+          qf[k][0] = __shfl_sync(FULL, qf[k][0], lane & 15);
+          qf[k][1] = __shfl_sync(FULL, qf[k][1], lane & 15);
+        }
+        const float r0 = __shfl_xor_sync(FULL, qs0, 2), r1 = __shfl_xor_sync(FULL, qs1, 2);
+        if ((lane & 3) >= 2) {
+          qs0 = r0;
+          qs1 = r1;
+        }
+      }
       q_prefetched = -1;
       if (pe_x < run.n && !run.fixed) {  // the run goes on into another sequence: fetch its query now
         SeqCursor nx = cur;
@@ -971,7 +1070,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
         rest = true;
         for (int k = 2; k < NS && k < n_stages; ++k) issue(k, k);
       }
-      int4_pages<D, W, 2, false, MODS, MTOK>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, lim0, lim1, lw0,
+      int4_pages<D, W, 2, false, MODS, MTOK, COMB>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, lim0, lim1, lw0,
                                              lw1, p, md);
       release(j, sj);
       release(j + 1, sj1);
@@ -987,7 +1086,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
         rest = true;
         for (int k = 2; k < NS && k < n_stages; ++k) issue(k, k);
       }
-      int4_pages<D, W, 1, true, MODS, MTOK>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, lim0, lim1, lw0,
+      int4_pages<D, W, 1, true, MODS, MTOK, COMB>(st, so, lo, qf, qs0, qs1, sm24, lane, nb, t0, t1, lim0, lim1, lw0,
                                             lw1, p, md);
       release(j, sj);
       j += 1;
@@ -1029,7 +1128,7 @@ static kvq_status launch_int4_w(const Int4Params &p, const SplitPlan &plan, cuda
   if (ensure_dynamic_smem(decode_int4_kernel<D, kStagesInt4, W, VAR>, smem, attr_done) != cudaSuccess)
     return KVQ_ERR_CUDA;
   const dim3 grid(plan.seg_ctas, plan.head_groups);
-  if (VAR == 0 && p.qfrag != nullptr) {  // single token: query pre-rotation, then the split kernel
+  if ((VAR == 0 || VAR == 3) && p.qfrag != nullptr) {  // single token: query pre-rotation, then the split kernel
     const long long warps = static_cast<long long>(p.s.B) * p.s.Hk;
     rotate_q_int4_kernel<D><<<static_cast<unsigned>((warps + 7) / 8), 256, 8 * Int4Geom<D>::QBYTES, s>>>(p);
     if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
@@ -1250,10 +1349,14 @@ extern "C" kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache
   }
   // sinks act in the merge only; window, soft cap and ALiBi need the modifier kernel (which also
   // takes multi-token decode); multi-token decode alone has its own
-  const int var = (p.softcap2 > 0.f || p.alibi != nullptr || sa.window > 0) ? 1 : (cg.mtok ? 2 : 0);
-  if (D == 128)
-    return var == 0 ? launch_int4<128, 0>(p, plan, s) : var == 1 ? launch_int4<128, 1>(p, plan, s) : launch_int4<128, 2>(p, plan, s);
-  return var == 0 ? launch_int4<64, 0>(p, plan, s) : var == 1 ? launch_int4<64, 1>(p, plan, s) : launch_int4<64, 2>(p, plan, s);
+  // a plain call with G <= 4 heads per kv head fills the MMA's idle columns with a second page
+  const int var = (p.softcap2 > 0.f || p.alibi != nullptr || sa.window > 0) ? 1 : cg.mtok ? 2 : (Hq / Hk <= 4 ? 3 : 0);
+  switch (var) {
+    case 0: return D == 128 ? launch_int4<128, 0>(p, plan, s) : launch_int4<64, 0>(p, plan, s);
+    case 1: return D == 128 ? launch_int4<128, 1>(p, plan, s) : launch_int4<64, 1>(p, plan, s);
+    case 2: return D == 128 ? launch_int4<128, 2>(p, plan, s) : launch_int4<64, 2>(p, plan, s);
+    default: return D == 128 ? launch_int4<128, 3>(p, plan, s) : launch_int4<64, 3>(p, plan, s);
+  }
 }
 
 extern "C" kvq_status kvq_decode_int4(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
