@@ -890,24 +890,27 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
       }
     }
   };
-  // the first piece's query rows go out before any page copy, so they do not queue behind the
-  // launch-time burst of page copies
+  // the first piece's query: raw rows (rotated here) go out before any page copy, so they do not
+  // queue behind the launch-time burst of page copies; the pre-kernel's fragments are fetched
+  // after the first page copies are out (waiting for that kernel must not delay them)
   uint8_t *qarea = kvq_dsmem + base + NS * Gm::STAGE + warp * Gm::QBYTES;
-  int q_prefetched = -1;  // sequence whose query rows fetch_query has started
-  if (sub < run.n) {
+  int q_prefetched = -1;  // sequence whose query rows / fragments are being copied
+  const bool pre_rotated = !MTOK && p.qfrag != nullptr;
+  auto prefetch_first = [&]() {
+    if (sub >= run.n) return;
     SeqCursor c0 = run.first;
     const long long X0 = run.base + sub;
     while (X0 >= c0.P + c0.np && c0.b < a.B) seq_next<MODS>(a, c0);
-    if (c0.b < a.B) {
-      if (!MTOK && p.qfrag != nullptr) {
-        asm volatile("griddepcontrol.wait;" ::: "memory");  // the fragments of the pre-kernel
-        fetch_frag<D>(p, qarea, c0.b, h, lane);
-      } else {
-        fetch_query<D, MTOK>(p, qarea, c0.b, h, lane);
-      }
-      q_prefetched = c0.b;
+    if (c0.b >= a.B) return;
+    if (pre_rotated) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // the fragments of the pre-kernel
+      fetch_frag<D>(p, qarea, c0.b, h, lane);
+    } else {
+      fetch_query<D, MTOK>(p, qarea, c0.b, h, lane);
     }
-  }
+    q_prefetched = c0.b;
+  };
+  if (!pre_rotated) prefetch_first();
   int cb = 0;        // warp 0: the batch of block ids its consumption has reached
   bool rest = false;  // warp 0: stages 2 .. NS - 1 issued
   if (warp == 0) {
@@ -920,6 +923,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     for (int k = 0; k < 2 && k < n_stages; ++k) issue(k, k);
   }
   __syncthreads();  // barrier init and the first block ids, before any other warp can refill
+  if (pre_rotated) prefetch_first();
   // A slot is refilled by the last warp done with it (the shared counter's old value is 7 mod 8):
   // no warp waits for another to notice the slot is free.
   auto release = [&](int k, int slot) {
