@@ -554,3 +554,29 @@ class Int4Decoder:
         _check(self._fn(q.data_ptr(), *self._head, out.data_ptr(), _out_code(out.dtype), *self._dims,
                         _stream(stream)), "kvq_decode_int4")
         return out
+
+
+class CapturedStep:
+    """A fixed sequence of calls on one stream, replayed as one CUDA graph.
+
+    step = CapturedStep(fn, stream) runs fn() once eagerly (which also sets the kernels' one-time
+    attributes), then captures fn() on `stream`; step() replays the capture on that stream,
+    asynchronously. fn must only enqueue work on `stream` (library calls, tensor copies between
+    fixed buffers -- e.g. a pinned host staging buffer to its device twin and an output back to
+    pinned memory); the buffers it touches keep their addresses, and their contents at replay
+    time are what the replay reads. A decode step whose inputs change from step to step copies
+    them into the same buffers before each replay, or inside fn."""
+
+    def __init__(self, fn, stream):
+        self.stream = stream
+        with torch.cuda.stream(stream):
+            fn()
+        stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=stream):
+            fn()
+        self._keep = fn
+
+    def __call__(self):
+        with torch.cuda.stream(self.stream):
+            self.graph.replay()

@@ -196,3 +196,39 @@ def test_prepared_writer_and_decoder_match_the_oracle():
         assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
     with pytest.raises(ValueError):
         kvq.Int4Writer(*caches, signs)(k.cuda()[:, :4], v.cuda()[:, :4], slots.cuda())
+
+
+def test_captured_step_replays_with_new_inputs():
+    """kvq.CapturedStep: a step of (host-to-device copy of a staging buffer, decode, copy back)
+    captured once and replayed with new staging contents gives, every replay, the oracle's rows for
+    those contents and the same bytes as an eager call."""
+    case = workloads.DecodeCase("graph", 3, 32, 8, 128, [300, 17, 1500], seed=72, outlier_channels=4)
+    c = Int4Case(case)
+    g = c.to_gpu()
+    stream = torch.cuda.Stream()
+    q_host = torch.empty(g["q"].shape, dtype=torch.bfloat16).pin_memory()
+    q_dev = torch.empty_like(g["q"])
+    out_dev = torch.empty((3, 32, 128), dtype=torch.float32, device="cuda")
+    out_host = torch.empty(out_dev.shape, dtype=torch.float32).pin_memory()
+    dec = kvq.Int4Decoder(g["kc"], g["vc"], g["ks"], g["vs"], g["bt"], g["lens"], g["signs"], c.scale, case.Hq)
+
+    def calls():
+        q_dev.copy_(q_host, non_blocking=True)
+        dec(q_dev, out_dev, stream=stream)
+        out_host.copy_(out_dev, non_blocking=True)
+
+    q_host.copy_(g["q"].cpu())
+    step = kvq.CapturedStep(calls, stream)
+    for seed in (0, 1, 2):
+        q_new = torch.randn(g["q"].shape, generator=torch.Generator().manual_seed(100 + seed)).to(torch.bfloat16)
+        q_host.copy_(q_new)
+        step()
+        stream.synchronize()
+        got = out_host.numpy().copy()
+        c.q = q_new
+        assert_close(got, c.oracle(), what="captured step, query set %d" % seed)
+        eager = torch.empty_like(out_dev)
+        kvq.kvq_decode_int4(q_new.cuda(), g["kc"], g["vc"], g["ks"], g["vs"], g["bt"], g["lens"], g["signs"],
+                            c.scale, out=eager)
+        assert np.array_equal(got, eager.cpu().numpy())
+    assert kvq.kvq_device_error() == (0, 0)
