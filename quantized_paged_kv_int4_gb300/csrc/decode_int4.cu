@@ -609,7 +609,7 @@ __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&s
                                            int lane, int nb, int t0, int t1, int lim0, int lim1, int lw0,
                                            int lw1, const Int4Params &p, const ScoreMods &md) {
   using Gm = Int4Geom<D>;
-  static_assert(!COMB || (!MODS && !MTOK), "combined columns: plain single-token decode only");
+  static_assert(!COMB || !MTOK, "combined columns: single-token decode only");
   constexpr bool PAIRED = COMB && NP == 2;  // two pages over the two column halves
   constexpr int NQ = PAIRED ? 1 : NP;       // pages of softmax operands per lane
   const int g = lane >> 2;
@@ -629,13 +629,14 @@ __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&s
   }
   if constexpr (MODS) {
 #pragma unroll
-    for (int i = 0; i < NP; ++i) {
+    for (int i = 0; i < NQ; ++i) {
       if (p.softcap2 > 0.f) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) pg[i].s[j] = p.softcap2 * tanh_fast(pg[i].s[j] * p.inv_softcap2);
       }
       if (p.alibi != nullptr) {
-        const int n = nb + i * W * kPage + g;  // token g's position (token g + 8: n + 8)
+        // token g's position (token g + 8: n + 8); a paired lane of columns 4..7 scores the second page
+        const int n = nb + (PAIRED ? (hi_half ? W * kPage : 0) : i * W * kPage) + g;
         const float e0 = static_cast<float>(n - md.qp0), e1 = static_cast<float>(n - md.qp1);
         pg[i].s[0] = fmaf(md.sl0, e0, pg[i].s[0]);
         pg[i].s[1] = fmaf(md.sl1, e1, pg[i].s[1]);
@@ -816,10 +817,11 @@ __device__ __forceinline__ void int4_finish(const SplitArgs &a, PieceState<D> &s
 // CTA's block ids in a shared ring two batches of 32 pages ahead of its own position (a refill
 // is at most NS * W <= 32 pages ahead of the slowest warp).
 // VAR 0: plain; 1: score modifiers (window, soft cap, ALiBi; multi-token decode allowed);
-// 2: multi-token decode only; 3: plain with combined columns (G <= 4, see int4_pages).
+// 2: multi-token decode only; 3: plain with combined columns (G <= 4, see int4_pages);
+// 4: score modifiers, single-token, combined columns (G <= 4).
 template <int D, int NS, int W, int VAR>
 __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_constant__ Int4Params p) {
-  constexpr bool MODS = VAR == 1, MTOK = VAR == 1 || VAR == 2, COMB = VAR == 3;
+  constexpr bool MODS = VAR == 1 || VAR == 4, MTOK = VAR == 1 || VAR == 2, COMB = VAR == 3 || VAR == 4;
   using Gm = Int4Geom<D>;
   constexpr int HB = 8 / W;
   constexpr int SCP = 64 * HB < 128 ? 128 : 64 * HB;  // one page's scale block, 128-byte aligned slots
@@ -944,8 +946,8 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   bool have_q = false, abort = false;
   float sm24 = 0.f;  // score scale of the piece: sm * log2 e * 2^24 (K operands) * 2^k (q shift)
   ScoreMods md{};
-  if constexpr (MODS) {  // MMA column n is query token n / G, head h G + n % G of it
-    const int c0 = 2 * (lane & 3), G = a.G;
+  if constexpr (MODS) {  // MMA column n is query token n / G, head h G + n % G of it (COMB: head n % 4)
+    const int c0 = COMB ? 2 * (lane & 1) : 2 * (lane & 3), G = a.G;
     const float lg2e = 1.4426950408889634f;
     md.sl0 = p.alibi != nullptr && c0 < G * a.Q ? __ldg(p.alibi + h * G + c0 % G) * lg2e : 0.f;
     md.sl1 = p.alibi != nullptr && c0 + 1 < G * a.Q ? __ldg(p.alibi + h * G + (c0 + 1) % G) * lg2e : 0.f;
@@ -1132,7 +1134,7 @@ static kvq_status launch_int4_w(const Int4Params &p, const SplitPlan &plan, cuda
   if (ensure_dynamic_smem(decode_int4_kernel<D, kStagesInt4, W, VAR>, smem, attr_done) != cudaSuccess)
     return KVQ_ERR_CUDA;
   const dim3 grid(plan.seg_ctas, plan.head_groups);
-  if ((VAR == 0 || VAR == 3) && p.qfrag != nullptr) {  // single token: query pre-rotation, then the split kernel
+  if ((VAR == 0 || VAR == 3 || VAR == 4) && p.qfrag != nullptr) {  // single token: query pre-rotation, then the split kernel
     const long long warps = static_cast<long long>(p.s.B) * p.s.Hk;
     rotate_q_int4_kernel<D><<<static_cast<unsigned>((warps + 7) / 8), 256, 8 * Int4Geom<D>::QBYTES, s>>>(p);
     if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
@@ -1353,12 +1355,14 @@ extern "C" kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache
   }
   // sinks act in the merge only; window, soft cap and ALiBi need the modifier kernel (which also
   // takes multi-token decode); multi-token decode alone has its own
-  // a plain call with G <= 4 heads per kv head fills the MMA's idle columns with a second page
-  const int var = (p.softcap2 > 0.f || p.alibi != nullptr || sa.window > 0) ? 1 : cg.mtok ? 2 : (Hq / Hk <= 4 ? 3 : 0);
+  // a single-token call with G <= 4 heads per kv head fills the MMA's idle columns with a second page
+  const bool scored = p.softcap2 > 0.f || p.alibi != nullptr || sa.window > 0, comb = Hq / Hk <= 4;
+  const int var = scored ? (cg.mtok || !comb ? 1 : 4) : cg.mtok ? 2 : (comb ? 3 : 0);
   switch (var) {
     case 0: return D == 128 ? launch_int4<128, 0>(p, plan, s) : launch_int4<64, 0>(p, plan, s);
     case 1: return D == 128 ? launch_int4<128, 1>(p, plan, s) : launch_int4<64, 1>(p, plan, s);
     case 2: return D == 128 ? launch_int4<128, 2>(p, plan, s) : launch_int4<64, 2>(p, plan, s);
+    case 4: return D == 128 ? launch_int4<128, 4>(p, plan, s) : launch_int4<64, 4>(p, plan, s);
     default: return D == 128 ? launch_int4<128, 3>(p, plan, s) : launch_int4<64, 3>(p, plan, s);
   }
 }
