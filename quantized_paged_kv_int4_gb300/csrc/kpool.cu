@@ -55,7 +55,12 @@ __device__ __forceinline__ float exp_pool(float x) {
 constexpr int kKpRow = 16 + 4;           // padded 16-element block (words)
 constexpr int kKpVec = 8 * kKpRow + 16;  // padded row: the 4 rows of a warp in two bank halves
 
-__global__ void __launch_bounds__(256) kpool_write_kernel(const KpoolParams p, long long tiles) {
+// KP > 0: the pool size as a compile-time constant (the slot loops unroll, so every slot's loads
+// are in flight together); KP == 0: any pool size from the parameters. Two CTAs per SM (at most
+// 128 registers): at one CTA per SM the unrolled form was slower than the rolled one.
+template <int KP>
+__global__ void __launch_bounds__(256, 2) kpool_write_kernel(const KpoolParams p, long long tiles) {
+  const int pool = KP > 0 ? KP : p.pool;
   __shared__ __align__(16) float s_buf[8][4 * kKpVec];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rw = lane >> 3, l8 = lane & 7;
@@ -68,11 +73,12 @@ __global__ void __launch_bounds__(256) kpool_write_kernel(const KpoolParams p, l
     // ---- pooled key of dims 16 l8 .. 16 l8 + 15
     float v[16];
     {
-      const long long kbase = (live ? row : 0) * p.pool * 128 + 16 * l8;
+      const long long kbase = (live ? row : 0) * pool * 128 + 16 * l8;
       float M[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) M[j] = -INFINITY;
-      for (int s = 0; s < p.pool; ++s) {
+#pragma unroll
+      for (int s = 0; s < pool; ++s) {
         const float4 *sc = reinterpret_cast<const float4 *>(p.slot_score + kbase + s * 128);
         const float4 *ap = reinterpret_cast<const float4 *>(p.ape + s * 128 + 16 * l8);
 #pragma unroll
@@ -87,7 +93,8 @@ __global__ void __launch_bounds__(256) kpool_write_kernel(const KpoolParams p, l
       float den[16], acc[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) den[j] = acc[j] = 0.f;
-      for (int s = 0; s < p.pool; ++s) {
+#pragma unroll
+      for (int s = 0; s < pool; ++s) {
         const float4 *sc = reinterpret_cast<const float4 *>(p.slot_score + kbase + s * 128);
         const float4 *ap = reinterpret_cast<const float4 *>(p.ape + s * 128 + 16 * l8);
         const uint4 *kr = reinterpret_cast<const uint4 *>(p.slot_k + kbase + s * 128);
@@ -380,6 +387,21 @@ bool take_flags_kpool(cudaStream_t stream, unsigned *host_word) {
 
 using namespace kvq;
 
+namespace kvq {
+template <int KP>
+static kvq_status launch_kpool_write(const KpoolParams &p, long long tiles, cudaStream_t s) {
+  static int per_sm = 0;  // resident CTAs per SM, from the occupancy calculator
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kpool_write_kernel<KP>, 256, 0) != cudaSuccess || n < 1) n = 1;
+    per_sm = n;
+  }
+  const long long cap = static_cast<long long>(sm_count() > 0 ? sm_count() : 1) * per_sm;
+  kpool_write_kernel<KP><<<static_cast<unsigned>(tiles < cap ? tiles : cap), 256, 0, s>>>(p, tiles);
+  return launch_status();
+}
+}  // namespace kvq
+
 extern "C" kvq_status kvq_kpool_write(uint8_t *kv_cache, const void *slot_k, const float *slot_score,
                                       const float *ape, const int64_t *loc, const uint8_t *write_mask,
                                       int64_t n_pools, int32_t pool_size, int32_t head_dim, int32_t page_size,
@@ -405,16 +427,11 @@ extern "C" kvq_status kvq_kpool_write(uint8_t *kv_cache, const void *slot_k, con
   p.num_blocks = num_blocks;
   p.round_scale = round_scale != 0;
   const long long tiles = (n_pools + 31) / 32;
-  static int per_sm = 0;
-  if (per_sm == 0) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kpool_write_kernel, 256, 0) != cudaSuccess || n < 1) n = 1;
-    per_sm = n;
+  switch (pool_size) {  // the common pool sizes unrolled
+    case 4: return launch_kpool_write<4>(p, tiles, reinterpret_cast<cudaStream_t>(stream));
+    case 2: return launch_kpool_write<2>(p, tiles, reinterpret_cast<cudaStream_t>(stream));
+    default: return launch_kpool_write<0>(p, tiles, reinterpret_cast<cudaStream_t>(stream));
   }
-  const long long cap = static_cast<long long>(sm_count() > 0 ? sm_count() : 1) * per_sm;
-  kpool_write_kernel<<<static_cast<unsigned>(tiles < cap ? tiles : cap), 256, 0,
-                       reinterpret_cast<cudaStream_t>(stream)>>>(p, tiles);
-  return launch_status();
 }
 
 extern "C" kvq_status kvq_kpool_seed_tail(void *tail, int64_t tail_block_stride, int64_t tail_half_stride,
