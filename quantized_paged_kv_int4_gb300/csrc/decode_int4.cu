@@ -56,8 +56,9 @@ struct Int4Params {
   float softcap2;       // USE_SOFTCAP: the cap in base-2 units (cap * log2 e), 0 = off
   float inv_softcap2;
   const float *alibi;   // USE_ALIBI_SLOPES: [Hq] slopes, or null
-  uint32_t *qfrag;      // single-token calls: the query fragments of rotate_q_int4_kernel
-                        // [B][Hk][QWORDS][32 lanes]; null in multi-token calls
+  uint32_t *qfrag;      // the query fragments of rotate_q_int4_kernel [B][Hk][QWORDS][32 lanes]
+                        // (B: the call's sequences, virtual ones in multi-token calls); null:
+                        // the split kernel rotates q itself
   unsigned long long wait_ns;  // limit of every bounded wait on a stage barrier
   int32_t withhold;     // error-path tests only: CTA (0, 0) never issues stage `withhold` (-1: none)
 };
@@ -405,11 +406,12 @@ __device__ __forceinline__ void load_frag(const Int4Params &p, uint8_t *qarea, i
   __syncwarp();
 }
 
-// Single-token decode: one warp per (sequence, kv head) rotates the query and builds its fp16 MMA
-// fragments (load_query) once, for every CTA that walks the sequence; the split kernel is launched
-// as its programmatic dependent, so the split kernel's setup and first page copies overlap this
-// kernel, and a piece change inside a CTA's run costs a 2.4 KB copy instead of a rotation.
-template <int D>
+// One warp per (sequence, kv head) -- virtual sequence in multi-token calls, whose MMA columns are
+// its query tokens' heads -- rotates the query and builds its fp16 MMA fragments (load_query) once,
+// for every CTA that walks the sequence; the split kernel is launched as its programmatic
+// dependent, so the split kernel's setup and first page copies overlap this kernel, and a piece
+// change inside a CTA's run costs a 2.4 KB copy instead of a rotation.
+template <int D, bool MTOK>
 __global__ void __launch_bounds__(256) rotate_q_int4_kernel(const __grid_constant__ Int4Params p) {
   using Gm = Int4Geom<D>;
   extern __shared__ __align__(16) uint8_t qsm[];
@@ -421,7 +423,7 @@ __global__ void __launch_bounds__(256) rotate_q_int4_kernel(const __grid_constan
   uint8_t *qarea = qsm + warp * Gm::QBYTES;
   uint32_t qf[D / 16][2];
   float qs0, qs1, qmul;
-  load_query<D, false>(p, qarea, b, h, lane, qf, qs0, qs1, qmul, false);
+  load_query<D, MTOK>(p, qarea, b, h, lane, qf, qs0, qs1, qmul, false);
   uint32_t *dst = p.qfrag + gw * Gm::QWORDS * 32 + lane;
 #pragma unroll
   for (int k = 0; k < D / 16; ++k) {
@@ -897,7 +899,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   // after the first page copies are out (waiting for that kernel must not delay them)
   uint8_t *qarea = kvq_dsmem + base + NS * Gm::STAGE + warp * Gm::QBYTES;
   int q_prefetched = -1;  // sequence whose query rows / fragments are being copied
-  const bool pre_rotated = !MTOK && p.qfrag != nullptr;
+  const bool pre_rotated = p.qfrag != nullptr;
   auto prefetch_first = [&]() {
     if (sub >= run.n) return;
     SeqCursor c0 = run.first;
@@ -1022,7 +1024,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     }
     if (!have_q) {
       float qmul;
-      if (!MTOK && p.qfrag != nullptr) {
+      if (pre_rotated) {
         if (q_prefetched != cur.b) asm volatile("griddepcontrol.wait;" ::: "memory");
         load_frag<D>(p, qarea, cur.b, h, lane, qf, qs0, qs1, qmul, q_prefetched == cur.b);
       } else {
@@ -1046,7 +1048,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
         SeqCursor nx = cur;
         seq_next<MODS>(a, nx);
         if (nx.b < a.B) {
-          if (!MTOK && p.qfrag != nullptr) {
+          if (pre_rotated) {
             asm volatile("griddepcontrol.wait;" ::: "memory");
             fetch_frag<D>(p, qarea, nx.b, h, lane);
           } else {
@@ -1134,9 +1136,13 @@ static kvq_status launch_int4_w(const Int4Params &p, const SplitPlan &plan, cuda
   if (ensure_dynamic_smem(decode_int4_kernel<D, kStagesInt4, W, VAR>, smem, attr_done) != cudaSuccess)
     return KVQ_ERR_CUDA;
   const dim3 grid(plan.seg_ctas, plan.head_groups);
-  if ((VAR == 0 || VAR == 3 || VAR == 4) && p.qfrag != nullptr) {  // single token: query pre-rotation, then the split kernel
+  if (p.qfrag != nullptr) {  // query pre-rotation, then the split kernel as its dependent
+    constexpr bool MTOK = VAR == 1 || VAR == 2;
     const long long warps = static_cast<long long>(p.s.B) * p.s.Hk;
-    rotate_q_int4_kernel<D><<<static_cast<unsigned>((warps + 7) / 8), 256, 8 * Int4Geom<D>::QBYTES, s>>>(p);
+    static size_t rot_done[kMaxDevices] = {};
+    if (ensure_dynamic_smem(rotate_q_int4_kernel<D, MTOK>, 8 * Int4Geom<D>::QBYTES, rot_done) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+    rotate_q_int4_kernel<D, MTOK><<<static_cast<unsigned>((warps + 7) / 8), 256, 8 * Int4Geom<D>::QBYTES, s>>>(p);
     if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
     if (launch_dependent(decode_int4_kernel<D, kStagesInt4, W, VAR>, grid, dim3(256), s, p, smem) != cudaSuccess)
       return KVQ_ERR_CUDA;
@@ -1252,7 +1258,9 @@ static size_t mods_workspace_bytes(int B, int Hq, int Hk, int D, int num_splits,
   if (!call_geom(B, Hq, Hk, mods, g)) return 0;
   if (!make_plan(static_cast<int>(g->nseq), Hk, num_splits, plan)) return 0;
   const size_t ws = workspace_bytes(static_cast<int>(g->nseq), g->QB * Hq, D, *plan);
-  return ws + (g->mtok ? round256(static_cast<size_t>(g->nseq) * sizeof(int4)) : qfrag_bytes(B, Hk, D));
+  // multi-token calls: the virtual-sequence list, then the query fragments of every virtual sequence
+  return ws + (g->mtok ? round256(static_cast<size_t>(g->nseq) * sizeof(int4)) : 0) +
+         qfrag_bytes(static_cast<int>(g->nseq), Hk, D);
 }
 
 }  // namespace kvq
@@ -1325,9 +1333,8 @@ extern "C" kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache
   int4 *vseq = cg.mtok ? reinterpret_cast<int4 *>(static_cast<uint8_t *>(workspace) +
                                                   kvq::workspace_bytes(nseq, cg.QB * Hq, D, plan))
                        : nullptr;
-  p.qfrag = cg.mtok ? nullptr
-                     : reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) +
-                                                    kvq::workspace_bytes(nseq, cg.QB * Hq, D, plan));
+  p.qfrag = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) + kvq::workspace_bytes(nseq, cg.QB * Hq, D, plan) +
+                                         (cg.mtok ? round256(static_cast<size_t>(nseq) * sizeof(int4)) : 0));
   sa.vseq = vseq;
   sa.signs = rht_signs;
   sa.out = out;
