@@ -57,8 +57,7 @@ struct Int4Params {
   float inv_softcap2;
   const float *alibi;   // USE_ALIBI_SLOPES: [Hq] slopes, or null
   uint32_t *qfrag;      // the query fragments of rotate_q_int4_kernel [B][Hk][QWORDS][32 lanes]
-                        // (B: the call's sequences, virtual ones in multi-token calls); null:
-                        // the split kernel rotates q itself
+                        // (B: the call's sequences, virtual ones in multi-token calls)
   unsigned long long wait_ns;  // limit of every bounded wait on a stage barrier
   int32_t withhold;     // error-path tests only: CTA (0, 0) never issues stage `withhold` (-1: none)
 };
@@ -894,27 +893,20 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
       }
     }
   };
-  // the first piece's query: raw rows (rotated here) go out before any page copy, so they do not
-  // queue behind the launch-time burst of page copies; the pre-kernel's fragments are fetched
-  // after the first page copies are out (waiting for that kernel must not delay them)
+  // the first piece's query fragments (written by the pre-kernel) are fetched after the first
+  // page copies are out: waiting for that kernel must not delay them
   uint8_t *qarea = kvq_dsmem + base + NS * Gm::STAGE + warp * Gm::QBYTES;
-  int q_prefetched = -1;  // sequence whose query rows / fragments are being copied
-  const bool pre_rotated = p.qfrag != nullptr;
+  int q_prefetched = -1;  // sequence whose query fragments are being copied
   auto prefetch_first = [&]() {
     if (sub >= run.n) return;
     SeqCursor c0 = run.first;
     const long long X0 = run.base + sub;
     while (X0 >= c0.P + c0.np && c0.b < a.B) seq_next<MODS>(a, c0);
     if (c0.b >= a.B) return;
-    if (pre_rotated) {
-      asm volatile("griddepcontrol.wait;" ::: "memory");  // the fragments of the pre-kernel
-      fetch_frag<D>(p, qarea, c0.b, h, lane);
-    } else {
-      fetch_query<D, MTOK>(p, qarea, c0.b, h, lane);
-    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the fragments of the pre-kernel
+    fetch_frag<D>(p, qarea, c0.b, h, lane);
     q_prefetched = c0.b;
   };
-  if (!pre_rotated) prefetch_first();
   int cb = 0;        // warp 0: the batch of block ids its consumption has reached
   bool rest = false;  // warp 0: stages 2 .. NS - 1 issued
   if (warp == 0) {
@@ -927,7 +919,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     for (int k = 0; k < 2 && k < n_stages; ++k) issue(k, k);
   }
   __syncthreads();  // barrier init and the first block ids, before any other warp can refill
-  if (pre_rotated) prefetch_first();
+  prefetch_first();
   // A slot is refilled by the last warp done with it (the shared counter's old value is 7 mod 8):
   // no warp waits for another to notice the slot is free.
   auto release = [&](int k, int slot) {
@@ -1024,12 +1016,8 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
     }
     if (!have_q) {
       float qmul;
-      if (pre_rotated) {
-        if (q_prefetched != cur.b) asm volatile("griddepcontrol.wait;" ::: "memory");
-        load_frag<D>(p, qarea, cur.b, h, lane, qf, qs0, qs1, qmul, q_prefetched == cur.b);
-      } else {
-        load_query<D, MTOK>(p, qarea, cur.b, h, lane, qf, qs0, qs1, qmul, q_prefetched == cur.b);
-      }
+      if (q_prefetched != cur.b) asm volatile("griddepcontrol.wait;" ::: "memory");
+      load_frag<D>(p, qarea, cur.b, h, lane, qf, qs0, qs1, qmul, q_prefetched == cur.b);
       sm24 = p.sm_log2 * kTwo24 * qmul;
       if constexpr (COMB) {  // columns 4..7 repeat columns 0..3 (lane l + 16 holds column n + 4)
 #pragma unroll
@@ -1048,12 +1036,8 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
         SeqCursor nx = cur;
         seq_next<MODS>(a, nx);
         if (nx.b < a.B) {
-          if (pre_rotated) {
-            asm volatile("griddepcontrol.wait;" ::: "memory");
-            fetch_frag<D>(p, qarea, nx.b, h, lane);
-          } else {
-            fetch_query<D, MTOK>(p, qarea, nx.b, h, lane);
-          }
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          fetch_frag<D>(p, qarea, nx.b, h, lane);
           q_prefetched = nx.b;
         }
       }
@@ -1136,20 +1120,16 @@ static kvq_status launch_int4_w(const Int4Params &p, const SplitPlan &plan, cuda
   if (ensure_dynamic_smem(decode_int4_kernel<D, kStagesInt4, W, VAR>, smem, attr_done) != cudaSuccess)
     return KVQ_ERR_CUDA;
   const dim3 grid(plan.seg_ctas, plan.head_groups);
-  if (p.qfrag != nullptr) {  // query pre-rotation, then the split kernel as its dependent
-    constexpr bool MTOK = VAR == 1 || VAR == 2;
-    const long long warps = static_cast<long long>(p.s.B) * p.s.Hk;
-    static size_t rot_done[kMaxDevices] = {};
-    if (ensure_dynamic_smem(rotate_q_int4_kernel<D, MTOK>, 8 * Int4Geom<D>::QBYTES, rot_done) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-    rotate_q_int4_kernel<D, MTOK><<<static_cast<unsigned>((warps + 7) / 8), 256, 8 * Int4Geom<D>::QBYTES, s>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
-    if (launch_dependent(decode_int4_kernel<D, kStagesInt4, W, VAR>, grid, dim3(256), s, p, smem) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-  } else {
-    decode_int4_kernel<D, kStagesInt4, W, VAR><<<grid, 256, smem, s>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
-  }
+  // query pre-rotation, then the split kernel as its programmatic dependent
+  constexpr bool MTOK = VAR == 1 || VAR == 2;
+  const long long warps = static_cast<long long>(p.s.B) * p.s.Hk;
+  static size_t rot_done[kMaxDevices] = {};
+  if (ensure_dynamic_smem(rotate_q_int4_kernel<D, MTOK>, 8 * Int4Geom<D>::QBYTES, rot_done) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  rotate_q_int4_kernel<D, MTOK><<<static_cast<unsigned>((warps + 7) / 8), 256, 8 * Int4Geom<D>::QBYTES, s>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  if (launch_dependent(decode_int4_kernel<D, kStagesInt4, W, VAR>, grid, dim3(256), s, p, smem) != cudaSuccess)
+    return KVQ_ERR_CUDA;
   const long long rows = static_cast<long long>(p.s.B) * p.s.Hq;
   if (launch_dependent(merge_kernel<D>, dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), s, p.s) != cudaSuccess)
     return KVQ_ERR_CUDA;
