@@ -703,7 +703,7 @@ __device__ __forceinline__ void int4_pages(PieceState<D> &st, const uint32_t (&s
     ml0 = fmaxf(ml0, fmaxf(pg[i].s[0], pg[i].s[2]));
     ml1 = fmaxf(ml1, fmaxf(pg[i].s[1], pg[i].s[3]));
   }
-  if (__any_sync(FULL, ml0 > st.m0 + kScoreCap || ml1 > st.m1 + kScoreCap || fmaxf(wm0, wm1) > kWeightHi)) {
+  if (__builtin_expect(__any_sync(FULL, ml0 > st.m0 + kScoreCap || ml1 > st.m1 + kScoreCap || fmaxf(wm0, wm1) > kWeightHi), 0)) {
     // every lane takes part in every reduction (no shuffle inside a conditional expression)
     const float ms0 = warp_max_g(ml0), ms1 = warp_max_g(ml1);
     const float wc0 = warp_max_g(wm0), wc1 = warp_max_g(wm1);
@@ -993,7 +993,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   // the flag, let the copies already issued land (bounded), and report failure
   auto wait_stage = [&](int k, int slot, int rnd) -> bool {
     const uint32_t fb = smem_u32(&s_full[slot]);
-    if (__all_sync(FULL, mbar_try_wait(fb, rnd & 1))) return true;
+    if (__builtin_expect(__all_sync(FULL, mbar_try_wait(fb, rnd & 1)), 1)) return true;
     if (__all_sync(FULL, mbar_wait(fb, rnd & 1, p.wait_ns))) return true;
     if (lane == 0) atomicOr(&g_flags_decode_int4, ERR_TIMEOUT);
     for (int i = k; i < k + NS && i < n_stages; ++i)
@@ -1053,7 +1053,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
       cb = ((j * W) >> 5) + 1;
       store_batch(cb + 1);
     }
-    if (pair) {
+    if (__builtin_expect(pair, 1)) {
       if (!wait_stage(j, sj, rj) || !wait_stage(j + 1, sj1, rj1)) {
         abort = true;
         break;
