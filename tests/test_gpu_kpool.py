@@ -31,7 +31,7 @@ def _both(n, pool, ps, seed, round_scale=True, mask=None, loc_override=None):
     return g.cpu().numpy(), ref, st, flags
 
 
-@pytest.mark.parametrize("pool", [1, 4, 7, 16])
+@pytest.mark.parametrize("pool", [1, 2, 4, 7, 16])  # 2 and 4: the unrolled kernels
 @pytest.mark.parametrize("round_scale", [True, False])
 def test_bit_exact(pool, round_scale):
     got, ref, st, flags = _both(333, pool, 16, seed=pool, round_scale=round_scale)
