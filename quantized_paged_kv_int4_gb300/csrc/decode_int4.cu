@@ -27,14 +27,15 @@
 //   * S^T[16 tokens x 8 heads] = K[16 x D] . Q^T  (q of a high-nibble dim pre-divided by 16);
 //   * O^T[D x 8 heads] += V^T[D x 16 tokens] . P_v^T with P_v = 2^(S - m) * scale_v in fp16, m a
 //     per-column softmax reference kept so that P_v stays inside fp16 for any value scale
-//     (decode_common.cuh); the tokens (the K dimension) and the D rows are permuted so that a
-//     lane's V bytes become A fragments with one PRMT per pair of m-tiles.
+//     (decode_common.cuh); the V^T fragments come from ldmatrix.x4.trans.
 // q enters as fp16 times a per-(sequence, kv head) power of two 2^-k (so no element can overflow),
-// and 2^k joins the score scale. In single-token calls a pre-kernel rotates q and builds these
-// fragments once per (sequence, kv head); the split kernel, its programmatic dependent, sets up
-// its run and issues its first page copies meanwhile and then copies the fragments (2.4 KB) at
-// each piece start. Multi-token calls rotate in the split kernel.
-// The G query heads of a kv head share every K/V byte loaded (GQA), padded to the MMA's N = 8.
+// and 2^k joins the score scale. A pre-kernel rotates q and builds these fragments once per
+// (sequence, kv head) -- per virtual sequence in multi-token calls; the split kernel, its
+// programmatic dependent, sets up its run and issues its first page copies meanwhile and then
+// copies the fragments (2.4 KB) at each piece start.
+// The G query heads of a kv head share every K/V byte loaded (GQA); with G <= 4 in single-token
+// calls the MMA's other columns score a second page (combined columns, int4_pages), otherwise
+// the columns past G are padding.
 
 #include <atomic>
 #include <mutex>
