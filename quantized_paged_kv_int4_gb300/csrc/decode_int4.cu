@@ -841,6 +841,13 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   const int h0 = blockIdx.y * HB, h = h0 + hl;
   const bool split_heads = a.Hk > 8;
 
+  {  // pull the block table into L2 while the run is planned (each CTA a slice of 128-byte lines)
+    const long long bytes = static_cast<long long>(a.B) * a.max_blocks * 4;
+    const long long lines = (bytes + 127) / 128, per = (lines + gridDim.x - 1) / gridDim.x;
+    const long long l0 = static_cast<long long>(blockIdx.x) * per;
+    for (long long l = l0 + threadIdx.x; l < l0 + per && l < lines; l += blockDim.x)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(p.block_table) + l * 128));
+  }
   PageRun run;
   if (!page_run<MODS>(a, &g_flags_decode_int4, &run)) return;  // uniform over the CTA
   const int n_stages = (run.n + W - 1) / W;
