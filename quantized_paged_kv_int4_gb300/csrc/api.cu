@@ -139,6 +139,48 @@ bool int4_tensor_maps(const void *k_cache, const void *v_cache, const void *k_sc
   return true;
 }
 
+bool tq_tensor_map(const void *cache, long long num_blocks, int Hk, int slot_bytes, int row_bytes, CUtensorMap *map) {
+  struct Entry {
+    const void *c;
+    long long nb;
+    int hk, sb, rb;
+    CUtensorMap map;
+  };
+  static std::mutex mu;
+  static Entry entries[16];
+  static int n_cached = 0, next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_cached; ++i) {
+    const Entry &e = entries[i];
+    if (e.c == cache && e.nb == num_blocks && e.hk == Hk && e.sb == slot_bytes && e.rb == row_bytes) {
+      *map = e.map;
+      return true;
+    }
+  }
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_tiled();
+  if (enc == nullptr) return false;
+  const cuuint64_t sb = static_cast<cuuint64_t>(slot_bytes);
+  const cuuint64_t dim[4] = {sb, 16, static_cast<cuuint64_t>(Hk), static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t stride[3] = {sb * Hk, sb, sb * Hk * 16};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(row_bytes), 16, 1, 1};
+  const cuuint32_t ones[4] = {1, 1, 1, 1};
+  CUtensorMap m;
+  if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(cache), dim, stride, box, ones,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  Entry &e = entries[next];
+  e.c = cache;
+  e.nb = num_blocks;
+  e.hk = Hk;
+  e.sb = slot_bytes;
+  e.rb = row_bytes;
+  e.map = m;
+  next = (next + 1) % 16;
+  if (n_cached < 16) ++n_cached;
+  *map = m;
+  return true;
+}
 
 size_t workspace_bytes(int B, int Hq, int D, const SplitPlan &plan) {
   const size_t rows = static_cast<size_t>(plan.slots) * plan.warps_per_head * Hq;

@@ -7,12 +7,15 @@
 // byte d / 2, high nibble for odd d; 3-bit: LSB-first stream); an online softmax accumulates
 // acc / l and lse per split, and the splits are merged by log-sum-exp (decode_common.cuh).
 //
-// GB300 design: the INT4 kernel's structure (one warp per kv head and run of pages, private
-// cp.async ring, mma.m16n8k16 for both contractions, separate merge kernel). Keys go to
-// fp16 with the hardware E4M3x2 -> f16x2 conversion (exact); q (fp32, shifted by a power of two
-// into the fp16 range, decode_common.cuh) is split into fp16 hi + lo parts, two MMAs per k-step,
-// so the score keeps ~22 bits. Value indices enter as exact fp16 subnormals (the index bits
-// masked into a zero-exponent fp16: idx * 2^-24, or idx * 2^-20 for a high nibble) weighted by
+// GB300 design: one warp per kv head and run of pages (the split of decode_common.cuh), each warp
+// with its own ring of page tiles brought by the tensor-memory accelerator: one 4-D box per
+// (page, kv head) lands the 16 slots' used bytes as [token][row] rows (no per-lane copies), and an
+// mbarrier per ring slot says when it has landed; mma.m16n8k16 for both contractions, separate
+// merge kernel. Keys go to fp16 with the hardware E4M3x2 -> f16x2 conversion (exact); q (fp32,
+// shifted by a power of two into the fp16 range, decode_common.cuh) is split into fp16 hi + lo
+// parts, two MMAs per k-step, so the score keeps ~22 bits; the lanes build their q fragments from
+// global memory directly. Value indices enter as exact fp16 subnormals (the index bits masked into
+// a zero-exponent fp16: idx * 2^-24, or idx * 2^-20 for a high nibble) weighted by
 // P_v = 2^(S - m) * scale in fp16 against a per-column softmax reference m that keeps P_v inside
 // fp16 (decode_common.cuh); the power of two is undone in the epilogue and sum_n p_n * zero_n is
 // added in fp32.
@@ -26,10 +29,9 @@ __device__ unsigned g_flags_decode_tq = 0;
 
 struct TqParams {
   SplitArgs s;
+  CUtensorMap map;  // the slot pool as {slot_bytes, 16, Hk, num_blocks}, box {row bytes, 16, 1, 1}
   const float *q;
-  const uint8_t *cache;
   const int32_t *block_table;
-  int32_t slot_bytes;
   float sc_log2;  // attn_scale * log2(e)
   int64_t num_blocks;
 };
@@ -40,15 +42,13 @@ constexpr uint32_t kHiTq = 0x00F000F0u;  // high nibbles -> idx * 2^-20
 template <int D, int VBITS>
 struct TqGeom {
   static constexpr int KCH = D / 4;             // K bytes per lane per row
-  static constexpr int KCHUNKS = KCH / 16;      // 16-byte copies per row
-  static constexpr int KB = 2 * 32 * KCH;       // two rows
+  static constexpr int KCHUNKS = KCH / 16;      // 16-byte reads per row
   static constexpr int VDB = (D * VBITS + 7) / 8;
-  static constexpr int VCH = VBITS == 4 ? D / 16 : 8;  // bytes per lane per token in the ring
-  static constexpr int VB = 4 * 32 * VCH;
-  static constexpr int STAGE = KB + VB + 128;
+  static constexpr int RB = (D + VDB + 4 + 15) / 16 * 16;  // staged bytes of a slot: key, values, scale, zero
+  static constexpr int TILE = kPage * RB;       // one (page, kv head) tile: 16 rows
+  static constexpr int VCH = D / 16;            // 4-bit values: bytes per lane per token
   static constexpr int KSTEPS = D / 16;
   static constexpr int MT = D / 16;
-  static constexpr int QBYTES = 2 * 8 * D * 2;  // fp16 hi and lo
 };
 
 __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two_bytes) {
@@ -56,17 +56,26 @@ __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two_bytes) {
   return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
 }
 
+// Per-warp ring state carried from piece to piece: tiles issued so far (ring slot and mbarrier
+// phase of tile K are K % NSTAGE and (K / NSTAGE) & 1), and whether a wait ran out.
+struct TqRing {
+  const uint8_t *ring_p;  // the warp's first ring slot
+  uint32_t ring;  // its shared-window address
+  uint32_t bar;   // shared address of its first mbarrier (8 bytes each)
+  uint32_t used;
+  bool failed;
+};
+
 // PACKQ (G <= 4): the q hi parts of the G heads fill MMA columns 0..3 and the lo parts columns
 // 4..7, so one MMA per k-step yields both halves of every score (added across lanes t, t ^ 2);
 // otherwise hi and lo take one MMA each.
 template <int D, int VBITS, int NSTAGE, bool PACKQ>
-__device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8_t *qarea, int b,
-                                         int h, int sub, int t0, int t1, long long slot) {
+__device__ __forceinline__ void tq_piece(const TqParams &p, TqRing &rg, int b, int h, int sub, int t0, int t1,
+                                         long long slot) {
   using Gm = TqGeom<D, VBITS>;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int G = p.s.G, WPH = p.s.warps_per_head, Hk = p.s.Hk;
-  const int SB = p.slot_bytes;
+  const int G = p.s.G, WPH = p.s.warps_per_head;
 
   const int pg0 = t0 / kPage, pglast = (t1 - 1) / kPage;
   const int first = pg0 + sub;
@@ -78,98 +87,81 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
   };
   int bids_cur = load_bids(0);
   int bids_next = load_bids(1);
-
-  // -------- query -> fp16 hi / lo parts (of q * 2^-k) in shared memory, then B fragments
-  float sc2;  // score scale of the piece: attn_scale * log2 e * 2^k
-  {
-    constexpr int J = D / 32;
-    const float *qb = p.q + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(h) * G) * D;
-    float qmax = 0.f;
-    for (int n = 0; n < G; ++n) {
-#pragma unroll
-      for (int j = 0; j < J; ++j) qmax = fmaxf(qmax, fabsf(qb[n * D + lane + 32 * j]));
-    }
-    const int qk = query_shift(warp_max(qmax), 0, &g_flags_decode_tq);
-    const float qdiv = pow2i(-qk);
-    sc2 = p.sc_log2 * pow2i(qk);
-    __half *qh = reinterpret_cast<__half *>(qarea);
-    for (int n = 0; n < 8; ++n) {
-#pragma unroll
-      for (int j = 0; j < J; ++j) {
-        const int e = lane + 32 * j;
-        const int head = PACKQ ? (n & 3) : n;
-        const float x = head < G ? qb[head * D + e] * qdiv : 0.f;
-        const __half hi = __float2half_rn(x);
-        const __half lo = __float2half_rn(x - __half2float(hi));
-        if constexpr (PACKQ) {
-          qh[n * D + e] = n < 4 ? hi : lo;
-        } else {
-          qh[n * D + e] = hi;
-          qh[8 * D + n * D + e] = lo;
-        }
-      }
-    }
-  }
-  __syncwarp();
-  uint32_t qhi[Gm::KSTEPS][2], qlo[PACKQ ? 1 : Gm::KSTEPS][2];
-  {
-    const __half *qh = reinterpret_cast<const __half *>(qarea) + g * D + t * Gm::KCH;
-#pragma unroll
-    for (int ks = 0; ks < Gm::KSTEPS; ++ks) {
-      const __half *r = qh + 4 * ks;
-      qhi[ks][0] = h2_as_u32(__halves2half2(r[0], r[1]));
-      qhi[ks][1] = h2_as_u32(__halves2half2(r[2], r[3]));
-      if constexpr (!PACKQ) {
-        qlo[ks][0] = h2_as_u32(__halves2half2(r[8 * D + 0], r[8 * D + 1]));
-        qlo[ks][1] = h2_as_u32(__halves2half2(r[8 * D + 2], r[8 * D + 3]));
-      }
-    }
-  }
-  __syncwarp();
-
-  const uint32_t ring_s = smem_u32(ring);
-  const long long row_stride = static_cast<long long>(Hk) * SB;
-  const long long page_bytes = kPage * row_stride;
-  // 3-bit: the lane's D/8 indices start at bit 3 * (D/8) * g of the value bytes
-  constexpr int kV3Bytes = 3 * D / 64;  // bytes per lane (6 at D = 128, 3 at D = 64)
-  const int v3_off = D + kV3Bytes * g;
-  const int v3_al = v3_off & ~3;
-  const uint8_t *head = p.cache + static_cast<long long>(h) * SB;
+  const uint32_t K0 = rg.used;  // this piece's tile k is ring tile K0 + k
+  // tile k of the piece into its ring slot: lane 0 arms the slot's mbarrier with the tile's bytes
+  // and starts the box copy (the warp has finished reading the slot: __syncwarp before the call)
   auto issue = [&](int k) {
+    if (k >= n_my) return;
     const int kk = k & 31;
     if (k > 0 && kk == 0) {
       bids_cur = bids_next;
       bids_next = load_bids((k >> 5) + 1);
     }
     const int blk = __shfl_sync(FULL, bids_cur, kk);
-    const bool in = k < n_my;
-    const bool ok = in && blk >= 0 && blk < p.num_blocks;
-    if (in && !ok && lane == 0) atomicOr(&g_flags_decode_tq, ERR_BLOCK);
-    const uint32_t st = ring_s + (k % NSTAGE) * Gm::STAGE;
-    const uint8_t *base = head + static_cast<long long>(ok ? blk : 0) * page_bytes;
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-#pragma unroll
-      for (int c = 0; c < Gm::KCHUNKS; ++c) {
-        cp_async<16>(st + ((r * Gm::KCHUNKS + c) * 32 + lane) * 16,
-                     base + (g + 8 * r) * row_stride + t * Gm::KCH + 16 * c, ok);
-      }
+    if (lane == 0) {
+      const bool ok = blk >= 0 && blk < p.num_blocks;
+      if (!ok) atomicOr(&g_flags_decode_tq, ERR_BLOCK);
+      const uint32_t sl = (K0 + k) % NSTAGE;
+      const uint32_t bar = rg.bar + 8 * sl;
+      fence_proxy_async();  // earlier reads of the slot come before the copy that refills it
+      mbar_arrive_expect_tx(bar, Gm::TILE);
+      tma_load_4d(rg.ring + sl * Gm::TILE, &p.map, 0, 0, h, ok ? blk : 0, bar);
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int tok = 2 * t + (i & 1) + 8 * (i >> 1);
-      const uint8_t *row = base + tok * row_stride;
-      const uint32_t dst = st + Gm::KB + (i * 32 + lane) * Gm::VCH;
-      if constexpr (VBITS == 4) {
-        cp_async<Gm::VCH>(dst, row + D + g * Gm::VCH, ok);
-      } else {
-        cp_async<4>(dst, row + v3_al, ok);
-        cp_async<4>(dst + 4, row + v3_al + 4, ok);
-      }
-    }
-    cp_async<4>(st + Gm::KB + Gm::VB + lane * 4, base + (lane & 15) * row_stride + D + Gm::VDB, ok);
-    cp_async_commit();
   };
+#pragma unroll
+  for (int k = 0; k < NSTAGE - 1; ++k) issue(k);
+
+  // -------- q -> fp16 hi / lo B fragments, straight from global memory: lane (g, t) holds column
+  // g (head g, or PACKQ: head g % 4, its hi part for g < 4 and its lo part for g >= 4) at the
+  // dims 32 t .. 32 t + 31 (D = 128) its K reads cover, k-step ks taking dims KCH t + 4 ks .. + 3
+  float sc2;  // score scale of the piece: attn_scale * log2 e * 2^k
+  uint32_t qhi[Gm::KSTEPS][2], qlo[PACKQ ? 1 : Gm::KSTEPS][2];
+  {
+    const int head = PACKQ ? (g & 3) : g;
+    const bool live = head < G;
+    const float4 *src = reinterpret_cast<const float4 *>(
+        p.q + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(h) * G + (live ? head : 0)) * D + t * Gm::KCH);
+    float qv[Gm::KCH];
+#pragma unroll
+    for (int j = 0; j < Gm::KCH / 4; ++j) {
+      const float4 v = live ? __ldg(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      qv[4 * j] = v.x;
+      qv[4 * j + 1] = v.y;
+      qv[4 * j + 2] = v.z;
+      qv[4 * j + 3] = v.w;
+    }
+    float qmax = 0.f;
+#pragma unroll
+    for (int j = 0; j < Gm::KCH; ++j) qmax = fmaxf(qmax, fabsf(qv[j]));
+    const int qk = query_shift(warp_max(qmax), 0, &g_flags_decode_tq);
+    const float qdiv = pow2i(-qk);
+    sc2 = p.sc_log2 * pow2i(qk);
+#pragma unroll
+    for (int ks = 0; ks < Gm::KSTEPS; ++ks) {
+      __half hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x = qv[4 * ks + e] * qdiv;
+        hi[e] = __float2half_rn(x);
+        lo[e] = __float2half_rn(x - __half2float(hi[e]));
+      }
+      if constexpr (PACKQ) {
+        const bool use_lo = g >= 4;
+        qhi[ks][0] = h2_as_u32(use_lo ? __halves2half2(lo[0], lo[1]) : __halves2half2(hi[0], hi[1]));
+        qhi[ks][1] = h2_as_u32(use_lo ? __halves2half2(lo[2], lo[3]) : __halves2half2(hi[2], hi[3]));
+      } else {
+        qhi[ks][0] = h2_as_u32(__halves2half2(hi[0], hi[1]));
+        qhi[ks][1] = h2_as_u32(__halves2half2(hi[2], hi[3]));
+        qlo[ks][0] = h2_as_u32(__halves2half2(lo[0], lo[1]));
+        qlo[ks][1] = h2_as_u32(__halves2half2(lo[2], lo[3]));
+      }
+    }
+  }
+
+  // 3-bit: the lane's D/8 indices per token start at bit 3 * (D/8) * g of the value bytes
+  constexpr int kV3Bytes = 3 * D / 64;  // bytes per lane (6 at D = 128, 3 at D = 64)
+  const int v3_off = D + kV3Bytes * g;
+  const int v3_al = v3_off & ~3;
 
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   float pz0 = 0.f, pz1 = 0.f;
@@ -177,23 +169,29 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
 #pragma unroll
   for (int i = 0; i < Gm::MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
-#pragma unroll
-  for (int k = 0; k < NSTAGE - 1; ++k) issue(k);
-
-  for (int k = 0; k < n_my; ++k) {
+  int k = 0;
+  for (; k < n_my; ++k) {
     issue(k + NSTAGE - 1);
-    cp_async_wait<NSTAGE - 1>();
-    __syncwarp();
-    const uint8_t *st = ring + (k % NSTAGE) * Gm::STAGE;
+    {
+      const uint32_t K = K0 + k;
+      const uint32_t bar = rg.bar + 8 * (K % NSTAGE), par = (K / NSTAGE) & 1;
+      if (!__all_sync(FULL, mbar_try_wait(bar, par)) && !__all_sync(FULL, mbar_wait(bar, par))) {
+        if (lane == 0) atomicOr(&g_flags_decode_tq, ERR_TIMEOUT);
+        rg.failed = true;
+        break;
+      }
+    }
+    const uint8_t *st = rg.ring_p + ((K0 + k) % NSTAGE) * Gm::TILE;
     const int nb = (first + k * WPH) * kPage;
     const bool ok0 = nb + g >= t0 && nb + g < t1;
     const bool ok1 = nb + g + 8 >= t0 && nb + g + 8 < t1;
+    const uint8_t *row0 = st + g * Gm::RB, *row1 = st + (g + 8) * Gm::RB;
 
     float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ch = 0; ch < Gm::KCHUNKS; ++ch) {
-      const uint4 ra = lds128(st + (ch * 32 + lane) * 16);
-      const uint4 rb = lds128(st + ((Gm::KCHUNKS + ch) * 32 + lane) * 16);
+      const uint4 ra = lds128(row0 + t * Gm::KCH + 16 * ch);
+      const uint4 rb = lds128(row1 + t * Gm::KCH + 16 * ch);
       const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -212,8 +210,7 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
 #pragma unroll
       for (int i = 0; i < 4; ++i) c[i] += __shfl_xor_sync(FULL, c[i], 2);  // hi (t < 2) + lo (t >= 2)
     }
-    const uint8_t *sb = st + Gm::KB + Gm::VB;
-    const uint32_t sz0 = lds32(sb + g * 4), sz1 = lds32(sb + (g + 8) * 4);
+    const uint32_t sz0 = lds32(row0 + D + Gm::VDB), sz1 = lds32(row1 + D + Gm::VDB);
     const float s00 = ok0 ? c[0] * sc2 : -INFINITY;
     const float s01 = ok0 ? c[1] * sc2 : -INFINITY;
     const float s10 = ok1 ? c[2] * sc2 : -INFINITY;
@@ -280,16 +277,17 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
     if constexpr (VBITS == 4) {
       constexpr int VW = Gm::VCH / 4;
       uint32_t va[VW], vb[VW], vc[VW], vd[VW];
+      const uint8_t *vr = st + D + g * Gm::VCH;  // tokens 2t, 2t + 1, 2t + 8, 2t + 9: the lane's dims 16 g ..
       if constexpr (VW == 2) {
-        const uint2 A = lds64(st + Gm::KB + lane * 8), B2 = lds64(st + Gm::KB + (32 + lane) * 8);
-        const uint2 C = lds64(st + Gm::KB + (64 + lane) * 8), E = lds64(st + Gm::KB + (96 + lane) * 8);
+        const uint2 A = lds64(vr + (2 * t) * Gm::RB), B2 = lds64(vr + (2 * t + 1) * Gm::RB);
+        const uint2 C = lds64(vr + (2 * t + 8) * Gm::RB), E = lds64(vr + (2 * t + 9) * Gm::RB);
         va[0] = A.x; va[1] = A.y; vb[0] = B2.x; vb[1] = B2.y;
         vc[0] = C.x; vc[1] = C.y; vd[0] = E.x; vd[1] = E.y;
       } else {
-        va[0] = lds32(st + Gm::KB + lane * 4);
-        vb[0] = lds32(st + Gm::KB + (32 + lane) * 4);
-        vc[0] = lds32(st + Gm::KB + (64 + lane) * 4);
-        vd[0] = lds32(st + Gm::KB + (96 + lane) * 4);
+        va[0] = lds32(vr + (2 * t) * Gm::RB);
+        vb[0] = lds32(vr + (2 * t + 1) * Gm::RB);
+        vc[0] = lds32(vr + (2 * t + 8) * Gm::RB);
+        vd[0] = lds32(vr + (2 * t + 9) * Gm::RB);
       }
 #pragma unroll
       for (int wi = 0; wi < VW; ++wi) {
@@ -308,9 +306,9 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
       const int sh = 8 * (v3_off - v3_al);
       unsigned long long w[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint2 r = lds64(st + Gm::KB + (i * 32 + lane) * 8);
-        w[i] = ((static_cast<unsigned long long>(r.y) << 32) | r.x) >> sh;
+      for (int i = 0; i < 4; ++i) {  // tokens 2t, 2t + 1, 2t + 8, 2t + 9
+        const uint8_t *r = st + (2 * t + (i & 1) + 8 * (i >> 1)) * Gm::RB + v3_al;
+        w[i] = ((static_cast<unsigned long long>(lds32(r + 4)) << 32) | lds32(r)) >> sh;
       }
 #pragma unroll
       for (int mt = 0; mt < Gm::MT; ++mt) {
@@ -330,8 +328,14 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
     }
     __syncwarp();
   }
-  cp_async_wait<0>();
-  __syncwarp();
+  rg.used = K0 + static_cast<uint32_t>(n_my);
+  if (rg.failed) {  // let the copies already issued land (bounded) before the CTA can exit
+    for (int j = k; j < n_my && j < k + NSTAGE; ++j) {
+      const uint32_t K = K0 + j;
+      mbar_wait(rg.bar + 8 * (K % NSTAGE), (K / NSTAGE) & 1, 100000000ull);
+    }
+    return;
+  }
 
   l0 = warp_sum_g(l0);
   l1 = warp_sum_g(l1);
@@ -352,23 +356,42 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, uint8_t *ring, uint8
   store_partial<D>(p.s, slot, sub, h, lane, o0, o1, lse0, lse1);
 }
 
+extern __shared__ __align__(128) uint8_t kvq_tq_dsmem[];
+
 template <int D, int VBITS, int NSTAGE, bool PACKQ>
-__global__ void __launch_bounds__(256, 2) decode_tq_kernel(const TqParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  asm volatile("griddepcontrol.launch_dependents;");  // let the merge kernel's launch begin early
+__global__ void __launch_bounds__(256, 2) decode_tq_kernel(const __grid_constant__ TqParams p) {
   using Gm = TqGeom<D, VBITS>;
-  const int warp = threadIdx.x >> 5;
-  uint8_t *ring = smem + warp * (NSTAGE * Gm::STAGE + Gm::QBYTES);
-  uint8_t *qarea = ring + NSTAGE * Gm::STAGE;
+  __shared__ __align__(8) uint64_t s_bar[8][NSTAGE];
+  asm volatile("griddepcontrol.launch_dependents;");  // let the merge kernel's launch begin early
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // ring slots start at the first 128-byte aligned offset of the dynamic buffer
+  const uint32_t dbase = smem_u32(kvq_tq_dsmem);
+  const uint32_t off = ((128u - (dbase & 127u)) & 127u) + warp * NSTAGE * Gm::TILE;
+  TqRing rg;
+  rg.ring_p = kvq_tq_dsmem + off;
+  rg.ring = dbase + off;
+  rg.bar = smem_u32(&s_bar[warp][0]);
+  rg.used = 0;
+  rg.failed = false;
+  if (lane == 0) {
+    for (int i = 0; i < NSTAGE; ++i) mbar_init(rg.bar + 8 * i, 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
   const int hl = warp % p.s.heads_per_cta;
   const int sub = warp / p.s.heads_per_cta;
   const int h = blockIdx.y * p.s.heads_per_cta + hl;
   for_each_piece(p.s, &g_flags_decode_tq, [&](int b, int t0, int t1, long long slot) {
-    tq_piece<D, VBITS, NSTAGE, PACKQ>(p, ring, qarea, b, h, sub, t0, t1, slot);
+    if (!rg.failed) tq_piece<D, VBITS, NSTAGE, PACKQ>(p, rg, b, h, sub, t0, t1, slot);
   });
 }
 
-constexpr int kStagesTq = 3;
+constexpr int kStagesTq = 4;
+
+template <int D, int VBITS>
+constexpr size_t tq_smem_bytes() {
+  return 8 * static_cast<size_t>(kStagesTq) * TqGeom<D, VBITS>::TILE + 128;
+}
 
 bool take_flags_decode_tq(cudaStream_t stream, unsigned *host_word) {
   static const unsigned zero = 0;
@@ -380,9 +403,11 @@ bool take_flags_decode_tq(cudaStream_t stream, unsigned *host_word) {
 }
 
 template <int D, int VBITS, bool PACKQ>
-static kvq_status launch_tq(const TqParams &p, const SplitPlan &plan, cudaStream_t s) {
+static kvq_status launch_tq(TqParams &p, const SplitPlan &plan, const uint8_t *cache, int slot_bytes, int Hk,
+                            cudaStream_t s) {
   using Gm = TqGeom<D, VBITS>;
-  const size_t smem = 8 * static_cast<size_t>(kStagesTq * Gm::STAGE + Gm::QBYTES);
+  if (!tq_tensor_map(cache, p.num_blocks, Hk, slot_bytes, Gm::RB, &p.map)) return KVQ_ERR_CUDA;
+  const size_t smem = tq_smem_bytes<D, VBITS>();
   static size_t attr_done[kMaxDevices] = {};
   if (ensure_dynamic_smem(decode_tq_kernel<D, VBITS, kStagesTq, PACKQ>, smem, attr_done) != cudaSuccess)
     return KVQ_ERR_CUDA;
@@ -448,21 +473,19 @@ extern "C" kvq_status kvq_decode_tq_lse(const float *q, const uint8_t *kv_cache,
   sa.out = out;
   sa.out_dtype = KVQ_F32;
   p.q = q;
-  p.cache = kv_cache;
   p.block_table = block_table;
-  p.slot_bytes = slot_bytes;
   p.sc_log2 = static_cast<float>(static_cast<double>(attn_scale) * 1.4426950408889634);
   p.num_blocks = num_blocks;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // packed q columns: faster for 3-bit values (127 vs 131 us on the 64 x 4096 workload), slower
-  // for 4-bit ones (131 vs 126 us), measured on GB300
-  const bool packq = sa.G <= 4 && value_bits == 3;
+  // packed q columns whenever G <= 4 (4-bit values on the 64 x 4096 workload: 94.1 vs 97.4 us per
+  // call, measured on GB300)
+  const bool packq = sa.G <= 4;
   if (D == 128) {
-    if (value_bits == 4) return packq ? launch_tq<128, 4, true>(p, plan, s) : launch_tq<128, 4, false>(p, plan, s);
-    return packq ? launch_tq<128, 3, true>(p, plan, s) : launch_tq<128, 3, false>(p, plan, s);
+    if (value_bits == 4) return packq ? launch_tq<128, 4, true>(p, plan, kv_cache, slot_bytes, Hk, s) : launch_tq<128, 4, false>(p, plan, kv_cache, slot_bytes, Hk, s);
+    return packq ? launch_tq<128, 3, true>(p, plan, kv_cache, slot_bytes, Hk, s) : launch_tq<128, 3, false>(p, plan, kv_cache, slot_bytes, Hk, s);
   }
-  if (value_bits == 4) return packq ? launch_tq<64, 4, true>(p, plan, s) : launch_tq<64, 4, false>(p, plan, s);
-  return packq ? launch_tq<64, 3, true>(p, plan, s) : launch_tq<64, 3, false>(p, plan, s);
+  if (value_bits == 4) return packq ? launch_tq<64, 4, true>(p, plan, kv_cache, slot_bytes, Hk, s) : launch_tq<64, 4, false>(p, plan, kv_cache, slot_bytes, Hk, s);
+  return packq ? launch_tq<64, 3, true>(p, plan, kv_cache, slot_bytes, Hk, s) : launch_tq<64, 3, false>(p, plan, kv_cache, slot_bytes, Hk, s);
 }
 
 extern "C" kvq_status kvq_decode_tq(const float *q, const uint8_t *kv_cache, int32_t slot_bytes,

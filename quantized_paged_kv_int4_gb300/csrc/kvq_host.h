@@ -63,6 +63,13 @@ struct Int4Maps {
 // Returns false if the driver entry point is unavailable or an encode fails.
 bool int4_tensor_maps(const void *k_cache, const void *v_cache, const void *k_scale, const void *v_scale,
                       long long num_blocks, int Hk, int D, Int4Maps *maps);
+// The TurboQuant combined-slot pool [num_blocks][16][Hk][slot_bytes] viewed as dims
+// {slot_bytes, 16, Hk, num_blocks} (token stride Hk * slot_bytes, head stride slot_bytes); box
+// {row_bytes, 16, 1, 1} = the first row_bytes of the 16 slots of one (page, head), stored
+// [token][row_bytes] without swizzle. slot_bytes and row_bytes multiples of 16, row_bytes <= 256
+// and <= slot_bytes. Cached like int4_tensor_maps; false if the driver entry point is unavailable
+// or the encode fails.
+bool tq_tensor_map(const void *cache, long long num_blocks, int Hk, int slot_bytes, int row_bytes, CUtensorMap *map);
 
 // Raise a kernel's dynamic shared-memory limit to `bytes` on the current device. The attribute
 // lives with the function in each device's context, so it is set once per (instantiation,
