@@ -9,10 +9,11 @@
 // key_packed_size (KPS) and dequantize as idx * scale + zero like the FP8-key layout; the splits
 // are merged by log-sum-exp (decode_common.cuh).
 //
-// GB300 design: the FP8-key kernel's structure (one warp per kv head and run of pages, private
-// cp.async ring, mma.m16n8k16 for both contractions), with whole slots staged: KPS is usually not
-// a multiple of 4 (MSE_BYTES + 2), so each stage row is the slot's bytes and the fields are read
-// from shared memory at any byte offset (aligned words + funnel shifts). Centroids go to the
+// GB300 design: the FP8-key kernel's structure (one warp per kv head and run of pages, a per-warp
+// ring of (page, head) tiles brought by one tensor-memory-accelerator box each, mma.m16n8k16 for
+// both contractions), with each slot's used bytes staged as one row: KPS is usually not a multiple
+// of 4 (MSE_BYTES + 2), so the fields are read from shared memory at any byte offset (aligned
+// words + funnel shifts). Centroids go to the
 // tensor cores as fp16 hi + lo parts: a pair table in shared memory maps two adjacent indices to
 // the hi pair and the lo pair of an A-fragment register in one 8-byte load; q as fp16 hi + lo as
 // in the FP8 path; three MMAs per k-step (hi.hi, hi.lo, lo.hi) keep ~22 bits of the product.
@@ -26,11 +27,11 @@ __device__ unsigned g_flags_decode_tq_mse = 0;
 
 struct TqMseParams {
   SplitArgs s;
+  CUtensorMap map;         // the slot pool as {slot_bytes, 16, Hk, num_blocks}, box {row bytes, 16, 1, 1}
   const float *q_rot;      // [B, Hq, D] fp32 (written by rotate_q_kernel into the workspace)
-  const uint8_t *cache;
   const int32_t *block_table;
   const float *centroids;  // [2^key_bits]
-  int32_t slot_bytes, kps, norm_correction;
+  int32_t kps, norm_correction;
   float sc_log2;           // attn_scale * log2(e)
   int64_t num_blocks;
 };
@@ -46,7 +47,6 @@ struct MseGeom {
   static constexpr int VDB = (D * VB + 7) / 8;
   static constexpr int KSTEPS = D / 16;
   static constexpr int MT = D / 16;
-  static constexpr int QBYTES = 2 * 8 * D * 2;      // fp16 hi and lo
   static constexpr int NPAIR = 1 << (2 * KB);       // index pairs
   // pair table: entry (i0 | i1 << KB) = {fp16 hi(c_i0) | hi(c_i1) << 16, lo(c_i0) | lo(c_i1) << 16},
   // in COPIES copies side by side (entry e of copy c at byte 8 (e COPIES + c): lane l reads copy
@@ -57,13 +57,24 @@ struct MseGeom {
   static constexpr int TABLE = NPAIR * 8 * COPIES + NPAIR * 4;
 };
 
-// Stage row stride for slot_bytes SB: a multiple of 16 (cp.async destination) whose word stride
-// is 4 mod 8 (rows g and g + 8 of a fragment fall in different banks).
-__host__ __device__ inline int mse_row_stride(int SB) {
-  int rs = (SB + 15) / 16 * 16;
+// Staged bytes of a slot holding its `used` bytes: a multiple of 16 (a box row) whose word stride
+// is 4 mod 8 (rows g and g + 8 of a fragment fall in different banks), i.e. an odd multiple of 16.
+// Bytes past the slot's end are out of the tensor and filled with zeros by the copy.
+inline int mse_row_bytes(int used) {
+  int rs = (used + 15) / 16 * 16;
   while (((rs / 4) & 7) != 4) rs += 16;
   return rs;
 }
+
+// Per-warp ring state carried from piece to piece: tiles issued so far (ring slot and mbarrier
+// phase of tile K are K % NSTAGE and (K / NSTAGE) & 1), and whether a wait ran out.
+struct MseRing {
+  const uint8_t *ring_p;  // the warp's first ring slot
+  uint32_t ring;          // its shared-window address
+  uint32_t bar;           // shared address of its first mbarrier (8 bytes each)
+  uint32_t used;
+  bool failed;
+};
 
 // 32 bits of a shared-memory row starting at any byte offset o (two aligned words, funnel shift)
 __device__ __forceinline__ uint32_t lds32_at(const uint8_t *row, int o) {
@@ -143,15 +154,15 @@ __device__ __forceinline__ uint32_t pair_offset(const uint32_t *w, int bit) {
 // shuffle adds column n + 4 into column n (columns 4..7 then repeat heads 0..3 and are dropped).
 // ctab: the power of two the table's centroids were divided by (2^kc, decode_tq_mse_kernel).
 template <int D, int KB, int VB, int NSTAGE, bool PACKQ>
-__device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring, uint8_t *qarea,
-                                             const uint2 *table, const float *sq, float ctab, int RS, int b,
-                                             int h, int sub, int t0, int t1, long long slot) {
+__device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, MseRing &rg, const uint2 *table,
+                                             const float *sq, float ctab, int RS, int b, int h, int sub,
+                                             int t0, int t1, long long slot) {
   using Gm = MseGeom<D, KB, VB>;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int G = p.s.G, WPH = p.s.warps_per_head, Hk = p.s.Hk;
-  const int SB = p.slot_bytes, KPS = p.kps;
-  const int STAGE = kPage * RS;
+  const int G = p.s.G, WPH = p.s.warps_per_head;
+  const int KPS = p.kps;
+  const int TILE = kPage * RS;
   const uint8_t *tb = reinterpret_cast<const uint8_t *>(table);
   const uint32_t copy_off = (lane & (Gm::COPIES - 1)) << 3;
 
@@ -166,31 +177,26 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
   int bids_cur = load_bids(0);
   int bids_next = load_bids(1);
 
-  const uint32_t ring_s = smem_u32(ring);
-  const long long row_stride = static_cast<long long>(Hk) * SB;
-  const long long page_bytes = kPage * row_stride;
-  const uint8_t *head = p.cache + static_cast<long long>(h) * SB;
-  // lanes 2r and 2r + 1 copy slot row r of a page: its even and odd 16-byte pieces, so each
-  // further piece of a lane is 32 bytes on in both memories
-  const int chunks = SB / 16;
-  const int n_cp = (chunks - (lane & 1) + 1) >> 1;
-  const long long src_lane = (lane >> 1) * row_stride + 16 * (lane & 1);
-  const uint32_t dst_lane = (lane >> 1) * RS + 16 * (lane & 1);
+  const uint32_t K0 = rg.used;  // this piece's tile k is ring tile K0 + k
+  // tile k of the piece into its ring slot: lane 0 arms the slot's mbarrier with the tile's bytes
+  // and starts the box copy (the warp has finished reading the slot: __syncwarp before the call)
   auto issue = [&](int k) {
+    if (k >= n_my) return;
     const int kk = k & 31;
     if (k > 0 && kk == 0) {
       bids_cur = bids_next;
       bids_next = load_bids((k >> 5) + 1);
     }
     const int blk = __shfl_sync(FULL, bids_cur, kk);
-    const bool in = k < n_my;
-    const bool ok = in && blk >= 0 && blk < p.num_blocks;
-    if (in && !ok && lane == 0) atomicOr(&g_flags_decode_tq_mse, ERR_BLOCK);
-    const uint32_t st = ring_s + (k % NSTAGE) * STAGE;
-    const uint8_t *src = head + static_cast<long long>(ok ? blk : 0) * page_bytes + src_lane;
-    const uint32_t dst = st + dst_lane;
-    for (int i = 0; i < n_cp; ++i) cp_async<16>(dst + 32 * i, src + 32 * i, ok);
-    cp_async_commit();
+    if (lane == 0) {
+      const bool ok = blk >= 0 && blk < p.num_blocks;
+      if (!ok) atomicOr(&g_flags_decode_tq_mse, ERR_BLOCK);
+      const uint32_t sl = (K0 + k) % NSTAGE;
+      const uint32_t bar = rg.bar + 8 * sl;
+      fence_proxy_async();  // earlier reads of the slot come before the copy that refills it
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(TILE));
+      tma_load_4d(rg.ring + sl * TILE, &p.map, 0, 0, h, ok ? blk : 0, bar);
+    }
   };
 
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -207,58 +213,66 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
   // overlap (a programmatic dependent launch), so wait for that grid first.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   float sc2;  // score scale of the piece: attn_scale * log2 e * 2^k (q shift) * 2^kc (table shift)
+  // q_rot -> fp16 hi / lo B fragments, straight from global memory: lane (g, t) holds column g
+  // (head g, or PACKQ: head g % 4, its hi part for g < 4 and its lo part for g >= 4) at the dims
+  // KCH t .. KCH t + KCH - 1, k-step ks taking dims KCH t + 4 ks .. + 3
+  uint32_t qhi[Gm::KSTEPS][2], qlo[PACKQ ? 1 : Gm::KSTEPS][2];
   {
-    constexpr int J = D / 32;
-    const float *qb = p.q_rot + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(h) * G) * D;
-    float qmax = 0.f;
-    for (int n = 0; n < G; ++n) {
+    const int head = PACKQ ? (g & 3) : g;
+    const bool live = head < G;
+    const float4 *src = reinterpret_cast<const float4 *>(
+        p.q_rot + (static_cast<long long>(b) * p.s.Hq + static_cast<long long>(h) * G + (live ? head : 0)) * D +
+        t * Gm::KCH);
+    float qv[Gm::KCH];
 #pragma unroll
-      for (int j = 0; j < J; ++j) qmax = fmaxf(qmax, fabsf(qb[n * D + lane + 32 * j]));
+    for (int j = 0; j < Gm::KCH / 4; ++j) {
+      const float4 v = live ? src[j] : make_float4(0.f, 0.f, 0.f, 0.f);  // written by the pre-kernel: no __ldg
+      qv[4 * j] = v.x;
+      qv[4 * j + 1] = v.y;
+      qv[4 * j + 2] = v.z;
+      qv[4 * j + 3] = v.w;
     }
+    float qmax = 0.f;
+#pragma unroll
+    for (int j = 0; j < Gm::KCH; ++j) qmax = fmaxf(qmax, fabsf(qv[j]));
     const int qk = query_shift(warp_max(qmax), 0, &g_flags_decode_tq_mse);
     const float qdiv = pow2i(-qk);
     sc2 = p.sc_log2 * pow2i(qk) * ctab;
-    __half *qh = reinterpret_cast<__half *>(qarea);
-    for (int n = 0; n < 8; ++n) {
-#pragma unroll
-      for (int j = 0; j < J; ++j) {
-        const int e = lane + 32 * j;
-        const int head = PACKQ ? (n & 3) : n;
-        const float x = head < G ? qb[head * D + e] * qdiv : 0.f;
-        const __half hi = __float2half_rn(x);
-        const __half lo = __float2half_rn(x - __half2float(hi));
-        if constexpr (PACKQ) {
-          qh[n * D + e] = n < 4 ? hi : lo;
-        } else {
-          qh[n * D + e] = hi;
-          qh[8 * D + n * D + e] = lo;
-        }
-      }
-    }
-  }
-  __syncwarp();
-  uint32_t qhi[Gm::KSTEPS][2], qlo[PACKQ ? 1 : Gm::KSTEPS][2];
-  {
-    const __half *qh = reinterpret_cast<const __half *>(qarea) + g * D + t * Gm::KCH;
 #pragma unroll
     for (int ks = 0; ks < Gm::KSTEPS; ++ks) {
-      const __half *r = qh + 4 * ks;
-      qhi[ks][0] = h2_as_u32(__halves2half2(r[0], r[1]));
-      qhi[ks][1] = h2_as_u32(__halves2half2(r[2], r[3]));
-      if constexpr (!PACKQ) {
-        qlo[ks][0] = h2_as_u32(__halves2half2(r[8 * D + 0], r[8 * D + 1]));
-        qlo[ks][1] = h2_as_u32(__halves2half2(r[8 * D + 2], r[8 * D + 3]));
+      __half hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x = qv[4 * ks + e] * qdiv;
+        hi[e] = __float2half_rn(x);
+        lo[e] = __float2half_rn(x - __half2float(hi[e]));
+      }
+      if constexpr (PACKQ) {
+        const bool use_lo = g >= 4;
+        qhi[ks][0] = h2_as_u32(use_lo ? __halves2half2(lo[0], lo[1]) : __halves2half2(hi[0], hi[1]));
+        qhi[ks][1] = h2_as_u32(use_lo ? __halves2half2(lo[2], lo[3]) : __halves2half2(hi[2], hi[3]));
+      } else {
+        qhi[ks][0] = h2_as_u32(__halves2half2(hi[0], hi[1]));
+        qhi[ks][1] = h2_as_u32(__halves2half2(hi[2], hi[3]));
+        qlo[ks][0] = h2_as_u32(__halves2half2(lo[0], lo[1]));
+        qlo[ks][1] = h2_as_u32(__halves2half2(lo[2], lo[3]));
       }
     }
   }
-  __syncwarp();
 
-
-  for (int k = 0; k < n_my; ++k) {
+  int k = 0;
+  for (; k < n_my; ++k) {
     issue(k + NSTAGE - 1);
-    cp_async_wait<NSTAGE - 1>();
-    __syncwarp();
-    const uint8_t *st = ring + (k % NSTAGE) * STAGE;
+    {
+      const uint32_t K = K0 + k;
+      const uint32_t bar = rg.bar + 8 * (K % NSTAGE), par = (K / NSTAGE) & 1;
+      if (!__all_sync(FULL, mbar_try_wait(bar, par)) && !__all_sync(FULL, mbar_wait(bar, par))) {
+        if (lane == 0) atomicOr(&g_flags_decode_tq_mse, ERR_TIMEOUT);
+        rg.failed = true;
+        break;
+      }
+    }
+    const uint8_t *st = rg.ring_p + ((K0 + k) % NSTAGE) * TILE;
     const int nb = (first + k * WPH) * kPage;
     const bool ok0 = nb + g >= t0 && nb + g < t1;
     const bool ok1 = nb + g + 8 >= t0 && nb + g + 8 < t1;
@@ -443,8 +457,14 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
     }
     __syncwarp();
   }
-  cp_async_wait<0>();
-  __syncwarp();
+  rg.used = K0 + static_cast<uint32_t>(n_my);
+  if (rg.failed) {  // let the copies already issued land (bounded) before the CTA can exit
+    for (int j = k; j < n_my && j < k + NSTAGE; ++j) {
+      const uint32_t K = K0 + j;
+      mbar_wait(rg.bar + 8 * (K % NSTAGE), (K / NSTAGE) & 1, 100000000ull);
+    }
+    return;
+  }
 
   l0 = warp_sum_g(l0);
   l1 = warp_sum_g(l1);
@@ -465,9 +485,12 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, uint8_t *ring
   store_partial<D>(p.s, slot, sub, h, lane, o0, o1, lse0, lse1);
 }
 
+extern __shared__ __align__(128) uint8_t kvq_mse_dsmem[];
+
 template <int D, int KB, int VB, int NSTAGE, bool PACKQ>
-__global__ void __launch_bounds__(256, 2) decode_tq_mse_kernel(const TqMseParams p, int RS) {
-  extern __shared__ __align__(16) uint8_t smem[];
+__global__ void __launch_bounds__(256, 2) decode_tq_mse_kernel(const __grid_constant__ TqMseParams p, int RS) {
+  uint8_t *smem = kvq_mse_dsmem;
+  __shared__ __align__(8) uint64_t s_bar[8][NSTAGE];
   asm volatile("griddepcontrol.launch_dependents;");  // let the merge kernel's launch begin early
   using Gm = MseGeom<D, KB, VB>;
   const int warp = threadIdx.x >> 5;
@@ -490,18 +513,29 @@ __global__ void __launch_bounds__(256, 2) decode_tq_mse_kernel(const TqMseParams
                           static_cast<uint32_t>(__half_as_ushort(l0)) | (static_cast<uint32_t>(__half_as_ushort(l1)) << 16));
     if (i % Gm::COPIES == 0) sq[e] = c0 * c0 + c1 * c1;
   }
+  // ring slots: after the table, from its first 128-byte aligned offset; each warp inits its barriers
+  const uint32_t dbase = smem_u32(smem);
+  const uint32_t off = ((dbase + Gm::TABLE + 127u) & ~127u) - dbase + warp * NSTAGE * kPage * RS;
+  MseRing rg;
+  rg.ring_p = smem + off;
+  rg.ring = dbase + off;
+  rg.bar = smem_u32(&s_bar[warp][0]);
+  rg.used = 0;
+  rg.failed = false;
+  if ((threadIdx.x & 31) == 0) {
+    for (int i = 0; i < NSTAGE; ++i) mbar_init(rg.bar + 8 * i, 1);
+    mbar_init_fence();
+  }
   __syncthreads();
-  uint8_t *ring = smem + Gm::TABLE + warp * (NSTAGE * kPage * RS + Gm::QBYTES);
-  uint8_t *qarea = ring + NSTAGE * kPage * RS;
   const int hl = warp % p.s.heads_per_cta;
   const int sub = warp / p.s.heads_per_cta;
   const int h = blockIdx.y * p.s.heads_per_cta + hl;
   for_each_piece(p.s, &g_flags_decode_tq_mse, [&](int b, int t0, int t1, long long slot) {
-    tq_mse_piece<D, KB, VB, NSTAGE, PACKQ>(p, ring, qarea, table, sq, pow2i(kc), RS, b, h, sub, t0, t1, slot);
+    if (!rg.failed) tq_mse_piece<D, KB, VB, NSTAGE, PACKQ>(p, rg, table, sq, pow2i(kc), RS, b, h, sub, t0, t1, slot);
   });
 }
 
-constexpr int kStagesMse = 3;
+constexpr int kStagesMse = 4;
 
 bool take_flags_decode_tq_mse(cudaStream_t stream, unsigned *host_word) {
   static const unsigned zero = 0;
@@ -513,11 +547,13 @@ bool take_flags_decode_tq_mse(cudaStream_t stream, unsigned *host_word) {
 }
 
 template <int D, int KB, int VB, bool PACKQ>
-static kvq_status launch_tq_mse(const TqMseParams &p, const SplitPlan &plan, const float *q, const float *Pi,
-                                float *q_rot, cudaStream_t s) {
+static kvq_status launch_tq_mse(TqMseParams &p, const SplitPlan &plan, const float *q, const float *Pi,
+                                float *q_rot, const uint8_t *cache, int slot_bytes, int Hk, cudaStream_t s) {
   using Gm = MseGeom<D, KB, VB>;
-  const int RS = mse_row_stride(p.slot_bytes);
-  const size_t smem = Gm::TABLE + 8 * static_cast<size_t>(kStagesMse * kPage * RS + Gm::QBYTES);
+  const int RS = mse_row_bytes(p.kps + Gm::VDB + 4);  // key part, values, scale and zero
+  if (RS > 256) return KVQ_ERR_UNSUPPORTED;
+  if (!tq_tensor_map(cache, p.num_blocks, Hk, slot_bytes, RS, &p.map)) return KVQ_ERR_CUDA;
+  const size_t smem = Gm::TABLE + 128 + 8 * static_cast<size_t>(kStagesMse * kPage * RS);
   if (smem > 227 * 1024) return KVQ_ERR_UNSUPPORTED;
   static size_t attr_done[kMaxDevices] = {};  // the size depends on slot_bytes: the largest set so far
   if (ensure_dynamic_smem(decode_tq_mse_kernel<D, KB, VB, kStagesMse, PACKQ>, smem, attr_done) != cudaSuccess)
@@ -612,10 +648,8 @@ extern "C" kvq_status kvq_decode_tq_mse(const float *q, const float *rotation, c
   sa.out = out;
   sa.out_dtype = KVQ_F32;
   p.q_rot = q_rot;
-  p.cache = kv_cache;
   p.block_table = block_table;
   p.centroids = centroids;
-  p.slot_bytes = slot_bytes;
   p.kps = key_packed_size;
   p.norm_correction = norm_correction != 0;
   p.sc_log2 = static_cast<float>(static_cast<double>(attn_scale) * 1.4426950408889634);
@@ -624,8 +658,8 @@ extern "C" kvq_status kvq_decode_tq_mse(const float *q, const float *rotation, c
   const bool packq = sa.G <= 4;
 #define KVQ_MSE_CASE(DD, KK, VV)                                                                     \
   if (D == DD && key_bits == KK && value_bits == VV)                                                 \
-    return packq ? launch_tq_mse<DD, KK, VV, true>(p, plan, q, rotation, q_rot, s)                   \
-                 : launch_tq_mse<DD, KK, VV, false>(p, plan, q, rotation, q_rot, s);
+    return packq ? launch_tq_mse<DD, KK, VV, true>(p, plan, q, rotation, q_rot, kv_cache, slot_bytes, Hk, s) \
+                 : launch_tq_mse<DD, KK, VV, false>(p, plan, q, rotation, q_rot, kv_cache, slot_bytes, Hk, s);
   KVQ_MSE_CASE(128, 3, 4)
   KVQ_MSE_CASE(128, 4, 4)
   KVQ_MSE_CASE(128, 3, 3)
