@@ -74,6 +74,36 @@ struct SplitArgs {
 constexpr float kWeightHi = 32768.f;
 constexpr float kScoreCap = 64.f;
 
+// 3-bit value indices as P.V MMA operands (the TurboQuant layouts). s[0..3]: the index streams
+// of tokens 2t, 2t + 1, 2t + 8, 2t + 9 (LSB first), the lane's dim j at bits 3j .. 3j + 2. Row r
+// of m-tile mt is the lane's dim 2 mt + r, and each A register holds that dim's indices of two
+// tokens as exact fp16 subnormals idx * 2^(p - 24), p = 3 (2 mt + r) mod 8 <= 7: the 16-bit
+// window of each stream that holds the field is moved into the register's half by one byte
+// permute and the field is masked where it lies. v3_scale(mt, r) = 2^(24 - p) undoes the scale.
+__device__ __forceinline__ void v3_windows(const unsigned long long (&s)[4], uint32_t (&win)[4][3]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {  // stream bytes 0..3, 2..5, 4..7
+    const uint32_t lo = static_cast<uint32_t>(s[i]), hi = static_cast<uint32_t>(s[i] >> 32);
+    win[i][0] = lo;
+    win[i][1] = __funnelshift_r(lo, hi, 16);
+    win[i][2] = hi;
+  }
+}
+__device__ __forceinline__ void v3_frag(const uint32_t (&win)[4][3], int mt, uint32_t (&a)[4]) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int bit = 3 * (2 * mt + r), jb = bit >> 3, p = bit & 7;
+    const int w = jb <= 1 ? 0 : (jb <= 3 ? 1 : 2), o = jb - 2 * w;  // window and byte in it
+    const uint32_t sel = o | (o + 1) << 4 | (o + 4) << 8 | (o + 5) << 12;
+    const uint32_t mask = (7u << p) * 0x10001u;
+#pragma unroll
+    for (int tp = 0; tp < 2; ++tp) a[2 * tp + r] = __byte_perm(win[2 * tp][w], win[2 * tp + 1][w], sel) & mask;
+  }
+}
+__host__ __device__ constexpr float v3_scale(int mt, int r) {
+  return static_cast<float>(1u << (24 - ((3 * (2 * mt + r)) & 7)));
+}
+
 // Starting point of a column's new reference: the step's largest score ms for a column with no
 // keys yet (ref = -inf), else the old reference raised to at least ms - kScoreCap.
 __device__ __forceinline__ float ref_base(float ref, float ms) {

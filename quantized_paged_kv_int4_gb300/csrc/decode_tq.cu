@@ -310,19 +310,12 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, TqRing &rg, int b, i
         const uint8_t *r = st + (2 * t + (i & 1) + 8 * (i >> 1)) * Gm::RB + v3_al;
         w[i] = ((static_cast<unsigned long long>(lds32(r + 4)) << 32) | lds32(r)) >> sh;
       }
+      uint32_t win[4][3];
+      v3_windows(w, win);
 #pragma unroll
       for (int mt = 0; mt < Gm::MT; ++mt) {
         uint32_t a[4];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {          // r = 0: dim 2 mt (row g), r = 1: dim 2 mt + 1 (row g + 8)
-          const int bit = 3 * (2 * mt + r);
-#pragma unroll
-          for (int tp = 0; tp < 2; ++tp) {     // tokens (2t, 2t+1) then (2t+8, 2t+9)
-            const uint32_t lo = static_cast<uint32_t>(w[2 * tp] >> bit) & 7u;
-            const uint32_t hi = static_cast<uint32_t>(w[2 * tp + 1] >> bit) & 7u;
-            a[2 * tp + r] = lo | (hi << 16);  // fp16 subnormals idx * 2^-24
-          }
-        }
+        v3_frag(win, mt, a);
         mma_f16_16816(acc[mt], a[0], a[1], a[2], a[3], b01, b23);
       }
     }
@@ -342,14 +335,14 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, TqRing &rg, int b, i
   pz0 = warp_sum_g(pz0);
   pz1 = warp_sum_g(pz1);
   const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-  constexpr float hs = VBITS == 4 ? 1048576.f : 16777216.f;  // 2^20: high nibbles enter 16x larger
   float o0[D / 8], o1[D / 8];
 #pragma unroll
-  for (int mt = 0; mt < Gm::MT; ++mt) {
-    o0[2 * mt] = (acc[mt][0] * 16777216.f + pz0) * inv0;
-    o1[2 * mt] = (acc[mt][1] * 16777216.f + pz1) * inv1;
-    o0[2 * mt + 1] = (acc[mt][2] * hs + pz0) * inv0;
-    o1[2 * mt + 1] = (acc[mt][3] * hs + pz1) * inv1;
+  for (int mt = 0; mt < Gm::MT; ++mt) {  // 4-bit: high nibbles enter 16x larger; 3-bit: v3_scale
+    const float s0 = VBITS == 4 ? 16777216.f : v3_scale(mt, 0), s1 = VBITS == 4 ? 1048576.f : v3_scale(mt, 1);
+    o0[2 * mt] = (acc[mt][0] * s0 + pz0) * inv0;
+    o1[2 * mt] = (acc[mt][1] * s0 + pz1) * inv1;
+    o0[2 * mt + 1] = (acc[mt][2] * s1 + pz0) * inv0;
+    o1[2 * mt + 1] = (acc[mt][3] * s1 + pz1) * inv1;
   }
   const float lse0 = l0 > 0.f ? m0 + log2f(l0) : -INFINITY;
   const float lse1 = l1 > 0.f ? m1 + log2f(l1) : -INFINITY;
