@@ -49,7 +49,9 @@ __device__ __forceinline__ float exp_pool(float x) {
   p = __fadd_rn(__fmul_rn(p, r), 0.5f);
   p = __fadd_rn(__fmul_rn(p, r), 1.0f);
   p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-  return n <= -126.f ? 0.f : ldexpf(p, static_cast<int>(fmaxf(n, -125.f)));
+  // p * 2^n for n in [-125, 127] (p in [0.7, 1.42], so the product is a normal number and exact):
+  // the power of two built from its exponent bits, the same value ldexp gives
+  return n <= -126.f ? 0.f : __fmul_rn(p, __int_as_float((static_cast<int>(fminf(n, 127.f)) + 127) << 23));
 }
 
 constexpr int kKpRow = 16 + 4;           // padded 16-element block (words)

@@ -220,13 +220,25 @@ __global__ void __launch_bounds__(128, 3) write_int4_kernel(const WriteParams p,
       for (int i = 0; i < NW; ++i) wb[i] = w[i];
     }
 
-    // min / max over the vector (bf16 pairs: exact), scale, zero-point and inverse per vector
-    __nv_bfloat162 mn2 = as_bf2(wb[0]), mx2 = mn2;
+    // min / max over the vector (bf16 pairs: exact, so any order gives the same result: eight
+    // independent chains, then a tree), scale, zero-point and inverse per vector
+    __nv_bfloat162 mnc[8], mxc[8];
 #pragma unroll
-    for (int i = 1; i < NW; ++i) {
-      mn2 = __hmin2(mn2, as_bf2(wb[i]));
-      mx2 = __hmax2(mx2, as_bf2(wb[i]));
+    for (int c = 0; c < 8; ++c) mnc[c] = mxc[c] = as_bf2(wb[c]);
+#pragma unroll
+    for (int i = 8; i < NW; ++i) {
+      mnc[i & 7] = __hmin2(mnc[i & 7], as_bf2(wb[i]));
+      mxc[i & 7] = __hmax2(mxc[i & 7], as_bf2(wb[i]));
     }
+#pragma unroll
+    for (int w = 4; w >= 1; w >>= 1) {
+#pragma unroll
+      for (int c = 0; c < w; ++c) {
+        mnc[c] = __hmin2(mnc[c], mnc[c + w]);
+        mxc[c] = __hmax2(mxc[c], mxc[c + w]);
+      }
+    }
+    const __nv_bfloat162 mn2 = mnc[0], mx2 = mxc[0];
     const float mn = fminf(__low2float(mn2), __high2float(mn2));
     const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
     const float scale = fmaxf(__fdiv_rn(__fsub_rn(mx, mn), 15.0f), 1e-6f);
