@@ -101,41 +101,55 @@ __device__ __forceinline__ uint32_t lds16_at(const uint8_t *row, int o) {
   return *reinterpret_cast<const uint16_t *>(row + o);  // o even
 }
 
-// q_rot[r][d] = sum_e q[r][e] * Pi[d][e] (fp32) for R = 8 rows per CTA (enough CTAs to fill the
-// GPU for a decode batch), one output dim per thread.
-constexpr int kRotRows = 8;
+// q_rot[r][d] = sum_e q[r][e] * Pi[d][e] (fp32, e in order) for R = 16 rows per CTA: Pi goes to
+// shared memory transposed (row e of the copy holds Pi[.][e], padded to D + 1 words so that both
+// the transposing stores and the reads across d are free of bank conflicts), the R query rows as
+// [e][r]; thread (d, group) accumulates rows group * RPT .. + RPT - 1 of output dim d.
+constexpr int kRotRows = 16;
 
 template <int D>
-__global__ void __launch_bounds__(D) rotate_q_kernel(const float *__restrict__ q, const float *__restrict__ Pi,
-                                                     float *__restrict__ q_rot, long long rows) {
+constexpr size_t rotate_q_smem() {
+  return (static_cast<size_t>(D) * (D + 1) + static_cast<size_t>(D) * kRotRows) * sizeof(float);
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) rotate_q_kernel(const float *__restrict__ q, const float *__restrict__ Pi,
+                                                       float *__restrict__ q_rot, long long rows) {
   asm volatile("griddepcontrol.launch_dependents;");  // the decode kernel may start its prologue
-  constexpr int R = kRotRows;
-  __shared__ __align__(16) float s_q[R][D];
+  constexpr int R = kRotRows, RPT = R * D / 256;  // rows per thread
+  extern __shared__ __align__(16) float s_rot[];
+  float *pt = s_rot, *qs = s_rot + D * (D + 1);
   const long long r0 = static_cast<long long>(blockIdx.x) * R;
-  const int d = threadIdx.x;
-  for (int i = d; i < R * D; i += D) {
-    const long long r = r0 + i / D;
-    s_q[i / D][i % D] = r < rows ? q[r * D + i % D] : 0.f;
+#pragma unroll 4
+  for (int i = threadIdx.x; i < D * D / 4; i += 256) {  // Pi[d][4 j .. 4 j + 3] -> pt[4 j + k][d]
+    const int d = i / (D / 4), j = i % (D / 4);
+    const float4 v = __ldg(reinterpret_cast<const float4 *>(Pi) + i);
+    pt[(4 * j) * (D + 1) + d] = v.x;
+    pt[(4 * j + 1) * (D + 1) + d] = v.y;
+    pt[(4 * j + 2) * (D + 1) + d] = v.z;
+    pt[(4 * j + 3) * (D + 1) + d] = v.w;
+  }
+  for (int i = threadIdx.x; i < R * D; i += 256) {
+    const int r = i / D, e = i % D;
+    qs[e * R + r] = r0 + r < rows ? q[(r0 + r) * D + e] : 0.f;
   }
   __syncthreads();
-  float acc[R];
+  const int d = threadIdx.x % D, grp = threadIdx.x / D;
+  float acc[RPT];
 #pragma unroll
-  for (int r = 0; r < R; ++r) acc[r] = 0.f;
-  const float4 *pr = reinterpret_cast<const float4 *>(Pi + static_cast<long long>(d) * D);
-  for (int e4 = 0; e4 < D / 4; ++e4) {
-    const float4 pv = __ldg(pr + e4);
+  for (int r = 0; r < RPT; ++r) acc[r] = 0.f;
+#pragma unroll 8
+  for (int e = 0; e < D; ++e) {
+    const float pv = pt[e * (D + 1) + d];
+    const float *qe = qs + e * R + grp * RPT;
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const float4 qv = *reinterpret_cast<const float4 *>(&s_q[r][4 * e4]);
-      acc[r] = fmaf(qv.x, pv.x, acc[r]);
-      acc[r] = fmaf(qv.y, pv.y, acc[r]);
-      acc[r] = fmaf(qv.z, pv.z, acc[r]);
-      acc[r] = fmaf(qv.w, pv.w, acc[r]);
-    }
+    for (int r = 0; r < RPT; ++r) acc[r] = fmaf(qe[r], pv, acc[r]);
   }
 #pragma unroll
-  for (int r = 0; r < R; ++r)
-    if (r0 + r < rows) q_rot[(r0 + r) * D + d] = acc[r];
+  for (int r = 0; r < RPT; ++r) {
+    const long long row = r0 + grp * RPT + r;
+    if (row < rows) q_rot[row * D + d] = acc[r];
+  }
 }
 
 // the 2 KB-bit field at bit `bit` (a compile-time constant) of the index words w, shifted to bit
@@ -552,7 +566,10 @@ static kvq_status launch_tq_mse(TqMseParams &p, const SplitPlan &plan, const flo
   if (ensure_dynamic_smem(decode_tq_mse_kernel<D, KB, VB, kStagesMse, PACKQ>, smem, attr_done) != cudaSuccess)
     return KVQ_ERR_CUDA;
   const long long rows = static_cast<long long>(p.s.B) * p.s.Hq;
-  rotate_q_kernel<D><<<static_cast<unsigned>((rows + kRotRows - 1) / kRotRows), D, 0, s>>>(q, Pi, q_rot, rows);
+  static size_t rot_done[kMaxDevices] = {};
+  if (ensure_dynamic_smem(rotate_q_kernel<D>, rotate_q_smem<D>(), rot_done) != cudaSuccess) return KVQ_ERR_CUDA;
+  rotate_q_kernel<D><<<static_cast<unsigned>((rows + kRotRows - 1) / kRotRows), 256, rotate_q_smem<D>(), s>>>(q, Pi, q_rot,
+                                                                                                               rows);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   const dim3 grid(plan.seg_ctas, plan.head_groups);
   {
