@@ -30,7 +30,7 @@ def _rank(rank, world, port, q):
         # rank r takes (r + 1) ms per step for (r + 1) GB: the job moved 3 GB per step in the
         # slowest rank's 2 ms
         args = types.SimpleNamespace(steps=4, warmup=3, workload="write_fwht", no_cpu_baseline=True)
-        res = {"total_ms": 4.0 * (rank + 1), "dominant_ms": [0.5, 0.5],
+        res = {"total_ms": 4.0 * (rank + 1), "dominant_ms": 0.5 * (rank + 1), "dominant_ms_events": [0.6, 0.6],
                "clocks": {"sm_mhz": 2000.0, "sm_max_mhz": 2070.0, "reasons": []}}
         line = bench.finish(args, d, res, 1e9 * (rank + 1), {"workload": "test"}, None, 2, "write_int4",
                             [], "f32")
@@ -64,4 +64,7 @@ def test_two_gloo_ranks():
         assert line["ms_per_step"] == pytest.approx(2.0)            # max over ranks
         assert line["value"] == pytest.approx(3e9 / 2e-3 / 1e9)  # whole-job bytes / slowest time
         assert line["gpu_launches"] == 8 and line["scaling"] == "weak"
+        # the dominant call: back-to-back average, max over ranks; the per-call-event figure beside it
+        assert line["roofline"]["avg_launch_us"] == pytest.approx(1000.0)
+        assert line["roofline"]["avg_launch_us_with_events"] == pytest.approx(600.0)
     assert got[0]["ref"] == "reference" and got[1]["ref"] is None
