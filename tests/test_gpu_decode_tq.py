@@ -40,3 +40,16 @@ def test_turboquant_full_size_sampled(bits):
     idx = [0, 40, 63]
     ref = c.oracle(batch_index=idx)
     assert_close(got[idx], ref[idx], what="tq full bits=%d" % bits)
+
+
+@pytest.mark.parametrize("bits", [4, 3])
+def test_slot_wider_than_its_fields(bits):
+    """slot_bytes 48 past the key, values, scale and zero (zero padding that is never read): the
+    page tiles take only each slot's used bytes."""
+    lens = [5, 200, 33]
+    case = workloads.DecodeCase("tqpad", len(lens), 16, 4, 128, lens, seed=90 + bits)
+    c = TqCase(case, bits, num_blocks=sum(workloads.pages_needed(lens)) + 2)
+    pad = torch.full(c.cache.shape[:-1] + (48,), 0xAB, dtype=torch.uint8)
+    c.cache = torch.cat([c.cache, pad], dim=-1).contiguous()
+    assert c.cache.shape[-1] % 16 == 0
+    assert_close(_run(c), c.oracle(), what="padded slot bits=%d" % bits)
