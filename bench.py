@@ -401,9 +401,11 @@ def e2e_int4(args, r, case, signs, scale, ws, S, dev, stream, dec_bytes):
     """Public API from pinned host memory: H2D inputs, write + decode, D2H output, sync.
 
     The step's host inputs (q, the new tokens' K and V, slot_mapping, seq_lens, block table) sit in
-    one pinned staging buffer at 256-byte aligned offsets and go over in one copy; the API calls
-    take views of the device copy. The step (copy in, write, decode, copy out) is replayed as one
-    CUDA graph through kvq.CapturedStep, and the host waits for it every step."""
+    one pinned staging buffer at 256-byte aligned offsets and go over in one copy (kvq_copy: the
+    SMs read the pinned buffer over the chip-to-chip link, so the copy is a kernel node of the
+    graph); the API calls take views of the device copy, and the output goes back to pinned memory
+    the same way. The step (copy in, write, decode, copy out) is replayed as one CUDA graph through
+    kvq.CapturedStep, and the host waits for it every step."""
     names = ("q", "k_new", "v_new", "slots", "lens", "bt")
     srcs = {k: getattr(r, k) for k in names}
     offs, total = {}, 0
@@ -430,10 +432,10 @@ def e2e_int4(args, r, case, signs, scale, ws, S, dev, stream, dec_bytes):
                               workspace=ws)
 
     def calls():
-        d_buf.copy_(h_buf, non_blocking=True)
+        kvq.kvq_copy(d_buf, h_buf, stream=stream)  # pinned host -> device by the SMs: a kernel node
         writer(d["k_new"], d["v_new"], d["slots"], stream=stream)
         decoder(d["q"], r.out, stream=stream)
-        out_h.copy_(r.out, non_blocking=True)
+        kvq.kvq_copy(out_h, r.out, stream=stream)
 
     captured = kvq.CapturedStep(calls, stream)
 

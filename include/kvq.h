@@ -10,8 +10,9 @@
  *   kvq_fwht128       fwht128_quant_fp8 / _fwht_quant_kernel
  *
  * Conventions shared by every call
- *   - Every pointer argument is a DEVICE pointer owned by the caller; the library allocates
- *     no memory on any call path and keeps no pointer after the call returns.
+ *   - Every pointer argument is a DEVICE pointer owned by the caller (kvq_copy_async also takes
+ *     pinned host memory); the library allocates no memory on any call path and keeps no
+ *     pointer after the call returns.
  *   - Every call is asynchronous on `stream` (NULL = the legacy default stream). KVQ_OK means
  *     the kernels were enqueued; data-dependent errors detected on the device (a block id
  *     outside [0, num_blocks), a slot outside the pool, a sequence longer than its block-table
@@ -392,6 +393,20 @@ KVQ_API kvq_status kvq_kpool_decode_update(uint8_t *kv_cache, int32_t page_size,
  */
 KVQ_API kvq_status kvq_fwht128(const void *x, uint8_t *y_e4m3, float *row_scale, int64_t rows,
                        kvq_stream_t stream);
+
+/*
+ * kvq_copy_async -- copy `bytes` bytes from src to dst with a kernel: the SMs' 16-byte loads and
+ * stores (plumbing for a serving step; no counterpart on the pages). Either pointer may be device
+ * memory or pinned host memory mapped into the device's address space (cudaHostAlloc /
+ * cudaMallocHost, pinned torch tensors), which the SMs of a Grace-Blackwell node reach over the
+ * coherent chip-to-chip link. A step's inputs can thus come in and its result go out as kernel
+ * nodes of the step's CUDA graph, with no hand-off to a copy engine between kernels.
+ *   dst, src   16-byte aligned, not overlapping; bytes a multiple of 16 (0: a no-op).
+ * Returns KVQ_ERR_INVALID_ARG for a null or misaligned pointer, a size that is not a multiple of
+ * 16, overlapping ranges, or a host pointer that is not pinned and mapped (checked with
+ * cudaPointerGetAttributes before anything is launched).
+ */
+KVQ_API kvq_status kvq_copy_async(void *dst, const void *src, size_t bytes, kvq_stream_t stream);
 
 /*
  * kvq_debug_set_wait -- for tests of the error path only (no counterpart on the pages).

@@ -201,9 +201,52 @@ void workspace_carve(void *workspace, int B, int Hq, int D, const SplitPlan &pla
   *seg_last = reinterpret_cast<int32_t *>(ws);
 }
 
+// kvq_copy_async: a grid-stride loop of 16-byte copies.
+__global__ void __launch_bounds__(256) copy16_kernel(uint4 *__restrict__ dst, const uint4 *__restrict__ src,
+                                                     long long n) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    dst[i] = src[i];
+}
+
+// The address a kernel uses for p: device (or managed) memory as it is, pinned host memory by its
+// mapped device address; false for anything else (pageable host memory, an unknown pointer).
+static bool device_view(const void *p, const void **view) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the error the query left
+    return false;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    *view = p;
+    return true;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr) {
+    *view = a.devicePointer;
+    return true;
+  }
+  return false;
+}
+
 }  // namespace kvq
 
 using namespace kvq;
+
+extern "C" kvq_status kvq_copy_async(void *dst, const void *src, size_t bytes, kvq_stream_t stream) {
+  if (bytes == 0) return KVQ_OK;
+  if (dst == nullptr || src == nullptr || bytes % 16 != 0 || !aligned(dst, 16) || !aligned(src, 16))
+    return KVQ_ERR_INVALID_ARG;
+  const void *d = nullptr, *s = nullptr;
+  if (!device_view(dst, &d) || !device_view(src, &s)) return KVQ_ERR_INVALID_ARG;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(d), b = reinterpret_cast<uintptr_t>(s);
+  if (a < b + bytes && b < a + bytes) return KVQ_ERR_INVALID_ARG;
+  const long long n = static_cast<long long>(bytes / 16);
+  const long long cap = static_cast<long long>(sm_count() > 0 ? sm_count() : 1) * 8;
+  const long long grid = (n + 255) / 256 < cap ? (n + 255) / 256 : cap;
+  copy16_kernel<<<static_cast<unsigned>(grid), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint4 *>(const_cast<void *>(d)), static_cast<const uint4 *>(s), n);
+  return launch_status();
+}
 
 extern "C" const char *kvq_status_string(kvq_status s) {
   switch (s) {
@@ -217,7 +260,7 @@ extern "C" const char *kvq_status_string(kvq_status s) {
   return "KVQ_ERR_UNKNOWN";
 }
 
-extern "C" int32_t kvq_abi_version(void) { return 4; }
+extern "C" int32_t kvq_abi_version(void) { return 5; }
 
 extern "C" size_t kvq_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hk, int32_t D,
                                              int32_t num_splits) {

@@ -27,8 +27,8 @@ C_FUNCTIONS = ("kvq_status_string", "kvq_abi_version", "kvq_write_int4", "kvq_de
                "kvq_decode_int4", "kvq_decode_int4_mods", "kvq_decode_int4_mods_workspace_bytes",
                "kvq_decode_int4_noalloc", "kvq_decode_tq",
                "kvq_decode_tq_lse", "kvq_decode_tq_mse_workspace_bytes", "kvq_decode_tq_mse", "kvq_kpool_write",
-               "kvq_kpool_seed_tail", "kvq_kpool_decode_update", "kvq_fwht128", "kvq_debug_set_wait",
-               "kvq_device_error")
+               "kvq_kpool_seed_tail", "kvq_kpool_decode_update", "kvq_fwht128", "kvq_copy_async",
+               "kvq_debug_set_wait", "kvq_device_error")
 KVQ_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lock = threading.Lock()
@@ -46,6 +46,7 @@ class ScoreMods(ctypes.Structure):
 _SIGS = {
     "kvq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kvq_abi_version": (c_i32, []),
+    "kvq_copy_async": (ctypes.c_int, [c_p, c_p, ctypes.c_size_t, c_p]),
     "kvq_write_int4": (ctypes.c_int, [c_p, c_p, c_i64, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_p, c_p, c_p,
                                       c_i32, c_i32, c_i32, c_i32, c_i64, c_p]),
     "kvq_decode_workspace_bytes": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32]),
@@ -554,6 +555,25 @@ class Int4Decoder:
         _check(self._fn(q.data_ptr(), *self._head, out.data_ptr(), _out_code(out.dtype), *self._dims,
                         _stream(stream)), "kvq_decode_int4")
         return out
+
+
+def kvq_copy(dst, src, stream=None):
+    """Copy src into dst (the same number of bytes) with the library's copy kernel on `stream`.
+    Each tensor may be a CUDA tensor or a pinned CPU tensor (read or written by the SMs over the
+    chip-to-chip link), so inside a captured step the copies are kernel nodes like the rest.
+    Both contiguous, 16-byte aligned, a multiple of 16 bytes. Returns dst."""
+    for t, n in ((dst, "dst"), (src, "src")):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError("%s must be a tensor" % n)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % n)
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError("%s must be a CUDA tensor or a pinned CPU tensor" % n)
+    nbytes = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nbytes:
+        raise ValueError("dst and src differ in size: %d vs %d bytes" % (nbytes, src.numel() * src.element_size()))
+    _check(lib().kvq_copy_async(_ptr(dst), _ptr(src), nbytes, _stream(stream)), "kvq_copy_async")
+    return dst
 
 
 class CapturedStep:

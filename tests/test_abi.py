@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings_and_version():
-    assert kvq.kvq_abi_version() == 4
+    assert kvq.kvq_abi_version() == 5
     for code in range(6):
         assert kvq.kvq_status_string(code).startswith("KVQ_")
     assert "UNKNOWN" in kvq.kvq_status_string(77)
