@@ -288,21 +288,25 @@ def run_kvq(args, dist):
     stream.synchronize()
     st, flags = kvq.kvq_device_error(stream)
     assert st == 0, flags
-    gw, gd = [], []
+    gw, gd, gs = [], [], []  # per replica: the write, the decode, and the whole step (both) as one graph
     for r in reps:
-        a, b = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        a, b, c = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.graph(a, stream=stream):
             write(r)
         with torch.cuda.graph(b, stream=stream):
             decode(r)
+        with torch.cuda.graph(c, stream=stream):
+            write(r)
+            decode(r)
         gw.append(a)
         gd.append(b)
+        gs.append(c)
 
     dec_bytes, kv_bytes = int4_decode_bytes(case.seq_lens, Q * Hq, Hk, D, window=mods.get("sliding_window", 0))
     dec_bytes += 8 * Hq if "sinks" in mods else 0  # sinks and slopes
     wr_bytes = B * Hk * (2 * D * 2 + 2 * (D // 2 + 4)) + 8 * B
     res = timed_steps(args, dist, stream, lambda i: gw[i % nrep].replay(), lambda i: gd[i % nrep].replay(),
-                      dev.index)
+                      dev.index, step=lambda i: gs[i % nrep].replay())
     st, flags = kvq.kvq_device_error(stream)
     assert st == 0, flags
 
@@ -313,7 +317,7 @@ def run_kvq(args, dist):
            "seq_lens": "U[1024,8192] seed 0, sum %d" % sum(case.seq_lens) if wl != "long_context_int4"
            else "131072 x 4, pages scattered in a %.0f GB pool" % (case.pool_bytes / 1e9),
            "num_splits": "heuristic (balanced)" if S == 0 else S, "rht": True, "out_dtype": "bf16",
-           "step": "kvq_write_int4 (B new tokens) + kvq_decode_int4",
+           "step": "kvq_write_int4 (B new tokens) + kvq_decode_int4, replayed as one CUDA graph",
            "l2": ("%d rotating cache replicas, %.0f MB read from each per step (%d x %.0f MB > 126 MB L2): "
                   "no L2 reuse across steps" % (nrep, kv_bytes / 1e6, nrep, kv_bytes / 1e6)) if nrep > 1
            else "single %.0f MB cache read per step (> L2)" % (kv_bytes / 1e6),
@@ -334,15 +338,19 @@ def run_kvq(args, dist):
                    "quantized_paged_kv_int4_gb300/csrc/kvq_device.cuh"], "f32")
 
 
-def timed_steps(args, dist, stream, first, second, dev_index):
+def timed_steps(args, dist, stream, first, second, dev_index, step=None):
     """W warm-up steps, a burn-in (clock sampling), then the timed region: K steps back to back
     between one event pair (the step time); K `second` calls (the dominant call) back to back
     between one event pair (its average launch duration, nothing inside the region but the calls);
     and K more steps with an event pair around each `second` call (the same duration seen with
     an event on each side, which adds about 2 us per call; reported beside it). Clocks are
-    sampled over all three."""
+    sampled over all three. `step(i)`, when given, replays step i as one graph (first and second
+    captured together) in the step-time pass."""
+    if step is None:
+        step = lambda i: (first(i), second(i))
     for i in range(args.warmup):
         with torch.cuda.stream(stream):
+            step(i)
             first(i)
             second(i)
     stream.synchronize()
@@ -368,8 +376,7 @@ def timed_steps(args, dist, stream, first, second, dev_index):
     with torch.cuda.stream(stream):
         start.record(stream)
         for i in range(K):
-            first(i)
-            second(i)
+            step(i)
         stop.record(stream)
     torch.cuda.synchronize()
     dist.barrier()
