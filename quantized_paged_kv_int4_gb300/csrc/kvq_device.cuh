@@ -62,6 +62,65 @@ __device__ __forceinline__ void butterfly_local(float (&x)[N]) {
 // ---------------------------------------------------------------------------------------------
 // PTX wrappers
 // ---------------------------------------------------------------------------------------------
+// Packed fp32 pairs (the Blackwell f32x2 ALU): add.rn / sub.rn .f32x2 round each component
+// exactly like the scalar instruction, so a pair of butterflies costs one instruction with the
+// same bits. (A packed multiply that feeds a packed add may be fused into a multiply-add by the
+// assembler: where two roundings are required, keep that step scalar.)
+__device__ __forceinline__ unsigned long long f2pack(float a, float b) {
+  return static_cast<unsigned long long>(__float_as_uint(a)) | (static_cast<unsigned long long>(__float_as_uint(b)) << 32);
+}
+__device__ __forceinline__ void f2unpack(unsigned long long v, float &a, float &b) {
+  a = __uint_as_float(static_cast<uint32_t>(v));
+  b = __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long sub2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// butterfly stages h = 1 .. N/2 over N consecutive elements (the pages' order): h = 1 scalar, h >= 2
+// on packed pairs (j, j + 1)
+template <int N>
+__device__ __forceinline__ void butterfly_local2(float (&x)[N]) {
+#pragma unroll
+  for (int j = 0; j < N; j += 2) {
+    const float a = x[j], b = x[j + 1];
+    x[j] = __fadd_rn(a, b);
+    x[j + 1] = __fsub_rn(a, b);
+  }
+#pragma unroll
+  for (int h = 2; h < N; h <<= 1) {
+#pragma unroll
+    for (int j = 0; j < N; j += 2) {
+      if (!(j & h)) {
+        const unsigned long long a = f2pack(x[j], x[j + 1]), b = f2pack(x[j + h], x[j + h + 1]);
+        f2unpack(add2(a, b), x[j], x[j + 1]);
+        f2unpack(sub2(a, b), x[j + h], x[j + h + 1]);
+      }
+    }
+  }
+}
+// the same stages over rows of two columns at once: element r of column c is x[c][r]
+__device__ __forceinline__ void butterfly_cols2(float (&x)[2][8]) {
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      if (!(r & h)) {
+        const unsigned long long a = f2pack(x[0][r], x[1][r]), b = f2pack(x[0][r + h], x[1][r + h]);
+        f2unpack(add2(a, b), x[0][r], x[1][r]);
+        f2unpack(sub2(a, b), x[0][r + h], x[1][r + h]);
+      }
+    }
+  }
+}
+
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -65,26 +65,9 @@ __device__ __forceinline__ uint32_t bf2_bits(float lo, float hi) {
   return w;
 }
 
-// Packed fp32 pairs (Blackwell f32x2 ALU): each component rounded exactly like the scalar op. Only
-// packed adds and subtracts are used: a packed multiply feeding a packed add can be fused into a
-// multiply-add by the assembler, which would drop the intermediate rounding.
-__device__ __forceinline__ unsigned long long f2pack(float a, float b) {
-  return static_cast<unsigned long long>(__float_as_uint(a)) | (static_cast<unsigned long long>(__float_as_uint(b)) << 32);
-}
-__device__ __forceinline__ void f2unpack(unsigned long long v, float &a, float &b) {
-  a = __uint_as_float(static_cast<uint32_t>(v));
-  b = __uint_as_float(static_cast<uint32_t>(v >> 32));
-}
-__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
-  unsigned long long d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ unsigned long long sub2(unsigned long long a, unsigned long long b) {
-  unsigned long long d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
+// The packed fp32 pair helpers (add2 / sub2, kvq_device.cuh) round each component exactly like
+// the scalar op. Only packed adds and subtracts are used: a packed multiply feeding a packed add
+// can be fused into a multiply-add by the assembler, which would drop the intermediate rounding.
 
 // One thread per (token, kv head) vector of K or V: the whole D-element rotation, the min / max,
 // the three divisions and the packing run in the thread, so nothing is repeated across lanes and
@@ -277,42 +260,6 @@ __global__ void __launch_bounds__(128, 3) write_int4_kernel(const WriteParams p,
     }
     cur = nxt;
     b ^= 1;
-  }
-}
-
-// butterfly stages h = 1 .. N/2 over N consecutive elements: h = 1 scalar, h >= 2 on pairs (j, j + 1)
-template <int N>
-__device__ __forceinline__ void butterfly_local2(float (&x)[N]) {
-#pragma unroll
-  for (int j = 0; j < N; j += 2) {
-    const float a = x[j], b = x[j + 1];
-    x[j] = __fadd_rn(a, b);
-    x[j + 1] = __fsub_rn(a, b);
-  }
-#pragma unroll
-  for (int h = 2; h < N; h <<= 1) {
-#pragma unroll
-    for (int j = 0; j < N; j += 2) {
-      if (!(j & h)) {
-        const unsigned long long a = f2pack(x[j], x[j + 1]), b = f2pack(x[j + h], x[j + h + 1]);
-        f2unpack(add2(a, b), x[j], x[j + 1]);
-        f2unpack(sub2(a, b), x[j + h], x[j + h + 1]);
-      }
-    }
-  }
-}
-// the same stages over rows of two columns at once: element r of column c is x[c][r]
-__device__ __forceinline__ void butterfly_cols2(float (&x)[2][8]) {
-#pragma unroll
-  for (int h = 1; h < 8; h <<= 1) {
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      if (!(r & h)) {
-        const unsigned long long a = f2pack(x[0][r], x[1][r]), b = f2pack(x[0][r + h], x[1][r + h]);
-        f2unpack(add2(a, b), x[0][r], x[1][r]);
-        f2unpack(sub2(a, b), x[0][r + h], x[1][r + h]);
-      }
-    }
   }
 }
 
