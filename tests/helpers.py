@@ -143,3 +143,15 @@ class MseCase:
         return turboquant.decode_tq_mse(self.q.numpy(), self.cache.numpy(), self.kb, self.kps, self.vb,
                                         self.cb.numpy(), norm_correction, self.Pi.numpy(), self.bt.numpy(),
                                         np.asarray(self.case.seq_lens), self.scale, batch_index=batch_index)
+
+
+def scatter_into_pool(cache, bt, num_blocks, seed):
+    """cache [n, 16, Hk, sb] (compact pages) placed at random blocks of a num_blocks pool on the GPU,
+    the pool's first and last blocks among them; returns (pool, block table into the pool)."""
+    n = cache.shape[0]
+    g = torch.Generator().manual_seed(seed)
+    mid = torch.randperm(num_blocks - 2, generator=g)[:max(n - 2, 0)] + 1
+    phys = torch.cat([torch.tensor([num_blocks - 1, 0]), mid])[:n]
+    pool = torch.empty((num_blocks,) + tuple(cache.shape[1:]), dtype=torch.uint8, device="cuda")
+    pool[phys.cuda()] = cache.cuda()
+    return pool, phys[bt.long()].to(torch.int32)

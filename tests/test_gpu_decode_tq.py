@@ -6,7 +6,7 @@ import torch
 
 from quantized_paged_kv_int4_gb300 import kvq, workloads
 
-from helpers import TqCase, assert_close
+from helpers import TqCase, assert_close, scatter_into_pool
 
 pytestmark = pytest.mark.gpu
 
@@ -53,3 +53,18 @@ def test_slot_wider_than_its_fields(bits):
     c.cache = torch.cat([c.cache, pad], dim=-1).contiguous()
     assert c.cache.shape[-1] % 16 == 0
     assert_close(_run(c), c.oracle(), what="padded slot bits=%d" % bits)
+
+
+def test_pages_scattered_in_a_4gb_pool():
+    """Pages scattered over a 150000-block pool (4 GB of 208-byte slots), its last block in use: the
+    page tiles' tensor map addresses the whole pool. The oracle reads the same pages compactly."""
+    lens = [300, 1000, 17]
+    case = workloads.DecodeCase("tqpool", len(lens), 32, 8, 128, lens, seed=71)
+    c = TqCase(case, 4)
+    pool, bt = scatter_into_pool(c.cache, c.bt, 150000, 71)
+    out = kvq.kvq_decode_tq(c.q.cuda(), pool, 4, bt.cuda(), c.lens.cuda(), c.scale)
+    st, flags = kvq.kvq_device_error()
+    assert st == 0 and flags == 0
+    assert_close(out.cpu().numpy(), c.oracle(), what="tq 4 GB pool")
+    del pool
+    torch.cuda.empty_cache()

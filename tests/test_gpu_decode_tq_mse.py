@@ -8,7 +8,7 @@ import torch
 from oracle import turboquant
 from quantized_paged_kv_int4_gb300 import kvq, workloads
 
-from helpers import MseCase, assert_close
+from helpers import MseCase, assert_close, scatter_into_pool
 
 pytestmark = pytest.mark.gpu
 
@@ -45,3 +45,19 @@ def test_full_size_sampled(key_bits, value_bits):
     got = c.gpu(False)
     idx = [0, 31, 63]
     assert_close(got[idx], c.oracle(False, batch_index=idx)[idx], what="mse full k%d v%d" % (key_bits, value_bits))
+
+
+def test_pages_scattered_in_a_large_pool():
+    """MSE-key slots scattered over a 200000-block pool (3.3 GB of 128-byte slots), its first and
+    last blocks in use; the oracle reads the same pages compactly."""
+    lens = [640, 33, 1500]
+    case = workloads.DecodeCase("msepool", len(lens), 32, 8, 128, lens, seed=72)
+    c = MseCase(case, 3, 4)
+    pool, bt = scatter_into_pool(c.cache, c.bt, 200000, 72)
+    out = kvq.kvq_decode_tq_mse(c.q.cuda(), c.Pi.cuda(), c.cb.cuda(), pool, c.kb, c.kps, c.vb, bt.cuda(),
+                                c.lens.cuda(), c.scale)
+    st, flags = kvq.kvq_device_error()
+    assert st == 0 and flags == 0
+    assert_close(out.cpu().numpy(), c.oracle(False), what="mse large pool")
+    del pool
+    torch.cuda.empty_cache()
