@@ -410,14 +410,15 @@ KVQ_API kvq_status kvq_copy_async(void *dst, const void *src, size_t bytes, kvq_
 
 /*
  * kvq_debug_set_wait -- for tests of the error path only (no counterpart on the pages).
- * Every wait of the INT4 decode kernel on a page copy is bounded; when one runs out the kernel
- * raises flag 8, lets the copies it has issued land, writes what it has and returns, so the
- * context stays usable. This call makes that path reachable on purpose, without any fault:
+ * Every wait of the decode kernels (INT4 and TurboQuant) on a page copy is bounded; when one runs
+ * out the kernel raises flag 8, lets the copies it has issued land, and returns, so the context
+ * stays usable. This call makes that path reachable on purpose, without any fault:
  *   wait_limit_ns   the limit of every such wait from now on in this process (0: the default, 2 s).
- *   withhold_stage  >= 0: the NEXT kvq_decode_int4 / kvq_decode_int4_mods call (that one call only)
- *                   does not issue the copies of that ring stage in its first CTA, so the wait on
- *                   it runs out after wait_limit_ns (plus ~0.1 s for the bounded drain) and flag 8
- *                   is raised; that call's results are not valid. -1: none.
+ *   withhold_stage  >= 0: the NEXT decode call (kvq_decode_int4, _int4_mods, _tq, _tq_lse or
+ *                   _tq_mse; that one call only) does not issue the copies of that ring stage in
+ *                   its first CTA (TurboQuant: of that ring tile of the CTA's first warp), so the
+ *                   wait on it runs out after wait_limit_ns (plus ~0.1 s for the bounded drain) and
+ *                   flag 8 is raised; that call's results are not valid. -1: none.
  * Returns KVQ_ERR_INVALID_ARG for withhold_stage < -1.
  */
 KVQ_API kvq_status kvq_debug_set_wait(uint64_t wait_limit_ns, int32_t withhold_stage);

@@ -2,6 +2,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -228,9 +229,21 @@ static bool device_view(const void *p, const void **view) {
   return false;
 }
 
+static std::atomic<unsigned long long> g_wait_ns{2000000000ull};
+static std::atomic<int> g_withhold{-1};
+unsigned long long debug_wait_ns() { return g_wait_ns.load(); }
+int debug_take_withhold() { return g_withhold.exchange(-1); }
+
 }  // namespace kvq
 
 using namespace kvq;
+
+extern "C" kvq_status kvq_debug_set_wait(uint64_t wait_limit_ns, int32_t withhold_stage) {
+  if (withhold_stage < -1) return KVQ_ERR_INVALID_ARG;
+  kvq::g_wait_ns.store(wait_limit_ns == 0 ? 2000000000ull : wait_limit_ns);
+  kvq::g_withhold.store(withhold_stage);
+  return KVQ_OK;
+}
 
 extern "C" kvq_status kvq_copy_async(void *dst, const void *src, size_t bytes, kvq_stream_t stream) {
   if (bytes == 0) return KVQ_OK;

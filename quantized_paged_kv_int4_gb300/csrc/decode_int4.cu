@@ -1159,19 +1159,6 @@ static kvq_status launch_int4(const Int4Params &p, const SplitPlan &plan, cudaSt
 
 using namespace kvq;
 
-namespace kvq {
-// Error-path test settings (kvq_debug_set_wait): the wait limit of the decode kernels' bounded
-// waits, and a stage whose copies the next INT4 decode call withholds (one call only).
-static std::atomic<unsigned long long> g_wait_ns{2000000000ull};
-static std::atomic<int> g_withhold{-1};
-}  // namespace kvq
-
-extern "C" kvq_status kvq_debug_set_wait(uint64_t wait_limit_ns, int32_t withhold_stage) {
-  if (withhold_stage < -1) return KVQ_ERR_INVALID_ARG;
-  kvq::g_wait_ns.store(wait_limit_ns == 0 ? 2000000000ull : wait_limit_ns);
-  kvq::g_withhold.store(withhold_stage);
-  return KVQ_OK;
-}
 
 namespace kvq {
 
@@ -1340,8 +1327,8 @@ extern "C" kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache
   p.softcap2 = static_cast<float>(cap2);
   p.inv_softcap2 = cap2 > 0.0 ? static_cast<float>(1.0 / cap2) : 0.f;
   p.alibi = mods ? mods->alibi_slopes : nullptr;
-  p.wait_ns = g_wait_ns.load();
-  p.withhold = g_withhold.exchange(-1);  // one call only
+  p.wait_ns = debug_wait_ns();
+  p.withhold = debug_take_withhold();  // one call only
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cg.mtok) {  // the virtual sequences, in stream order before the split kernel
     build_vseq_kernel<<<1, 256, 0, s>>>(mods->query_start_loc, mods->query_start_loc ? 0 : mods->q_len, seq_lens, B,

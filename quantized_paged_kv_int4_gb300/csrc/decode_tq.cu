@@ -34,6 +34,8 @@ struct TqParams {
   const int32_t *block_table;
   float sc_log2;  // attn_scale * log2(e)
   int64_t num_blocks;
+  unsigned long long wait_ns;  // limit of every bounded wait on a ring slot
+  int32_t withhold;            // error-path tests only: warp 0 of CTA (0, 0) never issues its ring tile `withhold`
 };
 
 constexpr uint32_t kLoTq = 0x000F000Fu;  // low nibbles -> fp16 subnormals idx * 2^-24
@@ -98,7 +100,9 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, TqRing &rg, int b, i
       bids_next = load_bids((k >> 5) + 1);
     }
     const int blk = __shfl_sync(FULL, bids_cur, kk);
-    if (lane == 0) {
+    const bool withheld = K0 + k == static_cast<uint32_t>(p.withhold) && blockIdx.x == 0 && blockIdx.y == 0 &&
+                          threadIdx.x < 32;  // its wait runs out: the error-path test
+    if (lane == 0 && !withheld) {
       const bool ok = blk >= 0 && blk < p.num_blocks;
       if (!ok) atomicOr(&g_flags_decode_tq, ERR_BLOCK);
       const uint32_t sl = (K0 + k) % NSTAGE;
@@ -175,7 +179,7 @@ __device__ __forceinline__ void tq_piece(const TqParams &p, TqRing &rg, int b, i
     {
       const uint32_t K = K0 + k;
       const uint32_t bar = rg.bar + 8 * (K % NSTAGE), par = (K / NSTAGE) & 1;
-      if (!__all_sync(FULL, mbar_try_wait(bar, par)) && !__all_sync(FULL, mbar_wait(bar, par))) {
+      if (!__all_sync(FULL, mbar_try_wait(bar, par)) && !__all_sync(FULL, mbar_wait(bar, par, p.wait_ns))) {
         if (lane == 0) atomicOr(&g_flags_decode_tq, ERR_TIMEOUT);
         rg.failed = true;
         break;
@@ -467,6 +471,8 @@ extern "C" kvq_status kvq_decode_tq_lse(const float *q, const uint8_t *kv_cache,
   sa.out_dtype = KVQ_F32;
   p.q = q;
   p.block_table = block_table;
+  p.wait_ns = debug_wait_ns();
+  p.withhold = debug_take_withhold();  // one call only
   p.sc_log2 = static_cast<float>(static_cast<double>(attn_scale) * 1.4426950408889634);
   p.num_blocks = num_blocks;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

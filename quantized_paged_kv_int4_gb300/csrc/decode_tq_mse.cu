@@ -34,6 +34,8 @@ struct TqMseParams {
   int32_t kps, norm_correction;
   float sc_log2;           // attn_scale * log2(e)
   int64_t num_blocks;
+  unsigned long long wait_ns;  // limit of every bounded wait on a ring slot
+  int32_t withhold;            // error-path tests only: warp 0 of CTA (0, 0) never issues its ring tile `withhold`
 };
 
 constexpr uint32_t kLoMse = 0x000F000Fu;
@@ -202,7 +204,9 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, MseRing &rg, 
       bids_next = load_bids((k >> 5) + 1);
     }
     const int blk = __shfl_sync(FULL, bids_cur, kk);
-    if (lane == 0) {
+    const bool withheld = K0 + k == static_cast<uint32_t>(p.withhold) && blockIdx.x == 0 && blockIdx.y == 0 &&
+                          threadIdx.x < 32;  // its wait runs out: the error-path test
+    if (lane == 0 && !withheld) {
       const bool ok = blk >= 0 && blk < p.num_blocks;
       if (!ok) atomicOr(&g_flags_decode_tq_mse, ERR_BLOCK);
       const uint32_t sl = (K0 + k) % NSTAGE;
@@ -280,7 +284,7 @@ __device__ __forceinline__ void tq_mse_piece(const TqMseParams &p, MseRing &rg, 
     {
       const uint32_t K = K0 + k;
       const uint32_t bar = rg.bar + 8 * (K % NSTAGE), par = (K / NSTAGE) & 1;
-      if (!__all_sync(FULL, mbar_try_wait(bar, par)) && !__all_sync(FULL, mbar_wait(bar, par))) {
+      if (!__all_sync(FULL, mbar_try_wait(bar, par)) && !__all_sync(FULL, mbar_wait(bar, par, p.wait_ns))) {
         if (lane == 0) atomicOr(&g_flags_decode_tq_mse, ERR_TIMEOUT);
         rg.failed = true;
         break;
@@ -659,6 +663,8 @@ extern "C" kvq_status kvq_decode_tq_mse(const float *q, const float *rotation, c
   sa.out_dtype = KVQ_F32;
   p.q_rot = q_rot;
   p.block_table = block_table;
+  p.wait_ns = debug_wait_ns();
+  p.withhold = debug_take_withhold();  // one call only
   p.centroids = centroids;
   p.kps = key_packed_size;
   p.norm_correction = norm_correction != 0;

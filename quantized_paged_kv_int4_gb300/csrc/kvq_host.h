@@ -27,6 +27,12 @@ bool take_flags_decode_tq(cudaStream_t stream, unsigned *host_word);
 bool take_flags_decode_tq_mse(cudaStream_t stream, unsigned *host_word);
 bool take_flags_kpool(cudaStream_t stream, unsigned *host_word);
 
+// Error-path test settings (kvq_debug_set_wait): the limit of the decode kernels' bounded waits on
+// page copies, and the ring stage whose copies the next decode call withholds (taken by that call:
+// -1 afterwards).
+unsigned long long debug_wait_ns();
+int debug_take_withhold();
+
 // Split-partition geometry shared by workspace sizing and the launches.
 struct SplitPlan {
   int heads_per_cta;   // kv heads one CTA covers (<= 8)

@@ -86,3 +86,41 @@ def test_a_wait_that_runs_out_is_reported_and_the_gpu_stays_usable():
     from helpers import assert_close
     for S in (2, 0):
         assert_close(run_int4(kvq, g, c.scale, num_splits=S).cpu().numpy(), c.oracle(), what="after the timeout")
+
+
+@pytest.mark.parametrize("kind", ["fp8", "mse"])
+def test_turboquant_wait_that_runs_out_is_reported(kind):
+    """The TurboQuant kernels' bounded waits: the next call withholds ring tile 2 of the first CTA's
+    first warp (its page copy is never issued), the wait on it runs out after 5 ms, flag 8 is
+    raised, and the following call on the same context is exact again."""
+    from helpers import MseCase, TqCase, assert_close
+    lens = [1200, 700, 2000]
+    case = workloads.DecodeCase("tqtimeout", len(lens), 32, 8, 128, lens, seed=62)
+    if kind == "fp8":
+        c = TqCase(case, 4)
+
+        def call():
+            return kvq.kvq_decode_tq(c.q.cuda(), c.cache.cuda(), c.bits, c.bt.cuda(), c.lens.cuda(), c.scale,
+                                     num_splits=2)
+
+        def ref():
+            return c.oracle()
+    else:
+        c = MseCase(case, 3, 4)
+
+        def call():
+            return kvq.kvq_decode_tq_mse(c.q.cuda(), c.Pi.cuda(), c.cb.cuda(), c.cache.cuda(), c.kb, c.kps, c.vb,
+                                         c.bt.cuda(), c.lens.cuda(), c.scale, num_splits=2)
+
+        def ref():
+            return c.oracle(False)
+    try:
+        kvq.kvq_debug_set_wait(5_000_000, 2)  # split 0 of sequence 0: 38 pages, one ring tile each per warp
+        call()
+        st, flags = kvq.kvq_device_error()
+        assert st == kvq.KVQ_ERR_OUT_OF_RANGE and flags == 8, (st, flags)
+    finally:
+        kvq.kvq_debug_set_wait(0, -1)
+    got = call()
+    assert kvq.kvq_device_error() == (0, 0)
+    assert_close(got.cpu().numpy(), ref(), what="%s after the timeout" % kind)
