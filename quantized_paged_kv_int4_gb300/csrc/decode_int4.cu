@@ -52,6 +52,7 @@ struct Int4Params {
   SplitArgs s;
   const __nv_bfloat16 *q;
   const int32_t *block_table;
+  int32_t bt_rows;  // rows of block_table (the real sequences; s.B counts virtual ones in multi-token calls)
   float sm_log2;  // softmax scale (divided by D when rotating) times log2(e)
   int64_t num_blocks;
   float softcap2;       // USE_SOFTCAP: the cap in base-2 units (cap * log2 e), 0 = off
@@ -842,7 +843,7 @@ __global__ void __launch_bounds__(256, 2) decode_int4_kernel(const __grid_consta
   const bool split_heads = a.Hk > 8;
 
   {  // pull the block table into L2 while the run is planned (each CTA a slice of 128-byte lines)
-    const long long bytes = static_cast<long long>(a.B) * a.max_blocks * 4;
+    const long long bytes = static_cast<long long>(p.bt_rows) * a.max_blocks * 4;
     const long long lines = (bytes + 127) / 128, per = (lines + gridDim.x - 1) / gridDim.x;
     const long long l0 = static_cast<long long>(blockIdx.x) * per;
     for (long long l = l0 + threadIdx.x; l < l0 + per && l < lines; l += blockDim.x)
@@ -1320,6 +1321,7 @@ extern "C" kvq_status kvq_decode_int4_mods(const void *q, const uint8_t *k_cache
   p.q = static_cast<const __nv_bfloat16 *>(q);
   if (!int4_tensor_maps(k_cache, v_cache, k_scale, v_scale, num_blocks, Hk, D, &p.maps)) return KVQ_ERR_CUDA;
   p.block_table = block_table;
+  p.bt_rows = B;
   const double sm = rht_signs ? static_cast<double>(softmax_scale) / D : softmax_scale;
   p.sm_log2 = static_cast<float>(sm * 1.4426950408889634);
   p.num_blocks = num_blocks;
