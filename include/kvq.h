@@ -294,7 +294,7 @@ KVQ_API kvq_status kvq_decode_tq_lse(const float *q, const uint8_t *kv_cache, in
  *   rotation      fp32 [D, D] (Pi), 16-byte aligned.   centroids  fp32 [2^key_bits].
  *   kv_cache      uint8 [num_blocks, 16, Hk, slot_bytes]; slot_bytes a multiple of 16, at most 512,
  *                 >= key_packed_size + ceil(D * value_bits / 8) + 4; that used part of a slot at
- *                 most 240 bytes (KVQ_ERR_UNSUPPORTED otherwise).
+ *                 most 236 bytes (KVQ_ERR_UNSUPPORTED otherwise).
  *   key_bits, value_bits  3 or 4.   key_packed_size  even, >= MSE_BYTES + 2.
  *   workspace     >= kvq_decode_tq_mse_workspace_bytes(...) bytes, 256-byte aligned (holds q_rot
  *                 and the split partials); contents need no initialisation.

@@ -60,10 +60,12 @@ struct MseGeom {
 };
 
 // Staged bytes of a slot holding its `used` bytes: a multiple of 16 (a box row) whose word stride
-// is 4 mod 8 (rows g and g + 8 of a fragment fall in different banks), i.e. an odd multiple of 16.
-// Bytes past the slot's end are out of the tensor and filled with zeros by the copy.
+// is 4 mod 8 (rows g and g + 8 of a fragment fall in different banks), i.e. an odd multiple of 16,
+// and at least used + 4: the unaligned 32-bit read of the last field (two aligned words) may take
+// up to 4 bytes past it, which must stay inside the row. Bytes past the slot's end are out of the
+// tensor and filled with zeros by the copy.
 inline int mse_row_bytes(int used) {
-  int rs = (used + 15) / 16 * 16;
+  int rs = (used + 4 + 15) / 16 * 16;
   while (((rs / 4) & 7) != 4) rs += 16;
   return rs;
 }

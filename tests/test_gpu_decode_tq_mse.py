@@ -61,3 +61,15 @@ def test_pages_scattered_in_a_large_pool():
     assert_close(out.cpu().numpy(), c.oracle(False), what="mse large pool")
     del pool
     torch.cuda.empty_cache()
+
+
+def test_used_bytes_an_odd_multiple_of_16():
+    """3-bit keys and values with the key part padded by 10: the used bytes of a slot are 112, an odd
+    multiple of 16 (the staged row keeps 4 bytes past them for the unaligned read of the scale
+    word, so the row is 144 wide)."""
+    lens = [300, 47]
+    case = workloads.DecodeCase("mse112", len(lens), 8, 2, 128, lens, seed=47)
+    c = MseCase(case, 3, 3, kps_pad=10)
+    assert c.kps + 48 + 4 == 112
+    for corr in (False, True):
+        assert_close(c.gpu(corr), c.oracle(corr), what="used 112 corr=%d" % corr)
