@@ -81,10 +81,13 @@ def test_empty_and_all_skipped():
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("Hk,D,T", [(1, 64, 777), (3, 128, 777), (5, 64, 1001), (12, 128, 2049)])
+@pytest.mark.parametrize("Hk,D,T", [(1, 64, 777), (3, 128, 777), (5, 64, 1001), (12, 128, 301), (12, 128, 2049),
+                                    (24, 64, 341), (6, 128, 1365), (6, 128, 1366)])
 def test_head_counts_and_ragged_tiles(Hk, D, T):
-    """Head counts that are not powers of two (the kernel splits a pair index into token and head
-    by a multiply-shift) and pair counts that leave a ragged last tile of 16 pairs."""
+    """Head counts that are not powers of two (the kernels split a pair index into token and head
+    by a multiply-shift) and pair counts that leave a ragged last tile of 16 pairs; writes of up to
+    8192 (token, head) pairs take the eight-lanes-per-vector kernel, larger ones the one-thread-per-
+    vector kernel (6 x 1365 = 8190 pairs sit just below the switch, 6 x 1366 = 8196 just above)."""
     k, v, slots, nb = workloads.write_case(T=T, Hk=Hk, D=D, hole_frac=0.1, seed=Hk)
     _write_both(k, v, slots, nb, Hk, D, workloads.rht_signs(D))
 
